@@ -1,0 +1,447 @@
+// Host side of the C ABI in gemm_epi.h: plans, argument checks, tensor-map encoding and
+// kernel launches.
+//
+// The plan/execute/free split follows the stateful Matmul API of "Fusing bias into cuBLASLt
+// matmul with nvmath-python for PyTorch inference" (blog.hotdry.top, 2025-09-22, code
+// example and the paragraph on operational parameters): the plan fixes shape, dtype, epilog
+// and bias layout and chooses the kernel configuration ("nvmath-python: cuBLAS and cuSOLVER
+// bindings", matmul-planning checklist: plan() picks the algorithm); execute() is
+// asynchronous; free() releases the plan.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "gemm_epi.h"
+#include "kernel_params.h"
+
+using namespace gemm_epi;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn encode_fn()
+{
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    return g_encode;
+}
+
+enum Variant { kEmpty = 0, kRowTile = 1, kSwapped = 2, kBiasOnly = 3 };
+
+constexpr int kSwappedMaxM = 256;
+constexpr unsigned long long kDefaultWaitNs = 2000ull * 1000 * 1000;  // 2 s
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+struct gemm_epi_plan_s {
+    int64_t m, n, k;
+    int dtype, epilog, bias_layout;
+    int device, sm_count;
+    // chosen configuration
+    int variant, bn, stages, smem, grid, group_m, tiles_m, tiles_n, k_blocks;
+    // options (0 = automatic)
+    int opt_variant, opt_bn, opt_split_k, opt_grid, opt_group_m;
+    unsigned long long wait_limit_ns;
+    int debug_stall;
+    int* d_status;
+    // tensor maps for the last (A, B, D) pointers
+    const void* key_A;
+    const void* key_B;
+    const void* key_D;
+    bool maps_valid;
+    CUtensorMap tm_A, tm_B, tm_D;
+    char desc[320];
+};
+
+namespace {
+
+int pick_rowtile_bn(int64_t m, int64_t n, int sm_count)
+{
+    const int64_t tm = (m + 127) / 128;
+    for (int bn : {256, 128}) {
+        const int64_t tiles = tm * ((n + bn - 1) / bn);
+        if (tiles >= sm_count) return bn;
+    }
+    return 64;
+}
+
+gemm_epi_status configure(gemm_epi_plan_s* p)
+{
+    p->maps_valid = false;
+    p->bn = p->stages = p->smem = p->grid = p->tiles_m = p->tiles_n = p->k_blocks = 0;
+    p->group_m = 1;
+    if (p->m == 0 || p->n == 0) {
+        p->variant = kEmpty;
+    } else if (p->k == 0) {
+        p->variant = kBiasOnly;
+    } else {
+        int v = p->opt_variant ? p->opt_variant : (p->m <= kSwappedMaxM ? kSwapped : kRowTile);
+        if (v == kSwapped && p->m > kSwappedMaxM) return GEMM_EPI_ERR_INVALID_ARG;
+        p->variant = v;
+        if (v == kRowTile) {
+            p->bn = p->opt_bn ? p->opt_bn : pick_rowtile_bn(p->m, p->n, p->sm_count);
+            p->tiles_m = static_cast<int>((p->m + 127) / 128);
+            p->tiles_n = static_cast<int>((p->n + p->bn - 1) / p->bn);
+            p->stages = rowtile_stages(p->bn);
+            p->smem = rowtile_smem_bytes(p->bn);
+        } else {
+            int bn = 16;
+            while (bn < p->m) bn *= 2;
+            p->bn = bn;
+            p->tiles_m = static_cast<int>((p->n + 127) / 128);
+            p->tiles_n = static_cast<int>((p->m + bn - 1) / bn);
+            p->stages = swapped_stages(bn);
+            p->smem = swapped_smem_bytes(bn);
+        }
+        p->k_blocks = static_cast<int>((p->k + 63) / 64);
+        const long long tiles = static_cast<long long>(p->tiles_m) * p->tiles_n;
+        long long grid = tiles < p->sm_count ? tiles : p->sm_count;
+        if (p->opt_grid > 0 && p->opt_grid < grid) grid = p->opt_grid;
+        p->grid = static_cast<int>(grid);
+        int gm = p->opt_group_m ? p->opt_group_m : 16;
+        if (gm > p->tiles_m) gm = p->tiles_m;
+        p->group_m = gm < 1 ? 1 : gm;
+    }
+    static const char* vname[] = {"empty", "row-tile", "swapped", "bias-only"};
+    static const char* ename[] = {"BIAS", "RELU_BIAS", "GELU_BIAS", "RELU_AUX_BIAS",
+                                  "BIAS_RESIDUAL", "NONE"};
+    snprintf(p->desc, sizeof(p->desc),
+             "m=%lld n=%lld k=%lld dtype=%s epilog=%s bias=%s variant=%s tile=128x%d bk=64 "
+             "stages=%d smem=%d tiles=%dx%d k_blocks=%d grid=%d group_m=%d sms=%d",
+             static_cast<long long>(p->m), static_cast<long long>(p->n),
+             static_cast<long long>(p->k), p->dtype == GEMM_EPI_BF16 ? "bf16" : "f16",
+             ename[p->epilog], p->bias_layout == GEMM_EPI_BIAS_M1 ? "(m,1)" : "(1,n)",
+             vname[p->variant], p->bn, p->stages, p->smem, p->tiles_m, p->tiles_n, p->k_blocks,
+             p->grid, p->group_m, p->sm_count);
+    if (p->variant == kRowTile || p->variant == kSwapped) {
+        cudaError_t e = p->variant == kRowTile ? rowtile_prepare(p->bn) : swapped_prepare(p->bn);
+        if (e != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
+    }
+    const char* log = getenv("GEMM_EPI_LOG");
+    if (log && log[0] == '1') fprintf(stderr, "[gemm_epi] plan: %s\n", p->desc);
+    return GEMM_EPI_OK;
+}
+
+bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,
+               uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+gemm_epi_status ensure_maps(gemm_epi_plan_s* p, const void* A, const void* B, void* D)
+{
+    if (p->maps_valid && p->key_A == A && p->key_B == B && p->key_D == D) return GEMM_EPI_OK;
+    p->maps_valid = false;
+    const CUtensorMapDataType dt = p->dtype == GEMM_EPI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint32_t a_rows = p->variant == kRowTile ? 128u : static_cast<uint32_t>(p->bn);
+    if (!encode_2d(&p->tm_A, A, dt, p->k, p->m, 64, a_rows, CU_TENSOR_MAP_SWIZZLE_128B))
+        return GEMM_EPI_ERR_LAUNCH;
+    if (!encode_2d(&p->tm_B, B, dt, p->n, p->k, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return GEMM_EPI_ERR_LAUNCH;
+    if (p->variant == kRowTile) {
+        if (!encode_2d(&p->tm_D, D, dt, p->n, p->m, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+            return GEMM_EPI_ERR_LAUNCH;
+    } else {
+        memset(&p->tm_D, 0, sizeof(p->tm_D));
+    }
+    p->key_A = A;
+    p->key_B = B;
+    p->key_D = D;
+    p->maps_valid = true;
+    return GEMM_EPI_OK;
+}
+
+gemm_epi_status check_device(const gemm_epi_plan_s* p)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_EPI_ERR_NO_DEVICE;
+    if (dev != p->device) return GEMM_EPI_ERR_INVALID_ARG;
+    return GEMM_EPI_OK;
+}
+
+gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const void* A, const void* B, const void* bias,
+                            const void* residual, void* D, uint32_t* aux, int epilog,
+                            cudaStream_t stream)
+{
+    gemm_epi_status st = ensure_maps(p, A, B, D);
+    if (st != GEMM_EPI_OK) return st;
+    GemmParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.tm_A = p->tm_A;
+    prm.tm_B = p->tm_B;
+    prm.tm_D = p->tm_D;
+    prm.bias = bias;
+    prm.residual = residual;
+    prm.D = D;
+    prm.aux = aux;
+    prm.status = p->d_status;
+    prm.wait_limit_ns = p->wait_limit_ns;
+    prm.m = static_cast<int>(p->m);
+    prm.n = static_cast<int>(p->n);
+    prm.k = static_cast<int>(p->k);
+    prm.tiles_m = p->tiles_m;
+    prm.tiles_n = p->tiles_n;
+    prm.k_blocks = p->k_blocks;
+    prm.group_m = p->group_m;
+    prm.epilog = epilog;
+    prm.bias_layout = p->bias_layout;
+    prm.bf16 = p->dtype == GEMM_EPI_BF16 ? 1 : 0;
+    prm.aux_ld = static_cast<int>((p->n + 31) / 32);
+    prm.debug_stall = p->debug_stall;
+    cudaError_t e = p->variant == kRowTile ? rowtile_launch(p->bn, prm, p->grid, stream)
+                                           : swapped_launch(p->bn, prm, p->grid, stream);
+    return e == cudaSuccess ? GEMM_EPI_OK : GEMM_EPI_ERR_LAUNCH;
+}
+
+gemm_epi_status check_operands(const gemm_epi_plan_s* p, const void* A, const void* B,
+                               const void* bias, const void* residual, const void* D,
+                               const uint32_t* aux)
+{
+    const bool needs_res = p->epilog == GEMM_EPI_BIAS_RESIDUAL;
+    const bool needs_aux = p->epilog == GEMM_EPI_RELU_AUX_BIAS;
+    if ((aux != nullptr) != needs_aux) return GEMM_EPI_ERR_INVALID_ARG;
+    if ((residual != nullptr) != needs_res) return GEMM_EPI_ERR_INVALID_ARG;
+    if (p->variant == kEmpty) return GEMM_EPI_OK;
+    if (!D) return GEMM_EPI_ERR_INVALID_ARG;
+    if (p->k > 0 && (!A || !B)) return GEMM_EPI_ERR_INVALID_ARG;
+    if (p->epilog != GEMM_EPI_NONE && !bias) return GEMM_EPI_ERR_INVALID_ARG;
+    if (!aligned(D, 16) || (A && !aligned(A, 16)) || (B && !aligned(B, 16)) ||
+        (residual && !aligned(residual, 16)) || (bias && !aligned(bias, 2)) ||
+        (aux && !aligned(aux, 4)))
+        return GEMM_EPI_ERR_MISALIGNED;
+    return GEMM_EPI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_epi_status gemm_epi_plan(gemm_epi_plan_t* out, int64_t m, int64_t n, int64_t k,
+                              gemm_epi_dtype dtype, gemm_epi_epilog epilog,
+                              gemm_epi_bias_layout bias_layout)
+{
+    if (!out) return GEMM_EPI_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
+    if (epilog < GEMM_EPI_BIAS || epilog > GEMM_EPI_NONE) return GEMM_EPI_ERR_INVALID_ARG;
+    if (bias_layout != GEMM_EPI_BIAS_M1 && bias_layout != GEMM_EPI_BIAS_1N)
+        return GEMM_EPI_ERR_INVALID_ARG;
+    const int64_t kMax = (1ll << 31) - 1;
+    if (m < 0 || n < 0 || k < 0 || m > kMax || n > kMax || k > kMax)
+        return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+    if (n % 8 != 0 || k % 8 != 0) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev < 1) {
+        cudaGetLastError();
+        return GEMM_EPI_ERR_NO_DEVICE;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_EPI_ERR_NO_DEVICE;
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3) return GEMM_EPI_ERR_ARCH;
+
+    gemm_epi_plan_s* p = new (std::nothrow) gemm_epi_plan_s();
+    if (!p) return GEMM_EPI_ERR_ALLOC;
+    p->m = m;
+    p->n = n;
+    p->k = k;
+    p->dtype = dtype;
+    p->epilog = epilog;
+    p->bias_layout = bias_layout;
+    p->device = dev;
+    p->sm_count = sms;
+    p->wait_limit_ns = kDefaultWaitNs;
+    if (cudaMalloc(reinterpret_cast<void**>(&p->d_status), sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        return GEMM_EPI_ERR_ALLOC;
+    }
+    if (cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess) {
+        cudaFree(p->d_status);
+        delete p;
+        return GEMM_EPI_ERR_ALLOC;
+    }
+    gemm_epi_status st = configure(p);
+    if (st != GEMM_EPI_OK) {
+        cudaFree(p->d_status);
+        delete p;
+        return st;
+    }
+    *out = p;
+    return GEMM_EPI_OK;
+}
+
+gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt, int64_t value)
+{
+    if (!p) return GEMM_EPI_ERR_INVALID_ARG;
+    gemm_epi_plan_s saved = *p;
+    switch (opt) {
+    case GEMM_EPI_OPT_VARIANT:
+        if (value < 0 || value > 2) return GEMM_EPI_ERR_INVALID_ARG;
+        p->opt_variant = static_cast<int>(value);
+        break;
+    case GEMM_EPI_OPT_TILE_N:
+        if (value != 0 && value != 64 && value != 128 && value != 256)
+            return GEMM_EPI_ERR_INVALID_ARG;
+        p->opt_bn = static_cast<int>(value);
+        break;
+    case GEMM_EPI_OPT_SPLIT_K:
+        if (value < 0 || value > 8) return GEMM_EPI_ERR_INVALID_ARG;
+        p->opt_split_k = static_cast<int>(value);
+        break;
+    case GEMM_EPI_OPT_GRID:
+        if (value < 0 || value > (1 << 20)) return GEMM_EPI_ERR_INVALID_ARG;
+        p->opt_grid = static_cast<int>(value);
+        break;
+    case GEMM_EPI_OPT_GROUP_M:
+        if (value < 0 || value > (1 << 20)) return GEMM_EPI_ERR_INVALID_ARG;
+        p->opt_group_m = static_cast<int>(value);
+        break;
+    case GEMM_EPI_OPT_WAIT_LIMIT_US:
+        if (value < 0 || value > 600ll * 1000 * 1000) return GEMM_EPI_ERR_INVALID_ARG;
+        p->wait_limit_ns = value == 0 ? kDefaultWaitNs : static_cast<unsigned long long>(value) * 1000ull;
+        return GEMM_EPI_OK;
+    case GEMM_EPI_OPT_DEBUG_STALL:
+        if (value != 0 && value != 1) return GEMM_EPI_ERR_INVALID_ARG;
+        p->debug_stall = static_cast<int>(value);
+        return GEMM_EPI_OK;
+    default:
+        return GEMM_EPI_ERR_INVALID_ARG;
+    }
+    gemm_epi_status st = configure(p);
+    if (st != GEMM_EPI_OK) {
+        *p = saved;  // keep the previous, valid configuration
+        p->maps_valid = false;
+    }
+    return st;
+}
+
+gemm_epi_status gemm_epi_execute_ex(gemm_epi_plan_t p, const void* A, const void* B,
+                                    const void* bias, const void* residual, void* D,
+                                    uint32_t* aux, cudaStream_t stream)
+{
+    if (!p) return GEMM_EPI_ERR_INVALID_ARG;
+    gemm_epi_status st = check_operands(p, A, B, bias, residual, D, aux);
+    if (st != GEMM_EPI_OK) return st;
+    if (p->variant == kEmpty) return GEMM_EPI_OK;
+    st = check_device(p);
+    if (st != GEMM_EPI_OK) return st;
+    const int bf16 = p->dtype == GEMM_EPI_BF16 ? 1 : 0;
+    const int aux_ld = static_cast<int>((p->n + 31) / 32);
+    if (p->variant == kBiasOnly) {
+        cudaError_t e = elementwise_launch(nullptr, bias, residual, D, aux, static_cast<int>(p->m),
+                                           static_cast<int>(p->n), p->epilog, p->bias_layout, bf16,
+                                           aux_ld, p->sm_count, stream);
+        return e == cudaSuccess ? GEMM_EPI_OK : GEMM_EPI_ERR_LAUNCH;
+    }
+    return launch_gemm(p, A, B, bias, residual, D, aux, p->epilog, stream);
+}
+
+gemm_epi_status gemm_epi_execute(gemm_epi_plan_t p, const void* A, const void* B,
+                                 const void* bias, void* D, uint32_t* aux, cudaStream_t stream)
+{
+    if (p && p->epilog == GEMM_EPI_BIAS_RESIDUAL) return GEMM_EPI_ERR_INVALID_ARG;
+    return gemm_epi_execute_ex(p, A, B, bias, nullptr, D, aux, stream);
+}
+
+gemm_epi_status gemm_epi_execute_unfused(gemm_epi_plan_t p, const void* A, const void* B,
+                                         const void* bias, const void* residual, void* pre,
+                                         void* D, uint32_t* aux, cudaStream_t stream)
+{
+    if (!p) return GEMM_EPI_ERR_INVALID_ARG;
+    gemm_epi_status st = check_operands(p, A, B, bias, residual, D, aux);
+    if (st != GEMM_EPI_OK) return st;
+    if (p->variant == kEmpty) return GEMM_EPI_OK;
+    if (!pre) return GEMM_EPI_ERR_INVALID_ARG;
+    if (!aligned(pre, 16)) return GEMM_EPI_ERR_MISALIGNED;
+    st = check_device(p);
+    if (st != GEMM_EPI_OK) return st;
+    const int bf16 = p->dtype == GEMM_EPI_BF16 ? 1 : 0;
+    const int aux_ld = static_cast<int>((p->n + 31) / 32);
+    const void* pre_in = nullptr;
+    if (p->variant != kBiasOnly) {
+        st = launch_gemm(p, A, B, nullptr, nullptr, pre, nullptr, EPI_NONE, stream);
+        if (st != GEMM_EPI_OK) return st;
+        pre_in = pre;
+    }
+    cudaError_t e = elementwise_launch(pre_in, bias, residual, D, aux, static_cast<int>(p->m),
+                                       static_cast<int>(p->n), p->epilog, p->bias_layout, bf16,
+                                       aux_ld, p->sm_count, stream);
+    return e == cudaSuccess ? GEMM_EPI_OK : GEMM_EPI_ERR_LAUNCH;
+}
+
+gemm_epi_status gemm_epi_free(gemm_epi_plan_t p)
+{
+    if (!p) return GEMM_EPI_OK;
+    if (p->d_status) cudaFree(p->d_status);
+    delete p;
+    return GEMM_EPI_OK;
+}
+
+gemm_epi_status gemm_epi_sync_status(gemm_epi_plan_t p, cudaStream_t stream)
+{
+    if (!p) return GEMM_EPI_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
+    int h = 0;
+    if (cudaMemcpy(&h, p->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMM_EPI_ERR_LAUNCH;
+    if (h != 0) {
+        cudaMemset(p->d_status, 0, sizeof(int));
+        return GEMM_EPI_ERR_DEVICE_TIMEOUT;
+    }
+    return GEMM_EPI_OK;
+}
+
+const char* gemm_epi_status_string(gemm_epi_status s)
+{
+    switch (s) {
+    case GEMM_EPI_OK: return "GEMM_EPI_OK";
+    case GEMM_EPI_ERR_INVALID_ARG: return "GEMM_EPI_ERR_INVALID_ARG: invalid argument";
+    case GEMM_EPI_ERR_UNSUPPORTED_SHAPE:
+        return "GEMM_EPI_ERR_UNSUPPORTED_SHAPE: sizes must be >= 0 and n, k multiples of 8";
+    case GEMM_EPI_ERR_MISALIGNED: return "GEMM_EPI_ERR_MISALIGNED: pointer alignment";
+    case GEMM_EPI_ERR_NO_DEVICE: return "GEMM_EPI_ERR_NO_DEVICE: no CUDA device";
+    case GEMM_EPI_ERR_ARCH: return "GEMM_EPI_ERR_ARCH: the current device is not sm_103";
+    case GEMM_EPI_ERR_ALLOC: return "GEMM_EPI_ERR_ALLOC: allocation failed";
+    case GEMM_EPI_ERR_LAUNCH: return "GEMM_EPI_ERR_LAUNCH: CUDA launch or encode failed";
+    case GEMM_EPI_ERR_DEVICE_TIMEOUT:
+        return "GEMM_EPI_ERR_DEVICE_TIMEOUT: a kernel gave up on a device-side wait";
+    default: return "GEMM_EPI_ERR_UNKNOWN";
+    }
+}
+
+const char* gemm_epi_plan_describe(gemm_epi_plan_t p) { return p ? p->desc : ""; }
+
+int64_t gemm_epi_aux_words_per_row(int64_t n) { return n <= 0 ? 0 : (n + 31) / 32; }
+
+}  // extern "C"

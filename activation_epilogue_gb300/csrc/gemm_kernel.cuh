@@ -1,0 +1,533 @@
+// Fused GEMM + bias/activation epilogue for sm_103a.
+//
+// D = epi(A . B + bias), computed as in "Fusing bias into cuBLASLt matmul with
+// nvmath-python for PyTorch inference" (blog.hotdry.top, 2025-09-22): the bias is added and
+// the activation applied right after the core GEMM, inside the same thread block, and the
+// intermediate matrix is never written back to device memory.
+//
+// One persistent CTA per SM, six warps with fixed roles:
+//   warp 0      TMA producer: one thread streams 64-deep K blocks of both operands into a
+//               ring of shared-memory stages (128-byte swizzle), arming a "full" mbarrier
+//               with the byte count of each stage.
+//   warp 1      allocates tensor memory; one thread issues tcgen05.mma (fp32 accumulate)
+//               into one of two TMEM accumulators and commits each consumed stage back to
+//               its "empty" mbarrier, and each finished tile to a "tmem full" mbarrier.
+//   warps 2-5   epilogue: each warp owns one 32-lane quarter of the accumulator; it reads
+//               32 columns at a time from TMEM, adds the bias (staged per warp in shared
+//               memory when it varies along the columns), applies the activation, builds
+//               the ReLU mask words, rounds to 16 bits and writes D through a swizzled
+//               shared-memory box and a TMA store.  While it drains one accumulator the
+//               MMA warp fills the other, so the epilogue overlaps the next tile's GEMM.
+//
+// Every mbarrier wait is bounded by a time limit; on expiry the waiting thread records the
+// failure in the plan's status word and raises a shared abort flag, every role leaves its
+// loop, in-flight copies and MMAs are drained, tensor memory is freed and the kernel returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernel_params.h"
+#include "ptx.cuh"
+
+namespace gemm_epi {
+
+constexpr int kBM = 128;        // MMA M: TMEM lanes
+constexpr int kBK = 64;         // K block: one 128-byte swizzle row of 16-bit elements
+constexpr int kUmmaK = 16;      // K of one tcgen05.mma.kind::f16
+constexpr int kThreads = 192;   // 6 warps
+constexpr int kEpiThreads = 128;
+constexpr int kPipeBudget = 192 * 1024;
+
+template <int BN>
+struct TileCfg {
+    static constexpr int kABytes = kBM * kBK * 2;  // MMA-A operand: 128 rows x 64 k
+    static constexpr int kBBytes = BN * kBK * 2;   // MMA-B operand: BN rows x 64 k
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStagesRaw = kPipeBudget / kStageBytes;
+    static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+    static constexpr int kChunk = BN < 32 ? BN : 32;            // columns per TMEM load
+    static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
+    static constexpr int kOffEpi = kStages * kStageBytes;        // 4 warps x 2 x 2 KB
+    static constexpr int kEpiBytes = 4 * 2 * 2048;
+    static constexpr int kOffBias = kOffEpi + kEpiBytes;         // 4 warps x 256 fp32
+    static constexpr int kBiasBytes = 4 * 256 * 4;
+    static constexpr int kOffBar = kOffBias + kBiasBytes;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
+    static_assert(kStages >= 2, "pipeline needs two stages");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+// mbarrier slots in the barrier area
+constexpr int kBarFull = 0;        // [8]
+constexpr int kBarEmpty = 8;       // [8]
+constexpr int kBarTmemFull = 16;   // [2]
+constexpr int kBarTmemEmpty = 18;  // [2]
+constexpr int kBarStall = 20;
+constexpr int kBarDrain = 21;
+constexpr int kOffHolder = 22 * 8;  // TMEM base address written by tcgen05.alloc
+constexpr int kOffAbort = kOffHolder + 4;
+
+constexpr unsigned long long kDrainLimitNs = 20ull * 1000 * 1000;  // 20 ms
+
+// Wait for the phase of `bar` with parity `parity` to complete.  Gives up (returns false)
+// when the abort flag is raised or after limit_ns nanoseconds; also after limit_ns / 8
+// polls, in case the global timer does not advance.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             const volatile int* abort_flag,
+                                             unsigned long long limit_ns, bool honour_abort = true)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    const unsigned long long max_polls = limit_ns / 8 + 1024;
+    for (unsigned long long poll = 1; poll < max_polls; ++poll) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((poll & 63) == 0) {
+            if (honour_abort && *abort_flag) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        }
+    }
+    return false;
+}
+
+__device__ __forceinline__ void record_failure(int* status, volatile int* abort_flag, int role)
+{
+    *abort_flag = 1;
+    __threadfence_block();
+    atomicCAS(status, 0, kCodeTimeout | role);
+}
+
+__device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& tm, int& tn)
+{
+    // Groups of group_m MMA-row tiles; inside a group the row tile varies fastest, so the
+    // CTAs running at one time share a few B panels and a few A panels in L2.
+    const int per_group = p.group_m * p.tiles_n;
+    const int g = tile / per_group;
+    const int first = g * p.group_m;
+    const int rows_in_group = min(p.tiles_m - first, p.group_m);
+    const int r = tile - g * per_group;
+    tm = first + r % rows_in_group;
+    tn = r / rows_in_group;
+}
+
+__device__ __forceinline__ float load_16bit(const void* base, long long idx, int bf16)
+{
+    const uint16_t h = static_cast<const uint16_t*>(base)[idx];
+    if (bf16) return __uint_as_float(static_cast<uint32_t>(h) << 16);
+    return __half2float(__ushort_as_half(h));
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, int bf16)
+{
+    if (bf16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint16_t to16(float a, int bf16)
+{
+    if (bf16) return __bfloat16_as_ushort(__float2bfloat16_rn(a));
+    return __half_as_ushort(__float2half_rn(a));
+}
+
+// erf-form GELU in fp32: x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)).
+__device__ __forceinline__ float gelu_erf(float x)
+{
+    return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+}
+
+// ------------------------------------------------------------------------------------------
+// producer: TMA loads
+// ------------------------------------------------------------------------------------------
+template <int BN, bool SWAP>
+__device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase, uint32_t bar0,
+                                             volatile int* abort_flag)
+{
+    using C = TileCfg<BN>;
+    const int num_tiles = p.tiles_m * p.tiles_n;
+    int stage = 0;
+    uint32_t phase = 0;
+    long long issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        int tm, tn;
+        tile_coords(tile, p, tm, tn);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!wait_bounded(bar0 + 8u * (kBarEmpty + stage), phase ^ 1u, abort_flag,
+                              p.wait_limit_ns)) {
+                if (!*abort_flag) record_failure(p.status, abort_flag, kRoleProducer);
+                ok = false;
+                break;
+            }
+            const uint32_t fb = bar0 + 8u * (kBarFull + stage);
+            mbar_arrive_expect_tx(fb, C::kStageBytes);
+            const uint32_t sa = sbase + stage * C::kStageBytes;
+            const uint32_t sb = sa + C::kABytes;
+            const int k0 = kb * kBK;
+            if (!SWAP) {
+                tma_load_2d(sa, &p.tm_A, fb, k0, tm * kBM);
+#pragma unroll
+                for (int q = 0; q < BN / 64; ++q)
+                    tma_load_2d(sb + q * 8192, &p.tm_B, fb, tn * BN + q * 64, k0);
+            } else {
+                tma_load_2d(sa, &p.tm_B, fb, tm * kBM, k0);
+                tma_load_2d(sa + 8192, &p.tm_B, fb, tm * kBM + 64, k0);
+                tma_load_2d(sb, &p.tm_A, fb, k0, tn * BN);
+            }
+            ++issued;
+            if (++stage == C::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok) {
+        // Let the copies already issued land before the CTA can exit.
+        const long long back = issued < C::kStages ? issued : C::kStages;
+        for (long long j = 1; j <= back; ++j) {
+            const long long f = issued - j;
+            const int s = static_cast<int>(f % C::kStages);
+            const uint32_t ph = static_cast<uint32_t>((f / C::kStages) & 1);
+            wait_bounded(bar0 + 8u * (kBarFull + s), ph, abort_flag, kDrainLimitNs, false);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// MMA issuer
+// ------------------------------------------------------------------------------------------
+template <int BN, bool SWAP>
+__device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uint32_t bar0,
+                                        uint32_t tmem_base, volatile int* abort_flag)
+{
+    using C = TileCfg<BN>;
+    // Row-tile: A operand K-major (rows of A), B operand N-major (rows of B).
+    // Swapped:  A operand N-major (rows of B), B operand K-major (rows of A).
+    const uint32_t idesc = make_idesc_f16(static_cast<uint32_t>(p.bf16), SWAP ? 1u : 0u,
+                                          SWAP ? 0u : 1u, kBM, BN);
+    const int num_tiles = p.tiles_m * p.tiles_n;
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool issued_any = false;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        if (!wait_bounded(bar0 + 8u * (kBarTmemEmpty + acc), acc_phase ^ 1u, abort_flag,
+                          p.wait_limit_ns)) {
+            if (!*abort_flag) record_failure(p.status, abort_flag, kRoleMma);
+            ok = false;
+            break;
+        }
+        tcgen05_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!wait_bounded(bar0 + 8u * (kBarFull + stage), phase, abort_flag,
+                              p.wait_limit_ns)) {
+                if (!*abort_flag) record_failure(p.status, abort_flag, kRoleMma);
+                ok = false;
+                break;
+            }
+            tcgen05_fence_after_sync();
+            const uint32_t sa = sbase + stage * C::kStageBytes;
+            const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+            for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                uint64_t ad, bd;
+                if (!SWAP) {
+                    // K-major: +32 bytes per 16-element K step inside the swizzled row;
+                    // 8-row groups 1024 bytes apart.
+                    ad = make_sdesc_sw128(sa + kk * 32, 0, 1024);
+                    // N-major: 64-column panels 8 KB apart, 8-row K groups 1 KB apart;
+                    // a 16-deep K step is 16 rows of 128 bytes.
+                    bd = make_sdesc_sw128(sb + kk * 2048, 8192, 1024);
+                } else {
+                    ad = make_sdesc_sw128(sa + kk * 2048, 8192, 1024);
+                    bd = make_sdesc_sw128(sb + kk * 32, 0, 1024);
+                }
+                mma_f16_ss(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+            issued_any = true;
+            mma_commit(bar0 + 8u * (kBarEmpty + stage));  // stage free once these MMAs finish
+            if (++stage == C::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        mma_commit(bar0 + 8u * (kBarTmemFull + acc));  // accumulator ready for the epilogue
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok && issued_any) {
+        // Wait for every MMA this thread issued before tensor memory is released.
+        mma_commit(bar0 + 8u * kBarDrain);
+        wait_bounded(bar0 + 8u * kBarDrain, 0, abort_flag, kDrainLimitNs, false);
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// epilogue
+// ------------------------------------------------------------------------------------------
+
+// Apply the activation to one chunk in place: v[] holds acc + bias on entry.
+template <int N>
+__device__ __forceinline__ void activate(float (&v)[N], int epilog)
+{
+    if (epilog == EPI_RELU_BIAS || epilog == EPI_RELU_AUX_BIAS) {
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] = v[j] > 0.0f ? v[j] : 0.0f;
+    } else if (epilog == EPI_GELU_BIAS) {
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] = gelu_erf(v[j]);
+    }
+}
+
+template <int BN, bool SWAP>
+__device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem, uint32_t sbase,
+                                             uint32_t bar0, uint32_t tmem_base,
+                                             volatile int* abort_flag)
+{
+    using C = TileCfg<BN>;
+    constexpr int CH = C::kChunk;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int ew = warp - 2;             // epilogue warp 0..3
+    const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
+    const int num_tiles = p.tiles_m * p.tiles_n;
+    const bool has_bias = p.epilog != EPI_NONE;
+    // Bias that varies along the accumulator's columns (staged in shared memory) or along
+    // its lanes (one value per thread).
+    const bool col_bias = has_bias && (SWAP ? p.bias_layout == 0 : p.bias_layout == 1);
+    const bool lane_bias = has_bias && !col_bias;
+    const int col_limit = SWAP ? p.m : p.n;   // extent of the accumulator-column coordinate
+    const int lane_limit = SWAP ? p.n : p.m;  // extent of the accumulator-lane coordinate
+    // This warp's own bias staging area: no other warp reads it, so a __syncwarp orders it.
+    float* sbias = reinterpret_cast<float*>(smem + C::kOffBias) + ew * 256;
+    uint8_t* epi_buf = smem + C::kOffEpi + ew * 2 * 2048;
+    const uint32_t epi_buf_u32 = sbase + C::kOffEpi + ew * 2 * 2048;
+    const uint16_t* R = static_cast<const uint16_t*>(p.residual);
+    uint16_t* Dp = static_cast<uint16_t*>(p.D);
+    uint32_t nstore = 0;
+
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        int tm, tn;
+        tile_coords(tile, p, tm, tn);
+        const int col_base = tn * BN;                          // first accumulator column
+        const int lane_base = tm * kBM + quarter * 32;         // this warp's first lane coord
+        const int lane_idx = lane_base + lane;
+        if (*abort_flag) break;
+        if (col_bias) {
+            __syncwarp();  // every lane is done reading the previous tile's values
+            for (int i = lane; i < BN; i += 32) {
+                const int c = col_base + i;
+                sbias[i] = c < col_limit ? load_16bit(p.bias, c, p.bf16) : 0.0f;
+            }
+            __syncwarp();
+        }
+        const float lb = (lane_bias && lane_idx < lane_limit) ? load_16bit(p.bias, lane_idx, p.bf16)
+                                                              : 0.0f;
+
+        if (!wait_bounded(bar0 + 8u * (kBarTmemFull + acc), acc_phase, abort_flag,
+                          p.wait_limit_ns)) {
+            if (!*abort_flag) record_failure(p.status, abort_flag, kRoleEpilogue);
+            break;
+        }
+        tcgen05_fence_after_sync();
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                static_cast<uint32_t>(acc * BN);
+        const int valid_cols = min(BN, col_limit - col_base);
+        const int nchunks = (valid_cols + CH - 1) / CH;
+        const bool warp_live = lane_base < lane_limit;
+
+        for (int c = 0; c < nchunks; ++c) {
+            uint32_t r[32];
+            __syncwarp();
+            if constexpr (CH == 32)
+                tmem_load_32cols(t_lane + c * 32, r);
+            else
+                tmem_load_16cols(t_lane + c * 16, r);
+            float v[CH];
+#pragma unroll
+            for (int j = 0; j < CH; ++j)
+                v[j] = __uint_as_float(r[j]) + (col_bias ? sbias[c * CH + j] : lb);
+
+            if constexpr (!SWAP) {
+                // ---- rows of D on lanes: thread = one row, 32 consecutive columns ----
+                const int row = lane_idx;
+                const int col0 = col_base + c * CH;
+                if (p.epilog == EPI_RELU_AUX_BIAS) {
+                    uint32_t word = 0;
+#pragma unroll
+                    for (int j = 0; j < CH; ++j)
+                        word |= (v[j] > 0.0f && col0 + j < p.n) ? (1u << j) : 0u;
+                    if (row < p.m) p.aux[static_cast<long long>(row) * p.aux_ld + col0 / 32] = word;
+                }
+                activate(v, p.epilog);
+                if (p.epilog == EPI_BIAS_RESIDUAL && row < p.m) {
+                    const uint16_t* rrow = R + static_cast<long long>(row) * p.n + col0;
+                    if (col0 + CH <= p.n) {
+#pragma unroll
+                        for (int j8 = 0; j8 < CH / 8; ++j8) {
+                            const uint4 w = __ldg(reinterpret_cast<const uint4*>(rrow) + j8);
+                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const uint32_t lo = ww[h] & 0xFFFFu, hi = ww[h] >> 16;
+                                if (p.bf16) {
+                                    v[j8 * 8 + 2 * h] += __uint_as_float(lo << 16);
+                                    v[j8 * 8 + 2 * h + 1] += __uint_as_float(hi << 16);
+                                } else {
+                                    v[j8 * 8 + 2 * h] +=
+                                        __half2float(__ushort_as_half(static_cast<uint16_t>(lo)));
+                                    v[j8 * 8 + 2 * h + 1] +=
+                                        __half2float(__ushort_as_half(static_cast<uint16_t>(hi)));
+                                }
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < CH; ++j)
+                            if (col0 + j < p.n) v[j] += load_16bit(rrow, j, p.bf16);
+                    }
+                }
+                if (warp_live) {
+                    // 32 rows x 32 columns of 16-bit = one 2 KB box, 64-byte rows, stored
+                    // with the 64-byte swizzle (16-byte chunk q of row r at q ^ ((r>>1)&3)).
+                    const uint32_t buf = nstore & 1u;
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                    uint8_t* rowp = epi_buf + buf * 2048 + lane * 64;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 w;
+                        w.x = pack2(v[8 * q + 0], v[8 * q + 1], p.bf16);
+                        w.y = pack2(v[8 * q + 2], v[8 * q + 3], p.bf16);
+                        w.z = pack2(v[8 * q + 4], v[8 * q + 5], p.bf16);
+                        w.w = pack2(v[8 * q + 6], v[8 * q + 7], p.bf16);
+                        *reinterpret_cast<uint4*>(rowp + ((q ^ ((lane >> 1) & 3)) << 4)) = w;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tm_D, epi_buf_u32 + buf * 2048, col0, lane_base);
+                        bulk_commit_group();
+                    }
+                    ++nstore;
+                }
+            } else {
+                // ---- columns of D on lanes: thread = one column, CH consecutive rows ----
+                const int col = lane_idx;
+                const bool col_ok = col < p.n;
+                const int t0 = col_base + c * CH;
+                if (p.epilog == EPI_RELU_AUX_BIAS) {
+                    const int word_idx = lane_base / 32;
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) {
+                        const uint32_t word = __ballot_sync(0xFFFFFFFFu, col_ok && v[j] > 0.0f);
+                        if (lane == 0 && t0 + j < p.m && word_idx < p.aux_ld)
+                            p.aux[static_cast<long long>(t0 + j) * p.aux_ld + word_idx] = word;
+                    }
+                }
+                activate(v, p.epilog);
+#pragma unroll
+                for (int j = 0; j < CH; ++j) {
+                    const int t = t0 + j;
+                    if (col_ok && t < p.m) {
+                        const long long idx = static_cast<long long>(t) * p.n + col;
+                        float o = v[j];
+                        if (p.epilog == EPI_BIAS_RESIDUAL) o += load_16bit(R, idx, p.bf16);
+                        Dp[idx] = to16(o, p.bf16);
+                    }
+                }
+            }
+        }
+        tcgen05_fence_before_sync();
+        mbar_arrive(bar0 + 8u * (kBarTmemEmpty + acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+    if constexpr (!SWAP) {
+        if (lane == 0) bulk_wait_group<0>();
+    }
+    __syncwarp();
+}
+
+// ------------------------------------------------------------------------------------------
+// the kernel
+// ------------------------------------------------------------------------------------------
+template <int BN, bool SWAP>
+__global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_constant__ GemmParams p)
+{
+    using C = TileCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + C::kOffBar;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffBar + kOffHolder);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + kOffAbort);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar0 + 8u * (kBarFull + s), 1);
+            mbar_init(bar0 + 8u * (kBarEmpty + s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar0 + 8u * (kBarTmemFull + a), 1);
+            mbar_init(bar0 + 8u * (kBarTmemEmpty + a), kEpiThreads);
+        }
+        mbar_init(bar0 + 8u * kBarStall, 1);
+        mbar_init(bar0 + 8u * kBarDrain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&p.tm_A);
+        prefetch_tensormap(&p.tm_B);
+        if (!SWAP) prefetch_tensormap(&p.tm_D);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+        tmem_relinquish_alloc_permit();
+    }
+    tcgen05_fence_before_sync();
+    __syncthreads();
+    tcgen05_fence_after_sync();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (p.debug_stall) {
+        // Test of the timeout path: wait on a barrier that nothing arrives at.
+        if (threadIdx.x == 0 &&
+            !wait_bounded(bar0 + 8u * kBarStall, 0, abort_flag, p.wait_limit_ns, false))
+            record_failure(p.status, abort_flag, kRoleStallTest);
+        __syncthreads();
+    }
+
+    if (!*abort_flag) {
+        if (warp == 0) {
+            if (lane == 0) run_producer<BN, SWAP>(p, sbase, bar0, abort_flag);
+            __syncwarp();
+        } else if (warp == 1) {
+            if (lane == 0) run_mma<BN, SWAP>(p, sbase, bar0, tmem_base, abort_flag);
+            __syncwarp();
+        } else {
+            run_epilogue<BN, SWAP>(p, smem, sbase, bar0, tmem_base, abort_flag);
+        }
+    }
+
+    tcgen05_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tcgen05_fence_after_sync();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+}  // namespace gemm_epi

@@ -1,0 +1,70 @@
+// Swapped small-m kernel instantiations: D^T tiles of 128 columns of D by BN rows of D,
+// BN in {16, 32, 64, 128, 256}.
+#include "gemm_kernel.cuh"
+
+namespace gemm_epi {
+
+namespace {
+template <int BN>
+cudaError_t prepare_one()
+{
+    return cudaFuncSetAttribute(gemm_epi_kernel<BN, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                TileCfg<BN>::kSmemBytes);
+}
+
+template <int BN>
+cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = TileCfg<BN>::kSmemBytes;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, gemm_epi_kernel<BN, true>, p);
+}
+}  // namespace
+
+#define GEMM_EPI_SWAPPED_CASES(F) F(16) F(32) F(64) F(128) F(256)
+
+cudaError_t swapped_prepare(int bn)
+{
+    switch (bn) {
+#define F(X) case X: return prepare_one<X>();
+        GEMM_EPI_SWAPPED_CASES(F)
+#undef F
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t swapped_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream)
+{
+    switch (bn) {
+#define F(X) case X: return launch_one<X>(p, grid, stream);
+        GEMM_EPI_SWAPPED_CASES(F)
+#undef F
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int swapped_smem_bytes(int bn)
+{
+    switch (bn) {
+#define F(X) case X: return TileCfg<X>::kSmemBytes;
+        GEMM_EPI_SWAPPED_CASES(F)
+#undef F
+    default: return 0;
+    }
+}
+
+int swapped_stages(int bn)
+{
+    switch (bn) {
+#define F(X) case X: return TileCfg<X>::kStages;
+        GEMM_EPI_SWAPPED_CASES(F)
+#undef F
+    default: return 0;
+    }
+}
+
+}  // namespace gemm_epi

@@ -1,0 +1,72 @@
+// Parameters shared by the host API and the kernels (internal; not part of the C ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gemm_epi {
+
+enum Epilog : int {
+    EPI_BIAS = 0,
+    EPI_RELU_BIAS = 1,
+    EPI_GELU_BIAS = 2,
+    EPI_RELU_AUX_BIAS = 3,
+    EPI_BIAS_RESIDUAL = 4,
+    EPI_NONE = 5
+};
+
+// Device status word values: 0 = fine, else (kCodeTimeout | role).
+enum : int {
+    kCodeTimeout = 0x100,
+    kRoleProducer = 1,
+    kRoleMma = 2,
+    kRoleEpilogue = 3,
+    kRoleStallTest = 4
+};
+
+// One launch of the fused kernel.  The MMA tile is 128 rows (MMA M) by BN columns (MMA N)
+// with an fp32 accumulator in tensor memory.
+//   row-tile kernel:  MMA rows = rows of D (from A), MMA columns = columns of D (from B);
+//   swapped kernel:   MMA rows = columns of D (from B), MMA columns = rows of D (from A),
+//                     i.e. it computes D^T = B^T A^T, for small m.
+struct GemmParams {
+    CUtensorMap tm_A;  // A[m][k]: K-major boxes {64 k, rows}, 128-byte swizzle
+    CUtensorMap tm_B;  // B[k][n]: N-major boxes {64 n, 64 k}, 128-byte swizzle
+    CUtensorMap tm_D;  // D[m][n]: store boxes {32 n, 32 m}, 64-byte swizzle (row-tile kernel)
+    const void* bias;
+    const void* residual;
+    void* D;
+    uint32_t* aux;
+    int* status;
+    unsigned long long wait_limit_ns;
+    int m, n, k;
+    int tiles_m;    // tiles along the MMA rows (128 each)
+    int tiles_n;    // tiles along the MMA columns (BN each)
+    int k_blocks;   // 64-deep K blocks per tile
+    int group_m;    // raster: MMA-row tiles per group
+    int epilog;
+    int bias_layout;  // 0 = (m,1), 1 = (1,n)
+    int bf16;         // 1 = bfloat16, 0 = binary16
+    int aux_ld;       // uint32 words per aux row
+    int debug_stall;
+};
+
+// Row-tile kernel (BN in {64, 128, 256}) and swapped small-m kernel (BN in {16 ... 256}).
+cudaError_t rowtile_prepare(int bn);
+cudaError_t rowtile_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream);
+int rowtile_smem_bytes(int bn);
+int rowtile_stages(int bn);
+
+cudaError_t swapped_prepare(int bn);
+cudaError_t swapped_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream);
+int swapped_smem_bytes(int bn);
+int swapped_stages(int bn);
+
+// Elementwise epilogue over a 16-bit pre-activation (the unfused baseline's second kernel;
+// pre == nullptr means pre = 0, which serves k == 0).
+cudaError_t elementwise_launch(const void* pre, const void* bias, const void* residual, void* D,
+                               uint32_t* aux, int m, int n, int epilog, int bias_layout, int bf16,
+                               int aux_ld, int sm_count, cudaStream_t stream);
+
+}  // namespace gemm_epi

@@ -1,0 +1,202 @@
+"""Python binding of the C ABI in ``include/gemm_epi.h`` (ctypes; argument marshalling only).
+
+Every function has the C name and forwards to ``libgemmepi.so``; the tensors are PyTorch
+CUDA tensors, used only as device memory, and the stream is the current torch stream
+unless one is given.  All the computation happens in the library's kernels: if the
+library is missing or cannot be loaded, the calls raise instead of computing anything
+another way.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libgemmepi.so")
+
+DTYPE = {"f16": 0, "bf16": 1}
+EPILOG = {"BIAS": 0, "RELU_BIAS": 1, "GELU_BIAS": 2, "RELU_AUX_BIAS": 3, "BIAS_RESIDUAL": 4,
+          "NONE": 5}
+BIAS_LAYOUT = {"M1": 0, "1N": 1}
+OPTION = {"VARIANT": 0, "TILE_N": 1, "SPLIT_K": 2, "GRID": 3, "GROUP_M": 4,
+          "WAIT_LIMIT_US": 5, "DEBUG_STALL": 6}
+STATUS = {0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED_SHAPE", 3: "ERR_MISALIGNED",
+          4: "ERR_NO_DEVICE", 5: "ERR_ARCH", 6: "ERR_ALLOC", 7: "ERR_LAUNCH",
+          8: "ERR_DEVICE_TIMEOUT"}
+
+# Every symbol include/gemm_epi.h declares.
+EXPORTS = ["gemm_epi_plan", "gemm_epi_plan_set_option", "gemm_epi_execute",
+           "gemm_epi_execute_ex", "gemm_epi_execute_unfused", "gemm_epi_free",
+           "gemm_epi_sync_status", "gemm_epi_status_string", "gemm_epi_plan_describe",
+           "gemm_epi_aux_words_per_row"]
+
+_lib = None
+_lock = threading.Lock()
+
+
+class GemmEpiError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+def load_library(path: str | None = None):
+    """Load libgemmepi.so (raises OSError if it is not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        lib = ctypes.CDLL(path or LIB_PATH)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.gemm_epi_plan.restype = i32
+        lib.gemm_epi_plan.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i32, i32, i32]
+        lib.gemm_epi_plan_set_option.restype = i32
+        lib.gemm_epi_plan_set_option.argtypes = [vp, i32, i64]
+        lib.gemm_epi_execute.restype = i32
+        lib.gemm_epi_execute.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+        lib.gemm_epi_execute_ex.restype = i32
+        lib.gemm_epi_execute_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.gemm_epi_execute_unfused.restype = i32
+        lib.gemm_epi_execute_unfused.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.gemm_epi_free.restype = i32
+        lib.gemm_epi_free.argtypes = [vp]
+        lib.gemm_epi_sync_status.restype = i32
+        lib.gemm_epi_sync_status.argtypes = [vp, vp]
+        lib.gemm_epi_status_string.restype = ctypes.c_char_p
+        lib.gemm_epi_status_string.argtypes = [i32]
+        lib.gemm_epi_plan_describe.restype = ctypes.c_char_p
+        lib.gemm_epi_plan_describe.argtypes = [vp]
+        lib.gemm_epi_aux_words_per_row.restype = i64
+        lib.gemm_epi_aux_words_per_row.argtypes = [i64]
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().gemm_epi_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise GemmEpiError(status, what)
+
+
+def _ptr(t):
+    """Device address of a tensor (None -> NULL); raw integers pass through."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous (row-major)")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ---- the C functions, by name -------------------------------------------------------------
+
+def gemm_epi_plan(m: int, n: int, k: int, dtype: str, epilog: str, bias_layout: str = "1N"):
+    h = ctypes.c_void_p()
+    _check(load_library().gemm_epi_plan(ctypes.byref(h), m, n, k, DTYPE[dtype], EPILOG[epilog],
+                                        BIAS_LAYOUT[bias_layout]), "gemm_epi_plan")
+    return h.value
+
+
+def gemm_epi_plan_set_option(plan, option: str, value: int):
+    _check(load_library().gemm_epi_plan_set_option(plan, OPTION[option], int(value)),
+           f"gemm_epi_plan_set_option({option}={value})")
+
+
+def gemm_epi_execute(plan, A, B, bias, D, aux=None, stream=None):
+    _check(load_library().gemm_epi_execute(plan, _ptr(A), _ptr(B), _ptr(bias), _ptr(D),
+                                           _ptr(aux), _stream(stream)), "gemm_epi_execute")
+
+
+def gemm_epi_execute_ex(plan, A, B, bias, residual, D, aux=None, stream=None):
+    _check(load_library().gemm_epi_execute_ex(plan, _ptr(A), _ptr(B), _ptr(bias),
+                                              _ptr(residual), _ptr(D), _ptr(aux),
+                                              _stream(stream)), "gemm_epi_execute_ex")
+
+
+def gemm_epi_execute_unfused(plan, A, B, bias, residual, pre, D, aux=None, stream=None):
+    _check(load_library().gemm_epi_execute_unfused(plan, _ptr(A), _ptr(B), _ptr(bias),
+                                                   _ptr(residual), _ptr(pre), _ptr(D),
+                                                   _ptr(aux), _stream(stream)),
+           "gemm_epi_execute_unfused")
+
+
+def gemm_epi_free(plan):
+    _check(load_library().gemm_epi_free(plan), "gemm_epi_free")
+
+
+def gemm_epi_sync_status(plan, stream=None) -> int:
+    """Returns the status code (0, or 8 = a device-side wait ran out)."""
+    return int(load_library().gemm_epi_sync_status(plan, _stream(stream)))
+
+
+def gemm_epi_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def gemm_epi_plan_describe(plan) -> str:
+    return load_library().gemm_epi_plan_describe(plan).decode()
+
+
+def gemm_epi_aux_words_per_row(n: int) -> int:
+    return int(load_library().gemm_epi_aux_words_per_row(n))
+
+
+# ---- a small owner object around a plan ---------------------------------------------------
+
+class Plan:
+    """A plan with its free() tied to the object (context manager or explicit free())."""
+
+    def __init__(self, m, n, k, dtype="bf16", epilog="BIAS", bias_layout="1N", **options):
+        self.m, self.n, self.k = m, n, k
+        self.dtype, self.epilog, self.bias_layout = dtype, epilog, bias_layout
+        self.handle = gemm_epi_plan(m, n, k, dtype, epilog, bias_layout)
+        for key, value in options.items():
+            gemm_epi_plan_set_option(self.handle, key.upper(), value)
+
+    def set_option(self, option: str, value: int):
+        gemm_epi_plan_set_option(self.handle, option.upper(), value)
+
+    def describe(self) -> str:
+        return gemm_epi_plan_describe(self.handle)
+
+    def execute(self, A, B, bias, D, aux=None, residual=None, stream=None):
+        gemm_epi_execute_ex(self.handle, A, B, bias, residual, D, aux, stream)
+
+    def execute_unfused(self, A, B, bias, pre, D, aux=None, residual=None, stream=None):
+        gemm_epi_execute_unfused(self.handle, A, B, bias, residual, pre, D, aux, stream)
+
+    def sync_status(self, stream=None) -> int:
+        return gemm_epi_sync_status(self.handle, stream)
+
+    def free(self):
+        if self.handle:
+            gemm_epi_free(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.free()
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass

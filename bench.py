@@ -1,0 +1,501 @@
+#!/usr/bin/env python
+"""Benchmark of the fused GEMM + bias/activation epilogue on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one fused call D = RELU(A.B + bias) on the largest RELU_BIAS workload
+(A[65536,8192] . B[8192,16384], bf16 in and out, fp32 accumulate), inputs resident in
+device memory.  Every input is larger than L2, so no flush is needed between steps.
+Rank 0 prints one JSON line: whole-job TFLOP/s, the roofline of the fused kernel, the
+end-to-end figure through the same API with host buffers (copies inside the timed region),
+the CPU oracle timed on a bounded sample, SM clocks sampled during the timed region, and
+extras: the unfused baseline on the same workload, the other workloads, and small-m
+microseconds per call.
+
+Under torchrun (N > 1) each rank runs its own replica of the workload on its own GPU
+(the problem is independent per GPU; no collective is on the data path); the JSON value
+is the sum of all ranks' work divided by the slowest rank's time.
+
+--impl reference times the reference arm: the CPU oracle as it stands, on this host's
+cores, on a bounded sample of the same workload per step (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused GEMM+epilogue TFLOP/s and % of GB300 bf16 peak; µs/call at small M"
+HEADLINE = "relu_bias_bf16_65536x16384x8192"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---- clocks during the timed region ---------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"]
+        except Exception:
+            sel = []
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        pw = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ---- timing helpers -------------------------------------------------------------------------
+
+def time_steps(fn, steps: int, warmup: int, stream, dist_barrier=None) -> float:
+    """Seconds for `steps` calls of fn() on `stream`, CUDA events, synchronised both sides."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if dist_barrier:
+        dist_barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist_barrier:
+        dist_barrier()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def time_cold(fn, iters: int, stream, flush) -> float:
+    """Median seconds of fn() with L2 flushed before every call (events around the call)."""
+    import torch
+    ts = []
+    for i in range(iters + 2):
+        flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 2:
+            ts.append(e0.elapsed_time(e1) / 1e3)
+    return statistics.median(ts)
+
+
+def time_graph(fn, calls: int, replays: int, stream) -> float:
+    """Seconds per call from a CUDA graph of `calls` back-to-back calls (hot L2)."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(calls):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(replays):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / (calls * replays)
+
+
+# ---- the CPU oracle on a sample -------------------------------------------------------------
+
+def oracle_sample_rate(A_rows_host, B_host, bias_host, w, target_s: float):
+    """(TFLOP/s, rows, seconds) of the oracle on `rows` full rows of the workload, sized so
+    one call takes about target_s seconds."""
+    import numpy as np
+
+    import oracle
+    rows = min(8, A_rows_host.shape[0])
+    while True:
+        t0 = time.perf_counter()
+        oracle.gemm_epi(A_rows_host[:rows], B_host, bias_host, dtype=w.dtype, epilog=w.epilog,
+                        bias_layout=w.bias_layout)
+        dt = time.perf_counter() - t0
+        if dt >= target_s * 0.5 or rows >= A_rows_host.shape[0]:
+            break
+        rows = int(min(A_rows_host.shape[0], max(rows * 2, rows * target_s / max(dt, 1e-3))))
+    flops = 2.0 * rows * w.n * w.k
+    return flops / dt / 1e12, rows, dt
+
+
+def cpu_inputs_for(w, rows_needed: int, dev):
+    """Host copies of the first rows of A, all of B and the bias (drawn on the device)."""
+    from activation_epilogue_gb300 import workloads
+    inp = workloads.gemm_inputs(w, device=dev)
+    A = inp["A"][:rows_needed].cpu()
+    B = inp["B"].cpu()
+    b = inp["bias"].cpu()
+    del inp
+    return A, B, b
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample per step."""
+    import torch
+
+    import oracle
+    from activation_epilogue_gb300 import workloads
+    w = workloads.GEMMS[HEADLINE]
+    oracle.build()
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    A, B, b = cpu_inputs_for(w, 4096, dev)
+    rate, rows, dt = oracle_sample_rate(A, B, b, w, target_s=2.0)
+    ts = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.gemm_epi(A[:rows], B, b, dtype=w.dtype, epilog=w.epilog, bias_layout=w.bias_layout)
+        if i >= args.warmup:
+            ts.append(time.perf_counter() - t0)
+    total = sum(ts)
+    flops = 2.0 * rows * w.n * w.k
+    value = flops * len(ts) / total / 1e12
+    sample = (f"{rows} full rows (all {w.n} columns, k={w.k}) of the {w.m}x{w.n}x{w.k} "
+              f"{w.epilog} problem per step, fp64 oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / len(ts) * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": HEADLINE, "m": w.m, "n": w.n, "k": w.k, "epilog": w.epilog,
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---- our arm ----------------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank, dist):
+    import torch
+
+    from activation_epilogue_gb300 import build as libbuild
+    from activation_epilogue_gb300 import gemm_epi, workloads
+
+    libbuild.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peaks_src = load_peaks()
+    barrier = (lambda: dist.barrier()) if dist is not None else None
+
+    w = workloads.GEMMS[args.workload]
+    td = workloads.TORCH_DTYPES[w.dtype]
+    inp = workloads.gemm_inputs(w, device=dev)
+    A, B, bias = inp["A"], inp["B"], inp["bias"]
+    D = torch.empty((w.m, w.n), dtype=td, device=dev)
+    aux = None
+    if w.epilog == "RELU_AUX_BIAS":
+        aux = torch.empty((w.m, (w.n + 31) // 32), dtype=torch.int32, device=dev)
+    plan = gemm_epi.Plan(w.m, w.n, w.k, w.dtype, w.epilog, w.bias_layout)
+    log(f"[bench] rank {rank}: {plan.describe()}")
+
+    def step():
+        plan.execute(A, B, bias, D, aux=aux)
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    secs = time_steps(step, args.steps, 0, stream, barrier)
+    clocks = sampler.stop() if sampler else None
+    st = plan.sync_status()
+    if st != 0:
+        raise RuntimeError(f"device status {gemm_epi.status_string(st)}")
+
+    if dist is not None:
+        t = torch.tensor([secs], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        secs = float(t.item())
+    flops_step = float(w.flops)
+    value = flops_step * args.steps * world / secs / 1e12
+    kernel_s = secs / args.steps
+    if rank != 0:
+        plan.free()
+        return
+
+    achieved = flops_step / kernel_s / 1e12
+    sustained = secs >= 1.0
+    peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    traffic = load_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": kernel_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "m": w.m, "n": w.n, "k": w.k, "epilog": w.epilog,
+                   "bias_layout": "(1,n)" if w.bias_layout == "1N" else "(m,1)",
+                   "l2": "inputs larger than L2 (no flush needed)",
+                   "parallelism": f"replicas x{world}", "plan": plan.describe()},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peaks_src} {'sustained' if sustained else 'burst'} bf16"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    plan_ms = kernel_s * 1e3
+    log(f"[bench] fused: {plan_ms:.3f} ms/step, {achieved:.1f} TFLOP/s "
+        f"({100 * achieved / peak:.1f}% of {peaks_src} peak {peak:.0f})")
+
+    # e2e through the same API with host buffers: H2D of the inputs, D2H of the result
+    if not args.no_e2e:
+        line["e2e"] = measure_e2e(plan, w, A, B, bias, D, aux, stream, args)
+    # extras before the CPU work, while the device buffers are still held
+    if not args.no_extras:
+        del inp
+        line["extras"] = measure_extras(plan, w, A, B, bias, D, aux, stream, peaks)
+    plan.free()
+    del A, B, D, aux
+    torch.cuda.empty_cache()
+    if not args.no_cpu_baseline and world == 1:
+        Ah, Bh, bh = cpu_inputs_for(w, 4096, dev)
+        rate, rows, dt = oracle_sample_rate(Ah, Bh, bh, w, target_s=args.cpu_seconds)
+        import oracle
+        line["cpu_baseline"] = {
+            "value": rate, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{rows} full rows (all {w.n} columns, k={w.k}) of the "
+                      f"{w.m}x{w.n}x{w.k} {w.epilog} problem, fp64 oracle, {dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary, if any."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            return json.load(fh).get(workload)
+    except Exception:
+        return None
+
+
+def measure_e2e(plan, w, A, B, bias, D, aux, stream, args):
+    import torch
+    Ah = torch.empty(A.shape, dtype=A.dtype, pin_memory=True)
+    Bh = torch.empty(B.shape, dtype=B.dtype, pin_memory=True)
+    bh = torch.empty(bias.shape, dtype=bias.dtype, pin_memory=True)
+    Ah.copy_(A)
+    Bh.copy_(B)
+    bh.copy_(bias)
+    Dh = torch.empty(D.shape, dtype=D.dtype, pin_memory=True)
+    auxh = None if aux is None else torch.empty(aux.shape, dtype=aux.dtype, pin_memory=True)
+
+    def e2e_step():
+        A.copy_(Ah, non_blocking=True)
+        B.copy_(Bh, non_blocking=True)
+        bias.copy_(bh, non_blocking=True)
+        plan.execute(A, B, bias, D, aux=aux)
+        Dh.copy_(D, non_blocking=True)
+        if aux is not None:
+            auxh.copy_(aux, non_blocking=True)
+
+    steps = max(2, min(args.steps, 5))
+    secs = time_steps(e2e_step, steps, 1, stream)
+    h2d = (A.numel() + B.numel() + bias.numel()) * A.element_size()
+    d2h = D.numel() * D.element_size() + (0 if aux is None else aux.numel() * 4)
+    return {"value": float(w.flops) * steps / secs / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": secs / steps * 1e3, "steps": steps}
+
+
+def measure_extras(plan, w, A, B, bias, D, aux, stream, peaks):
+    """Unfused baseline on the headline workload; the other workloads; small-m us/call."""
+    import torch
+
+    from activation_epilogue_gb300 import gemm_epi, workloads
+    out = {}
+    # unfused on the same workload: GEMM writes pre (bf16), elementwise pass reads it back
+    pre = torch.empty_like(D)
+    t_unf = time_steps(lambda: plan.execute_unfused(A, B, bias, pre, D, aux=aux), 5, 2, stream)
+    out["unfused_same_workload"] = {"ms_per_step": t_unf / 5 * 1e3,
+                                    "tflops": float(w.flops) * 5 / t_unf / 1e12,
+                                    "launches_per_step": 2,
+                                    "extra_bytes": 2 * w.m * w.n * 2}
+    del pre
+    torch.cuda.empty_cache()
+
+    flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.int32, device=A.device)
+
+    def flush():
+        flush_buf.zero_()
+
+    per = {}
+    for name, g in workloads.GEMMS.items():
+        if name == w.name:
+            continue
+        td = workloads.TORCH_DTYPES[g.dtype]
+        inp = workloads.gemm_inputs(g, device=A.device)
+        Dg = torch.empty((g.m, g.n), dtype=td, device=A.device)
+        auxg = (torch.empty((g.m, (g.n + 31) // 32), dtype=torch.int32, device=A.device)
+                if g.epilog == "RELU_AUX_BIAS" else None)
+        with gemm_epi.Plan(g.m, g.n, g.k, g.dtype, g.epilog, g.bias_layout) as pg:
+            fn = lambda: pg.execute(inp["A"], inp["B"], inp["bias"], Dg, aux=auxg)  # noqa: E731
+            cold = time_cold(fn, 20, stream, flush)
+            hot = time_graph(fn, 20, 10, stream)
+            pre = torch.empty_like(Dg)
+            fu = lambda: pg.execute_unfused(inp["A"], inp["B"], inp["bias"], pre, Dg, aux=auxg)  # noqa: E731
+            cold_unf = time_cold(fu, 20, stream, flush)
+            st = pg.sync_status()
+            desc = pg.describe()
+        e = 2
+        unavoidable = (g.m * g.k + g.k * g.n + (g.m if g.bias_layout == "M1" else g.n)
+                       + g.m * g.n) * e + (0 if auxg is None else auxg.numel() * 4)
+        per[name] = {
+            "us_per_call_cold_l2": cold * 1e6, "us_per_call_graph_hot_l2": hot * 1e6,
+            "tflops_cold": g.flops / cold / 1e12,
+            "hbm_gbs_cold": unavoidable / cold / 1e9,
+            "hbm_frac_cold": unavoidable / cold / 1e9 / peaks["hbm_gbs"],
+            "tensor_frac_cold": g.flops / cold / 1e12 / peaks["bf16_tflops"],
+            "unfused_us_cold_l2": cold_unf * 1e6, "unavoidable_bytes": unavoidable,
+            "status": st, "plan": desc}
+        del inp, Dg, auxg, pre
+    # the FFN block: GEMM1 (bias + GELU) then GEMM2 (bias + residual), two launches
+    f = workloads.FFNS["ffn_bf16_4096x1024x4096"]
+    fi = workloads.ffn_inputs(f, device=A.device)
+    H = torch.empty((f.t, f.f), dtype=torch.bfloat16, device=A.device)
+    Y = torch.empty((f.t, f.d), dtype=torch.bfloat16, device=A.device)
+    with gemm_epi.Plan(f.t, f.f, f.d, "bf16", "GELU_BIAS", "1N") as p1, \
+            gemm_epi.Plan(f.t, f.d, f.f, "bf16", "BIAS_RESIDUAL", "1N") as p2:
+        def ffn():
+            p1.execute(fi["X"], fi["W1"], fi["b1"], H)
+            p2.execute(H, fi["W2"], fi["b2"], Y, residual=fi["R"])
+        cold = time_cold(ffn, 20, stream, flush)
+        hot = time_graph(ffn, 10, 10, stream)
+        per[f.name] = {"us_per_call_cold_l2": cold * 1e6, "us_per_call_graph_hot_l2": hot * 1e6,
+                       "tflops_cold": f.flops / cold / 1e12,
+                       "tensor_frac_cold": f.flops / cold / 1e12 / peaks["bf16_tflops"],
+                       "launches": 2, "status": [p1.sync_status(), p2.sync_status()],
+                       "plans": [p1.describe(), p2.describe()]}
+    out["workloads"] = per
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        log("[bench] warm-up raised to 3 steps")
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    try:
+        run_ours(args, rank, world, local_rank, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+/*
+ * gemm_epi.h -- C ABI of the fused GEMM + bias/activation epilogue library (sm_103a).
+ *
+ *   D[m,n] = epi(A[m,k] . B[k,n] + bias)
+ *
+ * computed in one kernel, with fp32 accumulation in tensor memory; the pre-activation
+ * (A.B + bias) is never written to or read back from device memory.
+ *
+ * Where the operations come from:
+ *   "Fusing bias into cuBLASLt matmul with nvmath-python for PyTorch inference"
+ *   (blog.hotdry.top, 2025-09-22):
+ *     - code example: a stateful Matmul(a, b) object, .plan(epilog=..., epilog_inputs=
+ *       {"bias": bias}), .execute(), .free(); m, n, k = 1024, 512, 2048, fp16, bias (m,1);
+ *     - paragraph on the BIAS / RELU_BIAS epilogs: one fused kernel instead of three
+ *       (matmul, bias add, activation), no intermediate written back to global memory;
+ *     - paragraph on operational parameters: input, weight and bias share one dtype; the
+ *       bias is (m,1) or (1,n), any other shape fails; the plan must be freed;
+ *     - paragraph on limitations: RELU_AUX_BIAS also produces the mask backward needs;
+ *     - closing paragraph: GELU named as a further epilog.
+ *   "nvmath-python: cuBLAS and cuSOLVER bindings for ML linear algebra"
+ *   (blog.hotdry.top, 2025-09-19), matmul-planning checklist: plan() chooses the algorithm,
+ *     execute() is non-blocking.
+ *   "Operator fusion in model inference, from LayerNorm to residual connections"
+ *   (wmrh.cn/news/429806), section 1 flowchart: the FFN chain matmul -> bias -> GELU ->
+ *     matmul -> bias; section 3: the residual add folded into the producing op.
+ *
+ * Conventions for every call:
+ *   - A is m x k, B is k x n, D and the residual are m x n: all row-major, contiguous,
+ *     of the plan's dtype, in device memory.  The bias has m elements for the (m,1)
+ *     layout and n for (1,n), same dtype.  The caller owns all of them; the library never
+ *     allocates, frees or keeps them beyond the call.
+ *   - aux (RELU_AUX_BIAS only) is uint32 [m][ceil(n/32)] in device memory: bit (j mod 32)
+ *     of word floor(j/32) in row i is 1 iff the fp32 pre-activation at (i, j) is > 0;
+ *     bits for columns >= n are written 0.
+ *   - Shapes: m, n, k >= 0; n and k must be multiples of 8 (rows of A, B and D start on
+ *     16-byte boundaries, which the tensor-memory-access unit needs).  m == 0 or n == 0 is
+ *     an empty problem (nothing is launched); k == 0 gives D = epi(bias broadcast).
+ *   - Pointers A, B, D, residual and the unfused pre buffer must be 16-byte aligned; bias
+ *     2-byte aligned; aux 4-byte aligned.  D must not overlap A, B or bias; D may be the
+ *     residual buffer itself (an in-place residual add).
+ *   - All execute calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and return launch-time errors only; a device-side wait that ran out
+ *     its time limit is reported by gemm_epi_sync_status.
+ *   - A plan belongs to the device that was current when it was made; execute with that
+ *     device current.  Free it only after the work that uses it has completed.  One plan
+ *     must not be executed from several host threads at the same time.
+ *   - No call aborts the process; every failure is a status code.
+ */
+#ifndef GEMM_EPI_H_
+#define GEMM_EPI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t, without requiring the CUDA headers (same definition as cuda_runtime). */
+typedef struct CUstream_st* cudaStream_t;
+
+/* Opaque plan: the chosen kernel configuration, cached tensor-memory-access descriptors and
+ * a device status word.  Owned by the library. */
+typedef struct gemm_epi_plan_s* gemm_epi_plan_t;
+
+typedef enum {
+    GEMM_EPI_F16 = 0,  /* IEEE binary16 inputs and output */
+    GEMM_EPI_BF16 = 1  /* bfloat16 inputs and output */
+} gemm_epi_dtype;
+
+typedef enum {
+    GEMM_EPI_BIAS = 0,          /* D = A.B + bias */
+    GEMM_EPI_RELU_BIAS = 1,     /* D = max(A.B + bias, 0)  (+0 for every pre <= 0) */
+    GEMM_EPI_GELU_BIAS = 2,     /* D = GELU(A.B + bias), erf form: x * Phi(x) */
+    GEMM_EPI_RELU_AUX_BIAS = 3, /* as RELU_BIAS, and writes the aux mask [pre > 0] */
+    GEMM_EPI_BIAS_RESIDUAL = 4, /* D = A.B + bias + residual (FFN second GEMM) */
+    GEMM_EPI_NONE = 5           /* D = A.B (no bias; bias pointer ignored) */
+} gemm_epi_epilog;
+
+typedef enum {
+    GEMM_EPI_BIAS_M1 = 0, /* bias shape (m,1): bias[i] added to every column of row i */
+    GEMM_EPI_BIAS_1N = 1  /* bias shape (1,n): bias[j] added to every row of column j */
+} gemm_epi_bias_layout;
+
+typedef enum {
+    GEMM_EPI_OK = 0,
+    GEMM_EPI_ERR_INVALID_ARG = 1,       /* null handle/pointer, bad enum, aux misuse */
+    GEMM_EPI_ERR_UNSUPPORTED_SHAPE = 2, /* negative size, n or k not a multiple of 8 */
+    GEMM_EPI_ERR_MISALIGNED = 3,        /* a pointer breaks the alignment rules above */
+    GEMM_EPI_ERR_NO_DEVICE = 4,         /* no CUDA device / driver */
+    GEMM_EPI_ERR_ARCH = 5,              /* the current device is not sm_103 */
+    GEMM_EPI_ERR_ALLOC = 6,             /* the plan's own device or host allocation failed */
+    GEMM_EPI_ERR_LAUNCH = 7,            /* a CUDA call failed while encoding or launching */
+    GEMM_EPI_ERR_DEVICE_TIMEOUT = 8     /* a kernel gave up on a wait (see sync_status) */
+} gemm_epi_status;
+
+/* Plan-time settings (gemm_epi_plan_set_option).  0 always means "automatic". */
+typedef enum {
+    GEMM_EPI_OPT_VARIANT = 0,       /* 1 = row-tile kernel, 2 = swapped small-m kernel */
+    GEMM_EPI_OPT_TILE_N = 1,        /* row-tile kernel: N tile 64, 128 or 256 */
+    GEMM_EPI_OPT_SPLIT_K = 2,       /* swapped kernel: K slices per output tile, 1..8 */
+    GEMM_EPI_OPT_GRID = 3,          /* cap on persistent CTAs (<= SM count) */
+    GEMM_EPI_OPT_GROUP_M = 4,       /* tile raster: M tiles per group */
+    GEMM_EPI_OPT_WAIT_LIMIT_US = 5, /* device-side wait limit, microseconds (default 2 s) */
+    GEMM_EPI_OPT_DEBUG_STALL = 6    /* 1: the next launches wait on a barrier nothing
+                                       arrives at, run out the wait limit and report
+                                       GEMM_EPI_ERR_DEVICE_TIMEOUT (a test of the timeout
+                                       path; no copy or MMA is issued) */
+} gemm_epi_option;
+
+/*
+ * Make a plan for one problem shape, dtype, epilog and bias layout (the page's
+ * Matmul(a, b).plan(epilog=..., epilog_inputs={"bias": ...})).  Validates the arguments,
+ * checks the current device, picks the kernel configuration and allocates the plan's
+ * device status word.  *out is set to NULL on failure.
+ */
+gemm_epi_status gemm_epi_plan(gemm_epi_plan_t* out, int64_t m, int64_t n, int64_t k,
+                              gemm_epi_dtype dtype, gemm_epi_epilog epilog,
+                              gemm_epi_bias_layout bias_layout);
+
+/* Override one automatic choice of the plan (benchmarking and tests). */
+gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt,
+                                         int64_t value);
+
+/*
+ * Run the fused kernel: D = epi(A.B + bias), and the aux mask for RELU_AUX_BIAS (the
+ * page's .execute()).  aux must be non-NULL exactly for RELU_AUX_BIAS.  Not valid for
+ * BIAS_RESIDUAL (use gemm_epi_execute_ex).  bias may be NULL only for NONE.
+ */
+gemm_epi_status gemm_epi_execute(gemm_epi_plan_t p, const void* A, const void* B,
+                                 const void* bias, void* D, uint32_t* aux,
+                                 cudaStream_t stream);
+
+/* As gemm_epi_execute, with the residual operand (required for BIAS_RESIDUAL, must be
+ * NULL otherwise). */
+gemm_epi_status gemm_epi_execute_ex(gemm_epi_plan_t p, const void* A, const void* B,
+                                    const void* bias, const void* residual, void* D,
+                                    uint32_t* aux, cudaStream_t stream);
+
+/*
+ * The unfused baseline, for measuring what the fusion saves: one GEMM kernel writes
+ * pre0 = A.B rounded to the plan's dtype into the caller's `pre` buffer (m x n), then one
+ * elementwise kernel reads it back with the bias (and residual), applies the epilog and
+ * writes D (and aux).  Two launches, one extra round trip of m*n 16-bit values.
+ */
+gemm_epi_status gemm_epi_execute_unfused(gemm_epi_plan_t p, const void* A, const void* B,
+                                         const void* bias, const void* residual, void* pre,
+                                         void* D, uint32_t* aux, cudaStream_t stream);
+
+/* Release the plan (the page's .free()).  NULL is accepted and ignored. */
+gemm_epi_status gemm_epi_free(gemm_epi_plan_t p);
+
+/*
+ * Wait for `stream`, then read and clear the plan's device status word.  Returns
+ * GEMM_EPI_ERR_DEVICE_TIMEOUT if a kernel launched with this plan gave up on a
+ * device-side wait since the last call, else GEMM_EPI_OK (or ERR_LAUNCH if the stream
+ * itself reports an error).
+ */
+gemm_epi_status gemm_epi_sync_status(gemm_epi_plan_t p, cudaStream_t stream);
+
+/* Static string for a status code. */
+const char* gemm_epi_status_string(gemm_epi_status s);
+
+/* The plan's configuration as text (kernel variant, tiles, stages, grid), owned by the
+ * plan; the info log the matmul-planning checklist recommends reading. */
+const char* gemm_epi_plan_describe(gemm_epi_plan_t p);
+
+/* Number of uint32 words in one row of the aux mask: ceil(n / 32). */
+int64_t gemm_epi_aux_words_per_row(int64_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_EPI_H_ */

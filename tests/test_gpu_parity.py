@@ -1,0 +1,226 @@
+"""GPU parity: the fused kernels through the C ABI against the CPU oracle, element by element,
+at sizes that span several tiles and ragged tails in M, N and K."""
+import numpy as np
+import pytest
+import torch
+
+from activation_epilogue_gb300 import gemm_epi, workloads
+from parity_helpers import TD, TOL, check, rel_err, run
+
+pytestmark = pytest.mark.gpu
+
+EPILOGS = ["BIAS", "RELU_BIAS", "GELU_BIAS", "RELU_AUX_BIAS", "BIAS_RESIDUAL", "NONE"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from activation_epilogue_gb300 import build
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+
+
+def _inputs(m, n, k, dtype, layout, seed, kind="normal"):
+    return workloads.random_problem(m, n, k, dtype=dtype, bias_layout=layout, residual=True,
+                                    seed=seed, kind=kind)
+
+
+# ---- row-tile kernel: every N tile width, epilog, dtype and both bias layouts --------------
+
+@pytest.mark.parametrize("bn", [64, 128, 256])
+@pytest.mark.parametrize("epilog", EPILOGS)
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_rowtile_parity(bn, epilog, dtype):
+    m, n, k = 300, 520, 200            # 3 ragged M tiles, ragged N tiles, 4 K blocks (last 8)
+    layout = "M1" if (bn // 64 + EPILOGS.index(epilog)) % 2 else "1N"
+    p = _inputs(m, n, k, dtype, layout, seed=bn + 7 * EPILOGS.index(epilog))
+    check(p, m, n, k, dtype, epilog, layout, options={"VARIANT": 1, "TILE_N": bn})
+
+
+@pytest.mark.parametrize("layout", ["M1", "1N"])
+def test_rowtile_both_layouts_relu_aux(layout):
+    m, n, k = 384, 264, 136
+    p = _inputs(m, n, k, "bf16", layout, seed=5)
+    check(p, m, n, k, "bf16", "RELU_AUX_BIAS", layout, options={"VARIANT": 1, "TILE_N": 128})
+
+
+# ---- swapped small-m kernel -----------------------------------------------------------------
+
+@pytest.mark.parametrize("m", [1, 16, 20, 64, 100, 256])
+@pytest.mark.parametrize("epilog", EPILOGS)
+def test_swapped_parity(m, epilog):
+    n, k = 520, 200
+    layout = "M1" if (m + EPILOGS.index(epilog)) % 2 else "1N"
+    p = _inputs(m, n, k, "bf16", layout, seed=1000 + m)
+    check(p, m, n, k, "bf16", epilog, layout, options={"VARIANT": 2})
+
+
+def test_swapped_f16():
+    m, n, k = 48, 392, 264
+    p = _inputs(m, n, k, "f16", "1N", seed=77)
+    check(p, m, n, k, "f16", "GELU_BIAS", "1N", options={"VARIANT": 2})
+
+
+# ---- integer inputs: every correct result is bit-exact ------------------------------------
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("epilog", ["BIAS", "RELU_BIAS", "RELU_AUX_BIAS", "BIAS_RESIDUAL", "NONE"])
+def test_integer_inputs_bit_exact(variant, epilog):
+    m, n, k = (200 if variant == 1 else 40), 136, 64
+    p = _inputs(m, n, k, "bf16", "1N", seed=3, kind="int")
+    check(p, m, n, k, "bf16", epilog, "1N", options={"VARIANT": variant}, exact=True)
+    # the unfused baseline rounds A.B to bf16 first; with |A.B| <= 256 that is exact too
+    check(p, m, n, k, "bf16", epilog, "1N", options={"VARIANT": variant}, exact=True,
+          unfused=True)
+
+
+# ---- unfused baseline -----------------------------------------------------------------------
+
+@pytest.mark.parametrize("epilog", EPILOGS)
+def test_unfused_parity(epilog):
+    m, n, k = 300, 264, 136
+    p = _inputs(m, n, k, "bf16", "1N", seed=21)
+    check(p, m, n, k, "bf16", epilog, "1N", unfused=True)
+
+
+# ---- persistence: few CTAs walking many tiles (accumulator and ring phases wrap) ----------
+
+@pytest.mark.parametrize("grid,group_m", [(1, 1), (3, 2), (7, 16)])
+def test_persistent_tile_walk(grid, group_m):
+    m, n, k = 640, 512, 520            # 5 x 4 tiles of 128 x 128, 9 K blocks
+    p = _inputs(m, n, k, "bf16", "1N", seed=grid)
+    check(p, m, n, k, "bf16", "RELU_AUX_BIAS", "1N",
+          options={"VARIANT": 1, "TILE_N": 128, "GRID": grid, "GROUP_M": group_m})
+
+
+# ---- edge cases ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("m,n,k", [(1, 8, 8), (5, 8, 8), (129, 8, 8), (257, 40, 8), (300, 33 * 8, 72)])
+@pytest.mark.parametrize("epilog", ["RELU_AUX_BIAS", "GELU_BIAS", "BIAS_RESIDUAL"])
+def test_small_and_ragged(m, n, k, epilog):
+    p = _inputs(m, n, k, "bf16", "M1", seed=m + n + k)
+    check(p, m, n, k, "bf16", epilog, "M1")
+
+
+@pytest.mark.parametrize("epilog", ["BIAS", "RELU_AUX_BIAS", "GELU_BIAS", "BIAS_RESIDUAL"])
+@pytest.mark.parametrize("layout", ["M1", "1N"])
+def test_k_zero_is_activation_of_bias(epilog, layout):
+    m, n = 70, 72
+    p = _inputs(m, n, 0, "bf16", layout, seed=4)
+    check(p, m, n, 0, "bf16", epilog, layout)
+
+
+def test_empty_problem_launches_nothing():
+    dev = torch.device("cuda")
+    for m, n in [(0, 64), (64, 0)]:
+        D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        with gemm_epi.Plan(m, n, 64, "bf16", "BIAS", "1N") as plan:
+            A = torch.empty((m, 64), dtype=torch.bfloat16, device=dev)
+            B = torch.empty((64, n), dtype=torch.bfloat16, device=dev)
+            b = torch.empty((max(n, 1),), dtype=torch.bfloat16, device=dev)
+            plan.execute(A, B, b, D)
+            assert plan.sync_status() == 0
+            assert "empty" in plan.describe()
+
+
+def test_residual_in_place():
+    m, n, k = 260, 264, 128
+    p = _inputs(m, n, k, "bf16", "1N", seed=9)
+    dev = torch.device("cuda")
+    A, B, bias = p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev)
+    R = p["R"].to(dev)
+    with gemm_epi.Plan(m, n, k, "bf16", "BIAS_RESIDUAL", "1N") as plan:
+        plan.execute(A, B, bias, R, residual=R)       # D is the residual buffer
+        assert plan.sync_status() == 0
+    from parity_helpers import oracle_ref
+    want, _ = oracle_ref(p, "bf16", "BIAS_RESIDUAL", "1N")
+    assert rel_err(R, want) <= TOL["bf16"]
+
+
+# ---- closed forms on the GPU ----------------------------------------------------------------
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_zero_A_gives_exact_broadcast_bias(variant):
+    m, n, k = (200 if variant == 1 else 24), 136, 64
+    p = _inputs(m, n, k, "f16", "M1", seed=11)
+    p["A"] = torch.zeros_like(p["A"])
+    D, _, _ = run(p, m, n, k, "f16", "BIAS", "M1", options={"VARIANT": variant})
+    want = p["bias"][:, None].expand(m, n)
+    assert torch.equal(D, want)
+
+
+def test_identity_B_gives_A_plus_bias():
+    m, n = 192, 128
+    p = _inputs(m, n, n, "bf16", "1N", seed=12)
+    p["B"] = torch.eye(n, dtype=torch.bfloat16)
+    check(p, m, n, n, "bf16", "BIAS", "1N")
+
+
+def test_gelu_textbook_points_through_the_kernel():
+    # A = I (m = k), B holds chosen x values, bias = 0, so pre = x and D = GELU(x).
+    xs = torch.tensor([-3.0, -2.0, -1.5, -1.0, -0.5, 0.0, 0.5, 1.0, 1.5, 2.0, 2.5, 3.0],
+                      dtype=torch.float64)
+    m = k = 16
+    n = 16
+    Bx = torch.zeros(k, n, dtype=torch.float64)
+    Bx[: len(xs), 0] = xs
+    inputs = {"A": torch.eye(m, dtype=torch.float16), "B": Bx.to(torch.float16),
+              "bias": torch.zeros(n, dtype=torch.float16)}
+    D, _, _ = run(inputs, m, n, k, "f16", "GELU_BIAS", "1N")
+    from scipy.special import ndtr
+    want = xs.numpy() * ndtr(xs.numpy())
+    got = D[: len(xs), 0].double().numpy()
+    # binary16 rounding of the output: 2^-11 relative, plus fp32 erf error
+    assert np.max(np.abs(got - want) / (np.abs(want) + 1)) < 1.2e-3
+
+
+# ---- the timeout path -----------------------------------------------------------------------
+
+def test_device_wait_limit_reports_timeout_and_context_survives():
+    m, n, k = 256, 256, 128
+    p = _inputs(m, n, k, "bf16", "1N", seed=13)
+    dev = torch.device("cuda")
+    A, B, bias = p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev)
+    D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    with gemm_epi.Plan(m, n, k, "bf16", "BIAS", "1N", variant=1) as plan:
+        plan.set_option("WAIT_LIMIT_US", 20000)      # 20 ms
+        plan.set_option("DEBUG_STALL", 1)
+        plan.execute(A, B, bias, D)
+        assert plan.sync_status() == 8             # GEMM_EPI_ERR_DEVICE_TIMEOUT
+        assert plan.sync_status() == 0             # reading clears it
+        plan.set_option("DEBUG_STALL", 0)
+    # the context is still usable
+    check(p, m, n, k, "bf16", "BIAS", "1N")
+
+
+# ---- host-side validation with a device -----------------------------------------------------
+
+def test_execute_argument_errors():
+    dev = torch.device("cuda")
+    m, n, k = 64, 64, 64
+    A = torch.zeros((m, k), dtype=torch.bfloat16, device=dev)
+    B = torch.zeros((k, n), dtype=torch.bfloat16, device=dev)
+    b = torch.zeros((n,), dtype=torch.bfloat16, device=dev)
+    D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    aux = torch.empty((m, 2), dtype=torch.int32, device=dev)
+    with gemm_epi.Plan(m, n, k, "bf16", "RELU_AUX_BIAS", "1N") as plan:
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.execute(A, B, b, D)                               # aux missing
+        assert e.value.status == 1
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.execute(A, B, None, D, aux=aux)                   # bias missing
+        assert e.value.status == 1
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.execute(A.data_ptr() + 2, B, b, D, aux=aux)       # misaligned A
+        assert e.value.status == 3
+    with gemm_epi.Plan(m, n, k, "bf16", "BIAS", "1N") as plan:
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.execute(A, B, b, D, aux=aux)                      # aux not allowed
+        assert e.value.status == 1
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.set_option("TILE_N", 96)
+        assert e.value.status == 1
+    with gemm_epi.Plan(300, n, k, "bf16", "BIAS", "1N") as plan:
+        with pytest.raises(gemm_epi.GemmEpiError):
+            plan.set_option("VARIANT", 2)                          # swapped needs m <= 256
+        assert "row-tile" in plan.describe()                       # previous config kept
