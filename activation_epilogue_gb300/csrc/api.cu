@@ -187,7 +187,7 @@ gemm_epi_status check_device(const gemm_epi_plan_s* p)
 
 gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const void* A, const void* B, const void* bias,
                             const void* residual, void* D, uint32_t* aux, int epilog,
-                            cudaStream_t stream)
+                            cudaStream_t stream, bool pdl = false)
 {
     gemm_epi_status st = ensure_maps(p, A, B, D);
     if (st != GEMM_EPI_OK) return st;
@@ -214,9 +214,28 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const void* A, const void* B, co
     prm.bf16 = p->dtype == GEMM_EPI_BF16 ? 1 : 0;
     prm.aux_ld = static_cast<int>((p->n + 31) / 32);
     prm.debug_stall = p->debug_stall;
-    cudaError_t e = p->variant == kRowTile ? rowtile_launch(p->bn, prm, p->grid, stream)
-                                           : swapped_launch(p->bn, prm, p->grid, stream);
+    cudaError_t e = p->variant == kRowTile ? rowtile_launch(p->bn, prm, p->grid, stream, pdl)
+                                           : swapped_launch(p->bn, prm, p->grid, stream, pdl);
     return e == cudaSuccess ? GEMM_EPI_OK : GEMM_EPI_ERR_LAUNCH;
+}
+
+gemm_epi_status check_device(const gemm_epi_plan_s* p);
+
+// One fused call on an already-checked plan: empty problems launch nothing, k == 0 runs the
+// elementwise epilogue on the bias alone, everything else the GEMM kernel.
+gemm_epi_status run_plan(gemm_epi_plan_s* p, const void* A, const void* B, const void* bias,
+                         const void* residual, void* D, uint32_t* aux, cudaStream_t stream,
+                         bool pdl)
+{
+    if (p->variant == kEmpty) return GEMM_EPI_OK;
+    if (p->variant == kBiasOnly) {
+        cudaError_t e = elementwise_launch(nullptr, bias, residual, D, aux, static_cast<int>(p->m),
+                                           static_cast<int>(p->n), p->epilog, p->bias_layout,
+                                           p->dtype == GEMM_EPI_BF16 ? 1 : 0,
+                                           static_cast<int>((p->n + 31) / 32), p->sm_count, stream);
+        return e == cudaSuccess ? GEMM_EPI_OK : GEMM_EPI_ERR_LAUNCH;
+    }
+    return launch_gemm(p, A, B, bias, residual, D, aux, p->epilog, stream, pdl);
 }
 
 gemm_epi_status check_operands(const gemm_epi_plan_s* p, const void* A, const void* B,
@@ -356,15 +375,7 @@ gemm_epi_status gemm_epi_execute_ex(gemm_epi_plan_t p, const void* A, const void
     if (p->variant == kEmpty) return GEMM_EPI_OK;
     st = check_device(p);
     if (st != GEMM_EPI_OK) return st;
-    const int bf16 = p->dtype == GEMM_EPI_BF16 ? 1 : 0;
-    const int aux_ld = static_cast<int>((p->n + 31) / 32);
-    if (p->variant == kBiasOnly) {
-        cudaError_t e = elementwise_launch(nullptr, bias, residual, D, aux, static_cast<int>(p->m),
-                                           static_cast<int>(p->n), p->epilog, p->bias_layout, bf16,
-                                           aux_ld, p->sm_count, stream);
-        return e == cudaSuccess ? GEMM_EPI_OK : GEMM_EPI_ERR_LAUNCH;
-    }
-    return launch_gemm(p, A, B, bias, residual, D, aux, p->epilog, stream);
+    return run_plan(p, A, B, bias, residual, D, aux, stream, false);
 }
 
 gemm_epi_status gemm_epi_execute(gemm_epi_plan_t p, const void* A, const void* B,
@@ -441,6 +452,93 @@ const char* gemm_epi_status_string(gemm_epi_status s)
 }
 
 const char* gemm_epi_plan_describe(gemm_epi_plan_t p) { return p ? p->desc : ""; }
+
+// ---- the FFN block ----------------------------------------------------------------------
+
+struct gemm_epi_ffn_plan_s {
+    int64_t t, d, f;
+    int dtype;
+    gemm_epi_plan_t g1;  // H = GELU(X.W1 + b1):   t x f, k = d
+    gemm_epi_plan_t g2;  // Y = H.W2 + b2 + R:     t x d, k = f
+    void* H;
+};
+
+gemm_epi_status gemm_epi_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d, int64_t f,
+                                  gemm_epi_dtype dtype)
+{
+    if (!out) return GEMM_EPI_ERR_INVALID_ARG;
+    *out = nullptr;
+    gemm_epi_plan_t g1 = nullptr, g2 = nullptr;
+    gemm_epi_status st = gemm_epi_plan(&g1, t, f, d, dtype, GEMM_EPI_GELU_BIAS, GEMM_EPI_BIAS_1N);
+    if (st != GEMM_EPI_OK) return st;
+    st = gemm_epi_plan(&g2, t, d, f, dtype, GEMM_EPI_BIAS_RESIDUAL, GEMM_EPI_BIAS_1N);
+    if (st != GEMM_EPI_OK) {
+        gemm_epi_free(g1);
+        return st;
+    }
+    gemm_epi_ffn_plan_s* p = new (std::nothrow) gemm_epi_ffn_plan_s();
+    if (!p) {
+        gemm_epi_free(g1);
+        gemm_epi_free(g2);
+        return GEMM_EPI_ERR_ALLOC;
+    }
+    p->t = t;
+    p->d = d;
+    p->f = f;
+    p->dtype = dtype;
+    p->g1 = g1;
+    p->g2 = g2;
+    p->H = nullptr;
+    if (t > 0 && f > 0) {
+        if (cudaMalloc(&p->H, static_cast<size_t>(t) * static_cast<size_t>(f) * 2) != cudaSuccess) {
+            cudaGetLastError();
+            gemm_epi_free(g1);
+            gemm_epi_free(g2);
+            delete p;
+            return GEMM_EPI_ERR_ALLOC;
+        }
+    }
+    *out = p;
+    return GEMM_EPI_OK;
+}
+
+gemm_epi_status gemm_epi_ffn_execute(gemm_epi_ffn_plan_t p, const void* X, const void* W1,
+                                     const void* b1, const void* W2, const void* b2,
+                                     const void* R, void* Y, cudaStream_t stream)
+{
+    if (!p) return GEMM_EPI_ERR_INVALID_ARG;
+    gemm_epi_status st = check_operands(p->g1, X, W1, b1, nullptr, p->H ? p->H : Y, nullptr);
+    if (st != GEMM_EPI_OK) return st;
+    st = check_operands(p->g2, p->H, W2, b2, R, Y, nullptr);
+    if (st != GEMM_EPI_OK) return st;
+    if (p->t == 0 || p->d == 0) return GEMM_EPI_OK;
+    st = check_device(p->g1);
+    if (st != GEMM_EPI_OK) return st;
+    st = run_plan(p->g1, X, W1, b1, nullptr, p->H, nullptr, stream, false);
+    if (st != GEMM_EPI_OK) return st;
+    // GEMM 2 reads H only after GEMM 1 has completed (griddepcontrol.wait in its producer).
+    return run_plan(p->g2, p->H, W2, b2, R, Y, nullptr, stream, p->g1->variant != kEmpty);
+}
+
+const void* gemm_epi_ffn_hidden(gemm_epi_ffn_plan_t p) { return p ? p->H : nullptr; }
+
+gemm_epi_status gemm_epi_ffn_sync_status(gemm_epi_ffn_plan_t p, cudaStream_t stream)
+{
+    if (!p) return GEMM_EPI_ERR_INVALID_ARG;
+    gemm_epi_status s1 = gemm_epi_sync_status(p->g1, stream);
+    gemm_epi_status s2 = gemm_epi_sync_status(p->g2, stream);
+    return s1 != GEMM_EPI_OK ? s1 : s2;
+}
+
+gemm_epi_status gemm_epi_ffn_free(gemm_epi_ffn_plan_t p)
+{
+    if (!p) return GEMM_EPI_OK;
+    if (p->H) cudaFree(p->H);
+    gemm_epi_free(p->g1);
+    gemm_epi_free(p->g2);
+    delete p;
+    return GEMM_EPI_OK;
+}
 
 int64_t gemm_epi_aux_words_per_row(int64_t n) { return n <= 0 ? 0 : (n + 31) / 32; }
 

@@ -153,6 +153,10 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
     uint32_t phase = 0;
     long long issued = 0;
     bool ok = true;
+    // Under a programmatic dependent launch, operands may come from the previous grid:
+    // every global read and write of this kernel is ordered after this wait (the epilogue
+    // writes only after MMAs that consume these loads).
+    grid_dependency_wait();
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         int tm, tn;
         tile_coords(tile, p, tm, tn);
@@ -501,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     __syncthreads();
     tcgen05_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
+    if (threadIdx.x == 0) grid_launch_dependents();
 
     if (p.debug_stall) {
         // Test of the timeout path: wait on a barrier that nothing arrives at.

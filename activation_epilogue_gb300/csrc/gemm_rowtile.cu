@@ -13,13 +13,20 @@ cudaError_t prepare_one()
 }
 
 template <int BN>
-cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t stream)
+cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = TileCfg<BN>::kSmemBytes;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     return cudaLaunchKernelEx(&cfg, gemm_epi_kernel<BN, false>, p);
 }
 }  // namespace
@@ -34,12 +41,12 @@ cudaError_t rowtile_prepare(int bn)
     }
 }
 
-cudaError_t rowtile_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream)
+cudaError_t rowtile_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
 {
     switch (bn) {
-    case 64: return launch_one<64>(p, grid, stream);
-    case 128: return launch_one<128>(p, grid, stream);
-    case 256: return launch_one<256>(p, grid, stream);
+    case 64: return launch_one<64>(p, grid, stream, pdl);
+    case 128: return launch_one<128>(p, grid, stream, pdl);
+    case 256: return launch_one<256>(p, grid, stream, pdl);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -14,13 +14,20 @@ cudaError_t prepare_one()
 }
 
 template <int BN>
-cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t stream)
+cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = TileCfg<BN>::kSmemBytes;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     return cudaLaunchKernelEx(&cfg, gemm_epi_kernel<BN, true>, p);
 }
 }  // namespace
@@ -37,10 +44,10 @@ cudaError_t swapped_prepare(int bn)
     }
 }
 
-cudaError_t swapped_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream)
+cudaError_t swapped_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
 {
     switch (bn) {
-#define F(X) case X: return launch_one<X>(p, grid, stream);
+#define F(X) case X: return launch_one<X>(p, grid, stream, pdl);
         GEMM_EPI_SWAPPED_CASES(F)
 #undef F
     default: return cudaErrorInvalidValue;

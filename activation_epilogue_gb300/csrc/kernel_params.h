@@ -54,12 +54,13 @@ struct GemmParams {
 
 // Row-tile kernel (BN in {64, 128, 256}) and swapped small-m kernel (BN in {16 ... 256}).
 cudaError_t rowtile_prepare(int bn);
-cudaError_t rowtile_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream);
+// pdl: launch as a programmatic dependent of the previous grid on the stream.
+cudaError_t rowtile_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
 int rowtile_smem_bytes(int bn);
 int rowtile_stages(int bn);
 
 cudaError_t swapped_prepare(int bn);
-cudaError_t swapped_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t swapped_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
 int swapped_smem_bytes(int bn);
 int swapped_stages(int bn);
 

@@ -113,6 +113,21 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthread
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// ---- programmatic dependent launch ------------------------------------------------------
+
+// Block until the grids this one depends on have completed and their writes are visible
+// (returns at once when the launch has no programmatic dependency).
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next grid on the stream, if launched as a programmatic dependent, to start.
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- tcgen05 / TMEM ----------------------------------------------------------------------
 
 // Whole-warp: allocate `ncols` TMEM columns (power of two >= 32); the base address is

@@ -29,7 +29,8 @@ STATUS = {0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED_SHAPE", 3: "ERR_MIS
 EXPORTS = ["gemm_epi_plan", "gemm_epi_plan_set_option", "gemm_epi_execute",
            "gemm_epi_execute_ex", "gemm_epi_execute_unfused", "gemm_epi_free",
            "gemm_epi_sync_status", "gemm_epi_status_string", "gemm_epi_plan_describe",
-           "gemm_epi_aux_words_per_row"]
+           "gemm_epi_aux_words_per_row", "gemm_epi_ffn_plan", "gemm_epi_ffn_execute",
+           "gemm_epi_ffn_hidden", "gemm_epi_ffn_sync_status", "gemm_epi_ffn_free"]
 
 _lib = None
 _lock = threading.Lock()
@@ -70,6 +71,16 @@ def load_library(path: str | None = None):
         lib.gemm_epi_plan_describe.argtypes = [vp]
         lib.gemm_epi_aux_words_per_row.restype = i64
         lib.gemm_epi_aux_words_per_row.argtypes = [i64]
+        lib.gemm_epi_ffn_plan.restype = i32
+        lib.gemm_epi_ffn_plan.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i32]
+        lib.gemm_epi_ffn_execute.restype = i32
+        lib.gemm_epi_ffn_execute.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.gemm_epi_ffn_hidden.restype = vp
+        lib.gemm_epi_ffn_hidden.argtypes = [vp]
+        lib.gemm_epi_ffn_sync_status.restype = i32
+        lib.gemm_epi_ffn_sync_status.argtypes = [vp, vp]
+        lib.gemm_epi_ffn_free.restype = i32
+        lib.gemm_epi_ffn_free.argtypes = [vp]
         if path is None:
             _lib = lib
         return lib
@@ -155,6 +166,84 @@ def gemm_epi_plan_describe(plan) -> str:
 
 def gemm_epi_aux_words_per_row(n: int) -> int:
     return int(load_library().gemm_epi_aux_words_per_row(n))
+
+
+def gemm_epi_ffn_plan(t: int, d: int, f: int, dtype: str = "bf16"):
+    h = ctypes.c_void_p()
+    _check(load_library().gemm_epi_ffn_plan(ctypes.byref(h), t, d, f, DTYPE[dtype]),
+           "gemm_epi_ffn_plan")
+    return h.value
+
+
+def gemm_epi_ffn_execute(plan, X, W1, b1, W2, b2, R, Y, stream=None):
+    _check(load_library().gemm_epi_ffn_execute(plan, _ptr(X), _ptr(W1), _ptr(b1), _ptr(W2),
+                                               _ptr(b2), _ptr(R), _ptr(Y), _stream(stream)),
+           "gemm_epi_ffn_execute")
+
+
+def gemm_epi_ffn_hidden(plan) -> int:
+    return load_library().gemm_epi_ffn_hidden(plan) or 0
+
+
+def gemm_epi_ffn_sync_status(plan, stream=None) -> int:
+    return int(load_library().gemm_epi_ffn_sync_status(plan, _stream(stream)))
+
+
+def gemm_epi_ffn_free(plan):
+    _check(load_library().gemm_epi_ffn_free(plan), "gemm_epi_ffn_free")
+
+
+class FfnPlan:
+    """The FFN block Y = GELU(X.W1 + b1).W2 + b2 + R as one plan (two fused launches)."""
+
+    def __init__(self, t, d, f, dtype="bf16"):
+        self.t, self.d, self.f, self.dtype = t, d, f, dtype
+        self.handle = gemm_epi_ffn_plan(t, d, f, dtype)
+
+    def execute(self, X, W1, b1, W2, b2, R, Y, stream=None):
+        gemm_epi_ffn_execute(self.handle, X, W1, b1, W2, b2, R, Y, stream)
+
+    def hidden(self):
+        """The plan's H buffer as a torch tensor view (t x f) on the current device."""
+        import torch
+        ptr = gemm_epi_ffn_hidden(self.handle)
+        if not ptr:
+            return None
+        return _tensor_from_ptr(ptr, (self.t, self.f), self.dtype)
+
+    def sync_status(self, stream=None) -> int:
+        return gemm_epi_ffn_sync_status(self.handle, stream)
+
+    def free(self):
+        if self.handle:
+            gemm_epi_ffn_free(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.free()
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def _tensor_from_ptr(ptr: int, shape, dtype: str):
+    """A torch tensor that aliases library-owned device memory (read-only use)."""
+    import torch
+    td = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    n = 1
+    for s in shape:
+        n *= s
+
+    class _Holder:
+        __cuda_array_interface__ = {"shape": (n,), "typestr": "<i2", "data": (ptr, False),
+                                    "version": 3}
+    return torch.as_tensor(_Holder(), device="cuda").view(td).view(*shape)
 
 
 # ---- a small owner object around a plan ---------------------------------------------------

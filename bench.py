@@ -166,7 +166,8 @@ def time_graph(fn, calls: int, replays: int, stream) -> float:
     fn()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
+    capture = torch.cuda.Stream()          # capture needs a non-default stream
+    with torch.cuda.graph(g, stream=capture):
         for _ in range(calls):
             fn()
     g.replay()

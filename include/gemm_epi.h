@@ -168,6 +168,37 @@ const char* gemm_epi_plan_describe(gemm_epi_plan_t p);
 /* Number of uint32 words in one row of the aux mask: ceil(n / 32). */
 int64_t gemm_epi_aux_words_per_row(int64_t n);
 
+/* ---- the FFN block ---------------------------------------------------------------------
+ * "Operator fusion in model inference, from LayerNorm to residual connections"
+ * (wmrh.cn/news/429806), section 1 and its flowchart: the FFN sub-layer is matmul -> bias
+ * -> GELU -> matmul -> bias (five launches unfused); section 3: the residual add joins the
+ * op before it.  Here it is two fused launches:
+ *   GEMM 1:  H = GELU(X . W1 + b1)      X: t x d, W1: d x f, b1: f elements  (bias (1,f))
+ *   GEMM 2:  Y = H . W2 + b2 + R        W2: f x d, b2: d elements, R and Y: t x d
+ * H (t x f, the plan's dtype) lives in device memory the plan owns; it is written once by
+ * GEMM 1 and read once by GEMM 2.  GEMM 2 is launched as a programmatic dependent of GEMM 1
+ * on the same stream: its set-up overlaps GEMM 1's tail and it reads H only after GEMM 1
+ * has completed.  d and f must be multiples of 8; pointer rules as above. */
+typedef struct gemm_epi_ffn_plan_s* gemm_epi_ffn_plan_t;
+
+/* Plan the FFN block for t tokens, model width d and hidden width f; allocates H. */
+gemm_epi_status gemm_epi_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d, int64_t f,
+                                  gemm_epi_dtype dtype);
+
+/* Y = GELU(X.W1 + b1).W2 + b2 + R, asynchronous on `stream`.  Y may be R itself. */
+gemm_epi_status gemm_epi_ffn_execute(gemm_epi_ffn_plan_t p, const void* X, const void* W1,
+                                     const void* b1, const void* W2, const void* b2,
+                                     const void* R, void* Y, cudaStream_t stream);
+
+/* Device address of the plan's H buffer (t x f), valid until gemm_epi_ffn_free. */
+const void* gemm_epi_ffn_hidden(gemm_epi_ffn_plan_t p);
+
+/* As gemm_epi_sync_status, for both GEMMs of the block. */
+gemm_epi_status gemm_epi_ffn_sync_status(gemm_epi_ffn_plan_t p, cudaStream_t stream);
+
+/* Release the plan and its H buffer (after the work that uses them has completed). */
+gemm_epi_status gemm_epi_ffn_free(gemm_epi_ffn_plan_t p);
+
 #ifdef __cplusplus
 }
 #endif

@@ -224,3 +224,52 @@ def test_execute_argument_errors():
         with pytest.raises(gemm_epi.GemmEpiError):
             plan.set_option("VARIANT", 2)                          # swapped needs m <= 256
         assert "row-tile" in plan.describe()                       # previous config kept
+
+
+# ---- the FFN entry points -------------------------------------------------------------------
+
+@pytest.mark.parametrize("t,d,f", [(300, 136, 264), (16, 256, 520), (1, 8, 8)])
+def test_ffn_plan_parity(t, d, f):
+    import oracle
+    g = torch.Generator().manual_seed(t + d + f)
+
+    def r(*s, sc=1.0):
+        return (torch.randn(*s, generator=g) * sc).to(torch.bfloat16)
+    cpu = dict(X=r(t, d), W1=r(d, f, sc=0.1), b1=r(f, sc=0.1), W2=r(f, d, sc=0.1),
+               b2=r(d, sc=0.1), R=r(t, d))
+    dev = torch.device("cuda")
+    gi = {k: v.to(dev) for k, v in cpu.items()}
+    Y = torch.empty((t, d), dtype=torch.bfloat16, device=dev)
+    with gemm_epi.FfnPlan(t, d, f) as plan:
+        plan.execute(gi["X"], gi["W1"], gi["b1"], gi["W2"], gi["b2"], gi["R"], Y)
+        assert plan.sync_status() == 0
+        H = plan.hidden().cpu()
+        # twice in a row: the second call must give the same result
+        Y1 = Y.clone()
+        plan.execute(gi["X"], gi["W1"], gi["b1"], gi["W2"], gi["b2"], gi["R"], Y)
+        assert plan.sync_status() == 0
+        assert torch.equal(Y, Y1)
+    H_ref, H_exact, Y_ref = oracle.ffn(**cpu)
+    assert rel_err(H, H_exact) <= TOL["bf16"]
+    assert rel_err(Y, Y_ref) <= TOL["bf16"]
+    Y2 = oracle.gemm_epi(H, cpu["W2"], cpu["b2"], dtype="bf16", epilog="BIAS_RESIDUAL",
+                         residual=cpu["R"])
+    assert rel_err(Y, Y2) <= TOL["bf16"]
+
+
+def test_ffn_in_place_on_residual():
+    t, d, f = 200, 128, 256
+    g = torch.Generator().manual_seed(5)
+    dev = torch.device("cuda")
+
+    def r(*s, sc=1.0):
+        return (torch.randn(*s, generator=g) * sc).to(torch.bfloat16)
+    cpu = dict(X=r(t, d), W1=r(d, f, sc=0.1), b1=r(f, sc=0.1), W2=r(f, d, sc=0.1),
+               b2=r(d, sc=0.1), R=r(t, d))
+    gi = {k: v.to(dev) for k, v in cpu.items()}
+    with gemm_epi.FfnPlan(t, d, f) as plan:
+        plan.execute(gi["X"], gi["W1"], gi["b1"], gi["W2"], gi["b2"], gi["R"], gi["R"])
+        assert plan.sync_status() == 0
+    import oracle
+    _, _, Y_ref = oracle.ffn(**cpu)
+    assert rel_err(gi["R"], Y_ref) <= TOL["bf16"]
