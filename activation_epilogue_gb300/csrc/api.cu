@@ -447,6 +447,9 @@ const char* gemm_epi_status_string(gemm_epi_status s)
     case GEMM_EPI_ERR_LAUNCH: return "GEMM_EPI_ERR_LAUNCH: CUDA launch or encode failed";
     case GEMM_EPI_ERR_DEVICE_TIMEOUT:
         return "GEMM_EPI_ERR_DEVICE_TIMEOUT: a kernel gave up on a device-side wait";
+    case GEMM_EPI_ERR_SCRATCH_LIMIT:
+        return "GEMM_EPI_ERR_SCRATCH_LIMIT: t*f exceeds the static scratch of the "
+               "allocation-free FFN call (GEMM_EPI_FFN_NOALLOC_MAX_HIDDEN elements)";
     default: return "GEMM_EPI_ERR_UNKNOWN";
     }
 }
@@ -543,3 +546,110 @@ gemm_epi_status gemm_epi_ffn_free(gemm_epi_ffn_plan_t p)
 int64_t gemm_epi_aux_words_per_row(int64_t n) { return n <= 0 ? 0 : (n + 31) / 32; }
 
 }  // extern "C"
+
+// ---- the FFN block without allocation ------------------------------------------------------
+//
+// For callers that cannot allocate device memory.  The hidden activation and the status
+// words of the two launches live in one file-scope device array; its device address is
+// looked up once per device (with that device current) and then passed to the kernels.
+
+namespace {
+
+constexpr size_t kNoAllocStatusBytes = 256;  // two status words, padded to 256 bytes
+constexpr size_t kNoAllocHiddenBytes = static_cast<size_t>(GEMM_EPI_FFN_NOALLOC_MAX_HIDDEN) * 2;
+
+// In host code this name is only a stand-in; the device address comes from
+// cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char
+    g_ffn_noalloc_scratch[kNoAllocStatusBytes + kNoAllocHiddenBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+unsigned char* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on device `dev` (the current device); the first call
+// per device looks it up and zeroes the status words.
+gemm_epi_status noalloc_scratch(int dev, unsigned char** out)
+{
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return GEMM_EPI_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_ffn_noalloc_scratch) != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return GEMM_EPI_ERR_LAUNCH;
+        }
+        if (cudaMemset(ptr, 0, kNoAllocStatusBytes) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_EPI_ERR_LAUNCH;
+        }
+        g_noalloc_addr[dev] = static_cast<unsigned char*>(ptr);
+    }
+    *out = g_noalloc_addr[dev];
+    return GEMM_EPI_OK;
+}
+
+// A plan on the caller's stack whose status word points into the static scratch.
+gemm_epi_status stack_plan(gemm_epi_plan_s* p, int64_t m, int64_t n, int64_t k, int dtype,
+                           int epilog, int dev, int sms, int* status)
+{
+    memset(p, 0, sizeof(*p));
+    p->m = m;
+    p->n = n;
+    p->k = k;
+    p->dtype = dtype;
+    p->epilog = epilog;
+    p->bias_layout = GEMM_EPI_BIAS_1N;
+    p->device = dev;
+    p->sm_count = sms;
+    p->wait_limit_ns = kDefaultWaitNs;
+    p->d_status = status;
+    return configure(p);
+}
+
+}  // namespace
+
+extern "C" gemm_epi_status gemm_epi_ffn_execute_noalloc(int64_t t, int64_t d, int64_t f,
+                                                        gemm_epi_dtype dtype, const void* X,
+                                                        const void* W1, const void* b1,
+                                                        const void* W2, const void* b2,
+                                                        const void* R, void* Y,
+                                                        cudaStream_t stream)
+{
+    if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
+    const int64_t kMax = (1ll << 31) - 1;
+    if (t < 0 || d < 0 || f < 0 || t > kMax || d > kMax || f > kMax)
+        return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+    if (d % 8 != 0 || f % 8 != 0) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+    if (f > 0 && t > GEMM_EPI_FFN_NOALLOC_MAX_HIDDEN / f) return GEMM_EPI_ERR_SCRATCH_LIMIT;
+
+    int dev = 0, major = 0, minor = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_EPI_ERR_NO_DEVICE;
+    }
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3) return GEMM_EPI_ERR_ARCH;
+
+    unsigned char* scratch = nullptr;
+    gemm_epi_status st = noalloc_scratch(dev, &scratch);
+    if (st != GEMM_EPI_OK) return st;
+    int* status = reinterpret_cast<int*>(scratch);
+    void* H = scratch + kNoAllocStatusBytes;
+
+    gemm_epi_plan_s g1, g2;
+    st = stack_plan(&g1, t, f, d, dtype, GEMM_EPI_GELU_BIAS, dev, sms, status);
+    if (st != GEMM_EPI_OK) return st;
+    st = stack_plan(&g2, t, d, f, dtype, GEMM_EPI_BIAS_RESIDUAL, dev, sms, status + 1);
+    if (st != GEMM_EPI_OK) return st;
+    st = check_operands(&g1, X, W1, b1, nullptr, H, nullptr);
+    if (st != GEMM_EPI_OK) return st;
+    st = check_operands(&g2, H, W2, b2, R, Y, nullptr);
+    if (st != GEMM_EPI_OK) return st;
+    if (t == 0 || d == 0) return GEMM_EPI_OK;
+    st = run_plan(&g1, X, W1, b1, nullptr, H, nullptr, stream, false);
+    if (st != GEMM_EPI_OK) return st;
+    return run_plan(&g2, H, W2, b2, R, Y, nullptr, stream, g1.variant != kEmpty);
+}

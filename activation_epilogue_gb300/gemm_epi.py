@@ -23,14 +23,18 @@ OPTION = {"VARIANT": 0, "TILE_N": 1, "SPLIT_K": 2, "GRID": 3, "GROUP_M": 4,
           "WAIT_LIMIT_US": 5, "DEBUG_STALL": 6}
 STATUS = {0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED_SHAPE", 3: "ERR_MISALIGNED",
           4: "ERR_NO_DEVICE", 5: "ERR_ARCH", 6: "ERR_ALLOC", 7: "ERR_LAUNCH",
-          8: "ERR_DEVICE_TIMEOUT"}
+          8: "ERR_DEVICE_TIMEOUT", 9: "ERR_SCRATCH_LIMIT"}
 
 # Every symbol include/gemm_epi.h declares.
 EXPORTS = ["gemm_epi_plan", "gemm_epi_plan_set_option", "gemm_epi_execute",
            "gemm_epi_execute_ex", "gemm_epi_execute_unfused", "gemm_epi_free",
            "gemm_epi_sync_status", "gemm_epi_status_string", "gemm_epi_plan_describe",
            "gemm_epi_aux_words_per_row", "gemm_epi_ffn_plan", "gemm_epi_ffn_execute",
-           "gemm_epi_ffn_hidden", "gemm_epi_ffn_sync_status", "gemm_epi_ffn_free"]
+           "gemm_epi_ffn_hidden", "gemm_epi_ffn_sync_status", "gemm_epi_ffn_free",
+           "gemm_epi_ffn_execute_noalloc"]
+
+# Largest t * f the allocation-free FFN call accepts (its static scratch holds H).
+FFN_NOALLOC_MAX_HIDDEN = 16 * 1024 * 1024
 
 _lib = None
 _lock = threading.Lock()
@@ -81,6 +85,9 @@ def load_library(path: str | None = None):
         lib.gemm_epi_ffn_sync_status.argtypes = [vp, vp]
         lib.gemm_epi_ffn_free.restype = i32
         lib.gemm_epi_ffn_free.argtypes = [vp]
+        lib.gemm_epi_ffn_execute_noalloc.restype = i32
+        lib.gemm_epi_ffn_execute_noalloc.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, vp,
+                                                     vp, vp]
         if path is None:
             _lib = lib
         return lib
@@ -191,6 +198,16 @@ def gemm_epi_ffn_sync_status(plan, stream=None) -> int:
 
 def gemm_epi_ffn_free(plan):
     _check(load_library().gemm_epi_ffn_free(plan), "gemm_epi_ffn_free")
+
+
+def gemm_epi_ffn_execute_noalloc(t: int, d: int, f: int, dtype: str, X, W1, b1, W2, b2, R, Y,
+                                 stream=None):
+    """The FFN block without allocating: for callers that must not allocate device memory.
+    H lives in the library's static scratch, so calls on one device must not overlap."""
+    _check(load_library().gemm_epi_ffn_execute_noalloc(t, d, f, DTYPE[dtype], _ptr(X), _ptr(W1),
+                                                       _ptr(b1), _ptr(W2), _ptr(b2), _ptr(R),
+                                                       _ptr(Y), _stream(stream)),
+           "gemm_epi_ffn_execute_noalloc")
 
 
 class FfnPlan:

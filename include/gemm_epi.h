@@ -91,7 +91,9 @@ typedef enum {
     GEMM_EPI_ERR_ARCH = 5,              /* the current device is not sm_103 */
     GEMM_EPI_ERR_ALLOC = 6,             /* the plan's own device or host allocation failed */
     GEMM_EPI_ERR_LAUNCH = 7,            /* a CUDA call failed while encoding or launching */
-    GEMM_EPI_ERR_DEVICE_TIMEOUT = 8     /* a kernel gave up on a wait (see sync_status) */
+    GEMM_EPI_ERR_DEVICE_TIMEOUT = 8,    /* a kernel gave up on a wait (see sync_status) */
+    GEMM_EPI_ERR_SCRATCH_LIMIT = 9      /* the problem needs more than the fixed static
+                                           scratch of gemm_epi_ffn_execute_noalloc */
 } gemm_epi_status;
 
 /* Plan-time settings (gemm_epi_plan_set_option).  0 always means "automatic". */
@@ -198,6 +200,34 @@ gemm_epi_status gemm_epi_ffn_sync_status(gemm_epi_ffn_plan_t p, cudaStream_t str
 
 /* Release the plan and its H buffer (after the work that uses them has completed). */
 gemm_epi_status gemm_epi_ffn_free(gemm_epi_ffn_plan_t p);
+
+/*
+ * The FFN block without any allocation.  The pages have no counterpart: this call is for
+ * callers that cannot allocate device memory themselves, for instance a serving runtime
+ * that hands out all device memory from its own pool and forbids cudaMalloc once it has
+ * started, or code that runs in a context where an allocation would stall or fail.  Same
+ * computation and arguments as gemm_epi_ffn_plan + gemm_epi_ffn_execute, but there is no
+ * plan: the hidden activation H and the two launches' status words live in one static
+ * device array inside this library, of GEMM_EPI_FFN_NOALLOC_MAX_HIDDEN 16-bit elements
+ * (32 MiB) plus 256 bytes, which every GPU that loads the library keeps until the process
+ * exits.
+ *   - t * f > GEMM_EPI_FFN_NOALLOC_MAX_HIDDEN returns GEMM_EPI_ERR_SCRATCH_LIMIT and launches
+ *     nothing; other argument errors as gemm_epi_ffn_execute.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.  The first call on a device
+ *     looks up the array's device address (cudaGetSymbolAddress) and zeroes the status
+ *     words; make that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's H: calls
+ *     whose work overlaps on the GPU (different streams, or different host threads) race
+ *     on it and give wrong results; order them on one stream.
+ *   - A device-side wait that runs out its limit ends the kernels as in the planned path,
+ *     but is only recorded in the static status words, which this call does not report.
+ */
+#define GEMM_EPI_FFN_NOALLOC_MAX_HIDDEN (16ll * 1024 * 1024)
+gemm_epi_status gemm_epi_ffn_execute_noalloc(int64_t t, int64_t d, int64_t f,
+                                             gemm_epi_dtype dtype, const void* X,
+                                             const void* W1, const void* b1, const void* W2,
+                                             const void* b2, const void* R, void* Y,
+                                             cudaStream_t stream);
 
 #ifdef __cplusplus
 }
