@@ -56,6 +56,7 @@ struct gemm_epi_plan_s {
     int device, sm_count;
     // chosen configuration
     int variant, bn, stages, smem, grid, group_m, tiles_m, tiles_n, k_blocks;
+    int split, kb_per_split;  // split-K across a cluster (split == 1: persistent kernel)
     // options (0 = automatic)
     int opt_variant, opt_bn, opt_split_k, opt_grid, opt_group_m;
     unsigned long long wait_limit_ns;
@@ -72,14 +73,52 @@ struct gemm_epi_plan_s {
 
 namespace {
 
-int pick_rowtile_bn(int64_t m, int64_t n, int sm_count)
+// Split-K factor for a grid of `tiles` output tiles and `k_blocks` K blocks: used only
+// when the tiles fill less than half the SMs; at most 8 (a portable cluster), at least two
+// K blocks per slice, and no empty slice.
+int auto_split(long long tiles, int k_blocks, int sm_count)
+{
+    if (tiles * 2 > sm_count || k_blocks < 4) return 1;
+    long long s = sm_count / tiles;
+    if (s > 8) s = 8;
+    if (s > k_blocks / 2) s = k_blocks / 2;
+    return s < 2 ? 1 : static_cast<int>(s);
+}
+
+int normalise_split(int split, int k_blocks, int* kb_per_split)
+{
+    if (split > k_blocks) split = k_blocks;
+    if (split < 1) split = 1;
+    const int kpb = (k_blocks + split - 1) / split;
+    *kb_per_split = kpb;
+    return (k_blocks + kpb - 1) / kpb;
+}
+
+// N tile of the row-tile kernel.  When the widest tile already gives every SM a tile, that
+// one (fewest operand bytes per flop).  Otherwise the width whose busiest CTA moves the
+// fewest bytes: its K slices of operand stages, plus, under split-K, its share of the
+// partial-sum exchange.
+int pick_rowtile_bn(int64_t m, int64_t n, int k_blocks, int sm_count)
 {
     const int64_t tm = (m + 127) / 128;
-    for (int bn : {256, 128}) {
-        const int64_t tiles = tm * ((n + bn - 1) / bn);
-        if (tiles >= sm_count) return bn;
+    if (tm * ((n + 255) / 256) >= sm_count) return 256;
+    int best = 256;
+    double best_cost = 1e300;
+    for (int bn : {64, 128, 256}) {
+        const long long tiles = tm * ((n + bn - 1) / bn);
+        int kpb = 0;
+        const int split = normalise_split(auto_split(tiles, k_blocks, sm_count), k_blocks, &kpb);
+        const long long ctas = tiles * split;
+        const long long waves = (ctas + sm_count - 1) / sm_count;
+        const double stage = 16384.0 + bn * 128.0;
+        const double red = split > 1 ? (split - 1) * 128.0 * bn * 4.0 / split : 0.0;
+        const double cost = waves * (kpb * stage + red);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = bn;
+        }
     }
-    return 64;
+    return best;
 }
 
 gemm_epi_status configure(gemm_epi_plan_s* p)
@@ -87,6 +126,8 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
     p->maps_valid = false;
     p->bn = p->stages = p->smem = p->grid = p->tiles_m = p->tiles_n = p->k_blocks = 0;
     p->group_m = 1;
+    p->split = 1;
+    p->kb_per_split = 0;
     if (p->m == 0 || p->n == 0) {
         p->variant = kEmpty;
     } else if (p->k == 0) {
@@ -95,8 +136,9 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
         int v = p->opt_variant ? p->opt_variant : (p->m <= kSwappedMaxM ? kSwapped : kRowTile);
         if (v == kSwapped && p->m > kSwappedMaxM) return GEMM_EPI_ERR_INVALID_ARG;
         p->variant = v;
+        p->k_blocks = static_cast<int>((p->k + 63) / 64);
         if (v == kRowTile) {
-            p->bn = p->opt_bn ? p->opt_bn : pick_rowtile_bn(p->m, p->n, p->sm_count);
+            p->bn = p->opt_bn ? p->opt_bn : pick_rowtile_bn(p->m, p->n, p->k_blocks, p->sm_count);
             p->tiles_m = static_cast<int>((p->m + 127) / 128);
             p->tiles_n = static_cast<int>((p->n + p->bn - 1) / p->bn);
             p->stages = rowtile_stages(p->bn);
@@ -110,10 +152,19 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             p->stages = swapped_stages(bn);
             p->smem = swapped_smem_bytes(bn);
         }
-        p->k_blocks = static_cast<int>((p->k + 63) / 64);
         const long long tiles = static_cast<long long>(p->tiles_m) * p->tiles_n;
-        long long grid = tiles < p->sm_count ? tiles : p->sm_count;
-        if (p->opt_grid > 0 && p->opt_grid < grid) grid = p->opt_grid;
+        const int want_split =
+            p->opt_split_k > 0 ? p->opt_split_k : auto_split(tiles, p->k_blocks, p->sm_count);
+        p->split = normalise_split(want_split, p->k_blocks, &p->kb_per_split);
+        long long grid;
+        if (p->split > 1) {
+            grid = tiles * p->split;  // one cluster per tile, not persistent
+            if (grid > (1ll << 30)) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+        } else {
+            p->kb_per_split = p->k_blocks;
+            grid = tiles < p->sm_count ? tiles : p->sm_count;
+            if (p->opt_grid > 0 && p->opt_grid < grid) grid = p->opt_grid;
+        }
         p->grid = static_cast<int>(grid);
         int gm = p->opt_group_m ? p->opt_group_m : 16;
         if (gm > p->tiles_m) gm = p->tiles_m;
@@ -124,12 +175,12 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
                                   "BIAS_RESIDUAL", "NONE"};
     snprintf(p->desc, sizeof(p->desc),
              "m=%lld n=%lld k=%lld dtype=%s epilog=%s bias=%s variant=%s tile=128x%d bk=64 "
-             "stages=%d smem=%d tiles=%dx%d k_blocks=%d grid=%d group_m=%d sms=%d",
+             "stages=%d smem=%d tiles=%dx%d k_blocks=%d split_k=%d grid=%d group_m=%d sms=%d",
              static_cast<long long>(p->m), static_cast<long long>(p->n),
              static_cast<long long>(p->k), p->dtype == GEMM_EPI_BF16 ? "bf16" : "f16",
              ename[p->epilog], p->bias_layout == GEMM_EPI_BIAS_M1 ? "(m,1)" : "(1,n)",
              vname[p->variant], p->bn, p->stages, p->smem, p->tiles_m, p->tiles_n, p->k_blocks,
-             p->grid, p->group_m, p->sm_count);
+             p->split, p->grid, p->group_m, p->sm_count);
     if (p->variant == kRowTile || p->variant == kSwapped) {
         cudaError_t e = p->variant == kRowTile ? rowtile_prepare(p->bn) : swapped_prepare(p->bn);
         if (e != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
@@ -214,6 +265,8 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const void* A, const void* B, co
     prm.bf16 = p->dtype == GEMM_EPI_BF16 ? 1 : 0;
     prm.aux_ld = static_cast<int>((p->n + 31) / 32);
     prm.debug_stall = p->debug_stall;
+    prm.split = p->split;
+    prm.kb_per_split = p->kb_per_split;
     cudaError_t e = p->variant == kRowTile ? rowtile_launch(p->bn, prm, p->grid, stream, pdl)
                                            : swapped_launch(p->bn, prm, p->grid, stream, pdl);
     return e == cudaSuccess ? GEMM_EPI_OK : GEMM_EPI_ERR_LAUNCH;

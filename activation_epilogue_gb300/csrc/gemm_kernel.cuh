@@ -19,6 +19,13 @@
 //               shared-memory box and a TMA store.  While it drains one accumulator the
 //               MMA warp fills the other, so the epilogue overlaps the next tile's GEMM.
 //
+// Split-K (small grids): the CTAs of a cluster share one output tile, each accumulating a
+// slice of K in its own TMEM.  The tile's 32-column chunks are owned round-robin by the
+// cluster ranks; every CTA writes the partial sums of the chunks it does not own into its
+// (by then idle) stage ring, the cluster synchronises, and each owner adds the peers'
+// partials over distributed shared memory before running the epilogue on its chunks.  The
+// partial sums never leave the chip.
+//
 // Every mbarrier wait is bounded by a time limit; on expiry the waiting thread records the
 // failure in the plan's status word and raises a shared abort flag, every role leaves its
 // loop, in-flight copies and MMAs are drained, tensor memory is freed and the kernel returns.
@@ -55,7 +62,9 @@ struct TileCfg {
     static constexpr int kOffBar = kOffBias + kBiasBytes;
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
+    static constexpr int kRedBytes = kBM * BN * 4;  // one fp32 partial tile (split-K)
     static_assert(kStages >= 2, "pipeline needs two stages");
+    static_assert(kRedBytes <= kStages * kStageBytes, "partial tile must fit the stage ring");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -111,6 +120,48 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& 
     tn = r / rows_in_group;
 }
 
+// The tiles and K blocks one CTA works on.
+struct WorkRange {
+    int first, stride, end;  // tiles first, first + stride, ... below end
+    int kb_begin, kb_end;    // K blocks [kb_begin, kb_end) of each tile
+    int rank, split;         // cluster rank and size (split == 1: persistent, no cluster)
+};
+
+__device__ __forceinline__ WorkRange work_range(const GemmParams& p)
+{
+    WorkRange w;
+    if (p.split > 1) {
+        const int tile = static_cast<int>(cluster_id_x());
+        w.first = tile;
+        w.stride = 1;
+        w.end = tile + 1;
+        w.rank = static_cast<int>(cluster_ctarank());
+        w.split = p.split;
+        w.kb_begin = w.rank * p.kb_per_split;
+        w.kb_end = min(p.k_blocks, w.kb_begin + p.kb_per_split);
+    } else {
+        w.first = blockIdx.x;
+        w.stride = gridDim.x;
+        w.end = p.tiles_m * p.tiles_n;
+        w.rank = 0;
+        w.split = 1;
+        w.kb_begin = 0;
+        w.kb_end = p.k_blocks;
+    }
+    return w;
+}
+
+// Byte offset, in the partial-tile buffer, of 16-byte unit `unit` (4 fp32 columns) of
+// accumulator row `row`; units are XOR-swizzled by the row so that the 8 rows a quarter
+// warp touches land in different banks.
+template <int BN>
+__device__ __forceinline__ uint32_t red_offset(int row, int unit)
+{
+    constexpr int kUnits = BN / 4;
+    constexpr int kSw = kUnits < 8 ? kUnits - 1 : 7;
+    return static_cast<uint32_t>(row * (BN * 4) + ((unit ^ (row & kSw)) << 4));
+}
+
 __device__ __forceinline__ float load_16bit(const void* base, long long idx, int bf16)
 {
     const uint16_t h = static_cast<const uint16_t*>(base)[idx];
@@ -148,19 +199,18 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
                                              volatile int* abort_flag)
 {
     using C = TileCfg<BN>;
-    const int num_tiles = p.tiles_m * p.tiles_n;
+    const WorkRange w = work_range(p);
     int stage = 0;
     uint32_t phase = 0;
     long long issued = 0;
     bool ok = true;
-    // Under a programmatic dependent launch, operands may come from the previous grid:
-    // every global read and write of this kernel is ordered after this wait (the epilogue
-    // writes only after MMAs that consume these loads).
+    // Under a programmatic dependent launch the operands may come from the previous grid:
+    // the loads wait for it (the epilogue threads wait on their own before reading).
     grid_dependency_wait();
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+    for (int tile = w.first; ok && tile < w.end; tile += w.stride) {
         int tm, tn;
         tile_coords(tile, p, tm, tn);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
             if (!wait_bounded(bar0 + 8u * (kBarEmpty + stage), phase ^ 1u, abort_flag,
                               p.wait_limit_ns)) {
                 if (!*abort_flag) record_failure(p.status, abort_flag, kRoleProducer);
@@ -213,14 +263,14 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
     // Swapped:  A operand N-major (rows of B), B operand K-major (rows of A).
     const uint32_t idesc = make_idesc_f16(static_cast<uint32_t>(p.bf16), SWAP ? 1u : 0u,
                                           SWAP ? 0u : 1u, kBM, BN);
-    const int num_tiles = p.tiles_m * p.tiles_n;
+    const WorkRange w = work_range(p);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool issued_any = false;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+    for (int tile = w.first; ok && tile < w.end; tile += w.stride) {
         if (!wait_bounded(bar0 + 8u * (kBarTmemEmpty + acc), acc_phase ^ 1u, abort_flag,
                           p.wait_limit_ns)) {
             if (!*abort_flag) record_failure(p.status, abort_flag, kRoleMma);
@@ -229,7 +279,7 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
         }
         tcgen05_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
             if (!wait_bounded(bar0 + 8u * (kBarFull + stage), phase, abort_flag,
                               p.wait_limit_ns)) {
                 if (!*abort_flag) record_failure(p.status, abort_flag, kRoleMma);
@@ -253,7 +303,7 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
                     ad = make_sdesc_sw128(sa + kk * 2048, 8192, 1024);
                     bd = make_sdesc_sw128(sb + kk * 32, 0, 1024);
                 }
-                mma_f16_ss(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                mma_f16_ss(d_tmem, ad, bd, idesc, (kb > w.kb_begin || kk > 0) ? 1u : 0u);
             }
             issued_any = true;
             mma_commit(bar0 + 8u * (kBarEmpty + stage));  // stage free once these MMAs finish
@@ -291,6 +341,48 @@ __device__ __forceinline__ void activate(float (&v)[N], int epilog)
     }
 }
 
+// Split-K, before the cluster synchronises: write this CTA's partial sums of the chunks
+// it does not own into its partial-tile buffer (the stage ring, idle once every MMA of the
+// tile has completed).
+template <int BN, bool SWAP>
+__device__ __forceinline__ void publish_partials(const GemmParams& p, uint8_t* smem,
+                                                 uint32_t bar0, uint32_t tmem_base,
+                                                 volatile int* abort_flag)
+{
+    using C = TileCfg<BN>;
+    constexpr int CH = C::kChunk;
+    const WorkRange w = work_range(p);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int tm, tn;
+    tile_coords(w.first, p, tm, tn);
+    const int col_limit = SWAP ? p.m : p.n;
+    const int nchunks = (min(BN, col_limit - tn * BN) + CH - 1) / CH;
+    if (!wait_bounded(bar0 + 8u * kBarTmemFull, 0, abort_flag, p.wait_limit_ns)) {
+        if (!*abort_flag) record_failure(p.status, abort_flag, kRoleEpilogue);
+        return;
+    }
+    tcgen05_fence_after_sync();
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    for (int c = 0; c < nchunks; ++c) {
+        if (c % w.split == w.rank) continue;
+        uint32_t r[32];
+        __syncwarp();
+        if constexpr (CH == 32)
+            tmem_load_32cols(t_lane + c * 32, r);
+        else
+            tmem_load_16cols(t_lane + c * 16, r);
+#pragma unroll
+        for (int u = 0; u < CH / 4; ++u) {
+            uint4 q = make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+            *reinterpret_cast<uint4*>(smem + red_offset<BN>(row, c * (CH / 4) + u)) = q;
+        }
+    }
+    tcgen05_fence_before_sync();
+}
+
 template <int BN, bool SWAP>
 __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem, uint32_t sbase,
                                              uint32_t bar0, uint32_t tmem_base,
@@ -302,7 +394,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
     const int lane = threadIdx.x & 31;
     const int ew = warp - 2;             // epilogue warp 0..3
     const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
-    const int num_tiles = p.tiles_m * p.tiles_n;
+    const WorkRange w = work_range(p);
     const bool has_bias = p.epilog != EPI_NONE;
     // Bias that varies along the accumulator's columns (staged in shared memory) or along
     // its lanes (one value per thread).
@@ -317,10 +409,12 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
     const uint16_t* R = static_cast<const uint16_t*>(p.residual);
     uint16_t* Dp = static_cast<uint16_t*>(p.D);
     uint32_t nstore = 0;
+    // Bias, residual and the outputs may belong to a programmatic predecessor grid.
+    grid_dependency_wait();
 
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    for (int tile = w.first; tile < w.end; tile += w.stride) {
         int tm, tn;
         tile_coords(tile, p, tm, tn);
         const int col_base = tn * BN;                          // first accumulator column
@@ -350,7 +444,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         const int nchunks = (valid_cols + CH - 1) / CH;
         const bool warp_live = lane_base < lane_limit;
 
-        for (int c = 0; c < nchunks; ++c) {
+        for (int c = w.rank; c < nchunks; c += w.split) {
             uint32_t r[32];
             __syncwarp();
             if constexpr (CH == 32)
@@ -359,8 +453,29 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                 tmem_load_16cols(t_lane + c * 16, r);
             float v[CH];
 #pragma unroll
-            for (int j = 0; j < CH; ++j)
-                v[j] = __uint_as_float(r[j]) + (col_bias ? sbias[c * CH + j] : lb);
+            for (int j = 0; j < CH; ++j) v[j] = __uint_as_float(r[j]);
+            if (w.split > 1) {
+                // add the other ranks' partial sums of this chunk (distributed shared memory)
+                const int row = quarter * 32 + lane;
+                for (int peer = 0; peer < w.split; ++peer) {
+                    if (peer == w.rank) continue;
+                    float4 part[CH / 4];
+#pragma unroll
+                    for (int u = 0; u < CH / 4; ++u)
+                        part[u] = ld_shared_cluster_v4(map_shared_rank(
+                            sbase + red_offset<BN>(row, c * (CH / 4) + u),
+                            static_cast<uint32_t>(peer)));
+#pragma unroll
+                    for (int u = 0; u < CH / 4; ++u) {
+                        v[4 * u] += part[u].x;
+                        v[4 * u + 1] += part[u].y;
+                        v[4 * u + 2] += part[u].z;
+                        v[4 * u + 3] += part[u].w;
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < CH; ++j) v[j] += col_bias ? sbias[c * CH + j] : lb;
 
             if constexpr (!SWAP) {
                 // ---- rows of D on lanes: thread = one row, 32 consecutive columns ----
@@ -515,6 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         __syncthreads();
     }
 
+    const bool split = p.split > 1;
     if (!*abort_flag) {
         if (warp == 0) {
             if (lane == 0) run_producer<BN, SWAP>(p, sbase, bar0, abort_flag);
@@ -522,9 +638,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         } else if (warp == 1) {
             if (lane == 0) run_mma<BN, SWAP>(p, sbase, bar0, tmem_base, abort_flag);
             __syncwarp();
+        } else if (split) {
+            publish_partials<BN, SWAP>(p, smem, bar0, tmem_base, abort_flag);
         } else {
             run_epilogue<BN, SWAP>(p, smem, sbase, bar0, tmem_base, abort_flag);
         }
+    }
+    if (split) {
+        // Every thread of every CTA of the cluster reaches both barriers: each role above
+        // ends in bounded time, on success or on abort.
+        __syncwarp();
+        cluster_sync_all();  // partial sums written
+        if (warp >= 2 && !*abort_flag)
+            run_epilogue<BN, SWAP>(p, smem, sbase, bar0, tmem_base, abort_flag);
+        __syncwarp();
+        cluster_sync_all();  // the peers are done reading this CTA's partial sums
     }
 
     tcgen05_fence_before_sync();

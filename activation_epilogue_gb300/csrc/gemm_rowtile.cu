@@ -20,13 +20,22 @@ cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t stream, bool 
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = TileCfg<BN>::kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
     if (pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
     }
+    if (p.split > 1) {  // split-K: one cluster of `split` CTAs per output tile
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = static_cast<unsigned>(p.split);
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = na ? attr : nullptr;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, gemm_epi_kernel<BN, false>, p);
 }
 }  // namespace

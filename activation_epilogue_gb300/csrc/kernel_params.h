@@ -50,6 +50,12 @@ struct GemmParams {
     int bf16;         // 1 = bfloat16, 0 = binary16
     int aux_ld;       // uint32 words per aux row
     int debug_stall;
+    // Split-K across a thread-block cluster: split > 1 launches tiles * split CTAs in
+    // clusters of `split`; rank r of a cluster accumulates K blocks
+    // [r * kb_per_split, (r + 1) * kb_per_split) of the cluster's tile, and the partial
+    // sums are added on chip (distributed shared memory) before the epilogue.
+    int split;
+    int kb_per_split;
 };
 
 // Row-tile kernel (BN in {64, 128, 256}) and swapped small-m kernel (BN in {16 ... 256}).

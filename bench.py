@@ -268,6 +268,10 @@ def run_ours(args, rank, world, local_rank, dist):
     barrier = (lambda: dist.barrier()) if dist is not None else None
 
     w = workloads.GEMMS[args.workload]
+    if args.rows:
+        # a row slice of the same workload (same shapes of B and bias, same distributions)
+        import dataclasses
+        w = dataclasses.replace(w, m=args.rows, name=f"{w.name}_rows{args.rows}")
     td = workloads.TORCH_DTYPES[w.dtype]
     inp = workloads.gemm_inputs(w, device=dev)
     A, B, bias = inp["A"], inp["B"], inp["bias"]
@@ -275,7 +279,9 @@ def run_ours(args, rank, world, local_rank, dist):
     aux = None
     if w.epilog == "RELU_AUX_BIAS":
         aux = torch.empty((w.m, (w.n + 31) // 32), dtype=torch.int32, device=dev)
-    plan = gemm_epi.Plan(w.m, w.n, w.k, w.dtype, w.epilog, w.bias_layout)
+    opts = dict(kv.split("=") for kv in args.opt)
+    plan = gemm_epi.Plan(w.m, w.n, w.k, w.dtype, w.epilog, w.bias_layout,
+                         **{k: int(v) for k, v in opts.items()})
     log(f"[bench] rank {rank}: {plan.describe()}")
 
     def step():
@@ -307,13 +313,13 @@ def run_ours(args, rank, world, local_rank, dist):
     achieved = flops_step / kernel_s / 1e12
     sustained = secs >= 1.0
     peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
-    traffic = load_traffic(args.workload)
+    traffic = load_traffic(w.name)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": kernel_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": args.workload, "m": w.m, "n": w.n, "k": w.k, "epilog": w.epilog,
+        "config": {"workload": w.name, "m": w.m, "n": w.n, "k": w.k, "epilog": w.epilog,
                    "bias_layout": "(1,n)" if w.bias_layout == "1N" else "(m,1)",
                    "l2": "inputs larger than L2 (no flush needed)",
                    "parallelism": f"replicas x{world}", "plan": plan.describe()},
@@ -438,22 +444,32 @@ def measure_extras(plan, w, A, B, bias, D, aux, stream, peaks):
             "unfused_us_cold_l2": cold_unf * 1e6, "unavoidable_bytes": unavoidable,
             "status": st, "plan": desc}
         del inp, Dg, auxg, pre
-    # the FFN block: GEMM1 (bias + GELU) then GEMM2 (bias + residual), two launches
+    # the FFN block through its plan: GEMM1 (bias + GELU), then GEMM2 (bias + residual) as a
+    # programmatic dependent launch; and the unfused chain (GEMM, bias+GELU pass, GEMM,
+    # bias+residual pass: four launches, two extra round trips of pre-activations)
     f = workloads.FFNS["ffn_bf16_4096x1024x4096"]
     fi = workloads.ffn_inputs(f, device=A.device)
-    H = torch.empty((f.t, f.f), dtype=torch.bfloat16, device=A.device)
     Y = torch.empty((f.t, f.d), dtype=torch.bfloat16, device=A.device)
-    with gemm_epi.Plan(f.t, f.f, f.d, "bf16", "GELU_BIAS", "1N") as p1, \
+    H = torch.empty((f.t, f.f), dtype=torch.bfloat16, device=A.device)
+    pre1 = torch.empty((f.t, f.f), dtype=torch.bfloat16, device=A.device)
+    pre2 = torch.empty((f.t, f.d), dtype=torch.bfloat16, device=A.device)
+    with gemm_epi.FfnPlan(f.t, f.d, f.f, "bf16") as fp, \
+            gemm_epi.Plan(f.t, f.f, f.d, "bf16", "GELU_BIAS", "1N") as p1, \
             gemm_epi.Plan(f.t, f.d, f.f, "bf16", "BIAS_RESIDUAL", "1N") as p2:
         def ffn():
-            p1.execute(fi["X"], fi["W1"], fi["b1"], H)
-            p2.execute(H, fi["W2"], fi["b2"], Y, residual=fi["R"])
+            fp.execute(fi["X"], fi["W1"], fi["b1"], fi["W2"], fi["b2"], fi["R"], Y)
+
+        def ffn_unfused():
+            p1.execute_unfused(fi["X"], fi["W1"], fi["b1"], pre1, H)
+            p2.execute_unfused(H, fi["W2"], fi["b2"], pre2, Y, residual=fi["R"])
         cold = time_cold(ffn, 20, stream, flush)
         hot = time_graph(ffn, 10, 10, stream)
+        cold_unf = time_cold(ffn_unfused, 20, stream, flush)
         per[f.name] = {"us_per_call_cold_l2": cold * 1e6, "us_per_call_graph_hot_l2": hot * 1e6,
                        "tflops_cold": f.flops / cold / 1e12,
                        "tensor_frac_cold": f.flops / cold / 1e12 / peaks["bf16_tflops"],
-                       "launches": 2, "status": [p1.sync_status(), p2.sync_status()],
+                       "launches": 2, "unfused_us_cold_l2": cold_unf * 1e6,
+                       "unfused_launches": 4, "status": fp.sync_status(),
                        "plans": [p1.describe(), p2.describe()]}
     out["workloads"] = per
     return out
@@ -466,6 +482,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--opt", action="append", default=[], metavar="KEY=VALUE",
+                    help="plan option for the timed workload, e.g. SPLIT_K=1 (repeatable)")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="time only this many rows of the workload (for profiler captures)")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

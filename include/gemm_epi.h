@@ -100,7 +100,8 @@ typedef enum {
 typedef enum {
     GEMM_EPI_OPT_VARIANT = 0,       /* 1 = row-tile kernel, 2 = swapped small-m kernel */
     GEMM_EPI_OPT_TILE_N = 1,        /* row-tile kernel: N tile 64, 128 or 256 */
-    GEMM_EPI_OPT_SPLIT_K = 2,       /* swapped kernel: K slices per output tile, 1..8 */
+    GEMM_EPI_OPT_SPLIT_K = 2,       /* K slices per output tile, 1..8 (one cluster of that
+                                       many CTAs per tile; partial sums added on chip) */
     GEMM_EPI_OPT_GRID = 3,          /* cap on persistent CTAs (<= SM count) */
     GEMM_EPI_OPT_GROUP_M = 4,       /* tile raster: M tiles per group */
     GEMM_EPI_OPT_WAIT_LIMIT_US = 5, /* device-side wait limit, microseconds (default 2 s) */

@@ -273,3 +273,34 @@ def test_ffn_in_place_on_residual():
     import oracle
     _, _, Y_ref = oracle.ffn(**cpu)
     assert rel_err(gi["R"], Y_ref) <= TOL["bf16"]
+
+
+# ---- split-K across a cluster (partial sums added on chip) ---------------------------------
+
+@pytest.mark.parametrize("variant,bn,split", [(1, 64, 2), (1, 128, 3), (1, 256, 4), (1, 128, 8),
+                                              (2, 0, 2), (2, 0, 5), (2, 0, 8)])
+@pytest.mark.parametrize("epilog", ["BIAS", "GELU_BIAS", "RELU_AUX_BIAS", "BIAS_RESIDUAL"])
+def test_split_k_parity(variant, bn, split, epilog):
+    m, n, k = (300 if variant == 1 else 40), 520, 1000    # 16 K blocks, the last one 40 deep
+    layout = "M1" if (split + len(epilog)) % 2 else "1N"
+    p = _inputs(m, n, k, "bf16", layout, seed=split * 10 + variant)
+    opts = {"VARIANT": variant, "SPLIT_K": split}
+    if bn:
+        opts["TILE_N"] = bn
+    _, _, _, _, desc = check(p, m, n, k, "bf16", epilog, layout, options=opts)
+    kpb = -(-16 // split)                       # K blocks per slice; no slice is left empty
+    assert f"split_k={-(-16 // kpb)}" in desc
+
+
+@pytest.mark.parametrize("variant,split", [(1, 4), (2, 6)])
+def test_split_k_integer_bit_exact(variant, split):
+    m, n, k = (256 if variant == 1 else 16), 264, 512
+    p = _inputs(m, n, k, "bf16", "1N", seed=31, kind="int")
+    check(p, m, n, k, "bf16", "RELU_AUX_BIAS", "1N", options={"VARIANT": variant,
+                                                             "SPLIT_K": split}, exact=True)
+
+
+def test_small_m_plans_split_k():
+    with gemm_epi.Plan(16, 3072, 768, "bf16", "GELU_BIAS", "1N") as plan:
+        desc = plan.describe()
+    assert "variant=swapped" in desc and "split_k=6" in desc, desc
