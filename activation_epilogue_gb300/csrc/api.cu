@@ -59,6 +59,7 @@ struct gemm_epi_plan_s {
     int split, kb_per_split;  // split-K across a cluster (split == 1: persistent kernel)
     // options (0 = automatic)
     int opt_variant, opt_bn, opt_split_k, opt_grid, opt_group_m;
+    int prefetch;  // L2 prefetch distance in K blocks (GEMM_EPI_OPT_PREFETCH)
     unsigned long long wait_limit_ns;
     int debug_stall;
     int* d_status;
@@ -153,8 +154,24 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             p->smem = swapped_smem_bytes(bn);
         }
         const long long tiles = static_cast<long long>(p->tiles_m) * p->tiles_n;
-        const int want_split =
-            p->opt_split_k > 0 ? p->opt_split_k : auto_split(tiles, p->k_blocks, p->sm_count);
+        cudaError_t e = v == kRowTile ? rowtile_prepare(p->bn) : swapped_prepare(p->bn);
+        if (e != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
+        int want_split = p->opt_split_k;
+        if (want_split <= 0) {
+            // the largest automatic split whose clusters are all resident at once
+            want_split = auto_split(tiles, p->k_blocks, p->sm_count);
+            while (want_split > 1) {
+                int kpb = 0;
+                const int s = normalise_split(want_split, p->k_blocks, &kpb);
+                const int fit = v == kRowTile ? rowtile_max_clusters(p->bn, s)
+                                              : swapped_max_clusters(p->bn, s);
+                if (fit >= tiles) {
+                    want_split = s;
+                    break;
+                }
+                --want_split;
+            }
+        }
         p->split = normalise_split(want_split, p->k_blocks, &p->kb_per_split);
         long long grid;
         if (p->split > 1) {
@@ -181,10 +198,6 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
              ename[p->epilog], p->bias_layout == GEMM_EPI_BIAS_M1 ? "(m,1)" : "(1,n)",
              vname[p->variant], p->bn, p->stages, p->smem, p->tiles_m, p->tiles_n, p->k_blocks,
              p->split, p->grid, p->group_m, p->sm_count);
-    if (p->variant == kRowTile || p->variant == kSwapped) {
-        cudaError_t e = p->variant == kRowTile ? rowtile_prepare(p->bn) : swapped_prepare(p->bn);
-        if (e != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
-    }
     const char* log = getenv("GEMM_EPI_LOG");
     if (log && log[0] == '1') fprintf(stderr, "[gemm_epi] plan: %s\n", p->desc);
     return GEMM_EPI_OK;
@@ -219,7 +232,10 @@ gemm_epi_status ensure_maps(gemm_epi_plan_s* p, const void* A, const void* B, vo
         if (!encode_2d(&p->tm_D, D, dt, p->n, p->m, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
             return GEMM_EPI_ERR_LAUNCH;
     } else {
-        memset(&p->tm_D, 0, sizeof(p->tm_D));
+        // swapped kernel: boxes of 32 columns x (up to) 32 rows of D, transposed on chip
+        const uint32_t rows = p->bn < 32 ? static_cast<uint32_t>(p->bn) : 32u;
+        if (!encode_2d(&p->tm_D, D, dt, p->n, p->m, 32, rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return GEMM_EPI_ERR_LAUNCH;
     }
     p->key_A = A;
     p->key_B = B;
@@ -267,6 +283,7 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const void* A, const void* B, co
     prm.debug_stall = p->debug_stall;
     prm.split = p->split;
     prm.kb_per_split = p->kb_per_split;
+    prm.prefetch = p->prefetch;
     cudaError_t e = p->variant == kRowTile ? rowtile_launch(p->bn, prm, p->grid, stream, pdl)
                                            : swapped_launch(p->bn, prm, p->grid, stream, pdl);
     return e == cudaSuccess ? GEMM_EPI_OK : GEMM_EPI_ERR_LAUNCH;
@@ -402,6 +419,10 @@ gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt,
     case GEMM_EPI_OPT_WAIT_LIMIT_US:
         if (value < 0 || value > 600ll * 1000 * 1000) return GEMM_EPI_ERR_INVALID_ARG;
         p->wait_limit_ns = value == 0 ? kDefaultWaitNs : static_cast<unsigned long long>(value) * 1000ull;
+        return GEMM_EPI_OK;
+    case GEMM_EPI_OPT_PREFETCH:
+        if (value < 0 || value > 64) return GEMM_EPI_ERR_INVALID_ARG;
+        p->prefetch = static_cast<int>(value);
         return GEMM_EPI_OK;
     case GEMM_EPI_OPT_DEBUG_STALL:
         if (value != 0 && value != 1) return GEMM_EPI_ERR_INVALID_ARG;

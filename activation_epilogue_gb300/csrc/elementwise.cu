@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "gelu.cuh"
 #include "kernel_params.h"
 
 namespace gemm_epi {
@@ -63,7 +64,7 @@ __global__ void __launch_bounds__(256) elementwise_epilogue_kernel(
             if (epilog == EPI_RELU_BIAS || epilog == EPI_RELU_AUX_BIAS)
                 o = o > 0.0f ? o : 0.0f;
             else if (epilog == EPI_GELU_BIAS)
-                o = 0.5f * o * (1.0f + erff(o * 0.70710678118654752f));
+                o = gelu_erf_fast(o);
             const long long idx = static_cast<long long>(row) * n + col;
             if (ok) {
                 if (epilog == EPI_BIAS_RESIDUAL) o += ld16(residual, idx, bf16);

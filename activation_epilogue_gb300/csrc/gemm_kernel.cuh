@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "gelu.cuh"
 #include "kernel_params.h"
 #include "ptx.cuh"
 
@@ -185,53 +186,95 @@ __device__ __forceinline__ uint16_t to16(float a, int bf16)
     return __half_as_ushort(__float2half_rn(a));
 }
 
-// erf-form GELU in fp32: x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)).
-__device__ __forceinline__ float gelu_erf(float x)
-{
-    return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
-}
 
 // ------------------------------------------------------------------------------------------
 // producer: TMA loads
 // ------------------------------------------------------------------------------------------
+// Arm stage `stage` for K block `kb` of tile (tm, tn) and issue its TMA loads.
 template <int BN, bool SWAP>
-__device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase, uint32_t bar0,
-                                             volatile int* abort_flag)
+__device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase, uint32_t bar0,
+                                            int stage, int tm, int tn, int kb)
+{
+    using C = TileCfg<BN>;
+    const uint32_t fb = bar0 + 8u * (kBarFull + stage);
+    mbar_arrive_expect_tx(fb, C::kStageBytes);
+    const uint32_t sa = sbase + stage * C::kStageBytes;
+    const uint32_t sb = sa + C::kABytes;
+    const int k0 = kb * kBK;
+    if (!SWAP) {
+        tma_load_2d(sa, &p.tm_A, fb, k0, tm * kBM);
+#pragma unroll
+        for (int q = 0; q < BN / 64; ++q)
+            tma_load_2d(sb + q * 8192, &p.tm_B, fb, tn * BN + q * 64, k0);
+    } else {
+        tma_load_2d(sa, &p.tm_B, fb, tm * kBM, k0);
+        tma_load_2d(sa + 8192, &p.tm_B, fb, tm * kBM + 64, k0);
+        tma_load_2d(sb, &p.tm_A, fb, k0, tn * BN);
+    }
+}
+
+// L2 prefetch of the operand boxes of K block `kb` of tile (tm, tn).
+template <int BN, bool SWAP>
+__device__ __forceinline__ void prefetch_stage(const GemmParams& p, int tm, int tn, int kb)
+{
+    const int k0 = kb * kBK;
+    if (!SWAP) {
+        tma_prefetch_2d(&p.tm_A, k0, tm * kBM);
+#pragma unroll
+        for (int q = 0; q < BN / 64; ++q) tma_prefetch_2d(&p.tm_B, tn * BN + q * 64, k0);
+    } else {
+        tma_prefetch_2d(&p.tm_B, tm * kBM, k0);
+        tma_prefetch_2d(&p.tm_B, tm * kBM + 64, k0);
+        tma_prefetch_2d(&p.tm_A, k0, tn * BN);
+    }
+}
+
+// Before the CTA-wide set-up barrier, the thread that initialised the mbarriers fills the
+// fresh stage ring for the first tile (no "empty" wait is needed yet), so the first loads
+// overlap the tensor-memory allocation.  Returns the number of stages issued.
+template <int BN, bool SWAP>
+__device__ __forceinline__ int producer_prologue(const GemmParams& p, uint32_t sbase,
+                                                 uint32_t bar0)
 {
     using C = TileCfg<BN>;
     const WorkRange w = work_range(p);
-    int stage = 0;
-    uint32_t phase = 0;
-    long long issued = 0;
+    if (w.first >= w.end || p.debug_stall) return 0;
+    // Under a programmatic dependent launch the operands may come from the previous grid.
+    grid_dependency_wait();
+    int tm, tn;
+    tile_coords(w.first, p, tm, tn);
+    const int n = min(C::kStages, w.kb_end - w.kb_begin);
+    for (int i = 0; i < n; ++i) issue_stage<BN, SWAP>(p, sbase, bar0, i, tm, tn, w.kb_begin + i);
+    for (int i = 0; i < p.prefetch && w.kb_begin + n + i < w.kb_end; ++i)
+        prefetch_stage<BN, SWAP>(p, tm, tn, w.kb_begin + n + i);
+    return n;
+}
+
+// The producer loop, continuing after the `pre` stages the prologue issued.
+template <int BN, bool SWAP>
+__device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase, uint32_t bar0,
+                                             volatile int* abort_flag, int pre)
+{
+    using C = TileCfg<BN>;
+    const WorkRange w = work_range(p);
+    int stage = pre % C::kStages;
+    uint32_t phase = static_cast<uint32_t>((pre / C::kStages) & 1);
+    long long issued = pre;
     bool ok = true;
-    // Under a programmatic dependent launch the operands may come from the previous grid:
-    // the loads wait for it (the epilogue threads wait on their own before reading).
     grid_dependency_wait();
     for (int tile = w.first; ok && tile < w.end; tile += w.stride) {
         int tm, tn;
         tile_coords(tile, p, tm, tn);
-        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+        for (int kb = (tile == w.first ? w.kb_begin + pre : w.kb_begin); kb < w.kb_end; ++kb) {
             if (!wait_bounded(bar0 + 8u * (kBarEmpty + stage), phase ^ 1u, abort_flag,
                               p.wait_limit_ns)) {
                 if (!*abort_flag) record_failure(p.status, abort_flag, kRoleProducer);
                 ok = false;
                 break;
             }
-            const uint32_t fb = bar0 + 8u * (kBarFull + stage);
-            mbar_arrive_expect_tx(fb, C::kStageBytes);
-            const uint32_t sa = sbase + stage * C::kStageBytes;
-            const uint32_t sb = sa + C::kABytes;
-            const int k0 = kb * kBK;
-            if (!SWAP) {
-                tma_load_2d(sa, &p.tm_A, fb, k0, tm * kBM);
-#pragma unroll
-                for (int q = 0; q < BN / 64; ++q)
-                    tma_load_2d(sb + q * 8192, &p.tm_B, fb, tn * BN + q * 64, k0);
-            } else {
-                tma_load_2d(sa, &p.tm_B, fb, tm * kBM, k0);
-                tma_load_2d(sa + 8192, &p.tm_B, fb, tm * kBM + 64, k0);
-                tma_load_2d(sb, &p.tm_A, fb, k0, tn * BN);
-            }
+            issue_stage<BN, SWAP>(p, sbase, bar0, stage, tm, tn, kb);
+            if (p.prefetch && kb + p.prefetch < w.kb_end)
+                prefetch_stage<BN, SWAP>(p, tm, tn, kb + p.prefetch);
             ++issued;
             if (++stage == C::kStages) {
                 stage = 0;
@@ -337,7 +380,7 @@ __device__ __forceinline__ void activate(float (&v)[N], int epilog)
         for (int j = 0; j < N; ++j) v[j] = v[j] > 0.0f ? v[j] : 0.0f;
     } else if (epilog == EPI_GELU_BIAS) {
 #pragma unroll
-        for (int j = 0; j < N; ++j) v[j] = gelu_erf(v[j]);
+        for (int j = 0; j < N; ++j) v[j] = gelu_erf_fast(v[j]);
     }
 }
 
@@ -407,7 +450,6 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
     uint8_t* epi_buf = smem + C::kOffEpi + ew * 2 * 2048;
     const uint32_t epi_buf_u32 = sbase + C::kOffEpi + ew * 2 * 2048;
     const uint16_t* R = static_cast<const uint16_t*>(p.residual);
-    uint16_t* Dp = static_cast<uint16_t*>(p.D);
     uint32_t nstore = 0;
     // Bias, residual and the outputs may belong to a programmatic predecessor grid.
     grid_dependency_wait();
@@ -455,22 +497,34 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
 #pragma unroll
             for (int j = 0; j < CH; ++j) v[j] = __uint_as_float(r[j]);
             if (w.split > 1) {
-                // add the other ranks' partial sums of this chunk (distributed shared memory)
+                // Add the other ranks' partial sums of this chunk (distributed shared
+                // memory): four 16-byte units at a time, every peer's loads issued before
+                // any of them is consumed, so their latencies overlap.
                 const int row = quarter * 32 + lane;
-                for (int peer = 0; peer < w.split; ++peer) {
-                    if (peer == w.rank) continue;
-                    float4 part[CH / 4];
 #pragma unroll
-                    for (int u = 0; u < CH / 4; ++u)
-                        part[u] = ld_shared_cluster_v4(map_shared_rank(
-                            sbase + red_offset<BN>(row, c * (CH / 4) + u),
-                            static_cast<uint32_t>(peer)));
+                for (int u0 = 0; u0 < CH / 4; u0 += 4) {
+                    float4 part[7][4];
 #pragma unroll
-                    for (int u = 0; u < CH / 4; ++u) {
-                        v[4 * u] += part[u].x;
-                        v[4 * u + 1] += part[u].y;
-                        v[4 * u + 2] += part[u].z;
-                        v[4 * u + 3] += part[u].w;
+                    for (int pi = 0; pi < 7; ++pi) {
+                        if (pi < w.split - 1) {
+                            const uint32_t peer = static_cast<uint32_t>(pi < w.rank ? pi : pi + 1);
+#pragma unroll
+                            for (int uu = 0; uu < 4; ++uu)
+                                part[pi][uu] = ld_shared_cluster_v4(map_shared_rank(
+                                    sbase + red_offset<BN>(row, c * (CH / 4) + u0 + uu), peer));
+                        }
+                    }
+#pragma unroll
+                    for (int pi = 0; pi < 7; ++pi) {
+                        if (pi < w.split - 1) {
+#pragma unroll
+                            for (int uu = 0; uu < 4; ++uu) {
+                                v[4 * (u0 + uu)] += part[pi][uu].x;
+                                v[4 * (u0 + uu) + 1] += part[pi][uu].y;
+                                v[4 * (u0 + uu) + 2] += part[pi][uu].z;
+                                v[4 * (u0 + uu) + 3] += part[pi][uu].w;
+                            }
+                        }
                     }
                 }
             }
@@ -555,15 +609,29 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                     }
                 }
                 activate(v, p.epilog);
+                if (p.epilog == EPI_BIAS_RESIDUAL) {
 #pragma unroll
-                for (int j = 0; j < CH; ++j) {
-                    const int t = t0 + j;
-                    if (col_ok && t < p.m) {
-                        const long long idx = static_cast<long long>(t) * p.n + col;
-                        float o = v[j];
-                        if (p.epilog == EPI_BIAS_RESIDUAL) o += load_16bit(R, idx, p.bf16);
-                        Dp[idx] = to16(o, p.bf16);
+                    for (int j = 0; j < CH; ++j)
+                        if (col_ok && t0 + j < p.m)
+                            v[j] += load_16bit(R, static_cast<long long>(t0 + j) * p.n + col, p.bf16);
+                }
+                if (warp_live) {
+                    // Transpose through shared memory: row j of the box holds D[t0 + j][32
+                    // columns of this warp] (64 bytes; lane = column, so each row is written
+                    // by one conflict-free warp store), then one TMA store of the box.
+                    const uint32_t buf = nstore & 1u;
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                    uint16_t* tb = reinterpret_cast<uint16_t*>(epi_buf + buf * 2048);
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) tb[j * 32 + lane] = to16(v[j], p.bf16);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tm_D, epi_buf_u32 + buf * 2048, lane_base, t0);
+                        bulk_commit_group();
                     }
+                    ++nstore;
                 }
             }
         }
@@ -572,9 +640,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
     }
-    if constexpr (!SWAP) {
-        if (lane == 0) bulk_wait_group<0>();
-    }
+    if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
 }
 
@@ -594,6 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + kOffAbort);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    int pre = 0;  // stages the prologue issued (thread 0, which is also the producer)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -610,7 +677,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         fence_mbar_init();
         prefetch_tensormap(&p.tm_A);
         prefetch_tensormap(&p.tm_B);
-        if (!SWAP) prefetch_tensormap(&p.tm_D);
+        prefetch_tensormap(&p.tm_D);
+        pre = producer_prologue<BN, SWAP>(p, sbase, bar0);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
@@ -633,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     const bool split = p.split > 1;
     if (!*abort_flag) {
         if (warp == 0) {
-            if (lane == 0) run_producer<BN, SWAP>(p, sbase, bar0, abort_flag);
+            if (lane == 0) run_producer<BN, SWAP>(p, sbase, bar0, abort_flag, pre);
             __syncwarp();
         } else if (warp == 1) {
             if (lane == 0) run_mma<BN, SWAP>(p, sbase, bar0, tmem_base, abort_flag);

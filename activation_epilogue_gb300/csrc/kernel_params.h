@@ -33,7 +33,8 @@ enum : int {
 struct GemmParams {
     CUtensorMap tm_A;  // A[m][k]: K-major boxes {64 k, rows}, 128-byte swizzle
     CUtensorMap tm_B;  // B[k][n]: N-major boxes {64 n, 64 k}, 128-byte swizzle
-    CUtensorMap tm_D;  // D[m][n]: store boxes {32 n, 32 m}, 64-byte swizzle (row-tile kernel)
+    CUtensorMap tm_D;  // D[m][n]: store boxes {32 n, 32 m} with the 64-byte swizzle (row-tile
+                       // kernel) or {32 n, min(BN, 32) m} unswizzled (swapped kernel)
     const void* bias;
     const void* residual;
     void* D;
@@ -56,6 +57,10 @@ struct GemmParams {
     // sums are added on chip (distributed shared memory) before the epilogue.
     int split;
     int kb_per_split;
+    // The producer also prefetches into L2 the operand boxes of the K block this many
+    // blocks ahead of the one it loads (0 = off), so that a first touch of a panel in
+    // device memory overlaps the loads of the blocks before it.
+    int prefetch;
 };
 
 // Row-tile kernel (BN in {64, 128, 256}) and swapped small-m kernel (BN in {16 ... 256}).
@@ -69,6 +74,10 @@ cudaError_t swapped_prepare(int bn);
 cudaError_t swapped_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
 int swapped_smem_bytes(int bn);
 int swapped_stages(int bn);
+
+// Clusters of `split` CTAs of the kernel that can be resident at once (0 on error).
+int rowtile_max_clusters(int bn, int split);
+int swapped_max_clusters(int bn, int split);
 
 // Elementwise epilogue over a 16-bit pre-activation (the unfused baseline's second kernel;
 // pre == nullptr means pre = 0, which serves k == 0).

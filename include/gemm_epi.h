@@ -105,10 +105,12 @@ typedef enum {
     GEMM_EPI_OPT_GRID = 3,          /* cap on persistent CTAs (<= SM count) */
     GEMM_EPI_OPT_GROUP_M = 4,       /* tile raster: M tiles per group */
     GEMM_EPI_OPT_WAIT_LIMIT_US = 5, /* device-side wait limit, microseconds (default 2 s) */
-    GEMM_EPI_OPT_DEBUG_STALL = 6    /* 1: the next launches wait on a barrier nothing
+    GEMM_EPI_OPT_DEBUG_STALL = 6,   /* 1: the next launches wait on a barrier nothing
                                        arrives at, run out the wait limit and report
                                        GEMM_EPI_ERR_DEVICE_TIMEOUT (a test of the timeout
                                        path; no copy or MMA is issued) */
+    GEMM_EPI_OPT_PREFETCH = 7       /* L2 prefetch distance in 64-deep K blocks, 0..64
+                                       (0 = none) */
 } gemm_epi_option;
 
 /*

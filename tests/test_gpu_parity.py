@@ -303,4 +303,16 @@ def test_split_k_integer_bit_exact(variant, split):
 def test_small_m_plans_split_k():
     with gemm_epi.Plan(16, 3072, 768, "bf16", "GELU_BIAS", "1N") as plan:
         desc = plan.describe()
-    assert "variant=swapped" in desc and "split_k=6" in desc, desc
+    fields = dict(kv.split("=") for kv in desc.split() if "=" in kv)
+    assert fields["variant"] == "swapped", desc
+    # split across a cluster, with every cluster resident at once (one wave)
+    assert int(fields["split_k"]) > 1, desc
+    assert int(fields["grid"]) <= int(fields["sms"]), desc
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_l2_prefetch_option_keeps_results(variant):
+    m, n, k = (384 if variant == 1 else 64), 520, 1000
+    p = _inputs(m, n, k, "bf16", "1N", seed=41)
+    check(p, m, n, k, "bf16", "RELU_AUX_BIAS", "1N",
+          options={"VARIANT": variant, "PREFETCH": 4, "SPLIT_K": 1})
