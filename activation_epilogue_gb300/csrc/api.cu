@@ -60,6 +60,7 @@ struct gemm_epi_plan_s {
     // options (0 = automatic)
     int opt_variant, opt_bn, opt_split_k, opt_grid, opt_group_m;
     int prefetch;  // L2 prefetch distance in K blocks (GEMM_EPI_OPT_PREFETCH)
+    int no_pdl;    // 1: launch without programmatic dependent launch (GEMM_EPI_OPT_PDL = 0)
     unsigned long long wait_limit_ns;
     int debug_stall;
     int* d_status;
@@ -305,7 +306,7 @@ gemm_epi_status run_plan(gemm_epi_plan_s* p, const void* A, const void* B, const
                                            static_cast<int>((p->n + 31) / 32), p->sm_count, stream);
         return e == cudaSuccess ? GEMM_EPI_OK : GEMM_EPI_ERR_LAUNCH;
     }
-    return launch_gemm(p, A, B, bias, residual, D, aux, p->epilog, stream, pdl);
+    return launch_gemm(p, A, B, bias, residual, D, aux, p->epilog, stream, pdl && !p->no_pdl);
 }
 
 gemm_epi_status check_operands(const gemm_epi_plan_s* p, const void* A, const void* B,
@@ -424,6 +425,10 @@ gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt,
         if (value < 0 || value > 64) return GEMM_EPI_ERR_INVALID_ARG;
         p->prefetch = static_cast<int>(value);
         return GEMM_EPI_OK;
+    case GEMM_EPI_OPT_PDL:
+        if (value != 0 && value != 1) return GEMM_EPI_ERR_INVALID_ARG;
+        p->no_pdl = value ? 0 : 1;
+        return GEMM_EPI_OK;
     case GEMM_EPI_OPT_DEBUG_STALL:
         if (value != 0 && value != 1) return GEMM_EPI_ERR_INVALID_ARG;
         p->debug_stall = static_cast<int>(value);
@@ -449,7 +454,10 @@ gemm_epi_status gemm_epi_execute_ex(gemm_epi_plan_t p, const void* A, const void
     if (p->variant == kEmpty) return GEMM_EPI_OK;
     st = check_device(p);
     if (st != GEMM_EPI_OK) return st;
-    return run_plan(p, A, B, bias, residual, D, aux, stream, false);
+    // Every global access of the fused kernel waits for the previous grid on the stream
+    // (griddepcontrol.wait), so it is always launched as a programmatic dependent: its
+    // launch and set-up overlap the tail of whatever runs before it.
+    return run_plan(p, A, B, bias, residual, D, aux, stream, true);
 }
 
 gemm_epi_status gemm_epi_execute(gemm_epi_plan_t p, const void* A, const void* B,
@@ -591,7 +599,7 @@ gemm_epi_status gemm_epi_ffn_execute(gemm_epi_ffn_plan_t p, const void* X, const
     if (p->t == 0 || p->d == 0) return GEMM_EPI_OK;
     st = check_device(p->g1);
     if (st != GEMM_EPI_OK) return st;
-    st = run_plan(p->g1, X, W1, b1, nullptr, p->H, nullptr, stream, false);
+    st = run_plan(p->g1, X, W1, b1, nullptr, p->H, nullptr, stream, true);
     if (st != GEMM_EPI_OK) return st;
     // GEMM 2 reads H only after GEMM 1 has completed (griddepcontrol.wait in its producer).
     return run_plan(p->g2, p->H, W2, b2, R, Y, nullptr, stream, p->g1->variant != kEmpty);

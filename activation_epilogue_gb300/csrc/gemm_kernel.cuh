@@ -12,8 +12,9 @@
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma (fp32 accumulate)
 //               into one of two TMEM accumulators and commits each consumed stage back to
 //               its "empty" mbarrier, and each finished tile to a "tmem full" mbarrier.
-//   warps 2-5   epilogue: each warp owns one 32-lane quarter of the accumulator; it reads
-//               32 columns at a time from TMEM, adds the bias (staged per warp in shared
+//   warps 2-9   epilogue: two warps per 32-lane quarter of the accumulator, taking
+//               alternate 32-column chunks (two warps per scheduler hide the latency of the
+//               activation arithmetic); a warp reads a chunk from TMEM, adds the bias (staged per warp in shared
 //               memory when it varies along the columns), applies the activation, builds
 //               the ReLU mask words, rounds to 16 bits and writes D through a swizzled
 //               shared-memory box and a TMA store.  While it drains one accumulator the
@@ -43,8 +44,9 @@ namespace gemm_epi {
 constexpr int kBM = 128;        // MMA M: TMEM lanes
 constexpr int kBK = 64;         // K block: one 128-byte swizzle row of 16-bit elements
 constexpr int kUmmaK = 16;      // K of one tcgen05.mma.kind::f16
-constexpr int kThreads = 192;   // 6 warps
-constexpr int kEpiThreads = 128;
+constexpr int kEpiWarps = 8;    // two per TMEM lane quarter, alternating chunks
+constexpr int kThreads = 64 + 32 * kEpiWarps;   // producer, MMA, epilogue warps
+constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kPipeBudget = 192 * 1024;
 
 template <int BN>
@@ -56,10 +58,10 @@ struct TileCfg {
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
     static constexpr int kChunk = BN < 32 ? BN : 32;            // columns per TMEM load
     static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
-    static constexpr int kOffEpi = kStages * kStageBytes;        // 4 warps x 2 x 2 KB
-    static constexpr int kEpiBytes = 4 * 2 * 2048;
-    static constexpr int kOffBias = kOffEpi + kEpiBytes;         // 4 warps x 256 fp32
-    static constexpr int kBiasBytes = 4 * 256 * 4;
+    static constexpr int kOffEpi = kStages * kStageBytes;        // one 2 KB box per warp
+    static constexpr int kEpiBytes = kEpiWarps * 2048;
+    static constexpr int kOffBias = kOffEpi + kEpiBytes;         // 256 fp32 per warp
+    static constexpr int kBiasBytes = kEpiWarps * 256 * 4;
     static constexpr int kOffBar = kOffBias + kBiasBytes;
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
@@ -398,6 +400,7 @@ __device__ __forceinline__ void publish_partials(const GemmParams& p, uint8_t* s
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;  // which warp of this quarter's pair
     const int row = quarter * 32 + lane;
     int tm, tn;
     tile_coords(w.first, p, tm, tn);
@@ -409,7 +412,14 @@ __device__ __forceinline__ void publish_partials(const GemmParams& p, uint8_t* s
     }
     tcgen05_fence_after_sync();
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    for (int c = 0; c < nchunks; ++c) {
+    // The bias is read after the cluster barrier: start bringing it into L2 now.
+    if (p.epilog != EPI_NONE) {
+        const int nb = (SWAP ? p.bias_layout == 0 : p.bias_layout == 1) ? col_limit : (SWAP ? p.n : p.m);
+        const int idx = (SWAP ? p.bias_layout == 0 : p.bias_layout == 1) ? tn * BN + lane * 8
+                                                                          : tm * kBM + row;
+        if (idx < nb) prefetch_global_l2(static_cast<const uint16_t*>(p.bias) + idx);
+    }
+    for (int c = half; c < nchunks; c += 2) {
         if (c % w.split == w.rank) continue;
         uint32_t r[32];
         __syncwarp();
@@ -435,8 +445,9 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
     constexpr int CH = C::kChunk;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int ew = warp - 2;             // epilogue warp 0..3
+    const int ew = warp - 2;             // epilogue warp 0..7
     const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
+    const int half = ew >> 2;            // the pair's warps take alternate chunks
     const WorkRange w = work_range(p);
     const bool has_bias = p.epilog != EPI_NONE;
     // Bias that varies along the accumulator's columns (staged in shared memory) or along
@@ -447,10 +458,9 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
     const int lane_limit = SWAP ? p.n : p.m;  // extent of the accumulator-lane coordinate
     // This warp's own bias staging area: no other warp reads it, so a __syncwarp orders it.
     float* sbias = reinterpret_cast<float*>(smem + C::kOffBias) + ew * 256;
-    uint8_t* epi_buf = smem + C::kOffEpi + ew * 2 * 2048;
-    const uint32_t epi_buf_u32 = sbase + C::kOffEpi + ew * 2 * 2048;
+    uint8_t* epi_buf = smem + C::kOffEpi + ew * 2048;
+    const uint32_t epi_buf_u32 = sbase + C::kOffEpi + ew * 2048;
     const uint16_t* R = static_cast<const uint16_t*>(p.residual);
-    uint32_t nstore = 0;
     // Bias, residual and the outputs may belong to a programmatic predecessor grid.
     grid_dependency_wait();
 
@@ -486,7 +496,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         const int nchunks = (valid_cols + CH - 1) / CH;
         const bool warp_live = lane_base < lane_limit;
 
-        for (int c = w.rank; c < nchunks; c += w.split) {
+        for (int c = w.rank + half * w.split; c < nchunks; c += 2 * w.split) {
             uint32_t r[32];
             __syncwarp();
             if constexpr (CH == 32)
@@ -498,18 +508,18 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
             for (int j = 0; j < CH; ++j) v[j] = __uint_as_float(r[j]);
             if (w.split > 1) {
                 // Add the other ranks' partial sums of this chunk (distributed shared
-                // memory): four 16-byte units at a time, every peer's loads issued before
+                // memory): two 16-byte units at a time, every peer's loads issued before
                 // any of them is consumed, so their latencies overlap.
                 const int row = quarter * 32 + lane;
 #pragma unroll
-                for (int u0 = 0; u0 < CH / 4; u0 += 4) {
-                    float4 part[7][4];
+                for (int u0 = 0; u0 < CH / 4; u0 += 2) {
+                    float4 part[7][2];
 #pragma unroll
                     for (int pi = 0; pi < 7; ++pi) {
                         if (pi < w.split - 1) {
                             const uint32_t peer = static_cast<uint32_t>(pi < w.rank ? pi : pi + 1);
 #pragma unroll
-                            for (int uu = 0; uu < 4; ++uu)
+                            for (int uu = 0; uu < 2; ++uu)
                                 part[pi][uu] = ld_shared_cluster_v4(map_shared_rank(
                                     sbase + red_offset<BN>(row, c * (CH / 4) + u0 + uu), peer));
                         }
@@ -518,7 +528,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                     for (int pi = 0; pi < 7; ++pi) {
                         if (pi < w.split - 1) {
 #pragma unroll
-                            for (int uu = 0; uu < 4; ++uu) {
+                            for (int uu = 0; uu < 2; ++uu) {
                                 v[4 * (u0 + uu)] += part[pi][uu].x;
                                 v[4 * (u0 + uu) + 1] += part[pi][uu].y;
                                 v[4 * (u0 + uu) + 2] += part[pi][uu].z;
@@ -573,10 +583,9 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                 if (warp_live) {
                     // 32 rows x 32 columns of 16-bit = one 2 KB box, 64-byte rows, stored
                     // with the 64-byte swizzle (16-byte chunk q of row r at q ^ ((r>>1)&3)).
-                    const uint32_t buf = nstore & 1u;
-                    if (lane == 0) bulk_wait_group_read<1>();
+                    if (lane == 0) bulk_wait_group_read<0>();  // this warp's last box is read
                     __syncwarp();
-                    uint8_t* rowp = epi_buf + buf * 2048 + lane * 64;
+                    uint8_t* rowp = epi_buf + lane * 64;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         uint4 w;
@@ -589,10 +598,9 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&p.tm_D, epi_buf_u32 + buf * 2048, col0, lane_base);
+                        tma_store_2d(&p.tm_D, epi_buf_u32, col0, lane_base);
                         bulk_commit_group();
                     }
-                    ++nstore;
                 }
             } else {
                 // ---- columns of D on lanes: thread = one column, CH consecutive rows ----
@@ -619,19 +627,17 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                     // Transpose through shared memory: row j of the box holds D[t0 + j][32
                     // columns of this warp] (64 bytes; lane = column, so each row is written
                     // by one conflict-free warp store), then one TMA store of the box.
-                    const uint32_t buf = nstore & 1u;
-                    if (lane == 0) bulk_wait_group_read<1>();
+                    if (lane == 0) bulk_wait_group_read<0>();  // this warp's last box is read
                     __syncwarp();
-                    uint16_t* tb = reinterpret_cast<uint16_t*>(epi_buf + buf * 2048);
+                    uint16_t* tb = reinterpret_cast<uint16_t*>(epi_buf);
 #pragma unroll
                     for (int j = 0; j < CH; ++j) tb[j * 32 + lane] = to16(v[j], p.bf16);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&p.tm_D, epi_buf_u32 + buf * 2048, lane_base, t0);
+                        tma_store_2d(&p.tm_D, epi_buf_u32, lane_base, t0);
                         bulk_commit_group();
                     }
-                    ++nstore;
                 }
             }
         }
@@ -640,7 +646,9 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
     }
-    if (lane == 0) bulk_wait_group<0>();
+    // Shared memory may be released once the stores have read it; the grid's writes are
+    // complete when the grid is.
+    if (lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
 }
 
@@ -663,6 +671,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     int pre = 0;  // stages the prologue issued (thread 0, which is also the producer)
 
     if (threadIdx.x == 0) {
+        prefetch_tensormap(&p.tm_A);
+        prefetch_tensormap(&p.tm_B);
+        prefetch_tensormap(&p.tm_D);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar0 + 8u * (kBarFull + s), 1);
             mbar_init(bar0 + 8u * (kBarEmpty + s), 1);
@@ -675,9 +686,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         mbar_init(bar0 + 8u * kBarDrain, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tensormap(&p.tm_A);
-        prefetch_tensormap(&p.tm_B);
-        prefetch_tensormap(&p.tm_D);
         pre = producer_prologue<BN, SWAP>(p, sbase, bar0);
     }
     if (warp == 1) {

@@ -55,6 +55,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
+__device__ __forceinline__ void prefetch_global_l2(const void* ptr)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr) : "memory");
+}
+
 // ---- TMA ---------------------------------------------------------------------------------
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map)

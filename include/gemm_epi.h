@@ -40,7 +40,9 @@
  *     residual buffer itself (an in-place residual add).
  *   - All execute calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream) and return launch-time errors only; a device-side wait that ran out
- *     its time limit is reported by gemm_epi_sync_status.
+ *     its time limit is reported by gemm_epi_sync_status.  The fused kernel is launched as
+ *     a programmatic dependent of the stream's previous work: it may start its set-up
+ *     early, but reads and writes device memory only after that work has completed.
  *   - A plan belongs to the device that was current when it was made; execute with that
  *     device current.  Free it only after the work that uses it has completed.  One plan
  *     must not be executed from several host threads at the same time.
@@ -109,8 +111,12 @@ typedef enum {
                                        arrives at, run out the wait limit and report
                                        GEMM_EPI_ERR_DEVICE_TIMEOUT (a test of the timeout
                                        path; no copy or MMA is issued) */
-    GEMM_EPI_OPT_PREFETCH = 7       /* L2 prefetch distance in 64-deep K blocks, 0..64
+    GEMM_EPI_OPT_PREFETCH = 7,      /* L2 prefetch distance in 64-deep K blocks, 0..64
                                        (0 = none) */
+    GEMM_EPI_OPT_PDL = 8            /* 1 (default): launch the fused kernel as a
+                                       programmatic dependent of the previous work on the
+                                       stream (its set-up overlaps that work; every global
+                                       access still waits for it); 0: plain launch */
 } gemm_epi_option;
 
 /*

@@ -316,3 +316,34 @@ def test_l2_prefetch_option_keeps_results(variant):
     p = _inputs(m, n, k, "bf16", "1N", seed=41)
     check(p, m, n, k, "bf16", "RELU_AUX_BIAS", "1N",
           options={"VARIANT": variant, "PREFETCH": 4, "SPLIT_K": 1})
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_programmatic_launch_sees_preceding_writes(variant):
+    # The fused kernel starts as a programmatic dependent of the stream's previous work;
+    # its reads must still see what that work wrote.  Torch kernels rewrite A and the bias
+    # just before the call, and a second call consumes the first call's output.
+    m, n, k = (256 if variant == 1 else 48), 264, 264
+    p = _inputs(m, n, k, "bf16", "1N", seed=51)
+    q = _inputs(m, n, k, "bf16", "1N", seed=52)
+    dev = torch.device("cuda")
+    A, B, bias = p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev)
+    B2 = q["B"][:n, :].contiguous().to(dev) if n <= k else None
+    D1 = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    D2 = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    opts = {"VARIANT": variant}
+    with gemm_epi.Plan(m, n, k, "bf16", "BIAS", "1N", **opts) as p1, \
+            gemm_epi.Plan(m, n, n, "bf16", "GELU_BIAS", "1N", **opts) as p2:
+        for _ in range(3):
+            A.copy_(q["A"].to(dev))          # torch writes A ...
+            bias.copy_(q["bias"].to(dev))    # ... and the bias right before the call
+            p1.execute(A, B, bias, D1)
+            p2.execute(D1, B2, bias, D2)     # reads the previous call's output
+        assert p1.sync_status() == 0 and p2.sync_status() == 0
+    cur = {"A": q["A"], "B": p["B"], "bias": q["bias"]}
+    from parity_helpers import oracle_ref
+    want1, _ = oracle_ref(cur, "bf16", "BIAS", "1N")
+    assert rel_err(D1, want1) <= TOL["bf16"]
+    want2, _ = oracle_ref({"A": D1.cpu(), "B": B2.cpu(), "bias": q["bias"]}, "bf16", "GELU_BIAS",
+                          "1N")
+    assert rel_err(D2, want2) <= TOL["bf16"]
