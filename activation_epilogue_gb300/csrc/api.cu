@@ -41,7 +41,7 @@ EncodeTiledFn encode_fn()
     return g_encode;
 }
 
-enum Variant { kEmpty = 0, kRowTile = 1, kSwapped = 2, kBiasOnly = 3 };
+enum Variant { kEmpty = 0, kRowTile = 1, kSwapped = 2, kBiasOnly = 3, kRowPair = 4 };
 
 constexpr int kSwappedMaxM = 256;
 constexpr unsigned long long kDefaultWaitNs = 2000ull * 1000 * 1000;  // 2 s
@@ -135,11 +135,42 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
     } else if (p->k == 0) {
         p->variant = kBiasOnly;
     } else {
-        int v = p->opt_variant ? p->opt_variant : (p->m <= kSwappedMaxM ? kSwapped : kRowTile);
+        int v = p->opt_variant;
+        if (v == 0) {
+            // small m: swapped; enough 256 x 256 tiles for most CTA pairs: the pair kernel
+            // (half the operand bytes per flop in every SM); else the single-CTA row tiles
+            const long long pair_tiles = ((p->m + 255) / 256) * ((p->n + 255) / 256);
+            if (p->m <= kSwappedMaxM)
+                v = kSwapped;
+            else if (pair_tiles * 10 >= static_cast<long long>(p->sm_count / 2) * 8)
+                v = kRowPair;
+            else
+                v = kRowTile;
+        }
+        if (v == 3) v = kRowPair;  // option value 3 selects the CTA-pair kernel
         if (v == kSwapped && p->m > kSwappedMaxM) return GEMM_EPI_ERR_INVALID_ARG;
         p->variant = v;
         p->k_blocks = static_cast<int>((p->k + 63) / 64);
-        if (v == kRowTile) {
+        if (v == kRowPair) {
+            // CTA pairs on 256 x 256 tiles, persistent, no split
+            p->bn = 256;
+            p->tiles_m = static_cast<int>((p->m + 255) / 256);
+            p->tiles_n = static_cast<int>((p->n + 255) / 256);
+            p->stages = rowpair_stages();
+            p->smem = rowpair_smem_bytes();
+            if (rowpair_prepare() != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
+            const long long tiles = static_cast<long long>(p->tiles_m) * p->tiles_n;
+            long long pairs = rowpair_max_clusters();
+            if (pairs > p->sm_count / 2) pairs = p->sm_count / 2;
+            if (p->opt_grid > 0 && p->opt_grid / 2 < pairs) pairs = p->opt_grid / 2;
+            if (pairs < 1) return GEMM_EPI_ERR_LAUNCH;
+            if (pairs > tiles) pairs = tiles;
+            p->kb_per_split = p->k_blocks;
+            p->grid = static_cast<int>(2 * pairs);
+            int gm = p->opt_group_m ? p->opt_group_m : 8;
+            if (gm > p->tiles_m) gm = p->tiles_m;
+            p->group_m = gm < 1 ? 1 : gm;
+        } else if (v == kRowTile) {
             p->bn = p->opt_bn ? p->opt_bn : pick_rowtile_bn(p->m, p->n, p->k_blocks, p->sm_count);
             p->tiles_m = static_cast<int>((p->m + 127) / 128);
             p->tiles_n = static_cast<int>((p->n + p->bn - 1) / p->bn);
@@ -154,6 +185,9 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             p->stages = swapped_stages(bn);
             p->smem = swapped_smem_bytes(bn);
         }
+    }
+    if (p->variant == kRowTile || p->variant == kSwapped) {
+        const int v = p->variant;
         const long long tiles = static_cast<long long>(p->tiles_m) * p->tiles_n;
         cudaError_t e = v == kRowTile ? rowtile_prepare(p->bn) : swapped_prepare(p->bn);
         if (e != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
@@ -188,16 +222,16 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
         if (gm > p->tiles_m) gm = p->tiles_m;
         p->group_m = gm < 1 ? 1 : gm;
     }
-    static const char* vname[] = {"empty", "row-tile", "swapped", "bias-only"};
+    static const char* vname[] = {"empty", "row-tile", "swapped", "bias-only", "row-pair"};
     static const char* ename[] = {"BIAS", "RELU_BIAS", "GELU_BIAS", "RELU_AUX_BIAS",
                                   "BIAS_RESIDUAL", "NONE"};
     snprintf(p->desc, sizeof(p->desc),
-             "m=%lld n=%lld k=%lld dtype=%s epilog=%s bias=%s variant=%s tile=128x%d bk=64 "
+             "m=%lld n=%lld k=%lld dtype=%s epilog=%s bias=%s variant=%s tile=%dx%d bk=64 "
              "stages=%d smem=%d tiles=%dx%d k_blocks=%d split_k=%d grid=%d group_m=%d sms=%d",
              static_cast<long long>(p->m), static_cast<long long>(p->n),
              static_cast<long long>(p->k), p->dtype == GEMM_EPI_BF16 ? "bf16" : "f16",
              ename[p->epilog], p->bias_layout == GEMM_EPI_BIAS_M1 ? "(m,1)" : "(1,n)",
-             vname[p->variant], p->bn, p->stages, p->smem, p->tiles_m, p->tiles_n, p->k_blocks,
+             vname[p->variant], p->variant == kRowPair ? 256 : 128, p->bn, p->stages, p->smem, p->tiles_m, p->tiles_n, p->k_blocks,
              p->split, p->grid, p->group_m, p->sm_count);
     const char* log = getenv("GEMM_EPI_LOG");
     if (log && log[0] == '1') fprintf(stderr, "[gemm_epi] plan: %s\n", p->desc);
@@ -224,12 +258,13 @@ gemm_epi_status ensure_maps(gemm_epi_plan_s* p, const void* A, const void* B, vo
     p->maps_valid = false;
     const CUtensorMapDataType dt = p->dtype == GEMM_EPI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const uint32_t a_rows = p->variant == kRowTile ? 128u : static_cast<uint32_t>(p->bn);
+    const bool rows_of_a = p->variant == kRowTile || p->variant == kRowPair;
+    const uint32_t a_rows = rows_of_a ? 128u : static_cast<uint32_t>(p->bn);
     if (!encode_2d(&p->tm_A, A, dt, p->k, p->m, 64, a_rows, CU_TENSOR_MAP_SWIZZLE_128B))
         return GEMM_EPI_ERR_LAUNCH;
     if (!encode_2d(&p->tm_B, B, dt, p->n, p->k, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return GEMM_EPI_ERR_LAUNCH;
-    if (p->variant == kRowTile) {
+    if (rows_of_a) {
         if (!encode_2d(&p->tm_D, D, dt, p->n, p->m, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
             return GEMM_EPI_ERR_LAUNCH;
     } else {
@@ -285,8 +320,13 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const void* A, const void* B, co
     prm.split = p->split;
     prm.kb_per_split = p->kb_per_split;
     prm.prefetch = p->prefetch;
-    cudaError_t e = p->variant == kRowTile ? rowtile_launch(p->bn, prm, p->grid, stream, pdl)
-                                           : swapped_launch(p->bn, prm, p->grid, stream, pdl);
+    cudaError_t e;
+    if (p->variant == kRowPair)
+        e = rowpair_launch(prm, p->grid, stream, pdl);
+    else if (p->variant == kRowTile)
+        e = rowtile_launch(p->bn, prm, p->grid, stream, pdl);
+    else
+        e = swapped_launch(p->bn, prm, p->grid, stream, pdl);
     return e == cudaSuccess ? GEMM_EPI_OK : GEMM_EPI_ERR_LAUNCH;
 }
 
@@ -397,7 +437,7 @@ gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt,
     gemm_epi_plan_s saved = *p;
     switch (opt) {
     case GEMM_EPI_OPT_VARIANT:
-        if (value < 0 || value > 2) return GEMM_EPI_ERR_INVALID_ARG;
+        if (value < 0 || value > 3) return GEMM_EPI_ERR_INVALID_ARG;
         p->opt_variant = static_cast<int>(value);
         break;
     case GEMM_EPI_OPT_TILE_N:

@@ -49,10 +49,13 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;   // producer, MMA, epilogue warps
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kPipeBudget = 192 * 1024;
 
-template <int BN>
+// PAIR: a CTA pair computes a 256 x BN tile with cta_group::2 MMAs; each CTA holds 128 rows
+// of A and BN/2 rows (columns of D) of B per stage.
+template <int BN, bool PAIR = false>
 struct TileCfg {
-    static constexpr int kABytes = kBM * kBK * 2;  // MMA-A operand: 128 rows x 64 k
-    static constexpr int kBBytes = BN * kBK * 2;   // MMA-B operand: BN rows x 64 k
+    static constexpr int kBRows = PAIR ? BN / 2 : BN;
+    static constexpr int kABytes = kBM * kBK * 2;      // MMA-A operand: 128 rows x 64 k
+    static constexpr int kBBytes = kBRows * kBK * 2;   // MMA-B operand: kBRows rows x 64 k
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kStagesRaw = kPipeBudget / kStageBytes;
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
@@ -127,19 +130,32 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& 
 struct WorkRange {
     int first, stride, end;  // tiles first, first + stride, ... below end
     int kb_begin, kb_end;    // K blocks [kb_begin, kb_end) of each tile
-    int rank, split;         // cluster rank and size (split == 1: persistent, no cluster)
+    int rank, split;         // split-K: cluster rank and size (split == 1: no split)
+    int pair_rank;           // CTA pairs: 0 = the even CTA (issues the MMAs), 1 = the odd
 };
 
+template <bool PAIR = false>
 __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
 {
     WorkRange w;
-    if (p.split > 1) {
+    if (PAIR) {
+        // persistent CTA pairs (clusters of 2) walking 256-row tiles
+        w.first = static_cast<int>(cluster_id_x());
+        w.stride = static_cast<int>(gridDim.x / 2);
+        w.end = p.tiles_m * p.tiles_n;
+        w.rank = 0;
+        w.split = 1;
+        w.pair_rank = static_cast<int>(cluster_ctarank());
+        w.kb_begin = 0;
+        w.kb_end = p.k_blocks;
+    } else if (p.split > 1) {
         const int tile = static_cast<int>(cluster_id_x());
         w.first = tile;
         w.stride = 1;
         w.end = tile + 1;
         w.rank = static_cast<int>(cluster_ctarank());
         w.split = p.split;
+        w.pair_rank = 0;
         w.kb_begin = w.rank * p.kb_per_split;
         w.kb_end = min(p.k_blocks, w.kb_begin + p.kb_per_split);
     } else {
@@ -148,6 +164,7 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
         w.end = p.tiles_m * p.tiles_n;
         w.rank = 0;
         w.split = 1;
+        w.pair_rank = 0;
         w.kb_begin = 0;
         w.kb_end = p.k_blocks;
     }
@@ -193,16 +210,30 @@ __device__ __forceinline__ uint16_t to16(float a, int bf16)
 // producer: TMA loads
 // ------------------------------------------------------------------------------------------
 // Arm stage `stage` for K block `kb` of tile (tm, tn) and issue its TMA loads.
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, bool PAIR = false>
 __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase, uint32_t bar0,
                                             int stage, int tm, int tn, int kb)
 {
-    using C = TileCfg<BN>;
+    using C = TileCfg<BN, PAIR>;
     const uint32_t fb = bar0 + 8u * (kBarFull + stage);
-    mbar_arrive_expect_tx(fb, C::kStageBytes);
     const uint32_t sa = sbase + stage * C::kStageBytes;
     const uint32_t sb = sa + C::kABytes;
     const int k0 = kb * kBK;
+    if constexpr (PAIR) {
+        // Both CTAs' halves are counted on the even CTA's "full" barrier, which that CTA
+        // arms with the bytes of both (the odd CTA's bytes may land first: the
+        // transaction count is signed).
+        const uint32_t rank = cluster_ctarank();
+        if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::kStageBytes);
+        const uint32_t fb0 = map_shared_rank(fb, 0);
+        tma_load_2d_pair(sa, &p.tm_A, fb0, k0, tm * 2 * kBM + static_cast<int>(rank) * kBM);
+#pragma unroll
+        for (int q = 0; q < BN / 128; ++q)
+            tma_load_2d_pair(sb + q * 8192, &p.tm_B, fb0,
+                             tn * BN + static_cast<int>(rank) * (BN / 2) + q * 64, k0);
+        return;
+    }
+    mbar_arrive_expect_tx(fb, C::kStageBytes);
     if (!SWAP) {
         tma_load_2d(sa, &p.tm_A, fb, k0, tm * kBM);
 #pragma unroll
@@ -253,12 +284,12 @@ __device__ __forceinline__ int producer_prologue(const GemmParams& p, uint32_t s
 }
 
 // The producer loop, continuing after the `pre` stages the prologue issued.
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, bool PAIR = false>
 __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase, uint32_t bar0,
                                              volatile int* abort_flag, int pre)
 {
-    using C = TileCfg<BN>;
-    const WorkRange w = work_range(p);
+    using C = TileCfg<BN, PAIR>;
+    const WorkRange w = work_range<PAIR>(p);
     int stage = pre % C::kStages;
     uint32_t phase = static_cast<uint32_t>((pre / C::kStages) & 1);
     long long issued = pre;
@@ -274,8 +305,8 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
                 ok = false;
                 break;
             }
-            issue_stage<BN, SWAP>(p, sbase, bar0, stage, tm, tn, kb);
-            if (p.prefetch && kb + p.prefetch < w.kb_end)
+            issue_stage<BN, SWAP, PAIR>(p, sbase, bar0, stage, tm, tn, kb);
+            if (!PAIR && p.prefetch && kb + p.prefetch < w.kb_end)
                 prefetch_stage<BN, SWAP>(p, tm, tn, kb + p.prefetch);
             ++issued;
             if (++stage == C::kStages) {
@@ -284,8 +315,9 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
             }
         }
     }
-    if (!ok) {
-        // Let the copies already issued land before the CTA can exit.
+    if (!ok && !(PAIR && w.pair_rank != 0)) {
+        // Let the copies already issued land before the CTA can exit (in a pair, the even
+        // CTA's barriers count both CTAs' copies).
         const long long back = issued < C::kStages ? issued : C::kStages;
         for (long long j = 1; j <= back; ++j) {
             const long long f = issued - j;
@@ -299,16 +331,18 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
 // ------------------------------------------------------------------------------------------
 // MMA issuer
 // ------------------------------------------------------------------------------------------
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, bool PAIR = false>
 __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uint32_t bar0,
                                         uint32_t tmem_base, volatile int* abort_flag)
 {
-    using C = TileCfg<BN>;
+    using C = TileCfg<BN, PAIR>;
     // Row-tile: A operand K-major (rows of A), B operand N-major (rows of B).
     // Swapped:  A operand N-major (rows of B), B operand K-major (rows of A).
+    // Pair: M = 256 across the two CTAs; only the even CTA issues.
     const uint32_t idesc = make_idesc_f16(static_cast<uint32_t>(p.bf16), SWAP ? 1u : 0u,
-                                          SWAP ? 0u : 1u, kBM, BN);
-    const WorkRange w = work_range(p);
+                                          SWAP ? 0u : 1u, PAIR ? 2 * kBM : kBM, BN);
+    const WorkRange w = work_range<PAIR>(p);
+    if (PAIR && w.pair_rank != 0) return;
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -348,23 +382,37 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
                     ad = make_sdesc_sw128(sa + kk * 2048, 8192, 1024);
                     bd = make_sdesc_sw128(sb + kk * 32, 0, 1024);
                 }
-                mma_f16_ss(d_tmem, ad, bd, idesc, (kb > w.kb_begin || kk > 0) ? 1u : 0u);
+                if constexpr (PAIR)
+                    mma_f16_ss_pair(d_tmem, ad, bd, idesc, (kb > w.kb_begin || kk > 0) ? 1u : 0u);
+                else
+                    mma_f16_ss(d_tmem, ad, bd, idesc, (kb > w.kb_begin || kk > 0) ? 1u : 0u);
             }
             issued_any = true;
-            mma_commit(bar0 + 8u * (kBarEmpty + stage));  // stage free once these MMAs finish
+            // stage free (in both CTAs of a pair) once these MMAs finish
+            if constexpr (PAIR)
+                mma_commit_pair(bar0 + 8u * (kBarEmpty + stage), 0x3);
+            else
+                mma_commit(bar0 + 8u * (kBarEmpty + stage));
             if (++stage == C::kStages) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
         if (!ok) break;
-        mma_commit(bar0 + 8u * (kBarTmemFull + acc));  // accumulator ready for the epilogue
+        // accumulator ready for the epilogue (of both CTAs of a pair)
+        if constexpr (PAIR)
+            mma_commit_pair(bar0 + 8u * (kBarTmemFull + acc), 0x3);
+        else
+            mma_commit(bar0 + 8u * (kBarTmemFull + acc));
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
     }
     if (!ok && issued_any) {
         // Wait for every MMA this thread issued before tensor memory is released.
-        mma_commit(bar0 + 8u * kBarDrain);
+        if constexpr (PAIR)
+            mma_commit_pair(bar0 + 8u * kBarDrain, 0x1);
+        else
+            mma_commit(bar0 + 8u * kBarDrain);
         wait_bounded(bar0 + 8u * kBarDrain, 0, abort_flag, kDrainLimitNs, false);
     }
 }
@@ -436,19 +484,19 @@ __device__ __forceinline__ void publish_partials(const GemmParams& p, uint8_t* s
     tcgen05_fence_before_sync();
 }
 
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, bool PAIR = false>
 __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem, uint32_t sbase,
                                              uint32_t bar0, uint32_t tmem_base,
                                              volatile int* abort_flag)
 {
-    using C = TileCfg<BN>;
+    using C = TileCfg<BN, PAIR>;
     constexpr int CH = C::kChunk;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int ew = warp - 2;             // epilogue warp 0..7
     const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
     const int half = ew >> 2;            // the pair's warps take alternate chunks
-    const WorkRange w = work_range(p);
+    const WorkRange w = work_range<PAIR>(p);
     const bool has_bias = p.epilog != EPI_NONE;
     // Bias that varies along the accumulator's columns (staged in shared memory) or along
     // its lanes (one value per thread).
@@ -470,7 +518,9 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         int tm, tn;
         tile_coords(tile, p, tm, tn);
         const int col_base = tn * BN;                          // first accumulator column
-        const int lane_base = tm * kBM + quarter * 32;         // this warp's first lane coord
+        // this warp's first lane coordinate (a pair's odd CTA holds rows 128..255 of the tile)
+        const int lane_base = PAIR ? tm * 2 * kBM + w.pair_rank * kBM + quarter * 32
+                                   : tm * kBM + quarter * 32;
         const int lane_idx = lane_base + lane;
         if (*abort_flag) break;
         if (col_bias) {
@@ -642,7 +692,10 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
             }
         }
         tcgen05_fence_before_sync();
-        mbar_arrive(bar0 + 8u * (kBarTmemEmpty + acc));
+        if constexpr (PAIR)  // the even CTA's MMAs write both CTAs' accumulators
+            mbar_arrive_cluster(map_shared_rank(bar0 + 8u * (kBarTmemEmpty + acc), 0));
+        else
+            mbar_arrive(bar0 + 8u * (kBarTmemEmpty + acc));
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
     }
@@ -655,10 +708,10 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
 // ------------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------------
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_constant__ GemmParams p)
 {
-    using C = TileCfg<BN>;
+    using C = TileCfg<BN, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -680,20 +733,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar0 + 8u * (kBarTmemFull + a), 1);
-            mbar_init(bar0 + 8u * (kBarTmemEmpty + a), kEpiThreads);
+            mbar_init(bar0 + 8u * (kBarTmemEmpty + a), PAIR ? 2 * kEpiThreads : kEpiThreads);
         }
         mbar_init(bar0 + 8u * kBarStall, 1);
         mbar_init(bar0 + 8u * kBarDrain, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        pre = producer_prologue<BN, SWAP>(p, sbase, bar0);
+        // (a pair's first loads wait for both CTAs' barriers, after the cluster barrier)
+        if (!PAIR) pre = producer_prologue<BN, SWAP>(p, sbase, bar0);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
-        tmem_relinquish_alloc_permit();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_holder), C::kTmemCols);
+            tmem_relinquish_alloc_permit_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+            tmem_relinquish_alloc_permit();
+        }
     }
     tcgen05_fence_before_sync();
     __syncthreads();
+    // A pair's CTAs signal each other's barriers: both must be initialised first.
+    if constexpr (PAIR) cluster_sync_all();
     tcgen05_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
     if (threadIdx.x == 0) grid_launch_dependents();
@@ -709,15 +770,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     const bool split = p.split > 1;
     if (!*abort_flag) {
         if (warp == 0) {
-            if (lane == 0) run_producer<BN, SWAP>(p, sbase, bar0, abort_flag, pre);
+            if (lane == 0) run_producer<BN, SWAP, PAIR>(p, sbase, bar0, abort_flag, pre);
             __syncwarp();
         } else if (warp == 1) {
-            if (lane == 0) run_mma<BN, SWAP>(p, sbase, bar0, tmem_base, abort_flag);
+            if (lane == 0) run_mma<BN, SWAP, PAIR>(p, sbase, bar0, tmem_base, abort_flag);
             __syncwarp();
         } else if (split) {
             publish_partials<BN, SWAP>(p, smem, bar0, tmem_base, abort_flag);
         } else {
-            run_epilogue<BN, SWAP>(p, smem, sbase, bar0, tmem_base, abort_flag);
+            run_epilogue<BN, SWAP, PAIR>(p, smem, sbase, bar0, tmem_base, abort_flag);
         }
     }
     if (split) {
@@ -733,9 +794,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
 
     tcgen05_fence_before_sync();
     __syncthreads();
+    // In a pair, neither CTA leaves while the other may still signal its barriers or the
+    // even CTA's MMAs may still write its tensor memory.
+    if constexpr (PAIR) cluster_sync_all();
     if (warp == 1) {
         tcgen05_fence_after_sync();
-        tmem_dealloc(tmem_base, C::kTmemCols);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, C::kTmemCols);
+        else
+            tmem_dealloc(tmem_base, C::kTmemCols);
     }
 }
 

@@ -75,6 +75,13 @@ cudaError_t swapped_launch(int bn, const GemmParams& p, int grid, cudaStream_t s
 int swapped_smem_bytes(int bn);
 int swapped_stages(int bn);
 
+// Row-tile kernel run by CTA pairs (cta_group::2): 256 x 256 tiles, clusters of 2.
+cudaError_t rowpair_prepare();
+cudaError_t rowpair_launch(const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
+int rowpair_smem_bytes();
+int rowpair_stages();
+int rowpair_max_clusters();
+
 // Clusters of `split` CTAs of the kernel that can be resident at once (0 on error).
 int rowtile_max_clusters(int bn, int split);
 int swapped_max_clusters(int bn, int split);

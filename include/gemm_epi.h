@@ -100,7 +100,8 @@ typedef enum {
 
 /* Plan-time settings (gemm_epi_plan_set_option).  0 always means "automatic". */
 typedef enum {
-    GEMM_EPI_OPT_VARIANT = 0,       /* 1 = row-tile kernel, 2 = swapped small-m kernel */
+    GEMM_EPI_OPT_VARIANT = 0,       /* 1 = row-tile kernel, 2 = swapped small-m kernel,
+                                       3 = row-tile kernel run by CTA pairs (256-row tiles) */
     GEMM_EPI_OPT_TILE_N = 1,        /* row-tile kernel: N tile 64, 128 or 256 */
     GEMM_EPI_OPT_SPLIT_K = 2,       /* K slices per output tile, 1..8 (one cluster of that
                                        many CTAs per tile; partial sums added on chip) */

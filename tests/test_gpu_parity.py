@@ -347,3 +347,48 @@ def test_programmatic_launch_sees_preceding_writes(variant):
     want2, _ = oracle_ref({"A": D1.cpu(), "B": B2.cpu(), "bias": q["bias"]}, "bf16", "GELU_BIAS",
                           "1N")
     assert rel_err(D2, want2) <= TOL["bf16"]
+
+
+# ---- the CTA-pair row-tile kernel (cta_group::2, 256 x 256 tiles) -----------------------------
+
+@pytest.mark.parametrize("epilog", EPILOGS)
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_pair_parity(epilog, dtype):
+    m, n, k = 600, 520, 200            # 3 ragged 256-row tiles, 3 ragged 256-column tiles
+    layout = "M1" if EPILOGS.index(epilog) % 2 else "1N"
+    p = _inputs(m, n, k, dtype, layout, seed=61 + EPILOGS.index(epilog))
+    _, _, _, _, desc = check(p, m, n, k, dtype, epilog, layout, options={"VARIANT": 3})
+    assert "variant=row-pair" in desc
+
+
+@pytest.mark.parametrize("grid,group_m", [(2, 1), (4, 2), (6, 8)])
+def test_pair_persistent_walk(grid, group_m):
+    m, n, k = 1280, 768, 520           # 5 x 3 pair tiles, 9 K blocks, few pairs walking them
+    p = _inputs(m, n, k, "bf16", "1N", seed=grid + 70)
+    check(p, m, n, k, "bf16", "RELU_AUX_BIAS", "1N",
+          options={"VARIANT": 3, "GRID": grid, "GROUP_M": group_m})
+
+
+def test_pair_integer_bit_exact():
+    m, n, k = 512, 264, 64
+    p = _inputs(m, n, k, "bf16", "1N", seed=72, kind="int")
+    check(p, m, n, k, "bf16", "RELU_AUX_BIAS", "1N", options={"VARIANT": 3}, exact=True)
+
+
+def test_pair_timeout_path():
+    m, n, k = 512, 256, 128
+    p = _inputs(m, n, k, "bf16", "1N", seed=73)
+    dev = torch.device("cuda")
+    A, B, bias = p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev)
+    D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    with gemm_epi.Plan(m, n, k, "bf16", "BIAS", "1N", variant=3) as plan:
+        plan.set_option("WAIT_LIMIT_US", 20000)
+        plan.set_option("DEBUG_STALL", 1)
+        plan.execute(A, B, bias, D)
+        assert plan.sync_status() == 8
+        plan.set_option("DEBUG_STALL", 0)
+        plan.execute(A, B, bias, D)
+        assert plan.sync_status() == 0
+    from parity_helpers import oracle_ref
+    want, _ = oracle_ref(p, "bf16", "BIAS", "1N")
+    assert rel_err(D, want) <= TOL["bf16"]
