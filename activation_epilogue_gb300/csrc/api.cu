@@ -75,17 +75,11 @@ struct gemm_epi_plan_s {
 
 namespace {
 
-// Split-K factor for a grid of `tiles` output tiles and `k_blocks` K blocks: used only
-// when the tiles fill less than half the SMs; at most 8 (a portable cluster), at least two
-// K blocks per slice, and no empty slice.
-int auto_split(long long tiles, int k_blocks, int sm_count)
-{
-    if (tiles * 2 > sm_count || k_blocks < 4) return 1;
-    long long s = sm_count / tiles;
-    if (s > 8) s = 8;
-    if (s > k_blocks / 2) s = k_blocks / 2;
-    return s < 2 ? 1 : static_cast<int>(s);
-}
+// Split-K is used only when GEMM_EPI_OPT_SPLIT_K asks for it.  Measured on GB300, the
+// cluster launch, the two cluster barriers and the partial-sum exchange cost more than the
+// shorter K loop saves on every under-filled shape tried (1024x512x2048: 15.5 us unsplit vs
+// 19-20 us split; GELU T=16/64/256 x 3072 x 768: 9.2/11.1/16.8 us unsplit vs 10.2/22/28 us
+// with split 4), so a plan does not split by itself.
 
 int normalise_split(int split, int k_blocks, int* kb_per_split)
 {
@@ -98,8 +92,7 @@ int normalise_split(int split, int k_blocks, int* kb_per_split)
 
 // N tile of the row-tile kernel.  When the widest tile already gives every SM a tile, that
 // one (fewest operand bytes per flop).  Otherwise the width whose busiest CTA moves the
-// fewest bytes: its K slices of operand stages, plus, under split-K, its share of the
-// partial-sum exchange.
+// fewest operand bytes (waves of tiles x K blocks x stage bytes).
 int pick_rowtile_bn(int64_t m, int64_t n, int k_blocks, int sm_count)
 {
     const int64_t tm = (m + 127) / 128;
@@ -108,13 +101,8 @@ int pick_rowtile_bn(int64_t m, int64_t n, int k_blocks, int sm_count)
     double best_cost = 1e300;
     for (int bn : {64, 128, 256}) {
         const long long tiles = tm * ((n + bn - 1) / bn);
-        int kpb = 0;
-        const int split = normalise_split(auto_split(tiles, k_blocks, sm_count), k_blocks, &kpb);
-        const long long ctas = tiles * split;
-        const long long waves = (ctas + sm_count - 1) / sm_count;
-        const double stage = 16384.0 + bn * 128.0;
-        const double red = split > 1 ? (split - 1) * 128.0 * bn * 4.0 / split : 0.0;
-        const double cost = waves * (kpb * stage + red);
+        const long long waves = (tiles + sm_count - 1) / sm_count;
+        const double cost = static_cast<double>(waves) * k_blocks * (16384.0 + bn * 128.0);
         if (cost < best_cost) {
             best_cost = cost;
             best = bn;
@@ -191,22 +179,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
         const long long tiles = static_cast<long long>(p->tiles_m) * p->tiles_n;
         cudaError_t e = v == kRowTile ? rowtile_prepare(p->bn) : swapped_prepare(p->bn);
         if (e != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
-        int want_split = p->opt_split_k;
-        if (want_split <= 0) {
-            // the largest automatic split whose clusters are all resident at once
-            want_split = auto_split(tiles, p->k_blocks, p->sm_count);
-            while (want_split > 1) {
-                int kpb = 0;
-                const int s = normalise_split(want_split, p->k_blocks, &kpb);
-                const int fit = v == kRowTile ? rowtile_max_clusters(p->bn, s)
-                                              : swapped_max_clusters(p->bn, s);
-                if (fit >= tiles) {
-                    want_split = s;
-                    break;
-                }
-                --want_split;
-            }
-        }
+        const int want_split = p->opt_split_k > 0 ? p->opt_split_k : 1;
         p->split = normalise_split(want_split, p->k_blocks, &p->kb_per_split);
         long long grid;
         if (p->split > 1) {
@@ -327,7 +300,13 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const void* A, const void* B, co
         e = rowtile_launch(p->bn, prm, p->grid, stream, pdl);
     else
         e = swapped_launch(p->bn, prm, p->grid, stream, pdl);
-    return e == cudaSuccess ? GEMM_EPI_OK : GEMM_EPI_ERR_LAUNCH;
+    if (e != cudaSuccess) {
+        const char* log = getenv("GEMM_EPI_LOG");
+        if (log && log[0] == '1')
+            fprintf(stderr, "[gemm_epi] launch failed: %s (%s)\n", cudaGetErrorString(e), p->desc);
+        return GEMM_EPI_ERR_LAUNCH;
+    }
+    return GEMM_EPI_OK;
 }
 
 gemm_epi_status check_device(const gemm_epi_plan_s* p);

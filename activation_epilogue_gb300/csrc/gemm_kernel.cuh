@@ -525,9 +525,30 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         if (*abort_flag) break;
         if (col_bias) {
             __syncwarp();  // every lane is done reading the previous tile's values
-            for (int i = lane; i < BN; i += 32) {
-                const int c = col_base + i;
-                sbias[i] = c < col_limit ? load_16bit(p.bias, c, p.bf16) : 0.0f;
+            const uint16_t* bsrc = static_cast<const uint16_t*>(p.bias) + col_base;
+            if (col_base + BN <= col_limit && (reinterpret_cast<uintptr_t>(bsrc) & 15) == 0) {
+                // whole tile in range and 16-byte aligned: one 8-element load per lane
+                for (int i8 = lane; i8 < BN / 8; i8 += 32) {
+                    const uint4 w8 = __ldg(reinterpret_cast<const uint4*>(bsrc) + i8);
+                    const uint32_t ww[4] = {w8.x, w8.y, w8.z, w8.w};
+                    float f[8];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const uint16_t lo = static_cast<uint16_t>(ww[h] & 0xFFFFu);
+                        const uint16_t hi = static_cast<uint16_t>(ww[h] >> 16);
+                        f[2 * h] = p.bf16 ? __uint_as_float(static_cast<uint32_t>(lo) << 16)
+                                          : __half2float(__ushort_as_half(lo));
+                        f[2 * h + 1] = p.bf16 ? __uint_as_float(static_cast<uint32_t>(hi) << 16)
+                                              : __half2float(__ushort_as_half(hi));
+                    }
+                    reinterpret_cast<float4*>(sbias)[2 * i8] = make_float4(f[0], f[1], f[2], f[3]);
+                    reinterpret_cast<float4*>(sbias)[2 * i8 + 1] = make_float4(f[4], f[5], f[6], f[7]);
+                }
+            } else {
+                for (int i = lane; i < BN; i += 32) {
+                    const int c = col_base + i;
+                    sbias[i] = c < col_limit ? load_16bit(p.bias, c, p.bf16) : 0.0f;
+                }
             }
             __syncwarp();
         }
@@ -558,18 +579,18 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
             for (int j = 0; j < CH; ++j) v[j] = __uint_as_float(r[j]);
             if (w.split > 1) {
                 // Add the other ranks' partial sums of this chunk (distributed shared
-                // memory): two 16-byte units at a time, every peer's loads issued before
-                // any of them is consumed, so their latencies overlap.
+                // memory): one 16-byte unit at a time, every peer's load issued before any
+                // of them is consumed, so their latencies overlap.
                 const int row = quarter * 32 + lane;
 #pragma unroll
-                for (int u0 = 0; u0 < CH / 4; u0 += 2) {
-                    float4 part[7][2];
+                for (int u0 = 0; u0 < CH / 4; ++u0) {
+                    float4 part[7][1];
 #pragma unroll
                     for (int pi = 0; pi < 7; ++pi) {
                         if (pi < w.split - 1) {
                             const uint32_t peer = static_cast<uint32_t>(pi < w.rank ? pi : pi + 1);
 #pragma unroll
-                            for (int uu = 0; uu < 2; ++uu)
+                            for (int uu = 0; uu < 1; ++uu)
                                 part[pi][uu] = ld_shared_cluster_v4(map_shared_rank(
                                     sbase + red_offset<BN>(row, c * (CH / 4) + u0 + uu), peer));
                         }
@@ -578,7 +599,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                     for (int pi = 0; pi < 7; ++pi) {
                         if (pi < w.split - 1) {
 #pragma unroll
-                            for (int uu = 0; uu < 2; ++uu) {
+                            for (int uu = 0; uu < 1; ++uu) {
                                 v[4 * (u0 + uu)] += part[pi][uu].x;
                                 v[4 * (u0 + uu) + 1] += part[pi][uu].y;
                                 v[4 * (u0 + uu) + 2] += part[pi][uu].z;

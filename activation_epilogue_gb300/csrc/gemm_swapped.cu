@@ -39,27 +39,6 @@ cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t stream, bool 
     cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, gemm_epi_kernel<BN, true>, p);
 }
-template <int BN>
-int max_clusters_one(int split)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(split), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = TileCfg<BN>::kSmemBytes;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_epi_kernel<BN, true>, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    return n;
-}
 }  // namespace
 
 #define GEMM_EPI_SWAPPED_CASES(F) F(16) F(32) F(64) F(128) F(256)
@@ -104,17 +83,5 @@ int swapped_stages(int bn)
     }
 }
 
-
-int swapped_max_clusters(int bn, int split)
-{
-    switch (bn) {
-    case 16: return max_clusters_one<16>(split);
-    case 32: return max_clusters_one<32>(split);
-    case 64: return max_clusters_one<64>(split);
-    case 128: return max_clusters_one<128>(split);
-    case 256: return max_clusters_one<256>(split);
-    default: return 0;
-    }
-}
 
 }  // namespace gemm_epi

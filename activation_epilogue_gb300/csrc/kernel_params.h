@@ -82,9 +82,6 @@ int rowpair_smem_bytes();
 int rowpair_stages();
 int rowpair_max_clusters();
 
-// Clusters of `split` CTAs of the kernel that can be resident at once (0 on error).
-int rowtile_max_clusters(int bn, int split);
-int swapped_max_clusters(int bn, int split);
 
 // Elementwise epilogue over a 16-bit pre-activation (the unfused baseline's second kernel;
 // pre == nullptr means pre = 0, which serves k == 0).

@@ -300,14 +300,13 @@ def test_split_k_integer_bit_exact(variant, split):
                                                              "SPLIT_K": split}, exact=True)
 
 
-def test_small_m_plans_split_k():
+def test_small_m_plans_swapped_without_split():
+    # split-K is measured slower than the unsplit swapped kernel on these shapes
     with gemm_epi.Plan(16, 3072, 768, "bf16", "GELU_BIAS", "1N") as plan:
         desc = plan.describe()
     fields = dict(kv.split("=") for kv in desc.split() if "=" in kv)
     assert fields["variant"] == "swapped", desc
-    # split across a cluster, with every cluster resident at once (one wave)
-    assert int(fields["split_k"]) > 1, desc
-    assert int(fields["grid"]) <= int(fields["sms"]), desc
+    assert fields["split_k"] == "1", desc
 
 
 @pytest.mark.parametrize("variant", [1, 2])
