@@ -197,7 +197,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
     }
     static const char* vname[] = {"empty", "row-tile", "swapped", "bias-only", "row-pair"};
     static const char* ename[] = {"BIAS", "RELU_BIAS", "GELU_BIAS", "RELU_AUX_BIAS",
-                                  "BIAS_RESIDUAL", "NONE"};
+                                  "BIAS_RESIDUAL", "NONE", "TANH_BIAS"};
     snprintf(p->desc, sizeof(p->desc),
              "m=%lld n=%lld k=%lld dtype=%s epilog=%s bias=%s variant=%s tile=%dx%d bk=64 "
              "stages=%d smem=%d tiles=%dx%d k_blocks=%d split_k=%d grid=%d group_m=%d sms=%d",
@@ -358,7 +358,7 @@ gemm_epi_status gemm_epi_plan(gemm_epi_plan_t* out, int64_t m, int64_t n, int64_
     if (!out) return GEMM_EPI_ERR_INVALID_ARG;
     *out = nullptr;
     if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
-    if (epilog < GEMM_EPI_BIAS || epilog > GEMM_EPI_NONE) return GEMM_EPI_ERR_INVALID_ARG;
+    if (epilog < GEMM_EPI_BIAS || epilog > GEMM_EPI_TANH_BIAS) return GEMM_EPI_ERR_INVALID_ARG;
     if (bias_layout != GEMM_EPI_BIAS_M1 && bias_layout != GEMM_EPI_BIAS_1N)
         return GEMM_EPI_ERR_INVALID_ARG;
     const int64_t kMax = (1ll << 31) - 1;

@@ -65,6 +65,8 @@ __global__ void __launch_bounds__(256) elementwise_epilogue_kernel(
                 o = o > 0.0f ? o : 0.0f;
             else if (epilog == EPI_GELU_BIAS)
                 o = gelu_erf_fast(o);
+            else if (epilog == EPI_TANH_BIAS)
+                o = tanh_fast(o);
             const long long idx = static_cast<long long>(row) * n + col;
             if (ok) {
                 if (epilog == EPI_BIAS_RESIDUAL) o += ld16(residual, idx, bf16);

@@ -1,4 +1,6 @@
-// erf-form GELU, x * Phi(x), branch-free in fp32.
+// Activation functions of the epilogues, in fp32.
+//
+// erf-form GELU, x * Phi(x), branch-free.
 //
 // Phi is evaluated with formula 7.1.26 of Abramowitz & Stegun, Handbook of Mathematical
 // Functions (1964): for z >= 0,
@@ -25,6 +27,15 @@ __device__ __forceinline__ float gelu_erf_fast(float x)
     poly *= t;
     const float q = 0.5f * poly * __expf(-z * z);
     return x * (x < 0.0f ? q : 1.0f - q);
+}
+
+// tanh with the hardware approximation (relative error below 2^-10.9), well inside the
+// 16-bit output rounding of a bf16 result and the acceptance bound of an fp16 one.
+__device__ __forceinline__ float tanh_fast(float x)
+{
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 }  // namespace gemm_epi

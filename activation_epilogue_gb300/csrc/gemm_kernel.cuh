@@ -431,6 +431,9 @@ __device__ __forceinline__ void activate(float (&v)[N], int epilog)
     } else if (epilog == EPI_GELU_BIAS) {
 #pragma unroll
         for (int j = 0; j < N; ++j) v[j] = gelu_erf_fast(v[j]);
+    } else if (epilog == EPI_TANH_BIAS) {
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] = tanh_fast(v[j]);
     }
 }
 

@@ -13,7 +13,8 @@ enum Epilog : int {
     EPI_GELU_BIAS = 2,
     EPI_RELU_AUX_BIAS = 3,
     EPI_BIAS_RESIDUAL = 4,
-    EPI_NONE = 5
+    EPI_NONE = 5,
+    EPI_TANH_BIAS = 6
 };
 
 // Device status word values: 0 = fine, else (kCodeTimeout | role).

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(PKG, "libgemmepi.so")
 
 DTYPE = {"f16": 0, "bf16": 1}
 EPILOG = {"BIAS": 0, "RELU_BIAS": 1, "GELU_BIAS": 2, "RELU_AUX_BIAS": 3, "BIAS_RESIDUAL": 4,
-          "NONE": 5}
+          "NONE": 5, "TANH_BIAS": 6}
 BIAS_LAYOUT = {"M1": 0, "1N": 1}
 OPTION = {"VARIANT": 0, "TILE_N": 1, "SPLIT_K": 2, "GRID": 3, "GROUP_M": 4,
           "WAIT_LIMIT_US": 5, "DEBUG_STALL": 6, "PREFETCH": 7, "PDL": 8}

@@ -299,12 +299,8 @@ def run_ours(args, rank, world, local_rank, dist):
     if st != 0:
         raise RuntimeError(f"device status {gemm_epi.status_string(st)}")
 
-    if dist is not None:
-        t = torch.tensor([secs], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        secs = float(t.item())
     flops_step = float(w.flops)
-    value = flops_step * args.steps * world / secs / 1e12
+    secs, value = whole_job(secs, flops_step, args.steps, world, dist, dev)
     kernel_s = secs / args.steps
     if rank != 0:
         plan.free()
@@ -352,6 +348,17 @@ def run_ours(args, rank, world, local_rank, dist):
             "sample": f"{rows} full rows (all {w.n} columns, k={w.k}) of the "
                       f"{w.m}x{w.n}x{w.k} {w.epilog} problem, fp64 oracle, {dt:.1f} s"}
     print(json.dumps(line), flush=True)
+
+
+def whole_job(secs: float, flops_per_step: float, steps: int, world: int, dist, device):
+    """(slowest rank's seconds, whole-job TFLOP/s): every rank ran `steps` steps of its own
+    replica; the job's throughput is all ranks' work over the slowest rank's time."""
+    import torch
+    if dist is not None and world > 1:
+        t = torch.tensor([secs], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        secs = float(t.item())
+    return secs, flops_per_step * steps * world / secs / 1e12
 
 
 def load_traffic(workload: str):

@@ -16,6 +16,7 @@
  *     - paragraph on operational parameters: input, weight and bias share one dtype; the
  *       bias is (m,1) or (1,n), any other shape fails; the plan must be freed;
  *     - paragraph on limitations: RELU_AUX_BIAS also produces the mask backward needs;
+ *       Tanh is one of the predefined epilogs;
  *     - closing paragraph: GELU named as a further epilog.
  *   "nvmath-python: cuBLAS and cuSOLVER bindings for ML linear algebra"
  *   (blog.hotdry.top, 2025-09-19), matmul-planning checklist: plan() chooses the algorithm,
@@ -76,7 +77,9 @@ typedef enum {
     GEMM_EPI_GELU_BIAS = 2,     /* D = GELU(A.B + bias), erf form: x * Phi(x) */
     GEMM_EPI_RELU_AUX_BIAS = 3, /* as RELU_BIAS, and writes the aux mask [pre > 0] */
     GEMM_EPI_BIAS_RESIDUAL = 4, /* D = A.B + bias + residual (FFN second GEMM) */
-    GEMM_EPI_NONE = 5           /* D = A.B (no bias; bias pointer ignored) */
+    GEMM_EPI_NONE = 5,          /* D = A.B (no bias; bias pointer ignored) */
+    GEMM_EPI_TANH_BIAS = 6      /* D = tanh(A.B + bias) (the pages list Tanh among the
+                                   predefined epilogs) */
 } gemm_epi_epilog;
 
 typedef enum {

@@ -35,7 +35,8 @@ _lib = None
 
 DTYPES = {"f16": 0, "bf16": 1}
 EPILOGS = {"BIAS": 0, "RELU_BIAS": 1, "GELU_BIAS": 2, "RELU_AUX_BIAS": 3,
-           "BIAS_RESIDUAL": 4, "NONE": 5}
+           "BIAS_RESIDUAL": 4, "NONE": 5, "TANH_BIAS": 6, "GELU_AUX_BIAS": 7}
+BWD_KINDS = {"DRELU_BGRAD": 0, "DGELU_BGRAD": 1}
 BIAS_LAYOUTS = {"M1": 0, "1N": 1}
 
 
@@ -84,6 +85,10 @@ def _load():
     lib.oracle_aux_pack.argtypes = [vp, i64, i64, vp]
     lib.oracle_ffn.restype = i32
     lib.oracle_ffn.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.oracle_gelu_grad.restype = ctypes.c_double
+    lib.oracle_gelu_grad.argtypes = [ctypes.c_double]
+    lib.oracle_gemm_bwd.restype = i32
+    lib.oracle_gemm_bwd.argtypes = [i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp]
     lib.oracle_num_threads.restype = i32
     lib.oracle_num_threads.argtypes = []
     _lib = lib
@@ -177,3 +182,27 @@ def ffn(X, W1, b1, W2, b2, R, *, dtype: str = "bf16"):
     if rc != 0:
         raise ValueError("oracle_ffn: bad arguments or out of memory")
     return H, Hx, Y
+
+
+def gelu_grad(x: float) -> float:
+    return float(_load().oracle_gelu_grad(float(x)))
+
+
+def gemm_bwd(A, B, *, dtype: str, kind: str, bias_layout: str = "1N", mask=None, pre=None):
+    """(D, dbias) in double for the backward epilogues DRELU_BGRAD (mask: uint32 words
+    [m][ceil(n/32)]) and DGELU_BGRAD (pre: the stored 16-bit pre-activation, m x n)."""
+    A16, B16 = _bits(A), _bits(B)
+    m, k = A16.shape
+    n = B16.shape[1]
+    mk = None
+    if mask is not None:
+        mk = np.ascontiguousarray(mask).view(np.uint32).reshape(m, (n + 31) // 32)
+    pr = None if pre is None else _bits(pre)
+    D = np.empty((m, n), np.float64)
+    dbias = np.empty(m if bias_layout == "M1" else n, np.float64)
+    rc = _load().oracle_gemm_bwd(m, n, k, DTYPES[dtype], BWD_KINDS[kind],
+                                 BIAS_LAYOUTS[bias_layout], _ptr(A16), _ptr(B16), _ptr(mk),
+                                 _ptr(pr), _ptr(D), _ptr(dbias))
+    if rc != 0:
+        raise ValueError("oracle_gemm_bwd: bad arguments or out of memory")
+    return D, dbias

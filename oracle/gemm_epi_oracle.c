@@ -12,7 +12,8 @@
  *     D[m,n] = A[m,k] . B[k,n] + bias, with bias of shape (m,1) (added to every column)
  *     or (1,n) (added to every row); the BIAS / RELU_BIAS epilogs apply the bias and then
  *     the activation inside the matmul kernel; RELU_AUX_BIAS also emits a mask that the
- *     backward pass needs.
+ *     backward pass needs; the limitations paragraph lists Tanh among the predefined
+ *     epilogs (TANH_BIAS: tanh(A.B + bias)).
  *   "Operator fusion in model inference, from LayerNorm to residual connections"
  *   (wmrh.cn/news/429806), section 1 and its flowchart: the FFN chain
  *     matmul -> bias -> GELU -> matmul -> bias, and (section 3) the residual added to the
@@ -27,7 +28,11 @@
  *   - the aux mask bit for (i, j) is [pre(i, j) > 0] (strict), stored as bit (j mod 32) of
  *     32-bit word floor(j / 32) of row i, rows ceil(n / 32) words long, pad bits 0;
  *   - ReLU output is +0 whenever pre <= 0;
- *   - the FFN's hidden activation H is stored as bfloat16 rounded to nearest-even.
+ *   - the FFN's hidden activation H is stored as bfloat16 rounded to nearest-even;
+ *   - GELU_AUX_BIAS keeps the pre-activation for backward (the caller gets it as "pre");
+ *   - the backward epilogues multiply A.B by the ReLU mask (DRELU) or by GELU'(pre) of the
+ *     stored 16-bit pre-activation (DGELU), and reduce the product over the dimension the
+ *     bias was broadcast along to give the bias gradient.
  *
  * Rounding to 16 bits (used only for the FFN's stored H) is written from the IEEE 754
  * definitions of the two formats, with round-to-nearest, ties-to-even.
@@ -35,6 +40,7 @@
  * Build: gcc -O2 -fopenmp -ffp-contract=off -shared -fPIC (no fast-math), so the results
  * are the same on x86-64 and aarch64 hosts.
  */
+#define _GNU_SOURCE
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -51,8 +57,11 @@ enum {
     OR_EPI_GELU_BIAS = 2,
     OR_EPI_RELU_AUX_BIAS = 3,
     OR_EPI_BIAS_RESIDUAL = 4,
-    OR_EPI_NONE = 5
+    OR_EPI_NONE = 5,
+    OR_EPI_TANH_BIAS = 6,
+    OR_EPI_GELU_AUX_BIAS = 7
 };
+enum { OR_BWD_DRELU = 0, OR_BWD_DGELU = 1 };
 enum { OR_BIAS_M1 = 0, OR_BIAS_1N = 1 };
 
 /* ---- 16-bit decode, from the format definitions ------------------------------------- */
@@ -163,7 +172,10 @@ static double activation(int epilog, double pre)
     case OR_EPI_RELU_AUX_BIAS:
         return pre > 0.0 ? pre : 0.0;                /* +0 for every pre <= 0 */
     case OR_EPI_GELU_BIAS:
+    case OR_EPI_GELU_AUX_BIAS:
         return oracle_gelu(pre);
+    case OR_EPI_TANH_BIAS:
+        return tanh(pre);
     default:
         return pre;                                  /* BIAS, BIAS_RESIDUAL, NONE */
     }
@@ -188,7 +200,7 @@ int oracle_gemm_epi(int64_t m, int64_t n, int64_t k, int dtype, int epilog, int 
 {
     if (m < 0 || n < 0 || k < 0 || nrows < 0 || ncols < 0 || !rows || !cols || !D)
         return -1;
-    if (epilog < OR_EPI_BIAS || epilog > OR_EPI_NONE)
+    if (epilog < OR_EPI_BIAS || epilog > OR_EPI_GELU_AUX_BIAS)
         return -1;
     if (epilog != OR_EPI_NONE && !bias)
         return -1;
@@ -306,6 +318,60 @@ out:
     free(cf);
     free(cd);
     free(H);
+    return rc;
+}
+
+/* GELU'(x) = Phi(x) + x phi(x): the derivative of x Phi(x), phi the standard normal density. */
+double oracle_gelu_grad(double x)
+{
+    const double phi = exp(-0.5 * x * x) / sqrt(2.0 * M_PI);
+    return 0.5 * erfc(-x / sqrt(2.0)) + x * phi;
+}
+
+/*
+ * Backward epilogues.  With g(i, j) = bit (j mod 32) of word floor(j/32) of row i of `mask`
+ * (kind DRELU) or g(i, j) = GELU'(pre[i][j]) of the stored 16-bit pre-activation (kind
+ * DGELU):
+ *   dpre[i][j] = (A.B)[i][j] * g(i, j)            (D, m x n doubles)
+ *   dbias[j]   = sum over i of dpre[i][j]         (bias layout (1,n): n doubles)
+ *   dbias[i]   = sum over j of dpre[i][j]         (bias layout (m,1): m doubles)
+ * The products A.B come from oracle_gemm_epi with no epilog.  Returns 0, or -1.
+ */
+int oracle_gemm_bwd(int64_t m, int64_t n, int64_t k, int dtype, int kind, int bias_layout,
+                    const uint16_t* A, const uint16_t* B, const uint32_t* mask,
+                    const uint16_t* pre, double* D, double* dbias)
+{
+    if (m < 0 || n < 0 || k < 0 || !D || !dbias) return -1;
+    if (kind == OR_BWD_DRELU ? !mask : (kind == OR_BWD_DGELU ? !pre : 1)) return -1;
+    int rc = -1;
+    int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)(m > 0 ? m : 1));
+    int64_t* cols = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    if (!rows || !cols) goto out;
+    for (int64_t i = 0; i < m; ++i) rows[i] = i;
+    for (int64_t j = 0; j < n; ++j) cols[j] = j;
+    if (oracle_gemm_epi(m, n, k, dtype, OR_EPI_NONE, bias_layout, A, B, NULL, NULL, rows, m, cols,
+                        n, NULL, D) != 0)
+        goto out;
+    const int64_t ldw = (n + 31) / 32;
+    for (int64_t i = 0; i < m; ++i)
+        for (int64_t j = 0; j < n; ++j) {
+            double g;
+            if (kind == OR_BWD_DRELU)
+                g = (mask[i * ldw + j / 32] >> (j % 32)) & 1u ? 1.0 : 0.0;
+            else
+                g = oracle_gelu_grad(decode(dtype, pre[i * n + j]));
+            D[i * n + j] *= g;
+        }
+    const int64_t nb = bias_layout == OR_BIAS_M1 ? m : n;
+    for (int64_t b = 0; b < nb; ++b)
+        dbias[b] = 0.0;
+    for (int64_t i = 0; i < m; ++i)
+        for (int64_t j = 0; j < n; ++j)
+            dbias[bias_layout == OR_BIAS_M1 ? i : j] += D[i * n + j];
+    rc = 0;
+out:
+    free(rows);
+    free(cols);
     return rc;
 }
 

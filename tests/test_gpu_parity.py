@@ -9,7 +9,7 @@ from parity_helpers import TD, TOL, check, rel_err, run
 
 pytestmark = pytest.mark.gpu
 
-EPILOGS = ["BIAS", "RELU_BIAS", "GELU_BIAS", "RELU_AUX_BIAS", "BIAS_RESIDUAL", "NONE"]
+EPILOGS = ["BIAS", "RELU_BIAS", "GELU_BIAS", "RELU_AUX_BIAS", "BIAS_RESIDUAL", "NONE", "TANH_BIAS"]
 
 
 @pytest.fixture(scope="module", autouse=True)

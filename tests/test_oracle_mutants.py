@@ -28,6 +28,13 @@ MUTANTS = {
     "bf16 exponent bias": ("v = ldexp((double)(frac + 128), expo - 134);",
                            "v = ldexp((double)(frac + 128), expo - 133);"),
     "encode truncates": ("double q = nearbyint(scaled);", "double q = floor(scaled);"),
+    "tanh sign": ("return tanh(pre);", "return tanh(-pre);"),
+    "gelu grad drops density term": ("return 0.5 * erfc(-x / sqrt(2.0)) + x * phi;",
+                                     "return 0.5 * erfc(-x / sqrt(2.0));"),
+    "dbias sums the wrong axis": ("dbias[bias_layout == OR_BIAS_M1 ? i : j] += D[i * n + j];",
+                                  "dbias[bias_layout == OR_BIAS_M1 ? j % nb : i % nb] += D[i * n + j];"),
+    "drelu mask bit order": ("g = (mask[i * ldw + j / 32] >> (j % 32)) & 1u ? 1.0 : 0.0;",
+                             "g = (mask[i * ldw + j / 32] >> (31 - j % 32)) & 1u ? 1.0 : 0.0;"),
     "residual dropped": ("d = p + decode(dtype, residual[i * n + j]);", "d = p;"),
     "k loop drops last term": ("for (int64_t kk = 0; kk < k; ++kk) {\n                const double a",
                                "for (int64_t kk = 0; kk + 1 < k; ++kk) {\n                const double a"),

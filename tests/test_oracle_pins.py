@@ -123,7 +123,7 @@ def test_gelu_closed_forms(oracle):
 
 # ---- the GEMM + epilogue ------------------------------------------------------------------
 
-EPILOGS = ["BIAS", "RELU_BIAS", "GELU_BIAS", "RELU_AUX_BIAS", "BIAS_RESIDUAL", "NONE"]
+EPILOGS = ["BIAS", "RELU_BIAS", "GELU_BIAS", "RELU_AUX_BIAS", "BIAS_RESIDUAL", "NONE", "TANH_BIAS"]
 
 
 def _brute(dtype, epilog, layout, A, B, bias, R):
@@ -148,6 +148,8 @@ def _brute(dtype, epilog, layout, A, B, bias, R):
                 D[i, j] = s if s > 0 else 0.0
             elif epilog == "GELU_BIAS":
                 D[i, j] = s * float(ndtr(s))
+            elif epilog == "TANH_BIAS":
+                D[i, j] = math.tanh(s)
             elif epilog == "BIAS_RESIDUAL":
                 D[i, j] = s + Rd[i, j]
             else:
@@ -190,7 +192,7 @@ def test_medium_shapes_match_numpy_float64_matmul(oracle, epilog, layout):
         pre = pre + (bd[:, None] if layout == "M1" else bd[None, :])
     ref = {"BIAS": pre, "NONE": pre, "RELU_BIAS": np.maximum(pre, 0),
            "RELU_AUX_BIAS": np.maximum(pre, 0), "GELU_BIAS": pre * ndtr(pre),
-           "BIAS_RESIDUAL": pre + Rd}[epilog]
+           "BIAS_RESIDUAL": pre + Rd, "TANH_BIAS": np.tanh(pre)}[epilog]
     D = oracle.gemm_epi(p["A"], p["B"], None if epilog == "NONE" else p["bias"], dtype="bf16",
                         epilog=epilog, bias_layout=layout, residual=p["R"])
     np.testing.assert_allclose(D, ref, rtol=1e-11, atol=1e-12)
@@ -339,3 +341,111 @@ def test_bad_arguments_are_rejected(oracle):
         oracle.gemm_epi(p["A"], p["B"], p["bias"], dtype="bf16", epilog="BIAS_RESIDUAL")
     with pytest.raises(ValueError):
         oracle.gemm_epi(p["A"], p["B"], p["bias"], dtype="bf16", epilog="BIAS", rows=[4])
+
+
+def test_tanh_epilog_closed_forms(oracle):
+    # A = 0: D = tanh(bias); odd symmetry: negating A and the bias negates D.
+    m, n, k = 12, 40, 24
+    p = workloads.random_problem(m, n, k, dtype="bf16", seed=14)
+    bd = _lib_decode("bf16", _bits_np(p["bias"]))
+    D0 = oracle.gemm_epi(torch.zeros_like(p["A"]), p["B"], p["bias"], dtype="bf16",
+                         epilog="TANH_BIAS")
+    # C's tanh and numpy's may differ in the last bit
+    np.testing.assert_allclose(D0, np.broadcast_to(np.tanh(bd)[None, :], (m, n)), rtol=4e-16,
+                               atol=0)
+    D = oracle.gemm_epi(p["A"], p["B"], p["bias"], dtype="bf16", epilog="TANH_BIAS")
+    Dn = oracle.gemm_epi(-p["A"], p["B"], -p["bias"], dtype="bf16", epilog="TANH_BIAS")
+    np.testing.assert_allclose(Dn, -D, rtol=0, atol=1e-15)
+    assert np.all(np.abs(D) < 1.0)
+
+
+# ---- backward epilogues (DRELU_BGRAD, DGELU_BGRAD) -----------------------------------------
+
+def test_gelu_grad_matches_derivative_and_library(oracle):
+    from scipy.special import ndtr
+    from scipy.stats import norm
+    for x in np.linspace(-8, 8, 161):
+        h = 1e-5
+        num = (oracle.gelu(x + h) - oracle.gelu(x - h)) / (2 * h)
+        g = oracle.gelu_grad(x)
+        assert abs(g - num) < 1e-8, x
+        assert abs(g - (ndtr(x) + x * norm.pdf(x))) < 1e-14, x
+    assert oracle.gelu_grad(0.0) == 0.5
+
+
+def _t64(bits16, dtype="bf16"):
+    return torch.from_numpy(_lib_decode(dtype, _bits_np(bits16)))
+
+
+@pytest.mark.parametrize("layout", ["1N", "M1"])
+def test_drelu_bgrad_matches_autograd_of_the_forward_chain(oracle, layout):
+    # forward: pre = X.W1 + b1, H = relu(pre), Y = H.W2; backward from dY:
+    # dpre = (dY.W2^T) * [pre > 0], db1 = sum of dpre over the broadcast dimension
+    t, d, f = 24, 40, 56
+    g = torch.Generator().manual_seed(21)
+    X = torch.randn(t, d, generator=g).to(torch.bfloat16)
+    W1 = (torch.randn(d, f, generator=g) * 0.3).to(torch.bfloat16)
+    b1 = torch.randn(t if layout == "M1" else f, generator=g).to(torch.bfloat16)
+    W2 = (torch.randn(f, d, generator=g) * 0.3).to(torch.bfloat16)
+    dY = torch.randn(t, d, generator=g).to(torch.bfloat16)
+    _, pre = oracle.gemm_epi(X, W1, b1, dtype="bf16", epilog="RELU_AUX_BIAS", bias_layout=layout,
+                             want_pre=True)
+    mask = oracle.aux_pack(pre)
+    W2T = W2.t().contiguous()
+    D, dbias = oracle.gemm_bwd(dY, W2T, dtype="bf16", kind="DRELU_BGRAD", bias_layout=layout,
+                               mask=mask)
+    # the same chain with torch autograd in float64
+    Xd, W1d, W2d, dYd = _t64(X), _t64(W1), _t64(W2), _t64(dY)
+    bd = _t64(b1).requires_grad_(True)
+    pre_t = Xd @ W1d + (bd[:, None] if layout == "M1" else bd[None, :])
+    pre_t.retain_grad()
+    Y = torch.relu(pre_t) @ W2d
+    Y.backward(dYd)
+    np.testing.assert_allclose(D, pre_t.grad.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dbias, bd.grad.numpy(), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("layout", ["1N", "M1"])
+def test_dgelu_bgrad_matches_autograd_on_the_stored_pre(oracle, layout):
+    t, d, f = 20, 32, 48
+    g = torch.Generator().manual_seed(22)
+    pre16 = (torch.randn(t, f, generator=g) * 2).to(torch.bfloat16)   # the stored pre-activation
+    dY = torch.randn(t, d, generator=g).to(torch.bfloat16)
+    W2T = (torch.randn(d, f, generator=g) * 0.3).to(torch.bfloat16)
+    D, dbias = oracle.gemm_bwd(dY, W2T, dtype="bf16", kind="DGELU_BGRAD", bias_layout=layout,
+                               pre=pre16)
+    x = _t64(pre16).requires_grad_(True)
+    h = torch.nn.functional.gelu(x, approximate="none")
+    dH = _t64(dY) @ _t64(W2T)
+    h.backward(dH)
+    np.testing.assert_allclose(D, x.grad.numpy(), rtol=1e-10, atol=1e-12)
+    want_db = x.grad.numpy().sum(axis=1 if layout == "M1" else 0)
+    np.testing.assert_allclose(dbias, want_db, rtol=1e-10, atol=1e-10)
+
+
+def test_drelu_bgrad_brute_force_and_mask_extremes(oracle):
+    rng = np.random.default_rng(4)
+    for (m, n, k) in [(1, 1, 1), (3, 33, 5), (7, 64, 9), (5, 40, 3)]:
+        p = workloads.random_problem(m, n, k, dtype="f16", seed=m * 100 + n)
+        Ad, Bd = _lib_decode("f16", _bits_np(p["A"])), _lib_decode("f16", _bits_np(p["B"]))
+        bits = rng.integers(0, 2, size=(m, n)).astype(bool)
+        padded = np.zeros((m, ((n + 31) // 32) * 32), dtype=bool)
+        padded[:, :n] = bits
+        mask = np.packbits(padded, axis=1, bitorder="little").view("<u4").reshape(m, -1)
+        D, db = oracle.gemm_bwd(p["A"], p["B"], dtype="f16", kind="DRELU_BGRAD", mask=mask)
+        want = np.zeros((m, n))
+        for i in range(m):
+            for j in range(n):
+                s = 0.0
+                for kk in range(k):
+                    s += Ad[i, kk] * Bd[kk, j]
+                want[i, j] = s if bits[i, j] else 0.0
+        np.testing.assert_allclose(D, want, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(db, want.sum(axis=0), rtol=1e-12, atol=1e-12)
+        # all ones: the plain product and its column sums; all zeros: nothing
+        ones = np.full_like(mask, 0xFFFFFFFF)
+        D1, db1 = oracle.gemm_bwd(p["A"], p["B"], dtype="f16", kind="DRELU_BGRAD", mask=ones)
+        np.testing.assert_allclose(D1, Ad @ Bd, rtol=1e-12, atol=1e-12)
+        D0, db0 = oracle.gemm_bwd(p["A"], p["B"], dtype="f16", kind="DRELU_BGRAD",
+                                  mask=np.zeros_like(mask))
+        assert not D0.any() and not db0.any()
