@@ -196,8 +196,10 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
         p->group_m = gm < 1 ? 1 : gm;
     }
     static const char* vname[] = {"empty", "row-tile", "swapped", "bias-only", "row-pair"};
-    static const char* ename[] = {"BIAS", "RELU_BIAS", "GELU_BIAS", "RELU_AUX_BIAS",
-                                  "BIAS_RESIDUAL", "NONE", "TANH_BIAS"};
+    static const char* ename[] = {"BIAS",          "RELU_BIAS",     "GELU_BIAS",
+                                  "RELU_AUX_BIAS", "BIAS_RESIDUAL", "NONE",
+                                  "TANH_BIAS",     "GELU_AUX_BIAS", "DRELU_BGRAD",
+                                  "DGELU_BGRAD"};
     snprintf(p->desc, sizeof(p->desc),
              "m=%lld n=%lld k=%lld dtype=%s epilog=%s bias=%s variant=%s tile=%dx%d bk=64 "
              "stages=%d smem=%d tiles=%dx%d k_blocks=%d split_k=%d grid=%d group_m=%d sms=%d",
@@ -261,21 +263,22 @@ gemm_epi_status check_device(const gemm_epi_plan_s* p)
     return GEMM_EPI_OK;
 }
 
-gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const void* A, const void* B, const void* bias,
-                            const void* residual, void* D, uint32_t* aux, int epilog,
+gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, int epilog,
                             cudaStream_t stream, bool pdl = false)
 {
-    gemm_epi_status st = ensure_maps(p, A, B, D);
+    gemm_epi_status st = ensure_maps(p, ops.A, ops.B, ops.D);
     if (st != GEMM_EPI_OK) return st;
     GemmParams prm;
     memset(&prm, 0, sizeof(prm));
     prm.tm_A = p->tm_A;
     prm.tm_B = p->tm_B;
     prm.tm_D = p->tm_D;
-    prm.bias = bias;
-    prm.residual = residual;
-    prm.D = D;
-    prm.aux = aux;
+    prm.bias = ops.bias;
+    prm.residual = ops.residual;
+    prm.D = ops.D;
+    prm.aux = ops.aux;
+    prm.aux_in = ops.aux_in;
+    prm.dbias = ops.dbias;
     prm.status = p->d_status;
     prm.wait_limit_ns = p->wait_limit_ns;
     prm.m = static_cast<int>(p->m);
@@ -311,40 +314,82 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const void* A, const void* B, co
 
 gemm_epi_status check_device(const gemm_epi_plan_s* p);
 
-// One fused call on an already-checked plan: empty problems launch nothing, k == 0 runs the
-// elementwise epilogue on the bias alone, everything else the GEMM kernel.
-gemm_epi_status run_plan(gemm_epi_plan_s* p, const void* A, const void* B, const void* bias,
-                         const void* residual, void* D, uint32_t* aux, cudaStream_t stream,
-                         bool pdl)
+bool backward(int epilog) { return epilog == GEMM_EPI_DRELU_BGRAD || epilog == GEMM_EPI_DGELU_BGRAD; }
+
+int64_t dbias_len(const gemm_epi_plan_s* p) { return p->bias_layout == GEMM_EPI_BIAS_M1 ? p->m : p->n; }
+
+// Backward calls: dbias is accumulated atomically, so it starts from zero on the stream.
+gemm_epi_status zero_dbias(const gemm_epi_plan_s* p, const gemm_epi_operands& ops,
+                           cudaStream_t stream)
 {
-    if (p->variant == kEmpty) return GEMM_EPI_OK;
-    if (p->variant == kBiasOnly) {
-        cudaError_t e = elementwise_launch(nullptr, bias, residual, D, aux, static_cast<int>(p->m),
-                                           static_cast<int>(p->n), p->epilog, p->bias_layout,
-                                           p->dtype == GEMM_EPI_BF16 ? 1 : 0,
-                                           static_cast<int>((p->n + 31) / 32), p->sm_count, stream);
-        return e == cudaSuccess ? GEMM_EPI_OK : GEMM_EPI_ERR_LAUNCH;
-    }
-    return launch_gemm(p, A, B, bias, residual, D, aux, p->epilog, stream, pdl && !p->no_pdl);
+    if (!backward(p->epilog) || dbias_len(p) == 0) return GEMM_EPI_OK;
+    return cudaMemsetAsync(ops.dbias, 0, sizeof(float) * static_cast<size_t>(dbias_len(p)),
+                           stream) == cudaSuccess
+               ? GEMM_EPI_OK
+               : GEMM_EPI_ERR_LAUNCH;
 }
 
-gemm_epi_status check_operands(const gemm_epi_plan_s* p, const void* A, const void* B,
-                               const void* bias, const void* residual, const void* D,
-                               const uint32_t* aux)
+cudaError_t run_elementwise(const gemm_epi_plan_s* p, const void* pre,
+                            const gemm_epi_operands& ops, cudaStream_t stream)
 {
-    const bool needs_res = p->epilog == GEMM_EPI_BIAS_RESIDUAL;
-    const bool needs_aux = p->epilog == GEMM_EPI_RELU_AUX_BIAS;
-    if ((aux != nullptr) != needs_aux) return GEMM_EPI_ERR_INVALID_ARG;
-    if ((residual != nullptr) != needs_res) return GEMM_EPI_ERR_INVALID_ARG;
+    return elementwise_launch(pre, ops.bias, ops.residual, ops.D, ops.aux, ops.aux_in, ops.dbias,
+                              static_cast<int>(p->m), static_cast<int>(p->n), p->epilog,
+                              p->bias_layout, p->dtype == GEMM_EPI_BF16 ? 1 : 0,
+                              static_cast<int>((p->n + 31) / 32), p->sm_count, stream);
+}
+
+// One fused call on an already-checked plan: empty problems launch nothing, k == 0 runs the
+// elementwise epilogue on the bias alone, everything else the GEMM kernel.
+gemm_epi_status run_plan(gemm_epi_plan_s* p, const gemm_epi_operands& ops, cudaStream_t stream,
+                         bool pdl)
+{
+    gemm_epi_status st = zero_dbias(p, ops, stream);
+    if (st != GEMM_EPI_OK || p->variant == kEmpty) return st;
+    if (p->variant == kBiasOnly)
+        return run_elementwise(p, nullptr, ops, stream) == cudaSuccess ? GEMM_EPI_OK
+                                                                        : GEMM_EPI_ERR_LAUNCH;
+    // (a backward launch follows the memset of dbias: plain stream order)
+    return launch_gemm(p, ops, p->epilog, stream, pdl && !p->no_pdl && !backward(p->epilog));
+}
+
+gemm_epi_status check_operands(const gemm_epi_plan_s* p, const gemm_epi_operands& o)
+{
+    const int e = p->epilog;
+    const bool bwd = backward(e);
+    if (bwd && o.bias) return GEMM_EPI_ERR_INVALID_ARG;
+    if (bwd && dbias_len(p) > 0 && !o.dbias) return GEMM_EPI_ERR_INVALID_ARG;
+    if (o.dbias && !aligned(o.dbias, 4)) return GEMM_EPI_ERR_MISALIGNED;
+    // An empty problem touches no operand but dbias (its matrices may have no storage).
     if (p->variant == kEmpty) return GEMM_EPI_OK;
-    if (!D) return GEMM_EPI_ERR_INVALID_ARG;
-    if (p->k > 0 && (!A || !B)) return GEMM_EPI_ERR_INVALID_ARG;
-    if (p->epilog != GEMM_EPI_NONE && !bias) return GEMM_EPI_ERR_INVALID_ARG;
-    if (!aligned(D, 16) || (A && !aligned(A, 16)) || (B && !aligned(B, 16)) ||
-        (residual && !aligned(residual, 16)) || (bias && !aligned(bias, 2)) ||
-        (aux && !aligned(aux, 4)))
+    const bool needs_res = e == GEMM_EPI_BIAS_RESIDUAL;
+    const bool needs_aux = e == GEMM_EPI_RELU_AUX_BIAS || e == GEMM_EPI_GELU_AUX_BIAS;
+    if ((o.aux != nullptr) != needs_aux) return GEMM_EPI_ERR_INVALID_ARG;
+    if ((o.residual != nullptr) != needs_res) return GEMM_EPI_ERR_INVALID_ARG;
+    if ((o.aux_in != nullptr) != bwd || (o.dbias != nullptr) != bwd) return GEMM_EPI_ERR_INVALID_ARG;
+    if (!o.D) return GEMM_EPI_ERR_INVALID_ARG;
+    if (p->k > 0 && (!o.A || !o.B)) return GEMM_EPI_ERR_INVALID_ARG;
+    if (e != GEMM_EPI_NONE && !bwd && !o.bias) return GEMM_EPI_ERR_INVALID_ARG;
+    const uintptr_t aux_align = e == GEMM_EPI_GELU_AUX_BIAS ? 16 : 4;
+    const uintptr_t aux_in_align = e == GEMM_EPI_DGELU_BGRAD ? 16 : 4;
+    if (!aligned(o.D, 16) || (o.A && !aligned(o.A, 16)) || (o.B && !aligned(o.B, 16)) ||
+        (o.residual && !aligned(o.residual, 16)) || (o.bias && !aligned(o.bias, 2)) ||
+        (o.aux && !aligned(o.aux, aux_align)) || (o.aux_in && !aligned(o.aux_in, aux_in_align)))
         return GEMM_EPI_ERR_MISALIGNED;
     return GEMM_EPI_OK;
+}
+
+gemm_epi_operands make_operands(const void* A, const void* B, const void* bias,
+                                const void* residual, void* D, void* aux)
+{
+    gemm_epi_operands o;
+    memset(&o, 0, sizeof(o));
+    o.A = A;
+    o.B = B;
+    o.bias = bias;
+    o.residual = residual;
+    o.D = D;
+    o.aux = aux;
+    return o;
 }
 
 }  // namespace
@@ -358,7 +403,7 @@ gemm_epi_status gemm_epi_plan(gemm_epi_plan_t* out, int64_t m, int64_t n, int64_
     if (!out) return GEMM_EPI_ERR_INVALID_ARG;
     *out = nullptr;
     if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
-    if (epilog < GEMM_EPI_BIAS || epilog > GEMM_EPI_TANH_BIAS) return GEMM_EPI_ERR_INVALID_ARG;
+    if (epilog < GEMM_EPI_BIAS || epilog > GEMM_EPI_DGELU_BGRAD) return GEMM_EPI_ERR_INVALID_ARG;
     if (bias_layout != GEMM_EPI_BIAS_M1 && bias_layout != GEMM_EPI_BIAS_1N)
         return GEMM_EPI_ERR_INVALID_ARG;
     const int64_t kMax = (1ll << 31) - 1;
@@ -463,20 +508,27 @@ gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt,
     return st;
 }
 
+gemm_epi_status gemm_epi_execute_operands(gemm_epi_plan_t p, const gemm_epi_operands* ops,
+                                          cudaStream_t stream)
+{
+    if (!p || !ops) return GEMM_EPI_ERR_INVALID_ARG;
+    gemm_epi_status st = check_operands(p, *ops);
+    if (st != GEMM_EPI_OK) return st;
+    if (p->variant == kEmpty && (!backward(p->epilog) || dbias_len(p) == 0)) return GEMM_EPI_OK;
+    st = check_device(p);
+    if (st != GEMM_EPI_OK) return st;
+    // Every global access of the fused kernel waits for the previous grid on the stream
+    // (griddepcontrol.wait), so it is launched as a programmatic dependent: its launch and
+    // set-up overlap the tail of whatever runs before it.
+    return run_plan(p, *ops, stream, true);
+}
+
 gemm_epi_status gemm_epi_execute_ex(gemm_epi_plan_t p, const void* A, const void* B,
                                     const void* bias, const void* residual, void* D,
                                     uint32_t* aux, cudaStream_t stream)
 {
-    if (!p) return GEMM_EPI_ERR_INVALID_ARG;
-    gemm_epi_status st = check_operands(p, A, B, bias, residual, D, aux);
-    if (st != GEMM_EPI_OK) return st;
-    if (p->variant == kEmpty) return GEMM_EPI_OK;
-    st = check_device(p);
-    if (st != GEMM_EPI_OK) return st;
-    // Every global access of the fused kernel waits for the previous grid on the stream
-    // (griddepcontrol.wait), so it is always launched as a programmatic dependent: its
-    // launch and set-up overlap the tail of whatever runs before it.
-    return run_plan(p, A, B, bias, residual, D, aux, stream, true);
+    const gemm_epi_operands o = make_operands(A, B, bias, residual, D, aux);
+    return gemm_epi_execute_operands(p, &o, stream);
 }
 
 gemm_epi_status gemm_epi_execute(gemm_epi_plan_t p, const void* A, const void* B,
@@ -486,30 +538,40 @@ gemm_epi_status gemm_epi_execute(gemm_epi_plan_t p, const void* A, const void* B
     return gemm_epi_execute_ex(p, A, B, bias, nullptr, D, aux, stream);
 }
 
+gemm_epi_status gemm_epi_execute_operands_unfused(gemm_epi_plan_t p,
+                                                  const gemm_epi_operands* ops, void* pre,
+                                                  cudaStream_t stream)
+{
+    if (!p || !ops) return GEMM_EPI_ERR_INVALID_ARG;
+    gemm_epi_status st = check_operands(p, *ops);
+    if (st != GEMM_EPI_OK) return st;
+    if (p->variant != kEmpty) {
+        if (!pre) return GEMM_EPI_ERR_INVALID_ARG;
+        if (!aligned(pre, 16)) return GEMM_EPI_ERR_MISALIGNED;
+    } else if (!backward(p->epilog) || dbias_len(p) == 0) {
+        return GEMM_EPI_OK;
+    }
+    st = check_device(p);
+    if (st != GEMM_EPI_OK) return st;
+    st = zero_dbias(p, *ops, stream);
+    if (st != GEMM_EPI_OK || p->variant == kEmpty) return st;
+    const void* pre_in = nullptr;
+    if (p->variant != kBiasOnly) {
+        const gemm_epi_operands g = make_operands(ops->A, ops->B, nullptr, nullptr, pre, nullptr);
+        st = launch_gemm(p, g, EPI_NONE, stream);
+        if (st != GEMM_EPI_OK) return st;
+        pre_in = pre;
+    }
+    return run_elementwise(p, pre_in, *ops, stream) == cudaSuccess ? GEMM_EPI_OK
+                                                                   : GEMM_EPI_ERR_LAUNCH;
+}
+
 gemm_epi_status gemm_epi_execute_unfused(gemm_epi_plan_t p, const void* A, const void* B,
                                          const void* bias, const void* residual, void* pre,
                                          void* D, uint32_t* aux, cudaStream_t stream)
 {
-    if (!p) return GEMM_EPI_ERR_INVALID_ARG;
-    gemm_epi_status st = check_operands(p, A, B, bias, residual, D, aux);
-    if (st != GEMM_EPI_OK) return st;
-    if (p->variant == kEmpty) return GEMM_EPI_OK;
-    if (!pre) return GEMM_EPI_ERR_INVALID_ARG;
-    if (!aligned(pre, 16)) return GEMM_EPI_ERR_MISALIGNED;
-    st = check_device(p);
-    if (st != GEMM_EPI_OK) return st;
-    const int bf16 = p->dtype == GEMM_EPI_BF16 ? 1 : 0;
-    const int aux_ld = static_cast<int>((p->n + 31) / 32);
-    const void* pre_in = nullptr;
-    if (p->variant != kBiasOnly) {
-        st = launch_gemm(p, A, B, nullptr, nullptr, pre, nullptr, EPI_NONE, stream);
-        if (st != GEMM_EPI_OK) return st;
-        pre_in = pre;
-    }
-    cudaError_t e = elementwise_launch(pre_in, bias, residual, D, aux, static_cast<int>(p->m),
-                                       static_cast<int>(p->n), p->epilog, p->bias_layout, bf16,
-                                       aux_ld, p->sm_count, stream);
-    return e == cudaSuccess ? GEMM_EPI_OK : GEMM_EPI_ERR_LAUNCH;
+    const gemm_epi_operands o = make_operands(A, B, bias, residual, D, aux);
+    return gemm_epi_execute_operands_unfused(p, &o, pre, stream);
 }
 
 gemm_epi_status gemm_epi_free(gemm_epi_plan_t p)
@@ -611,17 +673,19 @@ gemm_epi_status gemm_epi_ffn_execute(gemm_epi_ffn_plan_t p, const void* X, const
                                      const void* R, void* Y, cudaStream_t stream)
 {
     if (!p) return GEMM_EPI_ERR_INVALID_ARG;
-    gemm_epi_status st = check_operands(p->g1, X, W1, b1, nullptr, p->H ? p->H : Y, nullptr);
+    const gemm_epi_operands o1 = make_operands(X, W1, b1, nullptr, p->H ? p->H : Y, nullptr);
+    const gemm_epi_operands o2 = make_operands(p->H, W2, b2, R, Y, nullptr);
+    gemm_epi_status st = check_operands(p->g1, o1);
     if (st != GEMM_EPI_OK) return st;
-    st = check_operands(p->g2, p->H, W2, b2, R, Y, nullptr);
+    st = check_operands(p->g2, o2);
     if (st != GEMM_EPI_OK) return st;
     if (p->t == 0 || p->d == 0) return GEMM_EPI_OK;
     st = check_device(p->g1);
     if (st != GEMM_EPI_OK) return st;
-    st = run_plan(p->g1, X, W1, b1, nullptr, p->H, nullptr, stream, true);
+    st = run_plan(p->g1, o1, stream, true);
     if (st != GEMM_EPI_OK) return st;
     // GEMM 2 reads H only after GEMM 1 has completed (griddepcontrol.wait in its producer).
-    return run_plan(p->g2, p->H, W2, b2, R, Y, nullptr, stream, p->g1->variant != kEmpty);
+    return run_plan(p->g2, o2, stream, p->g1->variant != kEmpty);
 }
 
 const void* gemm_epi_ffn_hidden(gemm_epi_ffn_plan_t p) { return p ? p->H : nullptr; }
@@ -745,12 +809,14 @@ extern "C" gemm_epi_status gemm_epi_ffn_execute_noalloc(int64_t t, int64_t d, in
     if (st != GEMM_EPI_OK) return st;
     st = stack_plan(&g2, t, d, f, dtype, GEMM_EPI_BIAS_RESIDUAL, dev, sms, status + 1);
     if (st != GEMM_EPI_OK) return st;
-    st = check_operands(&g1, X, W1, b1, nullptr, H, nullptr);
+    const gemm_epi_operands o1 = make_operands(X, W1, b1, nullptr, H, nullptr);
+    const gemm_epi_operands o2 = make_operands(H, W2, b2, R, Y, nullptr);
+    st = check_operands(&g1, o1);
     if (st != GEMM_EPI_OK) return st;
-    st = check_operands(&g2, H, W2, b2, R, Y, nullptr);
+    st = check_operands(&g2, o2);
     if (st != GEMM_EPI_OK) return st;
     if (t == 0 || d == 0) return GEMM_EPI_OK;
-    st = run_plan(&g1, X, W1, b1, nullptr, H, nullptr, stream, false);
+    st = run_plan(&g1, o1, stream, false);
     if (st != GEMM_EPI_OK) return st;
-    return run_plan(&g2, H, W2, b2, R, Y, nullptr, stream, g1.variant != kEmpty);
+    return run_plan(&g2, o2, stream, g1.variant != kEmpty);
 }

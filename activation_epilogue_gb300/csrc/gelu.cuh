@@ -29,6 +29,23 @@ __device__ __forceinline__ float gelu_erf_fast(float x)
     return x * (x < 0.0f ? q : 1.0f - q);
 }
 
+// GELU'(x) = Phi(x) + x phi(x), phi(x) = exp(-x^2/2) / sqrt(2 pi): the same tail q =
+// Phi(-|x|) (formula 7.1.26), and the density from the exponential it already computes.
+__device__ __forceinline__ float gelu_grad_fast(float x)
+{
+    const float z = fabsf(x) * 0.70710678118654752f;
+    const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
+    float poly = fmaf(t, 1.061405429f, -1.453152027f);
+    poly = fmaf(poly, t, 1.421413741f);
+    poly = fmaf(poly, t, -0.284496736f);
+    poly = fmaf(poly, t, 0.254829592f);
+    poly *= t;
+    const float e = __expf(-z * z);  // exp(-x^2 / 2)
+    const float q = 0.5f * poly * e;
+    const float phi_cdf = x < 0.0f ? q : 1.0f - q;
+    return fmaf(x * e, 0.39894228040143268f, phi_cdf);
+}
+
 // tanh with the hardware approximation (relative error below 2^-10.9), well inside the
 // 16-bit output rounding of a bf16 result and the acceptance bound of an fp16 one.
 __device__ __forceinline__ float tanh_fast(float x)

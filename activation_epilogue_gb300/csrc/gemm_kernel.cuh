@@ -20,6 +20,12 @@
 //               shared-memory box and a TMA store.  While it drains one accumulator the
 //               MMA warp fills the other, so the epilogue overlaps the next tile's GEMM.
 //
+// Backward epilogues (DRELU_BGRAD, DGELU_BGRAD): the accumulator is multiplied by the
+// stored ReLU mask bit or by GELU' of the stored pre-activation, written as D, and reduced
+// on chip into the bias gradient: sums along a thread's own row of the chunk stay in
+// registers until the tile is done, sums across the 32 lanes of a warp come from one
+// transpose-and-add butterfly; either way one fp32 atomic per warp and bias entry per tile.
+//
 // Split-K (small grids): the CTAs of a cluster share one output tile, each accumulating a
 // slice of K in its own TMEM.  The tile's 32-column chunks are owned round-robin by the
 // cluster ranks; every CTA writes the partial sums of the chunks it does not own into its
@@ -187,6 +193,12 @@ __device__ __forceinline__ float load_16bit(const void* base, long long idx, int
     const uint16_t h = static_cast<const uint16_t*>(base)[idx];
     if (bf16) return __uint_as_float(static_cast<uint32_t>(h) << 16);
     return __half2float(__ushort_as_half(h));
+}
+
+__device__ __forceinline__ float decode16(uint32_t h, int bf16)
+{
+    if (bf16) return __uint_as_float(h << 16);
+    return __half2float(__ushort_as_half(static_cast<uint16_t>(h)));
 }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, int bf16)
@@ -428,12 +440,90 @@ __device__ __forceinline__ void activate(float (&v)[N], int epilog)
     if (epilog == EPI_RELU_BIAS || epilog == EPI_RELU_AUX_BIAS) {
 #pragma unroll
         for (int j = 0; j < N; ++j) v[j] = v[j] > 0.0f ? v[j] : 0.0f;
-    } else if (epilog == EPI_GELU_BIAS) {
+    } else if (epilog == EPI_GELU_BIAS || epilog == EPI_GELU_AUX_BIAS) {
 #pragma unroll
         for (int j = 0; j < N; ++j) v[j] = gelu_erf_fast(v[j]);
     } else if (epilog == EPI_TANH_BIAS) {
 #pragma unroll
         for (int j = 0; j < N; ++j) v[j] = tanh_fast(v[j]);
+    }
+}
+
+// Sums over the 32 lanes of a warp of each of 32 columns: on entry lane l holds x[j], the
+// element (l, j) of a 32 x 32 block; on return lane l holds the sum of column l.  Each of
+// five rounds halves the columns a lane keeps and adds its partner's half of them
+// (16 + 8 + 4 + 2 + 1 = 31 shuffles, against 32 x 5 for 32 separate warp reductions).
+__device__ __forceinline__ float warp_column_sums(float (&x)[32], int lane)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+            const float send = upper ? x[i] : x[i + o];
+            const float keep = upper ? x[i + o] : x[i];
+            x[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+        }
+    }
+    return x[0];
+}
+
+// Row-tile backward factor: v[j] (row `row`, column col0 + j) times the ReLU mask bit or
+// GELU' of the stored pre-activation; 0 outside the matrix.
+__device__ __forceinline__ void backward_factor_row(const GemmParams& p, float (&v)[32], int row,
+                                                    int col0)
+{
+    const int valid = row < p.m ? min(32, p.n - col0) : 0;
+    if (p.epilog == EPI_DRELU_BGRAD) {
+        uint32_t mw = 0;
+        if (valid > 0)
+            mw = __ldg(static_cast<const uint32_t*>(p.aux_in) + static_cast<long long>(row) * p.aux_ld +
+                       col0 / 32);
+        if (valid < 32) mw &= (1u << valid) - 1u;  // valid == 0 clears every bit
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = ((mw >> j) & 1u) ? v[j] : 0.0f;
+        return;
+    }
+    const uint16_t* src = static_cast<const uint16_t*>(p.aux_in) + static_cast<long long>(row) * p.n + col0;
+    if (valid == 32) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 w = __ldg(reinterpret_cast<const uint4*>(src) + q);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                v[8 * q + 2 * h] *= gelu_grad_fast(decode16(ww[h] & 0xFFFFu, p.bf16));
+                v[8 * q + 2 * h + 1] *= gelu_grad_fast(decode16(ww[h] >> 16, p.bf16));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            v[j] = j < valid ? v[j] * gelu_grad_fast(decode16(src[j], p.bf16)) : 0.0f;
+    }
+}
+
+// Row-tile GELU_AUX_BIAS: the 32 pre-activation values of one row, rounded to 16 bits.
+__device__ __forceinline__ void store_pre_row(const GemmParams& p, const float (&v)[32], int row,
+                                              int col0)
+{
+    if (row >= p.m) return;
+    uint16_t* dst = static_cast<uint16_t*>(p.aux) + static_cast<long long>(row) * p.n + col0;
+    const int valid = min(32, p.n - col0);
+    if (valid == 32) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack2(v[8 * q + 0], v[8 * q + 1], p.bf16);
+            w.y = pack2(v[8 * q + 2], v[8 * q + 3], p.bf16);
+            w.z = pack2(v[8 * q + 4], v[8 * q + 5], p.bf16);
+            w.w = pack2(v[8 * q + 6], v[8 * q + 7], p.bf16);
+            reinterpret_cast<uint4*>(dst)[q] = w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < valid) dst[j] = to16(v[j], p.bf16);
     }
 }
 
@@ -500,10 +590,12 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
     const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
     const int half = ew >> 2;            // the pair's warps take alternate chunks
     const WorkRange w = work_range<PAIR>(p);
-    const bool has_bias = p.epilog != EPI_NONE;
-    // Bias that varies along the accumulator's columns (staged in shared memory) or along
-    // its lanes (one value per thread).
-    const bool col_bias = has_bias && (SWAP ? p.bias_layout == 0 : p.bias_layout == 1);
+    const bool bwd = is_backward(p.epilog);
+    const bool has_bias = p.epilog != EPI_NONE && !bwd;
+    // Bias (and, backward, bias gradient) that varies along the accumulator's columns
+    // (staged in shared memory; column sums) or along its lanes (one value per thread).
+    const bool along_cols = SWAP ? p.bias_layout == 0 : p.bias_layout == 1;
+    const bool col_bias = has_bias && along_cols;
     const bool lane_bias = has_bias && !col_bias;
     const int col_limit = SWAP ? p.m : p.n;   // extent of the accumulator-column coordinate
     const int lane_limit = SWAP ? p.n : p.m;  // extent of the accumulator-lane coordinate
@@ -569,6 +661,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         const int valid_cols = min(BN, col_limit - col_base);
         const int nchunks = (valid_cols + CH - 1) / CH;
         const bool warp_live = lane_base < lane_limit;
+        float lane_sum = 0.0f;  // backward, bias gradient along the lanes: this tile's sum
 
         for (int c = w.rank + half * w.split; c < nchunks; c += 2 * w.split) {
             uint32_t r[32];
@@ -624,7 +717,12 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
 #pragma unroll
                     for (int j = 0; j < CH; ++j)
                         word |= (v[j] > 0.0f && col0 + j < p.n) ? (1u << j) : 0u;
-                    if (row < p.m) p.aux[static_cast<long long>(row) * p.aux_ld + col0 / 32] = word;
+                    if (row < p.m)
+                        static_cast<uint32_t*>(p.aux)[static_cast<long long>(row) * p.aux_ld + col0 / 32] = word;
+                } else if (p.epilog == EPI_GELU_AUX_BIAS) {
+                    store_pre_row(p, v, row, col0);
+                } else if (bwd) {
+                    backward_factor_row(p, v, row, col0);
                 }
                 activate(v, p.epilog);
                 if (p.epilog == EPI_BIAS_RESIDUAL && row < p.m) {
@@ -681,13 +779,39 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                 const int col = lane_idx;
                 const bool col_ok = col < p.n;
                 const int t0 = col_base + c * CH;
+                const int word_idx = lane_base / 32;
                 if (p.epilog == EPI_RELU_AUX_BIAS) {
-                    const int word_idx = lane_base / 32;
 #pragma unroll
                     for (int j = 0; j < CH; ++j) {
                         const uint32_t word = __ballot_sync(0xFFFFFFFFu, col_ok && v[j] > 0.0f);
                         if (lane == 0 && t0 + j < p.m && word_idx < p.aux_ld)
-                            p.aux[static_cast<long long>(t0 + j) * p.aux_ld + word_idx] = word;
+                            static_cast<uint32_t*>(p.aux)[static_cast<long long>(t0 + j) * p.aux_ld + word_idx] = word;
+                    }
+                } else if (p.epilog == EPI_GELU_AUX_BIAS) {
+                    uint16_t* pre16 = static_cast<uint16_t*>(p.aux);
+#pragma unroll
+                    for (int j = 0; j < CH; ++j)
+                        if (col_ok && t0 + j < p.m)
+                            pre16[static_cast<long long>(t0 + j) * p.n + col] = to16(v[j], p.bf16);
+                } else if (p.epilog == EPI_DRELU_BGRAD) {
+                    // lane j < CH fetches the mask word of row t0 + j; bit `lane` of it
+                    uint32_t mrow = 0;
+                    if (lane < CH && t0 + lane < p.m && word_idx < p.aux_ld)
+                        mrow = __ldg(static_cast<const uint32_t*>(p.aux_in) +
+                                     static_cast<long long>(t0 + lane) * p.aux_ld + word_idx);
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) {
+                        const uint32_t mw = __shfl_sync(0xFFFFFFFFu, mrow, j);
+                        v[j] = (col_ok && ((mw >> lane) & 1u)) ? v[j] : 0.0f;
+                    }
+                } else if (p.epilog == EPI_DGELU_BGRAD) {
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) {
+                        float g = 0.0f;
+                        if (col_ok && t0 + j < p.m)
+                            g = gelu_grad_fast(load_16bit(p.aux_in, static_cast<long long>(t0 + j) * p.n + col,
+                                                          p.bf16));
+                        v[j] *= g;
                     }
                 }
                 activate(v, p.epilog);
@@ -714,7 +838,23 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                     }
                 }
             }
+            if (bwd && warp_live) {
+                // bias gradient of this chunk (entries outside the matrix are 0 here)
+                if (along_cols) {
+                    float x[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) x[j] = j < CH ? v[j] : 0.0f;
+                    const float colsum = warp_column_sums(x, lane);
+                    const int ci = col_base + c * CH + lane;
+                    if (lane < CH && ci < col_limit) atomicAdd(p.dbias + ci, colsum);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) lane_sum += v[j];
+                }
+            }
         }
+        if (bwd && !along_cols && lane_idx < lane_limit && w.rank + half * w.split < nchunks)
+            atomicAdd(p.dbias + lane_idx, lane_sum);
         tcgen05_fence_before_sync();
         if constexpr (PAIR)  // the even CTA's MMAs write both CTAs' accumulators
             mbar_arrive_cluster(map_shared_rank(bar0 + 8u * (kBarTmemEmpty + acc), 0));

@@ -14,8 +14,16 @@ enum Epilog : int {
     EPI_RELU_AUX_BIAS = 3,
     EPI_BIAS_RESIDUAL = 4,
     EPI_NONE = 5,
-    EPI_TANH_BIAS = 6
+    EPI_TANH_BIAS = 6,
+    EPI_GELU_AUX_BIAS = 7,  // as GELU_BIAS, and the pre-activation written to aux (16-bit)
+    EPI_DRELU_BGRAD = 8,    // D = A.B * mask bit (aux_in), dbias = sums of D
+    EPI_DGELU_BGRAD = 9     // D = A.B * GELU'(aux_in pre), dbias = sums of D
 };
+
+__host__ __device__ constexpr bool is_backward(int epilog)
+{
+    return epilog == EPI_DRELU_BGRAD || epilog == EPI_DGELU_BGRAD;
+}
 
 // Device status word values: 0 = fine, else (kCodeTimeout | role).
 enum : int {
@@ -39,7 +47,9 @@ struct GemmParams {
     const void* bias;
     const void* residual;
     void* D;
-    uint32_t* aux;
+    void* aux;            // RELU_AUX_BIAS: uint32 mask words; GELU_AUX_BIAS: 16-bit pre-activation
+    const void* aux_in;   // DRELU_BGRAD: mask words; DGELU_BGRAD: 16-bit pre-activation
+    float* dbias;         // backward epilogs: bias gradient (zeroed before the launch)
     int* status;
     unsigned long long wait_limit_ns;
     int m, n, k;
@@ -87,7 +97,8 @@ int rowpair_max_clusters();
 // Elementwise epilogue over a 16-bit pre-activation (the unfused baseline's second kernel;
 // pre == nullptr means pre = 0, which serves k == 0).
 cudaError_t elementwise_launch(const void* pre, const void* bias, const void* residual, void* D,
-                               uint32_t* aux, int m, int n, int epilog, int bias_layout, int bf16,
-                               int aux_ld, int sm_count, cudaStream_t stream);
+                               void* aux, const void* aux_in, float* dbias, int m, int n,
+                               int epilog, int bias_layout, int bf16, int aux_ld, int sm_count,
+                               cudaStream_t stream);
 
 }  // namespace gemm_epi

@@ -17,7 +17,8 @@ LIB_PATH = os.path.join(PKG, "libgemmepi.so")
 
 DTYPE = {"f16": 0, "bf16": 1}
 EPILOG = {"BIAS": 0, "RELU_BIAS": 1, "GELU_BIAS": 2, "RELU_AUX_BIAS": 3, "BIAS_RESIDUAL": 4,
-          "NONE": 5, "TANH_BIAS": 6}
+          "NONE": 5, "TANH_BIAS": 6, "GELU_AUX_BIAS": 7, "DRELU_BGRAD": 8, "DGELU_BGRAD": 9}
+BACKWARD = ("DRELU_BGRAD", "DGELU_BGRAD")
 BIAS_LAYOUT = {"M1": 0, "1N": 1}
 OPTION = {"VARIANT": 0, "TILE_N": 1, "SPLIT_K": 2, "GRID": 3, "GROUP_M": 4,
           "WAIT_LIMIT_US": 5, "DEBUG_STALL": 6, "PREFETCH": 7, "PDL": 8}
@@ -31,13 +32,21 @@ EXPORTS = ["gemm_epi_plan", "gemm_epi_plan_set_option", "gemm_epi_execute",
            "gemm_epi_sync_status", "gemm_epi_status_string", "gemm_epi_plan_describe",
            "gemm_epi_aux_words_per_row", "gemm_epi_ffn_plan", "gemm_epi_ffn_execute",
            "gemm_epi_ffn_hidden", "gemm_epi_ffn_sync_status", "gemm_epi_ffn_free",
-           "gemm_epi_ffn_execute_noalloc"]
+           "gemm_epi_ffn_execute_noalloc", "gemm_epi_execute_operands",
+           "gemm_epi_execute_operands_unfused"]
 
 # Largest t * f the allocation-free FFN call accepts (its static scratch holds H).
 FFN_NOALLOC_MAX_HIDDEN = 16 * 1024 * 1024
 
 _lib = None
 _lock = threading.Lock()
+
+
+class Operands(ctypes.Structure):
+    """gemm_epi_operands: every operand of one call (NULL where the epilog uses none)."""
+    _fields_ = [("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("residual", ctypes.c_void_p), ("D", ctypes.c_void_p), ("aux", ctypes.c_void_p),
+                ("aux_in", ctypes.c_void_p), ("dbias", ctypes.c_void_p)]
 
 
 class GemmEpiError(RuntimeError):
@@ -88,6 +97,10 @@ def load_library(path: str | None = None):
         lib.gemm_epi_ffn_execute_noalloc.restype = i32
         lib.gemm_epi_ffn_execute_noalloc.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, vp,
                                                      vp, vp]
+        lib.gemm_epi_execute_operands.restype = i32
+        lib.gemm_epi_execute_operands.argtypes = [vp, ctypes.POINTER(Operands), vp]
+        lib.gemm_epi_execute_operands_unfused.restype = i32
+        lib.gemm_epi_execute_operands_unfused.argtypes = [vp, ctypes.POINTER(Operands), vp, vp]
         if path is None:
             _lib = lib
         return lib
@@ -152,6 +165,26 @@ def gemm_epi_execute_unfused(plan, A, B, bias, residual, pre, D, aux=None, strea
                                                    _ptr(residual), _ptr(pre), _ptr(D),
                                                    _ptr(aux), _stream(stream)),
            "gemm_epi_execute_unfused")
+
+
+def _operands(A, B, bias, residual, D, aux, aux_in, dbias) -> Operands:
+    return Operands(_ptr(A), _ptr(B), _ptr(bias), _ptr(residual), _ptr(D), _ptr(aux),
+                    _ptr(aux_in), _ptr(dbias))
+
+
+def gemm_epi_execute_operands(plan, A, B, D, bias=None, residual=None, aux=None, aux_in=None,
+                              dbias=None, stream=None):
+    ops = _operands(A, B, bias, residual, D, aux, aux_in, dbias)
+    _check(load_library().gemm_epi_execute_operands(plan, ctypes.byref(ops), _stream(stream)),
+           "gemm_epi_execute_operands")
+
+
+def gemm_epi_execute_operands_unfused(plan, A, B, D, pre, bias=None, residual=None, aux=None,
+                                      aux_in=None, dbias=None, stream=None):
+    ops = _operands(A, B, bias, residual, D, aux, aux_in, dbias)
+    _check(load_library().gemm_epi_execute_operands_unfused(plan, ctypes.byref(ops), _ptr(pre),
+                                                            _stream(stream)),
+           "gemm_epi_execute_operands_unfused")
 
 
 def gemm_epi_free(plan):
@@ -281,11 +314,15 @@ class Plan:
     def describe(self) -> str:
         return gemm_epi_plan_describe(self.handle)
 
-    def execute(self, A, B, bias, D, aux=None, residual=None, stream=None):
-        gemm_epi_execute_ex(self.handle, A, B, bias, residual, D, aux, stream)
+    def execute(self, A, B, bias, D, aux=None, residual=None, stream=None, aux_in=None,
+                dbias=None):
+        gemm_epi_execute_operands(self.handle, A, B, D, bias=bias, residual=residual, aux=aux,
+                                  aux_in=aux_in, dbias=dbias, stream=stream)
 
-    def execute_unfused(self, A, B, bias, pre, D, aux=None, residual=None, stream=None):
-        gemm_epi_execute_unfused(self.handle, A, B, bias, residual, pre, D, aux, stream)
+    def execute_unfused(self, A, B, bias, pre, D, aux=None, residual=None, stream=None,
+                        aux_in=None, dbias=None):
+        gemm_epi_execute_operands_unfused(self.handle, A, B, D, pre, bias=bias, residual=residual,
+                                          aux=aux, aux_in=aux_in, dbias=dbias, stream=stream)
 
     def sync_status(self, stream=None) -> int:
         return gemm_epi_sync_status(self.handle, stream)

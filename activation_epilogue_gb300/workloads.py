@@ -20,6 +20,7 @@ from __future__ import annotations
 import math
 from dataclasses import dataclass, field
 
+import numpy as np
 import torch
 
 TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16}
@@ -153,3 +154,19 @@ def random_problem(m: int, n: int, k: int, *, dtype: str = "bf16", bias_layout: 
     if residual:
         out["R"] = draw((m, n), 1.0)
     return out
+
+
+def random_backward_problem(m: int, n: int, k: int, *, dtype: str = "bf16", seed: int = 0,
+                            device="cpu") -> dict:
+    """Inputs of a backward epilogue: A (m x k) and B (k x n) as in random_problem (the
+    incoming gradient and the weight), ReLU mask words uint32 [m][ceil(n/32)] with every bit
+    (the pad bits too) drawn fair, and a stored pre-activation ~ N(0, 2^2) in dtype."""
+    p = random_problem(m, n, k, dtype=dtype, seed=seed, device=device)
+    g = _generator(seed + 99991, device)
+    words = (n + 31) // 32
+    halves = torch.randint(0, 1 << 16, (m, words, 2), generator=g, dtype=torch.int64,
+                           device=device)
+    mask = (halves[..., 0] | (halves[..., 1] << 16)).to(torch.int64)
+    pre = _draw(g, (m, n), 2.0, dtype, device)
+    return {"A": p["A"], "B": p["B"],
+            "mask": mask.cpu().numpy().astype(np.uint32), "pre": pre}

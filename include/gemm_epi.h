@@ -17,7 +17,9 @@
  *       bias is (m,1) or (1,n), any other shape fails; the plan must be freed;
  *     - paragraph on limitations: RELU_AUX_BIAS also produces the mask backward needs;
  *       Tanh is one of the predefined epilogs;
- *     - closing paragraph: GELU named as a further epilog.
+ *     - closing paragraph: GELU and dBias named as further epilogs (the backward epilogs
+ *       below consume the mask of RELU_AUX_BIAS, or the pre-activation GELU_AUX_BIAS
+ *       keeps, and produce dBias).
  *   "nvmath-python: cuBLAS and cuSOLVER bindings for ML linear algebra"
  *   (blog.hotdry.top, 2025-09-19), matmul-planning checklist: plan() chooses the algorithm,
  *     execute() is non-blocking.
@@ -30,15 +32,16 @@
  *     of the plan's dtype, in device memory.  The bias has m elements for the (m,1)
  *     layout and n for (1,n), same dtype.  The caller owns all of them; the library never
  *     allocates, frees or keeps them beyond the call.
- *   - aux (RELU_AUX_BIAS only) is uint32 [m][ceil(n/32)] in device memory: bit (j mod 32)
+ *   - aux of RELU_AUX_BIAS is uint32 [m][ceil(n/32)] in device memory: bit (j mod 32)
  *     of word floor(j/32) in row i is 1 iff the fp32 pre-activation at (i, j) is > 0;
  *     bits for columns >= n are written 0.
  *   - Shapes: m, n, k >= 0; n and k must be multiples of 8 (rows of A, B and D start on
  *     16-byte boundaries, which the tensor-memory-access unit needs).  m == 0 or n == 0 is
- *     an empty problem (nothing is launched); k == 0 gives D = epi(bias broadcast).
+ *     an empty problem (no kernel is launched; a backward call still zeroes dbias);
+ *     k == 0 gives D = epi(bias broadcast) (backward: D = 0, dbias = 0).
  *   - Pointers A, B, D, residual and the unfused pre buffer must be 16-byte aligned; bias
- *     2-byte aligned; aux 4-byte aligned.  D must not overlap A, B or bias; D may be the
- *     residual buffer itself (an in-place residual add).
+ *     2-byte aligned; aux 4-byte aligned (16 for GELU_AUX_BIAS).  D must not overlap A, B
+ *     or bias; D may be the residual buffer itself (an in-place residual add).
  *   - All execute calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream) and return launch-time errors only; a device-side wait that ran out
  *     its time limit is reported by gemm_epi_sync_status.  The fused kernel is launched as
@@ -78,8 +81,17 @@ typedef enum {
     GEMM_EPI_RELU_AUX_BIAS = 3, /* as RELU_BIAS, and writes the aux mask [pre > 0] */
     GEMM_EPI_BIAS_RESIDUAL = 4, /* D = A.B + bias + residual (FFN second GEMM) */
     GEMM_EPI_NONE = 5,          /* D = A.B (no bias; bias pointer ignored) */
-    GEMM_EPI_TANH_BIAS = 6      /* D = tanh(A.B + bias) (the pages list Tanh among the
+    GEMM_EPI_TANH_BIAS = 6,     /* D = tanh(A.B + bias) (the pages list Tanh among the
                                    predefined epilogs) */
+    GEMM_EPI_GELU_AUX_BIAS = 7, /* as GELU_BIAS, and writes aux = the pre-activation
+                                   A.B + bias rounded to the plan's dtype (m x n, 16-bit),
+                                   the input the GELU backward needs */
+    GEMM_EPI_DRELU_BGRAD = 8,   /* backward of RELU_AUX_BIAS: D = (A.B) * mask, mask from
+                                   aux_in (the RELU_AUX_BIAS layout), and dbias = the sums
+                                   of that product along the bias's broadcast direction */
+    GEMM_EPI_DGELU_BGRAD = 9    /* backward of GELU_AUX_BIAS: D = (A.B) * GELU'(pre), pre
+                                   from aux_in (the GELU_AUX_BIAS layout), GELU'(x) =
+                                   Phi(x) + x phi(x); dbias as for DRELU_BGRAD */
 } gemm_epi_epilog;
 
 typedef enum {
@@ -89,7 +101,7 @@ typedef enum {
 
 typedef enum {
     GEMM_EPI_OK = 0,
-    GEMM_EPI_ERR_INVALID_ARG = 1,       /* null handle/pointer, bad enum, aux misuse */
+    GEMM_EPI_ERR_INVALID_ARG = 1,       /* null handle/pointer, bad enum, operand misuse */
     GEMM_EPI_ERR_UNSUPPORTED_SHAPE = 2, /* negative size, n or k not a multiple of 8 */
     GEMM_EPI_ERR_MISALIGNED = 3,        /* a pointer breaks the alignment rules above */
     GEMM_EPI_ERR_NO_DEVICE = 4,         /* no CUDA device / driver */
@@ -139,8 +151,10 @@ gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt,
 
 /*
  * Run the fused kernel: D = epi(A.B + bias), and the aux mask for RELU_AUX_BIAS (the
- * page's .execute()).  aux must be non-NULL exactly for RELU_AUX_BIAS.  Not valid for
- * BIAS_RESIDUAL (use gemm_epi_execute_ex).  bias may be NULL only for NONE.
+ * page's .execute()).  aux must be non-NULL exactly for RELU_AUX_BIAS (and GELU_AUX_BIAS,
+ * where it points to the 16-bit pre-activation).  Not valid for BIAS_RESIDUAL (use
+ * gemm_epi_execute_ex) nor the backward epilogs (use gemm_epi_execute_operands).  bias may
+ * be NULL only for NONE.
  */
 gemm_epi_status gemm_epi_execute(gemm_epi_plan_t p, const void* A, const void* B,
                                  const void* bias, void* D, uint32_t* aux,
@@ -161,6 +175,46 @@ gemm_epi_status gemm_epi_execute_ex(gemm_epi_plan_t p, const void* A, const void
 gemm_epi_status gemm_epi_execute_unfused(gemm_epi_plan_t p, const void* A, const void* B,
                                          const void* bias, const void* residual, void* pre,
                                          void* D, uint32_t* aux, cudaStream_t stream);
+
+/*
+ * Every operand of one call, for the epilogs that need more than execute_ex carries
+ * (GELU_AUX_BIAS, DRELU_BGRAD, DGELU_BGRAD; the others are accepted too).  Fields an
+ * epilog does not use must be NULL.  All are device pointers owned by the caller.
+ *   A, B, bias, residual, D   as in gemm_epi_execute_ex; no bias for the backward epilogs
+ *                             (the bias layout of the plan then says which way dbias runs);
+ *   aux       output: RELU_AUX_BIAS the uint32 mask words described above; GELU_AUX_BIAS the
+ *             16-bit pre-activation, m x n row-major, 16-byte aligned;
+ *   aux_in    input: DRELU_BGRAD mask words in the RELU_AUX_BIAS layout (pad bits ignored),
+ *             4-byte aligned; DGELU_BGRAD the 16-bit pre-activation in the GELU_AUX_BIAS
+ *             layout, 16-byte aligned;
+ *   dbias     output, DRELU_BGRAD and DGELU_BGRAD: fp32, m entries (bias layout (m,1): sums
+ *             over each row of D before rounding) or n entries ((1,n): sums over each
+ *             column), 4-byte aligned.  The call zeroes it on `stream` and the kernel adds
+ *             into it, so the summation order, and the last bits of dbias, may vary from
+ *             call to call.  D and dbias must not overlap any other operand.
+ * Backward calls are launched without the programmatic dependence described above.
+ */
+typedef struct {
+    const void* A;
+    const void* B;
+    const void* bias;
+    const void* residual;
+    void* D;
+    void* aux;
+    const void* aux_in;
+    float* dbias;
+} gemm_epi_operands;
+
+/* The fused kernel on the operands in *ops (any epilog of the plan). */
+gemm_epi_status gemm_epi_execute_operands(gemm_epi_plan_t p, const gemm_epi_operands* ops,
+                                          cudaStream_t stream);
+
+/* The unfused baseline (as gemm_epi_execute_unfused) on the operands in *ops: the GEMM
+ * writes pre0 = A.B to `pre`, the elementwise kernel applies the epilog (and, backward, the
+ * mask or GELU' factor and the dbias sums) from there. */
+gemm_epi_status gemm_epi_execute_operands_unfused(gemm_epi_plan_t p,
+                                                  const gemm_epi_operands* ops, void* pre,
+                                                  cudaStream_t stream);
 
 /* Release the plan (the page's .free()).  NULL is accepted and ignored. */
 gemm_epi_status gemm_epi_free(gemm_epi_plan_t p);

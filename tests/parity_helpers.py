@@ -53,6 +53,8 @@ def run(inputs: dict, m: int, n: int, k: int, dtype: str, epilog: str, layout: s
     aux = None
     if epilog == "RELU_AUX_BIAS":
         aux = torch.full((m, (n + 31) // 32), -1, dtype=torch.int32, device=dev)
+    elif epilog == "GELU_AUX_BIAS":
+        aux = torch.full((m, n), float("nan"), dtype=TD[dtype], device=dev)
     with gemm_epi.Plan(m, n, k, dtype, epilog, layout, **(options or {})) as plan:
         if unfused:
             pre = torch.empty((m, n), dtype=TD[dtype], device=dev)
@@ -62,8 +64,11 @@ def run(inputs: dict, m: int, n: int, k: int, dtype: str, epilog: str, layout: s
         status = plan.sync_status()
         desc = plan.describe()
     assert status == 0, f"device status {gemm_epi.status_string(status)} ({desc})"
-    words = None if aux is None else aux.cpu().numpy().view(np.uint32)
-    return D.cpu(), words, desc
+    if aux is None:
+        return D.cpu(), None, desc
+    if epilog == "GELU_AUX_BIAS":
+        return D.cpu(), aux.cpu(), desc  # the stored 16-bit pre-activation
+    return D.cpu(), aux.cpu().numpy().view(np.uint32), desc
 
 
 def oracle_ref(inputs: dict, dtype: str, epilog: str, layout: str):
@@ -85,7 +90,17 @@ def check(inputs, m, n, k, dtype, epilog, layout, unfused=False, options=None, e
     else:
         err = rel_err(D, want)
         assert err <= TOL[dtype], f"rel err {err:.3e} > {TOL[dtype]} ({desc})"
-    if words is not None:
+    if words is not None and epilog == "GELU_AUX_BIAS":
+        # the stored pre-activation: one rounding of the fp32 value to the output format
+        # (unfused: of bf16/f16(A.B) + bias, which adds one rounding of A.B)
+        got = words.float().double().numpy()
+        slack = 0.0
+        if unfused:
+            pre0 = oracle.gemm_epi(inputs["A"], inputs["B"], None, dtype=dtype, epilog="NONE")
+            slack = UNIT_ROUNDOFF[dtype] * np.abs(pre0)
+        bad = np.abs(got - pre) > TOL[dtype] * (np.abs(pre) + 1.0) + slack
+        assert not bad.any(), f"{int(bad.sum())} stored pre values off ({desc})"
+    elif words is not None:
         band = AUX_BAND
         if unfused:
             # The unfused baseline decides the mask on bf16/f16(A.B) + bias: its decision

@@ -58,15 +58,20 @@ def test_bad_enums_rejected(lib):
     import ctypes
     h = ctypes.c_void_p()
     assert lib.gemm_epi_plan(ctypes.byref(h), 8, 8, 8, 7, 0, 0) == 1
-    assert lib.gemm_epi_plan(ctypes.byref(h), 8, 8, 8, 0, 9, 0) == 1
+    assert lib.gemm_epi_plan(ctypes.byref(h), 8, 8, 8, 0, 10, 0) == 1
+    assert lib.gemm_epi_plan(ctypes.byref(h), 8, 8, 8, 0, -1, 0) == 1
     assert lib.gemm_epi_plan(ctypes.byref(h), 8, 8, 8, 0, 0, 5) == 1
     assert lib.gemm_epi_plan(None, 8, 8, 8, 0, 0, 0) == 1
     assert h.value is None
 
 
 def test_null_handles_are_safe(lib):
+    import ctypes
     assert lib.gemm_epi_free(None) == 0
     assert lib.gemm_epi_execute(None, None, None, None, None, None, None) == 1
+    ops = gemm_epi.Operands()
+    assert lib.gemm_epi_execute_operands(None, ctypes.byref(ops), None) == 1
+    assert lib.gemm_epi_execute_operands_unfused(None, ctypes.byref(ops), None, None) == 1
     assert lib.gemm_epi_sync_status(None, None) == 1
     assert lib.gemm_epi_plan_set_option(None, 0, 0) == 1
     assert lib.gemm_epi_plan_describe(None) == b""

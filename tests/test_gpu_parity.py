@@ -9,7 +9,8 @@ from parity_helpers import TD, TOL, check, rel_err, run
 
 pytestmark = pytest.mark.gpu
 
-EPILOGS = ["BIAS", "RELU_BIAS", "GELU_BIAS", "RELU_AUX_BIAS", "BIAS_RESIDUAL", "NONE", "TANH_BIAS"]
+EPILOGS = ["BIAS", "RELU_BIAS", "GELU_BIAS", "RELU_AUX_BIAS", "BIAS_RESIDUAL", "NONE", "TANH_BIAS",
+           "GELU_AUX_BIAS"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -102,7 +103,8 @@ def test_small_and_ragged(m, n, k, epilog):
     check(p, m, n, k, "bf16", epilog, "M1")
 
 
-@pytest.mark.parametrize("epilog", ["BIAS", "RELU_AUX_BIAS", "GELU_BIAS", "BIAS_RESIDUAL"])
+@pytest.mark.parametrize("epilog", ["BIAS", "RELU_AUX_BIAS", "GELU_BIAS", "BIAS_RESIDUAL",
+                                    "GELU_AUX_BIAS"])
 @pytest.mark.parametrize("layout", ["M1", "1N"])
 def test_k_zero_is_activation_of_bias(epilog, layout):
     m, n = 70, 72
