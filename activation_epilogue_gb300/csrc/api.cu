@@ -111,6 +111,20 @@ int pick_rowtile_bn(int64_t m, int64_t n, int k_blocks, int sm_count)
     return best;
 }
 
+// N tile of the CTA-pair kernel: 224 when it needs fewer 256-row tile waves over the resident
+// pairs than 256 does, else 256.  Both stage the same 32 KB of operands per CTA and K block
+// (224 wide leaves part of the second 64-column B panel unused), and measured on GB300 a
+// 224-wide tile costs about what a 256-wide one does, so only the wave count decides:
+// 4096 x 4096 on 76 pairs is 4 waves either way (256: 3.4 paid as 4), and 224 gives the
+// shorter last tile (4096 x 4096 x 1024 GELU: 38.5 us against 41.0 us).
+int pick_pair_bn(int64_t m, int64_t n, long long pairs)
+{
+    const int64_t tm = (m + 255) / 256;
+    const long long w256 = (tm * ((n + 255) / 256) + pairs - 1) / pairs;
+    const long long w224 = (tm * ((n + 223) / 224) + pairs - 1) / pairs;
+    return w224 <= w256 ? 224 : 256;
+}
+
 gemm_epi_status configure(gemm_epi_plan_s* p)
 {
     p->maps_valid = false;
@@ -140,18 +154,21 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
         p->variant = v;
         p->k_blocks = static_cast<int>((p->k + 63) / 64);
         if (v == kRowPair) {
-            // CTA pairs on 256 x 256 tiles, persistent, no split
-            p->bn = 256;
-            p->tiles_m = static_cast<int>((p->m + 255) / 256);
-            p->tiles_n = static_cast<int>((p->n + 255) / 256);
-            p->stages = rowpair_stages();
-            p->smem = rowpair_smem_bytes();
-            if (rowpair_prepare() != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
-            const long long tiles = static_cast<long long>(p->tiles_m) * p->tiles_n;
-            long long pairs = rowpair_max_clusters();
+            // CTA pairs on 256 x BN tiles, persistent, no split
+            if (p->opt_bn && p->opt_bn != 224 && p->opt_bn != 256)
+                return GEMM_EPI_ERR_INVALID_ARG;
+            if (rowpair_prepare(256) != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
+            long long pairs = rowpair_max_clusters(256);  // same shared memory for every BN
             if (pairs > p->sm_count / 2) pairs = p->sm_count / 2;
             if (p->opt_grid > 0 && p->opt_grid / 2 < pairs) pairs = p->opt_grid / 2;
             if (pairs < 1) return GEMM_EPI_ERR_LAUNCH;
+            p->bn = p->opt_bn ? p->opt_bn : pick_pair_bn(p->m, p->n, pairs);
+            p->tiles_m = static_cast<int>((p->m + 255) / 256);
+            p->tiles_n = static_cast<int>((p->n + p->bn - 1) / p->bn);
+            p->stages = rowpair_stages(p->bn);
+            p->smem = rowpair_smem_bytes(p->bn);
+            if (rowpair_prepare(p->bn) != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
+            const long long tiles = static_cast<long long>(p->tiles_m) * p->tiles_n;
             if (pairs > tiles) pairs = tiles;
             p->kb_per_split = p->k_blocks;
             p->grid = static_cast<int>(2 * pairs);
@@ -159,6 +176,8 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             if (gm > p->tiles_m) gm = p->tiles_m;
             p->group_m = gm < 1 ? 1 : gm;
         } else if (v == kRowTile) {
+            if (p->opt_bn && p->opt_bn != 64 && p->opt_bn != 128 && p->opt_bn != 256)
+                return GEMM_EPI_ERR_INVALID_ARG;
             p->bn = p->opt_bn ? p->opt_bn : pick_rowtile_bn(p->m, p->n, p->k_blocks, p->sm_count);
             p->tiles_m = static_cast<int>((p->m + 127) / 128);
             p->tiles_n = static_cast<int>((p->n + p->bn - 1) / p->bn);
@@ -298,7 +317,7 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, in
     prm.prefetch = p->prefetch;
     cudaError_t e;
     if (p->variant == kRowPair)
-        e = rowpair_launch(prm, p->grid, stream, pdl);
+        e = rowpair_launch(p->bn, prm, p->grid, stream, pdl);
     else if (p->variant == kRowTile)
         e = rowtile_launch(p->bn, prm, p->grid, stream, pdl);
     else
@@ -465,7 +484,7 @@ gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt,
         p->opt_variant = static_cast<int>(value);
         break;
     case GEMM_EPI_OPT_TILE_N:
-        if (value != 0 && value != 64 && value != 128 && value != 256)
+        if (value != 0 && value != 64 && value != 128 && value != 224 && value != 256)
             return GEMM_EPI_ERR_INVALID_ARG;
         p->opt_bn = static_cast<int>(value);
         break;

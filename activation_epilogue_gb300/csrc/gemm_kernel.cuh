@@ -55,18 +55,21 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;   // producer, MMA, epilogue warps
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kPipeBudget = 192 * 1024;
 
+constexpr int pow2_at_least(int x, int p = 32) { return p >= x ? p : pow2_at_least(x, 2 * p); }
+
 // PAIR: a CTA pair computes a 256 x BN tile with cta_group::2 MMAs; each CTA holds 128 rows
-// of A and BN/2 rows (columns of D) of B per stage.
+// of A and BN/2 rows (columns of D) of B per stage, staged as whole 64-row panels (for BN
+// 224 or 192 the last panel is partly unused).
 template <int BN, bool PAIR = false>
 struct TileCfg {
-    static constexpr int kBRows = PAIR ? BN / 2 : BN;
+    static constexpr int kBRows = PAIR ? (BN / 2 + 63) / 64 * 64 : BN;
     static constexpr int kABytes = kBM * kBK * 2;      // MMA-A operand: 128 rows x 64 k
     static constexpr int kBBytes = kBRows * kBK * 2;   // MMA-B operand: kBRows rows x 64 k
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kStagesRaw = kPipeBudget / kStageBytes;
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
     static constexpr int kChunk = BN < 32 ? BN : 32;            // columns per TMEM load
-    static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
+    static constexpr int kTmemCols = pow2_at_least(2 * BN);  // two accumulators
     static constexpr int kOffEpi = kStages * kStageBytes;        // one 2 KB box per warp
     static constexpr int kEpiBytes = kEpiWarps * 2048;
     static constexpr int kOffBias = kOffEpi + kEpiBytes;         // 256 fp32 per warp
@@ -240,7 +243,7 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase,
         const uint32_t fb0 = map_shared_rank(fb, 0);
         tma_load_2d_pair(sa, &p.tm_A, fb0, k0, tm * 2 * kBM + static_cast<int>(rank) * kBM);
 #pragma unroll
-        for (int q = 0; q < BN / 128; ++q)
+        for (int q = 0; q < C::kBRows / 64; ++q)
             tma_load_2d_pair(sb + q * 8192, &p.tm_B, fb0,
                              tn * BN + static_cast<int>(rank) * (BN / 2) + q * 64, k0);
         return;
@@ -470,11 +473,11 @@ __device__ __forceinline__ float warp_column_sums(float (&x)[32], int lane)
 
 // Row-tile backward factor: v[j] (row `row`, column col0 + j) times the ReLU mask bit or
 // GELU' of the stored pre-activation; 0 outside the matrix.
-__device__ __forceinline__ void backward_factor_row(const GemmParams& p, float (&v)[32], int row,
-                                                    int col0)
+__device__ __forceinline__ void backward_factor_row(const GemmParams& p, int epilog, float (&v)[32],
+                                                    int row, int col0)
 {
     const int valid = row < p.m ? min(32, p.n - col0) : 0;
-    if (p.epilog == EPI_DRELU_BGRAD) {
+    if (epilog == EPI_DRELU_BGRAD) {
         uint32_t mw = 0;
         if (valid > 0)
             mw = __ldg(static_cast<const uint32_t*>(p.aux_in) + static_cast<long long>(row) * p.aux_ld +
@@ -577,11 +580,14 @@ __device__ __forceinline__ void publish_partials(const GemmParams& p, uint8_t* s
     tcgen05_fence_before_sync();
 }
 
-template <int BN, bool SWAP, bool PAIR = false>
+// EPI >= 0 fixes the epilog at compile time (only its code is in the kernel); -1 reads it
+// from the parameters.
+template <int BN, bool SWAP, bool PAIR = false, int EPI = -1>
 __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem, uint32_t sbase,
                                              uint32_t bar0, uint32_t tmem_base,
                                              volatile int* abort_flag)
 {
+    const int epilog = EPI >= 0 ? EPI : p.epilog;
     using C = TileCfg<BN, PAIR>;
     constexpr int CH = C::kChunk;
     const int warp = threadIdx.x >> 5;
@@ -590,8 +596,8 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
     const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
     const int half = ew >> 2;            // the pair's warps take alternate chunks
     const WorkRange w = work_range<PAIR>(p);
-    const bool bwd = is_backward(p.epilog);
-    const bool has_bias = p.epilog != EPI_NONE && !bwd;
+    const bool bwd = is_backward(epilog);
+    const bool has_bias = epilog != EPI_NONE && !bwd;
     // Bias (and, backward, bias gradient) that varies along the accumulator's columns
     // (staged in shared memory; column sums) or along its lanes (one value per thread).
     const bool along_cols = SWAP ? p.bias_layout == 0 : p.bias_layout == 1;
@@ -712,20 +718,20 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                 // ---- rows of D on lanes: thread = one row, 32 consecutive columns ----
                 const int row = lane_idx;
                 const int col0 = col_base + c * CH;
-                if (p.epilog == EPI_RELU_AUX_BIAS) {
+                if (epilog == EPI_RELU_AUX_BIAS) {
                     uint32_t word = 0;
 #pragma unroll
                     for (int j = 0; j < CH; ++j)
                         word |= (v[j] > 0.0f && col0 + j < p.n) ? (1u << j) : 0u;
                     if (row < p.m)
                         static_cast<uint32_t*>(p.aux)[static_cast<long long>(row) * p.aux_ld + col0 / 32] = word;
-                } else if (p.epilog == EPI_GELU_AUX_BIAS) {
+                } else if (epilog == EPI_GELU_AUX_BIAS) {
                     store_pre_row(p, v, row, col0);
                 } else if (bwd) {
-                    backward_factor_row(p, v, row, col0);
+                    backward_factor_row(p, epilog, v, row, col0);
                 }
-                activate(v, p.epilog);
-                if (p.epilog == EPI_BIAS_RESIDUAL && row < p.m) {
+                activate(v, epilog);
+                if (epilog == EPI_BIAS_RESIDUAL && row < p.m) {
                     const uint16_t* rrow = R + static_cast<long long>(row) * p.n + col0;
                     if (col0 + CH <= p.n) {
 #pragma unroll
@@ -780,20 +786,20 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                 const bool col_ok = col < p.n;
                 const int t0 = col_base + c * CH;
                 const int word_idx = lane_base / 32;
-                if (p.epilog == EPI_RELU_AUX_BIAS) {
+                if (epilog == EPI_RELU_AUX_BIAS) {
 #pragma unroll
                     for (int j = 0; j < CH; ++j) {
                         const uint32_t word = __ballot_sync(0xFFFFFFFFu, col_ok && v[j] > 0.0f);
                         if (lane == 0 && t0 + j < p.m && word_idx < p.aux_ld)
                             static_cast<uint32_t*>(p.aux)[static_cast<long long>(t0 + j) * p.aux_ld + word_idx] = word;
                     }
-                } else if (p.epilog == EPI_GELU_AUX_BIAS) {
+                } else if (epilog == EPI_GELU_AUX_BIAS) {
                     uint16_t* pre16 = static_cast<uint16_t*>(p.aux);
 #pragma unroll
                     for (int j = 0; j < CH; ++j)
                         if (col_ok && t0 + j < p.m)
                             pre16[static_cast<long long>(t0 + j) * p.n + col] = to16(v[j], p.bf16);
-                } else if (p.epilog == EPI_DRELU_BGRAD) {
+                } else if (epilog == EPI_DRELU_BGRAD) {
                     // lane j < CH fetches the mask word of row t0 + j; bit `lane` of it
                     uint32_t mrow = 0;
                     if (lane < CH && t0 + lane < p.m && word_idx < p.aux_ld)
@@ -804,7 +810,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                         const uint32_t mw = __shfl_sync(0xFFFFFFFFu, mrow, j);
                         v[j] = (col_ok && ((mw >> lane) & 1u)) ? v[j] : 0.0f;
                     }
-                } else if (p.epilog == EPI_DGELU_BGRAD) {
+                } else if (epilog == EPI_DGELU_BGRAD) {
 #pragma unroll
                     for (int j = 0; j < CH; ++j) {
                         float g = 0.0f;
@@ -814,8 +820,8 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                         v[j] *= g;
                     }
                 }
-                activate(v, p.epilog);
-                if (p.epilog == EPI_BIAS_RESIDUAL) {
+                activate(v, epilog);
+                if (epilog == EPI_BIAS_RESIDUAL) {
 #pragma unroll
                     for (int j = 0; j < CH; ++j)
                         if (col_ok && t0 + j < p.m)
@@ -872,7 +878,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
 // ------------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------------
-template <int BN, bool SWAP, bool PAIR = false>
+template <int BN, bool SWAP, bool PAIR = false, int EPI = -1>
 __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_constant__ GemmParams p)
 {
     using C = TileCfg<BN, PAIR>;
@@ -942,7 +948,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         } else if (split) {
             publish_partials<BN, SWAP>(p, smem, bar0, tmem_base, abort_flag);
         } else {
-            run_epilogue<BN, SWAP, PAIR>(p, smem, sbase, bar0, tmem_base, abort_flag);
+            run_epilogue<BN, SWAP, PAIR, EPI>(p, smem, sbase, bar0, tmem_base, abort_flag);
         }
     }
     if (split) {

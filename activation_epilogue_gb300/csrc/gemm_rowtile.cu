@@ -1,5 +1,4 @@
-// Row-tile kernel instantiations: 128 x BN output tiles, BN in {64, 128, 256}, and the
-// CTA-pair kernel with 256 x 256 tiles.
+// Row-tile kernel instantiations: 128 x BN output tiles, BN in {64, 128, 256}.
 #include "gemm_kernel.cuh"
 
 namespace gemm_epi {
@@ -81,62 +80,5 @@ int rowtile_stages(int bn)
     }
 }
 
-
-// ---- CTA pairs -----------------------------------------------------------------------------
-
-cudaError_t rowpair_prepare()
-{
-    return cudaFuncSetAttribute(gemm_epi_kernel<256, false, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                TileCfg<256, true>::kSmemBytes);
-}
-
-cudaError_t rowpair_launch(const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = TileCfg<256, true>::kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    unsigned na = 0;
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = 2;
-    attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = 1;
-    ++na;
-    if (pdl) {
-        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemm_epi_kernel<256, false, true>, p);
-}
-
-int rowpair_smem_bytes() { return TileCfg<256, true>::kSmemBytes; }
-int rowpair_stages() { return TileCfg<256, true>::kStages; }
-
-int rowpair_max_clusters()
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = TileCfg<256, true>::kSmemBytes;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_epi_kernel<256, false, true>, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    return n;
-}
 
 }  // namespace gemm_epi

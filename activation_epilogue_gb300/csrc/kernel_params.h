@@ -87,11 +87,11 @@ int swapped_smem_bytes(int bn);
 int swapped_stages(int bn);
 
 // Row-tile kernel run by CTA pairs (cta_group::2): 256 x 256 tiles, clusters of 2.
-cudaError_t rowpair_prepare();
-cudaError_t rowpair_launch(const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
-int rowpair_smem_bytes();
-int rowpair_stages();
-int rowpair_max_clusters();
+cudaError_t rowpair_prepare(int bn);
+cudaError_t rowpair_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
+int rowpair_smem_bytes(int bn);
+int rowpair_stages(int bn);
+int rowpair_max_clusters(int bn);
 
 
 // Elementwise epilogue over a 16-bit pre-activation (the unfused baseline's second kernel;

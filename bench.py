@@ -479,7 +479,50 @@ def measure_extras(plan, w, A, B, bias, D, aux, stream, peaks):
                        "unfused_launches": 4, "status": fp.sync_status(),
                        "plans": [p1.describe(), p2.describe()]}
     out["workloads"] = per
+    out["backward"] = measure_backward(A.device, stream, flush, peaks)
     return out
+
+
+def measure_backward(device, stream, flush, peaks):
+    """GELU_AUX_BIAS (forward keeping pre) and the backward epilogues DRELU_BGRAD and
+    DGELU_BGRAD on a 4096 x 4096 x 4096 bf16 layer, bias (1,n): fused against unfused
+    (GEMM writing bf16(A.B), then the elementwise pass with the mask or GELU' factor and the
+    bias-gradient sums), cold L2."""
+    import numpy as np
+    import torch
+
+    from activation_epilogue_gb300 import gemm_epi, workloads
+    m = n = k = 4096
+    inp = workloads.random_backward_problem(m, n, k, dtype="bf16", seed=2024, device=device)
+    fw = workloads.random_problem(m, n, k, dtype="bf16", seed=2025, device=device)
+    mask = torch.from_numpy(inp["mask"].view(np.int32)).to(device)
+    D = torch.empty((m, n), dtype=torch.bfloat16, device=device)
+    pre = torch.empty_like(D)
+    aux16 = torch.empty_like(D)
+    dbias = torch.empty((n,), dtype=torch.float32, device=device)
+    flops = 2.0 * m * n * k
+    res = {}
+    for epilog in ["GELU_AUX_BIAS", "DRELU_BGRAD", "DGELU_BGRAD"]:
+        if epilog == "GELU_AUX_BIAS":
+            kw = dict(aux=aux16)
+            bias = fw["bias"]
+            extra = m * n * 2                                  # the stored pre-activation
+        else:
+            kw = dict(aux_in=mask if epilog == "DRELU_BGRAD" else inp["pre"], dbias=dbias)
+            bias = None
+            extra = mask.numel() * 4 if epilog == "DRELU_BGRAD" else m * n * 2
+        with gemm_epi.Plan(m, n, k, "bf16", epilog, "1N") as pl:
+            fn = lambda: pl.execute(inp["A"], inp["B"], bias, D, **kw)  # noqa: E731
+            fu = lambda: pl.execute_unfused(inp["A"], inp["B"], bias, pre, D, **kw)  # noqa: E731
+            cold = time_cold(fn, 20, stream, flush)
+            cold_unf = time_cold(fu, 20, stream, flush)
+            res[epilog] = {"shape": [m, n, k], "us_per_call_cold_l2": cold * 1e6,
+                           "tflops_cold": flops / cold / 1e12,
+                           "tensor_frac_cold": flops / cold / 1e12 / peaks["bf16_tflops"],
+                           "unfused_us_cold_l2": cold_unf * 1e6,
+                           "extra_aux_bytes": extra, "status": pl.sync_status(),
+                           "plan": pl.describe()}
+    return res
 
 
 def main():

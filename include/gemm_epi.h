@@ -117,7 +117,9 @@ typedef enum {
 typedef enum {
     GEMM_EPI_OPT_VARIANT = 0,       /* 1 = row-tile kernel, 2 = swapped small-m kernel,
                                        3 = row-tile kernel run by CTA pairs (256-row tiles) */
-    GEMM_EPI_OPT_TILE_N = 1,        /* row-tile kernel: N tile 64, 128 or 256 */
+    GEMM_EPI_OPT_TILE_N = 1,        /* N tile: 64, 128 or 256 for the row-tile kernel;
+                                       224 or 256 for the CTA-pair kernel (a width
+                                       the chosen kernel lacks is ERR_INVALID_ARG) */
     GEMM_EPI_OPT_SPLIT_K = 2,       /* K slices per output tile, 1..8 (one cluster of that
                                        many CTAs per tile; partial sums added on chip) */
     GEMM_EPI_OPT_GRID = 3,          /* cap on persistent CTAs (<= SM count) */

@@ -91,6 +91,8 @@ VARIANTS = [
     ("rowtile128", 300, 264, 200, {"VARIANT": 1, "TILE_N": 128}),
     ("rowtile256", 300, 520, 136, {"VARIANT": 1, "TILE_N": 256}),
     ("pair", 600, 520, 200, {"VARIANT": 3}),
+    ("pair224", 600, 520, 200, {"VARIANT": 3, "TILE_N": 224}),
+    ("pair224_ragged", 520, 600, 136, {"VARIANT": 3, "TILE_N": 224}),
     ("swapped1", 1, 264, 136, {"VARIANT": 2}),
     ("swapped16", 16, 264, 136, {"VARIANT": 2}),
     ("swapped40", 40, 392, 200, {"VARIANT": 2}),

@@ -352,14 +352,32 @@ def test_programmatic_launch_sees_preceding_writes(variant):
 
 # ---- the CTA-pair row-tile kernel (cta_group::2, 256 x 256 tiles) -----------------------------
 
+@pytest.mark.parametrize("bn", [256, 224])
 @pytest.mark.parametrize("epilog", EPILOGS)
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_pair_parity(epilog, dtype):
-    m, n, k = 600, 520, 200            # 3 ragged 256-row tiles, 3 ragged 256-column tiles
-    layout = "M1" if EPILOGS.index(epilog) % 2 else "1N"
-    p = _inputs(m, n, k, dtype, layout, seed=61 + EPILOGS.index(epilog))
-    _, _, _, _, desc = check(p, m, n, k, dtype, epilog, layout, options={"VARIANT": 3})
-    assert "variant=row-pair" in desc
+def test_pair_parity(bn, epilog, dtype):
+    m, n, k = 600, 520, 200            # 3 ragged 256-row tiles, 3 ragged column tiles
+    layout = "M1" if (EPILOGS.index(epilog) + bn // 32) % 2 else "1N"
+    p = _inputs(m, n, k, dtype, layout, seed=61 + EPILOGS.index(epilog) + bn)
+    _, _, _, _, desc = check(p, m, n, k, dtype, epilog, layout,
+                             options={"VARIANT": 3, "TILE_N": bn})
+    assert "variant=row-pair" in desc and f"tile=256x{bn} " in desc
+
+
+@pytest.mark.parametrize("m,n,want", [(4096, 4096, 224), (8192, 16384, 256), (65536, 16384, 256),
+                                      (4096, 1024, 256)])
+def test_pair_tile_width_choice(m, n, want):
+    """The planner trades tile width against wave quantization over the resident pairs."""
+    with gemm_epi.Plan(m, n, 1024, "bf16", "RELU_BIAS", "1N") as plan:
+        desc = plan.describe()
+    assert "variant=row-pair" in desc and f"tile=256x{want} " in desc, desc
+
+
+def test_pair_narrow_tile_persistent_walk():
+    m, n, k = 1280, 1000, 264          # 5 x 5 tiles of 256 x 224, 5 K blocks, 3 pairs walking
+    p = _inputs(m, n, k, "bf16", "1N", seed=88)
+    check(p, m, n, k, "bf16", "RELU_AUX_BIAS", "1N",
+          options={"VARIANT": 3, "TILE_N": 224, "GRID": 6, "GROUP_M": 2})
 
 
 @pytest.mark.parametrize("grid,group_m", [(2, 1), (4, 2), (6, 8)])
