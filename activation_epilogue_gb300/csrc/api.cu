@@ -638,6 +638,8 @@ const char* gemm_epi_status_string(gemm_epi_status s)
 
 const char* gemm_epi_plan_describe(gemm_epi_plan_t p) { return p ? p->desc : ""; }
 
+}  // extern "C"
+
 // ---- the FFN block ----------------------------------------------------------------------
 
 struct gemm_epi_ffn_plan_s {
@@ -646,7 +648,156 @@ struct gemm_epi_ffn_plan_s {
     gemm_epi_plan_t g1;  // H = GELU(X.W1 + b1):   t x f, k = d
     gemm_epi_plan_t g2;  // Y = H.W2 + b2 + R:     t x d, k = f
     void* H;
+    // one-launch mode: both GEMMs in one CTA-pair kernel (256 x 256 tiles)
+    int opt_launches;  // GEMM_EPI_FFN_OPT_LAUNCHES value (0 = automatic)
+    bool one_launch;   // the mode in use
+    int* ready;        // per 256-row block of H: epilogue warps done with it
+    int tiles_m, tiles_n1, tiles_n2, grid;
+    const void* key_X;
+    const void* key_W1;
+    const void* key_W2;
+    const void* key_Y;
+    bool maps_valid;
+    CUtensorMap tm_X, tm_W1, tm_Hs, tm_Hl, tm_W2, tm_Y;
+    char desc[400];
 };
+
+namespace {
+
+// One launch pays off on long walks: there the second GEMM's K loops run beside the first
+// GEMM's last tiles and their GELU epilogues instead of after them.  Measured on GB300
+// (bf16, hot L2): t x d x f = 8192 x 1024 x 4096, 640 tiles of 256 x 256: 100.8 us in one
+// launch, 102.7 us in two; 4096 x 2048 x 8192: 170.6 against 173.8 us; but 4096 x 1024 x 4096,
+// 320 tiles: 65.6 against 60.5 us, where the two-launch plan's 224-wide first GEMM fills
+// its four waves exactly.  So: one launch from six waves of tiles over the resident pairs.
+bool pick_one_launch(const gemm_epi_ffn_plan_s* p, long long pairs)
+{
+    if (p->opt_launches == 1) return true;
+    if (p->opt_launches == 2) return false;
+    if (p->g1->variant != kRowPair || p->g2->variant != kRowPair) return false;
+    const long long tiles = ((p->t + 255) / 256) * ((p->f + 255) / 256 + (p->d + 255) / 256);
+    return tiles >= 6 * pairs;
+}
+
+gemm_epi_status configure_ffn(gemm_epi_ffn_plan_s* p)
+{
+    p->maps_valid = false;
+    p->tiles_m = static_cast<int>((p->t + 255) / 256);
+    p->tiles_n1 = static_cast<int>((p->f + 255) / 256);
+    p->tiles_n2 = static_cast<int>((p->d + 255) / 256);
+    p->grid = 0;
+    if (ffn_pair_prepare() != cudaSuccess || rowpair_prepare(256) != cudaSuccess)
+        return GEMM_EPI_ERR_LAUNCH;
+    long long pairs = rowpair_max_clusters(256);
+    if (pairs > p->g1->sm_count / 2) pairs = p->g1->sm_count / 2;
+    p->one_launch = p->t > 0 && p->d > 0 && p->f > 0 && pick_one_launch(p, pairs);
+    if (p->one_launch) {
+        const long long tiles = static_cast<long long>(p->tiles_m) * (p->tiles_n1 + p->tiles_n2);
+        if (pairs > tiles) pairs = tiles;
+        if (pairs < 1) return GEMM_EPI_ERR_LAUNCH;
+        p->grid = static_cast<int>(2 * pairs);
+        if (!p->ready && cudaMalloc(reinterpret_cast<void**>(&p->ready),
+                                    sizeof(int) * static_cast<size_t>(p->tiles_m)) != cudaSuccess) {
+            cudaGetLastError();
+            p->ready = nullptr;
+            return GEMM_EPI_ERR_ALLOC;
+        }
+        snprintf(p->desc, sizeof(p->desc),
+                 "one launch: t=%lld d=%lld f=%lld, CTA pairs on 256x256 tiles: %dx%d GEMM-1 tiles "
+                 "then %dx%d GEMM-2 tiles, grid=%d",
+                 static_cast<long long>(p->t), static_cast<long long>(p->d),
+                 static_cast<long long>(p->f), p->tiles_m, p->tiles_n1, p->tiles_m, p->tiles_n2,
+                 p->grid);
+    } else {
+        snprintf(p->desc, sizeof(p->desc), "two launches: [%s] then [%s]", p->g1->desc,
+                 p->g2->desc);
+    }
+    return GEMM_EPI_OK;
+}
+
+gemm_epi_status ensure_ffn_maps(gemm_epi_ffn_plan_s* p, const void* X, const void* W1,
+                                const void* W2, void* Y)
+{
+    if (p->maps_valid && p->key_X == X && p->key_W1 == W1 && p->key_W2 == W2 && p->key_Y == Y)
+        return GEMM_EPI_OK;
+    p->maps_valid = false;
+    const CUtensorMapDataType dt = p->dtype == GEMM_EPI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint64_t t = static_cast<uint64_t>(p->t), d = static_cast<uint64_t>(p->d),
+                   f = static_cast<uint64_t>(p->f);
+    const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B, sw64 = CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!encode_2d(&p->tm_X, X, dt, d, t, 64, 128, sw128) ||
+        !encode_2d(&p->tm_W1, W1, dt, f, d, 64, 64, sw128) ||
+        !encode_2d(&p->tm_Hs, p->H, dt, f, t, 32, 32, sw64) ||
+        !encode_2d(&p->tm_Hl, p->H, dt, f, t, 64, 128, sw128) ||
+        !encode_2d(&p->tm_W2, W2, dt, d, f, 64, 64, sw128) ||
+        !encode_2d(&p->tm_Y, Y, dt, d, t, 32, 32, sw64))
+        return GEMM_EPI_ERR_LAUNCH;
+    p->key_X = X;
+    p->key_W1 = W1;
+    p->key_W2 = W2;
+    p->key_Y = Y;
+    p->maps_valid = true;
+    return GEMM_EPI_OK;
+}
+
+gemm_epi_status run_ffn_one_launch(gemm_epi_ffn_plan_s* p, const void* X, const void* W1,
+                                   const void* b1, const void* W2, const void* b2, const void* R,
+                                   void* Y, cudaStream_t stream)
+{
+    gemm_epi_status st = ensure_ffn_maps(p, X, W1, W2, Y);
+    if (st != GEMM_EPI_OK) return st;
+    if (cudaMemsetAsync(p->ready, 0, sizeof(int) * static_cast<size_t>(p->tiles_m), stream) !=
+        cudaSuccess)
+        return GEMM_EPI_ERR_LAUNCH;
+    const gemm_epi_plan_s* g1 = p->g1;
+    GemmParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.tm_A = p->tm_X;
+    prm.tm_B = p->tm_W1;
+    prm.tm_D = p->tm_Hs;
+    prm.bias = b1;
+    prm.D = p->H;
+    prm.status = g1->d_status;
+    prm.wait_limit_ns = g1->wait_limit_ns;
+    prm.m = static_cast<int>(p->t);
+    prm.n = static_cast<int>(p->f);
+    prm.k = static_cast<int>(p->d);
+    prm.tiles_m = p->tiles_m;
+    prm.tiles_n = p->tiles_n1;
+    prm.k_blocks = static_cast<int>((p->d + 63) / 64);
+    prm.group_m = p->tiles_m < 8 ? p->tiles_m : 8;
+    prm.epilog = EPI_GELU_BIAS;
+    prm.bias_layout = GEMM_EPI_BIAS_1N;
+    prm.bf16 = p->dtype == GEMM_EPI_BF16 ? 1 : 0;
+    prm.aux_ld = static_cast<int>((p->f + 31) / 32);
+    prm.split = 1;
+    prm.kb_per_split = prm.k_blocks;
+    prm.tm_A2 = p->tm_Hl;
+    prm.tm_B2 = p->tm_W2;
+    prm.tm_D2 = p->tm_Y;
+    prm.bias2 = b2;
+    prm.residual2 = R;
+    prm.ffn_ready = p->ready;
+    prm.ffn_ready_target = p->tiles_n1 * 2 * kEpilogueWarps;
+    prm.ffn_tiles2 = p->tiles_m * p->tiles_n2;
+    prm.n2 = static_cast<int>(p->d);
+    prm.tiles_n2 = p->tiles_n2;
+    prm.k_blocks2 = static_cast<int>((p->f + 63) / 64);
+    const cudaError_t e = ffn_pair_launch(prm, p->grid, stream);
+    if (e != cudaSuccess) {
+        const char* log = getenv("GEMM_EPI_LOG");
+        if (log && log[0] == '1')
+            fprintf(stderr, "[gemm_epi] FFN launch failed: %s (%s)\n", cudaGetErrorString(e),
+                    p->desc);
+        return GEMM_EPI_ERR_LAUNCH;
+    }
+    return GEMM_EPI_OK;
+}
+
+}  // namespace
+
+extern "C" {
 
 gemm_epi_status gemm_epi_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d, int64_t f,
                                   gemm_epi_dtype dtype)
@@ -674,18 +825,39 @@ gemm_epi_status gemm_epi_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d
     p->g1 = g1;
     p->g2 = g2;
     p->H = nullptr;
+    p->ready = nullptr;
     if (t > 0 && f > 0) {
         if (cudaMalloc(&p->H, static_cast<size_t>(t) * static_cast<size_t>(f) * 2) != cudaSuccess) {
             cudaGetLastError();
-            gemm_epi_free(g1);
-            gemm_epi_free(g2);
-            delete p;
+            gemm_epi_ffn_free(p);
             return GEMM_EPI_ERR_ALLOC;
         }
+    }
+    st = configure_ffn(p);
+    if (st != GEMM_EPI_OK) {
+        gemm_epi_ffn_free(p);
+        return st;
     }
     *out = p;
     return GEMM_EPI_OK;
 }
+
+gemm_epi_status gemm_epi_ffn_set_option(gemm_epi_ffn_plan_t p, gemm_epi_ffn_option opt,
+                                        int64_t value)
+{
+    if (!p) return GEMM_EPI_ERR_INVALID_ARG;
+    if (opt != GEMM_EPI_FFN_OPT_LAUNCHES || value < 0 || value > 2) return GEMM_EPI_ERR_INVALID_ARG;
+    const int saved = p->opt_launches;
+    p->opt_launches = static_cast<int>(value);
+    gemm_epi_status st = configure_ffn(p);
+    if (st != GEMM_EPI_OK) {
+        p->opt_launches = saved;
+        configure_ffn(p);
+    }
+    return st;
+}
+
+const char* gemm_epi_ffn_plan_describe(gemm_epi_ffn_plan_t p) { return p ? p->desc : ""; }
 
 gemm_epi_status gemm_epi_ffn_execute(gemm_epi_ffn_plan_t p, const void* X, const void* W1,
                                      const void* b1, const void* W2, const void* b2,
@@ -701,6 +873,7 @@ gemm_epi_status gemm_epi_ffn_execute(gemm_epi_ffn_plan_t p, const void* X, const
     if (p->t == 0 || p->d == 0) return GEMM_EPI_OK;
     st = check_device(p->g1);
     if (st != GEMM_EPI_OK) return st;
+    if (p->one_launch) return run_ffn_one_launch(p, X, W1, b1, W2, b2, R, Y, stream);
     st = run_plan(p->g1, o1, stream, true);
     if (st != GEMM_EPI_OK) return st;
     // GEMM 2 reads H only after GEMM 1 has completed (griddepcontrol.wait in its producer).
@@ -721,6 +894,7 @@ gemm_epi_status gemm_epi_ffn_free(gemm_epi_ffn_plan_t p)
 {
     if (!p) return GEMM_EPI_OK;
     if (p->H) cudaFree(p->H);
+    if (p->ready) cudaFree(p->ready);
     gemm_epi_free(p->g1);
     gemm_epi_free(p->g2);
     delete p;

@@ -1,0 +1,71 @@
+"""Fit of the logistic approximation of the standard normal CDF used by the GELU epilogue.
+
+    Phi(x) ~= 1 / (1 + exp(-P(x))),   P(x) = c1 x + c3 x^3 + c5 x^5,   |x| clamped to 8,
+
+the functional form of Bowling, Khasawneh, Kaewkuekool and Cho, "A logistic approximation to
+the cumulative normal distribution", J. Industrial Engineering and Management 2(1), 2009
+(who fit c1 x + c3 x^3), with the x^5 term added and the coefficients refitted here.  P is
+odd, so Phi(-x) = 1 - Phi(x) holds exactly and x < 0 needs no separate branch.  The fit is
+minimax on [0, 8] of |error of Phi| * max(1, |x|): the error GELU(x) = x Phi(x) inherits.
+For |x| >= 8 the true Phi is within 7e-16 of 0 or 1 and P(8) > 28, so the clamp costs
+nothing visible (the x^5 coefficient is negative and P would turn over near |x| = 11).
+
+Run it to reprint the constants that gelu.cuh holds (scipy, numpy; about a minute):
+
+    python activation_epilogue_gb300/csrc/fit_gelu_logistic.py
+"""
+import numpy as np
+from scipy.optimize import minimize
+from scipy.special import ndtr
+
+CLAMP = 8.0
+
+
+def weighted_error(c, xs, phi):
+    p = xs * (c[0] + xs * xs * (c[1] + xs * xs * c[2]))
+    return np.max(np.abs(1.0 / (1.0 + np.exp(-p)) - phi) * np.maximum(1.0, xs))
+
+
+def fit():
+    xs = np.linspace(0.0, CLAMP, 80001)
+    phi = ndtr(xs)
+    best = None
+    rng = np.random.default_rng(0)
+    for trial in range(12):
+        c0 = np.array([1.5976, 0.07056, 0.0]) * (1.0 + (0.05 * rng.standard_normal(3) if trial else 0))
+        r = minimize(weighted_error, c0, args=(xs, phi), method="Nelder-Mead",
+                     options={"maxiter": 40000, "xatol": 1e-14, "fatol": 1e-16})
+        r = minimize(weighted_error, r.x, args=(xs, phi), method="Nelder-Mead",
+                     options={"maxiter": 40000, "xatol": 1e-14, "fatol": 1e-16})
+        if best is None or r.fun < best.fun:
+            best = r
+    return best.x, best.fun
+
+
+def float32_gelu(x, c):
+    """The kernel's arithmetic in float32 (exp and the division exact here; the hardware
+    ex2.approx and fast division add about 2^-22 relative)."""
+    f = np.float32
+    x = np.asarray(x, np.float32)
+    xc = np.clip(x, f(-CLAMP), f(CLAMP))
+    x2 = xc * xc
+    k = -1.0 / np.log(2.0)  # exp(-P) = 2^(-P log2 e)
+    c5, c3, c1 = (f(ci * k) for ci in (c[2], c[1], c[0]))
+    p = np.float32(x2 * c5 + c3)
+    p = np.float32(p * x2 + c1)
+    e = np.exp2(np.float64(xc * p)).astype(np.float32)
+    return x / (f(1.0) + e)
+
+
+if __name__ == "__main__":
+    c, err = fit()
+    print("c1, c3, c5 =", float(c[0]), float(c[1]), float(c[2]))
+    print("max |Phi error| * max(1, |x|) on [0, 8] =", err)
+    k = -1.0 / np.log(2.0)
+    print("with -log2(e) folded in (the constants in gelu.cuh):",
+          [float(np.float32(ci * k)) for ci in c])
+    xs = np.linspace(-40.0, 40.0, 2000001)
+    g = float32_gelu(xs, c).astype(np.float64)
+    want = xs * ndtr(xs)
+    print("float32 GELU: max |error| / max(1, |x|) on [-40, 40] =",
+          np.max(np.abs(g - want) / np.maximum(1.0, np.abs(xs))))

@@ -50,7 +50,7 @@ namespace gemm_epi {
 constexpr int kBM = 128;        // MMA M: TMEM lanes
 constexpr int kBK = 64;         // K block: one 128-byte swizzle row of 16-bit elements
 constexpr int kUmmaK = 16;      // K of one tcgen05.mma.kind::f16
-constexpr int kEpiWarps = 8;    // two per TMEM lane quarter, alternating chunks
+constexpr int kEpiWarps = kEpilogueWarps;  // two per TMEM lane quarter, alternating chunks
 constexpr int kThreads = 64 + 32 * kEpiWarps;   // producer, MMA, epilogue warps
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kPipeBudget = 192 * 1024;
@@ -151,7 +151,7 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
         // persistent CTA pairs (clusters of 2) walking 256-row tiles
         w.first = static_cast<int>(cluster_id_x());
         w.stride = static_cast<int>(gridDim.x / 2);
-        w.end = p.tiles_m * p.tiles_n;
+        w.end = p.tiles_m * p.tiles_n + p.ffn_tiles2;
         w.rank = 0;
         w.split = 1;
         w.pair_rank = static_cast<int>(cluster_ctarank());
@@ -178,6 +178,53 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
         w.kb_end = p.k_blocks;
     }
     return w;
+}
+
+// One tile of the walk: which GEMM (0, or 1 = the second GEMM of a fused FFN block), its
+// coordinates and its last K block.
+struct TileInfo {
+    int prob, tm, tn, kb_end;
+};
+
+template <bool FFN>
+__device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int tile, const WorkRange& w)
+{
+    TileInfo t;
+    const int tiles1 = p.tiles_m * p.tiles_n;
+    if (!FFN || tile < tiles1) {
+        tile_coords(tile, p, t.tm, t.tn);
+        t.prob = 0;
+        t.kb_end = w.kb_end;
+    } else {
+        // GEMM 2 in row order: the row blocks of H finish roughly in that order
+        const int u = tile - tiles1;
+        t.tm = u / p.tiles_n2;
+        t.tn = u - t.tm * p.tiles_n2;
+        t.prob = 1;
+        t.kb_end = p.k_blocks2;
+    }
+    return t;
+}
+
+// FFN: wait until the row block of H a GEMM-2 tile reads is complete (bounded like the
+// mbarrier waits; false on abort or time-out).  The acquire load orders the TMA loads that
+// follow (after a proxy fence) behind the GEMM-1 stores it observes.
+__device__ __forceinline__ bool wait_ffn_ready(const GemmParams& p, int tm,
+                                               const volatile int* abort_flag)
+{
+    const int* flag = p.ffn_ready + tm;
+    if (ld_acquire_gpu(flag) >= p.ffn_ready_target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    const unsigned long long max_polls = p.wait_limit_ns / 32 + 1024;
+    for (unsigned long long poll = 1; poll < max_polls; ++poll) {
+        __nanosleep(32);
+        if (ld_acquire_gpu(flag) >= p.ffn_ready_target) return true;
+        if ((poll & 15) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > p.wait_limit_ns) return false;
+        }
+    }
+    return false;
 }
 
 // Byte offset, in the partial-tile buffer, of 16-byte unit `unit` (4 fp32 columns) of
@@ -227,7 +274,7 @@ __device__ __forceinline__ uint16_t to16(float a, int bf16)
 // Arm stage `stage` for K block `kb` of tile (tm, tn) and issue its TMA loads.
 template <int BN, bool SWAP, bool PAIR = false>
 __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase, uint32_t bar0,
-                                            int stage, int tm, int tn, int kb)
+                                            int stage, int tm, int tn, int kb, int prob = 0)
 {
     using C = TileCfg<BN, PAIR>;
     const uint32_t fb = bar0 + 8u * (kBarFull + stage);
@@ -241,10 +288,12 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase,
         const uint32_t rank = cluster_ctarank();
         if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::kStageBytes);
         const uint32_t fb0 = map_shared_rank(fb, 0);
-        tma_load_2d_pair(sa, &p.tm_A, fb0, k0, tm * 2 * kBM + static_cast<int>(rank) * kBM);
+        const CUtensorMap* mA = prob ? &p.tm_A2 : &p.tm_A;
+        const CUtensorMap* mB = prob ? &p.tm_B2 : &p.tm_B;
+        tma_load_2d_pair(sa, mA, fb0, k0, tm * 2 * kBM + static_cast<int>(rank) * kBM);
 #pragma unroll
         for (int q = 0; q < C::kBRows / 64; ++q)
-            tma_load_2d_pair(sb + q * 8192, &p.tm_B, fb0,
+            tma_load_2d_pair(sb + q * 8192, mB, fb0,
                              tn * BN + static_cast<int>(rank) * (BN / 2) + q * 64, k0);
         return;
     }
@@ -299,7 +348,7 @@ __device__ __forceinline__ int producer_prologue(const GemmParams& p, uint32_t s
 }
 
 // The producer loop, continuing after the `pre` stages the prologue issued.
-template <int BN, bool SWAP, bool PAIR = false>
+template <int BN, bool SWAP, bool PAIR = false, bool FFN = false>
 __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase, uint32_t bar0,
                                              volatile int* abort_flag, int pre)
 {
@@ -311,18 +360,25 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
     bool ok = true;
     grid_dependency_wait();
     for (int tile = w.first; ok && tile < w.end; tile += w.stride) {
-        int tm, tn;
-        tile_coords(tile, p, tm, tn);
-        for (int kb = (tile == w.first ? w.kb_begin + pre : w.kb_begin); kb < w.kb_end; ++kb) {
+        const TileInfo t = tile_info<FFN>(p, tile, w);
+        if (FFN && t.prob == 1) {
+            if (!wait_ffn_ready(p, t.tm, abort_flag)) {
+                if (!*abort_flag) record_failure(p.status, abort_flag, kRoleProducer);
+                ok = false;
+                break;
+            }
+            fence_proxy_async_global();
+        }
+        for (int kb = (tile == w.first ? w.kb_begin + pre : w.kb_begin); kb < t.kb_end; ++kb) {
             if (!wait_bounded(bar0 + 8u * (kBarEmpty + stage), phase ^ 1u, abort_flag,
                               p.wait_limit_ns)) {
                 if (!*abort_flag) record_failure(p.status, abort_flag, kRoleProducer);
                 ok = false;
                 break;
             }
-            issue_stage<BN, SWAP, PAIR>(p, sbase, bar0, stage, tm, tn, kb);
-            if (!PAIR && p.prefetch && kb + p.prefetch < w.kb_end)
-                prefetch_stage<BN, SWAP>(p, tm, tn, kb + p.prefetch);
+            issue_stage<BN, SWAP, PAIR>(p, sbase, bar0, stage, t.tm, t.tn, kb, t.prob);
+            if (!PAIR && p.prefetch && kb + p.prefetch < t.kb_end)
+                prefetch_stage<BN, SWAP>(p, t.tm, t.tn, kb + p.prefetch);
             ++issued;
             if (++stage == C::kStages) {
                 stage = 0;
@@ -346,7 +402,7 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
 // ------------------------------------------------------------------------------------------
 // MMA issuer
 // ------------------------------------------------------------------------------------------
-template <int BN, bool SWAP, bool PAIR = false>
+template <int BN, bool SWAP, bool PAIR = false, bool FFN = false>
 __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uint32_t bar0,
                                         uint32_t tmem_base, volatile int* abort_flag)
 {
@@ -373,7 +429,8 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
         }
         tcgen05_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+        const int kb_end = tile_info<FFN>(p, tile, w).kb_end;
+        for (int kb = w.kb_begin; kb < kb_end; ++kb) {
             if (!wait_bounded(bar0 + 8u * (kBarFull + stage), phase, abort_flag,
                               p.wait_limit_ns)) {
                 if (!*abort_flag) record_failure(p.status, abort_flag, kRoleMma);
@@ -587,7 +644,9 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                                              uint32_t bar0, uint32_t tmem_base,
                                              volatile int* abort_flag)
 {
-    const int epilog = EPI >= 0 ? EPI : p.epilog;
+    // The FFN kernel runs GELU_BIAS on GEMM-1 tiles and BIAS_RESIDUAL on GEMM-2 tiles.
+    constexpr bool FFN = EPI == kEpiFfn;
+    const int epilog0 = FFN ? EPI_GELU_BIAS : (EPI >= 0 ? EPI : p.epilog);
     using C = TileCfg<BN, PAIR>;
     constexpr int CH = C::kChunk;
     const int warp = threadIdx.x >> 5;
@@ -596,28 +655,33 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
     const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
     const int half = ew >> 2;            // the pair's warps take alternate chunks
     const WorkRange w = work_range<PAIR>(p);
-    const bool bwd = is_backward(epilog);
-    const bool has_bias = epilog != EPI_NONE && !bwd;
-    // Bias (and, backward, bias gradient) that varies along the accumulator's columns
-    // (staged in shared memory; column sums) or along its lanes (one value per thread).
-    const bool along_cols = SWAP ? p.bias_layout == 0 : p.bias_layout == 1;
-    const bool col_bias = has_bias && along_cols;
-    const bool lane_bias = has_bias && !col_bias;
-    const int col_limit = SWAP ? p.m : p.n;   // extent of the accumulator-column coordinate
-    const int lane_limit = SWAP ? p.n : p.m;  // extent of the accumulator-lane coordinate
     // This warp's own bias staging area: no other warp reads it, so a __syncwarp orders it.
     float* sbias = reinterpret_cast<float*>(smem + C::kOffBias) + ew * 256;
     uint8_t* epi_buf = smem + C::kOffEpi + ew * 2048;
     const uint32_t epi_buf_u32 = sbase + C::kOffEpi + ew * 2048;
-    const uint16_t* R = static_cast<const uint16_t*>(p.residual);
     // Bias, residual and the outputs may belong to a programmatic predecessor grid.
     grid_dependency_wait();
 
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = w.first; tile < w.end; tile += w.stride) {
-        int tm, tn;
-        tile_coords(tile, p, tm, tn);
+        const TileInfo t = tile_info<FFN>(p, tile, w);
+        const int tm = t.tm, tn = t.tn;
+        const bool second = FFN && t.prob == 1;  // GEMM 2 of the FFN block
+        const int epilog = second ? static_cast<int>(EPI_BIAS_RESIDUAL) : epilog0;
+        const int ncols = second ? p.n2 : p.n;    // columns of this tile's output
+        const void* bias_ptr = second ? p.bias2 : p.bias;
+        const uint16_t* R = static_cast<const uint16_t*>(second ? p.residual2 : p.residual);
+        const CUtensorMap* tmD = second ? &p.tm_D2 : &p.tm_D;
+        const bool bwd = is_backward(epilog);
+        const bool has_bias = epilog != EPI_NONE && !bwd;
+        // Bias (and, backward, bias gradient) that varies along the accumulator's columns
+        // (staged in shared memory; column sums) or along its lanes (one value per thread).
+        const bool along_cols = SWAP ? p.bias_layout == 0 : p.bias_layout == 1;
+        const bool col_bias = has_bias && along_cols;
+        const bool lane_bias = has_bias && !col_bias;
+        const int col_limit = SWAP ? p.m : ncols;   // extent of the accumulator-column coordinate
+        const int lane_limit = SWAP ? ncols : p.m;  // extent of the accumulator-lane coordinate
         const int col_base = tn * BN;                          // first accumulator column
         // this warp's first lane coordinate (a pair's odd CTA holds rows 128..255 of the tile)
         const int lane_base = PAIR ? tm * 2 * kBM + w.pair_rank * kBM + quarter * 32
@@ -626,7 +690,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         if (*abort_flag) break;
         if (col_bias) {
             __syncwarp();  // every lane is done reading the previous tile's values
-            const uint16_t* bsrc = static_cast<const uint16_t*>(p.bias) + col_base;
+            const uint16_t* bsrc = static_cast<const uint16_t*>(bias_ptr) + col_base;
             if (col_base + BN <= col_limit && (reinterpret_cast<uintptr_t>(bsrc) & 15) == 0) {
                 // whole tile in range and 16-byte aligned: one 8-element load per lane
                 for (int i8 = lane; i8 < BN / 8; i8 += 32) {
@@ -648,14 +712,26 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
             } else {
                 for (int i = lane; i < BN; i += 32) {
                     const int c = col_base + i;
-                    sbias[i] = c < col_limit ? load_16bit(p.bias, c, p.bf16) : 0.0f;
+                    sbias[i] = c < col_limit ? load_16bit(bias_ptr, c, p.bf16) : 0.0f;
                 }
             }
             __syncwarp();
         }
-        const float lb = (lane_bias && lane_idx < lane_limit) ? load_16bit(p.bias, lane_idx, p.bf16)
+        const float lb = (lane_bias && lane_idx < lane_limit) ? load_16bit(bias_ptr, lane_idx, p.bf16)
                                                               : 0.0f;
 
+        const int valid_cols = min(BN, col_limit - col_base);
+        const int nchunks = (valid_cols + CH - 1) / CH;
+        if (!SWAP && (epilog == EPI_BIAS_RESIDUAL || epilog == EPI_DGELU_BGRAD) &&
+            lane_idx < lane_limit) {
+            // While the MMAs of the tile finish, bring this thread's row segments of the
+            // 16-bit per-element input (residual, or stored pre-activation) into L2.
+            const uint16_t* src = epilog == EPI_BIAS_RESIDUAL
+                                      ? R
+                                      : static_cast<const uint16_t*>(p.aux_in);
+            for (int c = w.rank + half * w.split; c < nchunks; c += 2 * w.split)
+                prefetch_global_l2(src + static_cast<long long>(lane_idx) * ncols + col_base + c * CH);
+        }
         if (!wait_bounded(bar0 + 8u * (kBarTmemFull + acc), acc_phase, abort_flag,
                           p.wait_limit_ns)) {
             if (!*abort_flag) record_failure(p.status, abort_flag, kRoleEpilogue);
@@ -664,12 +740,26 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         tcgen05_fence_after_sync();
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                 static_cast<uint32_t>(acc * BN);
-        const int valid_cols = min(BN, col_limit - col_base);
-        const int nchunks = (valid_cols + CH - 1) / CH;
         const bool warp_live = lane_base < lane_limit;
         float lane_sum = 0.0f;  // backward, bias gradient along the lanes: this tile's sum
 
         for (int c = w.rank + half * w.split; c < nchunks; c += 2 * w.split) {
+            // Row-tile residual: this thread's 32 values, requested before the TMEM read so
+            // that the load latency overlaps it.
+            uint4 rres[4];
+            bool rfull = false;
+            if constexpr (!SWAP && CH == 32) {
+                if (epilog == EPI_BIAS_RESIDUAL) {
+                    const int col0 = col_base + c * CH;
+                    rfull = lane_idx < p.m && col0 + CH <= ncols;
+                    if (rfull) {
+                        const uint4* rp = reinterpret_cast<const uint4*>(
+                            R + static_cast<long long>(lane_idx) * ncols + col0);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) rres[q] = __ldg(rp + q);
+                    }
+                }
+            }
             uint32_t r[32];
             __syncwarp();
             if constexpr (CH == 32)
@@ -732,11 +822,11 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                 }
                 activate(v, epilog);
                 if (epilog == EPI_BIAS_RESIDUAL && row < p.m) {
-                    const uint16_t* rrow = R + static_cast<long long>(row) * p.n + col0;
-                    if (col0 + CH <= p.n) {
+                    const uint16_t* rrow = R + static_cast<long long>(row) * ncols + col0;
+                    if (rfull) {
 #pragma unroll
                         for (int j8 = 0; j8 < CH / 8; ++j8) {
-                            const uint4 w = __ldg(reinterpret_cast<const uint4*>(rrow) + j8);
+                            const uint4 w = rres[j8];
                             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                             for (int h = 0; h < 4; ++h) {
@@ -755,7 +845,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                     } else {
 #pragma unroll
                         for (int j = 0; j < CH; ++j)
-                            if (col0 + j < p.n) v[j] += load_16bit(rrow, j, p.bf16);
+                            if (col0 + j < ncols) v[j] += load_16bit(rrow, j, p.bf16);
                     }
                 }
                 if (warp_live) {
@@ -776,7 +866,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&p.tm_D, epi_buf_u32, col0, lane_base);
+                        tma_store_2d(tmD, epi_buf_u32, col0, lane_base);
                         bulk_commit_group();
                     }
                 }
@@ -868,6 +958,16 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
             mbar_arrive(bar0 + 8u * (kBarTmemEmpty + acc));
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
+        if (FFN && t.prob == 0) {
+            // This warp's stores of the tile's H are complete (not just read from shared
+            // memory): count the warp for the row block, with release semantics.
+            if (lane == 0) {
+                bulk_wait_group<0>();
+                fence_proxy_async_global();
+                red_release_gpu_add(p.ffn_ready + tm, 1);
+            }
+            __syncwarp();
+        }
     }
     // Shared memory may be released once the stores have read it; the grid's writes are
     // complete when the grid is.
@@ -893,10 +993,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     const int lane = threadIdx.x & 31;
     int pre = 0;  // stages the prologue issued (thread 0, which is also the producer)
 
+    constexpr bool FFN = EPI == kEpiFfn;
     if (threadIdx.x == 0) {
         prefetch_tensormap(&p.tm_A);
         prefetch_tensormap(&p.tm_B);
         prefetch_tensormap(&p.tm_D);
+        if (FFN) {
+            prefetch_tensormap(&p.tm_A2);
+            prefetch_tensormap(&p.tm_B2);
+            prefetch_tensormap(&p.tm_D2);
+        }
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar0 + 8u * (kBarFull + s), 1);
             mbar_init(bar0 + 8u * (kBarEmpty + s), 1);
@@ -940,10 +1046,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     const bool split = p.split > 1;
     if (!*abort_flag) {
         if (warp == 0) {
-            if (lane == 0) run_producer<BN, SWAP, PAIR>(p, sbase, bar0, abort_flag, pre);
+            if (lane == 0) run_producer<BN, SWAP, PAIR, FFN>(p, sbase, bar0, abort_flag, pre);
             __syncwarp();
         } else if (warp == 1) {
-            if (lane == 0) run_mma<BN, SWAP, PAIR>(p, sbase, bar0, tmem_base, abort_flag);
+            if (lane == 0) run_mma<BN, SWAP, PAIR, FFN>(p, sbase, bar0, tmem_base, abort_flag);
             __syncwarp();
         } else if (split) {
             publish_partials<BN, SWAP>(p, smem, bar0, tmem_base, abort_flag);

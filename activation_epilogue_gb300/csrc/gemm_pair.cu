@@ -2,7 +2,8 @@
 // cta_group::2 MMAs, one instantiation per epilog.  With the epilog fixed at compile time a
 // kernel carries only its own epilogue code: measured on GB300, the kernel that held every
 // epilog's fully unrolled code stalled its warps on instruction fetch (ncu: no_instruction
-// about 1.3 cycles per issued instruction in the GELU epilogue).
+// about 1.3 cycles per issued instruction in the GELU epilogue).  One more instantiation runs
+// a whole FFN block (GELU GEMM, then bias + residual GEMM) in a single launch.
 #include "gemm_kernel.cuh"
 
 namespace gemm_epi {
@@ -132,6 +133,13 @@ int rowpair_stages(int bn)
     case 256: return TileCfg<256, true>::kStages;
     default: return 0;
     }
+}
+
+cudaError_t ffn_pair_prepare() { return prepare_one<256, kEpiFfn>(); }
+
+cudaError_t ffn_pair_launch(const GemmParams& p, int grid, cudaStream_t stream)
+{
+    return launch_one<256, kEpiFfn>(p, grid, stream, false);
 }
 
 int rowpair_max_clusters(int bn)

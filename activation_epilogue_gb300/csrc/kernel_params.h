@@ -20,6 +20,12 @@ enum Epilog : int {
     EPI_DGELU_BGRAD = 9     // D = A.B * GELU'(aux_in pre), dbias = sums of D
 };
 
+// Template value of the CTA-pair kernel that runs a whole FFN block (two GEMMs) in one launch.
+constexpr int kEpiFfn = 100;
+
+// Epilogue warps per CTA (two per 32-lane quarter of tensor memory).
+constexpr int kEpilogueWarps = 8;
+
 __host__ __device__ constexpr bool is_backward(int epilog)
 {
     return epilog == EPI_DRELU_BGRAD || epilog == EPI_DGELU_BGRAD;
@@ -72,6 +78,20 @@ struct GemmParams {
     // blocks ahead of the one it loads (0 = off), so that a first touch of a panel in
     // device memory overlaps the loads of the blocks before it.
     int prefetch;
+    // FFN block in one launch (CTA-pair kernel, kEpiFfn): tiles [0, tiles_m * tiles_n) are
+    // GEMM 1, H = GELU(X.W1 + b1), described by the fields above (A = X, B = W1, D = H); the
+    // next ffn_tiles2 = tiles_m * tiles_n2 tiles are GEMM 2, Y = H.W2 + b2 + R, with the maps
+    // and sizes below.  A GEMM-2 tile loads its rows of H only once ffn_ready[its row tile]
+    // has reached ffn_ready_target, the number of epilogue warps of both CTAs over the
+    // GEMM-1 tiles of that row block, each of which adds 1 when its stores of H are done.
+    // ffn_tiles2 == 0 for every other launch.
+    CUtensorMap tm_A2, tm_B2, tm_D2;
+    const void* bias2;
+    const void* residual2;
+    int* ffn_ready;
+    int ffn_ready_target;
+    int ffn_tiles2;
+    int n2, tiles_n2, k_blocks2;
 };
 
 // Row-tile kernel (BN in {64, 128, 256}) and swapped small-m kernel (BN in {16 ... 256}).
@@ -92,6 +112,10 @@ cudaError_t rowpair_launch(int bn, const GemmParams& p, int grid, cudaStream_t s
 int rowpair_smem_bytes(int bn);
 int rowpair_stages(int bn);
 int rowpair_max_clusters(int bn);
+
+// The FFN block in one CTA-pair launch (256 x 256 tiles); never a programmatic dependent.
+cudaError_t ffn_pair_prepare();
+cudaError_t ffn_pair_launch(const GemmParams& p, int grid, cudaStream_t stream);
 
 
 // Elementwise epilogue over a 16-bit pre-activation (the unfused baseline's second kernel;

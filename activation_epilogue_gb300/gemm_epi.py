@@ -33,7 +33,9 @@ EXPORTS = ["gemm_epi_plan", "gemm_epi_plan_set_option", "gemm_epi_execute",
            "gemm_epi_aux_words_per_row", "gemm_epi_ffn_plan", "gemm_epi_ffn_execute",
            "gemm_epi_ffn_hidden", "gemm_epi_ffn_sync_status", "gemm_epi_ffn_free",
            "gemm_epi_ffn_execute_noalloc", "gemm_epi_execute_operands",
-           "gemm_epi_execute_operands_unfused"]
+           "gemm_epi_execute_operands_unfused", "gemm_epi_ffn_set_option",
+           "gemm_epi_ffn_plan_describe"]
+FFN_OPTION = {"LAUNCHES": 0}
 
 # Largest t * f the allocation-free FFN call accepts (its static scratch holds H).
 FFN_NOALLOC_MAX_HIDDEN = 16 * 1024 * 1024
@@ -97,6 +99,10 @@ def load_library(path: str | None = None):
         lib.gemm_epi_ffn_execute_noalloc.restype = i32
         lib.gemm_epi_ffn_execute_noalloc.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, vp,
                                                      vp, vp]
+        lib.gemm_epi_ffn_set_option.restype = i32
+        lib.gemm_epi_ffn_set_option.argtypes = [vp, i32, i64]
+        lib.gemm_epi_ffn_plan_describe.restype = ctypes.c_char_p
+        lib.gemm_epi_ffn_plan_describe.argtypes = [vp]
         lib.gemm_epi_execute_operands.restype = i32
         lib.gemm_epi_execute_operands.argtypes = [vp, ctypes.POINTER(Operands), vp]
         lib.gemm_epi_execute_operands_unfused.restype = i32
@@ -221,6 +227,15 @@ def gemm_epi_ffn_execute(plan, X, W1, b1, W2, b2, R, Y, stream=None):
            "gemm_epi_ffn_execute")
 
 
+def gemm_epi_ffn_set_option(plan, option: str, value: int):
+    _check(load_library().gemm_epi_ffn_set_option(plan, FFN_OPTION[option], int(value)),
+           f"gemm_epi_ffn_set_option({option}={value})")
+
+
+def gemm_epi_ffn_plan_describe(plan) -> str:
+    return load_library().gemm_epi_ffn_plan_describe(plan).decode()
+
+
 def gemm_epi_ffn_hidden(plan) -> int:
     return load_library().gemm_epi_ffn_hidden(plan) or 0
 
@@ -246,9 +261,14 @@ def gemm_epi_ffn_execute_noalloc(t: int, d: int, f: int, dtype: str, X, W1, b1, 
 class FfnPlan:
     """The FFN block Y = GELU(X.W1 + b1).W2 + b2 + R as one plan (two fused launches)."""
 
-    def __init__(self, t, d, f, dtype="bf16"):
+    def __init__(self, t, d, f, dtype="bf16", **options):
         self.t, self.d, self.f, self.dtype = t, d, f, dtype
         self.handle = gemm_epi_ffn_plan(t, d, f, dtype)
+        for key, value in options.items():
+            gemm_epi_ffn_set_option(self.handle, key.upper(), value)
+
+    def describe(self) -> str:
+        return gemm_epi_ffn_plan_describe(self.handle)
 
     def execute(self, X, W1, b1, W2, b2, R, Y, stream=None):
         gemm_epi_ffn_execute(self.handle, X, W1, b1, W2, b2, R, Y, stream)

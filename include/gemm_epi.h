@@ -256,7 +256,29 @@ typedef struct gemm_epi_ffn_plan_s* gemm_epi_ffn_plan_t;
 gemm_epi_status gemm_epi_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d, int64_t f,
                                   gemm_epi_dtype dtype);
 
-/* Y = GELU(X.W1 + b1).W2 + b2 + R, asynchronous on `stream`.  Y may be R itself. */
+/* How the plan runs the block (gemm_epi_ffn_set_option). */
+typedef enum {
+    GEMM_EPI_FFN_OPT_LAUNCHES = 0 /* 0 = automatic, 1 = one launch, 2 = two launches.
+                                     One launch: a single persistent kernel of CTA pairs
+                                     (256 x 256 tiles) takes the GEMM-1 tiles first, then
+                                     the GEMM-2 tiles; a GEMM-2 tile starts loading its
+                                     256 rows of H once every GEMM-1 tile of those rows has
+                                     been stored (a per-row-block counter in device memory,
+                                     which the call zeroes on `stream` first), so GEMM 2
+                                     overlaps the end of GEMM 1 and H is read back while it
+                                     is still in L2.  Automatic picks one launch when both
+                                     GEMMs use the CTA-pair kernel and the block has at
+                                     least six waves of tiles over the resident pairs. */
+} gemm_epi_ffn_option;
+
+gemm_epi_status gemm_epi_ffn_set_option(gemm_epi_ffn_plan_t p, gemm_epi_ffn_option opt,
+                                        int64_t value);
+
+/* The plan's mode and configuration as text, owned by the plan. */
+const char* gemm_epi_ffn_plan_describe(gemm_epi_ffn_plan_t p);
+
+/* Y = GELU(X.W1 + b1).W2 + b2 + R, asynchronous on `stream`.  Y may be R itself (each
+ * element of R is read by the thread that then writes that element of Y). */
 gemm_epi_status gemm_epi_ffn_execute(gemm_epi_ffn_plan_t p, const void* X, const void* W1,
                                      const void* b1, const void* W2, const void* b2,
                                      const void* R, void* Y, cudaStream_t stream);

@@ -176,6 +176,27 @@ def test_gelu_textbook_points_through_the_kernel():
     assert np.max(np.abs(got - want) / (np.abs(want) + 1)) < 1.2e-3
 
 
+def test_gelu_accuracy_on_a_dense_grid():
+    """16384 pre-activations in [-12, 12] through the fused kernel (A = I, bias = 0, f16):
+    the kernel's GELU is within 3.1e-5 * max(1, |x|) of x * Phi(x), plus the f16 rounding
+    of the output."""
+    from scipy.special import ndtr
+    m = k = 16
+    n = 1024
+    xs = torch.linspace(-12.0, 12.0, m * n, dtype=torch.float64).to(torch.float16)
+    inputs = {"A": torch.eye(m, dtype=torch.float16), "B": xs.reshape(k, n),
+              "bias": torch.zeros(n, dtype=torch.float16)}
+    for variant in (1, 3):
+        D, _, desc = run(inputs, m, n, k, "f16", "GELU_BIAS", "1N",
+                         options={"VARIANT": variant} if variant != 1 else None)
+        x = xs.double().numpy().reshape(k, n)
+        want = x * ndtr(x)
+        got = D.double().numpy()
+        bound = 3.1e-5 * np.maximum(1.0, np.abs(x)) + 2.0 ** -11 * np.abs(want) + 6e-8
+        bad = np.abs(got - want) > bound
+        assert not bad.any(), (desc, x[bad][:5], got[bad][:5], want[bad][:5])
+
+
 # ---- the timeout path -----------------------------------------------------------------------
 
 def test_device_wait_limit_reports_timeout_and_context_survives():
@@ -230,8 +251,9 @@ def test_execute_argument_errors():
 
 # ---- the FFN entry points -------------------------------------------------------------------
 
-@pytest.mark.parametrize("t,d,f", [(300, 136, 264), (16, 256, 520), (1, 8, 8)])
-def test_ffn_plan_parity(t, d, f):
+@pytest.mark.parametrize("launches", [0, 1, 2])
+@pytest.mark.parametrize("t,d,f", [(300, 136, 264), (16, 256, 520), (1, 8, 8), (520, 264, 776)])
+def test_ffn_plan_parity(t, d, f, launches):
     import oracle
     g = torch.Generator().manual_seed(t + d + f)
 
@@ -242,7 +264,9 @@ def test_ffn_plan_parity(t, d, f):
     dev = torch.device("cuda")
     gi = {k: v.to(dev) for k, v in cpu.items()}
     Y = torch.empty((t, d), dtype=torch.bfloat16, device=dev)
-    with gemm_epi.FfnPlan(t, d, f) as plan:
+    with gemm_epi.FfnPlan(t, d, f, launches=launches) as plan:
+        if launches:
+            assert plan.describe().startswith("one launch" if launches == 1 else "two launches")
         plan.execute(gi["X"], gi["W1"], gi["b1"], gi["W2"], gi["b2"], gi["R"], Y)
         assert plan.sync_status() == 0
         H = plan.hidden().cpu()
@@ -259,7 +283,8 @@ def test_ffn_plan_parity(t, d, f):
     assert rel_err(Y, Y2) <= TOL["bf16"]
 
 
-def test_ffn_in_place_on_residual():
+@pytest.mark.parametrize("launches", [1, 2])
+def test_ffn_in_place_on_residual(launches):
     t, d, f = 200, 128, 256
     g = torch.Generator().manual_seed(5)
     dev = torch.device("cuda")
@@ -269,12 +294,46 @@ def test_ffn_in_place_on_residual():
     cpu = dict(X=r(t, d), W1=r(d, f, sc=0.1), b1=r(f, sc=0.1), W2=r(f, d, sc=0.1),
                b2=r(d, sc=0.1), R=r(t, d))
     gi = {k: v.to(dev) for k, v in cpu.items()}
-    with gemm_epi.FfnPlan(t, d, f) as plan:
+    with gemm_epi.FfnPlan(t, d, f, launches=launches) as plan:
         plan.execute(gi["X"], gi["W1"], gi["b1"], gi["W2"], gi["b2"], gi["R"], gi["R"])
         assert plan.sync_status() == 0
     import oracle
     _, _, Y_ref = oracle.ffn(**cpu)
     assert rel_err(gi["R"], Y_ref) <= TOL["bf16"]
+
+
+def test_ffn_one_launch_many_row_blocks_few_pairs():
+    """Few CTA pairs walking many GEMM-1 and GEMM-2 tiles: GEMM-2 tiles wait on row blocks
+    that other pairs (and the same pair, earlier) finish; also repeated calls reuse the
+    zeroed counters."""
+    import oracle
+    t, d, f = 1300, 520, 1032
+    g = torch.Generator().manual_seed(44)
+
+    def r(*s, sc=1.0):
+        return (torch.randn(*s, generator=g) * sc).to(torch.bfloat16)
+    cpu = dict(X=r(t, d, sc=0.5), W1=r(d, f, sc=0.05), b1=r(f, sc=0.1), W2=r(f, d, sc=0.05),
+               b2=r(d, sc=0.1), R=r(t, d))
+    dev = torch.device("cuda")
+    gi = {k: v.to(dev) for k, v in cpu.items()}
+    Y = torch.empty((t, d), dtype=torch.bfloat16, device=dev)
+    with gemm_epi.FfnPlan(t, d, f, launches=1) as plan:
+        for _ in range(3):
+            plan.execute(gi["X"], gi["W1"], gi["b1"], gi["W2"], gi["b2"], gi["R"], Y)
+        assert plan.sync_status() == 0
+        H = plan.hidden().cpu()
+    H_ref, H_exact, Y_ref = oracle.ffn(**cpu)
+    assert rel_err(H, H_exact) <= TOL["bf16"]
+    assert rel_err(Y, Y_ref) <= TOL["bf16"]
+
+
+def test_ffn_option_rules():
+    with gemm_epi.FfnPlan(300, 136, 264) as plan:
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            gemm_epi.gemm_epi_ffn_set_option(plan.handle, "LAUNCHES", 3)
+        assert e.value.status == 1
+        gemm_epi.gemm_epi_ffn_set_option(plan.handle, "LAUNCHES", 2)
+        assert plan.describe().startswith("two launches")
 
 
 # ---- split-K across a cluster (partial sums added on chip) ---------------------------------

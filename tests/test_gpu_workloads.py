@@ -78,6 +78,24 @@ def test_ffn_full_parity():
     assert rel_err(Y, Y2) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("launches", [1, 2])
+def test_ffn_full_plan_parity(launches):
+    """The FFN plan on the full workload: one launch (both GEMMs in one persistent kernel)
+    and two launches."""
+    f = workloads.FFNS["ffn_bf16_4096x1024x4096"]
+    dev = torch.device("cuda")
+    fi = workloads.ffn_inputs(f, device=dev)
+    Y = torch.empty((f.t, f.d), dtype=torch.bfloat16, device=dev)
+    with gemm_epi.FfnPlan(f.t, f.d, f.f, "bf16", launches=launches) as plan:
+        plan.execute(fi["X"], fi["W1"], fi["b1"], fi["W2"], fi["b2"], fi["R"], Y)
+        assert plan.sync_status() == 0
+        H = plan.hidden().cpu()
+    cpu = {k: v.cpu() for k, v in fi.items()}
+    H_ref, H_exact, Y_ref = oracle.ffn(**cpu)
+    assert rel_err(H, H_exact) <= TOL["bf16"]
+    assert rel_err(Y, Y_ref) <= TOL["bf16"]
+
+
 def _large_rows(w):
     rng = np.random.default_rng(2024)
     rows = set(rng.choice(w.m, size=256, replace=False).tolist())
