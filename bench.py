@@ -451,35 +451,44 @@ def measure_extras(plan, w, A, B, bias, D, aux, stream, peaks):
             "unfused_us_cold_l2": cold_unf * 1e6, "unavoidable_bytes": unavoidable,
             "status": st, "plan": desc}
         del inp, Dg, auxg, pre
-    # the FFN block through its plan: GEMM1 (bias + GELU), then GEMM2 (bias + residual) as a
-    # programmatic dependent launch; and the unfused chain (GEMM, bias+GELU pass, GEMM,
-    # bias+residual pass: four launches, two extra round trips of pre-activations)
-    f = workloads.FFNS["ffn_bf16_4096x1024x4096"]
-    fi = workloads.ffn_inputs(f, device=A.device)
-    Y = torch.empty((f.t, f.d), dtype=torch.bfloat16, device=A.device)
-    H = torch.empty((f.t, f.f), dtype=torch.bfloat16, device=A.device)
-    pre1 = torch.empty((f.t, f.f), dtype=torch.bfloat16, device=A.device)
-    pre2 = torch.empty((f.t, f.d), dtype=torch.bfloat16, device=A.device)
-    with gemm_epi.FfnPlan(f.t, f.d, f.f, "bf16") as fp, \
-            gemm_epi.Plan(f.t, f.f, f.d, "bf16", "GELU_BIAS", "1N") as p1, \
-            gemm_epi.Plan(f.t, f.d, f.f, "bf16", "BIAS_RESIDUAL", "1N") as p2:
-        def ffn():
-            fp.execute(fi["X"], fi["W1"], fi["b1"], fi["W2"], fi["b2"], fi["R"], Y)
+    per.update(measure_ffn(A.device, stream, flush, peaks))
+    out["workloads"] = per
+    out["backward"] = measure_backward(A.device, stream, flush, peaks)
+    return out
 
+
+def measure_ffn(device, stream, flush, peaks):
+    """The FFN block through its plan (automatic mode, and one and two launches forced) and
+    the unfused chain (GEMM, bias+GELU pass, GEMM, bias+residual pass: four launches, two
+    extra round trips of pre-activations), cold L2 and CUDA Graph replay."""
+    import torch
+
+    from activation_epilogue_gb300 import gemm_epi, workloads
+    f = workloads.FFNS["ffn_bf16_4096x1024x4096"]
+    fi = workloads.ffn_inputs(f, device=device)
+    Y = torch.empty((f.t, f.d), dtype=torch.bfloat16, device=device)
+    H = torch.empty((f.t, f.f), dtype=torch.bfloat16, device=device)
+    pre1 = torch.empty((f.t, f.f), dtype=torch.bfloat16, device=device)
+    pre2 = torch.empty((f.t, f.d), dtype=torch.bfloat16, device=device)
+    out = {}
+    with gemm_epi.Plan(f.t, f.f, f.d, "bf16", "GELU_BIAS", "1N") as p1, \
+            gemm_epi.Plan(f.t, f.d, f.f, "bf16", "BIAS_RESIDUAL", "1N") as p2:
         def ffn_unfused():
             p1.execute_unfused(fi["X"], fi["W1"], fi["b1"], pre1, H)
             p2.execute_unfused(H, fi["W2"], fi["b2"], pre2, Y, residual=fi["R"])
-        cold = time_cold(ffn, 20, stream, flush)
-        hot = time_graph(ffn, 10, 10, stream)
         cold_unf = time_cold(ffn_unfused, 20, stream, flush)
-        per[f.name] = {"us_per_call_cold_l2": cold * 1e6, "us_per_call_graph_hot_l2": hot * 1e6,
-                       "tflops_cold": f.flops / cold / 1e12,
-                       "tensor_frac_cold": f.flops / cold / 1e12 / peaks["bf16_tflops"],
-                       "launches": 2, "unfused_us_cold_l2": cold_unf * 1e6,
-                       "unfused_launches": 4, "status": fp.sync_status(),
-                       "plans": [p1.describe(), p2.describe()]}
-    out["workloads"] = per
-    out["backward"] = measure_backward(A.device, stream, flush, peaks)
+        for mode, launches in [("", 0), ("_one_launch", 1), ("_two_launches", 2)]:
+            with gemm_epi.FfnPlan(f.t, f.d, f.f, "bf16", launches=launches) as fp:
+                def ffn():
+                    fp.execute(fi["X"], fi["W1"], fi["b1"], fi["W2"], fi["b2"], fi["R"], Y)
+                cold = time_cold(ffn, 20, stream, flush)
+                hot = time_graph(ffn, 10, 10, stream)
+                out[f.name + mode] = {
+                    "us_per_call_cold_l2": cold * 1e6, "us_per_call_graph_hot_l2": hot * 1e6,
+                    "tflops_cold": f.flops / cold / 1e12,
+                    "tensor_frac_cold": f.flops / cold / 1e12 / peaks["bf16_tflops"],
+                    "unfused_us_cold_l2": cold_unf * 1e6, "unfused_launches": 4,
+                    "status": fp.sync_status(), "plan": fp.describe()}
     return out
 
 
@@ -540,6 +549,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--only", choices=["backward", "ffn"],
+                    help="print only these measurements (one JSON object), for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
         log("[bench] warm-up raised to 3 steps")
@@ -552,6 +563,18 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             run_reference(args)
+        return
+
+    if args.only:
+        import torch
+        dev = torch.device("cuda", local_rank)
+        torch.cuda.set_device(dev)
+        stream = torch.cuda.current_stream()
+        flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+        measure = measure_backward if args.only == "backward" else measure_ffn
+        res = measure(dev, stream, flush_buf.zero_, load_peaks()[0])
+        if rank == 0:
+            print(json.dumps({args.only: res}))
         return
 
     dist = None
