@@ -21,81 +21,168 @@ __device__ __forceinline__ float ld16(const uint16_t* p, long long i, int bf16)
     return __half2float(__ushort_as_half(h));
 }
 
-__device__ __forceinline__ uint16_t st16(float a, int bf16)
+__device__ __forceinline__ float dec16(uint32_t h, int bf16)
 {
-    if (bf16) return __bfloat16_as_ushort(__float2bfloat16_rn(a));
-    return __half_as_ushort(__float2half_rn(a));
+    if (bf16) return __uint_as_float(h << 16);
+    return __half2float(__ushort_as_half(static_cast<uint16_t>(h)));
 }
 
-// One block task = 32 rows x 256 columns; warp w of the block takes columns 32 w .. 32 w + 31
-// of it (lane = column) and walks the 32 rows, so each row's 32 columns sit on the lanes:
-// one ballot gives an aux word, one warp sum a row's share of a bias gradient, and a
-// column's share of a bias gradient stays in its lane's register until the task ends.
+// 8 consecutive 16-bit values (one 16-byte load) to fp32.
+__device__ __forceinline__ void load8(const uint16_t* p, float (&x)[8], int bf16)
+{
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        x[2 * h] = dec16(ww[h] & 0xFFFFu, bf16);
+        x[2 * h + 1] = dec16(ww[h] >> 16, bf16);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack2_16(float a, float b, int bf16)
+{
+    if (bf16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void store8(uint16_t* p, const float (&x)[8], int bf16)
+{
+    uint4 w;
+    w.x = pack2_16(x[0], x[1], bf16);
+    w.y = pack2_16(x[2], x[3], bf16);
+    w.z = pack2_16(x[4], x[5], bf16);
+    w.w = pack2_16(x[6], x[7], bf16);
+    *reinterpret_cast<uint4*>(p) = w;
+}
+
+constexpr int kRows = 32;        // rows per block task
+constexpr int kCols = 256;       // columns per block task: 8 per lane
+constexpr int kWarps = 8;
+
+// One block task = 32 rows x 256 columns.  Lane l of every warp owns columns 8l .. 8l + 7 of
+// the task (one 16-byte access per row for each 16-bit matrix: a warp reads or writes 512
+// contiguous bytes of a row); warp w takes rows w, w + 8, w + 16, w + 24.  n is a multiple
+// of 8, so a lane's 8 columns are all inside the matrix or all outside.  A mask word
+// (32 columns) is spread over 4 lanes, 8 bits each, combined with two shuffles.  Bias
+// gradient: an (m,1) row's share is a warp sum; a (1,n) column's share is summed in the
+// lane over its rows, then over the 8 warps through shared memory, then one atomic per
+// column and task.
 __global__ void __launch_bounds__(256) elementwise_epilogue_kernel(
     const uint16_t* __restrict__ pre, const uint16_t* __restrict__ bias,
     const uint16_t* __restrict__ residual, uint16_t* __restrict__ D, void* __restrict__ aux,
     const void* __restrict__ aux_in, float* __restrict__ dbias, int m, int n, int epilog,
     int bias_layout, int bf16, int aux_ld)
 {
+    __shared__ float col_part[kWarps][kCols];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const bool bwd = is_backward(epilog);
     const bool has_bias = epilog != EPI_NONE && !bwd;
-    const long long groups_per_row = (n + 255) / 256;
-    const long long tasks = static_cast<long long>((m + 31) / 32) * groups_per_row;
+    const long long groups_per_row = (n + kCols - 1) / kCols;
+    const long long tasks = static_cast<long long>((m + kRows - 1) / kRows) * groups_per_row;
     for (long long task = blockIdx.x; task < tasks; task += gridDim.x) {
         const int rt = static_cast<int>(task / groups_per_row);
         const int g = static_cast<int>(task - static_cast<long long>(rt) * groups_per_row);
-        const int col32 = g * 256 + warp * 32;  // first column of this warp
-        const int col = col32 + lane;
+        const int col = g * kCols + lane * 8;  // this lane's first column
         const bool ok = col < n;
-        const int rows = min(32, m - rt * 32);
-        float col_sum = 0.0f;
-        for (int r = 0; r < rows; ++r) {
-            const int row = rt * 32 + r;
+        float cb[8];                           // (1,n) bias of the lane's columns
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            cb[j] = (has_bias && bias_layout == 1 && ok) ? ld16(bias, col + j, bf16) : 0.0f;
+        float csum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int r = warp; r < kRows; r += kWarps) {
+            const int row = rt * kRows + r;
+            if (row >= m) break;
             const long long idx = static_cast<long long>(row) * n + col;
-            float v = 0.0f;
-            if (ok) {
-                if (pre) v = ld16(pre, idx, bf16);
-                if (has_bias) v += ld16(bias, bias_layout == 0 ? row : col, bf16);
+            float v[8];
+            if (ok && pre) {
+                load8(pre + idx, v, bf16);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+            }
+            if (has_bias) {
+                const float rb = bias_layout == 0 ? ld16(bias, row, bf16) : 0.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] += bias_layout == 0 ? rb : cb[j];
             }
             if (epilog == EPI_RELU_AUX_BIAS) {
-                const uint32_t word = __ballot_sync(0xFFFFFFFFu, ok && v > 0.0f);
-                if (lane == 0 && col32 < n)
-                    static_cast<uint32_t*>(aux)[static_cast<long long>(row) * aux_ld + col32 / 32] = word;
+                uint32_t bits = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) bits |= (ok && v[j] > 0.0f) ? (1u << j) : 0u;
+                bits <<= 8 * (lane & 3);
+                bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 1);
+                bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 2);
+                if ((lane & 3) == 0 && ok)
+                    static_cast<uint32_t*>(aux)[static_cast<long long>(row) * aux_ld + col / 32] = bits;
             } else if (epilog == EPI_GELU_AUX_BIAS) {
-                if (ok) static_cast<uint16_t*>(aux)[idx] = st16(v, bf16);
+                if (ok) store8(static_cast<uint16_t*>(aux) + idx, v, bf16);
             } else if (epilog == EPI_DRELU_BGRAD) {
                 uint32_t mw = 0;
-                if (col32 < n)
-                    mw = static_cast<const uint32_t*>(aux_in)[static_cast<long long>(row) * aux_ld + col32 / 32];
-                v = (ok && ((mw >> lane) & 1u)) ? v : 0.0f;
+                if (ok)
+                    mw = static_cast<const uint32_t*>(aux_in)[static_cast<long long>(row) * aux_ld + col / 32];
+                mw >>= 8 * (lane & 3);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = ((mw >> j) & 1u) ? v[j] : 0.0f;
             } else if (epilog == EPI_DGELU_BGRAD) {
-                v = ok ? v * gelu_grad_fast(ld16(static_cast<const uint16_t*>(aux_in), idx, bf16)) : 0.0f;
-            }
-            float o = v;
-            if (epilog == EPI_RELU_BIAS || epilog == EPI_RELU_AUX_BIAS)
-                o = o > 0.0f ? o : 0.0f;
-            else if (epilog == EPI_GELU_BIAS || epilog == EPI_GELU_AUX_BIAS)
-                o = gelu_erf_fast(o);
-            else if (epilog == EPI_TANH_BIAS)
-                o = tanh_fast(o);
-            if (ok) {
-                if (epilog == EPI_BIAS_RESIDUAL) o += ld16(residual, idx, bf16);
-                D[idx] = st16(o, bf16);
+                if (ok) {
+                    float pv[8];
+                    load8(static_cast<const uint16_t*>(aux_in) + idx, pv, bf16);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[j] *= gelu_grad_fast(pv[j]);
+                }
             }
             if (bwd) {
                 if (bias_layout == 0) {
-                    float s = v;
+                    float sr = 0.0f;
 #pragma unroll
-                    for (int o2 = 16; o2 >= 1; o2 >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o2);
-                    if (lane == 0 && col32 < n) atomicAdd(dbias + row, s);
+                    for (int j = 0; j < 8; ++j) sr += v[j];
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) sr += __shfl_xor_sync(0xFFFFFFFFu, sr, o);
+                    if (lane == 0) atomicAdd(dbias + row, sr);
                 } else {
-                    col_sum += v;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) csum[j] += v[j];
                 }
             }
+            if (epilog == EPI_RELU_BIAS || epilog == EPI_RELU_AUX_BIAS) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = v[j] > 0.0f ? v[j] : 0.0f;
+            } else if (epilog == EPI_GELU_BIAS || epilog == EPI_GELU_AUX_BIAS) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = gelu_erf_fast(v[j]);
+            } else if (epilog == EPI_TANH_BIAS) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = tanh_fast(v[j]);
+            }
+            if (ok) {
+                if (epilog == EPI_BIAS_RESIDUAL) {
+                    float rv[8];
+                    load8(residual + idx, rv, bf16);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[j] += rv[j];
+                }
+                store8(D + idx, v, bf16);
+            }
         }
-        if (bwd && bias_layout == 1 && ok) atomicAdd(dbias + col, col_sum);
+        if (bwd && bias_layout == 1) {
+            // this task's column sums: over the warp's rows (registers), then the 8 warps
+#pragma unroll
+            for (int j = 0; j < 8; ++j) col_part[warp][lane * 8 + j] = csum[j];
+            __syncthreads();
+            const int c = g * kCols + static_cast<int>(threadIdx.x);
+            if (c < n) {
+                float t = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) t += col_part[w][threadIdx.x];
+                atomicAdd(dbias + c, t);
+            }
+            __syncthreads();
+        }
     }
 }
 
@@ -106,7 +193,7 @@ cudaError_t elementwise_launch(const void* pre, const void* bias, const void* re
                                int epilog, int bias_layout, int bf16, int aux_ld, int sm_count,
                                cudaStream_t stream)
 {
-    long long blocks = static_cast<long long>((m + 31) / 32) * ((n + 255) / 256);
+    long long blocks = static_cast<long long>((m + kRows - 1) / kRows) * ((n + kCols - 1) / kCols);
     const long long cap = static_cast<long long>(sm_count) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
