@@ -91,6 +91,14 @@ def _load():
     lib.oracle_gemm_bwd.argtypes = [i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp]
     lib.oracle_num_threads.restype = i32
     lib.oracle_num_threads.argtypes = []
+    f64 = ctypes.c_double
+    lib.oracle_layernorm.restype = i32
+    lib.oracle_layernorm.argtypes = [i64, i64, i32, vp, vp, vp, vp, f64, vp, vp]
+    lib.oracle_ln_gemm_gelu.restype = i32
+    lib.oracle_ln_gemm_gelu.argtypes = [i64, i64, i64, i32, vp, vp, vp, f64, vp, vp, vp]
+    lib.oracle_ln_ffn.restype = i32
+    lib.oracle_ln_ffn.argtypes = [i64, i64, i64, i32, vp, vp, vp, f64, vp, vp, vp, vp, vp, vp,
+                                  vp, vp]
     _lib = lib
     return lib
 
@@ -206,3 +214,52 @@ def gemm_bwd(A, B, *, dtype: str, kind: str, bias_layout: str = "1N", mask=None,
     if rc != 0:
         raise ValueError("oracle_gemm_bwd: bad arguments or out of memory")
     return D, dbias
+
+
+def layernorm(X, gamma, beta, *, eps: float, dtype: str, residual=None):
+    """(Y, stats) in double: LayerNorm of the rows of X (t x d) times gamma plus beta (plus
+    the residual), and per row (mean, 1 / sqrt(var + eps))."""
+    X16 = _bits(X)
+    t, d = X16.shape
+    g16, b16 = _bits(gamma).reshape(-1), _bits(beta).reshape(-1)
+    r16 = None if residual is None else _bits(residual)
+    Y = np.empty((t, d), np.float64)
+    stats = np.empty((t, 2), np.float64)
+    rc = _load().oracle_layernorm(t, d, DTYPES[dtype], _ptr(X16), _ptr(r16), _ptr(g16),
+                                  _ptr(b16), float(eps), _ptr(Y), _ptr(stats))
+    if rc != 0:
+        raise ValueError("oracle_layernorm: bad arguments")
+    return Y, stats
+
+
+def ln_gemm_gelu(A, gamma, beta, W, b, *, eps: float, dtype: str):
+    """D = GELU(LayerNorm(A) . W + b) in double (LayerNorm(A) not rounded)."""
+    A16, W16 = _bits(A), _bits(W)
+    m, k = A16.shape
+    n = W16.shape[1]
+    D = np.empty((m, n), np.float64)
+    rc = _load().oracle_ln_gemm_gelu(m, n, k, DTYPES[dtype], _ptr(A16),
+                                     _ptr(_bits(gamma).reshape(-1)),
+                                     _ptr(_bits(beta).reshape(-1)), float(eps), _ptr(W16),
+                                     _ptr(_bits(b).reshape(-1)), _ptr(D))
+    if rc != 0:
+        raise ValueError("oracle_ln_gemm_gelu: bad arguments or out of memory")
+    return D
+
+
+def ln_ffn(X, gamma, beta, W1, b1, W2, b2, R, *, eps: float, dtype: str = "bf16"):
+    """(H_bits, H_exact, Y) of the pre-LayerNorm FFN block."""
+    X16, W116, W216 = _bits(X), _bits(W1), _bits(W2)
+    t, d = X16.shape
+    f = W116.shape[1]
+    H = np.empty((t, f), np.uint16)
+    Hx = np.empty((t, f), np.float64)
+    Y = np.empty((t, d), np.float64)
+    rc = _load().oracle_ln_ffn(t, d, f, DTYPES[dtype], _ptr(X16), _ptr(_bits(gamma).reshape(-1)),
+                               _ptr(_bits(beta).reshape(-1)), float(eps), _ptr(W116),
+                               _ptr(_bits(b1).reshape(-1)), _ptr(W216),
+                               _ptr(_bits(b2).reshape(-1)), _ptr(_bits(R)), _ptr(H), _ptr(Hx),
+                               _ptr(Y))
+    if rc != 0:
+        raise ValueError("oracle_ln_ffn: bad arguments or out of memory")
+    return H, Hx, Y

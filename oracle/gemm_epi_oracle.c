@@ -17,7 +17,10 @@
  *   "Operator fusion in model inference, from LayerNorm to residual connections"
  *   (wmrh.cn/news/429806), section 1 and its flowchart: the FFN chain
  *     matmul -> bias -> GELU -> matmul -> bias, and (section 3) the residual added to the
- *     output of the op that precedes it.
+ *     output of the op that precedes it; section 2: LayerNorm,
+ *     y = (x - mu) / sqrt(sigma^2 + eps) * gamma + beta over each row, with the mean and
+ *     the variance taken in two passes as the section's code does, optionally followed by
+ *     a residual add (the section's LayerNorm-and-residual function).
  *
  * Readings where the pages are silent (each is listed with its reason in the design notes):
  *   - inputs are 16-bit (IEEE binary16 or bfloat16); every element is decoded exactly to
@@ -316,6 +319,117 @@ int oracle_ffn(int64_t t, int64_t d, int64_t f, int dtype,
 out:
     free(rows);
     free(cf);
+    free(cd);
+    free(H);
+    return rc;
+}
+
+/*
+ * LayerNorm of the rows of X (t x d): mu = sum(x) / d, var = sum((x - mu)^2) / d (the
+ * biased variance, second pass over the centred row), y = (x - mu) / sqrt(var + eps) *
+ * gamma + beta (+ residual when it is not NULL).  Y (t x d) in double; stats (may be NULL)
+ * receives mu and 1 / sqrt(var + eps) per row.
+ */
+int oracle_layernorm(int64_t t, int64_t d, int dtype, const uint16_t* X, const uint16_t* residual,
+                     const uint16_t* gamma, const uint16_t* beta, double eps, double* Y,
+                     double* stats)
+{
+    if (t < 0 || d < 0 || !X || !gamma || !beta || !Y || !(eps >= 0.0)) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < t; ++i) {
+        double sum = 0.0;
+        for (int64_t j = 0; j < d; ++j)
+            sum += decode(dtype, X[i * d + j]);
+        const double mu = d > 0 ? sum / (double)d : 0.0;
+        double ss = 0.0;
+        for (int64_t j = 0; j < d; ++j) {
+            const double c = decode(dtype, X[i * d + j]) - mu;
+            ss += c * c;
+        }
+        const double var = d > 0 ? ss / (double)d : 0.0;
+        const double rstd = 1.0 / sqrt(var + eps);
+        if (stats) {
+            stats[2 * i] = mu;
+            stats[2 * i + 1] = rstd;
+        }
+        for (int64_t j = 0; j < d; ++j) {
+            double y = (decode(dtype, X[i * d + j]) - mu) * rstd * decode(dtype, gamma[j]) +
+                       decode(dtype, beta[j]);
+            if (residual)
+                y += decode(dtype, residual[i * d + j]);
+            Y[i * d + j] = y;
+        }
+    }
+    return 0;
+}
+
+/*
+ * A GEMM on layer-normalised rows, the first GEMM of a pre-LayerNorm FFN block:
+ *   D = GELU(LayerNorm(A) . W + b)      A: m x k, gamma, beta: k, W: k x n, b: n
+ * LayerNorm(A) is kept in double (never rounded: it is an intermediate).
+ */
+int oracle_ln_gemm_gelu(int64_t m, int64_t n, int64_t k, int dtype, const uint16_t* A,
+                        const uint16_t* gamma, const uint16_t* beta, double eps,
+                        const uint16_t* W, const uint16_t* b, double* D)
+{
+    if (m < 0 || n < 0 || k < 0 || !A || !W || !b || !D) return -1;
+    double* An = (double*)malloc(sizeof(double) * (size_t)(m * k > 0 ? m * k : 1));
+    double* Wd = (double*)malloc(sizeof(double) * (size_t)(k * n > 0 ? k * n : 1));
+    if (!An || !Wd) {
+        free(An);
+        free(Wd);
+        return -1;
+    }
+    int rc = oracle_layernorm(m, k, dtype, A, NULL, gamma, beta, eps, An, NULL);
+    if (rc == 0) {
+        for (int64_t i = 0; i < k * n; ++i)
+            Wd[i] = decode(dtype, W[i]);
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t i = 0; i < m; ++i) {
+            for (int64_t j = 0; j < n; ++j)
+                D[i * n + j] = 0.0;
+            for (int64_t kk = 0; kk < k; ++kk) {
+                const double a = An[i * k + kk];
+                for (int64_t j = 0; j < n; ++j)
+                    D[i * n + j] += a * Wd[kk * n + j];
+            }
+            for (int64_t j = 0; j < n; ++j)
+                D[i * n + j] = oracle_gelu(D[i * n + j] + decode(dtype, b[j]));
+        }
+    }
+    free(An);
+    free(Wd);
+    return rc;
+}
+
+/*
+ * The pre-LayerNorm FFN block: H = round(GELU(LayerNorm(X) . W1 + b1)) stored in 16 bits,
+ * Y = H . W2 + b2 + R (the residual is usually X itself).  As oracle_ffn otherwise.
+ */
+int oracle_ln_ffn(int64_t t, int64_t d, int64_t f, int dtype, const uint16_t* X,
+                  const uint16_t* gamma, const uint16_t* beta, double eps, const uint16_t* W1,
+                  const uint16_t* b1, const uint16_t* W2, const uint16_t* b2, const uint16_t* R,
+                  uint16_t* H_bits, double* H_exact, double* Y)
+{
+    int rc = -1;
+    int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)(t > 0 ? t : 1));
+    int64_t* cd = (int64_t*)malloc(sizeof(int64_t) * (size_t)(d > 0 ? d : 1));
+    double* H = (double*)malloc(sizeof(double) * (size_t)(t * f > 0 ? t * f : 1));
+    if (!rows || !cd || !H)
+        goto out;
+    for (int64_t i = 0; i < t; ++i) rows[i] = i;
+    for (int64_t j = 0; j < d; ++j) cd[j] = j;
+    if (oracle_ln_gemm_gelu(t, f, d, dtype, X, gamma, beta, eps, W1, b1, H) != 0)
+        goto out;
+    if (H_exact)
+        memcpy(H_exact, H, sizeof(double) * (size_t)(t * f));
+    oracle_encode_array(dtype, H, t * f, H_bits);
+    if (oracle_gemm_epi(t, d, f, dtype, OR_EPI_BIAS_RESIDUAL, OR_BIAS_1N, H_bits, W2, b2, R,
+                        rows, t, cd, d, NULL, Y) != 0)
+        goto out;
+    rc = 0;
+out:
+    free(rows);
     free(cd);
     free(H);
     return rc;

@@ -36,6 +36,14 @@ MUTANTS = {
     "drelu mask bit order": ("g = (mask[i * ldw + j / 32] >> (j % 32)) & 1u ? 1.0 : 0.0;",
                              "g = (mask[i * ldw + j / 32] >> (31 - j % 32)) & 1u ? 1.0 : 0.0;"),
     "residual dropped": ("d = p + decode(dtype, residual[i * n + j]);", "d = p;"),
+    "layernorm eps dropped": ("const double rstd = 1.0 / sqrt(var + eps);",
+                              "const double rstd = 1.0 / sqrt(var);"),
+    "layernorm unbiased variance": ("const double var = d > 0 ? ss / (double)d : 0.0;",
+                                    "const double var = d > 1 ? ss / (double)(d - 1) : 0.0;"),
+    "layernorm gamma and beta swapped": ("* rstd * decode(dtype, gamma[j]) +\n                       decode(dtype, beta[j]);",
+                                         "* rstd * decode(dtype, beta[j]) +\n                       decode(dtype, gamma[j]);"),
+    "layernorm residual dropped": ("                y += decode(dtype, residual[i * d + j]);",
+                                   "                y += 0.0;"),
     "k loop drops last term": ("for (int64_t kk = 0; kk < k; ++kk) {\n                const double a",
                                "for (int64_t kk = 0; kk + 1 < k; ++kk) {\n                const double a"),
 }

@@ -449,3 +449,82 @@ def test_drelu_bgrad_brute_force_and_mask_extremes(oracle):
         D0, db0 = oracle.gemm_bwd(p["A"], p["B"], dtype="f16", kind="DRELU_BGRAD",
                                   mask=np.zeros_like(mask))
         assert not D0.any() and not db0.any()
+
+
+# ---- LayerNorm ("Operator fusion in model inference", section 2) ---------------------------
+
+def _ln_inputs(t, d, seed, dtype="bf16", offset=1.5, scale=3.0):
+    g = torch.Generator().manual_seed(seed)
+    td = workloads.TORCH_DTYPES[dtype]
+    X = (torch.randn(t, d, generator=g) * scale + offset).to(td)
+    gamma = (1.0 + 0.1 * torch.randn(d, generator=g)).to(td)
+    beta = (0.1 * torch.randn(d, generator=g)).to(td)
+    R = torch.randn(t, d, generator=g).to(td)
+    return X, gamma, beta, R
+
+
+@pytest.mark.parametrize("d,eps,dtype", [(1, 1e-5, "bf16"), (7, 0.0, "f16"), (64, 1e-5, "bf16"),
+                                         (1024, 1e-6, "bf16"), (300, 1e-5, "f16")])
+def test_layernorm_matches_torch_float64(oracle, d, eps, dtype):
+    X, gamma, beta, R = _ln_inputs(9, d, seed=d, dtype=dtype)
+    Xd, gd, bd, Rd = (_t64(x, dtype) for x in (X, gamma, beta, R))
+    ref = torch.nn.functional.layer_norm(Xd, (d,), gd, bd, eps).numpy()
+    Y, stats = oracle.layernorm(X, gamma, beta, eps=eps, dtype=dtype)
+    np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-12)
+    Yr, _ = oracle.layernorm(X, gamma, beta, eps=eps, dtype=dtype, residual=R)
+    np.testing.assert_allclose(Yr, ref + Rd.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(stats[:, 0], Xd.mean(1).numpy(), rtol=1e-13, atol=1e-13)
+    var = Xd.var(1, unbiased=False).numpy()
+    np.testing.assert_allclose(stats[:, 1], 1.0 / np.sqrt(var + eps), rtol=1e-12)
+
+
+def test_layernorm_invariants(oracle):
+    # integer-valued rows: a shift by an integer and a doubling stay exact in bf16
+    g = torch.Generator().manual_seed(3)
+    X = torch.randint(-40, 41, (6, 96), generator=g).to(torch.bfloat16)
+    ones = torch.ones(96, dtype=torch.bfloat16)
+    zeros = torch.zeros(96, dtype=torch.bfloat16)
+    Y, stats = oracle.layernorm(X, ones, zeros, eps=1e-5, dtype="bf16")
+    Ys, _ = oracle.layernorm(X + 7, ones, zeros, eps=1e-5, dtype="bf16")
+    np.testing.assert_allclose(Ys, Y, rtol=0, atol=1e-12)          # shift invariance
+    assert np.max(np.abs(Y.mean(1))) < 1e-12                          # centred
+    var = _t64(X).var(1, unbiased=False).numpy()
+    np.testing.assert_allclose((Y * Y).mean(1), var / (var + 1e-5), rtol=1e-12)
+    Y0, _ = oracle.layernorm(X, ones, zeros, eps=0.0, dtype="bf16")
+    Y2, _ = oracle.layernorm(X * 2, ones, zeros, eps=0.0, dtype="bf16")
+    np.testing.assert_allclose(Y2, Y0, rtol=0, atol=1e-12)          # scale invariance (eps 0)
+    # gamma scales, beta shifts, per column
+    gam = torch.arange(1, 97).to(torch.bfloat16)
+    bet = (torch.arange(96) - 48).to(torch.bfloat16)
+    Yg, _ = oracle.layernorm(X, gam, bet, eps=1e-5, dtype="bf16")
+    np.testing.assert_allclose(Yg, Y * _t64(gam).numpy() + _t64(bet).numpy(), rtol=1e-13,
+                               atol=1e-12)
+
+
+def test_ln_gemm_gelu_matches_library_chain(oracle):
+    from scipy.special import ndtr
+    m, k, n = 33, 72, 40
+    X, gamma, beta, _ = _ln_inputs(m, k, seed=5)
+    g = torch.Generator().manual_seed(6)
+    W = (torch.randn(k, n, generator=g) * 0.1).to(torch.bfloat16)
+    b = (torch.randn(n, generator=g) * 0.1).to(torch.bfloat16)
+    D = oracle.ln_gemm_gelu(X, gamma, beta, W, b, eps=1e-5, dtype="bf16")
+    xn = torch.nn.functional.layer_norm(_t64(X), (k,), _t64(gamma), _t64(beta), 1e-5).numpy()
+    pre = xn @ _t64(W).numpy() + _t64(b).numpy()
+    np.testing.assert_allclose(D, pre * ndtr(pre), rtol=1e-11, atol=1e-12)
+
+
+def test_ln_ffn_is_the_composition(oracle):
+    t, d, f = 17, 48, 64
+    X, gamma, beta, R = _ln_inputs(t, d, seed=8)
+    g = torch.Generator().manual_seed(9)
+    W1 = (torch.randn(d, f, generator=g) * 0.1).to(torch.bfloat16)
+    b1 = (torch.randn(f, generator=g) * 0.1).to(torch.bfloat16)
+    W2 = (torch.randn(f, d, generator=g) * 0.1).to(torch.bfloat16)
+    b2 = (torch.randn(d, generator=g) * 0.1).to(torch.bfloat16)
+    H, Hx, Y = oracle.ln_ffn(X, gamma, beta, W1, b1, W2, b2, R, eps=1e-5)
+    D = oracle.ln_gemm_gelu(X, gamma, beta, W1, b1, eps=1e-5, dtype="bf16")
+    np.testing.assert_array_equal(Hx, D)
+    np.testing.assert_array_equal(H, oracle.encode("bf16", D))
+    Y2 = oracle.gemm_epi(H, W2, b2, dtype="bf16", epilog="BIAS_RESIDUAL", residual=R)
+    np.testing.assert_array_equal(Y, Y2)
