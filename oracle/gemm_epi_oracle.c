@@ -388,10 +388,10 @@ int oracle_ln_gemm_gelu(int64_t m, int64_t n, int64_t k, int dtype, const uint16
         for (int64_t i = 0; i < m; ++i) {
             for (int64_t j = 0; j < n; ++j)
                 D[i * n + j] = 0.0;
-            for (int64_t kk = 0; kk < k; ++kk) {
-                const double a = An[i * k + kk];
+            for (int64_t q = 0; q < k; ++q) {
+                const double xq = An[i * k + q];
                 for (int64_t j = 0; j < n; ++j)
-                    D[i * n + j] += a * Wd[kk * n + j];
+                    D[i * n + j] += xq * Wd[q * n + j];
             }
             for (int64_t j = 0; j < n; ++j)
                 D[i * n + j] = oracle_gelu(D[i * n + j] + decode(dtype, b[j]));

@@ -42,6 +42,8 @@ MUTANTS = {
                                     "const double var = d > 1 ? ss / (double)(d - 1) : 0.0;"),
     "layernorm gamma and beta swapped": ("* rstd * decode(dtype, gamma[j]) +\n                       decode(dtype, beta[j]);",
                                          "* rstd * decode(dtype, beta[j]) +\n                       decode(dtype, gamma[j]);"),
+    "layernorm gemm drops last term": ("for (int64_t q = 0; q < k; ++q) {",
+                                       "for (int64_t q = 0; q + 1 < k; ++q) {"),
     "layernorm residual dropped": ("                y += decode(dtype, residual[i * d + j]);",
                                    "                y += 0.0;"),
     "k loop drops last term": ("for (int64_t kk = 0; kk < k; ++kk) {\n                const double a",
