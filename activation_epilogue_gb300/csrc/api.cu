@@ -142,7 +142,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             // small m: swapped; enough 256 x 256 tiles for most CTA pairs: the pair kernel
             // (half the operand bytes per flop in every SM); else the single-CTA row tiles
             const long long pair_tiles = ((p->m + 255) / 256) * ((p->n + 255) / 256);
-            if (p->m <= kSwappedMaxM)
+            if (p->m <= kSwappedMaxM && p->epilog != GEMM_EPI_LN_GELU_BIAS)
                 v = kSwapped;
             else if (pair_tiles * 10 >= static_cast<long long>(p->sm_count / 2) * 8)
                 v = kRowPair;
@@ -151,6 +151,8 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
         }
         if (v == 3) v = kRowPair;  // option value 3 selects the CTA-pair kernel
         if (v == kSwapped && p->m > kSwappedMaxM) return GEMM_EPI_ERR_INVALID_ARG;
+        // the swapped kernel has no LayerNorm epilogue
+        if (v == kSwapped && p->epilog == GEMM_EPI_LN_GELU_BIAS) return GEMM_EPI_ERR_INVALID_ARG;
         p->variant = v;
         p->k_blocks = static_cast<int>((p->k + 63) / 64);
         if (v == kRowPair) {
@@ -218,7 +220,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
     static const char* ename[] = {"BIAS",          "RELU_BIAS",     "GELU_BIAS",
                                   "RELU_AUX_BIAS", "BIAS_RESIDUAL", "NONE",
                                   "TANH_BIAS",     "GELU_AUX_BIAS", "DRELU_BGRAD",
-                                  "DGELU_BGRAD"};
+                                  "DGELU_BGRAD",   "LN_GELU_BIAS"};
     snprintf(p->desc, sizeof(p->desc),
              "m=%lld n=%lld k=%lld dtype=%s epilog=%s bias=%s variant=%s tile=%dx%d bk=64 "
              "stages=%d smem=%d tiles=%dx%d k_blocks=%d split_k=%d grid=%d group_m=%d sms=%d",
@@ -298,6 +300,9 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, in
     prm.aux = ops.aux;
     prm.aux_in = ops.aux_in;
     prm.dbias = ops.dbias;
+    prm.ln_stats = ops.ln_stats;
+    prm.ln_colsum = ops.ln_colsum;
+    prm.ln_bias = ops.ln_bias;
     prm.status = p->d_status;
     prm.wait_limit_ns = p->wait_limit_ns;
     prm.m = static_cast<int>(p->m);
@@ -351,10 +356,24 @@ gemm_epi_status zero_dbias(const gemm_epi_plan_s* p, const gemm_epi_operands& op
 cudaError_t run_elementwise(const gemm_epi_plan_s* p, const void* pre,
                             const gemm_epi_operands& ops, cudaStream_t stream)
 {
-    return elementwise_launch(pre, ops.bias, ops.residual, ops.D, ops.aux, ops.aux_in, ops.dbias,
-                              static_cast<int>(p->m), static_cast<int>(p->n), p->epilog,
-                              p->bias_layout, p->dtype == GEMM_EPI_BF16 ? 1 : 0,
-                              static_cast<int>((p->n + 31) / 32), p->sm_count, stream);
+    ElementwiseArgs a;
+    a.pre = pre;
+    a.bias = ops.bias;
+    a.residual = ops.residual;
+    a.D = ops.D;
+    a.aux = ops.aux;
+    a.aux_in = ops.aux_in;
+    a.dbias = ops.dbias;
+    a.ln_stats = ops.ln_stats;
+    a.ln_colsum = ops.ln_colsum;
+    a.ln_bias = ops.ln_bias;
+    a.m = static_cast<int>(p->m);
+    a.n = static_cast<int>(p->n);
+    a.epilog = p->epilog;
+    a.bias_layout = p->bias_layout;
+    a.bf16 = p->dtype == GEMM_EPI_BF16 ? 1 : 0;
+    a.aux_ld = static_cast<int>((p->n + 31) / 32);
+    return elementwise_launch(a, p->sm_count, stream);
 }
 
 // One fused call on an already-checked plan: empty problems launch nothing, k == 0 runs the
@@ -380,6 +399,12 @@ gemm_epi_status check_operands(const gemm_epi_plan_s* p, const gemm_epi_operands
     if (o.dbias && !aligned(o.dbias, 4)) return GEMM_EPI_ERR_MISALIGNED;
     // An empty problem touches no operand but dbias (its matrices may have no storage).
     if (p->variant == kEmpty) return GEMM_EPI_OK;
+    const bool ln = e == GEMM_EPI_LN_GELU_BIAS;
+    if (((o.ln_stats != nullptr) != ln) || ((o.ln_colsum != nullptr) != ln) ||
+        ((o.ln_bias != nullptr) != ln))
+        return GEMM_EPI_ERR_INVALID_ARG;
+    if (ln && (!aligned(o.ln_stats, 8) || !aligned(o.ln_colsum, 4) || !aligned(o.ln_bias, 4)))
+        return GEMM_EPI_ERR_MISALIGNED;
     const bool needs_res = e == GEMM_EPI_BIAS_RESIDUAL;
     const bool needs_aux = e == GEMM_EPI_RELU_AUX_BIAS || e == GEMM_EPI_GELU_AUX_BIAS;
     if ((o.aux != nullptr) != needs_aux) return GEMM_EPI_ERR_INVALID_ARG;
@@ -387,7 +412,8 @@ gemm_epi_status check_operands(const gemm_epi_plan_s* p, const gemm_epi_operands
     if ((o.aux_in != nullptr) != bwd || (o.dbias != nullptr) != bwd) return GEMM_EPI_ERR_INVALID_ARG;
     if (!o.D) return GEMM_EPI_ERR_INVALID_ARG;
     if (p->k > 0 && (!o.A || !o.B)) return GEMM_EPI_ERR_INVALID_ARG;
-    if (e != GEMM_EPI_NONE && !bwd && !o.bias) return GEMM_EPI_ERR_INVALID_ARG;
+    if (e != GEMM_EPI_NONE && !bwd && !ln && !o.bias) return GEMM_EPI_ERR_INVALID_ARG;
+    if (ln && o.bias) return GEMM_EPI_ERR_INVALID_ARG;
     const uintptr_t aux_align = e == GEMM_EPI_GELU_AUX_BIAS ? 16 : 4;
     const uintptr_t aux_in_align = e == GEMM_EPI_DGELU_BGRAD ? 16 : 4;
     if (!aligned(o.D, 16) || (o.A && !aligned(o.A, 16)) || (o.B && !aligned(o.B, 16)) ||
@@ -422,13 +448,14 @@ gemm_epi_status gemm_epi_plan(gemm_epi_plan_t* out, int64_t m, int64_t n, int64_
     if (!out) return GEMM_EPI_ERR_INVALID_ARG;
     *out = nullptr;
     if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
-    if (epilog < GEMM_EPI_BIAS || epilog > GEMM_EPI_DGELU_BGRAD) return GEMM_EPI_ERR_INVALID_ARG;
+    if (epilog < GEMM_EPI_BIAS || epilog > GEMM_EPI_LN_GELU_BIAS) return GEMM_EPI_ERR_INVALID_ARG;
     if (bias_layout != GEMM_EPI_BIAS_M1 && bias_layout != GEMM_EPI_BIAS_1N)
         return GEMM_EPI_ERR_INVALID_ARG;
     const int64_t kMax = (1ll << 31) - 1;
     if (m < 0 || n < 0 || k < 0 || m > kMax || n > kMax || k > kMax)
         return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
     if (n % 8 != 0 || k % 8 != 0) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+    if (epilog == GEMM_EPI_LN_GELU_BIAS && k == 0) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
 
     int ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev < 1) {
@@ -648,6 +675,8 @@ struct gemm_epi_ffn_plan_s {
     gemm_epi_plan_t g1;  // H = GELU(X.W1 + b1):   t x f, k = d
     gemm_epi_plan_t g2;  // Y = H.W2 + b2 + R:     t x d, k = f
     void* H;
+    bool layernorm;      // GEMM 1 is LN_GELU_BIAS on the raw X; stats holds (mu, rstd) per row
+    float* stats;
     // one-launch mode: both GEMMs in one CTA-pair kernel (256 x 256 tiles)
     int opt_launches;  // GEMM_EPI_FFN_OPT_LAUNCHES value (0 = automatic)
     bool one_launch;   // the mode in use
@@ -682,6 +711,12 @@ bool pick_one_launch(const gemm_epi_ffn_plan_s* p, long long pairs)
 gemm_epi_status configure_ffn(gemm_epi_ffn_plan_s* p)
 {
     p->maps_valid = false;
+    if (p->layernorm) {  // the one-launch kernel runs GELU_BIAS only
+        p->one_launch = false;
+        snprintf(p->desc, sizeof(p->desc), "two launches after the row statistics: [%s] then [%s]",
+                 p->g1->desc, p->g2->desc);
+        return GEMM_EPI_OK;
+    }
     p->tiles_m = static_cast<int>((p->t + 255) / 256);
     p->tiles_n1 = static_cast<int>((p->f + 255) / 256);
     p->tiles_n2 = static_cast<int>((p->d + 255) / 256);
@@ -799,13 +834,19 @@ gemm_epi_status run_ffn_one_launch(gemm_epi_ffn_plan_s* p, const void* X, const 
 
 extern "C" {
 
-gemm_epi_status gemm_epi_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d, int64_t f,
-                                  gemm_epi_dtype dtype)
+}  // extern "C"
+
+namespace {
+
+gemm_epi_status make_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d, int64_t f,
+                              gemm_epi_dtype dtype, bool layernorm)
 {
     if (!out) return GEMM_EPI_ERR_INVALID_ARG;
     *out = nullptr;
     gemm_epi_plan_t g1 = nullptr, g2 = nullptr;
-    gemm_epi_status st = gemm_epi_plan(&g1, t, f, d, dtype, GEMM_EPI_GELU_BIAS, GEMM_EPI_BIAS_1N);
+    gemm_epi_status st = gemm_epi_plan(&g1, t, f, d, dtype,
+                                       layernorm ? GEMM_EPI_LN_GELU_BIAS : GEMM_EPI_GELU_BIAS,
+                                       GEMM_EPI_BIAS_1N);
     if (st != GEMM_EPI_OK) return st;
     st = gemm_epi_plan(&g2, t, d, f, dtype, GEMM_EPI_BIAS_RESIDUAL, GEMM_EPI_BIAS_1N);
     if (st != GEMM_EPI_OK) {
@@ -826,9 +867,20 @@ gemm_epi_status gemm_epi_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d
     p->g2 = g2;
     p->H = nullptr;
     p->ready = nullptr;
+    p->stats = nullptr;
+    p->layernorm = layernorm;
     if (t > 0 && f > 0) {
         if (cudaMalloc(&p->H, static_cast<size_t>(t) * static_cast<size_t>(f) * 2) != cudaSuccess) {
             cudaGetLastError();
+            gemm_epi_ffn_free(p);
+            return GEMM_EPI_ERR_ALLOC;
+        }
+    }
+    if (layernorm && t > 0) {
+        if (cudaMalloc(reinterpret_cast<void**>(&p->stats), sizeof(float) * 2 * static_cast<size_t>(t)) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            p->stats = nullptr;
             gemm_epi_ffn_free(p);
             return GEMM_EPI_ERR_ALLOC;
         }
@@ -840,6 +892,138 @@ gemm_epi_status gemm_epi_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d
     }
     *out = p;
     return GEMM_EPI_OK;
+}
+
+// The current device, checked to be sm_103, and its SM count.
+gemm_epi_status current_device(int* sms)
+{
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev < 1) {
+        cudaGetLastError();
+        return GEMM_EPI_ERR_NO_DEVICE;
+    }
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_EPI_ERR_NO_DEVICE;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3) return GEMM_EPI_ERR_ARCH;
+    return GEMM_EPI_OK;
+}
+
+bool ln_shape_ok(int64_t t, int64_t d)
+{
+    const int64_t kMax = (1ll << 31) - 1;
+    return t >= 0 && d >= 8 && d % 8 == 0 && t <= kMax && d <= kMax && t * d <= (1ll << 40);
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_epi_status gemm_epi_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d, int64_t f,
+                                  gemm_epi_dtype dtype)
+{
+    return make_ffn_plan(out, t, d, f, dtype, false);
+}
+
+gemm_epi_status gemm_epi_ffn_plan_layernorm(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d,
+                                            int64_t f, gemm_epi_dtype dtype)
+{
+    if (d == 0) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+    return make_ffn_plan(out, t, d, f, dtype, true);
+}
+
+gemm_epi_status gemm_epi_ffn_execute_layernorm(gemm_epi_ffn_plan_t p, const void* X, float eps,
+                                               const void* W1_folded, const float* colsum,
+                                               const float* b1_folded, const void* W2,
+                                               const void* b2, const void* R, void* Y,
+                                               cudaStream_t stream)
+{
+    if (!p || !p->layernorm || !(eps >= 0.0f)) return GEMM_EPI_ERR_INVALID_ARG;
+    gemm_epi_operands o1 = make_operands(X, W1_folded, nullptr, nullptr, p->H ? p->H : Y, nullptr);
+    o1.ln_stats = p->stats ? p->stats : colsum;  // (t == 0: never read)
+    o1.ln_colsum = colsum;
+    o1.ln_bias = b1_folded;
+    const gemm_epi_operands o2 = make_operands(p->H, W2, b2, R, Y, nullptr);
+    gemm_epi_status st = check_operands(p->g1, o1);
+    if (st != GEMM_EPI_OK) return st;
+    st = check_operands(p->g2, o2);
+    if (st != GEMM_EPI_OK) return st;
+    if (p->t == 0) return GEMM_EPI_OK;
+    st = check_device(p->g1);
+    if (st != GEMM_EPI_OK) return st;
+    if (layernorm_stats_launch(X, static_cast<int>(p->t), static_cast<int>(p->d),
+                               p->dtype == GEMM_EPI_BF16 ? 1 : 0, eps, p->stats,
+                               p->g1->sm_count, stream) != cudaSuccess)
+        return GEMM_EPI_ERR_LAUNCH;
+    st = run_plan(p->g1, o1, stream, true);
+    if (st != GEMM_EPI_OK) return st;
+    return run_plan(p->g2, o2, stream, p->g1->variant != kEmpty);
+}
+
+gemm_epi_status gemm_epi_layernorm(int64_t t, int64_t d, gemm_epi_dtype dtype, const void* X,
+                                   const void* residual, const void* gamma, const void* beta,
+                                   float eps, void* Y, cudaStream_t stream)
+{
+    if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
+    if (!ln_shape_ok(t, d)) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+    if (!(eps >= 0.0f) || !(eps < 1e30f)) return GEMM_EPI_ERR_INVALID_ARG;
+    if (t == 0) return GEMM_EPI_OK;
+    if (!X || !gamma || !beta || !Y) return GEMM_EPI_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || !aligned(Y, 16) || (residual && !aligned(residual, 16)) ||
+        !aligned(gamma, 2) || !aligned(beta, 2))
+        return GEMM_EPI_ERR_MISALIGNED;
+    int sms = 0;
+    gemm_epi_status st = current_device(&sms);
+    if (st != GEMM_EPI_OK) return st;
+    return layernorm_launch(X, residual, gamma, beta, Y, static_cast<int>(t), static_cast<int>(d),
+                            dtype == GEMM_EPI_BF16 ? 1 : 0, eps, sms, stream) == cudaSuccess
+               ? GEMM_EPI_OK
+               : GEMM_EPI_ERR_LAUNCH;
+}
+
+gemm_epi_status gemm_epi_layernorm_stats(int64_t t, int64_t d, gemm_epi_dtype dtype,
+                                         const void* X, float eps, float* stats,
+                                         cudaStream_t stream)
+{
+    if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
+    if (!ln_shape_ok(t, d)) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+    if (!(eps >= 0.0f) || !(eps < 1e30f)) return GEMM_EPI_ERR_INVALID_ARG;
+    if (t == 0) return GEMM_EPI_OK;
+    if (!X || !stats) return GEMM_EPI_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || !aligned(stats, 8)) return GEMM_EPI_ERR_MISALIGNED;
+    int sms = 0;
+    gemm_epi_status st = current_device(&sms);
+    if (st != GEMM_EPI_OK) return st;
+    return layernorm_stats_launch(X, static_cast<int>(t), static_cast<int>(d),
+                                  dtype == GEMM_EPI_BF16 ? 1 : 0, eps, stats, sms, stream) ==
+                   cudaSuccess
+               ? GEMM_EPI_OK
+               : GEMM_EPI_ERR_LAUNCH;
+}
+
+gemm_epi_status gemm_epi_layernorm_fold(int64_t d, int64_t f, gemm_epi_dtype dtype,
+                                        const void* gamma, const void* beta, const void* W,
+                                        const void* b, void* W_folded, float* colsum,
+                                        float* bias_folded, cudaStream_t stream)
+{
+    if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
+    if (!ln_shape_ok(f, d) || f % 8 != 0) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+    if (f == 0) return GEMM_EPI_OK;
+    if (!gamma || !beta || !W || !b || !W_folded || !colsum || !bias_folded)
+        return GEMM_EPI_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(W_folded, 16) || !aligned(gamma, 2) || !aligned(beta, 2) ||
+        !aligned(b, 2) || !aligned(colsum, 4) || !aligned(bias_folded, 4))
+        return GEMM_EPI_ERR_MISALIGNED;
+    int sms = 0;
+    gemm_epi_status st = current_device(&sms);
+    if (st != GEMM_EPI_OK) return st;
+    return layernorm_fold_launch(gamma, beta, W, b, W_folded, colsum, bias_folded,
+                                 static_cast<int>(d), static_cast<int>(f),
+                                 dtype == GEMM_EPI_BF16 ? 1 : 0, sms, stream) == cudaSuccess
+               ? GEMM_EPI_OK
+               : GEMM_EPI_ERR_LAUNCH;
 }
 
 gemm_epi_status gemm_epi_ffn_set_option(gemm_epi_ffn_plan_t p, gemm_epi_ffn_option opt,
@@ -863,7 +1047,7 @@ gemm_epi_status gemm_epi_ffn_execute(gemm_epi_ffn_plan_t p, const void* X, const
                                      const void* b1, const void* W2, const void* b2,
                                      const void* R, void* Y, cudaStream_t stream)
 {
-    if (!p) return GEMM_EPI_ERR_INVALID_ARG;
+    if (!p || p->layernorm) return GEMM_EPI_ERR_INVALID_ARG;
     const gemm_epi_operands o1 = make_operands(X, W1, b1, nullptr, p->H ? p->H : Y, nullptr);
     const gemm_epi_operands o2 = make_operands(p->H, W2, b2, R, Y, nullptr);
     gemm_epi_status st = check_operands(p->g1, o1);
@@ -895,6 +1079,7 @@ gemm_epi_status gemm_epi_ffn_free(gemm_epi_ffn_plan_t p)
     if (!p) return GEMM_EPI_OK;
     if (p->H) cudaFree(p->H);
     if (p->ready) cudaFree(p->ready);
+    if (p->stats) cudaFree(p->stats);
     gemm_epi_free(p->g1);
     gemm_epi_free(p->g2);
     delete p;

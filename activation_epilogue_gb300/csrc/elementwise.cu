@@ -71,17 +71,23 @@ constexpr int kWarps = 8;
 // gradient: an (m,1) row's share is a warp sum; a (1,n) column's share is summed in the
 // lane over its rows, then over the 8 warps through shared memory, then one atomic per
 // column and task.
-__global__ void __launch_bounds__(256) elementwise_epilogue_kernel(
-    const uint16_t* __restrict__ pre, const uint16_t* __restrict__ bias,
-    const uint16_t* __restrict__ residual, uint16_t* __restrict__ D, void* __restrict__ aux,
-    const void* __restrict__ aux_in, float* __restrict__ dbias, int m, int n, int epilog,
-    int bias_layout, int bf16, int aux_ld)
+__global__ void __launch_bounds__(256) elementwise_epilogue_kernel(const ElementwiseArgs a)
 {
     __shared__ float col_part[kWarps][kCols];
+    const uint16_t* __restrict__ pre = static_cast<const uint16_t*>(a.pre);
+    const uint16_t* __restrict__ bias = static_cast<const uint16_t*>(a.bias);
+    const uint16_t* __restrict__ residual = static_cast<const uint16_t*>(a.residual);
+    uint16_t* __restrict__ D = static_cast<uint16_t*>(a.D);
+    void* aux = a.aux;
+    const void* aux_in = a.aux_in;
+    float* dbias = a.dbias;
+    const int m = a.m, n = a.n, epilog = a.epilog, bias_layout = a.bias_layout, bf16 = a.bf16,
+              aux_ld = a.aux_ld;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const bool bwd = is_backward(epilog);
-    const bool has_bias = epilog != EPI_NONE && !bwd;
+    const bool ln = epilog == EPI_LN_GELU_BIAS;
+    const bool has_bias = epilog != EPI_NONE && !bwd && !ln;
     const long long groups_per_row = (n + kCols - 1) / kCols;
     const long long tasks = static_cast<long long>((m + kRows - 1) / kRows) * groups_per_row;
     for (long long task = blockIdx.x; task < tasks; task += gridDim.x) {
@@ -90,9 +96,16 @@ __global__ void __launch_bounds__(256) elementwise_epilogue_kernel(
         const int col = g * kCols + lane * 8;  // this lane's first column
         const bool ok = col < n;
         float cb[8];                           // (1,n) bias of the lane's columns
+        float lc[8];                           // LayerNorm: c_j (and b'_j in cb)
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < 8; ++j) {
             cb[j] = (has_bias && bias_layout == 1 && ok) ? ld16(bias, col + j, bf16) : 0.0f;
+            lc[j] = 0.0f;
+            if (ln && ok) {
+                lc[j] = a.ln_colsum[col + j];
+                cb[j] = a.ln_bias[col + j];
+            }
+        }
         float csum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         for (int r = warp; r < kRows; r += kWarps) {
             const int row = rt * kRows + r;
@@ -109,6 +122,11 @@ __global__ void __launch_bounds__(256) elementwise_epilogue_kernel(
                 const float rb = bias_layout == 0 ? ld16(bias, row, bf16) : 0.0f;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) v[j] += bias_layout == 0 ? rb : cb[j];
+            }
+            if (ln) {
+                const float mu = a.ln_stats[2 * row], rs = a.ln_stats[2 * row + 1];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = ok ? fmaf(rs, fmaf(-mu, lc[j], v[j]), cb[j]) : 0.0f;
             }
             if (epilog == EPI_RELU_AUX_BIAS) {
                 uint32_t bits = 0;
@@ -152,7 +170,7 @@ __global__ void __launch_bounds__(256) elementwise_epilogue_kernel(
             if (epilog == EPI_RELU_BIAS || epilog == EPI_RELU_AUX_BIAS) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) v[j] = v[j] > 0.0f ? v[j] : 0.0f;
-            } else if (epilog == EPI_GELU_BIAS || epilog == EPI_GELU_AUX_BIAS) {
+            } else if (epilog == EPI_GELU_BIAS || epilog == EPI_GELU_AUX_BIAS || ln) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) v[j] = gelu_erf_fast(v[j]);
             } else if (epilog == EPI_TANH_BIAS) {
@@ -188,19 +206,13 @@ __global__ void __launch_bounds__(256) elementwise_epilogue_kernel(
 
 }  // namespace
 
-cudaError_t elementwise_launch(const void* pre, const void* bias, const void* residual, void* D,
-                               void* aux, const void* aux_in, float* dbias, int m, int n,
-                               int epilog, int bias_layout, int bf16, int aux_ld, int sm_count,
-                               cudaStream_t stream)
+cudaError_t elementwise_launch(const ElementwiseArgs& a, int sm_count, cudaStream_t stream)
 {
-    long long blocks = static_cast<long long>((m + kRows - 1) / kRows) * ((n + kCols - 1) / kCols);
+    long long blocks = static_cast<long long>((a.m + kRows - 1) / kRows) * ((a.n + kCols - 1) / kCols);
     const long long cap = static_cast<long long>(sm_count) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    elementwise_epilogue_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(pre), static_cast<const uint16_t*>(bias),
-        static_cast<const uint16_t*>(residual), static_cast<uint16_t*>(D), aux, aux_in, dbias, m,
-        n, epilog, bias_layout, bf16, aux_ld);
+    elementwise_epilogue_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

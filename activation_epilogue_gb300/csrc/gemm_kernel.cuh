@@ -72,8 +72,8 @@ struct TileCfg {
     static constexpr int kTmemCols = pow2_at_least(2 * BN);  // two accumulators
     static constexpr int kOffEpi = kStages * kStageBytes;        // one 2 KB box per warp
     static constexpr int kEpiBytes = kEpiWarps * 2048;
-    static constexpr int kOffBias = kOffEpi + kEpiBytes;         // 256 fp32 per warp
-    static constexpr int kBiasBytes = kEpiWarps * 256 * 4;
+    static constexpr int kOffBias = kOffEpi + kEpiBytes;         // 2 x 256 fp32 per warp
+    static constexpr int kBiasBytes = kEpiWarps * 512 * 4;
     static constexpr int kOffBar = kOffBias + kBiasBytes;
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
@@ -500,7 +500,7 @@ __device__ __forceinline__ void activate(float (&v)[N], int epilog)
     if (epilog == EPI_RELU_BIAS || epilog == EPI_RELU_AUX_BIAS) {
 #pragma unroll
         for (int j = 0; j < N; ++j) v[j] = v[j] > 0.0f ? v[j] : 0.0f;
-    } else if (epilog == EPI_GELU_BIAS || epilog == EPI_GELU_AUX_BIAS) {
+    } else if (epilog == EPI_GELU_BIAS || epilog == EPI_GELU_AUX_BIAS || epilog == EPI_LN_GELU_BIAS) {
 #pragma unroll
         for (int j = 0; j < N; ++j) v[j] = gelu_erf_fast(v[j]);
     } else if (epilog == EPI_TANH_BIAS) {
@@ -655,8 +655,9 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
     const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
     const int half = ew >> 2;            // the pair's warps take alternate chunks
     const WorkRange w = work_range<PAIR>(p);
-    // This warp's own bias staging area: no other warp reads it, so a __syncwarp orders it.
-    float* sbias = reinterpret_cast<float*>(smem + C::kOffBias) + ew * 256;
+    // This warp's own staging area for per-column values (bias; LayerNorm: two arrays of
+    // 256): no other warp reads it, so a __syncwarp orders it.
+    float* sbias = reinterpret_cast<float*>(smem + C::kOffBias) + ew * 512;
     uint8_t* epi_buf = smem + C::kOffEpi + ew * 2048;
     const uint32_t epi_buf_u32 = sbase + C::kOffEpi + ew * 2048;
     // Bias, residual and the outputs may belong to a programmatic predecessor grid.
@@ -674,7 +675,11 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         const uint16_t* R = static_cast<const uint16_t*>(second ? p.residual2 : p.residual);
         const CUtensorMap* tmD = second ? &p.tm_D2 : &p.tm_D;
         const bool bwd = is_backward(epilog);
-        const bool has_bias = epilog != EPI_NONE && !bwd;
+        // LayerNorm folded into the GEMM: pre = rstd_i (acc - mu_i c_j) + b'_j, with (mu, rstd)
+        // per row of D and (c, b') per column of D, in fp32
+        // (row-tile and pair kernels only: the planner never runs it on the swapped kernel)
+        const bool ln = !SWAP && epilog == EPI_LN_GELU_BIAS;
+        const bool has_bias = epilog != EPI_NONE && !bwd && !ln;
         // Bias (and, backward, bias gradient) that varies along the accumulator's columns
         // (staged in shared memory; column sums) or along its lanes (one value per thread).
         const bool along_cols = SWAP ? p.bias_layout == 0 : p.bias_layout == 1;
@@ -719,6 +724,27 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         }
         const float lb = (lane_bias && lane_idx < lane_limit) ? load_16bit(bias_ptr, lane_idx, p.bf16)
                                                               : 0.0f;
+        // LayerNorm values: staged per accumulator column (row-tile: c_j and b'_j; swapped:
+        // mu_i and rstd_i) and one pair per lane (row-tile: mu_i, rstd_i; swapped: c_j, b'_j)
+        float ln_la = 0.0f, ln_lb = 0.0f;
+        if (ln) {
+            __syncwarp();
+            for (int i = lane; i < BN; i += 32) {
+                const int ci = col_base + i;
+                float va = 0.0f, vb = 0.0f;
+                if (ci < col_limit) {
+                    va = SWAP ? p.ln_stats[2 * ci] : p.ln_colsum[ci];
+                    vb = SWAP ? p.ln_stats[2 * ci + 1] : p.ln_bias[ci];
+                }
+                sbias[i] = va;
+                sbias[256 + i] = vb;
+            }
+            __syncwarp();
+            if (lane_idx < lane_limit) {
+                ln_la = SWAP ? p.ln_colsum[lane_idx] : p.ln_stats[2 * lane_idx];
+                ln_lb = SWAP ? p.ln_bias[lane_idx] : p.ln_stats[2 * lane_idx + 1];
+            }
+        }
 
         const int valid_cols = min(BN, col_limit - col_base);
         const int nchunks = (valid_cols + CH - 1) / CH;
@@ -801,8 +827,18 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                     }
                 }
             }
+            if (!ln) {
 #pragma unroll
-            for (int j = 0; j < CH; ++j) v[j] += col_bias ? sbias[c * CH + j] : lb;
+                for (int j = 0; j < CH; ++j) v[j] += col_bias ? sbias[c * CH + j] : lb;
+            } else {
+#pragma unroll
+                for (int j = 0; j < CH; ++j) {
+                    const float sa = sbias[c * CH + j], sb = sbias[256 + c * CH + j];
+                    const float mu = SWAP ? sa : ln_la, rs = SWAP ? sb : ln_lb;
+                    const float cc = SWAP ? ln_la : sa, bb = SWAP ? ln_lb : sb;
+                    v[j] = fmaf(rs, fmaf(-mu, cc, v[j]), bb);
+                }
+            }
 
             if constexpr (!SWAP) {
                 // ---- rows of D on lanes: thread = one row, 32 consecutive columns ----

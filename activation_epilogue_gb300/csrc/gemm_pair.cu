@@ -25,7 +25,8 @@ cudaError_t prepare_all()
                              prepare_one<BN, EPI_GELU_BIAS>(),     prepare_one<BN, EPI_RELU_AUX_BIAS>(),
                              prepare_one<BN, EPI_BIAS_RESIDUAL>(), prepare_one<BN, EPI_NONE>(),
                              prepare_one<BN, EPI_TANH_BIAS>(),     prepare_one<BN, EPI_GELU_AUX_BIAS>(),
-                             prepare_one<BN, EPI_DRELU_BGRAD>(),   prepare_one<BN, EPI_DGELU_BGRAD>()};
+                             prepare_one<BN, EPI_DRELU_BGRAD>(),   prepare_one<BN, EPI_DGELU_BGRAD>(),
+                             prepare_one<BN, EPI_LN_GELU_BIAS>()};
     for (cudaError_t x : e)
         if (x != cudaSuccess) return x;
     return cudaSuccess;
@@ -70,6 +71,7 @@ cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream, bool p
     case EPI_GELU_AUX_BIAS: return launch_one<BN, EPI_GELU_AUX_BIAS>(p, grid, stream, pdl);
     case EPI_DRELU_BGRAD: return launch_one<BN, EPI_DRELU_BGRAD>(p, grid, stream, pdl);
     case EPI_DGELU_BGRAD: return launch_one<BN, EPI_DGELU_BGRAD>(p, grid, stream, pdl);
+    case EPI_LN_GELU_BIAS: return launch_one<BN, EPI_LN_GELU_BIAS>(p, grid, stream, pdl);
     default: return cudaErrorInvalidValue;
     }
 }

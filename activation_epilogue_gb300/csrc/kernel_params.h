@@ -17,7 +17,8 @@ enum Epilog : int {
     EPI_TANH_BIAS = 6,
     EPI_GELU_AUX_BIAS = 7,  // as GELU_BIAS, and the pre-activation written to aux (16-bit)
     EPI_DRELU_BGRAD = 8,    // D = A.B * mask bit (aux_in), dbias = sums of D
-    EPI_DGELU_BGRAD = 9     // D = A.B * GELU'(aux_in pre), dbias = sums of D
+    EPI_DGELU_BGRAD = 9,    // D = A.B * GELU'(aux_in pre), dbias = sums of D
+    EPI_LN_GELU_BIAS = 10   // D = GELU(rstd_i (A.B - mu_i c_j) + b'_j): LayerNorm folded in
 };
 
 // Template value of the CTA-pair kernel that runs a whole FFN block (two GEMMs) in one launch.
@@ -56,6 +57,9 @@ struct GemmParams {
     void* aux;            // RELU_AUX_BIAS: uint32 mask words; GELU_AUX_BIAS: 16-bit pre-activation
     const void* aux_in;   // DRELU_BGRAD: mask words; DGELU_BGRAD: 16-bit pre-activation
     float* dbias;         // backward epilogs: bias gradient (zeroed before the launch)
+    const float* ln_stats;   // LN_GELU_BIAS: (mu, rstd) per row of D (per row of A)
+    const float* ln_colsum;  // LN_GELU_BIAS: c_j, column sums of the folded weight
+    const float* ln_bias;    // LN_GELU_BIAS: b'_j = beta . W + b (fp32)
     int* status;
     unsigned long long wait_limit_ns;
     int m, n, k;
@@ -120,9 +124,33 @@ cudaError_t ffn_pair_launch(const GemmParams& p, int grid, cudaStream_t stream);
 
 // Elementwise epilogue over a 16-bit pre-activation (the unfused baseline's second kernel;
 // pre == nullptr means pre = 0, which serves k == 0).
-cudaError_t elementwise_launch(const void* pre, const void* bias, const void* residual, void* D,
-                               void* aux, const void* aux_in, float* dbias, int m, int n,
-                               int epilog, int bias_layout, int bf16, int aux_ld, int sm_count,
-                               cudaStream_t stream);
+struct ElementwiseArgs {
+    const void* pre;       // 16-bit A.B (nullptr: zero, the k == 0 problem)
+    const void* bias;
+    const void* residual;
+    void* D;
+    void* aux;
+    const void* aux_in;
+    float* dbias;
+    const float* ln_stats;
+    const float* ln_colsum;
+    const float* ln_bias;
+    int m, n, epilog, bias_layout, bf16, aux_ld;
+};
+cudaError_t elementwise_launch(const ElementwiseArgs& a, int sm_count, cudaStream_t stream);
+
+// LayerNorm kernels (csrc/layernorm.cu); d must be a multiple of 8.
+// stats[2i], stats[2i+1] = mean and 1/sqrt(var + eps) of row i of X (t x d).
+cudaError_t layernorm_stats_launch(const void* X, int t, int d, int bf16, float eps,
+                                   float* stats, int sm_count, cudaStream_t stream);
+// Y = LayerNorm(X) * gamma + beta (+ residual when not nullptr), one pass per row.
+cudaError_t layernorm_launch(const void* X, const void* residual, const void* gamma,
+                             const void* beta, void* Y, int t, int d, int bf16, float eps,
+                             int sm_count, cudaStream_t stream);
+// Folding LayerNorm's affine part into the following GEMM (W: d x f):
+// Wf[k][j] = 16-bit(gamma_k W[k][j]), colsum_j = sum_k Wf[k][j], bias_f_j = sum_k beta_k W[k][j] + b_j.
+cudaError_t layernorm_fold_launch(const void* gamma, const void* beta, const void* W,
+                                  const void* b, void* Wf, float* colsum, float* bias_f, int d,
+                                  int f, int bf16, int sm_count, cudaStream_t stream);
 
 }  // namespace gemm_epi

@@ -17,7 +17,8 @@ LIB_PATH = os.path.join(PKG, "libgemmepi.so")
 
 DTYPE = {"f16": 0, "bf16": 1}
 EPILOG = {"BIAS": 0, "RELU_BIAS": 1, "GELU_BIAS": 2, "RELU_AUX_BIAS": 3, "BIAS_RESIDUAL": 4,
-          "NONE": 5, "TANH_BIAS": 6, "GELU_AUX_BIAS": 7, "DRELU_BGRAD": 8, "DGELU_BGRAD": 9}
+          "NONE": 5, "TANH_BIAS": 6, "GELU_AUX_BIAS": 7, "DRELU_BGRAD": 8, "DGELU_BGRAD": 9,
+          "LN_GELU_BIAS": 10}
 BACKWARD = ("DRELU_BGRAD", "DGELU_BGRAD")
 BIAS_LAYOUT = {"M1": 0, "1N": 1}
 OPTION = {"VARIANT": 0, "TILE_N": 1, "SPLIT_K": 2, "GRID": 3, "GROUP_M": 4,
@@ -34,7 +35,9 @@ EXPORTS = ["gemm_epi_plan", "gemm_epi_plan_set_option", "gemm_epi_execute",
            "gemm_epi_ffn_hidden", "gemm_epi_ffn_sync_status", "gemm_epi_ffn_free",
            "gemm_epi_ffn_execute_noalloc", "gemm_epi_execute_operands",
            "gemm_epi_execute_operands_unfused", "gemm_epi_ffn_set_option",
-           "gemm_epi_ffn_plan_describe"]
+           "gemm_epi_ffn_plan_describe", "gemm_epi_layernorm", "gemm_epi_layernorm_stats",
+           "gemm_epi_layernorm_fold", "gemm_epi_ffn_plan_layernorm",
+           "gemm_epi_ffn_execute_layernorm"]
 FFN_OPTION = {"LAUNCHES": 0}
 
 # Largest t * f the allocation-free FFN call accepts (its static scratch holds H).
@@ -48,7 +51,9 @@ class Operands(ctypes.Structure):
     """gemm_epi_operands: every operand of one call (NULL where the epilog uses none)."""
     _fields_ = [("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("bias", ctypes.c_void_p),
                 ("residual", ctypes.c_void_p), ("D", ctypes.c_void_p), ("aux", ctypes.c_void_p),
-                ("aux_in", ctypes.c_void_p), ("dbias", ctypes.c_void_p)]
+                ("aux_in", ctypes.c_void_p), ("dbias", ctypes.c_void_p),
+                ("ln_stats", ctypes.c_void_p), ("ln_colsum", ctypes.c_void_p),
+                ("ln_bias", ctypes.c_void_p)]
 
 
 class GemmEpiError(RuntimeError):
@@ -103,6 +108,18 @@ def load_library(path: str | None = None):
         lib.gemm_epi_ffn_set_option.argtypes = [vp, i32, i64]
         lib.gemm_epi_ffn_plan_describe.restype = ctypes.c_char_p
         lib.gemm_epi_ffn_plan_describe.argtypes = [vp]
+        f32 = ctypes.c_float
+        lib.gemm_epi_layernorm.restype = i32
+        lib.gemm_epi_layernorm.argtypes = [i64, i64, i32, vp, vp, vp, vp, f32, vp, vp]
+        lib.gemm_epi_layernorm_stats.restype = i32
+        lib.gemm_epi_layernorm_stats.argtypes = [i64, i64, i32, vp, f32, vp, vp]
+        lib.gemm_epi_layernorm_fold.restype = i32
+        lib.gemm_epi_layernorm_fold.argtypes = [i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.gemm_epi_ffn_plan_layernorm.restype = i32
+        lib.gemm_epi_ffn_plan_layernorm.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i32]
+        lib.gemm_epi_ffn_execute_layernorm.restype = i32
+        lib.gemm_epi_ffn_execute_layernorm.argtypes = [vp, vp, f32, vp, vp, vp, vp, vp, vp, vp,
+                                                       vp]
         lib.gemm_epi_execute_operands.restype = i32
         lib.gemm_epi_execute_operands.argtypes = [vp, ctypes.POINTER(Operands), vp]
         lib.gemm_epi_execute_operands_unfused.restype = i32
@@ -173,24 +190,63 @@ def gemm_epi_execute_unfused(plan, A, B, bias, residual, pre, D, aux=None, strea
            "gemm_epi_execute_unfused")
 
 
-def _operands(A, B, bias, residual, D, aux, aux_in, dbias) -> Operands:
+def _operands(A, B, bias, residual, D, aux, aux_in, dbias, ln=None) -> Operands:
+    ln_stats, ln_colsum, ln_bias = ln if ln is not None else (None, None, None)
     return Operands(_ptr(A), _ptr(B), _ptr(bias), _ptr(residual), _ptr(D), _ptr(aux),
-                    _ptr(aux_in), _ptr(dbias))
+                    _ptr(aux_in), _ptr(dbias), _ptr(ln_stats), _ptr(ln_colsum), _ptr(ln_bias))
 
 
 def gemm_epi_execute_operands(plan, A, B, D, bias=None, residual=None, aux=None, aux_in=None,
-                              dbias=None, stream=None):
-    ops = _operands(A, B, bias, residual, D, aux, aux_in, dbias)
+                              dbias=None, stream=None, ln=None):
+    """ln: (stats, colsum, bias_folded) for the LN_GELU_BIAS epilog."""
+    ops = _operands(A, B, bias, residual, D, aux, aux_in, dbias, ln)
     _check(load_library().gemm_epi_execute_operands(plan, ctypes.byref(ops), _stream(stream)),
            "gemm_epi_execute_operands")
 
 
 def gemm_epi_execute_operands_unfused(plan, A, B, D, pre, bias=None, residual=None, aux=None,
-                                      aux_in=None, dbias=None, stream=None):
-    ops = _operands(A, B, bias, residual, D, aux, aux_in, dbias)
+                                      aux_in=None, dbias=None, stream=None, ln=None):
+    ops = _operands(A, B, bias, residual, D, aux, aux_in, dbias, ln)
     _check(load_library().gemm_epi_execute_operands_unfused(plan, ctypes.byref(ops), _ptr(pre),
                                                             _stream(stream)),
            "gemm_epi_execute_operands_unfused")
+
+
+def gemm_epi_layernorm(t: int, d: int, dtype: str, X, residual, gamma, beta, eps: float, Y,
+                       stream=None):
+    _check(load_library().gemm_epi_layernorm(t, d, DTYPE[dtype], _ptr(X), _ptr(residual),
+                                             _ptr(gamma), _ptr(beta), float(eps), _ptr(Y),
+                                             _stream(stream)), "gemm_epi_layernorm")
+
+
+def gemm_epi_layernorm_stats(t: int, d: int, dtype: str, X, eps: float, stats, stream=None):
+    _check(load_library().gemm_epi_layernorm_stats(t, d, DTYPE[dtype], _ptr(X), float(eps),
+                                                   _ptr(stats), _stream(stream)),
+           "gemm_epi_layernorm_stats")
+
+
+def gemm_epi_layernorm_fold(d: int, f: int, dtype: str, gamma, beta, W, b, W_folded, colsum,
+                            bias_folded, stream=None):
+    _check(load_library().gemm_epi_layernorm_fold(d, f, DTYPE[dtype], _ptr(gamma), _ptr(beta),
+                                                  _ptr(W), _ptr(b), _ptr(W_folded),
+                                                  _ptr(colsum), _ptr(bias_folded),
+                                                  _stream(stream)), "gemm_epi_layernorm_fold")
+
+
+def gemm_epi_ffn_plan_layernorm(t: int, d: int, f: int, dtype: str = "bf16"):
+    h = ctypes.c_void_p()
+    _check(load_library().gemm_epi_ffn_plan_layernorm(ctypes.byref(h), t, d, f, DTYPE[dtype]),
+           "gemm_epi_ffn_plan_layernorm")
+    return h.value
+
+
+def gemm_epi_ffn_execute_layernorm(plan, X, eps: float, W1_folded, colsum, b1_folded, W2, b2, R,
+                                   Y, stream=None):
+    _check(load_library().gemm_epi_ffn_execute_layernorm(plan, _ptr(X), float(eps),
+                                                         _ptr(W1_folded), _ptr(colsum),
+                                                         _ptr(b1_folded), _ptr(W2), _ptr(b2),
+                                                         _ptr(R), _ptr(Y), _stream(stream)),
+           "gemm_epi_ffn_execute_layernorm")
 
 
 def gemm_epi_free(plan):
@@ -261,9 +317,10 @@ def gemm_epi_ffn_execute_noalloc(t: int, d: int, f: int, dtype: str, X, W1, b1, 
 class FfnPlan:
     """The FFN block Y = GELU(X.W1 + b1).W2 + b2 + R as one plan (two fused launches)."""
 
-    def __init__(self, t, d, f, dtype="bf16", **options):
+    def __init__(self, t, d, f, dtype="bf16", layernorm=False, **options):
         self.t, self.d, self.f, self.dtype = t, d, f, dtype
-        self.handle = gemm_epi_ffn_plan(t, d, f, dtype)
+        self.handle = (gemm_epi_ffn_plan_layernorm(t, d, f, dtype) if layernorm
+                       else gemm_epi_ffn_plan(t, d, f, dtype))
         for key, value in options.items():
             gemm_epi_ffn_set_option(self.handle, key.upper(), value)
 
@@ -272,6 +329,11 @@ class FfnPlan:
 
     def execute(self, X, W1, b1, W2, b2, R, Y, stream=None):
         gemm_epi_ffn_execute(self.handle, X, W1, b1, W2, b2, R, Y, stream)
+
+    def execute_layernorm(self, X, eps, W1_folded, colsum, b1_folded, W2, b2, R, Y,
+                          stream=None):
+        gemm_epi_ffn_execute_layernorm(self.handle, X, eps, W1_folded, colsum, b1_folded, W2,
+                                       b2, R, Y, stream)
 
     def hidden(self):
         """The plan's H buffer as a torch tensor view (t x f) on the current device."""
@@ -335,14 +397,15 @@ class Plan:
         return gemm_epi_plan_describe(self.handle)
 
     def execute(self, A, B, bias, D, aux=None, residual=None, stream=None, aux_in=None,
-                dbias=None):
+                dbias=None, ln=None):
         gemm_epi_execute_operands(self.handle, A, B, D, bias=bias, residual=residual, aux=aux,
-                                  aux_in=aux_in, dbias=dbias, stream=stream)
+                                  aux_in=aux_in, dbias=dbias, stream=stream, ln=ln)
 
     def execute_unfused(self, A, B, bias, pre, D, aux=None, residual=None, stream=None,
-                        aux_in=None, dbias=None):
+                        aux_in=None, dbias=None, ln=None):
         gemm_epi_execute_operands_unfused(self.handle, A, B, D, pre, bias=bias, residual=residual,
-                                          aux=aux, aux_in=aux_in, dbias=dbias, stream=stream)
+                                          aux=aux, aux_in=aux_in, dbias=dbias, stream=stream,
+                                          ln=ln)
 
     def sync_status(self, stream=None) -> int:
         return gemm_epi_sync_status(self.handle, stream)

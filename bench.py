@@ -489,6 +489,37 @@ def measure_ffn(device, stream, flush, peaks):
                     "tensor_frac_cold": f.flops / cold / 1e12 / peaks["bf16_tflops"],
                     "unfused_us_cold_l2": cold_unf * 1e6, "unfused_launches": 4,
                     "status": fp.sync_status(), "plan": fp.describe()}
+    # the pre-LayerNorm block Y = X + FFN(LayerNorm(X)) (LayerNorm gamma ~ 1 + N(0, 0.1^2),
+    # beta ~ N(0, 0.1^2)): row statistics + GEMM 1 with the LayerNorm folded into its
+    # epilogue + GEMM 2, against the fused LayerNorm kernel writing LN(X) followed by the FFN
+    g = torch.Generator(device=device)
+    g.manual_seed(1006)
+    gamma = (1.0 + 0.1 * torch.randn(f.d, generator=g, device=device)).to(torch.bfloat16)
+    beta = (0.1 * torch.randn(f.d, generator=g, device=device)).to(torch.bfloat16)
+    W1f = torch.empty_like(fi["W1"])
+    cs = torch.empty(f.f, dtype=torch.float32, device=device)
+    b1f = torch.empty(f.f, dtype=torch.float32, device=device)
+    gemm_epi.gemm_epi_layernorm_fold(f.d, f.f, "bf16", gamma, beta, fi["W1"], fi["b1"], W1f, cs,
+                                     b1f)
+    Xn = torch.empty_like(fi["X"])
+    with gemm_epi.FfnPlan(f.t, f.d, f.f, "bf16", layernorm=True) as lp, \
+            gemm_epi.FfnPlan(f.t, f.d, f.f, "bf16") as fp:
+        def ln_ffn():
+            lp.execute_layernorm(fi["X"], 1e-5, W1f, cs, b1f, fi["W2"], fi["b2"], fi["X"], Y)
+
+        def ln_then_ffn():
+            gemm_epi.gemm_epi_layernorm(f.t, f.d, "bf16", fi["X"], None, gamma, beta, 1e-5, Xn)
+            fp.execute(Xn, fi["W1"], fi["b1"], fi["W2"], fi["b2"], fi["X"], Y)
+        cold = time_cold(ln_ffn, 20, stream, flush)
+        hot = time_graph(ln_ffn, 10, 10, stream)
+        cold_sep = time_cold(ln_then_ffn, 20, stream, flush)
+        hot_sep = time_graph(ln_then_ffn, 10, 10, stream)
+        out[f.name + "_layernorm"] = {
+            "us_per_call_cold_l2": cold * 1e6, "us_per_call_graph_hot_l2": hot * 1e6,
+            "tflops_cold": f.flops / cold / 1e12,
+            "separate_layernorm_us_cold_l2": cold_sep * 1e6,
+            "separate_layernorm_us_graph_hot_l2": hot_sep * 1e6,
+            "status": lp.sync_status(), "plan": lp.describe()}
     return out
 
 

@@ -89,9 +89,16 @@ typedef enum {
     GEMM_EPI_DRELU_BGRAD = 8,   /* backward of RELU_AUX_BIAS: D = (A.B) * mask, mask from
                                    aux_in (the RELU_AUX_BIAS layout), and dbias = the sums
                                    of that product along the bias's broadcast direction */
-    GEMM_EPI_DGELU_BGRAD = 9    /* backward of GELU_AUX_BIAS: D = (A.B) * GELU'(pre), pre
+    GEMM_EPI_DGELU_BGRAD = 9,   /* backward of GELU_AUX_BIAS: D = (A.B) * GELU'(pre), pre
                                    from aux_in (the GELU_AUX_BIAS layout), GELU'(x) =
                                    Phi(x) + x phi(x); dbias as for DRELU_BGRAD */
+    GEMM_EPI_LN_GELU_BIAS = 10  /* D = GELU(LayerNorm(A) . W + b) with the LayerNorm folded
+                                   into the epilogue: B is W' = diag(gamma) W from
+                                   gemm_epi_layernorm_fold, and the operands carry ln_stats
+                                   (mean, 1/sqrt(var + eps) per row of A, from
+                                   gemm_epi_layernorm_stats), ln_colsum and ln_bias; D =
+                                   GELU(rstd_i (A.B)_ij - rstd_i mu_i c_j + b'_j).  bias must
+                                   be NULL; k >= 1 */
 } gemm_epi_epilog;
 
 typedef enum {
@@ -205,6 +212,9 @@ typedef struct {
     void* aux;
     const void* aux_in;
     float* dbias;
+    const float* ln_stats;   /* LN_GELU_BIAS: m pairs (mean, rstd), 8-byte aligned */
+    const float* ln_colsum;  /* LN_GELU_BIAS: n column sums of W' */
+    const float* ln_bias;    /* LN_GELU_BIAS: n values beta . W + b */
 } gemm_epi_operands;
 
 /* The fused kernel on the operands in *ops (any epilog of the plan). */
@@ -217,6 +227,34 @@ gemm_epi_status gemm_epi_execute_operands(gemm_epi_plan_t p, const gemm_epi_oper
 gemm_epi_status gemm_epi_execute_operands_unfused(gemm_epi_plan_t p,
                                                   const gemm_epi_operands* ops, void* pre,
                                                   cudaStream_t stream);
+
+/* ---- LayerNorm ---------------------------------------------------------------------------
+ * "Operator fusion in model inference, from LayerNorm to residual connections"
+ * (wmrh.cn/news/429806), section 2: y = (x - mu) / sqrt(var + eps) * gamma + beta over each
+ * row of X (t x d; var the biased variance of the row), optionally plus a residual, in one
+ * pass.  d must be a multiple of 8 and >= 8; X, Y, residual, W and W_folded 16-byte
+ * aligned, gamma, beta, b 2-byte aligned, the fp32 outputs 4-byte (stats 8-byte) aligned;
+ * eps >= 0.  Asynchronous on `stream`; the caller owns every buffer. */
+
+/* Y = LayerNorm(X) * gamma + beta (+ residual when not NULL; Y may be X or the residual). */
+gemm_epi_status gemm_epi_layernorm(int64_t t, int64_t d, gemm_epi_dtype dtype, const void* X,
+                                   const void* residual, const void* gamma, const void* beta,
+                                   float eps, void* Y, cudaStream_t stream);
+
+/* stats[2i], stats[2i+1] = mean and 1/sqrt(var + eps) of row i of X: the per-row half of a
+ * LayerNorm folded into the next GEMM (epilog LN_GELU_BIAS). */
+gemm_epi_status gemm_epi_layernorm_stats(int64_t t, int64_t d, gemm_epi_dtype dtype,
+                                         const void* X, float eps, float* stats,
+                                         cudaStream_t stream);
+
+/* The per-column half, once per weight update, for the GEMM LayerNorm(x) . W + b (W: d x f):
+ * W_folded[k][j] = gamma_k W[k][j] rounded to the 16-bit type, colsum[j] = sum_k
+ * W_folded[k][j], bias_folded[j] = sum_k beta_k W[k][j] + b[j].  Then
+ * LN(x) . W + b = rstd (x . W_folded - mu colsum) + bias_folded. */
+gemm_epi_status gemm_epi_layernorm_fold(int64_t d, int64_t f, gemm_epi_dtype dtype,
+                                        const void* gamma, const void* beta, const void* W,
+                                        const void* b, void* W_folded, float* colsum,
+                                        float* bias_folded, cudaStream_t stream);
 
 /* Release the plan (the page's .free()).  NULL is accepted and ignored. */
 gemm_epi_status gemm_epi_free(gemm_epi_plan_t p);
@@ -288,6 +326,17 @@ const void* gemm_epi_ffn_hidden(gemm_epi_ffn_plan_t p);
 
 /* As gemm_epi_sync_status, for both GEMMs of the block. */
 gemm_epi_status gemm_epi_ffn_sync_status(gemm_epi_ffn_plan_t p, cudaStream_t stream);
+
+/* The pre-LayerNorm FFN block, Y = GELU(LayerNorm(X) . W1 + b1) . W2 + b2 + R (R usually X):
+ * a plan whose GEMM 1 uses the LN_GELU_BIAS epilog (two launches plus the row statistics).
+ * execute takes the folded W1 (gemm_epi_layernorm_fold) instead of W1, b1, gamma, beta. */
+gemm_epi_status gemm_epi_ffn_plan_layernorm(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d,
+                                            int64_t f, gemm_epi_dtype dtype);
+gemm_epi_status gemm_epi_ffn_execute_layernorm(gemm_epi_ffn_plan_t p, const void* X, float eps,
+                                               const void* W1_folded, const float* colsum,
+                                               const float* b1_folded, const void* W2,
+                                               const void* b2, const void* R, void* Y,
+                                               cudaStream_t stream);
 
 /* Release the plan and its H buffer (after the work that uses them has completed). */
 gemm_epi_status gemm_epi_ffn_free(gemm_epi_ffn_plan_t p);

@@ -58,7 +58,7 @@ def test_bad_enums_rejected(lib):
     import ctypes
     h = ctypes.c_void_p()
     assert lib.gemm_epi_plan(ctypes.byref(h), 8, 8, 8, 7, 0, 0) == 1
-    assert lib.gemm_epi_plan(ctypes.byref(h), 8, 8, 8, 0, 10, 0) == 1
+    assert lib.gemm_epi_plan(ctypes.byref(h), 8, 8, 8, 0, 11, 0) == 1
     assert lib.gemm_epi_plan(ctypes.byref(h), 8, 8, 8, 0, -1, 0) == 1
     assert lib.gemm_epi_plan(ctypes.byref(h), 8, 8, 8, 0, 0, 5) == 1
     assert lib.gemm_epi_plan(None, 8, 8, 8, 0, 0, 0) == 1
