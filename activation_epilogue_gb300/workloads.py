@@ -170,3 +170,18 @@ def random_backward_problem(m: int, n: int, k: int, *, dtype: str = "bf16", seed
     pre = _draw(g, (m, n), 2.0, dtype, device)
     return {"A": p["A"], "B": p["B"],
             "mask": mask.cpu().numpy().astype(np.uint32), "pre": pre}
+
+
+def random_fp8_problem(m: int, n: int, k: int, *, bias_layout: str = "1N", seed: int = 0,
+                       residual: bool = False, device="cpu") -> dict:
+    """Inputs of an FP8 GEMM: A (m x k) and Bt (n x k, B transposed) drawn N(0, 1) in fp32 and
+    rounded to E4M3 (torch's float8_e4m3fn conversion), per-tensor scales 1/sqrt(k) and 1/2
+    (so A.B scaled is O(1)), bias and residual N(0, 1) in bf16."""
+    g = _generator(seed, device)
+    A = torch.randn((m, k), generator=g, device=device).to(torch.float8_e4m3fn)
+    Bt = torch.randn((n, k), generator=g, device=device).to(torch.float8_e4m3fn)
+    out = {"A": A, "Bt": Bt, "scale_a": 1.0 / math.sqrt(max(k, 1)), "scale_b": 0.5,
+           "bias": _draw(g, (m if bias_layout == "M1" else n,), 1.0, "bf16", device)}
+    if residual:
+        out["R"] = _draw(g, (m, n), 1.0, "bf16", device)
+    return out

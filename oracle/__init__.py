@@ -92,6 +92,11 @@ def _load():
     lib.oracle_num_threads.restype = i32
     lib.oracle_num_threads.argtypes = []
     f64 = ctypes.c_double
+    lib.oracle_decode_e4m3.restype = f64
+    lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
+    lib.oracle_gemm_epi_fp8.restype = i32
+    lib.oracle_gemm_epi_fp8.argtypes = [i64, i64, i64, i32, i32, vp, vp, f64, f64, vp, vp, vp,
+                                        vp]
     lib.oracle_layernorm.restype = i32
     lib.oracle_layernorm.argtypes = [i64, i64, i32, vp, vp, vp, vp, f64, vp, vp]
     lib.oracle_ln_gemm_gelu.restype = i32
@@ -263,3 +268,41 @@ def ln_ffn(X, gamma, beta, W1, b1, W2, b2, R, *, eps: float, dtype: str = "bf16"
     if rc != 0:
         raise ValueError("oracle_ln_ffn: bad arguments or out of memory")
     return H, Hx, Y
+
+
+def _bytes8(x) -> np.ndarray:
+    """8-bit payload of a numpy uint8 array or a CPU torch 8-bit tensor (e.g. float8_e4m3fn)."""
+    if hasattr(x, "detach"):
+        import torch
+        x = x.detach().contiguous().cpu().view(torch.uint8).numpy()
+    x = np.ascontiguousarray(x)
+    if x.dtype.itemsize != 1:
+        raise TypeError(f"expected 8-bit elements, got {x.dtype}")
+    return x.view(np.uint8)
+
+
+def decode_e4m3(bits) -> np.ndarray:
+    b = _bytes8(bits)
+    lib = _load()
+    return np.array([lib.oracle_decode_e4m3(int(v)) for v in b.reshape(-1)],
+                    np.float64).reshape(b.shape)
+
+
+def gemm_epi_fp8(A, Bt, bias, *, scale_a: float, scale_b: float, epilog: str,
+                 bias_layout: str = "1N", residual=None, want_pre: bool = False):
+    """D (and pre) in double for E4M3 A (m x k) and Bt (n x k), bf16 bias / residual."""
+    A8, B8 = _bytes8(A), _bytes8(Bt)
+    m, k = A8.shape
+    n, k2 = B8.shape
+    if k2 != k:
+        raise ValueError("inner dimensions differ")
+    b16 = None if bias is None else _bits(bias).reshape(-1)
+    r16 = None if residual is None else _bits(residual)
+    D = np.empty((m, n), np.float64)
+    pre = np.empty_like(D) if want_pre else None
+    rc = _load().oracle_gemm_epi_fp8(m, n, k, EPILOGS[epilog], BIAS_LAYOUTS[bias_layout],
+                                     _ptr(A8), _ptr(B8), float(scale_a), float(scale_b),
+                                     _ptr(b16), _ptr(r16), _ptr(pre), _ptr(D))
+    if rc != 0:
+        raise ValueError("oracle_gemm_epi_fp8: bad arguments or out of memory")
+    return (D, pre) if want_pre else D

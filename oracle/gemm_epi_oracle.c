@@ -106,6 +106,27 @@ static double decode(int dtype, uint16_t h)
     return dtype == OR_BF16 ? oracle_decode_bf16(h) : oracle_decode_f16(h);
 }
 
+/*
+ * The 8-bit floating-point format E4M3 (the "FN" variant of the OCP 8-bit formats): 1 sign
+ * bit, 4 exponent bits with bias 7, 3 fraction bits; no infinities; S.1111.111 is NaN, so the
+ * largest finite magnitude is 1.75 * 2^8 = 448; exponent field 0 holds the subnormals
+ * frac/8 * 2^-6.
+ */
+double oracle_decode_e4m3(uint8_t h)
+{
+    const int sign = (h >> 7) & 1;
+    const int expo = (h >> 3) & 15;
+    const int frac = h & 7;
+    double v;
+    if (expo == 15 && frac == 7)
+        v = NAN;
+    else if (expo == 0)
+        v = ldexp((double)frac, -9);                  /* frac/8 * 2^(1-7) */
+    else
+        v = ldexp((double)(frac + 8), expo - 10);     /* (1 + frac/8) * 2^(expo-7) */
+    return sign ? -v : v;
+}
+
 /* ---- 16-bit encode, round to nearest, ties to even ---------------------------------- */
 
 /* A binary format with `fbits` fraction bits, `ebits` exponent bits and bias 2^(ebits-1)-1. */
@@ -433,6 +454,46 @@ out:
     free(cd);
     free(H);
     return rc;
+}
+
+/*
+ * FP8 inputs with per-tensor scales (the page names FP8 among the types the fused matmul
+ * supports): D = epi(sa * sb * (A . B) + bias), A: m x k E4M3 row-major, Bt: n x k E4M3
+ * row-major (B transposed: both operands contiguous along k), bias (m,1) or (1,n) and the
+ * residual in bfloat16, sa and sb the dequantisation scales.  pre (may be NULL) receives
+ * sa * sb * (A . B) + bias, D the output (both m x n, double).  Forward epilogs only.
+ */
+int oracle_gemm_epi_fp8(int64_t m, int64_t n, int64_t k, int epilog, int bias_layout,
+                        const uint8_t* A, const uint8_t* Bt, double sa, double sb,
+                        const uint16_t* bias, const uint16_t* residual, double* pre, double* D)
+{
+    if (m < 0 || n < 0 || k < 0 || !D) return -1;
+    if (epilog < OR_EPI_BIAS || epilog > OR_EPI_GELU_AUX_BIAS) return -1;
+    if (epilog != OR_EPI_NONE && !bias) return -1;
+    if (epilog == OR_EPI_BIAS_RESIDUAL && !residual) return -1;
+    double* Bd = (double*)malloc(sizeof(double) * (size_t)(n * k > 0 ? n * k : 1));
+    if (!Bd) return -1;
+    for (int64_t i = 0; i < n * k; ++i)
+        Bd[i] = oracle_decode_e4m3(Bt[i]);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < m; ++i) {
+        for (int64_t j = 0; j < n; ++j) {
+            double acc = 0.0;
+            for (int64_t q = 0; q < k; ++q)
+                acc += oracle_decode_e4m3(A[i * k + q]) * Bd[j * k + q];
+            const int64_t bi = bias_layout == OR_BIAS_M1 ? i : j;  /* the bias element */
+            const double beta = epilog != OR_EPI_NONE ? decode(OR_BF16, bias[bi]) : 0.0;
+            const double p = sa * sb * acc + beta;
+            double d = activation(epilog, p);
+            if (epilog == OR_EPI_BIAS_RESIDUAL)
+                d = p + decode(OR_BF16, residual[i * n + j]);
+            if (pre)
+                pre[i * n + j] = p;
+            D[i * n + j] = d;
+        }
+    }
+    free(Bd);
+    return 0;
 }
 
 /* GELU'(x) = Phi(x) + x phi(x): the derivative of x Phi(x), phi the standard normal density. */

@@ -36,6 +36,12 @@ MUTANTS = {
     "drelu mask bit order": ("g = (mask[i * ldw + j / 32] >> (j % 32)) & 1u ? 1.0 : 0.0;",
                              "g = (mask[i * ldw + j / 32] >> (31 - j % 32)) & 1u ? 1.0 : 0.0;"),
     "residual dropped": ("d = p + decode(dtype, residual[i * n + j]);", "d = p;"),
+    "e4m3 exponent bias": ("v = ldexp((double)(frac + 8), expo - 10);",
+                           "v = ldexp((double)(frac + 8), expo - 11);"),
+    "fp8 B not transposed": ("acc += oracle_decode_e4m3(A[i * k + q]) * Bd[j * k + q];",
+                             "acc += oracle_decode_e4m3(A[i * k + q]) * Bd[(q * n + j) % (n * k)];"),
+    "fp8 second scale dropped": ("const double p = sa * sb * acc + beta;",
+                                 "const double p = sa * acc + beta;"),
     "layernorm eps dropped": ("const double rstd = 1.0 / sqrt(var + eps);",
                               "const double rstd = 1.0 / sqrt(var);"),
     "layernorm unbiased variance": ("const double var = d > 0 ? ss / (double)d : 0.0;",

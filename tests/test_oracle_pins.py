@@ -528,3 +528,52 @@ def test_ln_ffn_is_the_composition(oracle):
     np.testing.assert_array_equal(H, oracle.encode("bf16", D))
     Y2 = oracle.gemm_epi(H, W2, b2, dtype="bf16", epilog="BIAS_RESIDUAL", residual=R)
     np.testing.assert_array_equal(Y, Y2)
+
+
+# ---- FP8 (E4M3) inputs with per-tensor scales ---------------------------------------------
+
+def test_e4m3_decode_every_pattern_matches_torch(oracle):
+    allb = np.arange(256, dtype=np.uint8)
+    got = oracle.decode_e4m3(allb)
+    want = torch.from_numpy(allb).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(want[ok]))
+    # the format's landmarks: largest finite, smallest normal, smallest subnormal, NaN
+    assert got[0x7E] == 448.0 and got[0x08] == 2.0 ** -6 and got[0x01] == 2.0 ** -9
+    assert np.isnan(got[0x7F]) and np.isnan(got[0xFF]) and got[0x80] == 0.0
+
+
+@pytest.mark.parametrize("epilog", ["BIAS", "RELU_BIAS", "GELU_BIAS", "BIAS_RESIDUAL", "NONE",
+                                    "TANH_BIAS"])
+@pytest.mark.parametrize("layout", ["M1", "1N"])
+def test_fp8_gemm_equals_the_bf16_oracle_on_the_same_values(oracle, epilog, layout):
+    # every E4M3 value is exact in bfloat16, so with unit scales the FP8 oracle must give
+    # the 16-bit oracle's result on A and B = Bt^T carried over exactly
+    m, n, k = 9, 40, 48
+    p = workloads.random_fp8_problem(m, n, k, bias_layout=layout, seed=len(epilog),
+                                     residual=True)
+    A16 = p["A"].to(torch.bfloat16)
+    B16 = p["Bt"].to(torch.bfloat16).t().contiguous()
+    assert torch.equal(A16.double(), p["A"].double()) and torch.equal(B16.t().double(), p["Bt"].double())
+    want = oracle.gemm_epi(A16, B16, p["bias"], dtype="bf16", epilog=epilog, bias_layout=layout,
+                           residual=p["R"])
+    got = oracle.gemm_epi_fp8(p["A"], p["Bt"], p["bias"], scale_a=1.0, scale_b=1.0,
+                              epilog=epilog, bias_layout=layout, residual=p["R"])
+    assert np.array_equal(got, want)
+
+
+def test_fp8_gemm_scales_and_library_matmul(oracle):
+    m, n, k = 12, 24, 64
+    p = workloads.random_fp8_problem(m, n, k, seed=3)
+    a = p["A"].double().numpy()
+    bt = p["Bt"].double().numpy()
+    sa, sb = 0.125, 3.0
+    want = sa * sb * (a @ bt.T) + p["bias"].double().numpy()[None, :]
+    got = oracle.gemm_epi_fp8(p["A"], p["Bt"], p["bias"], scale_a=sa, scale_b=sb, epilog="BIAS")
+    np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-12)
+    # only the product of the scales matters
+    got2 = oracle.gemm_epi_fp8(p["A"], p["Bt"], p["bias"], scale_a=sa * 4, scale_b=sb / 4,
+                               epilog="BIAS")
+    np.testing.assert_array_equal(got2, got)
