@@ -48,6 +48,13 @@ constexpr unsigned long long kDefaultWaitNs = 2000ull * 1000 * 1000;  // 2 s
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Epilogs built for E4M3 inputs (forward, no 16-bit auxiliary output).
+bool fp8_epilog(int e)
+{
+    return e == GEMM_EPI_BIAS || e == GEMM_EPI_RELU_BIAS || e == GEMM_EPI_GELU_BIAS ||
+           e == GEMM_EPI_RELU_AUX_BIAS || e == GEMM_EPI_BIAS_RESIDUAL || e == GEMM_EPI_NONE;
+}
+
 }  // namespace
 
 struct gemm_epi_plan_s {
@@ -136,6 +143,30 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
         p->variant = kEmpty;
     } else if (p->k == 0) {
         p->variant = kBiasOnly;
+    } else if (p->dtype == GEMM_EPI_E4M3) {
+        // E4M3: the CTA-pair kernel with 256 x 256 tiles and 128-deep K blocks, any shape
+        if ((p->opt_variant != 0 && p->opt_variant != 3) || (p->opt_bn != 0 && p->opt_bn != 256))
+            return GEMM_EPI_ERR_INVALID_ARG;
+        if (fp8_pair_prepare() != cudaSuccess || rowpair_prepare(256) != cudaSuccess)
+            return GEMM_EPI_ERR_LAUNCH;
+        p->variant = kRowPair;
+        p->bn = 256;
+        p->k_blocks = static_cast<int>((p->k + 127) / 128);
+        p->tiles_m = static_cast<int>((p->m + 255) / 256);
+        p->tiles_n = static_cast<int>((p->n + 255) / 256);
+        p->stages = rowpair_stages(256);
+        p->smem = rowpair_smem_bytes(256);
+        long long pairs = rowpair_max_clusters(256);
+        if (pairs > p->sm_count / 2) pairs = p->sm_count / 2;
+        if (p->opt_grid > 0 && p->opt_grid / 2 < pairs) pairs = p->opt_grid / 2;
+        if (pairs < 1) return GEMM_EPI_ERR_LAUNCH;
+        const long long tiles = static_cast<long long>(p->tiles_m) * p->tiles_n;
+        if (pairs > tiles) pairs = tiles;
+        p->kb_per_split = p->k_blocks;
+        p->grid = static_cast<int>(2 * pairs);
+        int gm = p->opt_group_m ? p->opt_group_m : 8;
+        if (gm > p->tiles_m) gm = p->tiles_m;
+        p->group_m = gm < 1 ? 1 : gm;
     } else {
         int v = p->opt_variant;
         if (v == 0) {
@@ -225,7 +256,8 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
              "m=%lld n=%lld k=%lld dtype=%s epilog=%s bias=%s variant=%s tile=%dx%d bk=64 "
              "stages=%d smem=%d tiles=%dx%d k_blocks=%d split_k=%d grid=%d group_m=%d sms=%d",
              static_cast<long long>(p->m), static_cast<long long>(p->n),
-             static_cast<long long>(p->k), p->dtype == GEMM_EPI_BF16 ? "bf16" : "f16",
+             static_cast<long long>(p->k),
+             p->dtype == GEMM_EPI_E4M3 ? "e4m3" : p->dtype == GEMM_EPI_BF16 ? "bf16" : "f16",
              ename[p->epilog], p->bias_layout == GEMM_EPI_BIAS_M1 ? "(m,1)" : "(1,n)",
              vname[p->variant], p->variant == kRowPair ? 256 : 128, p->bn, p->stages, p->smem, p->tiles_m, p->tiles_n, p->k_blocks,
              p->split, p->grid, p->group_m, p->sm_count);
@@ -235,12 +267,13 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
 }
 
 bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,
-               uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw)
+               uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw,
+               uint64_t elem_bytes = 2)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint64_t strides[1] = {inner * elem_bytes};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -252,6 +285,20 @@ gemm_epi_status ensure_maps(gemm_epi_plan_s* p, const void* A, const void* B, vo
 {
     if (p->maps_valid && p->key_A == A && p->key_B == B && p->key_D == D) return GEMM_EPI_OK;
     p->maps_valid = false;
+    if (p->dtype == GEMM_EPI_E4M3) {
+        // A [m][k] and B transposed [n][k], bytes, K-major boxes {128 k, 128 rows}; D bf16
+        const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        if (!encode_2d(&p->tm_A, A, u8, p->k, p->m, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
+            !encode_2d(&p->tm_B, B, u8, p->k, p->n, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
+            !encode_2d(&p->tm_D, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p->n, p->m, 32, 32,
+                       CU_TENSOR_MAP_SWIZZLE_64B))
+            return GEMM_EPI_ERR_LAUNCH;
+        p->key_A = A;
+        p->key_B = B;
+        p->key_D = D;
+        p->maps_valid = true;
+        return GEMM_EPI_OK;
+    }
     const CUtensorMapDataType dt = p->dtype == GEMM_EPI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const bool rows_of_a = p->variant == kRowTile || p->variant == kRowPair;
@@ -303,6 +350,8 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, in
     prm.ln_stats = ops.ln_stats;
     prm.ln_colsum = ops.ln_colsum;
     prm.ln_bias = ops.ln_bias;
+    prm.scale_a = ops.scale_a;
+    prm.scale_b = ops.scale_b;
     prm.status = p->d_status;
     prm.wait_limit_ns = p->wait_limit_ns;
     prm.m = static_cast<int>(p->m);
@@ -314,14 +363,16 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, in
     prm.group_m = p->group_m;
     prm.epilog = epilog;
     prm.bias_layout = p->bias_layout;
-    prm.bf16 = p->dtype == GEMM_EPI_BF16 ? 1 : 0;
+    prm.bf16 = p->dtype == GEMM_EPI_F16 ? 0 : 1;  // E4M3 plans write bf16
     prm.aux_ld = static_cast<int>((p->n + 31) / 32);
     prm.debug_stall = p->debug_stall;
     prm.split = p->split;
     prm.kb_per_split = p->kb_per_split;
     prm.prefetch = p->prefetch;
     cudaError_t e;
-    if (p->variant == kRowPair)
+    if (p->variant == kRowPair && p->dtype == GEMM_EPI_E4M3)
+        e = fp8_pair_launch(prm, p->grid, stream, pdl);
+    else if (p->variant == kRowPair)
         e = rowpair_launch(p->bn, prm, p->grid, stream, pdl);
     else if (p->variant == kRowTile)
         e = rowtile_launch(p->bn, prm, p->grid, stream, pdl);
@@ -371,7 +422,7 @@ cudaError_t run_elementwise(const gemm_epi_plan_s* p, const void* pre,
     a.n = static_cast<int>(p->n);
     a.epilog = p->epilog;
     a.bias_layout = p->bias_layout;
-    a.bf16 = p->dtype == GEMM_EPI_BF16 ? 1 : 0;
+    a.bf16 = p->dtype == GEMM_EPI_F16 ? 0 : 1;  // E4M3 plans write bf16
     a.aux_ld = static_cast<int>((p->n + 31) / 32);
     return elementwise_launch(a, p->sm_count, stream);
 }
@@ -399,6 +450,9 @@ gemm_epi_status check_operands(const gemm_epi_plan_s* p, const gemm_epi_operands
     if (o.dbias && !aligned(o.dbias, 4)) return GEMM_EPI_ERR_MISALIGNED;
     // An empty problem touches no operand but dbias (its matrices may have no storage).
     if (p->variant == kEmpty) return GEMM_EPI_OK;
+    const bool f8 = p->dtype == GEMM_EPI_E4M3;
+    if ((o.scale_a != nullptr) != f8 || (o.scale_b != nullptr) != f8) return GEMM_EPI_ERR_INVALID_ARG;
+    if (f8 && (!aligned(o.scale_a, 4) || !aligned(o.scale_b, 4))) return GEMM_EPI_ERR_MISALIGNED;
     const bool ln = e == GEMM_EPI_LN_GELU_BIAS;
     if (((o.ln_stats != nullptr) != ln) || ((o.ln_colsum != nullptr) != ln) ||
         ((o.ln_bias != nullptr) != ln))
@@ -447,14 +501,18 @@ gemm_epi_status gemm_epi_plan(gemm_epi_plan_t* out, int64_t m, int64_t n, int64_
 {
     if (!out) return GEMM_EPI_ERR_INVALID_ARG;
     *out = nullptr;
-    if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
+    if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16 && dtype != GEMM_EPI_E4M3)
+        return GEMM_EPI_ERR_INVALID_ARG;
     if (epilog < GEMM_EPI_BIAS || epilog > GEMM_EPI_LN_GELU_BIAS) return GEMM_EPI_ERR_INVALID_ARG;
+    if (dtype == GEMM_EPI_E4M3 && !fp8_epilog(epilog)) return GEMM_EPI_ERR_INVALID_ARG;
     if (bias_layout != GEMM_EPI_BIAS_M1 && bias_layout != GEMM_EPI_BIAS_1N)
         return GEMM_EPI_ERR_INVALID_ARG;
     const int64_t kMax = (1ll << 31) - 1;
     if (m < 0 || n < 0 || k < 0 || m > kMax || n > kMax || k > kMax)
         return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
     if (n % 8 != 0 || k % 8 != 0) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+    // E4M3 rows are k bytes long: a multiple of 16 for the tensor-memory-access unit
+    if (dtype == GEMM_EPI_E4M3 && k % 16 != 0) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
     if (epilog == GEMM_EPI_LN_GELU_BIAS && k == 0) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
 
     int ndev = 0;
@@ -603,7 +661,9 @@ gemm_epi_status gemm_epi_execute_operands_unfused(gemm_epi_plan_t p,
     if (st != GEMM_EPI_OK || p->variant == kEmpty) return st;
     const void* pre_in = nullptr;
     if (p->variant != kBiasOnly) {
-        const gemm_epi_operands g = make_operands(ops->A, ops->B, nullptr, nullptr, pre, nullptr);
+        gemm_epi_operands g = make_operands(ops->A, ops->B, nullptr, nullptr, pre, nullptr);
+        g.scale_a = ops->scale_a;  // E4M3: the GEMM applies the scales
+        g.scale_b = ops->scale_b;
         st = launch_gemm(p, g, EPI_NONE, stream);
         if (st != GEMM_EPI_OK) return st;
         pre_in = pre;
@@ -843,6 +903,7 @@ gemm_epi_status make_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d, in
 {
     if (!out) return GEMM_EPI_ERR_INVALID_ARG;
     *out = nullptr;
+    if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
     gemm_epi_plan_t g1 = nullptr, g2 = nullptr;
     gemm_epi_status st = gemm_epi_plan(&g1, t, f, d, dtype,
                                        layernorm ? GEMM_EPI_LN_GELU_BIAS : GEMM_EPI_GELU_BIAS,

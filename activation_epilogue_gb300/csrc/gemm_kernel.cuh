@@ -272,7 +272,7 @@ __device__ __forceinline__ uint16_t to16(float a, int bf16)
 // producer: TMA loads
 // ------------------------------------------------------------------------------------------
 // Arm stage `stage` for K block `kb` of tile (tm, tn) and issue its TMA loads.
-template <int BN, bool SWAP, bool PAIR = false>
+template <int BN, bool SWAP, bool PAIR = false, bool F8 = false>
 __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase, uint32_t bar0,
                                             int stage, int tm, int tn, int kb, int prob = 0)
 {
@@ -281,6 +281,18 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase,
     const uint32_t sa = sbase + stage * C::kStageBytes;
     const uint32_t sb = sa + C::kABytes;
     const int k0 = kb * kBK;
+    if constexpr (PAIR && F8) {
+        // E4M3: a K block is 128 elements (one 128-byte swizzle row); A rows and the rows of
+        // B transposed (columns of D) are both K-major boxes {128 k, 128 rows} of 16 KB.
+        static_assert(BN == 256, "the FP8 pair kernel runs 256-wide tiles");
+        const uint32_t rank = cluster_ctarank();
+        if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::kStageBytes);
+        const uint32_t fb0 = map_shared_rank(fb, 0);
+        const int k8 = kb * 128;
+        tma_load_2d_pair(sa, &p.tm_A, fb0, k8, tm * 2 * kBM + static_cast<int>(rank) * kBM);
+        tma_load_2d_pair(sb, &p.tm_B, fb0, k8, tn * BN + static_cast<int>(rank) * (BN / 2));
+        return;
+    }
     if constexpr (PAIR) {
         // Both CTAs' halves are counted on the even CTA's "full" barrier, which that CTA
         // arms with the bytes of both (the odd CTA's bytes may land first: the
@@ -348,7 +360,7 @@ __device__ __forceinline__ int producer_prologue(const GemmParams& p, uint32_t s
 }
 
 // The producer loop, continuing after the `pre` stages the prologue issued.
-template <int BN, bool SWAP, bool PAIR = false, bool FFN = false>
+template <int BN, bool SWAP, bool PAIR = false, bool FFN = false, bool F8 = false>
 __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase, uint32_t bar0,
                                              volatile int* abort_flag, int pre)
 {
@@ -376,7 +388,7 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
                 ok = false;
                 break;
             }
-            issue_stage<BN, SWAP, PAIR>(p, sbase, bar0, stage, t.tm, t.tn, kb, t.prob);
+            issue_stage<BN, SWAP, PAIR, F8>(p, sbase, bar0, stage, t.tm, t.tn, kb, t.prob);
             if (!PAIR && p.prefetch && kb + p.prefetch < t.kb_end)
                 prefetch_stage<BN, SWAP>(p, t.tm, t.tn, kb + p.prefetch);
             ++issued;
@@ -402,7 +414,7 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
 // ------------------------------------------------------------------------------------------
 // MMA issuer
 // ------------------------------------------------------------------------------------------
-template <int BN, bool SWAP, bool PAIR = false, bool FFN = false>
+template <int BN, bool SWAP, bool PAIR = false, bool FFN = false, bool F8 = false>
 __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uint32_t bar0,
                                         uint32_t tmem_base, volatile int* abort_flag)
 {
@@ -410,8 +422,10 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
     // Row-tile: A operand K-major (rows of A), B operand N-major (rows of B).
     // Swapped:  A operand N-major (rows of B), B operand K-major (rows of A).
     // Pair: M = 256 across the two CTAs; only the even CTA issues.
-    const uint32_t idesc = make_idesc_f16(static_cast<uint32_t>(p.bf16), SWAP ? 1u : 0u,
-                                          SWAP ? 0u : 1u, PAIR ? 2 * kBM : kBM, BN);
+    // E4M3 (F8): both operands K-major, 32 K elements (32 bytes) per MMA.
+    const uint32_t idesc = F8 ? make_idesc_e4m3(2 * kBM, BN)
+                              : make_idesc_f16(static_cast<uint32_t>(p.bf16), SWAP ? 1u : 0u,
+                                               SWAP ? 0u : 1u, PAIR ? 2 * kBM : kBM, BN);
     const WorkRange w = work_range<PAIR>(p);
     if (PAIR && w.pair_rank != 0) return;
     int stage = 0;
@@ -443,7 +457,10 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
 #pragma unroll
             for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
                 uint64_t ad, bd;
-                if (!SWAP) {
+                if (F8) {
+                    ad = make_sdesc_sw128(sa + kk * 32, 0, 1024);
+                    bd = make_sdesc_sw128(sb + kk * 32, 0, 1024);
+                } else if (!SWAP) {
                     // K-major: +32 bytes per 16-element K step inside the swizzled row;
                     // 8-row groups 1024 bytes apart.
                     ad = make_sdesc_sw128(sa + kk * 32, 0, 1024);
@@ -454,7 +471,9 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
                     ad = make_sdesc_sw128(sa + kk * 2048, 8192, 1024);
                     bd = make_sdesc_sw128(sb + kk * 32, 0, 1024);
                 }
-                if constexpr (PAIR)
+                if constexpr (PAIR && F8)
+                    mma_f8_ss_pair(d_tmem, ad, bd, idesc, (kb > w.kb_begin || kk > 0) ? 1u : 0u);
+                else if constexpr (PAIR)
                     mma_f16_ss_pair(d_tmem, ad, bd, idesc, (kb > w.kb_begin || kk > 0) ? 1u : 0u);
                 else
                     mma_f16_ss(d_tmem, ad, bd, idesc, (kb > w.kb_begin || kk > 0) ? 1u : 0u);
@@ -639,7 +658,7 @@ __device__ __forceinline__ void publish_partials(const GemmParams& p, uint8_t* s
 
 // EPI >= 0 fixes the epilog at compile time (only its code is in the kernel); -1 reads it
 // from the parameters.
-template <int BN, bool SWAP, bool PAIR = false, int EPI = -1>
+template <int BN, bool SWAP, bool PAIR = false, int EPI = -1, bool F8 = false>
 __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem, uint32_t sbase,
                                              uint32_t bar0, uint32_t tmem_base,
                                              volatile int* abort_flag)
@@ -662,6 +681,8 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
     const uint32_t epi_buf_u32 = sbase + C::kOffEpi + ew * 2048;
     // Bias, residual and the outputs may belong to a programmatic predecessor grid.
     grid_dependency_wait();
+    // E4M3 inputs: the per-tensor dequantisation scales
+    const float fp8_scale = F8 ? __ldg(p.scale_a) * __ldg(p.scale_b) : 1.0f;
 
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -826,6 +847,10 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                         }
                     }
                 }
+            }
+            if (F8) {
+#pragma unroll
+                for (int j = 0; j < CH; ++j) v[j] *= fp8_scale;
             }
             if (!ln) {
 #pragma unroll
@@ -1014,7 +1039,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
 // ------------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------------
-template <int BN, bool SWAP, bool PAIR = false, int EPI = -1>
+template <int BN, bool SWAP, bool PAIR = false, int EPI = -1, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_constant__ GemmParams p)
 {
     using C = TileCfg<BN, PAIR>;
@@ -1082,15 +1107,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     const bool split = p.split > 1;
     if (!*abort_flag) {
         if (warp == 0) {
-            if (lane == 0) run_producer<BN, SWAP, PAIR, FFN>(p, sbase, bar0, abort_flag, pre);
+            if (lane == 0) run_producer<BN, SWAP, PAIR, FFN, F8>(p, sbase, bar0, abort_flag, pre);
             __syncwarp();
         } else if (warp == 1) {
-            if (lane == 0) run_mma<BN, SWAP, PAIR, FFN>(p, sbase, bar0, tmem_base, abort_flag);
+            if (lane == 0) run_mma<BN, SWAP, PAIR, FFN, F8>(p, sbase, bar0, tmem_base, abort_flag);
             __syncwarp();
         } else if (split) {
             publish_partials<BN, SWAP>(p, smem, bar0, tmem_base, abort_flag);
         } else {
-            run_epilogue<BN, SWAP, PAIR, EPI>(p, smem, sbase, bar0, tmem_base, abort_flag);
+            run_epilogue<BN, SWAP, PAIR, EPI, F8>(p, smem, sbase, bar0, tmem_base, abort_flag);
         }
     }
     if (split) {

@@ -60,6 +60,11 @@ struct GemmParams {
     const float* ln_stats;   // LN_GELU_BIAS: (mu, rstd) per row of D (per row of A)
     const float* ln_colsum;  // LN_GELU_BIAS: c_j, column sums of the folded weight
     const float* ln_bias;    // LN_GELU_BIAS: b'_j = beta . W + b (fp32)
+    // FP8 (E4M3) inputs (CTA-pair kernel instantiated for them): tm_B maps B transposed
+    // (n x k, K-major boxes {128 k, 128 n}); K blocks are 128 deep; the accumulator is
+    // multiplied by *scale_a * *scale_b before the bias.
+    const float* scale_a;
+    const float* scale_b;
     int* status;
     unsigned long long wait_limit_ns;
     int m, n, k;
@@ -116,6 +121,11 @@ cudaError_t rowpair_launch(int bn, const GemmParams& p, int grid, cudaStream_t s
 int rowpair_smem_bytes(int bn);
 int rowpair_stages(int bn);
 int rowpair_max_clusters(int bn);
+
+// CTA-pair kernel on E4M3 inputs (256 x 256 tiles), epilogs BIAS, RELU_BIAS, GELU_BIAS,
+// RELU_AUX_BIAS, BIAS_RESIDUAL, NONE.
+cudaError_t fp8_pair_prepare();
+cudaError_t fp8_pair_launch(const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
 
 // The FFN block in one CTA-pair launch (256 x 256 tiles); never a programmatic dependent.
 cudaError_t ffn_pair_prepare();

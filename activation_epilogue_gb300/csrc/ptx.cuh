@@ -322,6 +322,25 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 // Instruction descriptor of tcgen05.mma.kind::f16 with an fp32 accumulator.
 //   bits 4-5 D format (1 = f32); 7-9 A format and 10-12 B format (0 = f16, 1 = bf16);
 //   15 / 16 A / B major (0 = K-major, 1 = MN-major); 17-22 N >> 3; 24-28 M >> 4.
+// kind::f8f6f4 with both operands E4M3 (format 0) and K-major, fp32 accumulator: the same
+// field layout as kind::f16 with the A and B format fields 0.
+__host__ __device__ constexpr uint32_t make_idesc_e4m3(uint32_t M, uint32_t N)
+{
+    return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D (+)= A . B for 8-bit floating-point operands (32 K elements per instruction), CTA pair.
+__device__ __forceinline__ void mma_f8_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __host__ __device__ constexpr uint32_t make_idesc_f16(uint32_t bf16, uint32_t a_mn_major,
                                                       uint32_t b_mn_major, uint32_t M, uint32_t N)
 {

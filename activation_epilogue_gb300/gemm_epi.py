@@ -15,7 +15,7 @@ import threading
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libgemmepi.so")
 
-DTYPE = {"f16": 0, "bf16": 1}
+DTYPE = {"f16": 0, "bf16": 1, "e4m3": 2}
 EPILOG = {"BIAS": 0, "RELU_BIAS": 1, "GELU_BIAS": 2, "RELU_AUX_BIAS": 3, "BIAS_RESIDUAL": 4,
           "NONE": 5, "TANH_BIAS": 6, "GELU_AUX_BIAS": 7, "DRELU_BGRAD": 8, "DGELU_BGRAD": 9,
           "LN_GELU_BIAS": 10}
@@ -53,7 +53,8 @@ class Operands(ctypes.Structure):
                 ("residual", ctypes.c_void_p), ("D", ctypes.c_void_p), ("aux", ctypes.c_void_p),
                 ("aux_in", ctypes.c_void_p), ("dbias", ctypes.c_void_p),
                 ("ln_stats", ctypes.c_void_p), ("ln_colsum", ctypes.c_void_p),
-                ("ln_bias", ctypes.c_void_p)]
+                ("ln_bias", ctypes.c_void_p), ("scale_a", ctypes.c_void_p),
+                ("scale_b", ctypes.c_void_p)]
 
 
 class GemmEpiError(RuntimeError):
@@ -190,23 +191,27 @@ def gemm_epi_execute_unfused(plan, A, B, bias, residual, pre, D, aux=None, strea
            "gemm_epi_execute_unfused")
 
 
-def _operands(A, B, bias, residual, D, aux, aux_in, dbias, ln=None) -> Operands:
+def _operands(A, B, bias, residual, D, aux, aux_in, dbias, ln=None, scales=None) -> Operands:
     ln_stats, ln_colsum, ln_bias = ln if ln is not None else (None, None, None)
+    scale_a, scale_b = scales if scales is not None else (None, None)
     return Operands(_ptr(A), _ptr(B), _ptr(bias), _ptr(residual), _ptr(D), _ptr(aux),
-                    _ptr(aux_in), _ptr(dbias), _ptr(ln_stats), _ptr(ln_colsum), _ptr(ln_bias))
+                    _ptr(aux_in), _ptr(dbias), _ptr(ln_stats), _ptr(ln_colsum), _ptr(ln_bias),
+                    _ptr(scale_a), _ptr(scale_b))
 
 
 def gemm_epi_execute_operands(plan, A, B, D, bias=None, residual=None, aux=None, aux_in=None,
-                              dbias=None, stream=None, ln=None):
-    """ln: (stats, colsum, bias_folded) for the LN_GELU_BIAS epilog."""
-    ops = _operands(A, B, bias, residual, D, aux, aux_in, dbias, ln)
+                              dbias=None, stream=None, ln=None, scales=None):
+    """ln: (stats, colsum, bias_folded) for the LN_GELU_BIAS epilog; scales: (scale_a,
+    scale_b) device fp32 scalars for E4M3 plans (B is then given transposed, n x k)."""
+    ops = _operands(A, B, bias, residual, D, aux, aux_in, dbias, ln, scales)
     _check(load_library().gemm_epi_execute_operands(plan, ctypes.byref(ops), _stream(stream)),
            "gemm_epi_execute_operands")
 
 
 def gemm_epi_execute_operands_unfused(plan, A, B, D, pre, bias=None, residual=None, aux=None,
-                                      aux_in=None, dbias=None, stream=None, ln=None):
-    ops = _operands(A, B, bias, residual, D, aux, aux_in, dbias, ln)
+                                      aux_in=None, dbias=None, stream=None, ln=None,
+                                      scales=None):
+    ops = _operands(A, B, bias, residual, D, aux, aux_in, dbias, ln, scales)
     _check(load_library().gemm_epi_execute_operands_unfused(plan, ctypes.byref(ops), _ptr(pre),
                                                             _stream(stream)),
            "gemm_epi_execute_operands_unfused")
@@ -397,15 +402,16 @@ class Plan:
         return gemm_epi_plan_describe(self.handle)
 
     def execute(self, A, B, bias, D, aux=None, residual=None, stream=None, aux_in=None,
-                dbias=None, ln=None):
+                dbias=None, ln=None, scales=None):
         gemm_epi_execute_operands(self.handle, A, B, D, bias=bias, residual=residual, aux=aux,
-                                  aux_in=aux_in, dbias=dbias, stream=stream, ln=ln)
+                                  aux_in=aux_in, dbias=dbias, stream=stream, ln=ln,
+                                  scales=scales)
 
     def execute_unfused(self, A, B, bias, pre, D, aux=None, residual=None, stream=None,
-                        aux_in=None, dbias=None, ln=None):
+                        aux_in=None, dbias=None, ln=None, scales=None):
         gemm_epi_execute_operands_unfused(self.handle, A, B, D, pre, bias=bias, residual=residual,
                                           aux=aux, aux_in=aux_in, dbias=dbias, stream=stream,
-                                          ln=ln)
+                                          ln=ln, scales=scales)
 
     def sync_status(self, stream=None) -> int:
         return gemm_epi_sync_status(self.handle, stream)

@@ -71,7 +71,16 @@ typedef struct gemm_epi_plan_s* gemm_epi_plan_t;
 
 typedef enum {
     GEMM_EPI_F16 = 0,  /* IEEE binary16 inputs and output */
-    GEMM_EPI_BF16 = 1  /* bfloat16 inputs and output */
+    GEMM_EPI_BF16 = 1, /* bfloat16 inputs and output */
+    GEMM_EPI_E4M3 = 2  /* 8-bit floating-point inputs (E4M3: 4 exponent bits, 3 fraction bits,
+                          bias 7, no infinities, max 448) with per-tensor fp32 scales; bias,
+                          residual and D in bfloat16.  A is m x k row-major; B is given
+                          TRANSPOSED, n x k row-major (both operands contiguous along k), and
+                          k must be a multiple of 16.  D = epi(scale_a * scale_b * (A.B) +
+                          bias), scale_a and scale_b device fp32 scalars in the operands.
+                          Epilogs BIAS, RELU_BIAS, GELU_BIAS, RELU_AUX_BIAS, BIAS_RESIDUAL,
+                          NONE (gemm_epi_execute_operands); runs on the CTA-pair kernel; the
+                          page names FP8 among the fused matmul's types */
 } gemm_epi_dtype;
 
 typedef enum {
@@ -215,6 +224,8 @@ typedef struct {
     const float* ln_stats;   /* LN_GELU_BIAS: m pairs (mean, rstd), 8-byte aligned */
     const float* ln_colsum;  /* LN_GELU_BIAS: n column sums of W' */
     const float* ln_bias;    /* LN_GELU_BIAS: n values beta . W + b */
+    const float* scale_a;    /* E4M3 plans: device fp32 scale of A (NULL otherwise) */
+    const float* scale_b;    /* E4M3 plans: device fp32 scale of B */
 } gemm_epi_operands;
 
 /* The fused kernel on the operands in *ops (any epilog of the plan). */
