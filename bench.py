@@ -454,7 +454,36 @@ def measure_extras(plan, w, A, B, bias, D, aux, stream, peaks):
     per.update(measure_ffn(A.device, stream, flush, peaks))
     out["workloads"] = per
     out["backward"] = measure_backward(A.device, stream, flush, peaks)
+    out["fp8"] = measure_fp8(A.device, stream, peaks)
     return out
+
+
+def measure_fp8(device, stream, peaks):
+    """RELU_BIAS on E4M3 inputs (per-tensor scales, bf16 bias and output) at 4096^3 and at the
+    headline shape: TFLOP/s against the FP8 peak taken as the measured bf16 peak x 2 (the
+    nominal dense ratio, 4.5 / 2.25 PFLOP/s).  Inputs larger than L2 at the headline shape;
+    4096^3 reported hot (back-to-back calls)."""
+    import torch
+
+    from activation_epilogue_gb300 import gemm_epi, workloads
+    peak8 = 2.0 * peaks["bf16_tflops"]
+    res = {}
+    for m, n, k in [(4096, 4096, 4096), (65536, 16384, 8192)]:
+        p = workloads.random_fp8_problem(m, n, k, seed=1008, device=device)
+        sa = torch.tensor([p["scale_a"]], dtype=torch.float32, device=device)
+        sb = torch.tensor([p["scale_b"]], dtype=torch.float32, device=device)
+        D = torch.empty((m, n), dtype=torch.bfloat16, device=device)
+        with gemm_epi.Plan(m, n, k, "e4m3", "RELU_BIAS", "1N") as pl:
+            fn = lambda: pl.execute(p["A"], p["Bt"], p["bias"], D, scales=(sa, sb))  # noqa: E731
+            steps = 5 if m > 8192 else 50
+            secs = time_steps(fn, steps, 3, stream) / steps
+            tf = 2.0 * m * n * k / secs / 1e12
+            res[f"relu_bias_e4m3_{m}x{n}x{k}"] = {
+                "us_per_call": secs * 1e6, "tflops": tf, "peak_tflops": peak8,
+                "frac_of_fp8_peak": tf / peak8, "status": pl.sync_status(), "plan": pl.describe()}
+        del p, D
+        torch.cuda.empty_cache()
+    return res
 
 
 def measure_ffn(device, stream, flush, peaks):
@@ -580,7 +609,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--only", choices=["backward", "ffn"],
+    ap.add_argument("--only", choices=["backward", "ffn", "fp8"],
                     help="print only these measurements (one JSON object), for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -602,8 +631,11 @@ def main():
         torch.cuda.set_device(dev)
         stream = torch.cuda.current_stream()
         flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
-        measure = measure_backward if args.only == "backward" else measure_ffn
-        res = measure(dev, stream, flush_buf.zero_, load_peaks()[0])
+        if args.only == "fp8":
+            res = measure_fp8(dev, stream, load_peaks()[0])
+        else:
+            measure = measure_backward if args.only == "backward" else measure_ffn
+            res = measure(dev, stream, flush_buf.zero_, load_peaks()[0])
         if rank == 0:
             print(json.dumps({args.only: res}))
         return
