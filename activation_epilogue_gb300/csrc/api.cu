@@ -253,13 +253,15 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
                                   "TANH_BIAS",     "GELU_AUX_BIAS", "DRELU_BGRAD",
                                   "DGELU_BGRAD",   "LN_GELU_BIAS"};
     snprintf(p->desc, sizeof(p->desc),
-             "m=%lld n=%lld k=%lld dtype=%s epilog=%s bias=%s variant=%s tile=%dx%d bk=64 "
+             "m=%lld n=%lld k=%lld dtype=%s epilog=%s bias=%s variant=%s tile=%dx%d bk=%d "
              "stages=%d smem=%d tiles=%dx%d k_blocks=%d split_k=%d grid=%d group_m=%d sms=%d",
              static_cast<long long>(p->m), static_cast<long long>(p->n),
              static_cast<long long>(p->k),
              p->dtype == GEMM_EPI_E4M3 ? "e4m3" : p->dtype == GEMM_EPI_BF16 ? "bf16" : "f16",
              ename[p->epilog], p->bias_layout == GEMM_EPI_BIAS_M1 ? "(m,1)" : "(1,n)",
-             vname[p->variant], p->variant == kRowPair ? 256 : 128, p->bn, p->stages, p->smem, p->tiles_m, p->tiles_n, p->k_blocks,
+             vname[p->variant], p->variant == kRowPair ? 256 : 128, p->bn,
+             p->dtype == GEMM_EPI_E4M3 ? 128 : 64, p->stages, p->smem, p->tiles_m, p->tiles_n,
+             p->k_blocks,
              p->split, p->grid, p->group_m, p->sm_count);
     const char* log = getenv("GEMM_EPI_LOG");
     if (log && log[0] == '1') fprintf(stderr, "[gemm_epi] plan: %s\n", p->desc);
