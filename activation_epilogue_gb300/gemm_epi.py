@@ -37,7 +37,7 @@ EXPORTS = ["gemm_epi_plan", "gemm_epi_plan_set_option", "gemm_epi_execute",
            "gemm_epi_execute_operands_unfused", "gemm_epi_ffn_set_option",
            "gemm_epi_ffn_plan_describe", "gemm_epi_layernorm", "gemm_epi_layernorm_stats",
            "gemm_epi_layernorm_fold", "gemm_epi_ffn_plan_layernorm",
-           "gemm_epi_ffn_execute_layernorm"]
+           "gemm_epi_ffn_execute_layernorm", "gemm_epi_execute_host"]
 FFN_OPTION = {"LAUNCHES": 0}
 
 # Largest t * f the allocation-free FFN call accepts (its static scratch holds H).
@@ -121,6 +121,8 @@ def load_library(path: str | None = None):
         lib.gemm_epi_ffn_execute_layernorm.restype = i32
         lib.gemm_epi_ffn_execute_layernorm.argtypes = [vp, vp, f32, vp, vp, vp, vp, vp, vp, vp,
                                                        vp]
+        lib.gemm_epi_execute_host.restype = i32
+        lib.gemm_epi_execute_host.argtypes = [vp, ctypes.POINTER(Operands), vp]
         lib.gemm_epi_execute_operands.restype = i32
         lib.gemm_epi_execute_operands.argtypes = [vp, ctypes.POINTER(Operands), vp]
         lib.gemm_epi_execute_operands_unfused.restype = i32
@@ -206,6 +208,14 @@ def gemm_epi_execute_operands(plan, A, B, D, bias=None, residual=None, aux=None,
     ops = _operands(A, B, bias, residual, D, aux, aux_in, dbias, ln, scales)
     _check(load_library().gemm_epi_execute_operands(plan, ctypes.byref(ops), _stream(stream)),
            "gemm_epi_execute_operands")
+
+
+def gemm_epi_execute_host(plan, A, B, D, bias=None, residual=None, aux=None, stream=None):
+    """The fused call on host tensors (CPU, contiguous, preferably pinned): copies in, GEMM and
+    copies out pipelined in row chunks by the library; ordered on `stream`."""
+    ops = _operands(A, B, bias, residual, D, aux, None, None)
+    _check(load_library().gemm_epi_execute_host(plan, ctypes.byref(ops), _stream(stream)),
+           "gemm_epi_execute_host")
 
 
 def gemm_epi_execute_operands_unfused(plan, A, B, D, pre, bias=None, residual=None, aux=None,
@@ -406,6 +416,10 @@ class Plan:
         gemm_epi_execute_operands(self.handle, A, B, D, bias=bias, residual=residual, aux=aux,
                                   aux_in=aux_in, dbias=dbias, stream=stream, ln=ln,
                                   scales=scales)
+
+    def execute_host(self, A, B, bias, D, aux=None, residual=None, stream=None):
+        gemm_epi_execute_host(self.handle, A, B, D, bias=bias, residual=residual, aux=aux,
+                              stream=stream)
 
     def execute_unfused(self, A, B, bias, pre, D, aux=None, residual=None, stream=None,
                         aux_in=None, dbias=None, ln=None, scales=None):

@@ -1,0 +1,95 @@
+"""The fused call on HOST buffers (gemm_epi_execute_host): chunked, pipelined copies and
+GEMMs, checked against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from activation_epilogue_gb300 import gemm_epi, workloads
+from parity_helpers import AUX_BAND, TD, TOL, aux_bad_bits, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from activation_epilogue_gb300 import build
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+
+
+def _host(t, pinned=True):
+    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=pinned)
+    h.copy_(t)
+    return h
+
+
+def _run_host(p, m, n, k, dtype, epilog, layout, pinned=True, plan=None, options=None):
+    A, B = _host(p["A"], pinned), _host(p["B"], pinned)
+    bias = _host(p["bias"], pinned) if epilog != "NONE" else None
+    R = _host(p["R"], pinned) if epilog == "BIAS_RESIDUAL" else None
+    D = torch.full((m, n), float("nan"), dtype=TD[dtype], pin_memory=pinned)
+    aux = None
+    if epilog == "RELU_AUX_BIAS":
+        aux = torch.full((m, (n + 31) // 32), -1, dtype=torch.int32, pin_memory=pinned)
+    elif epilog == "GELU_AUX_BIAS":
+        aux = torch.full((m, n), float("nan"), dtype=TD[dtype], pin_memory=pinned)
+    own = plan is None
+    if own:
+        plan = gemm_epi.Plan(m, n, k, dtype, epilog, layout, **(options or {}))
+    try:
+        plan.execute_host(A, B, bias, D, aux=aux, residual=R)
+        torch.cuda.current_stream().synchronize()
+        assert plan.sync_status() == 0
+    finally:
+        if own:
+            plan.free()
+    return D, aux
+
+
+@pytest.mark.parametrize("m", [300, 5000, 9000])
+@pytest.mark.parametrize("epilog,layout", [("BIAS", "M1"), ("RELU_AUX_BIAS", "1N"),
+                                           ("BIAS_RESIDUAL", "1N"), ("GELU_AUX_BIAS", "M1"),
+                                           ("TANH_BIAS", "1N"), ("NONE", "1N")])
+def test_execute_host_parity(m, epilog, layout):
+    n, k = 264, 136
+    p = workloads.random_problem(m, n, k, dtype="bf16", bias_layout=layout, residual=True,
+                                 seed=m + len(epilog))
+    D, aux = _run_host(p, m, n, k, "bf16", epilog, layout)
+    want, pre = oracle.gemm_epi(p["A"], p["B"], None if epilog == "NONE" else p["bias"],
+                                dtype="bf16", epilog=epilog, bias_layout=layout,
+                                residual=p["R"] if epilog == "BIAS_RESIDUAL" else None,
+                                want_pre=True)
+    assert rel_err(D, want) <= TOL["bf16"]
+    if epilog == "RELU_AUX_BIAS":
+        assert aux_bad_bits(aux.numpy().view(np.uint32), pre, AUX_BAND) == 0
+    if epilog == "GELU_AUX_BIAS":
+        assert rel_err(aux, pre) <= TOL["bf16"]
+
+
+def test_execute_host_pageable_memory_and_reuse():
+    m, n, k = 3000, 520, 200
+    p = workloads.random_problem(m, n, k, dtype="f16", seed=3)
+    want = oracle.gemm_epi(p["A"], p["B"], p["bias"], dtype="f16", epilog="GELU_BIAS")
+    with gemm_epi.Plan(m, n, k, "f16", "GELU_BIAS", "1N") as plan:
+        for pinned in (False, True, True):
+            D, _ = _run_host(p, m, n, k, "f16", "GELU_BIAS", "1N", pinned=pinned, plan=plan)
+            assert rel_err(D, want) <= TOL["f16"]
+        plan.set_option("TILE_N", 128)          # the chunk plans are rebuilt
+        D, _ = _run_host(p, m, n, k, "f16", "GELU_BIAS", "1N", plan=plan)
+        assert rel_err(D, want) <= TOL["f16"]
+
+
+def test_execute_host_rules():
+    h = torch.zeros((64, 64), dtype=torch.bfloat16, pin_memory=True)
+    with gemm_epi.Plan(64, 64, 64, "bf16", "DRELU_BGRAD", "1N") as plan:
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.execute_host(h, h, None, h)
+        assert e.value.status == 1
+    with gemm_epi.Plan(64, 64, 64, "bf16", "BIAS", "1N") as plan:
+        with pytest.raises(gemm_epi.GemmEpiError) as e:        # bias missing
+            plan.execute_host(h, h, None, h)
+        assert e.value.status == 1
+    with gemm_epi.Plan(0, 64, 64, "bf16", "BIAS", "1N") as plan:  # empty: nothing to do
+        plan.execute_host(None, None, None, None)
