@@ -21,8 +21,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgemmepi.so")
-SOURCES = ["api.cu", "gemm_pair.cu", "gemm_rowtile.cu", "gemm_swapped.cu", "elementwise.cu",
-           "layernorm.cu"]
+SOURCES = ["api.cu", "host_exec.cu", "ffn_api.cu", "layernorm_api.cu", "gemm_pair.cu",
+           "gemm_rowtile.cu", "gemm_swapped.cu", "elementwise.cu", "layernorm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -13,10 +13,10 @@
 #include <mutex>
 #include <new>
 
-#include "gemm_epi.h"
-#include "kernel_params.h"
+#include "plan.h"
 
 using namespace gemm_epi;
+using namespace gemm_epi_impl;
 
 namespace {
 
@@ -40,50 +40,6 @@ EncodeTiledFn encode_fn()
     });
     return g_encode;
 }
-
-enum Variant { kEmpty = 0, kRowTile = 1, kSwapped = 2, kBiasOnly = 3, kRowPair = 4 };
-
-constexpr int kSwappedMaxM = 256;
-constexpr unsigned long long kDefaultWaitNs = 2000ull * 1000 * 1000;  // 2 s
-
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// Epilogs built for E4M3 inputs (forward, no 16-bit auxiliary output).
-bool fp8_epilog(int e)
-{
-    return e == GEMM_EPI_BIAS || e == GEMM_EPI_RELU_BIAS || e == GEMM_EPI_GELU_BIAS ||
-           e == GEMM_EPI_RELU_AUX_BIAS || e == GEMM_EPI_BIAS_RESIDUAL || e == GEMM_EPI_NONE;
-}
-
-}  // namespace
-
-struct HostPipe;
-
-struct gemm_epi_plan_s {
-    int64_t m, n, k;
-    int dtype, epilog, bias_layout;
-    int device, sm_count;
-    // chosen configuration
-    int variant, bn, stages, smem, grid, group_m, tiles_m, tiles_n, k_blocks;
-    int split, kb_per_split;  // split-K across a cluster (split == 1: persistent kernel)
-    // options (0 = automatic)
-    int opt_variant, opt_bn, opt_split_k, opt_grid, opt_group_m;
-    int prefetch;  // L2 prefetch distance in K blocks (GEMM_EPI_OPT_PREFETCH)
-    int no_pdl;    // 1: launch without programmatic dependent launch (GEMM_EPI_OPT_PDL = 0)
-    unsigned long long wait_limit_ns;
-    int debug_stall;
-    int* d_status;
-    // tensor maps for the last (A, B, D) pointers
-    const void* key_A;
-    const void* key_B;
-    const void* key_D;
-    bool maps_valid;
-    CUtensorMap tm_A, tm_B, tm_D;
-    char desc[320];
-    HostPipe* host;  // gemm_epi_execute_host's streams, buffers and chunk plans
-};
-
-namespace {
 
 // Split-K is used only when GEMM_EPI_OPT_SPLIT_K asks for it.  Measured on GB300, the
 // cluster launch, the two cluster barriers and the partial-sum exchange cost more than the
@@ -133,6 +89,16 @@ int pick_pair_bn(int64_t m, int64_t n, long long pairs)
     const long long w256 = (tm * ((n + 255) / 256) + pairs - 1) / pairs;
     const long long w224 = (tm * ((n + 223) / 224) + pairs - 1) / pairs;
     return w224 <= w256 ? 224 : 256;
+}
+
+}  // namespace
+
+namespace gemm_epi_impl {
+
+bool fp8_epilog(int e)
+{
+    return e == GEMM_EPI_BIAS || e == GEMM_EPI_RELU_BIAS || e == GEMM_EPI_GELU_BIAS ||
+           e == GEMM_EPI_RELU_AUX_BIAS || e == GEMM_EPI_BIAS_RESIDUAL || e == GEMM_EPI_NONE;
 }
 
 gemm_epi_status configure(gemm_epi_plan_s* p)
@@ -273,7 +239,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
 
 bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,
                uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw,
-               uint64_t elem_bytes = 2)
+               uint64_t elem_bytes)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
@@ -336,8 +302,24 @@ gemm_epi_status check_device(const gemm_epi_plan_s* p)
     return GEMM_EPI_OK;
 }
 
+gemm_epi_status current_device(int* sms)
+{
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev < 1) {
+        cudaGetLastError();
+        return GEMM_EPI_ERR_NO_DEVICE;
+    }
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_EPI_ERR_NO_DEVICE;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3) return GEMM_EPI_ERR_ARCH;
+    return GEMM_EPI_OK;
+}
+
 gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, int epilog,
-                            cudaStream_t stream, bool pdl = false)
+                            cudaStream_t stream, bool pdl)
 {
     gemm_epi_status st = ensure_maps(p, ops.A, ops.B, ops.D);
     if (st != GEMM_EPI_OK) return st;
@@ -392,8 +374,6 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, in
     return GEMM_EPI_OK;
 }
 
-gemm_epi_status check_device(const gemm_epi_plan_s* p);
-
 bool backward(int epilog) { return epilog == GEMM_EPI_DRELU_BGRAD || epilog == GEMM_EPI_DGELU_BGRAD; }
 
 int64_t dbias_len(const gemm_epi_plan_s* p) { return p->bias_layout == GEMM_EPI_BIAS_M1 ? p->m : p->n; }
@@ -432,8 +412,6 @@ cudaError_t run_elementwise(const gemm_epi_plan_s* p, const void* pre,
     return elementwise_launch(a, p->sm_count, stream);
 }
 
-// One fused call on an already-checked plan: empty problems launch nothing, k == 0 runs the
-// elementwise epilogue on the bias alone, everything else the GEMM kernel.
 gemm_epi_status run_plan(gemm_epi_plan_s* p, const gemm_epi_operands& ops, cudaStream_t stream,
                          bool pdl)
 {
@@ -496,211 +474,7 @@ gemm_epi_operands make_operands(const void* A, const void* B, const void* bias,
     return o;
 }
 
-}  // namespace
-
-// ---- host buffers: row chunks, pipelined copies and GEMMs ---------------------------------
-
-// gemm_epi_execute_host: A, D (and residual, aux) are split into row chunks; chunk j's
-// host-to-device copy, GEMM and device-to-host copy run on three streams, each waiting only
-// for what it needs, with two device slots per chunked operand, so the copies of chunks
-// j+1 and j-1 overlap the GEMM of chunk j.  B and the bias are copied once per call.
-struct HostPipe {
-    int64_t chunk = 0;  // rows per chunk (the last may be shorter)
-    cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
-    cudaEvent_t ev_start = nullptr, ev_shared = nullptr;
-    cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_comp[2] = {nullptr, nullptr},
-                ev_out[2] = {nullptr, nullptr};
-    void* dA[2] = {nullptr, nullptr};
-    void* dD[2] = {nullptr, nullptr};
-    void* dR[2] = {nullptr, nullptr};
-    void* dAux[2] = {nullptr, nullptr};
-    void* dB = nullptr;
-    void* dBias = nullptr;
-    gemm_epi_plan_s full{}, last{};  // the chunk plans (sharing the parent's status word)
-    bool has_last = false;
-};
-
-namespace {
-
-void destroy_host_pipe(gemm_epi_plan_s* p)
-{
-    HostPipe* h = p->host;
-    if (!h) return;
-    for (cudaStream_t st : {h->s_in, h->s_comp, h->s_out})
-        if (st) {
-            cudaStreamSynchronize(st);
-            cudaStreamDestroy(st);
-        }
-    for (cudaEvent_t e : {h->ev_start, h->ev_shared, h->ev_in[0], h->ev_in[1], h->ev_comp[0],
-                          h->ev_comp[1], h->ev_out[0], h->ev_out[1]})
-        if (e) cudaEventDestroy(e);
-    for (void* b : {h->dA[0], h->dA[1], h->dD[0], h->dD[1], h->dR[0], h->dR[1], h->dAux[0],
-                    h->dAux[1], h->dB, h->dBias})
-        if (b) cudaFree(b);
-    delete h;
-    p->host = nullptr;
-}
-
-// Rows per chunk: about 1024-row chunks, at most 16 of them (a chunk of a large problem still
-// fills the machine), whole 128-row tiles.  The copies out cannot start before the first
-// chunk's inputs are in and its GEMM is done, so more, smaller chunks shorten that fill;
-// measured on GB300 with ~190 GB/s each way to pinned host memory, the 65536 x 16384 x 8192
-// step is then bound by the 2 GiB copy of D out.
-int64_t host_chunk_rows(int64_t m)
-{
-    int64_t chunks = m / 1024;
-    if (chunks < 1) chunks = 1;
-    if (chunks > 16) chunks = 16;
-    int64_t rows = (m + chunks - 1) / chunks;
-    rows = (rows + 127) / 128 * 128;
-    return rows < m ? rows : m;
-}
-
-gemm_epi_status chunk_plan(const gemm_epi_plan_s* p, int64_t rows, gemm_epi_plan_s* c)
-{
-    memset(c, 0, sizeof(*c));
-    c->m = rows;
-    c->n = p->n;
-    c->k = p->k;
-    c->dtype = p->dtype;
-    c->epilog = p->epilog;
-    c->bias_layout = p->bias_layout;
-    c->device = p->device;
-    c->sm_count = p->sm_count;
-    c->opt_variant = p->opt_variant;
-    c->opt_bn = p->opt_bn;
-    c->opt_split_k = p->opt_split_k;
-    c->opt_grid = p->opt_grid;
-    c->opt_group_m = p->opt_group_m;
-    c->prefetch = p->prefetch;
-    c->no_pdl = p->no_pdl;
-    c->wait_limit_ns = p->wait_limit_ns;
-    c->d_status = p->d_status;
-    return configure(c);
-}
-
-gemm_epi_status make_host_pipe(gemm_epi_plan_s* p)
-{
-    if (p->host) return GEMM_EPI_OK;
-    HostPipe* h = new (std::nothrow) HostPipe();
-    if (!h) return GEMM_EPI_ERR_ALLOC;
-    p->host = h;
-    h->chunk = host_chunk_rows(p->m);
-    gemm_epi_status st = chunk_plan(p, h->chunk, &h->full);
-    const int64_t rem = p->m % h->chunk;
-    h->has_last = rem != 0;
-    if (st == GEMM_EPI_OK && h->has_last) st = chunk_plan(p, rem, &h->last);
-    if (st != GEMM_EPI_OK) {
-        destroy_host_pipe(p);
-        return st;
-    }
-    bool ok = true;
-    for (cudaStream_t* st2 : {&h->s_in, &h->s_comp, &h->s_out})
-        ok = ok && cudaStreamCreateWithFlags(st2, cudaStreamNonBlocking) == cudaSuccess;
-    for (cudaEvent_t* e : {&h->ev_start, &h->ev_shared, &h->ev_in[0], &h->ev_in[1], &h->ev_comp[0],
-                           &h->ev_comp[1], &h->ev_out[0], &h->ev_out[1]})
-        ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
-    const size_t e2 = 2;
-    const size_t a_bytes = static_cast<size_t>(h->chunk) * p->k * e2;
-    const size_t d_bytes = static_cast<size_t>(h->chunk) * p->n * e2;
-    const size_t aux_bytes = static_cast<size_t>(h->chunk) * ((p->n + 31) / 32) * 4;
-    const size_t b_bytes = static_cast<size_t>(p->k) * p->n * e2;
-    const size_t bias_bytes = static_cast<size_t>(p->bias_layout == GEMM_EPI_BIAS_M1 ? p->m : p->n) * e2;
-    auto alloc = [&](void** ptr, size_t bytes) {
-        if (!ok || bytes == 0) return;
-        ok = cudaMalloc(ptr, bytes) == cudaSuccess;
-    };
-    for (int s = 0; s < 2; ++s) {
-        alloc(&h->dA[s], a_bytes);
-        alloc(&h->dD[s], d_bytes);
-        if (p->epilog == GEMM_EPI_BIAS_RESIDUAL) alloc(&h->dR[s], d_bytes);
-        if (p->epilog == GEMM_EPI_RELU_AUX_BIAS || p->epilog == GEMM_EPI_GELU_AUX_BIAS)
-            alloc(&h->dAux[s], p->epilog == GEMM_EPI_GELU_AUX_BIAS ? d_bytes : aux_bytes);
-    }
-    alloc(&h->dB, b_bytes);
-    if (p->epilog != GEMM_EPI_NONE) alloc(&h->dBias, bias_bytes);
-    if (!ok) {
-        cudaGetLastError();
-        destroy_host_pipe(p);
-        return GEMM_EPI_ERR_ALLOC;
-    }
-    return GEMM_EPI_OK;
-}
-
-gemm_epi_status run_host(gemm_epi_plan_s* p, const gemm_epi_operands& o, cudaStream_t stream)
-{
-    gemm_epi_status st = make_host_pipe(p);
-    if (st != GEMM_EPI_OK) return st;
-    HostPipe* h = p->host;
-    const size_t e2 = 2;
-    const int64_t ldw = (p->n + 31) / 32;
-    const size_t aux_row = p->epilog == GEMM_EPI_GELU_AUX_BIAS ? static_cast<size_t>(p->n) * e2
-                                                             : static_cast<size_t>(ldw) * 4;
-    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
-    bool ok = cudaEventRecord(h->ev_start, stream) == cudaSuccess;
-    for (cudaStream_t s : {h->s_in, h->s_comp, h->s_out})
-        ok = ok && cudaStreamWaitEvent(s, h->ev_start, 0) == cudaSuccess;
-    // operands every chunk needs
-    if (ok && h->dB)
-        ok = cudaMemcpyAsync(h->dB, o.B, static_cast<size_t>(p->k) * p->n * e2, h2d, h->s_in) ==
-             cudaSuccess;
-    if (ok && h->dBias)
-        ok = cudaMemcpyAsync(h->dBias, o.bias,
-                             static_cast<size_t>(p->bias_layout == GEMM_EPI_BIAS_M1 ? p->m : p->n) * e2,
-                             h2d, h->s_in) == cudaSuccess;
-    ok = ok && cudaEventRecord(h->ev_shared, h->s_in) == cudaSuccess;
-    const int64_t nchunks = (p->m + h->chunk - 1) / h->chunk;
-    int last_slot = 0;
-    for (int64_t j = 0; ok && j < nchunks; ++j) {
-        const int s = static_cast<int>(j & 1);
-        const int64_t r0 = j * h->chunk;
-        const int64_t rows = p->m - r0 < h->chunk ? p->m - r0 : h->chunk;
-        gemm_epi_plan_s* c = rows == h->chunk ? &h->full : &h->last;
-        // in: slot s is free once the GEMM of chunk j - 2 has read it
-        ok = cudaStreamWaitEvent(h->s_in, h->ev_comp[s], 0) == cudaSuccess;
-        if (ok && p->k > 0)
-            ok = cudaMemcpyAsync(h->dA[s], static_cast<const char*>(o.A) + r0 * p->k * e2,
-                                 static_cast<size_t>(rows) * p->k * e2, h2d, h->s_in) == cudaSuccess;
-        if (ok && h->dR[s])
-            ok = cudaMemcpyAsync(h->dR[s], static_cast<const char*>(o.residual) + r0 * p->n * e2,
-                                 static_cast<size_t>(rows) * p->n * e2, h2d, h->s_in) == cudaSuccess;
-        ok = ok && cudaEventRecord(h->ev_in[s], h->s_in) == cudaSuccess;
-        // the GEMM: after its inputs, and after chunk j - 2's results left slot s
-        ok = ok && cudaStreamWaitEvent(h->s_comp, h->ev_in[s], 0) == cudaSuccess &&
-             cudaStreamWaitEvent(h->s_comp, h->ev_shared, 0) == cudaSuccess &&
-             cudaStreamWaitEvent(h->s_comp, h->ev_out[s], 0) == cudaSuccess;
-        if (!ok) break;
-        gemm_epi_operands co = make_operands(
-            h->dA[s], h->dB,
-            h->dBias ? static_cast<const char*>(h->dBias) +
-                           (p->bias_layout == GEMM_EPI_BIAS_M1 ? r0 * static_cast<int64_t>(e2) : 0)
-                     : nullptr,
-            h->dR[s], h->dD[s], h->dAux[s]);
-        st = run_plan(c, co, h->s_comp, false);
-        if (st != GEMM_EPI_OK) return st;
-        ok = cudaEventRecord(h->ev_comp[s], h->s_comp) == cudaSuccess;
-        // out
-        ok = ok && cudaStreamWaitEvent(h->s_out, h->ev_comp[s], 0) == cudaSuccess;
-        if (ok)
-            ok = cudaMemcpyAsync(static_cast<char*>(o.D) + r0 * p->n * e2, h->dD[s],
-                                 static_cast<size_t>(rows) * p->n * e2, d2h, h->s_out) == cudaSuccess;
-        if (ok && h->dAux[s])
-            ok = cudaMemcpyAsync(static_cast<char*>(o.aux) + r0 * aux_row, h->dAux[s],
-                                 static_cast<size_t>(rows) * aux_row, d2h, h->s_out) == cudaSuccess;
-        ok = ok && cudaEventRecord(h->ev_out[s], h->s_out) == cudaSuccess;
-        last_slot = s;
-    }
-    // the caller's stream continues once the last results are in host memory (the copies
-    // on s_out run in order, so the last one is the end of all of them)
-    ok = ok && cudaStreamWaitEvent(stream, h->ev_out[last_slot], 0) == cudaSuccess;
-    if (!ok) {
-        cudaGetLastError();
-        return GEMM_EPI_ERR_LAUNCH;
-    }
-    return GEMM_EPI_OK;
-}
-
-}  // namespace
+}  // namespace gemm_epi_impl
 
 extern "C" {
 
@@ -883,21 +657,6 @@ gemm_epi_status gemm_epi_execute_operands_unfused(gemm_epi_plan_t p,
                                                                    : GEMM_EPI_ERR_LAUNCH;
 }
 
-gemm_epi_status gemm_epi_execute_host(gemm_epi_plan_t p, const gemm_epi_operands* ops,
-                                      cudaStream_t stream)
-{
-    if (!p || !ops) return GEMM_EPI_ERR_INVALID_ARG;
-    const int e = p->epilog;
-    if (p->dtype == GEMM_EPI_E4M3 || backward(e) || e == GEMM_EPI_LN_GELU_BIAS)
-        return GEMM_EPI_ERR_INVALID_ARG;
-    gemm_epi_status st = check_operands(p, *ops);
-    if (st != GEMM_EPI_OK) return st;
-    if (p->variant == kEmpty) return GEMM_EPI_OK;
-    st = check_device(p);
-    if (st != GEMM_EPI_OK) return st;
-    return run_host(p, *ops, stream);
-}
-
 gemm_epi_status gemm_epi_execute_unfused(gemm_epi_plan_t p, const void* A, const void* B,
                                          const void* bias, const void* residual, void* pre,
                                          void* D, uint32_t* aux, cudaStream_t stream)
@@ -952,537 +711,6 @@ const char* gemm_epi_status_string(gemm_epi_status s)
 
 const char* gemm_epi_plan_describe(gemm_epi_plan_t p) { return p ? p->desc : ""; }
 
-}  // extern "C"
-
-// ---- the FFN block ----------------------------------------------------------------------
-
-struct gemm_epi_ffn_plan_s {
-    int64_t t, d, f;
-    int dtype;
-    gemm_epi_plan_t g1;  // H = GELU(X.W1 + b1):   t x f, k = d
-    gemm_epi_plan_t g2;  // Y = H.W2 + b2 + R:     t x d, k = f
-    void* H;
-    bool layernorm;      // GEMM 1 is LN_GELU_BIAS on the raw X; stats holds (mu, rstd) per row
-    float* stats;
-    // one-launch mode: both GEMMs in one CTA-pair kernel (256 x 256 tiles)
-    int opt_launches;  // GEMM_EPI_FFN_OPT_LAUNCHES value (0 = automatic)
-    bool one_launch;   // the mode in use
-    int* ready;        // per 256-row block of H: epilogue warps done with it
-    int tiles_m, tiles_n1, tiles_n2, grid;
-    const void* key_X;
-    const void* key_W1;
-    const void* key_W2;
-    const void* key_Y;
-    bool maps_valid;
-    CUtensorMap tm_X, tm_W1, tm_Hs, tm_Hl, tm_W2, tm_Y;
-    char desc[400];
-};
-
-namespace {
-
-// One launch pays off on long walks: there the second GEMM's K loops run beside the first
-// GEMM's last tiles and their GELU epilogues instead of after them.  Measured on GB300
-// (bf16, hot L2): t x d x f = 8192 x 1024 x 4096, 640 tiles of 256 x 256: 100.8 us in one
-// launch, 102.7 us in two; 4096 x 2048 x 8192: 170.6 against 173.8 us; but 4096 x 1024 x 4096,
-// 320 tiles: 65.6 against 60.5 us, where the two-launch plan's 224-wide first GEMM fills
-// its four waves exactly.  So: one launch from six waves of tiles over the resident pairs.
-bool pick_one_launch(const gemm_epi_ffn_plan_s* p, long long pairs)
-{
-    if (p->opt_launches == 1) return true;
-    if (p->opt_launches == 2) return false;
-    if (p->g1->variant != kRowPair || p->g2->variant != kRowPair) return false;
-    const long long tiles = ((p->t + 255) / 256) * ((p->f + 255) / 256 + (p->d + 255) / 256);
-    return tiles >= 6 * pairs;
-}
-
-gemm_epi_status configure_ffn(gemm_epi_ffn_plan_s* p)
-{
-    p->maps_valid = false;
-    if (p->layernorm) {  // the one-launch kernel runs GELU_BIAS only
-        p->one_launch = false;
-        snprintf(p->desc, sizeof(p->desc), "two launches after the row statistics: [%s] then [%s]",
-                 p->g1->desc, p->g2->desc);
-        return GEMM_EPI_OK;
-    }
-    p->tiles_m = static_cast<int>((p->t + 255) / 256);
-    p->tiles_n1 = static_cast<int>((p->f + 255) / 256);
-    p->tiles_n2 = static_cast<int>((p->d + 255) / 256);
-    p->grid = 0;
-    if (ffn_pair_prepare() != cudaSuccess || rowpair_prepare(256) != cudaSuccess)
-        return GEMM_EPI_ERR_LAUNCH;
-    long long pairs = rowpair_max_clusters(256);
-    if (pairs > p->g1->sm_count / 2) pairs = p->g1->sm_count / 2;
-    p->one_launch = p->t > 0 && p->d > 0 && p->f > 0 && pick_one_launch(p, pairs);
-    if (p->one_launch) {
-        const long long tiles = static_cast<long long>(p->tiles_m) * (p->tiles_n1 + p->tiles_n2);
-        if (pairs > tiles) pairs = tiles;
-        if (pairs < 1) return GEMM_EPI_ERR_LAUNCH;
-        p->grid = static_cast<int>(2 * pairs);
-        if (!p->ready && cudaMalloc(reinterpret_cast<void**>(&p->ready),
-                                    sizeof(int) * static_cast<size_t>(p->tiles_m)) != cudaSuccess) {
-            cudaGetLastError();
-            p->ready = nullptr;
-            return GEMM_EPI_ERR_ALLOC;
-        }
-        snprintf(p->desc, sizeof(p->desc),
-                 "one launch: t=%lld d=%lld f=%lld, CTA pairs on 256x256 tiles: %dx%d GEMM-1 tiles "
-                 "then %dx%d GEMM-2 tiles, grid=%d",
-                 static_cast<long long>(p->t), static_cast<long long>(p->d),
-                 static_cast<long long>(p->f), p->tiles_m, p->tiles_n1, p->tiles_m, p->tiles_n2,
-                 p->grid);
-    } else {
-        snprintf(p->desc, sizeof(p->desc), "two launches: [%s] then [%s]", p->g1->desc,
-                 p->g2->desc);
-    }
-    return GEMM_EPI_OK;
-}
-
-gemm_epi_status ensure_ffn_maps(gemm_epi_ffn_plan_s* p, const void* X, const void* W1,
-                                const void* W2, void* Y)
-{
-    if (p->maps_valid && p->key_X == X && p->key_W1 == W1 && p->key_W2 == W2 && p->key_Y == Y)
-        return GEMM_EPI_OK;
-    p->maps_valid = false;
-    const CUtensorMapDataType dt = p->dtype == GEMM_EPI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const uint64_t t = static_cast<uint64_t>(p->t), d = static_cast<uint64_t>(p->d),
-                   f = static_cast<uint64_t>(p->f);
-    const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B, sw64 = CU_TENSOR_MAP_SWIZZLE_64B;
-    if (!encode_2d(&p->tm_X, X, dt, d, t, 64, 128, sw128) ||
-        !encode_2d(&p->tm_W1, W1, dt, f, d, 64, 64, sw128) ||
-        !encode_2d(&p->tm_Hs, p->H, dt, f, t, 32, 32, sw64) ||
-        !encode_2d(&p->tm_Hl, p->H, dt, f, t, 64, 128, sw128) ||
-        !encode_2d(&p->tm_W2, W2, dt, d, f, 64, 64, sw128) ||
-        !encode_2d(&p->tm_Y, Y, dt, d, t, 32, 32, sw64))
-        return GEMM_EPI_ERR_LAUNCH;
-    p->key_X = X;
-    p->key_W1 = W1;
-    p->key_W2 = W2;
-    p->key_Y = Y;
-    p->maps_valid = true;
-    return GEMM_EPI_OK;
-}
-
-gemm_epi_status run_ffn_one_launch(gemm_epi_ffn_plan_s* p, const void* X, const void* W1,
-                                   const void* b1, const void* W2, const void* b2, const void* R,
-                                   void* Y, cudaStream_t stream)
-{
-    gemm_epi_status st = ensure_ffn_maps(p, X, W1, W2, Y);
-    if (st != GEMM_EPI_OK) return st;
-    if (cudaMemsetAsync(p->ready, 0, sizeof(int) * static_cast<size_t>(p->tiles_m), stream) !=
-        cudaSuccess)
-        return GEMM_EPI_ERR_LAUNCH;
-    const gemm_epi_plan_s* g1 = p->g1;
-    GemmParams prm;
-    memset(&prm, 0, sizeof(prm));
-    prm.tm_A = p->tm_X;
-    prm.tm_B = p->tm_W1;
-    prm.tm_D = p->tm_Hs;
-    prm.bias = b1;
-    prm.D = p->H;
-    prm.status = g1->d_status;
-    prm.wait_limit_ns = g1->wait_limit_ns;
-    prm.m = static_cast<int>(p->t);
-    prm.n = static_cast<int>(p->f);
-    prm.k = static_cast<int>(p->d);
-    prm.tiles_m = p->tiles_m;
-    prm.tiles_n = p->tiles_n1;
-    prm.k_blocks = static_cast<int>((p->d + 63) / 64);
-    prm.group_m = p->tiles_m < 8 ? p->tiles_m : 8;
-    prm.epilog = EPI_GELU_BIAS;
-    prm.bias_layout = GEMM_EPI_BIAS_1N;
-    prm.bf16 = p->dtype == GEMM_EPI_BF16 ? 1 : 0;
-    prm.aux_ld = static_cast<int>((p->f + 31) / 32);
-    prm.split = 1;
-    prm.kb_per_split = prm.k_blocks;
-    prm.tm_A2 = p->tm_Hl;
-    prm.tm_B2 = p->tm_W2;
-    prm.tm_D2 = p->tm_Y;
-    prm.bias2 = b2;
-    prm.residual2 = R;
-    prm.ffn_ready = p->ready;
-    prm.ffn_ready_target = p->tiles_n1 * 2 * kEpilogueWarps;
-    prm.ffn_tiles2 = p->tiles_m * p->tiles_n2;
-    prm.n2 = static_cast<int>(p->d);
-    prm.tiles_n2 = p->tiles_n2;
-    prm.k_blocks2 = static_cast<int>((p->f + 63) / 64);
-    const cudaError_t e = ffn_pair_launch(prm, p->grid, stream);
-    if (e != cudaSuccess) {
-        const char* log = getenv("GEMM_EPI_LOG");
-        if (log && log[0] == '1')
-            fprintf(stderr, "[gemm_epi] FFN launch failed: %s (%s)\n", cudaGetErrorString(e),
-                    p->desc);
-        return GEMM_EPI_ERR_LAUNCH;
-    }
-    return GEMM_EPI_OK;
-}
-
-}  // namespace
-
-extern "C" {
-
-}  // extern "C"
-
-namespace {
-
-gemm_epi_status make_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d, int64_t f,
-                              gemm_epi_dtype dtype, bool layernorm)
-{
-    if (!out) return GEMM_EPI_ERR_INVALID_ARG;
-    *out = nullptr;
-    if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
-    gemm_epi_plan_t g1 = nullptr, g2 = nullptr;
-    gemm_epi_status st = gemm_epi_plan(&g1, t, f, d, dtype,
-                                       layernorm ? GEMM_EPI_LN_GELU_BIAS : GEMM_EPI_GELU_BIAS,
-                                       GEMM_EPI_BIAS_1N);
-    if (st != GEMM_EPI_OK) return st;
-    st = gemm_epi_plan(&g2, t, d, f, dtype, GEMM_EPI_BIAS_RESIDUAL, GEMM_EPI_BIAS_1N);
-    if (st != GEMM_EPI_OK) {
-        gemm_epi_free(g1);
-        return st;
-    }
-    gemm_epi_ffn_plan_s* p = new (std::nothrow) gemm_epi_ffn_plan_s();
-    if (!p) {
-        gemm_epi_free(g1);
-        gemm_epi_free(g2);
-        return GEMM_EPI_ERR_ALLOC;
-    }
-    p->t = t;
-    p->d = d;
-    p->f = f;
-    p->dtype = dtype;
-    p->g1 = g1;
-    p->g2 = g2;
-    p->H = nullptr;
-    p->ready = nullptr;
-    p->stats = nullptr;
-    p->layernorm = layernorm;
-    if (t > 0 && f > 0) {
-        if (cudaMalloc(&p->H, static_cast<size_t>(t) * static_cast<size_t>(f) * 2) != cudaSuccess) {
-            cudaGetLastError();
-            gemm_epi_ffn_free(p);
-            return GEMM_EPI_ERR_ALLOC;
-        }
-    }
-    if (layernorm && t > 0) {
-        if (cudaMalloc(reinterpret_cast<void**>(&p->stats), sizeof(float) * 2 * static_cast<size_t>(t)) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            p->stats = nullptr;
-            gemm_epi_ffn_free(p);
-            return GEMM_EPI_ERR_ALLOC;
-        }
-    }
-    st = configure_ffn(p);
-    if (st != GEMM_EPI_OK) {
-        gemm_epi_ffn_free(p);
-        return st;
-    }
-    *out = p;
-    return GEMM_EPI_OK;
-}
-
-// The current device, checked to be sm_103, and its SM count.
-gemm_epi_status current_device(int* sms)
-{
-    int ndev = 0;
-    if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev < 1) {
-        cudaGetLastError();
-        return GEMM_EPI_ERR_NO_DEVICE;
-    }
-    int dev = 0, major = 0, minor = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_EPI_ERR_NO_DEVICE;
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
-    if (major != 10 || minor != 3) return GEMM_EPI_ERR_ARCH;
-    return GEMM_EPI_OK;
-}
-
-bool ln_shape_ok(int64_t t, int64_t d)
-{
-    const int64_t kMax = (1ll << 31) - 1;
-    return t >= 0 && d >= 8 && d % 8 == 0 && t <= kMax && d <= kMax && t * d <= (1ll << 40);
-}
-
-}  // namespace
-
-extern "C" {
-
-gemm_epi_status gemm_epi_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d, int64_t f,
-                                  gemm_epi_dtype dtype)
-{
-    return make_ffn_plan(out, t, d, f, dtype, false);
-}
-
-gemm_epi_status gemm_epi_ffn_plan_layernorm(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d,
-                                            int64_t f, gemm_epi_dtype dtype)
-{
-    if (d == 0) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
-    return make_ffn_plan(out, t, d, f, dtype, true);
-}
-
-gemm_epi_status gemm_epi_ffn_execute_layernorm(gemm_epi_ffn_plan_t p, const void* X, float eps,
-                                               const void* W1_folded, const float* colsum,
-                                               const float* b1_folded, const void* W2,
-                                               const void* b2, const void* R, void* Y,
-                                               cudaStream_t stream)
-{
-    if (!p || !p->layernorm || !(eps >= 0.0f)) return GEMM_EPI_ERR_INVALID_ARG;
-    gemm_epi_operands o1 = make_operands(X, W1_folded, nullptr, nullptr, p->H ? p->H : Y, nullptr);
-    o1.ln_stats = p->stats ? p->stats : colsum;  // (t == 0: never read)
-    o1.ln_colsum = colsum;
-    o1.ln_bias = b1_folded;
-    const gemm_epi_operands o2 = make_operands(p->H, W2, b2, R, Y, nullptr);
-    gemm_epi_status st = check_operands(p->g1, o1);
-    if (st != GEMM_EPI_OK) return st;
-    st = check_operands(p->g2, o2);
-    if (st != GEMM_EPI_OK) return st;
-    if (p->t == 0) return GEMM_EPI_OK;
-    st = check_device(p->g1);
-    if (st != GEMM_EPI_OK) return st;
-    if (layernorm_stats_launch(X, static_cast<int>(p->t), static_cast<int>(p->d),
-                               p->dtype == GEMM_EPI_BF16 ? 1 : 0, eps, p->stats,
-                               p->g1->sm_count, stream) != cudaSuccess)
-        return GEMM_EPI_ERR_LAUNCH;
-    st = run_plan(p->g1, o1, stream, true);
-    if (st != GEMM_EPI_OK) return st;
-    return run_plan(p->g2, o2, stream, p->g1->variant != kEmpty);
-}
-
-gemm_epi_status gemm_epi_layernorm(int64_t t, int64_t d, gemm_epi_dtype dtype, const void* X,
-                                   const void* residual, const void* gamma, const void* beta,
-                                   float eps, void* Y, cudaStream_t stream)
-{
-    if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
-    if (!ln_shape_ok(t, d)) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
-    if (!(eps >= 0.0f) || !(eps < 1e30f)) return GEMM_EPI_ERR_INVALID_ARG;
-    if (t == 0) return GEMM_EPI_OK;
-    if (!X || !gamma || !beta || !Y) return GEMM_EPI_ERR_INVALID_ARG;
-    if (!aligned(X, 16) || !aligned(Y, 16) || (residual && !aligned(residual, 16)) ||
-        !aligned(gamma, 2) || !aligned(beta, 2))
-        return GEMM_EPI_ERR_MISALIGNED;
-    int sms = 0;
-    gemm_epi_status st = current_device(&sms);
-    if (st != GEMM_EPI_OK) return st;
-    return layernorm_launch(X, residual, gamma, beta, Y, static_cast<int>(t), static_cast<int>(d),
-                            dtype == GEMM_EPI_BF16 ? 1 : 0, eps, sms, stream) == cudaSuccess
-               ? GEMM_EPI_OK
-               : GEMM_EPI_ERR_LAUNCH;
-}
-
-gemm_epi_status gemm_epi_layernorm_stats(int64_t t, int64_t d, gemm_epi_dtype dtype,
-                                         const void* X, float eps, float* stats,
-                                         cudaStream_t stream)
-{
-    if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
-    if (!ln_shape_ok(t, d)) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
-    if (!(eps >= 0.0f) || !(eps < 1e30f)) return GEMM_EPI_ERR_INVALID_ARG;
-    if (t == 0) return GEMM_EPI_OK;
-    if (!X || !stats) return GEMM_EPI_ERR_INVALID_ARG;
-    if (!aligned(X, 16) || !aligned(stats, 8)) return GEMM_EPI_ERR_MISALIGNED;
-    int sms = 0;
-    gemm_epi_status st = current_device(&sms);
-    if (st != GEMM_EPI_OK) return st;
-    return layernorm_stats_launch(X, static_cast<int>(t), static_cast<int>(d),
-                                  dtype == GEMM_EPI_BF16 ? 1 : 0, eps, stats, sms, stream) ==
-                   cudaSuccess
-               ? GEMM_EPI_OK
-               : GEMM_EPI_ERR_LAUNCH;
-}
-
-gemm_epi_status gemm_epi_layernorm_fold(int64_t d, int64_t f, gemm_epi_dtype dtype,
-                                        const void* gamma, const void* beta, const void* W,
-                                        const void* b, void* W_folded, float* colsum,
-                                        float* bias_folded, cudaStream_t stream)
-{
-    if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
-    if (!ln_shape_ok(f, d) || f % 8 != 0) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
-    if (f == 0) return GEMM_EPI_OK;
-    if (!gamma || !beta || !W || !b || !W_folded || !colsum || !bias_folded)
-        return GEMM_EPI_ERR_INVALID_ARG;
-    if (!aligned(W, 16) || !aligned(W_folded, 16) || !aligned(gamma, 2) || !aligned(beta, 2) ||
-        !aligned(b, 2) || !aligned(colsum, 4) || !aligned(bias_folded, 4))
-        return GEMM_EPI_ERR_MISALIGNED;
-    int sms = 0;
-    gemm_epi_status st = current_device(&sms);
-    if (st != GEMM_EPI_OK) return st;
-    return layernorm_fold_launch(gamma, beta, W, b, W_folded, colsum, bias_folded,
-                                 static_cast<int>(d), static_cast<int>(f),
-                                 dtype == GEMM_EPI_BF16 ? 1 : 0, sms, stream) == cudaSuccess
-               ? GEMM_EPI_OK
-               : GEMM_EPI_ERR_LAUNCH;
-}
-
-gemm_epi_status gemm_epi_ffn_set_option(gemm_epi_ffn_plan_t p, gemm_epi_ffn_option opt,
-                                        int64_t value)
-{
-    if (!p) return GEMM_EPI_ERR_INVALID_ARG;
-    if (opt != GEMM_EPI_FFN_OPT_LAUNCHES || value < 0 || value > 2) return GEMM_EPI_ERR_INVALID_ARG;
-    const int saved = p->opt_launches;
-    p->opt_launches = static_cast<int>(value);
-    gemm_epi_status st = configure_ffn(p);
-    if (st != GEMM_EPI_OK) {
-        p->opt_launches = saved;
-        configure_ffn(p);
-    }
-    return st;
-}
-
-const char* gemm_epi_ffn_plan_describe(gemm_epi_ffn_plan_t p) { return p ? p->desc : ""; }
-
-gemm_epi_status gemm_epi_ffn_execute(gemm_epi_ffn_plan_t p, const void* X, const void* W1,
-                                     const void* b1, const void* W2, const void* b2,
-                                     const void* R, void* Y, cudaStream_t stream)
-{
-    if (!p || p->layernorm) return GEMM_EPI_ERR_INVALID_ARG;
-    const gemm_epi_operands o1 = make_operands(X, W1, b1, nullptr, p->H ? p->H : Y, nullptr);
-    const gemm_epi_operands o2 = make_operands(p->H, W2, b2, R, Y, nullptr);
-    gemm_epi_status st = check_operands(p->g1, o1);
-    if (st != GEMM_EPI_OK) return st;
-    st = check_operands(p->g2, o2);
-    if (st != GEMM_EPI_OK) return st;
-    if (p->t == 0 || p->d == 0) return GEMM_EPI_OK;
-    st = check_device(p->g1);
-    if (st != GEMM_EPI_OK) return st;
-    if (p->one_launch) return run_ffn_one_launch(p, X, W1, b1, W2, b2, R, Y, stream);
-    st = run_plan(p->g1, o1, stream, true);
-    if (st != GEMM_EPI_OK) return st;
-    // GEMM 2 reads H only after GEMM 1 has completed (griddepcontrol.wait in its producer).
-    return run_plan(p->g2, o2, stream, p->g1->variant != kEmpty);
-}
-
-const void* gemm_epi_ffn_hidden(gemm_epi_ffn_plan_t p) { return p ? p->H : nullptr; }
-
-gemm_epi_status gemm_epi_ffn_sync_status(gemm_epi_ffn_plan_t p, cudaStream_t stream)
-{
-    if (!p) return GEMM_EPI_ERR_INVALID_ARG;
-    gemm_epi_status s1 = gemm_epi_sync_status(p->g1, stream);
-    gemm_epi_status s2 = gemm_epi_sync_status(p->g2, stream);
-    return s1 != GEMM_EPI_OK ? s1 : s2;
-}
-
-gemm_epi_status gemm_epi_ffn_free(gemm_epi_ffn_plan_t p)
-{
-    if (!p) return GEMM_EPI_OK;
-    if (p->H) cudaFree(p->H);
-    if (p->ready) cudaFree(p->ready);
-    if (p->stats) cudaFree(p->stats);
-    gemm_epi_free(p->g1);
-    gemm_epi_free(p->g2);
-    delete p;
-    return GEMM_EPI_OK;
-}
-
 int64_t gemm_epi_aux_words_per_row(int64_t n) { return n <= 0 ? 0 : (n + 31) / 32; }
 
 }  // extern "C"
-
-// ---- the FFN block without allocation ------------------------------------------------------
-//
-// For callers that cannot allocate device memory.  The hidden activation and the status
-// words of the two launches live in one file-scope device array; its device address is
-// looked up once per device (with that device current) and then passed to the kernels.
-
-namespace {
-
-constexpr size_t kNoAllocStatusBytes = 256;  // two status words, padded to 256 bytes
-constexpr size_t kNoAllocHiddenBytes = static_cast<size_t>(GEMM_EPI_FFN_NOALLOC_MAX_HIDDEN) * 2;
-
-// In host code this name is only a stand-in; the device address comes from
-// cudaGetSymbolAddress below.
-static __device__ __align__(256) unsigned char
-    g_ffn_noalloc_scratch[kNoAllocStatusBytes + kNoAllocHiddenBytes];
-
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mu;
-unsigned char* g_noalloc_addr[kNoAllocMaxDevices] = {};
-
-// Device address of the scratch array on device `dev` (the current device); the first call
-// per device looks it up and zeroes the status words.
-gemm_epi_status noalloc_scratch(int dev, unsigned char** out)
-{
-    if (dev < 0 || dev >= kNoAllocMaxDevices) return GEMM_EPI_ERR_INVALID_ARG;
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_ffn_noalloc_scratch) != cudaSuccess || !ptr) {
-            cudaGetLastError();
-            return GEMM_EPI_ERR_LAUNCH;
-        }
-        if (cudaMemset(ptr, 0, kNoAllocStatusBytes) != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_EPI_ERR_LAUNCH;
-        }
-        g_noalloc_addr[dev] = static_cast<unsigned char*>(ptr);
-    }
-    *out = g_noalloc_addr[dev];
-    return GEMM_EPI_OK;
-}
-
-// A plan on the caller's stack whose status word points into the static scratch.
-gemm_epi_status stack_plan(gemm_epi_plan_s* p, int64_t m, int64_t n, int64_t k, int dtype,
-                           int epilog, int dev, int sms, int* status)
-{
-    memset(p, 0, sizeof(*p));
-    p->m = m;
-    p->n = n;
-    p->k = k;
-    p->dtype = dtype;
-    p->epilog = epilog;
-    p->bias_layout = GEMM_EPI_BIAS_1N;
-    p->device = dev;
-    p->sm_count = sms;
-    p->wait_limit_ns = kDefaultWaitNs;
-    p->d_status = status;
-    return configure(p);
-}
-
-}  // namespace
-
-extern "C" gemm_epi_status gemm_epi_ffn_execute_noalloc(int64_t t, int64_t d, int64_t f,
-                                                        gemm_epi_dtype dtype, const void* X,
-                                                        const void* W1, const void* b1,
-                                                        const void* W2, const void* b2,
-                                                        const void* R, void* Y,
-                                                        cudaStream_t stream)
-{
-    if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
-    const int64_t kMax = (1ll << 31) - 1;
-    if (t < 0 || d < 0 || f < 0 || t > kMax || d > kMax || f > kMax)
-        return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
-    if (d % 8 != 0 || f % 8 != 0) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
-    if (f > 0 && t > GEMM_EPI_FFN_NOALLOC_MAX_HIDDEN / f) return GEMM_EPI_ERR_SCRATCH_LIMIT;
-
-    int dev = 0, major = 0, minor = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_EPI_ERR_NO_DEVICE;
-    }
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (major != 10 || minor != 3) return GEMM_EPI_ERR_ARCH;
-
-    unsigned char* scratch = nullptr;
-    gemm_epi_status st = noalloc_scratch(dev, &scratch);
-    if (st != GEMM_EPI_OK) return st;
-    int* status = reinterpret_cast<int*>(scratch);
-    void* H = scratch + kNoAllocStatusBytes;
-
-    gemm_epi_plan_s g1, g2;
-    st = stack_plan(&g1, t, f, d, dtype, GEMM_EPI_GELU_BIAS, dev, sms, status);
-    if (st != GEMM_EPI_OK) return st;
-    st = stack_plan(&g2, t, d, f, dtype, GEMM_EPI_BIAS_RESIDUAL, dev, sms, status + 1);
-    if (st != GEMM_EPI_OK) return st;
-    const gemm_epi_operands o1 = make_operands(X, W1, b1, nullptr, H, nullptr);
-    const gemm_epi_operands o2 = make_operands(H, W2, b2, R, Y, nullptr);
-    st = check_operands(&g1, o1);
-    if (st != GEMM_EPI_OK) return st;
-    st = check_operands(&g2, o2);
-    if (st != GEMM_EPI_OK) return st;
-    if (t == 0 || d == 0) return GEMM_EPI_OK;
-    st = run_plan(&g1, o1, stream, false);
-    if (st != GEMM_EPI_OK) return st;
-    return run_plan(&g2, o2, stream, g1.variant != kEmpty);
-}

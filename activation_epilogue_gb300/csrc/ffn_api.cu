@@ -1,0 +1,449 @@
+// The FFN block as one plan ("Operator fusion in model inference, from LayerNorm to residual
+// connections" (wmrh.cn/news/429806), section 1 and its flowchart; section 3 for the
+// residual): GEMM 1 with bias + GELU, GEMM 2 with bias + residual, run as two fused launches
+// or as one persistent CTA-pair kernel; optionally behind a LayerNorm folded into GEMM 1's
+// epilogue (section 2); and an allocation-free form of the plain block.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "plan.h"
+
+using namespace gemm_epi;
+using namespace gemm_epi_impl;
+
+struct gemm_epi_ffn_plan_s {
+    int64_t t, d, f;
+    int dtype;
+    gemm_epi_plan_t g1;  // H = GELU(X.W1 + b1):   t x f, k = d
+    gemm_epi_plan_t g2;  // Y = H.W2 + b2 + R:     t x d, k = f
+    void* H;
+    bool layernorm;      // GEMM 1 is LN_GELU_BIAS on the raw X; stats holds (mu, rstd) per row
+    float* stats;
+    // one-launch mode: both GEMMs in one CTA-pair kernel (256 x 256 tiles)
+    int opt_launches;  // GEMM_EPI_FFN_OPT_LAUNCHES value (0 = automatic)
+    bool one_launch;   // the mode in use
+    int* ready;        // per 256-row block of H: epilogue warps done with it
+    int tiles_m, tiles_n1, tiles_n2, grid;
+    const void* key_X;
+    const void* key_W1;
+    const void* key_W2;
+    const void* key_Y;
+    bool maps_valid;
+    CUtensorMap tm_X, tm_W1, tm_Hs, tm_Hl, tm_W2, tm_Y;
+    char desc[400];
+};
+
+namespace {
+
+// One launch pays off on long walks: there the second GEMM's K loops run beside the first
+// GEMM's last tiles and their GELU epilogues instead of after them.  Measured on GB300
+// (bf16, hot L2): t x d x f = 8192 x 1024 x 4096, 640 tiles of 256 x 256: 100.8 us in one
+// launch, 102.7 us in two; 4096 x 2048 x 8192: 170.6 against 173.8 us; but 4096 x 1024 x 4096,
+// 320 tiles: 65.6 against 60.5 us, where the two-launch plan's 224-wide first GEMM fills
+// its four waves exactly.  So: one launch from six waves of tiles over the resident pairs.
+bool pick_one_launch(const gemm_epi_ffn_plan_s* p, long long pairs)
+{
+    if (p->opt_launches == 1) return true;
+    if (p->opt_launches == 2) return false;
+    if (p->g1->variant != kRowPair || p->g2->variant != kRowPair) return false;
+    const long long tiles = ((p->t + 255) / 256) * ((p->f + 255) / 256 + (p->d + 255) / 256);
+    return tiles >= 6 * pairs;
+}
+
+gemm_epi_status configure_ffn(gemm_epi_ffn_plan_s* p)
+{
+    p->maps_valid = false;
+    if (p->layernorm) {  // the one-launch kernel runs GELU_BIAS only
+        p->one_launch = false;
+        snprintf(p->desc, sizeof(p->desc), "two launches after the row statistics: [%s] then [%s]",
+                 p->g1->desc, p->g2->desc);
+        return GEMM_EPI_OK;
+    }
+    p->tiles_m = static_cast<int>((p->t + 255) / 256);
+    p->tiles_n1 = static_cast<int>((p->f + 255) / 256);
+    p->tiles_n2 = static_cast<int>((p->d + 255) / 256);
+    p->grid = 0;
+    if (ffn_pair_prepare() != cudaSuccess || rowpair_prepare(256) != cudaSuccess)
+        return GEMM_EPI_ERR_LAUNCH;
+    long long pairs = rowpair_max_clusters(256);
+    if (pairs > p->g1->sm_count / 2) pairs = p->g1->sm_count / 2;
+    p->one_launch = p->t > 0 && p->d > 0 && p->f > 0 && pick_one_launch(p, pairs);
+    if (p->one_launch) {
+        const long long tiles = static_cast<long long>(p->tiles_m) * (p->tiles_n1 + p->tiles_n2);
+        if (pairs > tiles) pairs = tiles;
+        if (pairs < 1) return GEMM_EPI_ERR_LAUNCH;
+        p->grid = static_cast<int>(2 * pairs);
+        if (!p->ready && cudaMalloc(reinterpret_cast<void**>(&p->ready),
+                                    sizeof(int) * static_cast<size_t>(p->tiles_m)) != cudaSuccess) {
+            cudaGetLastError();
+            p->ready = nullptr;
+            return GEMM_EPI_ERR_ALLOC;
+        }
+        snprintf(p->desc, sizeof(p->desc),
+                 "one launch: t=%lld d=%lld f=%lld, CTA pairs on 256x256 tiles: %dx%d GEMM-1 tiles "
+                 "then %dx%d GEMM-2 tiles, grid=%d",
+                 static_cast<long long>(p->t), static_cast<long long>(p->d),
+                 static_cast<long long>(p->f), p->tiles_m, p->tiles_n1, p->tiles_m, p->tiles_n2,
+                 p->grid);
+    } else {
+        snprintf(p->desc, sizeof(p->desc), "two launches: [%s] then [%s]", p->g1->desc,
+                 p->g2->desc);
+    }
+    return GEMM_EPI_OK;
+}
+
+gemm_epi_status ensure_ffn_maps(gemm_epi_ffn_plan_s* p, const void* X, const void* W1,
+                                const void* W2, void* Y)
+{
+    if (p->maps_valid && p->key_X == X && p->key_W1 == W1 && p->key_W2 == W2 && p->key_Y == Y)
+        return GEMM_EPI_OK;
+    p->maps_valid = false;
+    const CUtensorMapDataType dt = p->dtype == GEMM_EPI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint64_t t = static_cast<uint64_t>(p->t), d = static_cast<uint64_t>(p->d),
+                   f = static_cast<uint64_t>(p->f);
+    const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B, sw64 = CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!encode_2d(&p->tm_X, X, dt, d, t, 64, 128, sw128) ||
+        !encode_2d(&p->tm_W1, W1, dt, f, d, 64, 64, sw128) ||
+        !encode_2d(&p->tm_Hs, p->H, dt, f, t, 32, 32, sw64) ||
+        !encode_2d(&p->tm_Hl, p->H, dt, f, t, 64, 128, sw128) ||
+        !encode_2d(&p->tm_W2, W2, dt, d, f, 64, 64, sw128) ||
+        !encode_2d(&p->tm_Y, Y, dt, d, t, 32, 32, sw64))
+        return GEMM_EPI_ERR_LAUNCH;
+    p->key_X = X;
+    p->key_W1 = W1;
+    p->key_W2 = W2;
+    p->key_Y = Y;
+    p->maps_valid = true;
+    return GEMM_EPI_OK;
+}
+
+gemm_epi_status run_ffn_one_launch(gemm_epi_ffn_plan_s* p, const void* X, const void* W1,
+                                   const void* b1, const void* W2, const void* b2, const void* R,
+                                   void* Y, cudaStream_t stream)
+{
+    gemm_epi_status st = ensure_ffn_maps(p, X, W1, W2, Y);
+    if (st != GEMM_EPI_OK) return st;
+    if (cudaMemsetAsync(p->ready, 0, sizeof(int) * static_cast<size_t>(p->tiles_m), stream) !=
+        cudaSuccess)
+        return GEMM_EPI_ERR_LAUNCH;
+    const gemm_epi_plan_s* g1 = p->g1;
+    GemmParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.tm_A = p->tm_X;
+    prm.tm_B = p->tm_W1;
+    prm.tm_D = p->tm_Hs;
+    prm.bias = b1;
+    prm.D = p->H;
+    prm.status = g1->d_status;
+    prm.wait_limit_ns = g1->wait_limit_ns;
+    prm.m = static_cast<int>(p->t);
+    prm.n = static_cast<int>(p->f);
+    prm.k = static_cast<int>(p->d);
+    prm.tiles_m = p->tiles_m;
+    prm.tiles_n = p->tiles_n1;
+    prm.k_blocks = static_cast<int>((p->d + 63) / 64);
+    prm.group_m = p->tiles_m < 8 ? p->tiles_m : 8;
+    prm.epilog = EPI_GELU_BIAS;
+    prm.bias_layout = GEMM_EPI_BIAS_1N;
+    prm.bf16 = p->dtype == GEMM_EPI_BF16 ? 1 : 0;
+    prm.aux_ld = static_cast<int>((p->f + 31) / 32);
+    prm.split = 1;
+    prm.kb_per_split = prm.k_blocks;
+    prm.tm_A2 = p->tm_Hl;
+    prm.tm_B2 = p->tm_W2;
+    prm.tm_D2 = p->tm_Y;
+    prm.bias2 = b2;
+    prm.residual2 = R;
+    prm.ffn_ready = p->ready;
+    prm.ffn_ready_target = p->tiles_n1 * 2 * kEpilogueWarps;
+    prm.ffn_tiles2 = p->tiles_m * p->tiles_n2;
+    prm.n2 = static_cast<int>(p->d);
+    prm.tiles_n2 = p->tiles_n2;
+    prm.k_blocks2 = static_cast<int>((p->f + 63) / 64);
+    const cudaError_t e = ffn_pair_launch(prm, p->grid, stream);
+    if (e != cudaSuccess) {
+        const char* log = getenv("GEMM_EPI_LOG");
+        if (log && log[0] == '1')
+            fprintf(stderr, "[gemm_epi] FFN launch failed: %s (%s)\n", cudaGetErrorString(e),
+                    p->desc);
+        return GEMM_EPI_ERR_LAUNCH;
+    }
+    return GEMM_EPI_OK;
+}
+
+gemm_epi_status make_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d, int64_t f,
+                              gemm_epi_dtype dtype, bool layernorm)
+{
+    if (!out) return GEMM_EPI_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
+    gemm_epi_plan_t g1 = nullptr, g2 = nullptr;
+    gemm_epi_status st = gemm_epi_plan(&g1, t, f, d, dtype,
+                                       layernorm ? GEMM_EPI_LN_GELU_BIAS : GEMM_EPI_GELU_BIAS,
+                                       GEMM_EPI_BIAS_1N);
+    if (st != GEMM_EPI_OK) return st;
+    st = gemm_epi_plan(&g2, t, d, f, dtype, GEMM_EPI_BIAS_RESIDUAL, GEMM_EPI_BIAS_1N);
+    if (st != GEMM_EPI_OK) {
+        gemm_epi_free(g1);
+        return st;
+    }
+    gemm_epi_ffn_plan_s* p = new (std::nothrow) gemm_epi_ffn_plan_s();
+    if (!p) {
+        gemm_epi_free(g1);
+        gemm_epi_free(g2);
+        return GEMM_EPI_ERR_ALLOC;
+    }
+    p->t = t;
+    p->d = d;
+    p->f = f;
+    p->dtype = dtype;
+    p->g1 = g1;
+    p->g2 = g2;
+    p->H = nullptr;
+    p->ready = nullptr;
+    p->stats = nullptr;
+    p->layernorm = layernorm;
+    if (t > 0 && f > 0) {
+        if (cudaMalloc(&p->H, static_cast<size_t>(t) * static_cast<size_t>(f) * 2) != cudaSuccess) {
+            cudaGetLastError();
+            gemm_epi_ffn_free(p);
+            return GEMM_EPI_ERR_ALLOC;
+        }
+    }
+    if (layernorm && t > 0) {
+        if (cudaMalloc(reinterpret_cast<void**>(&p->stats), sizeof(float) * 2 * static_cast<size_t>(t)) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            p->stats = nullptr;
+            gemm_epi_ffn_free(p);
+            return GEMM_EPI_ERR_ALLOC;
+        }
+    }
+    st = configure_ffn(p);
+    if (st != GEMM_EPI_OK) {
+        gemm_epi_ffn_free(p);
+        return st;
+    }
+    *out = p;
+    return GEMM_EPI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_epi_status gemm_epi_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d, int64_t f,
+                                  gemm_epi_dtype dtype)
+{
+    return make_ffn_plan(out, t, d, f, dtype, false);
+}
+
+gemm_epi_status gemm_epi_ffn_plan_layernorm(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d,
+                                            int64_t f, gemm_epi_dtype dtype)
+{
+    if (d == 0) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+    return make_ffn_plan(out, t, d, f, dtype, true);
+}
+
+gemm_epi_status gemm_epi_ffn_execute_layernorm(gemm_epi_ffn_plan_t p, const void* X, float eps,
+                                               const void* W1_folded, const float* colsum,
+                                               const float* b1_folded, const void* W2,
+                                               const void* b2, const void* R, void* Y,
+                                               cudaStream_t stream)
+{
+    if (!p || !p->layernorm || !(eps >= 0.0f)) return GEMM_EPI_ERR_INVALID_ARG;
+    gemm_epi_operands o1 = make_operands(X, W1_folded, nullptr, nullptr, p->H ? p->H : Y, nullptr);
+    o1.ln_stats = p->stats ? p->stats : colsum;  // (t == 0: never read)
+    o1.ln_colsum = colsum;
+    o1.ln_bias = b1_folded;
+    const gemm_epi_operands o2 = make_operands(p->H, W2, b2, R, Y, nullptr);
+    gemm_epi_status st = check_operands(p->g1, o1);
+    if (st != GEMM_EPI_OK) return st;
+    st = check_operands(p->g2, o2);
+    if (st != GEMM_EPI_OK) return st;
+    if (p->t == 0) return GEMM_EPI_OK;
+    st = check_device(p->g1);
+    if (st != GEMM_EPI_OK) return st;
+    if (layernorm_stats_launch(X, static_cast<int>(p->t), static_cast<int>(p->d),
+                               p->dtype == GEMM_EPI_BF16 ? 1 : 0, eps, p->stats,
+                               p->g1->sm_count, stream) != cudaSuccess)
+        return GEMM_EPI_ERR_LAUNCH;
+    st = run_plan(p->g1, o1, stream, true);
+    if (st != GEMM_EPI_OK) return st;
+    return run_plan(p->g2, o2, stream, p->g1->variant != kEmpty);
+}
+
+gemm_epi_status gemm_epi_ffn_set_option(gemm_epi_ffn_plan_t p, gemm_epi_ffn_option opt,
+                                        int64_t value)
+{
+    if (!p) return GEMM_EPI_ERR_INVALID_ARG;
+    if (opt != GEMM_EPI_FFN_OPT_LAUNCHES || value < 0 || value > 2) return GEMM_EPI_ERR_INVALID_ARG;
+    const int saved = p->opt_launches;
+    p->opt_launches = static_cast<int>(value);
+    gemm_epi_status st = configure_ffn(p);
+    if (st != GEMM_EPI_OK) {
+        p->opt_launches = saved;
+        configure_ffn(p);
+    }
+    return st;
+}
+
+const char* gemm_epi_ffn_plan_describe(gemm_epi_ffn_plan_t p) { return p ? p->desc : ""; }
+
+gemm_epi_status gemm_epi_ffn_execute(gemm_epi_ffn_plan_t p, const void* X, const void* W1,
+                                     const void* b1, const void* W2, const void* b2,
+                                     const void* R, void* Y, cudaStream_t stream)
+{
+    if (!p || p->layernorm) return GEMM_EPI_ERR_INVALID_ARG;
+    const gemm_epi_operands o1 = make_operands(X, W1, b1, nullptr, p->H ? p->H : Y, nullptr);
+    const gemm_epi_operands o2 = make_operands(p->H, W2, b2, R, Y, nullptr);
+    gemm_epi_status st = check_operands(p->g1, o1);
+    if (st != GEMM_EPI_OK) return st;
+    st = check_operands(p->g2, o2);
+    if (st != GEMM_EPI_OK) return st;
+    if (p->t == 0 || p->d == 0) return GEMM_EPI_OK;
+    st = check_device(p->g1);
+    if (st != GEMM_EPI_OK) return st;
+    if (p->one_launch) return run_ffn_one_launch(p, X, W1, b1, W2, b2, R, Y, stream);
+    st = run_plan(p->g1, o1, stream, true);
+    if (st != GEMM_EPI_OK) return st;
+    // GEMM 2 reads H only after GEMM 1 has completed (griddepcontrol.wait in its producer).
+    return run_plan(p->g2, o2, stream, p->g1->variant != kEmpty);
+}
+
+const void* gemm_epi_ffn_hidden(gemm_epi_ffn_plan_t p) { return p ? p->H : nullptr; }
+
+gemm_epi_status gemm_epi_ffn_sync_status(gemm_epi_ffn_plan_t p, cudaStream_t stream)
+{
+    if (!p) return GEMM_EPI_ERR_INVALID_ARG;
+    gemm_epi_status s1 = gemm_epi_sync_status(p->g1, stream);
+    gemm_epi_status s2 = gemm_epi_sync_status(p->g2, stream);
+    return s1 != GEMM_EPI_OK ? s1 : s2;
+}
+
+gemm_epi_status gemm_epi_ffn_free(gemm_epi_ffn_plan_t p)
+{
+    if (!p) return GEMM_EPI_OK;
+    if (p->H) cudaFree(p->H);
+    if (p->ready) cudaFree(p->ready);
+    if (p->stats) cudaFree(p->stats);
+    gemm_epi_free(p->g1);
+    gemm_epi_free(p->g2);
+    delete p;
+    return GEMM_EPI_OK;
+}
+
+}  // extern "C"
+
+// ---- the FFN block without allocation ------------------------------------------------------
+//
+// For callers that cannot allocate device memory.  The hidden activation and the status
+// words of the two launches live in one file-scope device array; its device address is
+// looked up once per device (with that device current) and then passed to the kernels.
+
+namespace {
+
+constexpr size_t kNoAllocStatusBytes = 256;  // two status words, padded to 256 bytes
+constexpr size_t kNoAllocHiddenBytes = static_cast<size_t>(GEMM_EPI_FFN_NOALLOC_MAX_HIDDEN) * 2;
+
+// In host code this name is only a stand-in; the device address comes from
+// cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char
+    g_ffn_noalloc_scratch[kNoAllocStatusBytes + kNoAllocHiddenBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+unsigned char* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on device `dev` (the current device); the first call
+// per device looks it up and zeroes the status words.
+gemm_epi_status noalloc_scratch(int dev, unsigned char** out)
+{
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return GEMM_EPI_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_ffn_noalloc_scratch) != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return GEMM_EPI_ERR_LAUNCH;
+        }
+        if (cudaMemset(ptr, 0, kNoAllocStatusBytes) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_EPI_ERR_LAUNCH;
+        }
+        g_noalloc_addr[dev] = static_cast<unsigned char*>(ptr);
+    }
+    *out = g_noalloc_addr[dev];
+    return GEMM_EPI_OK;
+}
+
+// A plan on the caller's stack whose status word points into the static scratch.
+gemm_epi_status stack_plan(gemm_epi_plan_s* p, int64_t m, int64_t n, int64_t k, int dtype,
+                           int epilog, int dev, int sms, int* status)
+{
+    memset(p, 0, sizeof(*p));
+    p->m = m;
+    p->n = n;
+    p->k = k;
+    p->dtype = dtype;
+    p->epilog = epilog;
+    p->bias_layout = GEMM_EPI_BIAS_1N;
+    p->device = dev;
+    p->sm_count = sms;
+    p->wait_limit_ns = kDefaultWaitNs;
+    p->d_status = status;
+    return configure(p);
+}
+
+}  // namespace
+
+extern "C" gemm_epi_status gemm_epi_ffn_execute_noalloc(int64_t t, int64_t d, int64_t f,
+                                                        gemm_epi_dtype dtype, const void* X,
+                                                        const void* W1, const void* b1,
+                                                        const void* W2, const void* b2,
+                                                        const void* R, void* Y,
+                                                        cudaStream_t stream)
+{
+    if (dtype != GEMM_EPI_F16 && dtype != GEMM_EPI_BF16) return GEMM_EPI_ERR_INVALID_ARG;
+    const int64_t kMax = (1ll << 31) - 1;
+    if (t < 0 || d < 0 || f < 0 || t > kMax || d > kMax || f > kMax)
+        return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+    if (d % 8 != 0 || f % 8 != 0) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+    if (f > 0 && t > GEMM_EPI_FFN_NOALLOC_MAX_HIDDEN / f) return GEMM_EPI_ERR_SCRATCH_LIMIT;
+
+    int dev = 0, major = 0, minor = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_EPI_ERR_NO_DEVICE;
+    }
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3) return GEMM_EPI_ERR_ARCH;
+
+    unsigned char* scratch = nullptr;
+    gemm_epi_status st = noalloc_scratch(dev, &scratch);
+    if (st != GEMM_EPI_OK) return st;
+    int* status = reinterpret_cast<int*>(scratch);
+    void* H = scratch + kNoAllocStatusBytes;
+
+    gemm_epi_plan_s g1, g2;
+    st = stack_plan(&g1, t, f, d, dtype, GEMM_EPI_GELU_BIAS, dev, sms, status);
+    if (st != GEMM_EPI_OK) return st;
+    st = stack_plan(&g2, t, d, f, dtype, GEMM_EPI_BIAS_RESIDUAL, dev, sms, status + 1);
+    if (st != GEMM_EPI_OK) return st;
+    const gemm_epi_operands o1 = make_operands(X, W1, b1, nullptr, H, nullptr);
+    const gemm_epi_operands o2 = make_operands(H, W2, b2, R, Y, nullptr);
+    st = check_operands(&g1, o1);
+    if (st != GEMM_EPI_OK) return st;
+    st = check_operands(&g2, o2);
+    if (st != GEMM_EPI_OK) return st;
+    if (t == 0 || d == 0) return GEMM_EPI_OK;
+    st = run_plan(&g1, o1, stream, false);
+    if (st != GEMM_EPI_OK) return st;
+    return run_plan(&g2, o2, stream, g1.variant != kEmpty);
+}

@@ -1,0 +1,84 @@
+// Internal to the library (not part of the C ABI): the plan object and the helpers the C
+// entry points share.  api.cu holds the GEMM plans and their launches, host_exec.cu the
+// host-buffer call, ffn_api.cu the FFN block (and its allocation-free form),
+// layernorm_api.cu the LayerNorm calls.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gemm_epi.h"
+#include "kernel_params.h"
+
+namespace gemm_epi_impl {
+
+enum Variant { kEmpty = 0, kRowTile = 1, kSwapped = 2, kBiasOnly = 3, kRowPair = 4 };
+
+constexpr int kSwappedMaxM = 256;
+constexpr unsigned long long kDefaultWaitNs = 2000ull * 1000 * 1000;  // 2 s
+
+struct HostPipe;
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace gemm_epi_impl
+
+struct gemm_epi_plan_s {
+    int64_t m, n, k;
+    int dtype, epilog, bias_layout;
+    int device, sm_count;
+    // chosen configuration
+    int variant, bn, stages, smem, grid, group_m, tiles_m, tiles_n, k_blocks;
+    int split, kb_per_split;  // split-K across a cluster (split == 1: persistent kernel)
+    // options (0 = automatic)
+    int opt_variant, opt_bn, opt_split_k, opt_grid, opt_group_m;
+    int prefetch;  // L2 prefetch distance in K blocks (GEMM_EPI_OPT_PREFETCH)
+    int no_pdl;    // 1: launch without programmatic dependent launch (GEMM_EPI_OPT_PDL = 0)
+    unsigned long long wait_limit_ns;
+    int debug_stall;
+    int* d_status;
+    // tensor maps for the last (A, B, D) pointers
+    const void* key_A;
+    const void* key_B;
+    const void* key_D;
+    bool maps_valid;
+    CUtensorMap tm_A, tm_B, tm_D;
+    char desc[320];
+    gemm_epi_impl::HostPipe* host;  // gemm_epi_execute_host's streams, buffers and chunk plans
+};
+
+namespace gemm_epi_impl {
+
+// Epilogs built for E4M3 inputs (forward, no 16-bit auxiliary output).
+bool fp8_epilog(int e);
+bool backward(int epilog);
+int64_t dbias_len(const gemm_epi_plan_s* p);
+
+// Pick the kernel and its configuration for the plan's shape and options.
+gemm_epi_status configure(gemm_epi_plan_s* p);
+bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,
+               uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw,
+               uint64_t elem_bytes = 2);
+gemm_epi_status ensure_maps(gemm_epi_plan_s* p, const void* A, const void* B, void* D);
+gemm_epi_status check_device(const gemm_epi_plan_s* p);
+// The current device, checked to be sm_103, and its SM count.
+gemm_epi_status current_device(int* sms);
+gemm_epi_status check_operands(const gemm_epi_plan_s* p, const gemm_epi_operands& o);
+gemm_epi_operands make_operands(const void* A, const void* B, const void* bias,
+                                const void* residual, void* D, void* aux);
+gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, int epilog,
+                            cudaStream_t stream, bool pdl = false);
+gemm_epi_status zero_dbias(const gemm_epi_plan_s* p, const gemm_epi_operands& ops,
+                           cudaStream_t stream);
+cudaError_t run_elementwise(const gemm_epi_plan_s* p, const void* pre,
+                            const gemm_epi_operands& ops, cudaStream_t stream);
+// One fused call on an already-checked plan (empty problems launch nothing, k == 0 runs the
+// elementwise epilogue on the bias alone).
+gemm_epi_status run_plan(gemm_epi_plan_s* p, const gemm_epi_operands& ops, cudaStream_t stream,
+                         bool pdl);
+// host_exec.cu
+void destroy_host_pipe(gemm_epi_plan_s* p);
+gemm_epi_status run_host(gemm_epi_plan_s* p, const gemm_epi_operands& o, cudaStream_t stream);
+
+}  // namespace gemm_epi_impl
