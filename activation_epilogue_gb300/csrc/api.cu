@@ -557,7 +557,7 @@ gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt,
         p->opt_bn = static_cast<int>(value);
         break;
     case GEMM_EPI_OPT_SPLIT_K:
-        if (value < 0 || value > 8) return GEMM_EPI_ERR_INVALID_ARG;
+        if (value < 0 || value > 4) return GEMM_EPI_ERR_INVALID_ARG;
         p->opt_split_k = static_cast<int>(value);
         break;
     case GEMM_EPI_OPT_GRID:

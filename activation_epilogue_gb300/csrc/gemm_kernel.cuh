@@ -54,6 +54,7 @@ constexpr int kEpiWarps = kEpilogueWarps;  // two per TMEM lane quarter, alterna
 constexpr int kThreads = 64 + 32 * kEpiWarps;   // producer, MMA, epilogue warps
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kPipeBudget = 192 * 1024;
+constexpr int kMaxSplit = 4;    // split-K: CTAs per cluster at most
 
 constexpr int pow2_at_least(int x, int p = 32) { return p >= x ? p : pow2_at_least(x, 2 * p); }
 
@@ -179,6 +180,11 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
     }
     return w;
 }
+
+// Split-K: the rank of the cluster that owns (reduces, then runs the epilogue of) chunk c
+// of TMEM lane quarter q.  Spreading (quarter, chunk) units over the ranks shares the
+// reduction among the CTAs even when a tile has a single chunk.
+__device__ __forceinline__ int split_owner(int q, int c, int split) { return (4 * c + q) % split; }
 
 // One tile of the walk: which GEMM (0, or 1 = the second GEMM of a fused FFN block), its
 // coordinates and its last K block.
@@ -640,7 +646,7 @@ __device__ __forceinline__ void publish_partials(const GemmParams& p, uint8_t* s
         if (idx < nb) prefetch_global_l2(static_cast<const uint16_t*>(p.bias) + idx);
     }
     for (int c = half; c < nchunks; c += 2) {
-        if (c % w.split == w.rank) continue;
+        if (split_owner(quarter, c, w.split) == w.rank) continue;
         uint32_t r[32];
         __syncwarp();
         if constexpr (CH == 32)
@@ -673,7 +679,8 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
     const int ew = warp - 2;             // epilogue warp 0..7
     const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
     const int half = ew >> 2;            // the pair's warps take alternate chunks
-    const WorkRange w = work_range<PAIR>(p);
+    WorkRange w = work_range<PAIR>(p);
+    if (PAIR) w.split = 1;  // (compile-time: the pair kernel never splits K)
     // This warp's own staging area for per-column values (bias; LayerNorm: two arrays of
     // 256): no other warp reads it, so a __syncwarp orders it.
     float* sbias = reinterpret_cast<float*>(smem + C::kOffBias) + ew * 512;
@@ -776,8 +783,9 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
             const uint16_t* src = epilog == EPI_BIAS_RESIDUAL
                                       ? R
                                       : static_cast<const uint16_t*>(p.aux_in);
-            for (int c = w.rank + half * w.split; c < nchunks; c += 2 * w.split)
-                prefetch_global_l2(src + static_cast<long long>(lane_idx) * ncols + col_base + c * CH);
+            for (int c = half; c < nchunks; c += 2)
+                if (split_owner(quarter, c, w.split) == w.rank)
+                    prefetch_global_l2(src + static_cast<long long>(lane_idx) * ncols + col_base + c * CH);
         }
         if (!wait_bounded(bar0 + 8u * (kBarTmemFull + acc), acc_phase, abort_flag,
                           p.wait_limit_ns)) {
@@ -790,7 +798,8 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         const bool warp_live = lane_base < lane_limit;
         float lane_sum = 0.0f;  // backward, bias gradient along the lanes: this tile's sum
 
-        for (int c = w.rank + half * w.split; c < nchunks; c += 2 * w.split) {
+        for (int c = half; c < nchunks; c += 2) {
+            if (split_owner(quarter, c, w.split) != w.rank) continue;
             // Row-tile residual: this thread's 32 values, requested before the TMEM read so
             // that the load latency overlaps it.
             uint4 rres[4];
@@ -818,27 +827,30 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
             for (int j = 0; j < CH; ++j) v[j] = __uint_as_float(r[j]);
             if (w.split > 1) {
                 // Add the other ranks' partial sums of this chunk (distributed shared
-                // memory): one 16-byte unit at a time, every peer's load issued before any
-                // of them is consumed, so their latencies overlap.
+                // memory) in batches of 16-byte units: every load of a batch (units x
+                // peers) is issued before any is consumed, so one remote round trip serves
+                // a whole 16-column chunk (two units per trip for 32-column chunks, whose
+                // registers are needed elsewhere).
                 const int row = quarter * 32 + lane;
+                constexpr int kUB = CH == 16 ? 4 : 2;
 #pragma unroll
-                for (int u0 = 0; u0 < CH / 4; ++u0) {
-                    float4 part[7][1];
+                for (int u0 = 0; u0 < CH / 4; u0 += kUB) {
+                    float4 part[kMaxSplit - 1][kUB];
 #pragma unroll
-                    for (int pi = 0; pi < 7; ++pi) {
+                    for (int pi = 0; pi < kMaxSplit - 1; ++pi) {
                         if (pi < w.split - 1) {
                             const uint32_t peer = static_cast<uint32_t>(pi < w.rank ? pi : pi + 1);
 #pragma unroll
-                            for (int uu = 0; uu < 1; ++uu)
+                            for (int uu = 0; uu < kUB; ++uu)
                                 part[pi][uu] = ld_shared_cluster_v4(map_shared_rank(
                                     sbase + red_offset<BN>(row, c * (CH / 4) + u0 + uu), peer));
                         }
                     }
 #pragma unroll
-                    for (int pi = 0; pi < 7; ++pi) {
+                    for (int pi = 0; pi < kMaxSplit - 1; ++pi) {
                         if (pi < w.split - 1) {
 #pragma unroll
-                            for (int uu = 0; uu < 1; ++uu) {
+                            for (int uu = 0; uu < kUB; ++uu) {
                                 v[4 * (u0 + uu)] += part[pi][uu].x;
                                 v[4 * (u0 + uu) + 1] += part[pi][uu].y;
                                 v[4 * (u0 + uu) + 2] += part[pi][uu].z;
@@ -1010,8 +1022,12 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                 }
             }
         }
-        if (bwd && !along_cols && lane_idx < lane_limit && w.rank + half * w.split < nchunks)
-            atomicAdd(p.dbias + lane_idx, lane_sum);
+        if (bwd && !along_cols && lane_idx < lane_limit) {
+            bool any_chunk = false;  // this warp owned a chunk of the tile
+            for (int c = half; c < nchunks; c += 2)
+                any_chunk = any_chunk || split_owner(quarter, c, w.split) == w.rank;
+            if (any_chunk) atomicAdd(p.dbias + lane_idx, lane_sum);
+        }
         tcgen05_fence_before_sync();
         if constexpr (PAIR)  // the even CTA's MMAs write both CTAs' accumulators
             mbar_arrive_cluster(map_shared_rank(bar0 + 8u * (kBarTmemEmpty + acc), 0));

@@ -136,7 +136,7 @@ typedef enum {
     GEMM_EPI_OPT_TILE_N = 1,        /* N tile: 64, 128 or 256 for the row-tile kernel;
                                        224 or 256 for the CTA-pair kernel (a width
                                        the chosen kernel lacks is ERR_INVALID_ARG) */
-    GEMM_EPI_OPT_SPLIT_K = 2,       /* K slices per output tile, 1..8 (one cluster of that
+    GEMM_EPI_OPT_SPLIT_K = 2,       /* K slices per output tile, 1..4 (one cluster of that
                                        many CTAs per tile; partial sums added on chip) */
     GEMM_EPI_OPT_GRID = 3,          /* cap on persistent CTAs (<= SM count) */
     GEMM_EPI_OPT_GROUP_M = 4,       /* tile raster: M tiles per group */

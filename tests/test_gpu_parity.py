@@ -338,8 +338,8 @@ def test_ffn_option_rules():
 
 # ---- split-K across a cluster (partial sums added on chip) ---------------------------------
 
-@pytest.mark.parametrize("variant,bn,split", [(1, 64, 2), (1, 128, 3), (1, 256, 4), (1, 128, 8),
-                                              (2, 0, 2), (2, 0, 5), (2, 0, 8)])
+@pytest.mark.parametrize("variant,bn,split", [(1, 64, 2), (1, 128, 3), (1, 256, 4), (1, 64, 4),
+                                              (2, 0, 2), (2, 0, 3), (2, 0, 4)])
 @pytest.mark.parametrize("epilog", ["BIAS", "GELU_BIAS", "RELU_AUX_BIAS", "BIAS_RESIDUAL"])
 def test_split_k_parity(variant, bn, split, epilog):
     m, n, k = (300 if variant == 1 else 40), 520, 1000    # 16 K blocks, the last one 40 deep
@@ -353,7 +353,7 @@ def test_split_k_parity(variant, bn, split, epilog):
     assert f"split_k={-(-16 // kpb)}" in desc
 
 
-@pytest.mark.parametrize("variant,split", [(1, 4), (2, 6)])
+@pytest.mark.parametrize("variant,split", [(1, 4), (2, 3)])
 def test_split_k_integer_bit_exact(variant, split):
     m, n, k = (256 if variant == 1 else 16), 264, 512
     p = _inputs(m, n, k, "bf16", "1N", seed=31, kind="int")
