@@ -144,8 +144,12 @@ def time_steps(fn, steps: int, warmup: int, stream, dist_barrier=None) -> float:
 
 
 def time_cold(fn, iters: int, stream, flush) -> float:
-    """Median seconds of fn() with L2 flushed before every call (events around the call)."""
+    """Seconds of fn() with L2 flushed before every call (events around the call): the mean
+    of 2 x iters samples without the top and bottom tenth.  The event clock of the GB300
+    boxes advances in steps of about 2 us, so a median of single calls lands on those steps;
+    a trimmed mean over many calls resolves fractions of a step."""
     import torch
+    iters *= 2
     ts = []
     for i in range(iters + 2):
         flush()
@@ -157,7 +161,9 @@ def time_cold(fn, iters: int, stream, flush) -> float:
         torch.cuda.synchronize()
         if i >= 2:
             ts.append(e0.elapsed_time(e1) / 1e3)
-    return statistics.median(ts)
+    ts.sort()
+    cut = len(ts) // 10
+    return statistics.mean(ts[cut:len(ts) - cut])
 
 
 def time_graph(fn, calls: int, replays: int, stream) -> float:
