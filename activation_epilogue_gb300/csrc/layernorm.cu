@@ -3,9 +3,10 @@
 // gamma + beta over each row, optionally plus a residual, done in one kernel.
 //
 // Three kernels:
-//   * layernorm_kernel: the section's fused LayerNorm (+ residual), one warp per row: a
-//     pass for the mean, a pass for the variance of the centred row (the rows are re-read
-//     from L1/L2), a pass that normalises and writes; 16-byte accesses.
+//   * layernorm_kernel: the section's fused LayerNorm (+ residual), one warp per row: the
+//     mean, the variance of the centred row and the normalised output, from the row held
+//     in registers (d <= 1024; longer rows are re-read from L1/L2 for each pass);
+//     16-byte accesses.
 //   * layernorm_stats_kernel: only the per-row mean and 1/sqrt(var + eps).  With them the
 //     LayerNorm in front of a GEMM folds into the GEMM's epilogue:
 //         LN(x) . W + b = rstd (x . W' - mu c) + b',
@@ -90,6 +91,51 @@ __device__ __forceinline__ void row_stats(const uint16_t* x, int d, int bf16, fl
     rstd = rsqrtf(var + eps);  // hardware reciprocal square root (about 2 ulp)
 }
 
+// Rows of at most kRegVec * 256 elements are held in registers: every load of the row is
+// issued before any is used (one memory round trip per row instead of one per 256
+// columns), and the variance and the normalisation reuse the values.
+constexpr int kRegVec = 4;  // d <= 1024: about 50 registers, four 256-thread blocks per SM
+
+__device__ __forceinline__ void row_load_regs(const uint16_t* x, int d, int bf16, int lane,
+                                              float (&v)[kRegVec][8])
+{
+#pragma unroll
+    for (int i = 0; i < kRegVec; ++i) {
+        const int c = i * 256 + lane * 8;
+        if (c < d) {
+            load8(x + c, v[i], bf16);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[i][j] = 0.0f;
+        }
+    }
+}
+
+__device__ __forceinline__ void row_stats_regs(const float (&v)[kRegVec][8], int d, int lane,
+                                               float eps, float& mu, float& rstd)
+{
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kRegVec; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s += v[i][j];
+    const float inv_d = __fdividef(1.0f, static_cast<float>(d));
+    mu = warp_sum(s) * inv_d;
+    float q = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kRegVec; ++i) {
+        if (i * 256 + lane * 8 < d) {  // (padding lanes hold 0, not mu)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float e = v[i][j] - mu;
+                q = fmaf(e, e, q);
+            }
+        }
+    }
+    rstd = rsqrtf(warp_sum(q) * inv_d + eps);
+}
+
+template <bool REGS>
 __global__ void __launch_bounds__(256) layernorm_stats_kernel(const uint16_t* __restrict__ X,
                                                               int t, int d, int bf16, float eps,
                                                               float* __restrict__ stats)
@@ -99,7 +145,13 @@ __global__ void __launch_bounds__(256) layernorm_stats_kernel(const uint16_t* __
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
     for (long long r = warp; r < t; r += nwarps) {
         float mu, rstd;
-        row_stats(X + r * d, d, bf16, eps, lane, mu, rstd);
+        if constexpr (REGS) {
+            float v[kRegVec][8];
+            row_load_regs(X + r * d, d, bf16, lane, v);
+            row_stats_regs(v, d, lane, eps, mu, rstd);
+        } else {
+            row_stats(X + r * d, d, bf16, eps, lane, mu, rstd);
+        }
         if (lane == 0) {
             stats[2 * r] = mu;
             stats[2 * r + 1] = rstd;
@@ -118,6 +170,27 @@ __global__ void __launch_bounds__(256) layernorm_kernel(
     for (long long r = warp; r < t; r += nwarps) {
         const uint16_t* x = X + r * d;
         float mu, rstd;
+        if (d <= kRegVec * 256) {
+            float v[kRegVec][8];
+            row_load_regs(x, d, bf16, lane, v);
+            row_stats_regs(v, d, lane, eps, mu, rstd);
+#pragma unroll
+            for (int i = 0; i < kRegVec; ++i) {
+                const int c = i * 256 + lane * 8;
+                if (c >= d) continue;
+                float rv[8];
+                if (R) load8(R + r * d + c, rv, bf16);
+                float y[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float o = (v[i][j] - mu) * rstd * dec(gamma[c + j], bf16) +
+                                    dec(beta[c + j], bf16);
+                    y[j] = R ? o + rv[j] : o;
+                }
+                store8(Y + r * d + c, y, bf16);
+            }
+            continue;
+        }
         row_stats(x, d, bf16, eps, lane, mu, rstd);
         for (int c = lane * 8; c < d; c += 256) {
             float v[8];
@@ -189,8 +262,12 @@ unsigned grid_for_rows(long long rows, int sm_count)
 cudaError_t layernorm_stats_launch(const void* X, int t, int d, int bf16, float eps,
                                    float* stats, int sm_count, cudaStream_t stream)
 {
-    layernorm_stats_kernel<<<grid_for_rows(t, sm_count), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(X), t, d, bf16, eps, stats);
+    if (d <= kRegVec * 256)
+        layernorm_stats_kernel<true><<<grid_for_rows(t, sm_count), 256, 0, stream>>>(
+            static_cast<const uint16_t*>(X), t, d, bf16, eps, stats);
+    else
+        layernorm_stats_kernel<false><<<grid_for_rows(t, sm_count), 256, 0, stream>>>(
+            static_cast<const uint16_t*>(X), t, d, bf16, eps, stats);
     return cudaGetLastError();
 }
 
