@@ -41,11 +41,16 @@ EncodeTiledFn encode_fn()
     return g_encode;
 }
 
-// Split-K is used only when GEMM_EPI_OPT_SPLIT_K asks for it.  Measured on GB300, the
-// cluster launch, the two cluster barriers and the partial-sum exchange cost more than the
-// shorter K loop saves on every under-filled shape tried (1024x512x2048: 15.5 us unsplit vs
-// 19-20 us split; GELU T=16/64/256 x 3072 x 768: 9.2/11.1/16.8 us unsplit vs 10.2/22/28 us
-// with split 4), so a plan does not split by itself.
+// Split-K is used only when GEMM_EPI_OPT_SPLIT_K asks for it.  Measured on GB300 it does
+// not pay on the under-filled shapes tried.  Through a cluster (DSMEM): 1024x512x2048
+// 15.5 us unsplit vs 19-20 us split; GELU T=16/64/256 x 3072 x 768 9.2/11.1/16.8 us unsplit
+// vs 10.2/22/28 us with split 4 (T=16 graph-replayed: 6.5 us against 6.8 us, the one gain).
+// Through device memory: GELU T=16 x 3072 x 768 with 2/4/6 slices 13.0/13.0/13.5 us cold,
+// 8.1/7.5/7.5 us hot, against 11.0 / 6.8 us unsplit; the publish, count and reload of the
+// partial tiles cost more than the shorter K loop saves.  Narrower swapped tiles (below)
+// add CTAs without any of that.
+constexpr int kMaxClusterSplit = 4;  // CTAs per cluster (kernel: kMaxSplit)
+constexpr int kMaxGlobalSplit = 8;   // K slices through device memory (kernel: kMaxGSplit)
 
 int normalise_split(int split, int k_blocks, int* kb_per_split)
 {
@@ -77,6 +82,22 @@ int pick_rowtile_bn(int64_t m, int64_t n, int k_blocks, int sm_count)
     return best;
 }
 
+// Tile width (rows of D) of the swapped small-m kernel: the narrowest that still gives
+// every tile its own SM, else one tile over all m rows.  The operand W is then read by
+// several tiles (the later reads hit L2), but more SMs stream it: measured on GB300 at
+// 256 x 3072 x 768 GELU, 64-row tiles (96 CTAs) take 12.9 us cold / 8.2 us hot against
+// 17.2 / 11.5 us for one 256-row tile (24 CTAs); at 64 x 3072 x 768, 16-row tiles 7.0 us
+// hot against 7.8 us.
+int pick_swapped_bn(int64_t m, int64_t n, int sm_count)
+{
+    int full = 16;
+    while (full < m) full *= 2;
+    const int64_t tiles_n = (n + 127) / 128;
+    for (int bn = 16; bn < full; bn *= 2)
+        if (tiles_n * ((m + bn - 1) / bn) <= sm_count) return bn;
+    return full;
+}
+
 // N tile of the CTA-pair kernel: 224 when it needs fewer 256-row tile waves over the resident
 // pairs than 256 does, else 256.  Both stage the same 32 KB of operands per CTA and K block
 // (224 wide leaves part of the second 64-column B panel unused), and measured on GB300 a
@@ -101,12 +122,46 @@ bool fp8_epilog(int e)
            e == GEMM_EPI_RELU_AUX_BIAS || e == GEMM_EPI_BIAS_RESIDUAL || e == GEMM_EPI_NONE;
 }
 
+// The split-K workspace for the configured shape: kept when large enough, else replaced
+// (the old buffers stay if an allocation fails).  The counts start at zero; each launch
+// leaves them at zero.
+gemm_epi_status ensure_split_ws(gemm_epi_plan_s* p)
+{
+    const size_t tiles = static_cast<size_t>(p->tiles_m) * p->tiles_n;
+    const size_t ws_bytes = tiles * p->split * 128 * p->bn * sizeof(float);
+    if (p->d_split_ws && p->split_ws_bytes >= ws_bytes && p->split_count_len >= tiles)
+        return GEMM_EPI_OK;
+    float* ws = nullptr;
+    unsigned* cnt = nullptr;
+    if (cudaMalloc(reinterpret_cast<void**>(&ws), ws_bytes) != cudaSuccess ||
+        cudaMalloc(reinterpret_cast<void**>(&cnt), tiles * sizeof(unsigned)) != cudaSuccess) {
+        cudaGetLastError();
+        if (ws) cudaFree(ws);
+        return GEMM_EPI_ERR_ALLOC;
+    }
+    // (the legacy stream orders the memset; synchronise so that launches on any stream see it)
+    if (cudaMemset(cnt, 0, tiles * sizeof(unsigned)) != cudaSuccess ||
+        cudaStreamSynchronize(nullptr) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(ws);
+        cudaFree(cnt);
+        return GEMM_EPI_ERR_ALLOC;
+    }
+    release_split_ws(p);
+    p->d_split_ws = ws;
+    p->d_split_count = cnt;
+    p->split_ws_bytes = ws_bytes;
+    p->split_count_len = tiles;
+    return GEMM_EPI_OK;
+}
+
 gemm_epi_status configure(gemm_epi_plan_s* p)
 {
     p->maps_valid = false;
     p->bn = p->stages = p->smem = p->grid = p->tiles_m = p->tiles_n = p->k_blocks = 0;
     p->group_m = 1;
     p->split = 1;
+    p->split_global = 0;
     p->kb_per_split = 0;
     if (p->m == 0 || p->n == 0) {
         p->variant = kEmpty;
@@ -186,8 +241,10 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             p->stages = rowtile_stages(p->bn);
             p->smem = rowtile_smem_bytes(p->bn);
         } else {
-            int bn = 16;
-            while (bn < p->m) bn *= 2;
+            if (p->opt_bn && p->opt_bn != 16 && p->opt_bn != 32 && p->opt_bn != 64 &&
+                p->opt_bn != 128 && p->opt_bn != 256)
+                return GEMM_EPI_ERR_INVALID_ARG;
+            int bn = p->opt_bn ? p->opt_bn : pick_swapped_bn(p->m, p->n, p->sm_count);
             p->bn = bn;
             p->tiles_m = static_cast<int>((p->n + 127) / 128);
             p->tiles_n = static_cast<int>((p->m + bn - 1) / bn);
@@ -201,10 +258,16 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
         cudaError_t e = v == kRowTile ? rowtile_prepare(p->bn) : swapped_prepare(p->bn);
         if (e != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
         const int want_split = p->opt_split_k > 0 ? p->opt_split_k : 1;
+        const bool via_cluster = p->opt_split_mode == 1;
+        if (want_split > (via_cluster ? kMaxClusterSplit : kMaxGlobalSplit))
+            return GEMM_EPI_ERR_INVALID_ARG;
         p->split = normalise_split(want_split, p->k_blocks, &p->kb_per_split);
         long long grid;
         if (p->split > 1) {
-            grid = tiles * p->split;  // one cluster per tile, not persistent
+            // one CTA per (tile, K slice), not persistent; in clusters of `split` CTAs when
+            // the slices meet on chip
+            p->split_global = via_cluster ? 0 : 1;
+            grid = tiles * p->split;
             if (grid > (1ll << 30)) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
         } else {
             p->kb_per_split = p->k_blocks;
@@ -223,7 +286,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
                                   "DGELU_BGRAD",   "LN_GELU_BIAS"};
     snprintf(p->desc, sizeof(p->desc),
              "m=%lld n=%lld k=%lld dtype=%s epilog=%s bias=%s variant=%s tile=%dx%d bk=%d "
-             "stages=%d smem=%d tiles=%dx%d k_blocks=%d split_k=%d grid=%d group_m=%d sms=%d",
+             "stages=%d smem=%d tiles=%dx%d k_blocks=%d split_k=%d%s grid=%d group_m=%d sms=%d",
              static_cast<long long>(p->m), static_cast<long long>(p->n),
              static_cast<long long>(p->k),
              p->dtype == GEMM_EPI_E4M3 ? "e4m3" : p->dtype == GEMM_EPI_BF16 ? "bf16" : "f16",
@@ -231,10 +294,22 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
              vname[p->variant], p->variant == kRowPair ? 256 : 128, p->bn,
              p->dtype == GEMM_EPI_E4M3 ? 128 : 64, p->stages, p->smem, p->tiles_m, p->tiles_n,
              p->k_blocks,
-             p->split, p->grid, p->group_m, p->sm_count);
+             p->split, p->split > 1 ? (p->split_global ? "(device memory)" : "(cluster)") : "",
+             p->grid, p->group_m, p->sm_count);
     const char* log = getenv("GEMM_EPI_LOG");
     if (log && log[0] == '1') fprintf(stderr, "[gemm_epi] plan: %s\n", p->desc);
+    if (p->split_global) return ensure_split_ws(p);
     return GEMM_EPI_OK;
+}
+
+void release_split_ws(gemm_epi_plan_s* p)
+{
+    if (p->d_split_ws) cudaFree(p->d_split_ws);
+    if (p->d_split_count) cudaFree(p->d_split_count);
+    p->d_split_ws = nullptr;
+    p->d_split_count = nullptr;
+    p->split_ws_bytes = 0;
+    p->split_count_len = 0;
 }
 
 bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,
@@ -355,6 +430,9 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, in
     prm.debug_stall = p->debug_stall;
     prm.split = p->split;
     prm.kb_per_split = p->kb_per_split;
+    prm.split_global = p->split_global;
+    prm.split_ws = p->d_split_ws;
+    prm.split_count = p->d_split_count;
     prm.prefetch = p->prefetch;
     cudaError_t e;
     if (p->variant == kRowPair && p->dtype == GEMM_EPI_E4M3)
@@ -552,13 +630,18 @@ gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt,
         p->opt_variant = static_cast<int>(value);
         break;
     case GEMM_EPI_OPT_TILE_N:
-        if (value != 0 && value != 64 && value != 128 && value != 224 && value != 256)
+        if (value != 0 && value != 16 && value != 32 && value != 64 && value != 128 &&
+            value != 224 && value != 256)
             return GEMM_EPI_ERR_INVALID_ARG;
         p->opt_bn = static_cast<int>(value);
         break;
     case GEMM_EPI_OPT_SPLIT_K:
-        if (value < 0 || value > 4) return GEMM_EPI_ERR_INVALID_ARG;
+        if (value < 0 || value > kMaxGlobalSplit) return GEMM_EPI_ERR_INVALID_ARG;
         p->opt_split_k = static_cast<int>(value);
+        break;
+    case GEMM_EPI_OPT_SPLIT_MODE:
+        if (value < 0 || value > 2) return GEMM_EPI_ERR_INVALID_ARG;
+        p->opt_split_mode = static_cast<int>(value);
         break;
     case GEMM_EPI_OPT_GRID:
         if (value < 0 || value > (1 << 20)) return GEMM_EPI_ERR_INVALID_ARG;
@@ -669,6 +752,7 @@ gemm_epi_status gemm_epi_free(gemm_epi_plan_t p)
 {
     if (!p) return GEMM_EPI_OK;
     destroy_host_pipe(p);
+    release_split_ws(p);
     if (p->d_status) cudaFree(p->d_status);
     delete p;
     return GEMM_EPI_OK;

@@ -396,6 +396,7 @@ gemm_epi_status stack_plan(gemm_epi_plan_s* p, int64_t m, int64_t n, int64_t k, 
     p->sm_count = sms;
     p->wait_limit_ns = kDefaultWaitNs;
     p->d_status = status;
+    p->opt_split_k = 1;  // no split-K workspace to allocate
     return configure(p);
 }
 

@@ -26,12 +26,14 @@
 // registers until the tile is done, sums across the 32 lanes of a warp come from one
 // transpose-and-add butterfly; either way one fp32 atomic per warp and bias entry per tile.
 //
-// Split-K (small grids): the CTAs of a cluster share one output tile, each accumulating a
-// slice of K in its own TMEM.  The tile's 32-column chunks are owned round-robin by the
-// cluster ranks; every CTA writes the partial sums of the chunks it does not own into its
-// (by then idle) stage ring, the cluster synchronises, and each owner adds the peers'
-// partials over distributed shared memory before running the epilogue on its chunks.  The
-// partial sums never leave the chip.
+// Split-K (small grids), two forms.  Cluster: the CTAs of a cluster share one output tile,
+// each accumulating a slice of K in its own TMEM.  The tile's 32-column chunks are owned
+// round-robin by the cluster ranks; every CTA writes the partial sums of the chunks it does
+// not own into its (by then idle) stage ring, the cluster synchronises, and each owner adds
+// the peers' partials over distributed shared memory before running the epilogue on its
+// chunks.  Device memory: independent CTAs write their fp32 partial tiles to a workspace
+// (it stays in L2) and count themselves per tile; the CTA that arrives last adds the
+// slices in slice order and runs the epilogue.  No CTA waits for another.
 //
 // Every mbarrier wait is bounded by a time limit; on expiry the waiting thread records the
 // failure in the plan's status word and raises a shared abort flag, every role leaves its
@@ -55,6 +57,7 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;   // producer, MMA, epilogue warps
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kPipeBudget = 192 * 1024;
 constexpr int kMaxSplit = 4;    // split-K: CTAs per cluster at most
+constexpr int kMaxGSplit = 8;   // split-K through device memory: K slices per tile at most
 
 constexpr int pow2_at_least(int x, int p = 32) { return p >= x ? p : pow2_at_least(x, 2 * p); }
 
@@ -93,6 +96,7 @@ constexpr int kBarStall = 20;
 constexpr int kBarDrain = 21;
 constexpr int kOffHolder = 22 * 8;  // TMEM base address written by tcgen05.alloc
 constexpr int kOffAbort = kOffHolder + 4;
+constexpr int kOffLast = kOffAbort + 4;  // split-K through device memory: "this CTA is last"
 
 constexpr unsigned long long kDrainLimitNs = 20ull * 1000 * 1000;  // 20 ms
 
@@ -141,6 +145,7 @@ struct WorkRange {
     int first, stride, end;  // tiles first, first + stride, ... below end
     int kb_begin, kb_end;    // K blocks [kb_begin, kb_end) of each tile
     int rank, split;         // split-K: cluster rank and size (split == 1: no split)
+    int grank, gsplit;       // split-K through device memory: K slice and slices (1: none)
     int pair_rank;           // CTA pairs: 0 = the even CTA (issues the MMAs), 1 = the odd
 };
 
@@ -158,6 +163,22 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
         w.pair_rank = static_cast<int>(cluster_ctarank());
         w.kb_begin = 0;
         w.kb_end = p.k_blocks;
+        w.grank = 0;
+        w.gsplit = 1;
+    } else if (p.split > 1 && p.split_global) {
+        // one (tile, K slice) per CTA
+        const int tile = static_cast<int>(blockIdx.x) / p.split;
+        w.first = tile;
+        w.stride = 1;
+        w.end = tile + 1;
+        w.rank = 0;
+        w.split = 1;
+        w.grank = static_cast<int>(blockIdx.x) - tile * p.split;
+        w.gsplit = p.split;
+        w.pair_rank = 0;
+        w.kb_begin = w.grank * p.kb_per_split;
+        w.kb_end = min(p.k_blocks, w.kb_begin + p.kb_per_split);
+        return w;
     } else if (p.split > 1) {
         const int tile = static_cast<int>(cluster_id_x());
         w.first = tile;
@@ -165,6 +186,8 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
         w.end = tile + 1;
         w.rank = static_cast<int>(cluster_ctarank());
         w.split = p.split;
+        w.grank = 0;
+        w.gsplit = 1;
         w.pair_rank = 0;
         w.kb_begin = w.rank * p.kb_per_split;
         w.kb_end = min(p.k_blocks, w.kb_begin + p.kb_per_split);
@@ -174,6 +197,8 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
         w.end = p.tiles_m * p.tiles_n;
         w.rank = 0;
         w.split = 1;
+        w.grank = 0;
+        w.gsplit = 1;
         w.pair_rank = 0;
         w.kb_begin = 0;
         w.kb_end = p.k_blocks;
@@ -662,6 +687,141 @@ __device__ __forceinline__ void publish_partials(const GemmParams& p, uint8_t* s
     tcgen05_fence_before_sync();
 }
 
+// Split-K through device memory: float4 index of 16-byte unit u (4 fp32 columns) of chunk c
+// of accumulator row `row` in K slice s of tile `tile`.  One unit of a warp's 32 rows is
+// 512 contiguous bytes.
+template <int BN>
+__device__ __forceinline__ long long gsplit_index(const GemmParams& p, int tile, int s, int c,
+                                                  int u, int row)
+{
+    constexpr int CH = TileCfg<BN>::kChunk;
+    return ((static_cast<long long>(tile) * p.split + s) * (BN / 4) + c * (CH / 4) + u) * kBM + row;
+}
+
+// Split-K through device memory, every epilogue thread of every CTA: write this CTA's
+// partial tile (all its chunks) to the workspace, then count the CTA for its tile.  Returns
+// true in the CTA that arrived last, which then reduces and runs the epilogue.  A CTA that
+// gave up on a wait still counts itself (so the count returns to zero); its status word
+// entry reports the failure.
+template <int BN, bool SWAP>
+__device__ __noinline__ bool publish_partials_global(const GemmParams& p, uint8_t* smem,
+                                                        uint32_t bar0, uint32_t tmem_base,
+                                                        volatile int* abort_flag)
+{
+    using C = TileCfg<BN>;
+    constexpr int CH = C::kChunk;
+    const WorkRange w = work_range(p);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;  // which warp of this quarter's pair
+    const int row = quarter * 32 + lane;
+    const int tile = w.first;
+    int tm, tn;
+    tile_coords(tile, p, tm, tn);
+    const int col_limit = SWAP ? p.m : p.n;
+    const int nchunks = (min(BN, col_limit - tn * BN) + CH - 1) / CH;
+    // The workspace and the counts may still be in use by a programmatic predecessor.
+    grid_dependency_wait();
+    bool ok = !*abort_flag;
+    if (ok && !wait_bounded(bar0 + 8u * kBarTmemFull, 0, abort_flag, p.wait_limit_ns)) {
+        if (!*abort_flag) record_failure(p.status, abort_flag, kRoleEpilogue);
+        ok = false;
+    }
+    if (ok) {
+        tcgen05_fence_after_sync();
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+        float4* ws = reinterpret_cast<float4*>(p.split_ws);
+        for (int c = half; c < nchunks; c += 2) {
+            uint32_t r[32];
+            __syncwarp();
+            if constexpr (CH == 32)
+                tmem_load_32cols(t_lane + c * 32, r);
+            else
+                tmem_load_16cols(t_lane + c * 16, r);
+#pragma unroll
+            for (int u = 0; u < CH / 4; ++u)
+                __stcg(ws + gsplit_index<BN>(p, tile, w.grank, c, u, row),
+                       make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                                   __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])));
+        }
+        tcgen05_fence_before_sync();
+    }
+    // Count the CTA with one acquire-release atomic after the barrier: the release makes the
+    // stores of every epilogue thread (ordered before it by the barrier) visible to the CTA
+    // that sees the final count, and in that CTA the acquire orders the workspace loads
+    // (after the second barrier) behind the other slices' stores.
+    named_barrier_sync(1, kEpiThreads);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + kOffLast);
+    if (threadIdx.x == 64) {
+        const unsigned before = atom_add_acq_rel_gpu(p.split_count + tile, 1u);
+        const bool last = before + 1 == static_cast<unsigned>(p.split);
+        if (last) p.split_count[tile] = 0u;  // every CTA of the tile has counted itself
+        *last_flag = last ? 1 : 0;
+    }
+    named_barrier_sync(1, kEpiThreads);
+    const bool last = *last_flag != 0;
+    if (!last || !ok) return last;
+    // The last CTA: add the K slices of each of its chunks in slice order (its own from
+    // tensor memory, the others from the workspace, every load of a batch issued first) and
+    // put the sum back into tensor memory, where the epilogue reads it.
+    tcgen05_fence_after_sync();
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float4* ws = reinterpret_cast<const float4*>(p.split_ws);
+    constexpr int kUB = CH == 16 ? 4 : 2;  // 16-byte units per batch
+    for (int c = half; c < nchunks; c += 2) {
+        uint32_t r[32];
+        __syncwarp();
+        if constexpr (CH == 32)
+            tmem_load_32cols(t_lane + c * 32, r);
+        else
+            tmem_load_16cols(t_lane + c * 16, r);
+#pragma unroll
+        for (int u0 = 0; u0 < CH / 4; u0 += kUB) {
+            float4 part[kMaxGSplit - 1][kUB];
+#pragma unroll
+            for (int pi = 0; pi < kMaxGSplit - 1; ++pi) {
+                if (pi < w.gsplit - 1) {
+                    const int s = pi < w.grank ? pi : pi + 1;
+#pragma unroll
+                    for (int uu = 0; uu < kUB; ++uu)
+                        part[pi][uu] = __ldcg(ws + gsplit_index<BN>(p, tile, s, c, u0 + uu, row));
+                }
+            }
+#pragma unroll
+            for (int uu = 0; uu < kUB; ++uu) {
+                const int j = 4 * (u0 + uu);
+                const float4 own = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                               __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                float4 a = w.grank == 0 ? own : part[0][uu];
+#pragma unroll
+                for (int s = 1; s < kMaxGSplit; ++s) {
+                    if (s < w.gsplit) {
+                        // (indices fixed at compile time: part stays in registers)
+                        const float4 b = s == w.grank ? own
+                                         : s < w.grank && s < kMaxGSplit - 1 ? part[s][uu]
+                                                                              : part[s - 1][uu];
+                        a.x += b.x;
+                        a.y += b.y;
+                        a.z += b.z;
+                        a.w += b.w;
+                    }
+                }
+                r[j] = __float_as_uint(a.x);
+                r[j + 1] = __float_as_uint(a.y);
+                r[j + 2] = __float_as_uint(a.z);
+                r[j + 3] = __float_as_uint(a.w);
+            }
+        }
+        if constexpr (CH == 32)
+            tmem_store_32cols(t_lane + c * 32, r);
+        else
+            tmem_store_16cols(t_lane + c * 16, r);
+    }
+    tcgen05_fence_before_sync();
+    return true;
+}
+
 // EPI >= 0 fixes the epilog at compile time (only its code is in the kernel); -1 reads it
 // from the parameters.
 template <int BN, bool SWAP, bool PAIR = false, int EPI = -1, bool F8 = false>
@@ -1120,19 +1280,43 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         __syncthreads();
     }
 
-    const bool split = p.split > 1;
-    if (!*abort_flag) {
-        if (warp == 0) {
-            if (lane == 0) run_producer<BN, SWAP, PAIR, FFN, F8>(p, sbase, bar0, abort_flag, pre);
-            __syncwarp();
-        } else if (warp == 1) {
-            if (lane == 0) run_mma<BN, SWAP, PAIR, FFN, F8>(p, sbase, bar0, tmem_base, abort_flag);
-            __syncwarp();
-        } else if (split) {
-            publish_partials<BN, SWAP>(p, smem, bar0, tmem_base, abort_flag);
-        } else {
-            run_epilogue<BN, SWAP, PAIR, EPI, F8>(p, smem, sbase, bar0, tmem_base, abort_flag);
+    const bool split = !PAIR && p.split > 1 && !p.split_global;  // (pairs never split)
+    const bool gsplit = !PAIR && p.split > 1 && p.split_global;
+    if constexpr (PAIR) {
+        if (!*abort_flag) {
+            if (warp == 0) {
+                if (lane == 0) run_producer<BN, SWAP, PAIR, FFN, F8>(p, sbase, bar0, abort_flag, pre);
+                __syncwarp();
+            } else if (warp == 1) {
+                if (lane == 0) run_mma<BN, SWAP, PAIR, FFN, F8>(p, sbase, bar0, tmem_base, abort_flag);
+                __syncwarp();
+            } else if (split) {
+                publish_partials<BN, SWAP>(p, smem, bar0, tmem_base, abort_flag);
+            } else {
+                run_epilogue<BN, SWAP, PAIR, EPI, F8>(p, smem, sbase, bar0, tmem_base, abort_flag);
+            }
         }
+    } else {
+        bool epilogue = false;  // this thread runs the epilogue below
+        if (!*abort_flag) {
+            if (warp == 0) {
+                if (lane == 0) run_producer<BN, SWAP, PAIR, FFN, F8>(p, sbase, bar0, abort_flag, pre);
+                __syncwarp();
+            } else if (warp == 1) {
+                if (lane == 0) run_mma<BN, SWAP, PAIR, FFN, F8>(p, sbase, bar0, tmem_base, abort_flag);
+                __syncwarp();
+            } else if (split) {
+                publish_partials<BN, SWAP>(p, smem, bar0, tmem_base, abort_flag);
+            } else {
+                epilogue = !gsplit;
+            }
+        }
+        // Split-K through device memory: every epilogue thread, aborted or not, takes part
+        // in the count; the last CTA of the tile runs the epilogue.
+        if (gsplit && warp >= 2)
+            epilogue = publish_partials_global<BN, SWAP>(p, smem, bar0, tmem_base, abort_flag) &&
+                       !*abort_flag;
+        if (epilogue) run_epilogue<BN, SWAP, PAIR, EPI, F8>(p, smem, sbase, bar0, tmem_base, abort_flag);
     }
     if (split) {
         // Every thread of every CTA of the cluster reaches both barriers: each role above

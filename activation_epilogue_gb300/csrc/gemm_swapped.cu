@@ -28,7 +28,7 @@ cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t stream, bool 
         attr[na].val.programmaticStreamSerializationAllowed = 1;
         ++na;
     }
-    if (p.split > 1) {  // split-K: one cluster of `split` CTAs per output tile
+    if (p.split > 1 && !p.split_global) {  // split-K: one cluster of `split` CTAs per tile
         attr[na].id = cudaLaunchAttributeClusterDimension;
         attr[na].val.clusterDim.x = static_cast<unsigned>(p.split);
         attr[na].val.clusterDim.y = 1;

@@ -43,6 +43,8 @@ void destroy_host_pipe(gemm_epi_plan_s* p)
     for (void* b : {h->dA[0], h->dA[1], h->dD[0], h->dD[1], h->dR[0], h->dR[1], h->dAux[0],
                     h->dAux[1], h->dB, h->dBias})
         if (b) cudaFree(b);
+    release_split_ws(&h->full);
+    release_split_ws(&h->last);
     delete h;
     p->host = nullptr;
 }
@@ -78,6 +80,7 @@ gemm_epi_status chunk_plan(const gemm_epi_plan_s* p, int64_t rows, gemm_epi_plan
     c->opt_variant = p->opt_variant;
     c->opt_bn = p->opt_bn;
     c->opt_split_k = p->opt_split_k;
+    c->opt_split_mode = p->opt_split_mode;
     c->opt_grid = p->opt_grid;
     c->opt_group_m = p->opt_group_m;
     c->prefetch = p->prefetch;

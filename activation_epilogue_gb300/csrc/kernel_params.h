@@ -83,6 +83,15 @@ struct GemmParams {
     // sums are added on chip (distributed shared memory) before the epilogue.
     int split;
     int kb_per_split;
+    // Split-K through device memory instead (split_global == 1, split > 1): tiles * split
+    // CTAs, no cluster; CTA b takes K slice b % split of tile b / split, writes its fp32
+    // partial tile to split_ws ([tile][slice][128 x BN]) and counts itself in
+    // split_count[tile]; the CTA that arrives last adds the slices in slice order (the
+    // result does not depend on the arrival order), runs the epilogue and sets the count
+    // back to zero for the next launch.
+    int split_global;
+    float* split_ws;
+    unsigned* split_count;
     // The producer also prefetches into L2 the operand boxes of the K block this many
     // blocks ahead of the one it loads (0 = off), so that a first touch of a panel in
     // device memory overlaps the loads of the blocks before it.

@@ -30,9 +30,15 @@ struct gemm_epi_plan_s {
     int device, sm_count;
     // chosen configuration
     int variant, bn, stages, smem, grid, group_m, tiles_m, tiles_n, k_blocks;
-    int split, kb_per_split;  // split-K across a cluster (split == 1: persistent kernel)
+    int split, kb_per_split;  // split-K slices (split == 1: persistent kernel)
+    int split_global;         // 1: the slices meet in device memory, 0: in a cluster
     // options (0 = automatic)
-    int opt_variant, opt_bn, opt_split_k, opt_grid, opt_group_m;
+    int opt_variant, opt_bn, opt_split_k, opt_grid, opt_group_m, opt_split_mode;
+    // split-K through device memory: fp32 partial tiles [tile][slice][128 x bn] and the
+    // per-tile arrival counts (zero between launches), allocated when the plan is configured
+    float* d_split_ws;
+    unsigned* d_split_count;
+    size_t split_ws_bytes, split_count_len;
     int prefetch;  // L2 prefetch distance in K blocks (GEMM_EPI_OPT_PREFETCH)
     int no_pdl;    // 1: launch without programmatic dependent launch (GEMM_EPI_OPT_PDL = 0)
     unsigned long long wait_limit_ns;
@@ -55,8 +61,11 @@ bool fp8_epilog(int e);
 bool backward(int epilog);
 int64_t dbias_len(const gemm_epi_plan_s* p);
 
-// Pick the kernel and its configuration for the plan's shape and options.
+// Pick the kernel and its configuration for the plan's shape and options (allocates the
+// split-K workspace when the configuration needs one).
 gemm_epi_status configure(gemm_epi_plan_s* p);
+// Free the split-K workspace of a plan (NULL-safe on its fields).
+void release_split_ws(gemm_epi_plan_s* p);
 bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,
                uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw,
                uint64_t elem_bytes = 2);

@@ -134,10 +134,11 @@ typedef enum {
     GEMM_EPI_OPT_VARIANT = 0,       /* 1 = row-tile kernel, 2 = swapped small-m kernel,
                                        3 = row-tile kernel run by CTA pairs (256-row tiles) */
     GEMM_EPI_OPT_TILE_N = 1,        /* N tile: 64, 128 or 256 for the row-tile kernel;
-                                       224 or 256 for the CTA-pair kernel (a width
+                                       224 or 256 for the CTA-pair kernel; 16, 32, 64, 128
+                                       or 256 rows of D for the swapped kernel (a width
                                        the chosen kernel lacks is ERR_INVALID_ARG) */
-    GEMM_EPI_OPT_SPLIT_K = 2,       /* K slices per output tile, 1..4 (one cluster of that
-                                       many CTAs per tile; partial sums added on chip) */
+    GEMM_EPI_OPT_SPLIT_K = 2,       /* K slices per output tile, 1..8 (one CTA per tile and
+                                       slice; how the partial sums meet: SPLIT_MODE) */
     GEMM_EPI_OPT_GRID = 3,          /* cap on persistent CTAs (<= SM count) */
     GEMM_EPI_OPT_GROUP_M = 4,       /* tile raster: M tiles per group */
     GEMM_EPI_OPT_WAIT_LIMIT_US = 5, /* device-side wait limit, microseconds (default 2 s) */
@@ -147,10 +148,15 @@ typedef enum {
                                        path; no copy or MMA is issued) */
     GEMM_EPI_OPT_PREFETCH = 7,      /* L2 prefetch distance in 64-deep K blocks, 0..64
                                        (0 = none) */
-    GEMM_EPI_OPT_PDL = 8            /* 1 (default): launch the fused kernel as a
+    GEMM_EPI_OPT_PDL = 8,           /* 1 (default): launch the fused kernel as a
                                        programmatic dependent of the previous work on the
                                        stream (its set-up overlaps that work; every global
                                        access still waits for it); 0: plain launch */
+    GEMM_EPI_OPT_SPLIT_MODE = 9     /* split-K partial sums: 0 (default) or 2 = through a
+                                       device-memory workspace the plan owns (slices 1..8;
+                                       the last CTA of a tile adds them in slice order);
+                                       1 = within a thread-block cluster over distributed
+                                       shared memory (slices 1..4) */
 } gemm_epi_option;
 
 /*

@@ -99,6 +99,10 @@ VARIANTS = [
     ("swapped256", 256, 264, 136, {"VARIANT": 2}),
     ("split3_rowtile", 260, 264, 520, {"VARIANT": 1, "TILE_N": 128, "SPLIT_K": 3}),
     ("split2_swapped", 24, 264, 264, {"VARIANT": 2, "SPLIT_K": 2}),
+    ("split3_rowtile_cluster", 260, 264, 520, {"VARIANT": 1, "TILE_N": 128, "SPLIT_K": 3,
+                                               "SPLIT_MODE": 1}),
+    ("split6_swapped", 40, 392, 776, {"VARIANT": 2, "TILE_N": 16, "SPLIT_K": 6}),
+    ("swapped_narrow", 100, 392, 200, {"VARIANT": 2, "TILE_N": 32}),
     ("persistent", 640, 512, 520, {"VARIANT": 1, "TILE_N": 128, "GRID": 3, "GROUP_M": 2}),
 ]
 

@@ -151,6 +151,7 @@ VARIANTS = [
     ("pair256", 600, 520, 200, {"VARIANT": 3, "TILE_N": 256}),
     ("pair224", 520, 600, 136, {"VARIANT": 3, "TILE_N": 224}),
     ("split3", 260, 264, 520, {"VARIANT": 1, "TILE_N": 128, "SPLIT_K": 3}),
+    ("split3_cluster", 260, 264, 520, {"VARIANT": 1, "TILE_N": 128, "SPLIT_K": 3, "SPLIT_MODE": 1}),
     ("small_m_default", 16, 3072, 768, None),
     ("default", 1000, 776, 328, None),
 ]

@@ -336,29 +336,130 @@ def test_ffn_option_rules():
         assert plan.describe().startswith("two launches")
 
 
-# ---- split-K across a cluster (partial sums added on chip) ---------------------------------
+# ---- split-K: partial sums through device memory (mode 2) or across a cluster (mode 1) -----
 
-@pytest.mark.parametrize("variant,bn,split", [(1, 64, 2), (1, 128, 3), (1, 256, 4), (1, 64, 4),
-                                              (2, 0, 2), (2, 0, 3), (2, 0, 4)])
+SPLIT_CASES = [(1, 1, 64, 2), (1, 1, 128, 3), (1, 1, 256, 4), (1, 1, 64, 4),
+               (1, 2, 0, 2), (1, 2, 0, 3), (1, 2, 0, 4),
+               (2, 1, 64, 2), (2, 1, 128, 3), (2, 1, 256, 4), (2, 1, 64, 8),
+               (2, 2, 0, 2), (2, 2, 0, 6), (2, 2, 0, 8), (2, 2, 16, 5)]
+
+
+@pytest.mark.parametrize("mode,variant,bn,split", SPLIT_CASES)
 @pytest.mark.parametrize("epilog", ["BIAS", "GELU_BIAS", "RELU_AUX_BIAS", "BIAS_RESIDUAL"])
-def test_split_k_parity(variant, bn, split, epilog):
+def test_split_k_parity(mode, variant, bn, split, epilog):
     m, n, k = (300 if variant == 1 else 40), 520, 1000    # 16 K blocks, the last one 40 deep
     layout = "M1" if (split + len(epilog)) % 2 else "1N"
-    p = _inputs(m, n, k, "bf16", layout, seed=split * 10 + variant)
-    opts = {"VARIANT": variant, "SPLIT_K": split}
+    p = _inputs(m, n, k, "bf16", layout, seed=split * 10 + variant + 100 * mode)
+    opts = {"VARIANT": variant, "SPLIT_K": split, "SPLIT_MODE": mode}
     if bn:
         opts["TILE_N"] = bn
     _, _, _, _, desc = check(p, m, n, k, "bf16", epilog, layout, options=opts)
     kpb = -(-16 // split)                       # K blocks per slice; no slice is left empty
-    assert f"split_k={-(-16 // kpb)}" in desc
+    where = "(device memory)" if mode == 2 else "(cluster)"
+    assert f"split_k={-(-16 // kpb)}{where}" in desc
 
 
-@pytest.mark.parametrize("variant,split", [(1, 4), (2, 3)])
-def test_split_k_integer_bit_exact(variant, split):
+@pytest.mark.parametrize("mode,variant,split", [(1, 1, 4), (1, 2, 3), (2, 1, 4), (2, 2, 6)])
+def test_split_k_integer_bit_exact(mode, variant, split):
     m, n, k = (256 if variant == 1 else 16), 264, 512
     p = _inputs(m, n, k, "bf16", "1N", seed=31, kind="int")
     check(p, m, n, k, "bf16", "RELU_AUX_BIAS", "1N", options={"VARIANT": variant,
-                                                             "SPLIT_K": split}, exact=True)
+                                                             "SPLIT_K": split,
+                                                             "SPLIT_MODE": mode}, exact=True)
+
+
+def test_split_k_device_memory_repeats_and_is_deterministic():
+    # The per-tile counts return to zero after every launch, so a plan can be executed again
+    # (with other inputs); the slices are added in slice order, so results repeat bit for bit.
+    from parity_helpers import oracle_ref
+    m, n, k = 24, 776, 1544
+    dev = torch.device("cuda")
+    with gemm_epi.Plan(m, n, k, "bf16", "GELU_BIAS", "1N", variant=2) as plan:
+        plan.set_option("SPLIT_K", 7)
+        plan.set_option("SPLIT_MODE", 2)
+        assert "split_k=7(device memory)" in plan.describe()
+        for seed in (1, 2):
+            p = _inputs(m, n, k, "bf16", "1N", seed=500 + seed)
+            A, B, bias = p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev)
+            outs = []
+            for _ in range(4):
+                D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+                plan.execute(A, B, bias, D)
+                outs.append(D)
+            assert plan.sync_status() == 0
+            for D in outs[1:]:
+                assert torch.equal(D, outs[0])
+            want, _ = oracle_ref(p, "bf16", "GELU_BIAS", "1N")
+            assert rel_err(outs[0], want) <= TOL["bf16"]
+
+
+def test_split_k_device_memory_after_timeout():
+    # A launch that gives up on a wait still counts every CTA, so the next launch is right.
+    from parity_helpers import oracle_ref
+    m, n, k = 32, 520, 1000
+    p = _inputs(m, n, k, "bf16", "1N", seed=61)
+    dev = torch.device("cuda")
+    A, B, bias = p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev)
+    D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    with gemm_epi.Plan(m, n, k, "bf16", "BIAS", "1N", variant=2) as plan:
+        plan.set_option("SPLIT_K", 4)
+        plan.set_option("SPLIT_MODE", 2)
+        plan.set_option("WAIT_LIMIT_US", 20000)
+        plan.set_option("DEBUG_STALL", 1)
+        plan.execute(A, B, bias, D)
+        assert plan.sync_status() == 8
+        plan.set_option("DEBUG_STALL", 0)
+        plan.execute(A, B, bias, D)
+        assert plan.sync_status() == 0
+    want, _ = oracle_ref(p, "bf16", "BIAS", "1N")
+    assert rel_err(D, want) <= TOL["bf16"]
+
+
+def test_split_option_rules():
+    with gemm_epi.Plan(40, 520, 1000, "bf16", "BIAS", "1N", variant=2) as plan:
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.set_option("SPLIT_K", 9)
+        assert e.value.status == 1
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.set_option("SPLIT_MODE", 3)
+        assert e.value.status == 1
+        plan.set_option("SPLIT_MODE", 1)
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.set_option("SPLIT_K", 5)            # a cluster holds at most 4 slices
+        assert e.value.status == 1
+        plan.set_option("SPLIT_MODE", 2)
+        plan.set_option("SPLIT_K", 5)
+        assert "split_k=4(device memory)" in plan.describe()   # 16 K blocks: 4 x 4
+
+
+# ---- swapped kernel with tiles narrower than m (several tiles along the rows of D) --------
+
+@pytest.mark.parametrize("m,bn", [(40, 16), (100, 32), (256, 64), (200, 16)])
+@pytest.mark.parametrize("epilog", ["GELU_BIAS", "RELU_AUX_BIAS", "BIAS_RESIDUAL", "GELU_AUX_BIAS"])
+def test_swapped_narrow_tiles(m, bn, epilog):
+    n, k = 392, 328
+    layout = "M1" if (m + len(epilog)) % 2 else "1N"
+    p = _inputs(m, n, k, "bf16", layout, seed=900 + m + bn)
+    _, _, _, _, desc = check(p, m, n, k, "bf16", epilog, layout,
+                             options={"VARIANT": 2, "TILE_N": bn})
+    assert f"tile=128x{bn}" in desc
+
+
+@pytest.mark.parametrize("m", [1, 16, 64, 100, 256])
+def test_small_m_tile_width_choice(m):
+    # the narrowest power-of-two tile (>= 16 rows) whose tiles all get their own SM
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = 3072
+    full = 16
+    while full < m:
+        full *= 2
+    want = full
+    for bn in (16, 32, 64, 128):
+        if bn < full and (n // 128) * -(-m // bn) <= sms:
+            want = bn
+            break
+    with gemm_epi.Plan(m, n, 768, "bf16", "GELU_BIAS", "1N") as plan:
+        assert f"tile=128x{want}" in plan.describe(), plan.describe()
 
 
 def test_small_m_plans_swapped_without_split():

@@ -35,12 +35,14 @@ def _case(i):
         opts["VARIANT"] = variant
     if variant == 1:
         opts["TILE_N"] = r.choice([64, 128, 256])
-        if r.random() < 0.3:
-            opts["SPLIT_K"] = r.randint(2, 4)
     if variant == 3:
         opts["TILE_N"] = r.choice([224, 256])
     if variant == 2 and r.random() < 0.3:
-        opts["SPLIT_K"] = r.randint(2, 4)
+        opts["TILE_N"] = r.choice([16, 32, 64, 128, 256])
+    if variant in (1, 2) and r.random() < 0.3:
+        mode = r.choice([1, 2])                  # cluster, device memory
+        opts["SPLIT_MODE"] = mode
+        opts["SPLIT_K"] = r.randint(2, 4 if mode == 1 else 8)
     return dict(m=m, n=n, k=k, dtype=r.choice(["bf16", "f16"]), epilog=r.choice(EPILOGS),
                 layout=r.choice(["M1", "1N"]), opts=opts, unfused=r.random() < 0.15,
                 seed=r.randint(0, 10 ** 6))
