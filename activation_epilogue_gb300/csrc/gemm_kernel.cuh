@@ -958,8 +958,62 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         const bool warp_live = lane_base < lane_limit;
         float lane_sum = 0.0f;  // backward, bias gradient along the lanes: this tile's sum
 
+        // CTA-pair kernels, plain forward epilogs: each 32-column chunk in two 16-column
+        // halves, the second half's TMEM load in flight while the first is processed (fewer
+        // live registers, so the activations of 16 values interleave).
+        constexpr bool kHalves = PAIR && CH == 32 &&
+                                 (FFN || EPI == EPI_BIAS || EPI == EPI_RELU_BIAS ||
+                                  EPI == EPI_GELU_BIAS || EPI == EPI_NONE || EPI == EPI_TANH_BIAS);
+        const bool halves = kHalves && (epilog == EPI_BIAS || epilog == EPI_RELU_BIAS ||
+                                        epilog == EPI_GELU_BIAS || epilog == EPI_NONE ||
+                                        epilog == EPI_TANH_BIAS);
         for (int c = half; c < nchunks; c += 2) {
             if (split_owner(quarter, c, w.split) != w.rank) continue;
+            if constexpr (kHalves) {
+                if (halves) {
+                    uint8_t* rowp = epi_buf + lane * 64;
+                    uint32_t ra[16], rb[16];
+                    __syncwarp();
+                    tmem_load_16cols_async(t_lane + c * CH, ra);
+                    tmem_wait_ld(ra);
+                    tmem_load_16cols_async(t_lane + c * CH + 16, rb);
+                    if (warp_live && lane == 0) bulk_wait_group_read<0>();  // last box read
+                    __syncwarp();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (h == 1) tmem_wait_ld(rb);
+                        float v[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            v[j] = __uint_as_float(h == 0 ? ra[j] : rb[j]);
+                            if (F8) v[j] *= fp8_scale;
+                            v[j] += col_bias ? sbias[c * CH + 16 * h + j] : lb;
+                        }
+                        activate(v, epilog);
+                        if (warp_live) {
+#pragma unroll
+                            for (int qq = 0; qq < 2; ++qq) {
+                                const int q = 2 * h + qq;
+                                uint4 w4;
+                                w4.x = pack2(v[8 * qq + 0], v[8 * qq + 1], p.bf16);
+                                w4.y = pack2(v[8 * qq + 2], v[8 * qq + 3], p.bf16);
+                                w4.z = pack2(v[8 * qq + 4], v[8 * qq + 5], p.bf16);
+                                w4.w = pack2(v[8 * qq + 6], v[8 * qq + 7], p.bf16);
+                                *reinterpret_cast<uint4*>(rowp + ((q ^ ((lane >> 1) & 3)) << 4)) = w4;
+                            }
+                        }
+                    }
+                    if (warp_live) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(tmD, epi_buf_u32, col_base + c * CH, lane_base);
+                            bulk_commit_group();
+                        }
+                    }
+                    continue;
+                }
+            }
             // Row-tile residual: this thread's 32 values, requested before the TMEM read so
             // that the load latency overlaps it.
             uint4 rres[4];

@@ -399,6 +399,32 @@ __device__ __forceinline__ void tmem_load_16cols(uint32_t taddr, uint32_t (&r)[3
         : "memory");
 }
 
+// Start loading 16 consecutive fp32 columns of this thread's TMEM lane; the registers are
+// valid only after tmem_wait_ld on them.
+__device__ __forceinline__ void tmem_load_16cols_async(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Wait for this thread's outstanding TMEM loads; r (their destination) is marked as written
+// here, so that nothing reads it earlier.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+
 // Store 32 (or 16) consecutive fp32 columns of this thread's TMEM lane and wait until the
 // stores are done.
 __device__ __forceinline__ void tmem_store_32cols(uint32_t taddr, const uint32_t (&r)[32])
