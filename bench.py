@@ -388,7 +388,34 @@ def run_ours(args, rank, world, local_rank, dist):
             "value": rate, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{rows} full rows (all {w.n} columns, k={w.k}) of the "
                       f"{w.m}x{w.n}x{w.k} {w.epilog} problem, fp64 oracle, {dt:.1f} s"}
+        if not args.no_extras:
+            line["cpu_baseline"]["full_problems"] = oracle_full_problems(dev)
     print(json.dumps(line), flush=True)
+
+
+def oracle_full_problems(dev) -> dict:
+    """The oracle, as it stands, on each of the smaller workloads in full (one call each,
+    inputs drawn on the device as for the fused runs, then copied to the host): seconds and
+    TFLOP/s, the CPU time beside each GPU row."""
+    import oracle
+    from activation_epilogue_gb300 import workloads
+    out = {}
+    for name, g in workloads.GEMMS.items():
+        if g.flops > 3e11:
+            continue  # the headline problem: sampled above
+        inp = {k: v.cpu() for k, v in workloads.gemm_inputs(g, device=dev).items()}
+        t0 = time.perf_counter()
+        oracle.gemm_epi(inp["A"], inp["B"], inp["bias"], dtype=g.dtype, epilog=g.epilog,
+                        bias_layout=g.bias_layout)
+        dt = time.perf_counter() - t0
+        out[name] = {"seconds": dt, "tflops": g.flops / dt / 1e12}
+    for name, f in workloads.FFNS.items():
+        fi = {k: v.cpu() for k, v in workloads.ffn_inputs(f, device=dev).items()}
+        t0 = time.perf_counter()
+        oracle.ffn(fi["X"], fi["W1"], fi["b1"], fi["W2"], fi["b2"], fi["R"], dtype=f.dtype)
+        dt = time.perf_counter() - t0
+        out[name] = {"seconds": dt, "tflops": f.flops / dt / 1e12}
+    return out
 
 
 def whole_job(secs: float, flops_per_step: float, steps: int, world: int, dist, device):
