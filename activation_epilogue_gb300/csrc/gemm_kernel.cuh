@@ -64,7 +64,9 @@ constexpr int pow2_at_least(int x, int p = 32) { return p >= x ? p : pow2_at_lea
 // PAIR: a CTA pair computes a 256 x BN tile with cta_group::2 MMAs; each CTA holds 128 rows
 // of A and BN/2 rows (columns of D) of B per stage, staged as whole 64-row panels (for BN
 // 224 or 192 the last panel is partly unused).
-template <int BN, bool PAIR = false>
+// EW: epilogue warps (8, or 16 for the CTA-pair kernels of the costlier activations on short
+// K; with more than 8 the bias is shuffled between lanes instead of staged in shared memory).
+template <int BN, bool PAIR = false, int EW = 8>
 struct TileCfg {
     static constexpr int kBRows = PAIR ? (BN / 2 + 63) / 64 * 64 : BN;
     static constexpr int kABytes = kBM * kBK * 2;      // MMA-A operand: 128 rows x 64 k
@@ -75,9 +77,9 @@ struct TileCfg {
     static constexpr int kChunk = BN < 32 ? BN : 32;            // columns per TMEM load
     static constexpr int kTmemCols = pow2_at_least(2 * BN);  // two accumulators
     static constexpr int kOffEpi = kStages * kStageBytes;        // one 2 KB box per warp
-    static constexpr int kEpiBytes = kEpiWarps * 2048;
+    static constexpr int kEpiBytes = EW * 2048;
     static constexpr int kOffBias = kOffEpi + kEpiBytes;         // 2 x 256 fp32 per warp
-    static constexpr int kBiasBytes = kEpiWarps * 512 * 4;
+    static constexpr int kBiasBytes = EW == 8 ? EW * 512 * 4 : 0;
     static constexpr int kOffBar = kOffBias + kBiasBytes;
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
@@ -824,7 +826,7 @@ __device__ __noinline__ bool publish_partials_global(const GemmParams& p, uint8_
 
 // EPI >= 0 fixes the epilog at compile time (only its code is in the kernel); -1 reads it
 // from the parameters.
-template <int BN, bool SWAP, bool PAIR = false, int EPI = -1, bool F8 = false>
+template <int BN, bool SWAP, bool PAIR = false, int EPI = -1, bool F8 = false, int EW = 8>
 __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem, uint32_t sbase,
                                              uint32_t bar0, uint32_t tmem_base,
                                              volatile int* abort_flag)
@@ -832,18 +834,21 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
     // The FFN kernel runs GELU_BIAS on GEMM-1 tiles and BIAS_RESIDUAL on GEMM-2 tiles.
     constexpr bool FFN = EPI == kEpiFfn;
     const int epilog0 = FFN ? EPI_GELU_BIAS : (EPI >= 0 ? EPI : p.epilog);
-    using C = TileCfg<BN, PAIR>;
+    using C = TileCfg<BN, PAIR, EW>;
     constexpr int CH = C::kChunk;
+    constexpr int kParts = EW / 4;       // warps per TMEM lane quarter
+    constexpr int kOwn = (BN / CH + kParts - 1) / kParts;  // most chunks a warp takes
+    static_assert(EW == 8 || (PAIR && CH == 32 && EW % 4 == 0), "more warps: CTA-pair kernels only");
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int ew = warp - 2;             // epilogue warp 0..7
+    const int ew = warp - 2;             // epilogue warp 0 .. EW-1
     const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
-    const int half = ew >> 2;            // the pair's warps take alternate chunks
+    const int part = ew >> 2;            // a quarter's warps take every kParts-th chunk
     WorkRange w = work_range<PAIR>(p);
     if (PAIR) w.split = 1;  // (compile-time: the pair kernel never splits K)
     // This warp's own staging area for per-column values (bias; LayerNorm: two arrays of
-    // 256): no other warp reads it, so a __syncwarp orders it.
-    float* sbias = reinterpret_cast<float*>(smem + C::kOffBias) + ew * 512;
+    // 256): no other warp reads it, so a __syncwarp orders it.  (None with more warps.)
+    float* sbias = EW == 8 ? reinterpret_cast<float*>(smem + C::kOffBias) + ew * 512 : nullptr;
     uint8_t* epi_buf = smem + C::kOffEpi + ew * 2048;
     const uint32_t epi_buf_u32 = sbase + C::kOffEpi + ew * 2048;
     // Bias, residual and the outputs may belong to a programmatic predecessor grid.
@@ -866,7 +871,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         // LayerNorm folded into the GEMM: pre = rstd_i (acc - mu_i c_j) + b'_j, with (mu, rstd)
         // per row of D and (c, b') per column of D, in fp32
         // (row-tile and pair kernels only: the planner never runs it on the swapped kernel)
-        const bool ln = !SWAP && epilog == EPI_LN_GELU_BIAS;
+        const bool ln = EW == 8 && !SWAP && epilog == EPI_LN_GELU_BIAS;
         const bool has_bias = epilog != EPI_NONE && !bwd && !ln;
         // Bias (and, backward, bias gradient) that varies along the accumulator's columns
         // (staged in shared memory; column sums) or along its lanes (one value per thread).
@@ -881,7 +886,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                                    : tm * kBM + quarter * 32;
         const int lane_idx = lane_base + lane;
         if (*abort_flag) break;
-        if (col_bias) {
+        if (EW == 8 && col_bias) {
             __syncwarp();  // every lane is done reading the previous tile's values
             const uint16_t* bsrc = static_cast<const uint16_t*>(bias_ptr) + col_base;
             if (col_base + BN <= col_limit && (reinterpret_cast<uintptr_t>(bsrc) & 15) == 0) {
@@ -936,6 +941,15 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
 
         const int valid_cols = min(BN, col_limit - col_base);
         const int nchunks = (valid_cols + CH - 1) / CH;
+        // more warps: lane l holds the bias of column l of each of its chunks (shuffled out)
+        float bl[EW == 8 ? 1 : kOwn];
+        if constexpr (EW != 8) {
+#pragma unroll
+            for (int i = 0; i < kOwn; ++i) {
+                const int col = col_base + (part + i * kParts) * CH + lane;
+                bl[i] = col_bias && col < col_limit ? load_16bit(bias_ptr, col, p.bf16) : 0.0f;
+            }
+        }
         if (!SWAP && (epilog == EPI_BIAS_RESIDUAL || epilog == EPI_DGELU_BGRAD) &&
             lane_idx < lane_limit) {
             // While the MMAs of the tile finish, bring this thread's row segments of the
@@ -943,7 +957,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
             const uint16_t* src = epilog == EPI_BIAS_RESIDUAL
                                       ? R
                                       : static_cast<const uint16_t*>(p.aux_in);
-            for (int c = half; c < nchunks; c += 2)
+            for (int c = part; c < nchunks; c += kParts)
                 if (split_owner(quarter, c, w.split) == w.rank)
                     prefetch_global_l2(src + static_cast<long long>(lane_idx) * ncols + col_base + c * CH);
         }
@@ -967,10 +981,17 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         const bool halves = kHalves && (epilog == EPI_BIAS || epilog == EPI_RELU_BIAS ||
                                         epilog == EPI_GELU_BIAS || epilog == EPI_NONE ||
                                         epilog == EPI_TANH_BIAS);
-        for (int c = half; c < nchunks; c += 2) {
+        for (int c = part; c < nchunks; c += kParts) {
             if (split_owner(quarter, c, w.split) != w.rank) continue;
             if constexpr (kHalves) {
                 if (halves) {
+                    float bcur = 0.0f;  // more warps: this lane's bias value for the chunk
+                    if constexpr (EW != 8) {
+                        const int oi = (c - part) / kParts;
+                        bcur = bl[0];
+#pragma unroll
+                        for (int i = 1; i < kOwn; ++i) bcur = oi == i ? bl[i] : bcur;
+                    }
                     uint8_t* rowp = epi_buf + lane * 64;
                     uint32_t ra[16], rb[16];
                     __syncwarp();
@@ -987,7 +1008,10 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                         for (int j = 0; j < 16; ++j) {
                             v[j] = __uint_as_float(h == 0 ? ra[j] : rb[j]);
                             if (F8) v[j] *= fp8_scale;
-                            v[j] += col_bias ? sbias[c * CH + 16 * h + j] : lb;
+                            if constexpr (EW == 8)
+                                v[j] += col_bias ? sbias[c * CH + 16 * h + j] : lb;
+                            else
+                                v[j] += col_bias ? __shfl_sync(0xFFFFFFFFu, bcur, 16 * h + j) : lb;
                         }
                         activate(v, epilog);
                         if (warp_live) {
@@ -1014,6 +1038,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                     continue;
                 }
             }
+            if constexpr (EW != 8) continue;  // (more warps: plain forward epilogs only)
             // Row-tile residual: this thread's 32 values, requested before the TMEM read so
             // that the load latency overlaps it.
             uint4 rres[4];
@@ -1238,7 +1263,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         }
         if (bwd && !along_cols && lane_idx < lane_limit) {
             bool any_chunk = false;  // this warp owned a chunk of the tile
-            for (int c = half; c < nchunks; c += 2)
+            for (int c = part; c < nchunks; c += kParts)
                 any_chunk = any_chunk || split_owner(quarter, c, w.split) == w.rank;
             if (any_chunk) atomicAdd(p.dbias + lane_idx, lane_sum);
         }
@@ -1269,10 +1294,10 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
 // ------------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------------
-template <int BN, bool SWAP, bool PAIR = false, int EPI = -1, bool F8 = false>
-__global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_constant__ GemmParams p)
+template <int BN, bool SWAP, bool PAIR = false, int EPI = -1, bool F8 = false, int EW = 8>
+__global__ void __launch_bounds__(64 + 32 * EW, 1) gemm_epi_kernel(const __grid_constant__ GemmParams p)
 {
-    using C = TileCfg<BN, PAIR>;
+    using C = TileCfg<BN, PAIR, EW>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -1300,7 +1325,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar0 + 8u * (kBarTmemFull + a), 1);
-            mbar_init(bar0 + 8u * (kBarTmemEmpty + a), PAIR ? 2 * kEpiThreads : kEpiThreads);
+            mbar_init(bar0 + 8u * (kBarTmemEmpty + a), (PAIR ? 2 : 1) * 32 * EW);
         }
         mbar_init(bar0 + 8u * kBarStall, 1);
         mbar_init(bar0 + 8u * kBarDrain, 1);
@@ -1347,7 +1372,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
             } else if (split) {
                 publish_partials<BN, SWAP>(p, smem, bar0, tmem_base, abort_flag);
             } else {
-                run_epilogue<BN, SWAP, PAIR, EPI, F8>(p, smem, sbase, bar0, tmem_base, abort_flag);
+                run_epilogue<BN, SWAP, PAIR, EPI, F8, EW>(p, smem, sbase, bar0, tmem_base, abort_flag);
             }
         }
     } else {

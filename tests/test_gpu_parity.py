@@ -524,6 +524,21 @@ def test_pair_parity(bn, epilog, dtype):
     assert "variant=row-pair" in desc and f"tile=256x{bn} " in desc
 
 
+@pytest.mark.parametrize("bn", [256, 224])
+@pytest.mark.parametrize("epilog", ["GELU_BIAS", "TANH_BIAS"])
+@pytest.mark.parametrize("k,grid", [(200, 0), (264, 6), (520, 0), (600, 4)])
+def test_pair_epilogue_warp_variants(bn, epilog, k, grid):
+    # GELU_BIAS and TANH_BIAS run 16 epilogue warps (bias shuffled between lanes) when K <= 512
+    # and 8 otherwise; both, with a few pairs walking many tiles, and both bias layouts
+    m, n = 1280, 1000
+    layout = "M1" if (k + bn) % 3 == 0 else "1N"
+    p = _inputs(m, n, k, "bf16", layout, seed=k + bn + len(epilog))
+    opts = {"VARIANT": 3, "TILE_N": bn}
+    if grid:
+        opts["GRID"] = grid
+    check(p, m, n, k, "bf16", epilog, layout, options=opts)
+
+
 @pytest.mark.parametrize("m,n,want", [(4096, 4096, 224), (8192, 16384, 256), (65536, 16384, 256),
                                       (4096, 1024, 256)])
 def test_pair_tile_width_choice(m, n, want):
