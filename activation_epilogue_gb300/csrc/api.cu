@@ -162,6 +162,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
     p->group_m = 1;
     p->split = 1;
     p->split_global = 0;
+    p->pair_mc = 0;
     p->kb_per_split = 0;
     if (p->m == 0 || p->n == 0) {
         p->variant = kEmpty;
@@ -204,7 +205,26 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             else
                 v = kRowTile;
         }
-        if (v == 3) v = kRowPair;  // option value 3 selects the CTA-pair kernel
+        // (option values: 1 row-tile, 2 swapped, 3 CTA pairs, 4 CTA pairs in clusters of two
+        // pairs sharing B; the internal Variant codes differ)
+        if (p->opt_variant == 4) {
+            p->pair_mc = 1;
+            v = kRowPair;
+        } else if (p->opt_variant == 0 && v == kRowPair) {
+            // Two pairs per cluster once there are two waves of double tiles: each B panel is
+            // read once for two row tiles, in step.  Measured on GB300 (same box, runs
+            // alternating): 65536 x 16384 x 8192 RELU_BIAS DRAM reads 39.5 -> 23.9 GB per
+            // launch and 1734 -> 1775 TFLOP/s (20-step bench, mean of three each); 4096^3
+            // RELU_BIAS 1597 -> 1642 TFLOP/s.  Clusters of four leave 8 of 152 SMs idle, which
+            // a single wave cannot make up (4096 x 1024 x 4096: equal), so shallower problems
+            // keep single pairs.
+            if (rowpair_prepare(256) != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
+            long long clusters = rowpair_max_clusters4(256);
+            if (clusters > p->sm_count / 4) clusters = p->sm_count / 4;
+            const long long dtiles = ((p->m + 511) / 512) * ((p->n + 255) / 256);
+            if (clusters > 0 && dtiles >= 2 * clusters) p->pair_mc = 1;
+        }
+        if (p->opt_variant == 3) v = kRowPair;  // option value 3: the CTA-pair kernel
         if (v == kSwapped && p->m > kSwappedMaxM) return GEMM_EPI_ERR_INVALID_ARG;
         // the swapped kernel has no LayerNorm epilogue
         if (v == kSwapped && p->epilog == GEMM_EPI_LN_GELU_BIAS) return GEMM_EPI_ERR_INVALID_ARG;
@@ -219,7 +239,15 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             if (pairs > p->sm_count / 2) pairs = p->sm_count / 2;
             if (p->opt_grid > 0 && p->opt_grid / 2 < pairs) pairs = p->opt_grid / 2;
             if (pairs < 1) return GEMM_EPI_ERR_LAUNCH;
-            p->bn = p->opt_bn ? p->opt_bn : pick_pair_bn(p->m, p->n, pairs);
+            if (p->pair_mc) {
+                // width by the waves of double tiles (two 256-row tiles) over the clusters
+                long long clusters = rowpair_max_clusters4(256);
+                if (clusters > p->sm_count / 4) clusters = p->sm_count / 4;
+                p->bn = p->opt_bn ? p->opt_bn
+                                  : pick_pair_bn((p->m + 511) / 512 * 256, p->n, clusters > 0 ? clusters : 1);
+            } else {
+                p->bn = p->opt_bn ? p->opt_bn : pick_pair_bn(p->m, p->n, pairs);
+            }
             p->tiles_m = static_cast<int>((p->m + 255) / 256);
             p->tiles_n = static_cast<int>((p->n + p->bn - 1) / p->bn);
             p->stages = rowpair_stages(p->bn);
@@ -232,6 +260,21 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             int gm = p->opt_group_m ? p->opt_group_m : 8;
             if (gm > p->tiles_m) gm = p->tiles_m;
             p->group_m = gm < 1 ? 1 : gm;
+            if (p->pair_mc) {
+                // clusters of two pairs on double rows of tiles (the group counts double
+                // rows); an odd last row tile leaves its second pair without rows of A
+                long long clusters = rowpair_max_clusters4(p->bn);
+                if (clusters > p->sm_count / 4) clusters = p->sm_count / 4;
+                if (p->opt_grid > 0 && p->opt_grid / 4 < clusters) clusters = p->opt_grid / 4;
+                if (clusters < 1) return GEMM_EPI_ERR_LAUNCH;
+                const int tiles_m2 = (p->tiles_m + 1) / 2;
+                const long long dtiles = static_cast<long long>(tiles_m2) * p->tiles_n;
+                if (clusters > dtiles) clusters = dtiles;
+                p->grid = static_cast<int>(4 * clusters);
+                int gm2 = p->opt_group_m ? (p->opt_group_m + 1) / 2 : 4;
+                if (gm2 > tiles_m2) gm2 = tiles_m2;
+                p->group_m = gm2 < 1 ? 1 : gm2;
+            }
         } else if (v == kRowTile) {
             if (p->opt_bn && p->opt_bn != 64 && p->opt_bn != 128 && p->opt_bn != 256)
                 return GEMM_EPI_ERR_INVALID_ARG;
@@ -291,7 +334,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
              static_cast<long long>(p->k),
              p->dtype == GEMM_EPI_E4M3 ? "e4m3" : p->dtype == GEMM_EPI_BF16 ? "bf16" : "f16",
              ename[p->epilog], p->bias_layout == GEMM_EPI_BIAS_M1 ? "(m,1)" : "(1,n)",
-             vname[p->variant], p->variant == kRowPair ? 256 : 128, p->bn,
+             p->pair_mc ? "row-pair-x2" : vname[p->variant], p->variant == kRowPair ? 256 : 128, p->bn,
              p->dtype == GEMM_EPI_E4M3 ? 128 : 64, p->stages, p->smem, p->tiles_m, p->tiles_n,
              p->k_blocks,
              p->split, p->split > 1 ? (p->split_global ? "(device memory)" : "(cluster)") : "",
@@ -433,6 +476,8 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, in
     prm.split_global = p->split_global;
     prm.split_ws = p->d_split_ws;
     prm.split_count = p->d_split_count;
+    prm.pair_mc = p->pair_mc;
+    prm.tiles_m2 = (p->tiles_m + 1) / 2;
     prm.prefetch = p->prefetch;
     cudaError_t e;
     if (p->variant == kRowPair && p->dtype == GEMM_EPI_E4M3)
@@ -626,7 +671,7 @@ gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt,
     gemm_epi_plan_s saved = *p;
     switch (opt) {
     case GEMM_EPI_OPT_VARIANT:
-        if (value < 0 || value > 3) return GEMM_EPI_ERR_INVALID_ARG;
+        if (value < 0 || value > 4) return GEMM_EPI_ERR_INVALID_ARG;
         p->opt_variant = static_cast<int>(value);
         break;
     case GEMM_EPI_OPT_TILE_N:

@@ -149,6 +149,7 @@ struct WorkRange {
     int rank, split;         // split-K: cluster rank and size (split == 1: no split)
     int grank, gsplit;       // split-K through device memory: K slice and slices (1: none)
     int pair_rank;           // CTA pairs: 0 = the even CTA (issues the MMAs), 1 = the odd
+    int pair_index;          // clusters of two pairs: which pair of the cluster (else 0)
 };
 
 template <bool PAIR = false>
@@ -156,13 +157,16 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
 {
     WorkRange w;
     if (PAIR) {
-        // persistent CTA pairs (clusters of 2) walking 256-row tiles
+        // persistent CTA pairs (clusters of 2) walking 256-row tiles, or clusters of two
+        // pairs walking double rows of tiles
+        const int cr = static_cast<int>(cluster_ctarank());
         w.first = static_cast<int>(cluster_id_x());
-        w.stride = static_cast<int>(gridDim.x / 2);
-        w.end = p.tiles_m * p.tiles_n + p.ffn_tiles2;
+        w.stride = static_cast<int>(gridDim.x / (p.pair_mc ? 4 : 2));
+        w.end = p.pair_mc ? p.tiles_m2 * p.tiles_n : p.tiles_m * p.tiles_n + p.ffn_tiles2;
         w.rank = 0;
         w.split = 1;
-        w.pair_rank = static_cast<int>(cluster_ctarank());
+        w.pair_rank = cr & 1;
+        w.pair_index = p.pair_mc ? cr >> 1 : 0;
         w.kb_begin = 0;
         w.kb_end = p.k_blocks;
         w.grank = 0;
@@ -178,6 +182,7 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
         w.grank = static_cast<int>(blockIdx.x) - tile * p.split;
         w.gsplit = p.split;
         w.pair_rank = 0;
+        w.pair_index = 0;
         w.kb_begin = w.grank * p.kb_per_split;
         w.kb_end = min(p.k_blocks, w.kb_begin + p.kb_per_split);
         return w;
@@ -191,6 +196,7 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
         w.grank = 0;
         w.gsplit = 1;
         w.pair_rank = 0;
+        w.pair_index = 0;
         w.kb_begin = w.rank * p.kb_per_split;
         w.kb_end = min(p.k_blocks, w.kb_begin + p.kb_per_split);
     } else {
@@ -202,6 +208,7 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
         w.grank = 0;
         w.gsplit = 1;
         w.pair_rank = 0;
+        w.pair_index = 0;
         w.kb_begin = 0;
         w.kb_end = p.k_blocks;
     }
@@ -224,7 +231,18 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int tile, con
 {
     TileInfo t;
     const int tiles1 = p.tiles_m * p.tiles_n;
-    if (!FFN || tile < tiles1) {
+    if (!FFN && p.pair_mc) {
+        // a double row of tiles: this pair's row tile of it
+        const int per_group = p.group_m * p.tiles_n;  // (group_m counts double rows here)
+        const int g = tile / per_group;
+        const int first = g * p.group_m;
+        const int rows_in_group = min(p.tiles_m2 - first, p.group_m);
+        const int r = tile - g * per_group;
+        t.tm = 2 * (first + r % rows_in_group) + w.pair_index;
+        t.tn = r / rows_in_group;
+        t.prob = 0;
+        t.kb_end = w.kb_end;
+    } else if (!FFN || tile < tiles1) {
         tile_coords(tile, p, t.tm, t.tn);
         t.prob = 0;
         t.kb_end = w.kb_end;
@@ -330,12 +348,23 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase,
         // Both CTAs' halves are counted on the even CTA's "full" barrier, which that CTA
         // arms with the bytes of both (the odd CTA's bytes may land first: the
         // transaction count is signed).
-        const uint32_t rank = cluster_ctarank();
+        const uint32_t cr = cluster_ctarank();
+        const uint32_t rank = cr & 1u;
         if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::kStageBytes);
-        const uint32_t fb0 = map_shared_rank(fb, 0);
+        const uint32_t fb0 = map_shared_rank(fb, cr & ~1u);
         const CUtensorMap* mA = prob ? &p.tm_A2 : &p.tm_A;
         const CUtensorMap* mB = prob ? &p.tm_B2 : &p.tm_B;
         tma_load_2d_pair(sa, mA, fb0, k0, tm * 2 * kBM + static_cast<int>(rank) * kBM);
+        if (p.pair_mc) {
+            // two pairs, one column tile: each CTA loads one of the two 64-column panels of
+            // its half of B and multicasts it to the same half in both pairs
+            static_assert(C::kBRows == 128, "two 64-column panels per CTA");
+            const uint32_t pp = cr >> 1;
+            tma_load_2d_pair_mc(sb + pp * 8192, mB, fb0,
+                                tn * BN + static_cast<int>(rank) * (BN / 2) + static_cast<int>(pp) * 64,
+                                k0, static_cast<uint16_t>((1u << rank) | (1u << (2u + rank))));
+            return;
+        }
 #pragma unroll
         for (int q = 0; q < C::kBRows / 64; ++q)
             tma_load_2d_pair(sb + q * 8192, mB, fb0,
@@ -461,6 +490,11 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
                                                SWAP ? 0u : 1u, PAIR ? 2 * kBM : kBM, BN);
     const WorkRange w = work_range<PAIR>(p);
     if (PAIR && w.pair_rank != 0) return;
+    // commit targets: this (even) CTA, its pair, every CTA whose stages these MMAs read from
+    const uint32_t self = PAIR ? cluster_ctarank() : 0u;
+    const uint16_t mask_self = static_cast<uint16_t>(1u << self);
+    const uint16_t mask_pair = static_cast<uint16_t>(3u << self);
+    const uint16_t mask_all = p.pair_mc ? 0xF : 0x3;
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -512,9 +546,10 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
                     mma_f16_ss(d_tmem, ad, bd, idesc, (kb > w.kb_begin || kk > 0) ? 1u : 0u);
             }
             issued_any = true;
-            // stage free (in both CTAs of a pair) once these MMAs finish
+            // stage free (in both CTAs of a pair, or all four CTAs of a cluster of two pairs,
+            // whose "empty" barriers then wait for both pairs' commits) once these MMAs finish
             if constexpr (PAIR)
-                mma_commit_pair(bar0 + 8u * (kBarEmpty + stage), 0x3);
+                mma_commit_pair(bar0 + 8u * (kBarEmpty + stage), mask_all);
             else
                 mma_commit(bar0 + 8u * (kBarEmpty + stage));
             if (++stage == C::kStages) {
@@ -525,7 +560,7 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
         if (!ok) break;
         // accumulator ready for the epilogue (of both CTAs of a pair)
         if constexpr (PAIR)
-            mma_commit_pair(bar0 + 8u * (kBarTmemFull + acc), 0x3);
+            mma_commit_pair(bar0 + 8u * (kBarTmemFull + acc), mask_pair);
         else
             mma_commit(bar0 + 8u * (kBarTmemFull + acc));
         acc ^= 1;
@@ -534,7 +569,7 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
     if (!ok && issued_any) {
         // Wait for every MMA this thread issued before tensor memory is released.
         if constexpr (PAIR)
-            mma_commit_pair(bar0 + 8u * kBarDrain, 0x1);
+            mma_commit_pair(bar0 + 8u * kBarDrain, mask_self);
         else
             mma_commit(bar0 + 8u * kBarDrain);
         wait_bounded(bar0 + 8u * kBarDrain, 0, abort_flag, kDrainLimitNs, false);
@@ -1269,7 +1304,8 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         }
         tcgen05_fence_before_sync();
         if constexpr (PAIR)  // the even CTA's MMAs write both CTAs' accumulators
-            mbar_arrive_cluster(map_shared_rank(bar0 + 8u * (kBarTmemEmpty + acc), 0));
+            mbar_arrive_cluster(map_shared_rank(bar0 + 8u * (kBarTmemEmpty + acc),
+                                                cluster_ctarank() & ~1u));
         else
             mbar_arrive(bar0 + 8u * (kBarTmemEmpty + acc));
         acc ^= 1;
@@ -1321,7 +1357,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1) gemm_epi_kernel(const __grid_
         }
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar0 + 8u * (kBarFull + s), 1);
-            mbar_init(bar0 + 8u * (kBarEmpty + s), 1);
+            mbar_init(bar0 + 8u * (kBarEmpty + s), PAIR && p.pair_mc ? 2 : 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar0 + 8u * (kBarTmemFull + a), 1);

@@ -92,6 +92,12 @@ struct GemmParams {
     int split_global;
     float* split_ws;
     unsigned* split_count;
+    // CTA-pair kernel in clusters of two pairs (pair_mc == 1): the pairs of a cluster take
+    // the row tiles 2 tm2 and 2 tm2 + 1 of one column tile (tiles_m2 = double rows), load
+    // each B panel once and multicast it to both pairs, and free a stage only when both
+    // pairs' MMAs have read it.
+    int pair_mc;
+    int tiles_m2;
     // The producer also prefetches into L2 the operand boxes of the K block this many
     // blocks ahead of the one it loads (0 = off), so that a first touch of a panel in
     // device memory overlaps the loads of the blocks before it.
@@ -130,6 +136,8 @@ cudaError_t rowpair_launch(int bn, const GemmParams& p, int grid, cudaStream_t s
 int rowpair_smem_bytes(int bn);
 int rowpair_stages(int bn);
 int rowpair_max_clusters(int bn);
+// Resident clusters of two CTA pairs (four CTAs) of the pair kernel.
+int rowpair_max_clusters4(int bn);
 
 // CTA-pair kernel on E4M3 inputs (256 x 256 tiles), epilogs BIAS, RELU_BIAS, GELU_BIAS,
 // RELU_AUX_BIAS, BIAS_RESIDUAL, NONE.

@@ -32,6 +32,7 @@ struct gemm_epi_plan_s {
     int variant, bn, stages, smem, grid, group_m, tiles_m, tiles_n, k_blocks;
     int split, kb_per_split;  // split-K slices (split == 1: persistent kernel)
     int split_global;         // 1: the slices meet in device memory, 0: in a cluster
+    int pair_mc;              // CTA-pair kernel in clusters of two pairs sharing B
     // options (0 = automatic)
     int opt_variant, opt_bn, opt_split_k, opt_grid, opt_group_m, opt_split_mode;
     // split-K through device memory: fp32 partial tiles [tile][slice][128 x bn] and the

@@ -539,11 +539,68 @@ def test_pair_epilogue_warp_variants(bn, epilog, k, grid):
     check(p, m, n, k, "bf16", epilog, layout, options=opts)
 
 
+# ---- the CTA-pair kernel in clusters of two pairs sharing B (multicast) ----------------------
+
+@pytest.mark.parametrize("bn", [256, 224])
+@pytest.mark.parametrize("epilog", EPILOGS)
+def test_pair_x2_parity(bn, epilog):
+    m, n, k = 1000, 520, 200           # 4 ragged 256-row tiles = 2 double rows, ragged N and K
+    layout = "M1" if (EPILOGS.index(epilog) + bn // 32) % 2 else "1N"
+    p = _inputs(m, n, k, "bf16", layout, seed=161 + EPILOGS.index(epilog) + bn)
+    _, _, _, _, desc = check(p, m, n, k, "bf16", epilog, layout,
+                             options={"VARIANT": 4, "TILE_N": bn})
+    assert "variant=row-pair-x2" in desc and f"tile=256x{bn} " in desc
+
+
+@pytest.mark.parametrize("m", [300, 600, 1280])
+def test_pair_x2_odd_row_tiles(m):
+    # an odd number of 256-row tiles: the last cluster's second pair has no rows of A
+    n, k = 776, 328
+    p = _inputs(m, n, k, "f16", "1N", seed=m + 5)
+    check(p, m, n, k, "f16", "RELU_AUX_BIAS", "1N", options={"VARIANT": 4})
+
+
+@pytest.mark.parametrize("grid,group_m", [(4, 1), (8, 2), (12, 8)])
+def test_pair_x2_persistent_walk(grid, group_m):
+    m, n, k = 2304, 1000, 520          # 9 row tiles (5 double rows), 5 column tiles, 9 K blocks
+    p = _inputs(m, n, k, "bf16", "1N", seed=grid + 170)
+    check(p, m, n, k, "bf16", "GELU_BIAS", "1N",
+          options={"VARIANT": 4, "GRID": grid, "GROUP_M": group_m})
+
+
+def test_pair_x2_integer_bit_exact():
+    m, n, k = 1024, 264, 64
+    p = _inputs(m, n, k, "bf16", "1N", seed=172, kind="int")
+    check(p, m, n, k, "bf16", "RELU_AUX_BIAS", "1N", options={"VARIANT": 4}, exact=True)
+
+
+@pytest.mark.parametrize("m,n,x2", [(65536, 16384, True), (8192, 16384, True), (4096, 4096, True),
+                                    (4096, 1024, False), (8192, 8192, True), (2048, 2048, False)])
+def test_pair_x2_automatic_choice(m, n, x2):
+    # two pairs per cluster once the double tiles fill two waves of the resident clusters
+    with gemm_epi.Plan(m, n, 4096, "bf16", "RELU_BIAS", "1N") as plan:
+        d = plan.describe()
+    assert ("variant=row-pair-x2" in d) == x2, d
+
+
+def test_pair_x2_option_rules():
+    with gemm_epi.Plan(1024, 1024, 1024, "e4m3", "RELU_BIAS", "1N") as plan:
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.set_option("VARIANT", 4)   # E4M3 plans run single pairs only
+        assert e.value.status == 1
+    with gemm_epi.Plan(1024, 1024, 1024, "bf16", "RELU_BIAS", "1N") as plan:
+        plan.set_option("VARIANT", 4)
+        d = plan.describe()
+        assert "variant=row-pair-x2" in d and " grid=" in d
+        grid = int(d.split(" grid=")[1].split()[0])
+        assert grid % 4 == 0
+
+
 @pytest.mark.parametrize("m,n,want", [(4096, 4096, 224), (8192, 16384, 256), (65536, 16384, 256),
                                       (4096, 1024, 256)])
 def test_pair_tile_width_choice(m, n, want):
     """The planner trades tile width against wave quantization over the resident pairs."""
-    with gemm_epi.Plan(m, n, 1024, "bf16", "RELU_BIAS", "1N") as plan:
+    with gemm_epi.Plan(m, n, 1024, "bf16", "RELU_BIAS", "1N", variant=3) as plan:
         desc = plan.describe()
     assert "variant=row-pair" in desc and f"tile=256x{want} " in desc, desc
 
