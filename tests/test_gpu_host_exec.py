@@ -93,3 +93,28 @@ def test_execute_host_rules():
         assert e.value.status == 1
     with gemm_epi.Plan(0, 64, 64, "bf16", "BIAS", "1N") as plan:  # empty: nothing to do
         plan.execute_host(None, None, None, None)
+
+
+def test_execute_host_large_chunks_two_pair_clusters():
+    # 16 chunks of 1280 rows x 8192 columns: each chunk plan runs the CTA-pair kernel in
+    # clusters of two pairs sharing B; rows on and around chunk edges checked by the oracle,
+    # and the whole result against the same plan on device buffers (the same kernels)
+    m, n, k = 20480, 8192, 64
+    p = workloads.random_problem(m, n, k, dtype="bf16", bias_layout="1N", residual=False,
+                                 seed=2048)
+    with gemm_epi.Plan(m, n, k, "bf16", "RELU_AUX_BIAS", "1N") as plan:
+        assert "variant=row-pair-x2" in plan.describe()
+        D, aux = _run_host(p, m, n, k, "bf16", "RELU_AUX_BIAS", "1N", plan=plan)
+        dev = torch.device("cuda")
+        Dd = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        auxd = torch.empty((m, n // 32), dtype=torch.int32, device=dev)
+        plan.execute(p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev), Dd, aux=auxd)
+        assert plan.sync_status() == 0
+    assert torch.equal(D, Dd.cpu())
+    assert torch.equal(aux, auxd.cpu())
+    rows = [0, 1, 1279, 1280, 1281, 2559, 2560, 10239, 10240, 20478, 20479]
+    want, pre = oracle.gemm_epi(p["A"][rows], p["B"], p["bias"], dtype="bf16",
+                                epilog="RELU_AUX_BIAS", bias_layout="1N", want_pre=True)
+    assert rel_err(D[rows], want) <= TOL["bf16"]
+    words = aux[rows].numpy().view(np.uint32)
+    assert aux_bad_bits(words, pre, AUX_BAND) == 0
