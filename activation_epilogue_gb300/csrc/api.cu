@@ -170,7 +170,8 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
         p->variant = kBiasOnly;
     } else if (p->dtype == GEMM_EPI_E4M3) {
         // E4M3: the CTA-pair kernel with 256 x 256 tiles and 128-deep K blocks, any shape
-        if ((p->opt_variant != 0 && p->opt_variant != 3) || (p->opt_bn != 0 && p->opt_bn != 256))
+        if ((p->opt_variant != 0 && p->opt_variant != 3 && p->opt_variant != 4) ||
+            (p->opt_bn != 0 && p->opt_bn != 256))
             return GEMM_EPI_ERR_INVALID_ARG;
         if (fp8_pair_prepare() != cudaSuccess || rowpair_prepare(256) != cudaSuccess)
             return GEMM_EPI_ERR_LAUNCH;
@@ -192,6 +193,24 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
         int gm = p->opt_group_m ? p->opt_group_m : 8;
         if (gm > p->tiles_m) gm = p->tiles_m;
         p->group_m = gm < 1 ? 1 : gm;
+        // clusters of two pairs sharing B only when asked for: E4M3 moves half the bytes
+        // per flop, and measured on GB300 the clusters were level or slower at
+        // 65536 x 16384 x 8192 and 8192^3 (3283-3344 against 3299-3550 TFLOP/s; 3300-3603
+        // against 3585-3649), faster only at 4096^3 (3064-3076 against 2998-3010)
+        long long clusters = rowpair_max_clusters4(256);
+        if (clusters > p->sm_count / 4) clusters = p->sm_count / 4;
+        const int tiles_m2 = (p->tiles_m + 1) / 2;
+        const long long dtiles = static_cast<long long>(tiles_m2) * p->tiles_n;
+        if (p->opt_variant == 4) {
+            if (p->opt_grid > 0 && p->opt_grid / 4 < clusters) clusters = p->opt_grid / 4;
+            if (clusters < 1) return GEMM_EPI_ERR_LAUNCH;
+            if (clusters > dtiles) clusters = dtiles;
+            p->pair_mc = 1;
+            p->grid = static_cast<int>(4 * clusters);
+            int gm2 = p->opt_group_m ? (p->opt_group_m + 1) / 2 : 4;
+            if (gm2 > tiles_m2) gm2 = tiles_m2;
+            p->group_m = gm2 < 1 ? 1 : gm2;
+        }
     } else {
         int v = p->opt_variant;
         if (v == 0) {
@@ -378,7 +397,7 @@ gemm_epi_status ensure_maps(gemm_epi_plan_s* p, const void* A, const void* B, vo
         // A [m][k] and B transposed [n][k], bytes, K-major boxes {128 k, 128 rows}; D bf16
         const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
         if (!encode_2d(&p->tm_A, A, u8, p->k, p->m, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
-            !encode_2d(&p->tm_B, B, u8, p->k, p->n, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
+            !encode_2d(&p->tm_B, B, u8, p->k, p->n, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
             !encode_2d(&p->tm_D, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p->n, p->m, 32, 32,
                        CU_TENSOR_MAP_SWIZZLE_64B))
             return GEMM_EPI_ERR_LAUNCH;

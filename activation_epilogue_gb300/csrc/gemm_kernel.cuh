@@ -333,15 +333,25 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase,
     const uint32_t sb = sa + C::kABytes;
     const int k0 = kb * kBK;
     if constexpr (PAIR && F8) {
-        // E4M3: a K block is 128 elements (one 128-byte swizzle row); A rows and the rows of
-        // B transposed (columns of D) are both K-major boxes {128 k, 128 rows} of 16 KB.
+        // E4M3: a K block is 128 elements (one 128-byte swizzle row); A rows are a K-major
+        // box {128 k, 128 rows} of 16 KB, the rows of B transposed (columns of D) two
+        // K-major boxes {128 k, 64 rows} of 8 KB (one each per pair of a cluster sharing B)
         static_assert(BN == 256, "the FP8 pair kernel runs 256-wide tiles");
-        const uint32_t rank = cluster_ctarank();
+        const uint32_t cr = cluster_ctarank();
+        const uint32_t rank = cr & 1u;
         if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::kStageBytes);
-        const uint32_t fb0 = map_shared_rank(fb, 0);
+        const uint32_t fb0 = map_shared_rank(fb, cr & ~1u);
         const int k8 = kb * 128;
+        const int brow = tn * BN + static_cast<int>(rank) * (BN / 2);
         tma_load_2d_pair(sa, &p.tm_A, fb0, k8, tm * 2 * kBM + static_cast<int>(rank) * kBM);
-        tma_load_2d_pair(sb, &p.tm_B, fb0, k8, tn * BN + static_cast<int>(rank) * (BN / 2));
+        if (p.pair_mc) {
+            const uint32_t pp = cr >> 1;
+            tma_load_2d_pair_mc(sb + pp * 8192, &p.tm_B, fb0, k8, brow + static_cast<int>(pp) * 64,
+                                static_cast<uint16_t>((1u << rank) | (1u << (2u + rank))));
+            return;
+        }
+        tma_load_2d_pair(sb, &p.tm_B, fb0, k8, brow);
+        tma_load_2d_pair(sb + 8192, &p.tm_B, fb0, k8, brow + 64);
         return;
     }
     if constexpr (PAIR) {

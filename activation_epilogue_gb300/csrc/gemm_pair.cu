@@ -173,7 +173,7 @@ cudaError_t fp8_launch_one(const GemmParams& p, int grid, cudaStream_t stream, b
     cudaLaunchAttribute attr[2];
     unsigned na = 0;
     attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.x = p.pair_mc ? 4 : 2;  // one pair, or two sharing B
     attr[na].val.clusterDim.y = 1;
     attr[na].val.clusterDim.z = 1;
     ++na;

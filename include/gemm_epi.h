@@ -134,7 +134,8 @@ typedef enum {
     GEMM_EPI_OPT_VARIANT = 0,       /* 1 = row-tile kernel, 2 = swapped small-m kernel,
                                        3 = row-tile kernel run by CTA pairs (256-row tiles),
                                        4 = CTA pairs in clusters of two pairs that share
-                                       each B panel (TMA multicast; not for E4M3) */
+                                       each B panel (TMA multicast); E4M3 plans take 0, 3
+                                       or 4 */
     GEMM_EPI_OPT_TILE_N = 1,        /* N tile: 64, 128 or 256 for the row-tile kernel;
                                        224 or 256 for the CTA-pair kernel; 16, 32, 64, 128
                                        or 256 rows of D for the swapped kernel (a width

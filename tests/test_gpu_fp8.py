@@ -76,6 +76,33 @@ def test_fp8_parity(epilog, shape):
     assert "dtype=e4m3" in desc and "variant=row-pair" in desc
 
 
+@pytest.mark.parametrize("epilog", EPILOGS)
+@pytest.mark.parametrize("shape", [(1000, 520, 208), (600, 264, 1040), (300, 776, 400)])
+def test_fp8_two_pair_clusters(epilog, shape):
+    # clusters of two pairs sharing B (64-row boxes of B transposed, multicast); 600 and 300
+    # rows leave the last cluster's second pair without rows of A
+    m, n, k = shape
+    layout = "M1" if (len(epilog) + m) % 3 == 0 else "1N"
+    p = workloads.random_fp8_problem(m, n, k, bias_layout=layout, seed=m + n + k + 7 * len(epilog),
+                                     residual=True)
+    _, _, desc = _check(p, m, n, k, epilog, layout, options={"VARIANT": 4})
+    assert "dtype=e4m3" in desc and "variant=row-pair-x2" in desc
+
+
+def test_fp8_two_pair_clusters_walk():
+    m, n, k = 2304, 1000, 512          # 9 row tiles, 4 column tiles, few clusters walking
+    p = workloads.random_fp8_problem(m, n, k, bias_layout="1N", seed=2304, residual=True)
+    _check(p, m, n, k, "RELU_AUX_BIAS", "1N", options={"VARIANT": 4, "GRID": 8})
+
+
+@pytest.mark.parametrize("m,n", [(65536, 16384), (4096, 4096), (1024, 1024)])
+def test_fp8_runs_single_pairs_unless_asked(m, n):
+    with gemm_epi.Plan(m, n, 8192, "e4m3", "RELU_BIAS", "1N") as plan:
+        assert "variant=row-pair " in plan.describe()
+        plan.set_option("VARIANT", 4)
+        assert "variant=row-pair-x2 " in plan.describe()
+
+
 @pytest.mark.parametrize("epilog", ["RELU_AUX_BIAS", "BIAS_RESIDUAL", "GELU_BIAS"])
 def test_fp8_unfused(epilog):
     m, n, k = 300, 264, 208

@@ -586,8 +586,10 @@ def test_pair_x2_automatic_choice(m, n, x2):
 def test_pair_x2_option_rules():
     with gemm_epi.Plan(1024, 1024, 1024, "e4m3", "RELU_BIAS", "1N") as plan:
         with pytest.raises(gemm_epi.GemmEpiError) as e:
-            plan.set_option("VARIANT", 4)   # E4M3 plans run single pairs only
+            plan.set_option("VARIANT", 1)   # E4M3 plans run the CTA-pair kernel only
         assert e.value.status == 1
+        plan.set_option("VARIANT", 4)
+        assert "variant=row-pair-x2" in plan.describe()
     with gemm_epi.Plan(1024, 1024, 1024, "bf16", "RELU_BIAS", "1N") as plan:
         plan.set_option("VARIANT", 4)
         d = plan.describe()
