@@ -397,7 +397,8 @@ gemm_epi_status ensure_maps(gemm_epi_plan_s* p, const void* A, const void* B, vo
         // A [m][k] and B transposed [n][k], bytes, K-major boxes {128 k, 128 rows}; D bf16
         const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
         if (!encode_2d(&p->tm_A, A, u8, p->k, p->m, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
-            !encode_2d(&p->tm_B, B, u8, p->k, p->n, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
+            !encode_2d(&p->tm_B, B, u8, p->k, p->n, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
+            !encode_2d(&p->tm_B64, B, u8, p->k, p->n, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
             !encode_2d(&p->tm_D, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p->n, p->m, 32, 32,
                        CU_TENSOR_MAP_SWIZZLE_64B))
             return GEMM_EPI_ERR_LAUNCH;
@@ -464,6 +465,7 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, in
     memset(&prm, 0, sizeof(prm));
     prm.tm_A = p->tm_A;
     prm.tm_B = p->tm_B;
+    if (p->dtype == GEMM_EPI_E4M3) prm.tm_B2 = p->tm_B64;  // (tm_B2 is otherwise the FFN's)
     prm.tm_D = p->tm_D;
     prm.bias = ops.bias;
     prm.residual = ops.residual;

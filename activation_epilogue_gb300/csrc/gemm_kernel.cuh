@@ -333,9 +333,10 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase,
     const uint32_t sb = sa + C::kABytes;
     const int k0 = kb * kBK;
     if constexpr (PAIR && F8) {
-        // E4M3: a K block is 128 elements (one 128-byte swizzle row); A rows are a K-major
-        // box {128 k, 128 rows} of 16 KB, the rows of B transposed (columns of D) two
-        // K-major boxes {128 k, 64 rows} of 8 KB (one each per pair of a cluster sharing B)
+        // E4M3: a K block is 128 elements (one 128-byte swizzle row); A rows and the rows of
+        // B transposed (columns of D) are K-major boxes {128 k, 128 rows} of 16 KB; in a
+        // cluster of two pairs sharing B each CTA loads one {128 k, 64 rows} box of its
+        // half (map tm_B2) and multicasts it
         static_assert(BN == 256, "the FP8 pair kernel runs 256-wide tiles");
         const uint32_t cr = cluster_ctarank();
         const uint32_t rank = cr & 1u;
@@ -346,12 +347,11 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase,
         tma_load_2d_pair(sa, &p.tm_A, fb0, k8, tm * 2 * kBM + static_cast<int>(rank) * kBM);
         if (p.pair_mc) {
             const uint32_t pp = cr >> 1;
-            tma_load_2d_pair_mc(sb + pp * 8192, &p.tm_B, fb0, k8, brow + static_cast<int>(pp) * 64,
+            tma_load_2d_pair_mc(sb + pp * 8192, &p.tm_B2, fb0, k8, brow + static_cast<int>(pp) * 64,
                                 static_cast<uint16_t>((1u << rank) | (1u << (2u + rank))));
             return;
         }
         tma_load_2d_pair(sb, &p.tm_B, fb0, k8, brow);
-        tma_load_2d_pair(sb + 8192, &p.tm_B, fb0, k8, brow + 64);
         return;
     }
     if constexpr (PAIR) {

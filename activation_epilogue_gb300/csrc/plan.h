@@ -51,6 +51,7 @@ struct gemm_epi_plan_s {
     const void* key_D;
     bool maps_valid;
     CUtensorMap tm_A, tm_B, tm_D;
+    CUtensorMap tm_B64;  // E4M3: B transposed in 64-row boxes (clusters of two pairs)
     char desc[320];
     gemm_epi_impl::HostPipe* host;  // gemm_epi_execute_host's streams, buffers and chunk plans
 };
