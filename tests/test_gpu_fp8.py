@@ -166,3 +166,19 @@ def test_fp8_rules():
         plan.execute(A, A, b, D, scales=(s, s))
         assert plan.sync_status() == 0
         assert torch.equal(D.cpu(), torch.zeros(64, 64, dtype=torch.bfloat16))
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_fp8_random_cases(i):
+    # seeded random shapes (k a multiple of 16), epilogs, layouts, single pairs or clusters
+    import random
+    r = random.Random(7000 + i)
+    m, n, k = r.randint(1, 900), 8 * r.randint(1, 100), 16 * r.randint(1, 40)
+    epilog = r.choice(EPILOGS)
+    layout = r.choice(["M1", "1N"])
+    opts = {"VARIANT": r.choice([3, 4])}
+    if r.random() < 0.3:
+        opts["GRID"] = r.choice([4, 8])
+    p = workloads.random_fp8_problem(m, n, k, bias_layout=layout, seed=r.randint(0, 10 ** 6),
+                                     residual=True)
+    _check(p, m, n, k, epilog, layout, options=opts)

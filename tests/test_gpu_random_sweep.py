@@ -26,7 +26,7 @@ def _built():
 
 def _case(i):
     r = random.Random(9000 + i)
-    variant = r.choice([0, 0, 1, 2, 3])
+    variant = r.choice([0, 0, 1, 2, 3, 4])
     m = r.choice([1, 7, 64, 129, 200, 256]) if variant == 2 else r.randint(1, 700)
     n = 8 * r.randint(1, 90)
     k = 8 * r.randint(1, 80)
@@ -35,8 +35,10 @@ def _case(i):
         opts["VARIANT"] = variant
     if variant == 1:
         opts["TILE_N"] = r.choice([64, 128, 256])
-    if variant == 3:
+    if variant in (3, 4):
         opts["TILE_N"] = r.choice([224, 256])
+        if r.random() < 0.3:
+            opts["GRID"] = r.choice([4, 8, 12])
     if variant == 2 and r.random() < 0.3:
         opts["TILE_N"] = r.choice([16, 32, 64, 128, 256])
     if variant in (1, 2) and r.random() < 0.3:
@@ -48,7 +50,7 @@ def _case(i):
                 seed=r.randint(0, 10 ** 6))
 
 
-@pytest.mark.parametrize("i", range(48))
+@pytest.mark.parametrize("i", range(64))
 def test_random_case(i):
     c = _case(i)
     p = workloads.random_problem(c["m"], c["n"], c["k"], dtype=c["dtype"], bias_layout=c["layout"],
