@@ -628,13 +628,14 @@ def test_pair_integer_bit_exact():
     check(p, m, n, k, "bf16", "RELU_AUX_BIAS", "1N", options={"VARIANT": 3}, exact=True)
 
 
-def test_pair_timeout_path():
+@pytest.mark.parametrize("variant", [3, 4])
+def test_pair_timeout_path(variant):
     m, n, k = 512, 256, 128
     p = _inputs(m, n, k, "bf16", "1N", seed=73)
     dev = torch.device("cuda")
     A, B, bias = p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev)
     D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-    with gemm_epi.Plan(m, n, k, "bf16", "BIAS", "1N", variant=3) as plan:
+    with gemm_epi.Plan(m, n, k, "bf16", "BIAS", "1N", variant=variant) as plan:
         plan.set_option("WAIT_LIMIT_US", 20000)
         plan.set_option("DEBUG_STALL", 1)
         plan.execute(A, B, bias, D)
