@@ -462,6 +462,17 @@ def test_small_m_tile_width_choice(m):
         assert f"tile=128x{want}" in plan.describe(), plan.describe()
 
 
+def test_row_tiles_over_long_k_split_in_a_cluster():
+    # 64 row tiles of 128 x 64 on 152 SMs over 32 K blocks: two K slices through a cluster
+    with gemm_epi.Plan(1024, 512, 2048, "f16", "BIAS", "M1") as plan:
+        d = plan.describe()
+    assert "variant=row-tile" in d and "split_k=2(cluster)" in d, d
+    with gemm_epi.Plan(1024, 512, 512, "f16", "BIAS", "M1") as plan:   # 8 K blocks: no split
+        assert "split_k=1 " in plan.describe()
+    p = _inputs(1024, 512, 2048, "f16", "M1", seed=1001)
+    check(p, 1024, 512, 2048, "f16", "BIAS", "M1")
+
+
 def test_small_m_plans_swapped_without_split():
     # split-K is measured slower than the unsplit swapped kernel on these shapes
     with gemm_epi.Plan(16, 3072, 768, "bf16", "GELU_BIAS", "1N") as plan:
