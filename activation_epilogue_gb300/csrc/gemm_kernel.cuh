@@ -5,17 +5,20 @@
 // the activation applied right after the core GEMM, inside the same thread block, and the
 // intermediate matrix is never written back to device memory.
 //
-// One persistent CTA per SM, six warps with fixed roles:
+// One persistent CTA per SM (or per SM of a CTA pair, or of a cluster of two pairs), with
+// warps in fixed roles:
 //   warp 0      TMA producer: one thread streams 64-deep K blocks of both operands into a
 //               ring of shared-memory stages (128-byte swizzle), arming a "full" mbarrier
 //               with the byte count of each stage.
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma (fp32 accumulate)
 //               into one of two TMEM accumulators and commits each consumed stage back to
 //               its "empty" mbarrier, and each finished tile to a "tmem full" mbarrier.
-//   warps 2-9   epilogue: two warps per 32-lane quarter of the accumulator, taking
-//               alternate 32-column chunks (two warps per scheduler hide the latency of the
-//               activation arithmetic); a warp reads a chunk from TMEM, adds the bias (staged per warp in shared
-//               memory when it varies along the columns), applies the activation, builds
+//   warps 2..   epilogue (EW warps: 8, or 16 for GELU/TANH pair tiles on short K): EW / 4
+//               warps per 32-lane quarter of the accumulator, taking every (EW / 4)-th
+//               32-column chunk (several warps per scheduler hide the latency of the
+//               activation arithmetic); a warp reads a chunk from TMEM, adds the bias
+//               (staged per warp in shared memory, or shuffled between lanes with more
+//               warps, when it varies along the columns), applies the activation, builds
 //               the ReLU mask words, rounds to 16 bits and writes D through a swizzled
 //               shared-memory box and a TMA store.  While it drains one accumulator the
 //               MMA warp fills the other, so the epilogue overlaps the next tile's GEMM.
