@@ -657,3 +657,40 @@ def test_pair_timeout_path(variant):
     from parity_helpers import oracle_ref
     want, _ = oracle_ref(p, "bf16", "BIAS", "1N")
     assert rel_err(D, want) <= TOL["bf16"]
+
+
+def test_plans_run_concurrently_on_separate_streams():
+    # each plan owns its status word, workspace and tensor maps: different plans may run at
+    # the same time on different streams (a cluster-of-pairs plan, a small-m plan with a
+    # device-memory split and a row-tile plan split through a cluster)
+    from parity_helpers import oracle_ref
+    dev = torch.device("cuda")
+    cases = [(4096, 4096, 256, "RELU_AUX_BIAS", {}),
+             (24, 776, 1544, "GELU_BIAS", {"SPLIT_K": 4}),
+             (1024, 512, 2048, "BIAS", {})]
+    plans, outs, ins = [], [], []
+    streams = [torch.cuda.Stream() for _ in cases]
+    try:
+        for i, (m, n, k, epi, opts) in enumerate(cases):
+            p = _inputs(m, n, k, "bf16", "1N", seed=300 + i)
+            A, B, bias = p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev)
+            D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+            aux = torch.empty((m, (n + 31) // 32), dtype=torch.int32, device=dev) \
+                if epi == "RELU_AUX_BIAS" else None
+            plan = gemm_epi.Plan(m, n, k, "bf16", epi, "1N", **opts)
+            plans.append(plan)
+            ins.append((p, epi))
+            outs.append((A, B, bias, D, aux))
+        torch.cuda.synchronize()
+        for rep in range(3):
+            for plan, s, (A, B, bias, D, aux) in zip(plans, streams, outs):
+                with torch.cuda.stream(s):
+                    plan.execute(A, B, bias, D, aux=aux)
+        torch.cuda.synchronize()
+        for plan, (p, epi), (A, B, bias, D, aux) in zip(plans, ins, outs):
+            assert plan.sync_status() == 0
+            want, _ = oracle_ref(p, "bf16", epi, "1N")
+            assert rel_err(D.cpu(), want) <= TOL["bf16"], plan.describe()
+    finally:
+        for plan in plans:
+            plan.free()
