@@ -143,6 +143,10 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& 
     const int r = tile - g * per_group;
     tm = first + r % rows_in_group;
     tn = r / rows_in_group;
+    // Odd groups walk the column tiles backwards, so a group starts on the B panels the
+    // previous one read last (still in L2).  Measured on GB300 at 65536 x 16384 x 8192
+    // RELU_BIAS: DRAM reads 26.5-27.4 -> 21.3-24.3 GB per launch, 1755 -> 1762 TFLOP/s.
+    if (g & 1) tn = p.tiles_n - 1 - tn;
 }
 
 // The tiles and K blocks one CTA works on.
@@ -243,6 +247,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int tile, con
         const int r = tile - g * per_group;
         t.tm = 2 * (first + r % rows_in_group) + w.pair_index;
         t.tn = r / rows_in_group;
+        if (g & 1) t.tn = p.tiles_n - 1 - t.tn;  // (snake order, as in tile_coords)
         t.prob = 0;
         t.kb_end = w.kb_end;
     } else if (!FFN || tile < tiles1) {
