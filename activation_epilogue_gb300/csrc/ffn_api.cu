@@ -33,7 +33,7 @@ struct gemm_epi_ffn_plan_s {
     const void* key_Y;
     bool maps_valid;
     CUtensorMap tm_X, tm_W1, tm_Hs, tm_Hl, tm_W2, tm_Y;
-    char desc[400];
+    char desc[720];  // room for both GEMM plans' descriptions (320 bytes each) and the text
 };
 
 namespace {
