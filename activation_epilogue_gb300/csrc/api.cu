@@ -164,6 +164,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
     p->split = 1;
     p->split_global = 0;
     p->pair_mc = 0;
+    p->swap_m64 = 0;
     p->kb_per_split = 0;
     if (p->m == 0 || p->n == 0) {
         p->variant = kEmpty;
@@ -311,6 +312,22 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             p->bn = bn;
             p->tiles_m = static_cast<int>((p->n + 127) / 128);
             p->tiles_n = static_cast<int>((p->m + bn - 1) / bn);
+            // 64 columns of D per tile (64-row MMAs), on request only: twice the CTAs copy B,
+            // but the K loop is bound by the copies' round trips, not by the SMs' copy rate.
+            // Measured on GB300 (CUDA graph, L2 flushed / hot, two runs): 16x3072x768
+            // GELU_BIAS 7.2-7.5 / 6.9 us against 6.6-7.5 / 7.0 us with 128 columns; at m = 64
+            // and 256 (152 CTAs) 10.8 and 12.3 us against 7.5-7.8 and 8.3-8.5 us.
+            const bool m64_epilog = p->epilog == GEMM_EPI_BIAS || p->epilog == GEMM_EPI_RELU_BIAS ||
+                                    p->epilog == GEMM_EPI_GELU_BIAS || p->epilog == GEMM_EPI_NONE ||
+                                    p->epilog == GEMM_EPI_TANH_BIAS ||
+                                    p->epilog == GEMM_EPI_BIAS_RESIDUAL ||
+                                    p->epilog == GEMM_EPI_GELU_AUX_BIAS;
+            const bool m64_split = p->opt_split_k > 1;
+            if (p->opt_tile_m == 64) {
+                if (!m64_epilog || m64_split) return GEMM_EPI_ERR_INVALID_ARG;
+                p->swap_m64 = 1;
+            }
+            if (p->swap_m64) p->tiles_m = static_cast<int>((p->n + 63) / 64);
             p->stages = swapped_stages(bn);
             p->smem = swapped_smem_bytes(bn);
         }
@@ -363,7 +380,8 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
              static_cast<long long>(p->k),
              p->dtype == GEMM_EPI_E4M3 ? "e4m3" : p->dtype == GEMM_EPI_BF16 ? "bf16" : "f16",
              ename[p->epilog], p->bias_layout == GEMM_EPI_BIAS_M1 ? "(m,1)" : "(1,n)",
-             p->pair_mc ? "row-pair-x2" : vname[p->variant], p->variant == kRowPair ? 256 : 128, p->bn,
+             p->pair_mc ? "row-pair-x2" : vname[p->variant],
+             p->variant == kRowPair ? 256 : p->swap_m64 ? 64 : 128, p->bn,
              p->dtype == GEMM_EPI_E4M3 ? 128 : 64, p->stages, p->smem, p->tiles_m, p->tiles_n,
              p->k_blocks,
              p->split, p->split > 1 ? (p->split_global ? "(device memory)" : "(cluster)") : "",
@@ -430,9 +448,11 @@ gemm_epi_status ensure_maps(gemm_epi_plan_s* p, const void* A, const void* B, vo
         if (!encode_2d(&p->tm_D, D, dt, p->n, p->m, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
             return GEMM_EPI_ERR_LAUNCH;
     } else {
-        // swapped kernel: boxes of 32 columns x (up to) 32 rows of D, transposed on chip
+        // swapped kernel: boxes of 32 columns (16 with 64-column tiles) x (up to) 32 rows
+        // of D, transposed on chip
         const uint32_t rows = p->bn < 32 ? static_cast<uint32_t>(p->bn) : 32u;
-        if (!encode_2d(&p->tm_D, D, dt, p->n, p->m, 32, rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        const uint32_t cols = p->swap_m64 ? 16u : 32u;
+        if (!encode_2d(&p->tm_D, D, dt, p->n, p->m, cols, rows, CU_TENSOR_MAP_SWIZZLE_NONE))
             return GEMM_EPI_ERR_LAUNCH;
     }
     p->key_A = A;
@@ -508,6 +528,7 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, in
     prm.split_ws = p->d_split_ws;
     prm.split_count = p->d_split_count;
     prm.pair_mc = p->pair_mc;
+    prm.swap_m64 = p->swap_m64;
     prm.tiles_m2 = (p->tiles_m + 1) / 2;
     prm.prefetch = p->prefetch;
     cudaError_t e;
@@ -718,6 +739,10 @@ gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt,
     case GEMM_EPI_OPT_SPLIT_MODE:
         if (value < 0 || value > 2) return GEMM_EPI_ERR_INVALID_ARG;
         p->opt_split_mode = static_cast<int>(value);
+        break;
+    case GEMM_EPI_OPT_TILE_M:
+        if (value != 0 && value != 64 && value != 128) return GEMM_EPI_ERR_INVALID_ARG;
+        p->opt_tile_m = static_cast<int>(value);
         break;
     case GEMM_EPI_OPT_GRID:
         if (value < 0 || value > (1 << 20)) return GEMM_EPI_ERR_INVALID_ARG;

@@ -389,13 +389,19 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase,
                              tn * BN + static_cast<int>(rank) * (BN / 2) + q * 64, k0);
         return;
     }
-    mbar_arrive_expect_tx(fb, C::kStageBytes);
     if (!SWAP) {
+        mbar_arrive_expect_tx(fb, C::kStageBytes);
         tma_load_2d(sa, &p.tm_A, fb, k0, tm * kBM);
 #pragma unroll
         for (int q = 0; q < BN / 64; ++q)
             tma_load_2d(sb + q * 8192, &p.tm_B, fb, tn * BN + q * 64, k0);
+    } else if (p.swap_m64) {
+        // 64 MMA rows: one 64-column box of B (the second half of the A area stays unused)
+        mbar_arrive_expect_tx(fb, C::kStageBytes - 8192);
+        tma_load_2d(sa, &p.tm_B, fb, tm * 64, k0);
+        tma_load_2d(sb, &p.tm_A, fb, k0, tn * BN);
     } else {
+        mbar_arrive_expect_tx(fb, C::kStageBytes);
         tma_load_2d(sa, &p.tm_B, fb, tm * kBM, k0);
         tma_load_2d(sa + 8192, &p.tm_B, fb, tm * kBM + 64, k0);
         tma_load_2d(sb, &p.tm_A, fb, k0, tn * BN);
@@ -411,6 +417,9 @@ __device__ __forceinline__ void prefetch_stage(const GemmParams& p, int tm, int 
         tma_prefetch_2d(&p.tm_A, k0, tm * kBM);
 #pragma unroll
         for (int q = 0; q < BN / 64; ++q) tma_prefetch_2d(&p.tm_B, tn * BN + q * 64, k0);
+    } else if (p.swap_m64) {
+        tma_prefetch_2d(&p.tm_B, tm * 64, k0);
+        tma_prefetch_2d(&p.tm_A, k0, tn * BN);
     } else {
         tma_prefetch_2d(&p.tm_B, tm * kBM, k0);
         tma_prefetch_2d(&p.tm_B, tm * kBM + 64, k0);
@@ -505,7 +514,8 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
     // E4M3 (F8): both operands K-major, 32 K elements (32 bytes) per MMA.
     const uint32_t idesc = F8 ? make_idesc_e4m3(2 * kBM, BN)
                               : make_idesc_f16(static_cast<uint32_t>(p.bf16), SWAP ? 1u : 0u,
-                                               SWAP ? 0u : 1u, PAIR ? 2 * kBM : kBM, BN);
+                                               SWAP ? 0u : 1u,
+                                               PAIR ? 2 * kBM : (SWAP && p.swap_m64 ? 64 : kBM), BN);
     const WorkRange w = work_range<PAIR>(p);
     if (PAIR && w.pair_rank != 0) return;
     // commit targets: this (even) CTA, its pair, every CTA whose stages these MMAs read from
@@ -935,9 +945,12 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         const int lane_limit = SWAP ? ncols : p.m;  // extent of the accumulator-lane coordinate
         const int col_base = tn * BN;                          // first accumulator column
         // this warp's first lane coordinate (a pair's odd CTA holds rows 128..255 of the tile)
-        const int lane_base = PAIR ? tm * 2 * kBM + w.pair_rank * kBM + quarter * 32
-                                   : tm * kBM + quarter * 32;
-        const int lane_idx = lane_base + lane;
+        // (64-row swapped tiles: 16 columns of D per warp, in lanes 0-15)
+        const bool m64 = SWAP && p.swap_m64;
+        const int lane_base = PAIR  ? tm * 2 * kBM + w.pair_rank * kBM + quarter * 32
+                              : m64 ? tm * 64 + quarter * 16
+                                    : tm * kBM + quarter * 32;
+        const int lane_idx = m64 && lane >= 16 ? lane_limit : lane_base + lane;
         if (*abort_flag) break;
         if (EW == 8 && col_bias) {
             __syncwarp();  // every lane is done reading the previous tile's values
@@ -1289,8 +1302,16 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                     if (lane == 0) bulk_wait_group_read<0>();  // this warp's last box is read
                     __syncwarp();
                     uint16_t* tb = reinterpret_cast<uint16_t*>(epi_buf);
+                    if (m64) {
+                        // a 16-column box (rows of 32 bytes) from lanes 0-15
+                        if (lane < 16) {
 #pragma unroll
-                    for (int j = 0; j < CH; ++j) tb[j * 32 + lane] = to16(v[j], p.bf16);
+                            for (int j = 0; j < CH; ++j) tb[j * 16 + lane] = to16(v[j], p.bf16);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < CH; ++j) tb[j * 32 + lane] = to16(v[j], p.bf16);
+                    }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {

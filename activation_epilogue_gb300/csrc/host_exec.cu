@@ -81,6 +81,7 @@ gemm_epi_status chunk_plan(const gemm_epi_plan_s* p, int64_t rows, gemm_epi_plan
     c->opt_bn = p->opt_bn;
     c->opt_split_k = p->opt_split_k;
     c->opt_split_mode = p->opt_split_mode;
+    c->opt_tile_m = p->opt_tile_m;
     c->opt_grid = p->opt_grid;
     c->opt_group_m = p->opt_group_m;
     c->prefetch = p->prefetch;

@@ -98,6 +98,12 @@ struct GemmParams {
     // pairs' MMAs have read it.
     int pair_mc;
     int tiles_m2;
+    // Swapped kernel with 64 MMA rows per tile (swap_m64 == 1): each tile is 64 columns of
+    // D (one 64-column box of B per stage), the MMA runs M = 64, and its rows sit in TMEM
+    // lanes 0-15 of each lane quarter (row r in lane 32 (r / 16) + r % 16), so every
+    // epilogue warp owns 16 columns of D.  Only for epilogs whose outputs are per element
+    // (no mask words, no backward) and without a K split.
+    int swap_m64;
     // The producer also prefetches into L2 the operand boxes of the K block this many
     // blocks ahead of the one it loads (0 = off), so that a first touch of a panel in
     // device memory overlaps the loads of the blocks before it.

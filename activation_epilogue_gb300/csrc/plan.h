@@ -33,8 +33,9 @@ struct gemm_epi_plan_s {
     int split, kb_per_split;  // split-K slices (split == 1: persistent kernel)
     int split_global;         // 1: the slices meet in device memory, 0: in a cluster
     int pair_mc;              // CTA-pair kernel in clusters of two pairs sharing B
+    int swap_m64;             // swapped kernel with 64 MMA rows (columns of D) per tile
     // options (0 = automatic)
-    int opt_variant, opt_bn, opt_split_k, opt_grid, opt_group_m, opt_split_mode;
+    int opt_variant, opt_bn, opt_split_k, opt_grid, opt_group_m, opt_split_mode, opt_tile_m;
     // split-K through device memory: fp32 partial tiles [tile][slice][128 x bn] and the
     // per-tile arrival counts (zero between launches), allocated when the plan is configured
     float* d_split_ws;

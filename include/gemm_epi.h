@@ -155,11 +155,16 @@ typedef enum {
                                        programmatic dependent of the previous work on the
                                        stream (its set-up overlaps that work; every global
                                        access still waits for it); 0: plain launch */
-    GEMM_EPI_OPT_SPLIT_MODE = 9     /* split-K partial sums: 0 (default) or 2 = through a
+    GEMM_EPI_OPT_SPLIT_MODE = 9,    /* split-K partial sums: 0 (default) or 2 = through a
                                        device-memory workspace the plan owns (slices 1..8;
                                        the last CTA of a tile adds them in slice order);
                                        1 = within a thread-block cluster over distributed
                                        shared memory (slices 1..4) */
+    GEMM_EPI_OPT_TILE_M = 10        /* swapped kernel: columns of D per tile (MMA rows), 128
+                                       (the automatic choice) or 64 (on request; only the
+                                       epilogs BIAS, RELU_BIAS, GELU_BIAS, NONE, TANH_BIAS,
+                                       BIAS_RESIDUAL and GELU_AUX_BIAS, without a K split,
+                                       else ERR_INVALID_ARG) */
 } gemm_epi_option;
 
 /*

@@ -441,7 +441,7 @@ def test_swapped_narrow_tiles(m, bn, epilog):
     layout = "M1" if (m + len(epilog)) % 2 else "1N"
     p = _inputs(m, n, k, "bf16", layout, seed=900 + m + bn)
     _, _, _, _, desc = check(p, m, n, k, "bf16", epilog, layout,
-                             options={"VARIANT": 2, "TILE_N": bn})
+                             options={"VARIANT": 2, "TILE_N": bn, "TILE_M": 128})
     assert f"tile=128x{bn}" in desc
 
 
@@ -460,6 +460,60 @@ def test_small_m_tile_width_choice(m):
             break
     with gemm_epi.Plan(m, n, 768, "bf16", "GELU_BIAS", "1N") as plan:
         assert f"tile=128x{want}" in plan.describe(), plan.describe()
+
+
+# ---- swapped kernel with 64 columns of D per tile (64-row MMAs) -----------------------------
+
+M64_EPILOGS = ["BIAS", "RELU_BIAS", "GELU_BIAS", "NONE", "TANH_BIAS", "BIAS_RESIDUAL",
+               "GELU_AUX_BIAS"]
+
+
+@pytest.mark.parametrize("m,n,k,bn", [(1, 264, 136, 16), (16, 200, 72, 16), (40, 392, 200, 16),
+                                      (100, 136, 328, 32), (256, 520, 200, 64),
+                                      (20, 3072, 768, 16)])
+@pytest.mark.parametrize("epilog", M64_EPILOGS)
+def test_swapped_m64_parity(m, n, k, bn, epilog):
+    # ragged n (the last tile's later lane quarters hold no columns), both bias layouts,
+    # both dtypes
+    layout = "M1" if (m + len(epilog)) % 2 else "1N"
+    dtype = "f16" if (m + k) % 3 == 0 else "bf16"
+    p = _inputs(m, n, k, dtype, layout, seed=1300 + m + n)
+    _, _, _, _, desc = check(p, m, n, k, dtype, epilog, layout,
+                             options={"VARIANT": 2, "TILE_N": bn, "TILE_M": 64})
+    assert f"tile=64x{bn}" in desc, desc
+
+
+@pytest.mark.parametrize("epilog", ["BIAS", "RELU_BIAS", "NONE", "BIAS_RESIDUAL"])
+def test_swapped_m64_integer_bit_exact(epilog):
+    m, n, k = 24, 328, 136
+    p = _inputs(m, n, k, "bf16", "1N", seed=1400, kind="int")
+    check(p, m, n, k, "bf16", epilog, "1N", options={"VARIANT": 2, "TILE_M": 64}, exact=True)
+
+
+def test_swapped_m64_only_on_request():
+    with gemm_epi.Plan(16, 3072, 768, "bf16", "GELU_BIAS", "1N") as plan:
+        assert "variant=swapped tile=128x16" in plan.describe(), plan.describe()
+        plan.set_option("TILE_M", 64)
+        assert "variant=swapped tile=64x16" in plan.describe(), plan.describe()
+        plan.set_option("TILE_M", 0)
+        assert "variant=swapped tile=128x16" in plan.describe(), plan.describe()
+
+
+def test_swapped_m64_option_rules():
+    with gemm_epi.Plan(16, 264, 136, "bf16", "RELU_AUX_BIAS", "1N", variant=2) as plan:
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.set_option("TILE_M", 64)
+        assert e.value.status == 1
+        assert "tile=128x" in plan.describe()          # previous configuration kept
+    with gemm_epi.Plan(16, 264, 136, "bf16", "GELU_BIAS", "1N", variant=2) as plan:
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.set_option("TILE_M", 32)
+        assert e.value.status == 1
+        plan.set_option("SPLIT_K", 2)                  # a K split keeps 128-column tiles
+        assert "tile=128x" in plan.describe() and "split_k=2" in plan.describe()
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.set_option("TILE_M", 64)
+        assert e.value.status == 1
 
 
 def test_row_tiles_over_long_k_split_in_a_cluster():
