@@ -34,6 +34,30 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name), name
 
 
+def _header_enums():
+    text = open(os.path.join(ROOT, "include", "gemm_epi.h")).read()
+    return {name: int(v) for name, v in re.findall(r"\b(GEMM_EPI_\w+)\s*=\s*(\d+)", text)}
+
+
+def test_binding_tables_match_the_header():
+    """Every enum value the binding passes through the C ABI is the header's, and every
+    option the header declares has a binding name."""
+    h = _header_enums()
+    assert {f"GEMM_EPI_{k.upper()}": v for k, v in gemm_epi.DTYPE.items()} == \
+        {k: v for k, v in h.items() if k in ("GEMM_EPI_F16", "GEMM_EPI_BF16", "GEMM_EPI_E4M3")}
+    for name, v in gemm_epi.EPILOG.items():
+        assert h[f"GEMM_EPI_{name}"] == v, name
+    for name, v in gemm_epi.BIAS_LAYOUT.items():
+        assert h[f"GEMM_EPI_BIAS_{name}"] == v, name
+    for v, name in gemm_epi.STATUS.items():
+        assert h[f"GEMM_EPI_{name}"] == v, name
+    opts = {k[len("GEMM_EPI_OPT_"):]: v for k, v in h.items() if k.startswith("GEMM_EPI_OPT_")}
+    assert opts == gemm_epi.OPTION
+    ffn = {k[len("GEMM_EPI_FFN_OPT_"):]: v for k, v in h.items()
+           if k.startswith("GEMM_EPI_FFN_OPT_")}
+    assert ffn == gemm_epi.FFN_OPTION
+
+
 def test_status_strings(lib):
     for code, name in gemm_epi.STATUS.items():
         assert name in gemm_epi.status_string(code)
