@@ -1,16 +1,19 @@
 // Activation functions of the epilogues, in fp32.
 //
 // erf-form GELU, x * Phi(x), in the forward epilogues: Phi from a logistic approximation,
-//     Phi(x) ~= 1 / (1 + exp(-(c1 x + c3 x^3 + c5 x^5))),   |x| clamped to 8,
+//     Phi(x) ~= 1 / (1 + exp(-x (c1 + c3 s + c5 s^2))),   s = min(x^2, 64),
 // the form of Bowling et al., "A logistic approximation to the cumulative normal
 // distribution" (J. Industrial Engineering and Management, 2009), with an x^5 term and
 // coefficients refitted minimax on [0, 8] (fit_gelu_logistic.py beside this file):
 // |Phi error| * max(1, |x|) <= 3.1e-5, so |GELU error| <= 3.1e-5 * max(1, |x|), two orders
 // below the rounding of a bf16 result and well inside an f16 result's acceptance bound.
-// Per element: two min/max, two multiplies, two FMAs, one ex2, one add, one fast divide:
-// half the instructions of the formula-7.1.26 version below, which matters because the
-// epilogue warps, two per scheduler, are bound by instruction issue.  P is odd, so
-// Phi(-x) = 1 - Phi(x) holds exactly and every element takes the same path.
+// Beyond |x| = 8 the exponent grows linearly in x with the sign it has at 8, so Phi
+// saturates; clamping the square (one min) rather than x (two) gives the same bits for
+// |x| <= 8.  Per element: two multiplies, one min, two FMAs, one multiply, one ex2, one
+// add, one fast divide: under half the instructions of the formula-7.1.26 version below,
+// which matters because the epilogue's instruction count is its cost (it also takes issue
+// slots from the MMA warp).  The exponent is odd in x, so Phi(-x) = 1 - Phi(x) holds
+// exactly and every element takes the same path.
 //
 // GELU' in the backward epilogue uses formula 7.1.26 of Abramowitz & Stegun, Handbook of
 // Mathematical Functions (1964): for z >= 0,
@@ -36,10 +39,9 @@ __device__ __forceinline__ float gelu_erf_fast(float x)
 {
     // c1, c3, c5 of the fit times -log2(e): exp(-P(x)) = 2^(x * (k1 + k3 x^2 + k5 x^4))
     constexpr float k1 = -2.3014667034f, k3 = -0.10654459149f, k5 = 0.00098442099988f;
-    const float xc = fminf(fmaxf(x, -8.0f), 8.0f);
-    const float x2 = xc * xc;
+    const float x2 = fminf(x * x, 64.0f);
     const float p = fmaf(fmaf(x2, k5, k3), x2, k1);
-    return __fdividef(x, 1.0f + exp2_approx(xc * p));
+    return __fdividef(x, 1.0f + exp2_approx(x * p));
 }
 
 // GELU'(x) = Phi(x) + x phi(x), phi(x) = exp(-x^2/2) / sqrt(2 pi): the same tail q =
