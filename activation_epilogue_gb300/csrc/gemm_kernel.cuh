@@ -90,6 +90,7 @@ struct TileCfg {
     static_assert(kStages >= 2, "pipeline needs two stages");
     static_assert(kRedBytes <= kStages * kStageBytes, "partial tile must fit the stage ring");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kOffBias % 16 == 0, "per-warp bias staging is read with 16-byte loads");
 };
 
 // mbarrier slots in the barrier area
@@ -608,6 +609,28 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
 // epilogue
 // ------------------------------------------------------------------------------------------
 
+// Add the bias to N consecutive accumulator columns: the staged per-column values (four at
+// a time, 16-byte broadcast loads: sb is 16-byte aligned, as the staging area and every
+// chunk's offset are) or one per-lane value.
+template <int N>
+__device__ __forceinline__ void add_bias(float (&v)[N], const float* sb, bool col_bias, float lb)
+{
+    if (col_bias) {
+        const float4* s4 = reinterpret_cast<const float4*>(sb);
+#pragma unroll
+        for (int q = 0; q < N / 4; ++q) {
+            const float4 b = s4[q];
+            v[4 * q] += b.x;
+            v[4 * q + 1] += b.y;
+            v[4 * q + 2] += b.z;
+            v[4 * q + 3] += b.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] += lb;
+    }
+}
+
 // Apply the activation to one chunk in place: v[] holds acc + bias on entry.
 template <int N>
 __device__ __forceinline__ void activate(float (&v)[N], int epilog)
@@ -1074,11 +1097,10 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                         for (int j = 0; j < 16; ++j) {
                             v[j] = __uint_as_float(h == 0 ? ra[j] : rb[j]);
                             if (F8) v[j] *= fp8_scale;
-                            if constexpr (EW == 8)
-                                v[j] += col_bias ? sbias[c * CH + 16 * h + j] : lb;
-                            else
+                            if constexpr (EW != 8)
                                 v[j] += col_bias ? __shfl_sync(0xFFFFFFFFu, bcur, 16 * h + j) : lb;
                         }
+                        if constexpr (EW == 8) add_bias<16>(v, sbias + c * CH + 16 * h, col_bias, lb);
                         activate(v, epilog);
                         if (warp_live) {
 #pragma unroll
@@ -1170,8 +1192,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                 for (int j = 0; j < CH; ++j) v[j] *= fp8_scale;
             }
             if (!ln) {
-#pragma unroll
-                for (int j = 0; j < CH; ++j) v[j] += col_bias ? sbias[c * CH + j] : lb;
+                add_bias<CH>(v, sbias + c * CH, col_bias, lb);
             } else {
 #pragma unroll
                 for (int j = 0; j < CH; ++j) {
