@@ -164,7 +164,7 @@ typedef enum {
                                        (the automatic choice) or 64 (on request; only the
                                        epilogs BIAS, RELU_BIAS, GELU_BIAS, NONE, TANH_BIAS,
                                        BIAS_RESIDUAL and GELU_AUX_BIAS, without a K split,
-                                       else ERR_INVALID_ARG) */
+                                       else ERR_INVALID_ARG); the other kernels ignore it */
 } gemm_epi_option;
 
 /*
