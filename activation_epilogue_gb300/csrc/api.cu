@@ -163,7 +163,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
     p->group_m = 1;
     p->split = 1;
     p->split_global = 0;
-    p->pair_mc = 0;
+    p->dyn_order = 0;
     p->swap_m64 = 0;
     p->kb_per_split = 0;
     if (p->m == 0 || p->n == 0) {
@@ -172,8 +172,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
         p->variant = kBiasOnly;
     } else if (p->dtype == GEMM_EPI_E4M3) {
         // E4M3: the CTA-pair kernel with 256 x 256 tiles and 128-deep K blocks, any shape
-        if ((p->opt_variant != 0 && p->opt_variant != 3 && p->opt_variant != 4) ||
-            (p->opt_bn != 0 && p->opt_bn != 256))
+        if ((p->opt_variant != 0 && p->opt_variant != 3) || (p->opt_bn != 0 && p->opt_bn != 256))
             return GEMM_EPI_ERR_INVALID_ARG;
         if (fp8_pair_prepare() != cudaSuccess || rowpair_prepare(256) != cudaSuccess)
             return GEMM_EPI_ERR_LAUNCH;
@@ -195,24 +194,6 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
         int gm = p->opt_group_m ? p->opt_group_m : 8;
         if (gm > p->tiles_m) gm = p->tiles_m;
         p->group_m = gm < 1 ? 1 : gm;
-        // clusters of two pairs sharing B only when asked for: E4M3 moves half the bytes
-        // per flop, and measured on GB300 the clusters were level or slower at
-        // 65536 x 16384 x 8192 and 8192^3 (3283-3344 against 3299-3550 TFLOP/s; 3300-3603
-        // against 3585-3649), faster only at 4096^3 (3064-3076 against 2998-3010)
-        long long clusters = rowpair_max_clusters4(256);
-        if (clusters > p->sm_count / 4) clusters = p->sm_count / 4;
-        const int tiles_m2 = (p->tiles_m + 1) / 2;
-        const long long dtiles = static_cast<long long>(tiles_m2) * p->tiles_n;
-        if (p->opt_variant == 4) {
-            if (p->opt_grid > 0 && p->opt_grid / 4 < clusters) clusters = p->opt_grid / 4;
-            if (clusters < 1) return GEMM_EPI_ERR_LAUNCH;
-            if (clusters > dtiles) clusters = dtiles;
-            p->pair_mc = 1;
-            p->grid = static_cast<int>(4 * clusters);
-            int gm2 = p->opt_group_m ? (p->opt_group_m + 1) / 2 : 4;
-            if (gm2 > tiles_m2) gm2 = tiles_m2;
-            p->group_m = gm2 < 1 ? 1 : gm2;
-        }
     } else {
         int v = p->opt_variant;
         if (v == 0) {
@@ -226,25 +207,8 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             else
                 v = kRowTile;
         }
-        // (option values: 1 row-tile, 2 swapped, 3 CTA pairs, 4 CTA pairs in clusters of two
-        // pairs sharing B; the internal Variant codes differ)
-        if (p->opt_variant == 4) {
-            p->pair_mc = 1;
-            v = kRowPair;
-        } else if (p->opt_variant == 0 && v == kRowPair) {
-            // Two pairs per cluster once there are two waves of double tiles: each B panel is
-            // read once for two row tiles, in step.  Measured on GB300 (same box, runs
-            // alternating): 65536 x 16384 x 8192 RELU_BIAS DRAM reads 39.5 -> 23.9 GB per
-            // launch and 1734 -> 1775 TFLOP/s (20-step bench, mean of three each); 4096^3
-            // RELU_BIAS 1597 -> 1642 TFLOP/s.  Clusters of four leave 8 of 152 SMs idle, which
-            // a single wave cannot make up (4096 x 1024 x 4096: equal), so shallower problems
-            // keep single pairs.
-            if (rowpair_prepare(256) != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
-            long long clusters = rowpair_max_clusters4(256);
-            if (clusters > p->sm_count / 4) clusters = p->sm_count / 4;
-            const long long dtiles = ((p->m + 511) / 512) * ((p->n + 255) / 256);
-            if (clusters > 0 && dtiles >= 2 * clusters) p->pair_mc = 1;
-        }
+        // (option values: 1 row-tile, 2 swapped, 3 CTA pairs; the internal Variant codes
+        // differ)
         if (p->opt_variant == 3) v = kRowPair;  // option value 3: the CTA-pair kernel
         if (v == kSwapped && p->m > kSwappedMaxM) return GEMM_EPI_ERR_INVALID_ARG;
         // the swapped kernel has no LayerNorm epilogue
@@ -260,15 +224,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             if (pairs > p->sm_count / 2) pairs = p->sm_count / 2;
             if (p->opt_grid > 0 && p->opt_grid / 2 < pairs) pairs = p->opt_grid / 2;
             if (pairs < 1) return GEMM_EPI_ERR_LAUNCH;
-            if (p->pair_mc) {
-                // width by the waves of double tiles (two 256-row tiles) over the clusters
-                long long clusters = rowpair_max_clusters4(256);
-                if (clusters > p->sm_count / 4) clusters = p->sm_count / 4;
-                p->bn = p->opt_bn ? p->opt_bn
-                                  : pick_pair_bn((p->m + 511) / 512 * 256, p->n, clusters > 0 ? clusters : 1);
-            } else {
-                p->bn = p->opt_bn ? p->opt_bn : pick_pair_bn(p->m, p->n, pairs);
-            }
+            p->bn = p->opt_bn ? p->opt_bn : pick_pair_bn(p->m, p->n, pairs);
             p->tiles_m = static_cast<int>((p->m + 255) / 256);
             p->tiles_n = static_cast<int>((p->n + p->bn - 1) / p->bn);
             p->stages = rowpair_stages(p->bn);
@@ -281,21 +237,6 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             int gm = p->opt_group_m ? p->opt_group_m : 8;
             if (gm > p->tiles_m) gm = p->tiles_m;
             p->group_m = gm < 1 ? 1 : gm;
-            if (p->pair_mc) {
-                // clusters of two pairs on double rows of tiles (the group counts double
-                // rows); an odd last row tile leaves its second pair without rows of A
-                long long clusters = rowpair_max_clusters4(p->bn);
-                if (clusters > p->sm_count / 4) clusters = p->sm_count / 4;
-                if (p->opt_grid > 0 && p->opt_grid / 4 < clusters) clusters = p->opt_grid / 4;
-                if (clusters < 1) return GEMM_EPI_ERR_LAUNCH;
-                const int tiles_m2 = (p->tiles_m + 1) / 2;
-                const long long dtiles = static_cast<long long>(tiles_m2) * p->tiles_n;
-                if (clusters > dtiles) clusters = dtiles;
-                p->grid = static_cast<int>(4 * clusters);
-                int gm2 = p->opt_group_m ? (p->opt_group_m + 1) / 2 : 4;
-                if (gm2 > tiles_m2) gm2 = tiles_m2;
-                p->group_m = gm2 < 1 ? 1 : gm2;
-            }
         } else if (v == kRowTile) {
             if (p->opt_bn && p->opt_bn != 64 && p->opt_bn != 128 && p->opt_bn != 256)
                 return GEMM_EPI_ERR_INVALID_ARG;
@@ -368,6 +309,9 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
         if (gm > p->tiles_m) gm = p->tiles_m;
         p->group_m = gm < 1 ? 1 : gm;
     }
+    // CTA pairs take their tiles from the plan's device counter unless told otherwise (or
+    // the plan has none, as a plan on the caller's stack may not).
+    if (p->variant == kRowPair) p->dyn_order = p->opt_tile_order != 1 && p->d_sched != nullptr;
     static const char* vname[] = {"empty", "row-tile", "swapped", "bias-only", "row-pair"};
     static const char* ename[] = {"BIAS",          "RELU_BIAS",     "GELU_BIAS",
                                   "RELU_AUX_BIAS", "BIAS_RESIDUAL", "NONE",
@@ -375,17 +319,19 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
                                   "DGELU_BGRAD",   "LN_GELU_BIAS"};
     snprintf(p->desc, sizeof(p->desc),
              "m=%lld n=%lld k=%lld dtype=%s epilog=%s bias=%s variant=%s tile=%dx%d bk=%d "
-             "stages=%d smem=%d tiles=%dx%d k_blocks=%d split_k=%d%s grid=%d group_m=%d sms=%d",
+             "stages=%d smem=%d tiles=%dx%d k_blocks=%d split_k=%d%s grid=%d group_m=%d%s sms=%d",
              static_cast<long long>(p->m), static_cast<long long>(p->n),
              static_cast<long long>(p->k),
              p->dtype == GEMM_EPI_E4M3 ? "e4m3" : p->dtype == GEMM_EPI_BF16 ? "bf16" : "f16",
              ename[p->epilog], p->bias_layout == GEMM_EPI_BIAS_M1 ? "(m,1)" : "(1,n)",
-             p->pair_mc ? "row-pair-x2" : vname[p->variant],
+             vname[p->variant],
              p->variant == kRowPair ? 256 : p->swap_m64 ? 64 : 128, p->bn,
              p->dtype == GEMM_EPI_E4M3 ? 128 : 64, p->stages, p->smem, p->tiles_m, p->tiles_n,
              p->k_blocks,
              p->split, p->split > 1 ? (p->split_global ? "(device memory)" : "(cluster)") : "",
-             p->grid, p->group_m, p->sm_count);
+             p->grid, p->group_m,
+             p->variant != kRowPair ? "" : p->dyn_order ? " order=dynamic" : " order=static",
+             p->sm_count);
     const char* log = getenv("GEMM_EPI_LOG");
     if (log && log[0] == '1') fprintf(stderr, "[gemm_epi] plan: %s\n", p->desc);
     if (p->split_global) return ensure_split_ws(p);
@@ -426,7 +372,6 @@ gemm_epi_status ensure_maps(gemm_epi_plan_s* p, const void* A, const void* B, vo
         const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
         if (!encode_2d(&p->tm_A, A, u8, p->k, p->m, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
             !encode_2d(&p->tm_B, B, u8, p->k, p->n, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
-            !encode_2d(&p->tm_B64, B, u8, p->k, p->n, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
             !encode_2d(&p->tm_D, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p->n, p->m, 32, 32,
                        CU_TENSOR_MAP_SWIZZLE_64B))
             return GEMM_EPI_ERR_LAUNCH;
@@ -495,7 +440,6 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, in
     memset(&prm, 0, sizeof(prm));
     prm.tm_A = p->tm_A;
     prm.tm_B = p->tm_B;
-    if (p->dtype == GEMM_EPI_E4M3) prm.tm_B2 = p->tm_B64;  // (tm_B2 is otherwise the FFN's)
     prm.tm_D = p->tm_D;
     prm.bias = ops.bias;
     prm.residual = ops.residual;
@@ -527,9 +471,8 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, in
     prm.split_global = p->split_global;
     prm.split_ws = p->d_split_ws;
     prm.split_count = p->d_split_count;
-    prm.pair_mc = p->pair_mc;
+    prm.sched = p->dyn_order ? p->d_sched : nullptr;
     prm.swap_m64 = p->swap_m64;
-    prm.tiles_m2 = (p->tiles_m + 1) / 2;
     prm.prefetch = p->prefetch;
     cudaError_t e;
     if (p->variant == kRowPair && p->dtype == GEMM_EPI_E4M3)
@@ -697,16 +640,18 @@ gemm_epi_status gemm_epi_plan(gemm_epi_plan_t* out, int64_t m, int64_t n, int64_
     p->device = dev;
     p->sm_count = sms;
     p->wait_limit_ns = kDefaultWaitNs;
-    if (cudaMalloc(reinterpret_cast<void**>(&p->d_status), sizeof(int)) != cudaSuccess) {
+    // status word at byte 0, the CTA pairs' tile counter (two words) at byte 8
+    if (cudaMalloc(reinterpret_cast<void**>(&p->d_status), kPlanWordsBytes) != cudaSuccess) {
         cudaGetLastError();
         delete p;
         return GEMM_EPI_ERR_ALLOC;
     }
-    if (cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess) {
+    if (cudaMemset(p->d_status, 0, kPlanWordsBytes) != cudaSuccess) {
         cudaFree(p->d_status);
         delete p;
         return GEMM_EPI_ERR_ALLOC;
     }
+    p->d_sched = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(p->d_status) + 8);
     gemm_epi_status st = configure(p);
     if (st != GEMM_EPI_OK) {
         cudaFree(p->d_status);
@@ -723,7 +668,7 @@ gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt,
     gemm_epi_plan_s saved = *p;
     switch (opt) {
     case GEMM_EPI_OPT_VARIANT:
-        if (value < 0 || value > 4) return GEMM_EPI_ERR_INVALID_ARG;
+        if (value < 0 || value > 3) return GEMM_EPI_ERR_INVALID_ARG;
         p->opt_variant = static_cast<int>(value);
         break;
     case GEMM_EPI_OPT_TILE_N:
@@ -743,6 +688,10 @@ gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt,
     case GEMM_EPI_OPT_TILE_M:
         if (value != 0 && value != 64 && value != 128) return GEMM_EPI_ERR_INVALID_ARG;
         p->opt_tile_m = static_cast<int>(value);
+        break;
+    case GEMM_EPI_OPT_TILE_ORDER:
+        if (value < 0 || value > 2) return GEMM_EPI_ERR_INVALID_ARG;
+        p->opt_tile_order = static_cast<int>(value);
         break;
     case GEMM_EPI_OPT_GRID:
         if (value < 0 || value > (1 << 20)) return GEMM_EPI_ERR_INVALID_ARG;

@@ -139,6 +139,7 @@ gemm_epi_status run_ffn_one_launch(gemm_epi_ffn_plan_s* p, const void* X, const 
     prm.bias = b1;
     prm.D = p->H;
     prm.status = g1->d_status;
+    prm.sched = g1->dyn_order ? g1->d_sched : nullptr;
     prm.wait_limit_ns = g1->wait_limit_ns;
     prm.m = static_cast<int>(p->t);
     prm.n = static_cast<int>(p->f);
@@ -341,13 +342,15 @@ gemm_epi_status gemm_epi_ffn_free(gemm_epi_ffn_plan_t p)
 
 // ---- the FFN block without allocation ------------------------------------------------------
 //
-// For callers that cannot allocate device memory.  The hidden activation and the status
-// words of the two launches live in one file-scope device array; its device address is
-// looked up once per device (with that device current) and then passed to the kernels.
+// For callers that cannot allocate device memory.  The hidden activation, and the status
+// words and tile counters of the two launches, live in one file-scope device array; its
+// device address is looked up on every call (with the device current) and passed to the
+// kernels.
 
 namespace {
 
-constexpr size_t kNoAllocStatusBytes = 256;  // two status words, padded to 256 bytes
+// two status words (bytes 0 and 4) and two tile counters (bytes 8 and 16), padded to 256
+constexpr size_t kNoAllocStatusBytes = 256;
 constexpr size_t kNoAllocHiddenBytes = static_cast<size_t>(GEMM_EPI_FFN_NOALLOC_MAX_HIDDEN) * 2;
 
 // In host code this name is only a stand-in; the device address comes from
@@ -359,31 +362,34 @@ constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 unsigned char* g_noalloc_addr[kNoAllocMaxDevices] = {};
 
-// Device address of the scratch array on device `dev` (the current device); the first call
-// per device looks it up and zeroes the status words.
+// Device address of the scratch array on device `dev` (the current device), looked up on
+// every call (the lookup allocates nothing).  When it differs from the last one seen on the
+// device (the first call, or the module was loaded again after a cudaDeviceReset), the
+// status words and tile counters are zeroed.
 gemm_epi_status noalloc_scratch(int dev, unsigned char** out)
 {
     if (dev < 0 || dev >= kNoAllocMaxDevices) return GEMM_EPI_ERR_INVALID_ARG;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_ffn_noalloc_scratch) != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return GEMM_EPI_ERR_LAUNCH;
+    }
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_ffn_noalloc_scratch) != cudaSuccess || !ptr) {
-            cudaGetLastError();
-            return GEMM_EPI_ERR_LAUNCH;
-        }
+    if (g_noalloc_addr[dev] != ptr) {
         if (cudaMemset(ptr, 0, kNoAllocStatusBytes) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_EPI_ERR_LAUNCH;
         }
         g_noalloc_addr[dev] = static_cast<unsigned char*>(ptr);
     }
-    *out = g_noalloc_addr[dev];
+    *out = static_cast<unsigned char*>(ptr);
     return GEMM_EPI_OK;
 }
 
-// A plan on the caller's stack whose status word points into the static scratch.
+// A plan on the caller's stack whose status word and tile counter point into the static
+// scratch.
 gemm_epi_status stack_plan(gemm_epi_plan_s* p, int64_t m, int64_t n, int64_t k, int dtype,
-                           int epilog, int dev, int sms, int* status)
+                           int epilog, int dev, int sms, int* status, unsigned* sched)
 {
     memset(p, 0, sizeof(*p));
     p->m = m;
@@ -396,6 +402,7 @@ gemm_epi_status stack_plan(gemm_epi_plan_s* p, int64_t m, int64_t n, int64_t k, 
     p->sm_count = sms;
     p->wait_limit_ns = kDefaultWaitNs;
     p->d_status = status;
+    p->d_sched = sched;
     p->opt_split_k = 1;  // no split-K workspace to allocate
     return configure(p);
 }
@@ -430,12 +437,13 @@ extern "C" gemm_epi_status gemm_epi_ffn_execute_noalloc(int64_t t, int64_t d, in
     gemm_epi_status st = noalloc_scratch(dev, &scratch);
     if (st != GEMM_EPI_OK) return st;
     int* status = reinterpret_cast<int*>(scratch);
+    unsigned* sched = reinterpret_cast<unsigned*>(scratch + 8);
     void* H = scratch + kNoAllocStatusBytes;
 
     gemm_epi_plan_s g1, g2;
-    st = stack_plan(&g1, t, f, d, dtype, GEMM_EPI_GELU_BIAS, dev, sms, status);
+    st = stack_plan(&g1, t, f, d, dtype, GEMM_EPI_GELU_BIAS, dev, sms, status, sched);
     if (st != GEMM_EPI_OK) return st;
-    st = stack_plan(&g2, t, d, f, dtype, GEMM_EPI_BIAS_RESIDUAL, dev, sms, status + 1);
+    st = stack_plan(&g2, t, d, f, dtype, GEMM_EPI_BIAS_RESIDUAL, dev, sms, status + 1, sched + 2);
     if (st != GEMM_EPI_OK) return st;
     const gemm_epi_operands o1 = make_operands(X, W1, b1, nullptr, H, nullptr);
     const gemm_epi_operands o2 = make_operands(H, W2, b2, R, Y, nullptr);

@@ -5,11 +5,12 @@
 // the activation applied right after the core GEMM, inside the same thread block, and the
 // intermediate matrix is never written back to device memory.
 //
-// One persistent CTA per SM (or per SM of a CTA pair, or of a cluster of two pairs), with
-// warps in fixed roles:
+// One persistent CTA per SM (or per SM of a CTA pair), with warps in fixed roles:
 //   warp 0      TMA producer: one thread streams 64-deep K blocks of both operands into a
 //               ring of shared-memory stages (128-byte swizzle), arming a "full" mbarrier
-//               with the byte count of each stage.
+//               with the byte count of each stage.  In a CTA pair, the even CTA's producer
+//               also decides the pair's next tile (statically, or from a device-wide
+//               counter) and hands the tile indices to the other roles of both CTAs.
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma (fp32 accumulate)
 //               into one of two TMEM accumulators and commits each consumed stage back to
 //               its "empty" mbarrier, and each finished tile to a "tmem full" mbarrier.
@@ -84,7 +85,7 @@ struct TileCfg {
     static constexpr int kOffBias = kOffEpi + kEpiBytes;         // 2 x 256 fp32 per warp
     static constexpr int kBiasBytes = EW == 8 ? EW * 512 * 4 : 0;
     static constexpr int kOffBar = kOffBias + kBiasBytes;
-    static constexpr int kBarBytes = 256;
+    static constexpr int kBarBytes = 512;
     static constexpr int kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
     static constexpr int kRedBytes = kBM * BN * 4;  // one fp32 partial tile (split-K)
     static_assert(kStages >= 2, "pipeline needs two stages");
@@ -103,21 +104,29 @@ constexpr int kBarDrain = 21;
 constexpr int kOffHolder = 22 * 8;  // TMEM base address written by tcgen05.alloc
 constexpr int kOffAbort = kOffHolder + 4;
 constexpr int kOffLast = kOffAbort + 4;  // split-K through device memory: "this CTA is last"
+// CTA pairs: the ring of tile indices (see sched_publish)
+constexpr int kSchedSlots = 8;
+constexpr int kBarSchedFull = 24;         // [8] in each CTA: slot written
+constexpr int kBarSchedEmpty = 32;        // [8] in the even CTA: slot read by every consumer
+constexpr int kOffSchedSlot = 40 * 8;     // int[8] in each CTA: the tile indices
+static_assert(kOffLast + 4 <= kBarSchedFull * 8, "barrier area layout");
 
 constexpr unsigned long long kDrainLimitNs = 20ull * 1000 * 1000;  // 20 ms
 
 // Wait for the phase of `bar` with parity `parity` to complete.  Gives up (returns false)
 // when the abort flag is raised or after limit_ns nanoseconds; also after limit_ns / 8
-// polls, in case the global timer does not advance.
+// polls, in case the global timer does not advance.  CLUSTER: acquire at cluster scope (the
+// barrier is signalled from the other CTA of a pair, after it wrote data read here).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              const volatile int* abort_flag,
                                              unsigned long long limit_ns, bool honour_abort = true)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     const unsigned long long max_polls = limit_ns / 8 + 1024;
     for (unsigned long long poll = 1; poll < max_polls; ++poll) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if ((poll & 63) == 0) {
             if (honour_abort && *abort_flag) return false;
             if (globaltimer_ns() - t0 > limit_ns) return false;
@@ -157,7 +166,6 @@ struct WorkRange {
     int rank, split;         // split-K: cluster rank and size (split == 1: no split)
     int grank, gsplit;       // split-K through device memory: K slice and slices (1: none)
     int pair_rank;           // CTA pairs: 0 = the even CTA (issues the MMAs), 1 = the odd
-    int pair_index;          // clusters of two pairs: which pair of the cluster (else 0)
 };
 
 template <bool PAIR = false>
@@ -165,16 +173,15 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
 {
     WorkRange w;
     if (PAIR) {
-        // persistent CTA pairs (clusters of 2) walking 256-row tiles, or clusters of two
-        // pairs walking double rows of tiles
+        // persistent CTA pairs (clusters of 2) walking 256-row tiles: first tile and the
+        // static stride (the tiles after the first come through the pair's tile ring)
         const int cr = static_cast<int>(cluster_ctarank());
         w.first = static_cast<int>(cluster_id_x());
-        w.stride = static_cast<int>(gridDim.x / (p.pair_mc ? 4 : 2));
-        w.end = p.pair_mc ? p.tiles_m2 * p.tiles_n : p.tiles_m * p.tiles_n + p.ffn_tiles2;
+        w.stride = static_cast<int>(gridDim.x / 2);
+        w.end = p.tiles_m * p.tiles_n + p.ffn_tiles2;
         w.rank = 0;
         w.split = 1;
         w.pair_rank = cr & 1;
-        w.pair_index = p.pair_mc ? cr >> 1 : 0;
         w.kb_begin = 0;
         w.kb_end = p.k_blocks;
         w.grank = 0;
@@ -190,7 +197,6 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
         w.grank = static_cast<int>(blockIdx.x) - tile * p.split;
         w.gsplit = p.split;
         w.pair_rank = 0;
-        w.pair_index = 0;
         w.kb_begin = w.grank * p.kb_per_split;
         w.kb_end = min(p.k_blocks, w.kb_begin + p.kb_per_split);
         return w;
@@ -204,7 +210,6 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
         w.grank = 0;
         w.gsplit = 1;
         w.pair_rank = 0;
-        w.pair_index = 0;
         w.kb_begin = w.rank * p.kb_per_split;
         w.kb_end = min(p.k_blocks, w.kb_begin + p.kb_per_split);
     } else {
@@ -216,7 +221,6 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
         w.grank = 0;
         w.gsplit = 1;
         w.pair_rank = 0;
-        w.pair_index = 0;
         w.kb_begin = 0;
         w.kb_end = p.k_blocks;
     }
@@ -239,19 +243,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int tile, con
 {
     TileInfo t;
     const int tiles1 = p.tiles_m * p.tiles_n;
-    if (!FFN && p.pair_mc) {
-        // a double row of tiles: this pair's row tile of it
-        const int per_group = p.group_m * p.tiles_n;  // (group_m counts double rows here)
-        const int g = tile / per_group;
-        const int first = g * p.group_m;
-        const int rows_in_group = min(p.tiles_m2 - first, p.group_m);
-        const int r = tile - g * per_group;
-        t.tm = 2 * (first + r % rows_in_group) + w.pair_index;
-        t.tn = r / rows_in_group;
-        if (g & 1) t.tn = p.tiles_n - 1 - t.tn;  // (snake order, as in tile_coords)
-        t.prob = 0;
-        t.kb_end = w.kb_end;
-    } else if (!FFN || tile < tiles1) {
+    if (!FFN || tile < tiles1) {
         tile_coords(tile, p, t.tm, t.tn);
         t.prob = 0;
         t.kb_end = w.kb_end;
@@ -285,6 +277,84 @@ __device__ __forceinline__ bool wait_ffn_ready(const GemmParams& p, int tm,
         }
     }
     return false;
+}
+
+// ---- tile order of the CTA-pair kernels ---------------------------------------------------
+// Every role of both CTAs starts with the pair's first tile, the cluster index.  The even
+// CTA's producer thread decides the later ones: statically (+ the number of pairs), or from
+// the device-wide counter p.sched (tiles handed out in raster order, as pairs become free).
+// It hands each index, in order, to the other roles of both CTAs through a ring of
+// kSchedSlots words that exists in both CTAs: slot s has a "full" barrier in each CTA (one
+// arrival, the even producer's) and an "empty" barrier in the even CTA that counts the
+// consumers (the even CTA's MMA thread, the odd CTA's producer, and every epilogue warp of
+// both CTAs).  The pair's tile j >= 1 travels in slot (j - 1) mod kSchedSlots; an index at
+// or past the end of the walk ends it.
+template <int EW>
+__host__ __device__ constexpr uint32_t sched_consumers() { return 2u + 2u * EW; }
+
+// Even producer: publish `tile` as the pair's tile j (j >= 1) to both CTAs.
+__device__ __forceinline__ bool sched_publish(uint32_t bar0, int j, int tile,
+                                              const volatile int* abort_flag,
+                                              unsigned long long limit_ns)
+{
+    const int s = (j - 1) % kSchedSlots;
+    const uint32_t ph = static_cast<uint32_t>(((j - 1) / kSchedSlots) & 1);
+    // every consumer has read this slot's previous index
+    if (!wait_bounded<true>(bar0 + 8u * (kBarSchedEmpty + s), ph ^ 1u, abort_flag, limit_ns))
+        return false;
+    const uint32_t slot = bar0 + kOffSchedSlot + 4u * static_cast<uint32_t>(s);
+    const uint32_t full = bar0 + 8u * (kBarSchedFull + s);
+    const uint32_t peer = cluster_ctarank() ^ 1u;
+    st_shared_u32(slot, static_cast<uint32_t>(tile));
+    st_shared_cluster_u32(map_shared_rank(slot, peer), static_cast<uint32_t>(tile));
+    mbar_arrive(full);                                 // release: the local write above
+    mbar_arrive_cluster(map_shared_rank(full, peer));  // release.cluster: the remote write
+    return true;
+}
+
+// Consumer (one thread): the pair's tile j (j >= 1); releases the slot after reading it.
+__device__ __forceinline__ bool sched_take(uint32_t bar0, int j, int& tile,
+                                           const volatile int* abort_flag,
+                                           unsigned long long limit_ns)
+{
+    const int s = (j - 1) % kSchedSlots;
+    const uint32_t ph = static_cast<uint32_t>(((j - 1) / kSchedSlots) & 1);
+    if (!wait_bounded<true>(bar0 + 8u * (kBarSchedFull + s), ph, abort_flag, limit_ns))
+        return false;
+    tile = static_cast<int>(ld_shared_u32(bar0 + kOffSchedSlot + 4u * static_cast<uint32_t>(s)));
+    const uint32_t empty = bar0 + 8u * (kBarSchedEmpty + s);
+    const uint32_t cr = cluster_ctarank();
+    if (cr & 1u)
+        mbar_arrive_cluster(map_shared_rank(empty, cr & ~1u));
+    else
+        mbar_arrive(empty);
+    return true;
+}
+
+// The whole warp: the pair's tile j (j >= 1), taken by lane 0 and broadcast.
+__device__ __forceinline__ bool sched_take_warp(uint32_t bar0, int j, int& tile,
+                                                const volatile int* abort_flag,
+                                                unsigned long long limit_ns)
+{
+    int ok = 0, t = 0;
+    if ((threadIdx.x & 31) == 0) ok = sched_take(bar0, j, t, abort_flag, limit_ns) ? 1 : 0;
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    tile = __shfl_sync(0xFFFFFFFFu, t, 0);
+    return ok != 0;
+}
+
+// Run by each pair's even CTA, thread 0 (the producer, after its last use of the counter):
+// count the pair as done; the last pair sets the counter and the count back to zero, so the
+// next launch finds them at zero.  Every pair reaches this whether or not it aborted.
+__device__ __forceinline__ void sched_finish(const GemmParams& p)
+{
+    __threadfence();
+    const unsigned pairs = gridDim.x / 2;
+    if (atomicAdd(p.sched + 1, 1u) == pairs - 1) {
+        __threadfence();
+        atomicExch(p.sched, 0u);
+        atomicExch(p.sched + 1, 0u);
+    }
 }
 
 // Byte offset, in the partial-tile buffer, of 16-byte unit `unit` (4 fp32 columns) of
@@ -343,9 +413,7 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase,
     const int k0 = kb * kBK;
     if constexpr (PAIR && F8) {
         // E4M3: a K block is 128 elements (one 128-byte swizzle row); A rows and the rows of
-        // B transposed (columns of D) are K-major boxes {128 k, 128 rows} of 16 KB; in a
-        // cluster of two pairs sharing B each CTA loads one {128 k, 64 rows} box of its
-        // half (map tm_B2) and multicasts it
+        // B transposed (columns of D) are K-major boxes {128 k, 128 rows} of 16 KB
         static_assert(BN == 256, "the FP8 pair kernel runs 256-wide tiles");
         const uint32_t cr = cluster_ctarank();
         const uint32_t rank = cr & 1u;
@@ -354,12 +422,6 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase,
         const int k8 = kb * 128;
         const int brow = tn * BN + static_cast<int>(rank) * (BN / 2);
         tma_load_2d_pair(sa, &p.tm_A, fb0, k8, tm * 2 * kBM + static_cast<int>(rank) * kBM);
-        if (p.pair_mc) {
-            const uint32_t pp = cr >> 1;
-            tma_load_2d_pair_mc(sb + pp * 8192, &p.tm_B2, fb0, k8, brow + static_cast<int>(pp) * 64,
-                                static_cast<uint16_t>((1u << rank) | (1u << (2u + rank))));
-            return;
-        }
         tma_load_2d_pair(sb, &p.tm_B, fb0, k8, brow);
         return;
     }
@@ -374,16 +436,6 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase,
         const CUtensorMap* mA = prob ? &p.tm_A2 : &p.tm_A;
         const CUtensorMap* mB = prob ? &p.tm_B2 : &p.tm_B;
         tma_load_2d_pair(sa, mA, fb0, k0, tm * 2 * kBM + static_cast<int>(rank) * kBM);
-        if (p.pair_mc) {
-            // two pairs, one column tile: each CTA loads one of the two 64-column panels of
-            // its half of B and multicasts it to the same half in both pairs
-            static_assert(C::kBRows == 128, "two 64-column panels per CTA");
-            const uint32_t pp = cr >> 1;
-            tma_load_2d_pair_mc(sb + pp * 8192, mB, fb0,
-                                tn * BN + static_cast<int>(rank) * (BN / 2) + static_cast<int>(pp) * 64,
-                                k0, static_cast<uint16_t>((1u << rank) | (1u << (2u + rank))));
-            return;
-        }
 #pragma unroll
         for (int q = 0; q < C::kBRows / 64; ++q)
             tma_load_2d_pair(sb + q * 8192, mB, fb0,
@@ -461,7 +513,27 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
     long long issued = pre;
     bool ok = true;
     grid_dependency_wait();
-    for (int tile = w.first; ok && tile < w.end; tile += w.stride) {
+    const bool even = !PAIR || w.pair_rank == 0;
+    const bool dyn = PAIR && even && p.sched != nullptr;
+    int tile = w.first;
+    for (int j = 0; ok; ++j) {
+        if (PAIR && j > 0) {
+            if (even) {
+                if (!sched_publish(bar0, j, tile, abort_flag, p.wait_limit_ns)) {
+                    if (!*abort_flag) record_failure(p.status, abort_flag, kRoleProducer);
+                    ok = false;
+                    break;
+                }
+            } else if (!sched_take(bar0, j, tile, abort_flag, p.wait_limit_ns)) {
+                if (!*abort_flag) record_failure(p.status, abort_flag, kRoleProducer);
+                ok = false;
+                break;
+            }
+        }
+        if (tile >= w.end) break;
+        // The next tile: asked for now, its index is needed only after this tile's loads.
+        unsigned ticket = 0;
+        if (dyn) ticket = atomicAdd(p.sched, 1u);
         const TileInfo t = tile_info<FFN>(p, tile, w);
         if (FFN && t.prob == 1) {
             if (!wait_ffn_ready(p, t.tm, abort_flag)) {
@@ -471,7 +543,7 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
             }
             fence_proxy_async_global();
         }
-        for (int kb = (tile == w.first ? w.kb_begin + pre : w.kb_begin); kb < t.kb_end; ++kb) {
+        for (int kb = (j == 0 ? w.kb_begin + pre : w.kb_begin); kb < t.kb_end; ++kb) {
             if (!wait_bounded(bar0 + 8u * (kBarEmpty + stage), phase ^ 1u, abort_flag,
                               p.wait_limit_ns)) {
                 if (!*abort_flag) record_failure(p.status, abort_flag, kRoleProducer);
@@ -486,6 +558,12 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
                 stage = 0;
                 phase ^= 1u;
             }
+        }
+        if (dyn) {
+            const long long nxt = static_cast<long long>(w.stride) + ticket;
+            tile = nxt < w.end ? static_cast<int>(nxt) : w.end;
+        } else if (even) {
+            tile = tile + w.stride < w.end ? tile + w.stride : w.end;
         }
     }
     if (!ok && !(PAIR && w.pair_rank != 0)) {
@@ -523,14 +601,24 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
     const uint32_t self = PAIR ? cluster_ctarank() : 0u;
     const uint16_t mask_self = static_cast<uint16_t>(1u << self);
     const uint16_t mask_pair = static_cast<uint16_t>(3u << self);
-    const uint16_t mask_all = p.pair_mc ? 0xF : 0x3;
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool issued_any = false;
     bool ok = true;
-    for (int tile = w.first; ok && tile < w.end; tile += w.stride) {
+    int tile = w.first;
+    for (int j = 0; ok; ++j) {
+        if (j > 0) {
+            if (!PAIR) {
+                tile += w.stride;
+            } else if (!sched_take(bar0, j, tile, abort_flag, p.wait_limit_ns)) {
+                if (!*abort_flag) record_failure(p.status, abort_flag, kRoleMma);
+                ok = false;
+                break;
+            }
+        }
+        if (tile >= w.end) break;
         if (!wait_bounded(bar0 + 8u * (kBarTmemEmpty + acc), acc_phase ^ 1u, abort_flag,
                           p.wait_limit_ns)) {
             if (!*abort_flag) record_failure(p.status, abort_flag, kRoleMma);
@@ -575,10 +663,9 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
                     mma_f16_ss(d_tmem, ad, bd, idesc, (kb > w.kb_begin || kk > 0) ? 1u : 0u);
             }
             issued_any = true;
-            // stage free (in both CTAs of a pair, or all four CTAs of a cluster of two pairs,
-            // whose "empty" barriers then wait for both pairs' commits) once these MMAs finish
+            // stage free (in both CTAs of a pair) once these MMAs finish
             if constexpr (PAIR)
-                mma_commit_pair(bar0 + 8u * (kBarEmpty + stage), mask_all);
+                mma_commit_pair(bar0 + 8u * (kBarEmpty + stage), mask_pair);
             else
                 mma_commit(bar0 + 8u * (kBarEmpty + stage));
             if (++stage == C::kStages) {
@@ -944,7 +1031,17 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
 
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = w.first; tile < w.end; tile += w.stride) {
+    int tile = w.first;
+    for (int j = 0;; ++j) {
+        if (j > 0) {
+            if (!PAIR) {
+                tile += w.stride;
+            } else if (!sched_take_warp(bar0, j, tile, abort_flag, p.wait_limit_ns)) {
+                if (!*abort_flag) record_failure(p.status, abort_flag, kRoleEpilogue);
+                break;
+            }
+        }
+        if (tile >= w.end) break;
         const TileInfo t = tile_info<FFN>(p, tile, w);
         const int tm = t.tm, tn = t.tn;
         const bool second = FFN && t.prob == 1;  // GEMM 2 of the FFN block
@@ -1417,7 +1514,13 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1) gemm_epi_kernel(const __grid_
         }
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar0 + 8u * (kBarFull + s), 1);
-            mbar_init(bar0 + 8u * (kBarEmpty + s), PAIR && p.pair_mc ? 2 : 1);
+            mbar_init(bar0 + 8u * (kBarEmpty + s), 1);
+        }
+        if (PAIR) {
+            for (int s = 0; s < kSchedSlots; ++s) {
+                mbar_init(bar0 + 8u * (kBarSchedFull + s), 1);
+                mbar_init(bar0 + 8u * (kBarSchedEmpty + s), sched_consumers<EW>());
+            }
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar0 + 8u * (kBarTmemFull + a), 1);
@@ -1516,6 +1619,9 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1) gemm_epi_kernel(const __grid_
         else
             tmem_dealloc(tmem_base, C::kTmemCols);
     }
+    // The pair's producer is done with the tile counter.
+    if (PAIR && p.sched != nullptr && threadIdx.x == 0 && (cluster_ctarank() & 1u) == 0)
+        sched_finish(p);
 }
 
 }  // namespace gemm_epi

@@ -54,7 +54,7 @@ cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t stream, bool 
     cudaLaunchAttribute attr[2];
     unsigned na = 0;
     attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = p.pair_mc ? 4 : 2;  // one pair, or two sharing B
+    attr[na].val.clusterDim.x = 2;  // one CTA pair
     attr[na].val.clusterDim.y = 1;
     attr[na].val.clusterDim.z = 1;
     ++na;
@@ -92,8 +92,9 @@ cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream, bool p
 }
 
 template <int BN>
-int max_clusters_one(unsigned size = 2)
+int max_clusters_one()
 {
+    constexpr unsigned size = 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(size, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -173,7 +174,7 @@ cudaError_t fp8_launch_one(const GemmParams& p, int grid, cudaStream_t stream, b
     cudaLaunchAttribute attr[2];
     unsigned na = 0;
     attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = p.pair_mc ? 4 : 2;  // one pair, or two sharing B
+    attr[na].val.clusterDim.x = 2;  // one CTA pair
     attr[na].val.clusterDim.y = 1;
     attr[na].val.clusterDim.z = 1;
     ++na;
@@ -222,15 +223,6 @@ int rowpair_max_clusters(int bn)
     switch (bn) {
     case 224: return max_clusters_one<224>();
     case 256: return max_clusters_one<256>();
-    default: return 0;
-    }
-}
-
-int rowpair_max_clusters4(int bn)
-{
-    switch (bn) {
-    case 224: return max_clusters_one<224>(4);
-    case 256: return max_clusters_one<256>(4);
     default: return 0;
     }
 }

@@ -88,6 +88,8 @@ gemm_epi_status chunk_plan(const gemm_epi_plan_s* p, int64_t rows, gemm_epi_plan
     c->no_pdl = p->no_pdl;
     c->wait_limit_ns = p->wait_limit_ns;
     c->d_status = p->d_status;
+    c->d_sched = p->d_sched;  // (the chunk launches run in stream order on one stream)
+    c->opt_tile_order = p->opt_tile_order;
     return configure(c);
 }
 

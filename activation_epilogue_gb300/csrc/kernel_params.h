@@ -92,12 +92,14 @@ struct GemmParams {
     int split_global;
     float* split_ws;
     unsigned* split_count;
-    // CTA-pair kernel in clusters of two pairs (pair_mc == 1): the pairs of a cluster take
-    // the row tiles 2 tm2 and 2 tm2 + 1 of one column tile (tiles_m2 = double rows), load
-    // each B panel once and multicast it to both pairs, and free a stage only when both
-    // pairs' MMAs have read it.
-    int pair_mc;
-    int tiles_m2;
+    // CTA-pair kernels: order of the tiles.  sched == nullptr: static, pair q takes tiles
+    // q, q + pairs, q + 2 pairs, ...  Otherwise each pair takes tile q first and then the
+    // tile pairs + atomicAdd(&sched[0], 1) each time it starts one, until the walk ends;
+    // sched[1] counts the pairs that have finished, and the last one sets both words back
+    // to zero, so every launch finds them at zero.  Handing out tiles in raster order keeps
+    // the tiles in flight a contiguous window of the walk (pairs that run slower do not
+    // fall behind the others), so the operand panels they share are still in L2.
+    unsigned* sched;
     // Swapped kernel with 64 MMA rows per tile (swap_m64 == 1): each tile is 64 columns of
     // D (one 64-column box of B per stage), the MMA runs M = 64, and its rows sit in TMEM
     // lanes 0-15 of each lane quarter (row r in lane 32 (r / 16) + r % 16), so every
@@ -142,8 +144,6 @@ cudaError_t rowpair_launch(int bn, const GemmParams& p, int grid, cudaStream_t s
 int rowpair_smem_bytes(int bn);
 int rowpair_stages(int bn);
 int rowpair_max_clusters(int bn);
-// Resident clusters of two CTA pairs (four CTAs) of the pair kernel.
-int rowpair_max_clusters4(int bn);
 
 // CTA-pair kernel on E4M3 inputs (256 x 256 tiles), epilogs BIAS, RELU_BIAS, GELU_BIAS,
 // RELU_AUX_BIAS, BIAS_RESIDUAL, NONE.

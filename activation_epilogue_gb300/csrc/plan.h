@@ -16,6 +16,8 @@ namespace gemm_epi_impl {
 enum Variant { kEmpty = 0, kRowTile = 1, kSwapped = 2, kBiasOnly = 3, kRowPair = 4 };
 
 constexpr int kSwappedMaxM = 256;
+// A plan's own device words: the status word (byte 0) and the tile counter (bytes 8-15).
+constexpr size_t kPlanWordsBytes = 16;
 constexpr unsigned long long kDefaultWaitNs = 2000ull * 1000 * 1000;  // 2 s
 
 struct HostPipe;
@@ -32,10 +34,11 @@ struct gemm_epi_plan_s {
     int variant, bn, stages, smem, grid, group_m, tiles_m, tiles_n, k_blocks;
     int split, kb_per_split;  // split-K slices (split == 1: persistent kernel)
     int split_global;         // 1: the slices meet in device memory, 0: in a cluster
-    int pair_mc;              // CTA-pair kernel in clusters of two pairs sharing B
+    int dyn_order;            // CTA-pair kernel: tiles handed out by the device counter
     int swap_m64;             // swapped kernel with 64 MMA rows (columns of D) per tile
     // options (0 = automatic)
     int opt_variant, opt_bn, opt_split_k, opt_grid, opt_group_m, opt_split_mode, opt_tile_m;
+    int opt_tile_order;
     // split-K through device memory: fp32 partial tiles [tile][slice][128 x bn] and the
     // per-tile arrival counts (zero between launches), allocated when the plan is configured
     float* d_split_ws;
@@ -46,13 +49,15 @@ struct gemm_epi_plan_s {
     unsigned long long wait_limit_ns;
     int debug_stall;
     int* d_status;
+    // CTA-pair kernels' tile counter (two words, zero between launches; see GemmParams::sched),
+    // in the same allocation as the status word; NULL: static tile order only
+    unsigned* d_sched;
     // tensor maps for the last (A, B, D) pointers
     const void* key_A;
     const void* key_B;
     const void* key_D;
     bool maps_valid;
     CUtensorMap tm_A, tm_B, tm_D;
-    CUtensorMap tm_B64;  // E4M3: B transposed in 64-row boxes (clusters of two pairs)
     char desc[320];
     gemm_epi_impl::HostPipe* host;  // gemm_epi_execute_host's streams, buffers and chunk plans
 };

@@ -12,9 +12,11 @@ the CPU oracle timed on a bounded sample, SM clocks sampled during the timed reg
 extras: the unfused baseline on the same workload, the other workloads, and small-m
 microseconds per call.
 
-Under torchrun (N > 1) each rank runs its own replica of the workload on its own GPU
-(the problem is independent per GPU; no collective is on the data path); the JSON value
-is the sum of all ranks' work divided by the slowest rank's time.
+With N > 1 each rank runs its own replica of the workload on its own GPU (the problem is
+independent per GPU; no collective is on the data path); the JSON value is the sum of all
+ranks' work divided by the slowest rank's time.  The ranks come from torchrun, or, when no
+launcher set WORLD_SIZE, the script starts N replica processes itself (one per GPU, a local
+rendezvous); n_gpus is the rank count either way.
 
 --impl reference times the reference arm: the CPU oracle as it stands, on this host's
 cores, on a bounded sample of the same workload per step (rank 0 only).
@@ -255,8 +257,9 @@ def cpu_inputs_for(w, rows_needed: int, dev):
     return A, B, b
 
 
-def run_reference(args):
-    """The reference arm: the CPU oracle, as it stands, on a bounded sample per step."""
+def run_reference(args, world: int):
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample per step (rank 0
+    of `world` ranks runs it; the line reports the job's rank count)."""
     import torch
 
     import oracle
@@ -279,7 +282,7 @@ def run_reference(args):
               f"{w.epilog} problem per step, fp64 oracle")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total / len(ts) * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": HEADLINE, "m": w.m, "n": w.n, "k": w.k, "epilog": w.epilog,
@@ -660,7 +663,7 @@ def measure_backward(device, stream, flush, peaks):
     return res
 
 
-def main():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -677,18 +680,46 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--only", choices=["backward", "ffn", "fp8"],
                     help="print only these measurements (one JSON object), for profiling")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
     if args.warmup < 3:
         log("[bench] warm-up raised to 3 steps")
         args.warmup = 3
+    return args
 
+
+# ---- replicas without a launcher --------------------------------------------------------------
+
+def _replica_main(local_rank: int, argv, world: int, port: int):
+    """Entry point of one replica process started by launch_replicas: the rank variables a
+    launcher would set, then the same code path as under torchrun."""
+    os.environ.update(RANK=str(local_rank), LOCAL_RANK=str(local_rank), WORLD_SIZE=str(world),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    rank_main(parse_args(argv))
+
+
+def launch_replicas(argv, world: int, target=_replica_main):
+    """`--gpus N` with no launcher around the process: start N replica processes (spawn, one
+    per GPU, a local rendezvous on 127.0.0.1), wait for all of them; raises if one fails."""
+    import socket
+
+    import torch.multiprocessing as mp
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    mp.start_processes(target, args=(list(argv), world, port), nprocs=world, join=True,
+                       start_method="spawn")
+
+
+def rank_main(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
     if args.impl == "reference":
         if rank == 0:
-            run_reference(args)
+            run_reference(args, world)
         return
 
     if args.only:
@@ -710,14 +741,28 @@ def main():
     if world > 1:
         import torch
         import torch.distributed as tdist
-        torch.cuda.set_device(local_rank)
-        tdist.init_process_group("nccl")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        tdist.init_process_group(backend)
         dist = tdist
     try:
         run_ours(args, rank, world, local_rank, dist)
     finally:
         if dist is not None:
             dist.destroy_process_group()
+
+
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
+    args = parse_args(argv)
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        launch_replicas(argv, args.gpus)
+        return
+    if int(os.environ.get("WORLD_SIZE", "1")) != args.gpus:
+        log(f"[bench] --gpus {args.gpus} but WORLD_SIZE={os.environ.get('WORLD_SIZE', '1')}: "
+            "reporting the launcher's rank count")
+    rank_main(args)
 
 
 if __name__ == "__main__":

@@ -49,7 +49,10 @@
  *     early, but reads and writes device memory only after that work has completed.
  *   - A plan belongs to the device that was current when it was made; execute with that
  *     device current.  Free it only after the work that uses it has completed.  One plan
- *     must not be executed from several host threads at the same time.
+ *     must not be executed from several host threads at the same time, and its launches
+ *     must not run concurrently on the GPU (two streams without an ordering between them):
+ *     they share the plan's status word and tile counter.  Different plans may run
+ *     concurrently.
  *   - No call aborts the process; every failure is a status code.
  */
 #ifndef GEMM_EPI_H_
@@ -65,8 +68,9 @@ extern "C" {
 /* cudaStream_t, without requiring the CUDA headers (same definition as cuda_runtime). */
 typedef struct CUstream_st* cudaStream_t;
 
-/* Opaque plan: the chosen kernel configuration, cached tensor-memory-access descriptors and
- * a device status word.  Owned by the library. */
+/* Opaque plan: the chosen kernel configuration, cached tensor-memory-access descriptors, a
+ * device status word and a device tile counter (zero between launches).  Owned by the
+ * library. */
 typedef struct gemm_epi_plan_s* gemm_epi_plan_t;
 
 typedef enum {
@@ -132,10 +136,8 @@ typedef enum {
 /* Plan-time settings (gemm_epi_plan_set_option).  0 always means "automatic". */
 typedef enum {
     GEMM_EPI_OPT_VARIANT = 0,       /* 1 = row-tile kernel, 2 = swapped small-m kernel,
-                                       3 = row-tile kernel run by CTA pairs (256-row tiles),
-                                       4 = CTA pairs in clusters of two pairs that share
-                                       each B panel (TMA multicast); E4M3 plans take 0, 3
-                                       or 4 */
+                                       3 = row-tile kernel run by CTA pairs (256-row tiles);
+                                       E4M3 plans take 0 or 3 */
     GEMM_EPI_OPT_TILE_N = 1,        /* N tile: 64, 128 or 256 for the row-tile kernel;
                                        224 or 256 for the CTA-pair kernel; 16, 32, 64, 128
                                        or 256 rows of D for the swapped kernel (a width
@@ -160,11 +162,18 @@ typedef enum {
                                        the last CTA of a tile adds them in slice order);
                                        1 = within a thread-block cluster over distributed
                                        shared memory (slices 1..4) */
-    GEMM_EPI_OPT_TILE_M = 10        /* swapped kernel: columns of D per tile (MMA rows), 128
+    GEMM_EPI_OPT_TILE_M = 10,       /* swapped kernel: columns of D per tile (MMA rows), 128
                                        (the automatic choice) or 64 (on request; only the
                                        epilogs BIAS, RELU_BIAS, GELU_BIAS, NONE, TANH_BIAS,
                                        BIAS_RESIDUAL and GELU_AUX_BIAS, without a K split,
                                        else ERR_INVALID_ARG); the other kernels ignore it */
+    GEMM_EPI_OPT_TILE_ORDER = 11    /* CTA-pair kernel: 2 (the automatic choice) = each
+                                       pair takes its next tile, in raster order, from a
+                                       counter in the plan's device memory when it starts
+                                       one; 1 = static, pair q takes tiles q, q + pairs,
+                                       ...; the other kernels ignore it.  With 2 the plan's
+                                       launches must not overlap on the GPU (they share the
+                                       counter) */
 } gemm_epi_option;
 
 /*
@@ -392,13 +401,15 @@ gemm_epi_status gemm_epi_ffn_free(gemm_epi_ffn_plan_t p);
  * computation and arguments as gemm_epi_ffn_plan + gemm_epi_ffn_execute, but there is no
  * plan: the hidden activation H and the two launches' status words live in one static
  * device array inside this library, of GEMM_EPI_FFN_NOALLOC_MAX_HIDDEN 16-bit elements
- * (32 MiB) plus 256 bytes, which every GPU that loads the library keeps until the process
- * exits.
+ * (32 MiB) plus 256 bytes (the launches' status words and tile counters), which every GPU
+ * that loads the library keeps until the process exits.
  *   - t * f > GEMM_EPI_FFN_NOALLOC_MAX_HIDDEN returns GEMM_EPI_ERR_SCRATCH_LIMIT and launches
  *     nothing; other argument errors as gemm_epi_ffn_execute.
- *   - No cudaMalloc, cudaFree or other allocating call is made.  The first call on a device
- *     looks up the array's device address (cudaGetSymbolAddress) and zeroes the status
- *     words; make that first call before any stream capture.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.  Every call looks up the
+ *     array's device address (cudaGetSymbolAddress); the first call on a device, and the
+ *     first after a cudaDeviceReset has loaded the library's module again at a new
+ *     address, also zeroes the status words and tile counters with a synchronous
+ *     cudaMemset: make that first call before any stream capture.
  *   - Every call on a device shares the one array, which keeps the last call's H: calls
  *     whose work overlaps on the GPU (different streams, or different host threads) race
  *     on it and give wrong results; order them on one stream.

@@ -103,7 +103,8 @@ VARIANTS = [
                                                "SPLIT_MODE": 1}),
     ("split6_swapped", 40, 392, 776, {"VARIANT": 2, "TILE_N": 16, "SPLIT_K": 6}),
     ("swapped_narrow", 100, 392, 200, {"VARIANT": 2, "TILE_N": 32}),
-    ("pair_x2", 1000, 520, 200, {"VARIANT": 4}),
+    ("pair_static", 1000, 520, 200, {"VARIANT": 3, "TILE_ORDER": 1}),
+    ("pair_dynamic_walk", 1000, 520, 200, {"VARIANT": 3, "TILE_ORDER": 2, "GRID": 4}),
     ("persistent", 640, 512, 520, {"VARIANT": 1, "TILE_N": 128, "GRID": 3, "GROUP_M": 2}),
 ]
 

@@ -78,29 +78,28 @@ def test_fp8_parity(epilog, shape):
 
 @pytest.mark.parametrize("epilog", EPILOGS)
 @pytest.mark.parametrize("shape", [(1000, 520, 208), (600, 264, 1040), (300, 776, 400)])
-def test_fp8_two_pair_clusters(epilog, shape):
-    # clusters of two pairs sharing B (64-row boxes of B transposed, multicast); 600 and 300
-    # rows leave the last cluster's second pair without rows of A
+def test_fp8_static_tile_order(epilog, shape):
+    # the pair kernel with the static tile order (the automatic one is the dynamic order)
     m, n, k = shape
     layout = "M1" if (len(epilog) + m) % 3 == 0 else "1N"
     p = workloads.random_fp8_problem(m, n, k, bias_layout=layout, seed=m + n + k + 7 * len(epilog),
                                      residual=True)
-    _, _, desc = _check(p, m, n, k, epilog, layout, options={"VARIANT": 4})
-    assert "dtype=e4m3" in desc and "variant=row-pair-x2" in desc
+    _, _, desc = _check(p, m, n, k, epilog, layout, options={"TILE_ORDER": 1})
+    assert "dtype=e4m3" in desc and "order=static" in desc
 
 
-def test_fp8_two_pair_clusters_walk():
-    m, n, k = 2304, 1000, 512          # 9 row tiles, 4 column tiles, few clusters walking
+@pytest.mark.parametrize("order", [1, 2])
+def test_fp8_walk(order):
+    m, n, k = 2304, 1000, 512          # 9 row tiles, 4 column tiles, few pairs walking
     p = workloads.random_fp8_problem(m, n, k, bias_layout="1N", seed=2304, residual=True)
-    _check(p, m, n, k, "RELU_AUX_BIAS", "1N", options={"VARIANT": 4, "GRID": 8})
+    _check(p, m, n, k, "RELU_AUX_BIAS", "1N", options={"GRID": 8, "TILE_ORDER": order})
 
 
 @pytest.mark.parametrize("m,n", [(65536, 16384), (4096, 4096), (1024, 1024)])
-def test_fp8_runs_single_pairs_unless_asked(m, n):
+def test_fp8_plan_is_a_pair_plan_with_dynamic_order(m, n):
     with gemm_epi.Plan(m, n, 8192, "e4m3", "RELU_BIAS", "1N") as plan:
-        assert "variant=row-pair " in plan.describe()
-        plan.set_option("VARIANT", 4)
-        assert "variant=row-pair-x2 " in plan.describe()
+        d = plan.describe()
+        assert "variant=row-pair " in d and "order=dynamic" in d
 
 
 @pytest.mark.parametrize("epilog", ["RELU_AUX_BIAS", "BIAS_RESIDUAL", "GELU_BIAS"])
@@ -170,13 +169,13 @@ def test_fp8_rules():
 
 @pytest.mark.parametrize("i", range(16))
 def test_fp8_random_cases(i):
-    # seeded random shapes (k a multiple of 16), epilogs, layouts, single pairs or clusters
+    # seeded random shapes (k a multiple of 16), epilogs, layouts, both tile orders
     import random
     r = random.Random(7000 + i)
     m, n, k = r.randint(1, 900), 8 * r.randint(1, 100), 16 * r.randint(1, 40)
     epilog = r.choice(EPILOGS)
     layout = r.choice(["M1", "1N"])
-    opts = {"VARIANT": r.choice([3, 4])}
+    opts = {"VARIANT": 3, "TILE_ORDER": r.choice([1, 2])}
     if r.random() < 0.3:
         opts["GRID"] = r.choice([4, 8])
     p = workloads.random_fp8_problem(m, n, k, bias_layout=layout, seed=r.randint(0, 10 ** 6),

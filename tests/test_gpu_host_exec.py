@@ -95,15 +95,16 @@ def test_execute_host_rules():
         plan.execute_host(None, None, None, None)
 
 
-def test_execute_host_large_chunks_two_pair_clusters():
-    # 16 chunks of 1280 rows x 8192 columns: each chunk plan runs the CTA-pair kernel in
-    # clusters of two pairs sharing B; rows on and around chunk edges checked by the oracle,
-    # and the whole result against the same plan on device buffers (the same kernels)
+def test_execute_host_large_chunks_pair_kernel():
+    # 16 chunks of 1280 rows x 8192 columns: each chunk plan runs the CTA-pair kernel with
+    # the dynamic tile order (the chunk plans share the plan's tile counter, launching in
+    # turn on one stream); rows on and around chunk edges checked by the oracle, and the
+    # whole result against the same plan on device buffers (the same kernels)
     m, n, k = 20480, 8192, 64
     p = workloads.random_problem(m, n, k, dtype="bf16", bias_layout="1N", residual=False,
                                  seed=2048)
     with gemm_epi.Plan(m, n, k, "bf16", "RELU_AUX_BIAS", "1N") as plan:
-        assert "variant=row-pair-x2" in plan.describe()
+        assert "variant=row-pair " in plan.describe() and "order=dynamic" in plan.describe()
         D, aux = _run_host(p, m, n, k, "bf16", "RELU_AUX_BIAS", "1N", plan=plan)
         dev = torch.device("cuda")
         Dd = torch.empty((m, n), dtype=torch.bfloat16, device=dev)

@@ -4,8 +4,8 @@ D, the residual, the stored 16-bit pre-activation and the backward input are ind
 row * n + column, and the mask words as row * ceil(n/32) + word.  At m x n = 139264 x 16384
 (2.28e9 elements, 4.6 GB per 16-bit matrix) every row from 131072 on lies past 2^31.  A
 32-bit product would wrap there, so these tests compare sampled rows on both sides of that
-line, in every kernel that such a shape can reach: the automatic plan (clusters of CTA
-pairs), the single-CTA row tiles, and the unfused baseline's elementwise kernel.  K = 64
+line, in every kernel that such a shape can reach: the automatic plan (CTA pairs,
+dynamic tile order), the single-CTA row tiles, and the unfused baseline's elementwise kernel.  K = 64
 keeps the GEMMs and the oracle's rows cheap.
 """
 import numpy as np

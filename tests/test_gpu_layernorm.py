@@ -150,7 +150,8 @@ VARIANTS = [
     ("rowtile256", 300, 520, 1024, {"VARIANT": 1, "TILE_N": 256}),
     ("pair256", 600, 520, 200, {"VARIANT": 3, "TILE_N": 256}),
     ("pair224", 520, 600, 136, {"VARIANT": 3, "TILE_N": 224}),
-    ("pair_x2", 1000, 600, 136, {"VARIANT": 4}),
+    ("pair_static", 1000, 600, 136, {"VARIANT": 3, "TILE_ORDER": 1}),
+    ("pair_dynamic_walk", 1000, 600, 136, {"VARIANT": 3, "TILE_ORDER": 2, "GRID": 4}),
     ("split3", 260, 264, 520, {"VARIANT": 1, "TILE_N": 128, "SPLIT_K": 3}),
     ("split3_cluster", 260, 264, 520, {"VARIANT": 1, "TILE_N": 128, "SPLIT_K": 3, "SPLIT_MODE": 1}),
     ("small_m_default", 16, 3072, 768, None),

@@ -604,63 +604,92 @@ def test_pair_epilogue_warp_variants(bn, epilog, k, grid):
     check(p, m, n, k, "bf16", epilog, layout, options=opts)
 
 
-# ---- the CTA-pair kernel in clusters of two pairs sharing B (multicast) ----------------------
+# ---- the CTA-pair kernel's tile order: static, or handed out by the plan's device counter ----
 
+ORDERS = {"static": 1, "dynamic": 2}
+
+
+@pytest.mark.parametrize("order", ["static", "dynamic"])
 @pytest.mark.parametrize("bn", [256, 224])
 @pytest.mark.parametrize("epilog", EPILOGS)
-def test_pair_x2_parity(bn, epilog):
-    m, n, k = 1000, 520, 200           # 4 ragged 256-row tiles = 2 double rows, ragged N and K
+def test_pair_order_parity(order, bn, epilog):
+    m, n, k = 1000, 520, 200           # 4 ragged 256-row tiles, ragged N and K
     layout = "M1" if (EPILOGS.index(epilog) + bn // 32) % 2 else "1N"
     p = _inputs(m, n, k, "bf16", layout, seed=161 + EPILOGS.index(epilog) + bn)
     _, _, _, _, desc = check(p, m, n, k, "bf16", epilog, layout,
-                             options={"VARIANT": 4, "TILE_N": bn})
-    assert "variant=row-pair-x2" in desc and f"tile=256x{bn} " in desc
+                             options={"VARIANT": 3, "TILE_N": bn, "TILE_ORDER": ORDERS[order]})
+    assert "variant=row-pair" in desc and f"tile=256x{bn} " in desc and f"order={order}" in desc
 
 
-@pytest.mark.parametrize("m", [300, 600, 1280])
-def test_pair_x2_odd_row_tiles(m):
-    # an odd number of 256-row tiles: the last cluster's second pair has no rows of A
-    n, k = 776, 328
-    p = _inputs(m, n, k, "f16", "1N", seed=m + 5)
-    check(p, m, n, k, "f16", "RELU_AUX_BIAS", "1N", options={"VARIANT": 4})
-
-
-@pytest.mark.parametrize("grid,group_m", [(4, 1), (8, 2), (12, 8)])
-def test_pair_x2_persistent_walk(grid, group_m):
-    m, n, k = 2304, 1000, 520          # 9 row tiles (5 double rows), 5 column tiles, 9 K blocks
+@pytest.mark.parametrize("grid,group_m", [(2, 1), (4, 2), (8, 3), (12, 8)])
+def test_pair_dynamic_walk(grid, group_m):
+    # 9 x 5 tiles, 9 K blocks, few pairs: most tiles come from the counter
+    m, n, k = 2304, 1000, 520
     p = _inputs(m, n, k, "bf16", "1N", seed=grid + 170)
     check(p, m, n, k, "bf16", "GELU_BIAS", "1N",
-          options={"VARIANT": 4, "GRID": grid, "GROUP_M": group_m})
+          options={"VARIANT": 3, "GRID": grid, "GROUP_M": group_m, "TILE_ORDER": 2})
 
 
-def test_pair_x2_integer_bit_exact():
+def test_pair_dynamic_counter_back_at_zero_between_launches():
+    # every launch must find the counter at zero: repeated launches of one plan (each on new
+    # inputs) and of two plans in turn, all exact on integer inputs
+    from parity_helpers import oracle_ref
+    dev = torch.device("cuda")
+    shapes = [(1536, 776, 136), (768, 1288, 72)]
+    plans = [gemm_epi.Plan(m, n, k, "bf16", "RELU_AUX_BIAS", "1N", variant=3, grid=10)
+             for m, n, k in shapes]
+    try:
+        for rep in range(4):
+            for i, ((m, n, k), plan) in enumerate(zip(shapes, plans)):
+                assert "order=dynamic" in plan.describe()
+                p = _inputs(m, n, k, "bf16", "1N", seed=500 + 10 * rep + i, kind="int")
+                A, B, bias = p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev)
+                D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+                aux = torch.empty((m, (n + 31) // 32), dtype=torch.int32, device=dev)
+                plan.execute(A, B, bias, D, aux=aux)
+                assert plan.sync_status() == 0
+                want, _ = oracle_ref(p, "bf16", "RELU_AUX_BIAS", "1N")
+                assert np.array_equal(D.float().cpu().double().numpy(), want), (rep, i)
+    finally:
+        for plan in plans:
+            plan.free()
+
+
+def test_pair_dynamic_integer_bit_exact():
     m, n, k = 1024, 264, 64
     p = _inputs(m, n, k, "bf16", "1N", seed=172, kind="int")
-    check(p, m, n, k, "bf16", "RELU_AUX_BIAS", "1N", options={"VARIANT": 4}, exact=True)
+    check(p, m, n, k, "bf16", "RELU_AUX_BIAS", "1N", options={"VARIANT": 3, "TILE_ORDER": 2},
+          exact=True)
 
 
-@pytest.mark.parametrize("m,n,x2", [(65536, 16384, True), (8192, 16384, True), (4096, 4096, True),
-                                    (4096, 1024, False), (8192, 8192, True), (2048, 2048, False)])
-def test_pair_x2_automatic_choice(m, n, x2):
-    # two pairs per cluster once the double tiles fill two waves of the resident clusters
+@pytest.mark.parametrize("m,n", [(65536, 16384), (8192, 16384), (4096, 4096), (4096, 1024)])
+def test_pair_order_automatic_choice(m, n):
+    # CTA-pair plans hand out their tiles from the counter unless told otherwise
     with gemm_epi.Plan(m, n, 4096, "bf16", "RELU_BIAS", "1N") as plan:
         d = plan.describe()
-    assert ("variant=row-pair-x2" in d) == x2, d
+        assert "variant=row-pair " in d and "order=dynamic" in d, d
+        plan.set_option("TILE_ORDER", 1)
+        assert "order=static" in plan.describe()
 
 
-def test_pair_x2_option_rules():
+def test_pair_option_rules():
     with gemm_epi.Plan(1024, 1024, 1024, "e4m3", "RELU_BIAS", "1N") as plan:
-        with pytest.raises(gemm_epi.GemmEpiError) as e:
-            plan.set_option("VARIANT", 1)   # E4M3 plans run the CTA-pair kernel only
-        assert e.value.status == 1
-        plan.set_option("VARIANT", 4)
-        assert "variant=row-pair-x2" in plan.describe()
+        for v in (1, 2, 4):
+            with pytest.raises(gemm_epi.GemmEpiError) as e:
+                plan.set_option("VARIANT", v)   # E4M3 plans run the CTA-pair kernel only
+            assert e.value.status == 1
+        assert "variant=row-pair " in plan.describe()
     with gemm_epi.Plan(1024, 1024, 1024, "bf16", "RELU_BIAS", "1N") as plan:
-        plan.set_option("VARIANT", 4)
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.set_option("VARIANT", 4)       # no such kernel
+        assert e.value.status == 1
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.set_option("TILE_ORDER", 3)
+        assert e.value.status == 1
+        plan.set_option("VARIANT", 3)
         d = plan.describe()
-        assert "variant=row-pair-x2" in d and " grid=" in d
         grid = int(d.split(" grid=")[1].split()[0])
-        assert grid % 4 == 0
+        assert grid % 2 == 0 and "order=dynamic" in d
 
 
 @pytest.mark.parametrize("m,n,want", [(4096, 4096, 224), (8192, 16384, 256), (65536, 16384, 256),
@@ -693,14 +722,17 @@ def test_pair_integer_bit_exact():
     check(p, m, n, k, "bf16", "RELU_AUX_BIAS", "1N", options={"VARIANT": 3}, exact=True)
 
 
-@pytest.mark.parametrize("variant", [3, 4])
-def test_pair_timeout_path(variant):
-    m, n, k = 512, 256, 128
+@pytest.mark.parametrize("order", [1, 2])
+def test_pair_timeout_path(order):
+    # after a launch that ran out its wait limit, the next launch is correct (with the
+    # dynamic order: the aborted launch left the tile counter at zero)
+    m, n, k = 1024, 768, 128
     p = _inputs(m, n, k, "bf16", "1N", seed=73)
     dev = torch.device("cuda")
     A, B, bias = p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev)
     D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-    with gemm_epi.Plan(m, n, k, "bf16", "BIAS", "1N", variant=variant) as plan:
+    with gemm_epi.Plan(m, n, k, "bf16", "BIAS", "1N", variant=3, tile_order=order,
+                       grid=4) as plan:
         plan.set_option("WAIT_LIMIT_US", 20000)
         plan.set_option("DEBUG_STALL", 1)
         plan.execute(A, B, bias, D)
@@ -714,9 +746,10 @@ def test_pair_timeout_path(variant):
 
 
 def test_plans_run_concurrently_on_separate_streams():
-    # each plan owns its status word, workspace and tensor maps: different plans may run at
-    # the same time on different streams (a cluster-of-pairs plan, a small-m plan with a
-    # device-memory split and a row-tile plan split through a cluster)
+    # each plan owns its status word, tile counter, workspace and tensor maps: different
+    # plans may run at the same time on different streams (a CTA-pair plan with the dynamic
+    # tile order, a small-m plan with a device-memory split and a row-tile plan split
+    # through a cluster)
     from parity_helpers import oracle_ref
     dev = torch.device("cuda")
     cases = [(4096, 4096, 256, "RELU_AUX_BIAS", {}),

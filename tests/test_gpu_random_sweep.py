@@ -1,6 +1,6 @@
-"""A seeded random sweep over shapes, dtypes, epilogs, bias layouts and kernel variants, each
-case checked element by element against the CPU oracle (the fixed-shape tests cover the
-edges deliberately; this covers the combinations between them)."""
+"""A seeded random sweep over shapes, dtypes, epilogs, bias layouts, kernel variants and tile
+orders, each case checked element by element against the CPU oracle (the fixed-shape tests
+cover the edges deliberately; this covers the combinations between them)."""
 import random
 
 import numpy as np
@@ -26,13 +26,15 @@ def _built():
 
 def _case(i):
     r = random.Random(9000 + i)
-    variant = r.choice([0, 0, 1, 2, 3, 4])
+    variant = r.choice([0, 0, 1, 2, 3, 4])      # 4: the CTA-pair kernel, static tile order
     m = r.choice([1, 7, 64, 129, 200, 256]) if variant == 2 else r.randint(1, 700)
     n = 8 * r.randint(1, 90)
     k = 8 * r.randint(1, 80)
     opts = {}
     if variant:
-        opts["VARIANT"] = variant
+        opts["VARIANT"] = min(variant, 3)
+    if variant in (3, 4):
+        opts["TILE_ORDER"] = 2 if variant == 3 else 1
     if variant == 1:
         opts["TILE_N"] = r.choice([64, 128, 256])
     if variant in (3, 4):
