@@ -113,6 +113,58 @@ int pick_pair_bn(int64_t m, int64_t n, long long pairs)
     return w224 <= w256 ? 224 : 256;
 }
 
+// Small-m kernel configuration: rows-of-D tile bn (16, 32 or 64, at least m), `split` K
+// slices of kb 64-deep blocks each (a cluster of `split` CTAs per 128-column tile), copies of
+// B box_k rows deep, and the shared memory per CTA.  Takes the most slices whose CTAs all run
+// at once (one CTA per SM: the shared memory is padded so that two never share one, which
+// would halve the copy bandwidth each gets) and fit in shared memory; want_split > 0 asks for
+// that many (lowered, like the other kernels' splits, until no slice is empty).  False if no
+// configuration fits (k too long for one slab per CTA).
+struct SmallMCfg {
+    int bn, split, kb, box_k, smem;
+};
+constexpr int kSmallMMaxM = 64;
+constexpr int kSmallMMinSmem = 116 * 1024;
+constexpr int kSmemLimit = 227 * 1024;
+
+bool smallm_epilog(int e)
+{
+    return e == GEMM_EPI_BIAS || e == GEMM_EPI_RELU_BIAS || e == GEMM_EPI_GELU_BIAS ||
+           e == GEMM_EPI_RELU_AUX_BIAS || e == GEMM_EPI_BIAS_RESIDUAL || e == GEMM_EPI_NONE ||
+           e == GEMM_EPI_TANH_BIAS || e == GEMM_EPI_GELU_AUX_BIAS;
+}
+
+bool pick_smallm(int64_t m, int64_t n, int64_t k, int sms, int want_split, SmallMCfg* c)
+{
+    if (m < 1 || m > kSmallMMaxM || n < 1 || k < 1) return false;
+    c->bn = m <= 16 ? 16 : m <= 32 ? 32 : 64;
+    const int64_t tiles = (n + 127) / 128;
+    const int kblocks = static_cast<int>((k + 63) / 64);
+    const int top = want_split > 0 ? want_split : (kblocks < 8 ? kblocks : 8);
+    for (int s = top; s >= 1; --s) {
+        const int kb = (kblocks + s - 1) / s;
+        const int split = (kblocks + kb - 1) / kb;  // no empty slice
+        const int need = smallm_smem_bytes(c->bn, kb * 64, split);
+        if (need <= 0) continue;  // the split does not divide the rows: a smaller one
+        if (need > kSmemLimit) {
+            if (want_split > 0) return false;  // (fewer slices need more)
+            continue;
+        }
+        const int smem = need > kSmallMMinSmem ? need : kSmallMMinSmem;
+        if (want_split == 0 && split > 1) {
+            const int clusters = smallm_max_clusters(c->bn, split, smem);
+            if (clusters < 1 || tiles > clusters) continue;  // every cluster resident at once
+        }
+        c->split = split;
+        c->kb = kb;
+        c->smem = smem;
+        const int kc = kb * 64;
+        c->box_k = kc % 256 == 0 ? 256 : kc % 192 == 0 ? 192 : kc % 128 == 0 ? 128 : 64;
+        return true;
+    }
+    return false;
+}
+
 }  // namespace
 
 namespace gemm_epi_impl {
@@ -165,6 +217,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
     p->split_global = 0;
     p->dyn_order = 0;
     p->swap_m64 = 0;
+    p->box_k = 0;
     p->kb_per_split = 0;
     if (p->m == 0 || p->n == 0) {
         p->variant = kEmpty;
@@ -206,9 +259,15 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
                 v = kRowPair;
             else
                 v = kRowTile;
+            // m <= 64 with a forward epilog and a K slab that fits a CTA: the small-m kernel
+            SmallMCfg sc;
+            if (v == kSwapped && smallm_epilog(p->epilog) && p->opt_split_k == 0 &&
+                smallm_prepare() == cudaSuccess &&
+                pick_smallm(p->m, p->n, p->k, p->sm_count, 0, &sc))
+                v = kSmallM;
         }
-        // (option values: 1 row-tile, 2 swapped, 3 CTA pairs; the internal Variant codes
-        // differ)
+        // (option values: 1 row-tile, 2 swapped, 3 CTA pairs, 5 small-m; the internal
+        // Variant codes differ)
         if (p->opt_variant == 3) v = kRowPair;  // option value 3: the CTA-pair kernel
         if (v == kSwapped && p->m > kSwappedMaxM) return GEMM_EPI_ERR_INVALID_ARG;
         // the swapped kernel has no LayerNorm epilogue
@@ -237,6 +296,31 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             int gm = p->opt_group_m ? p->opt_group_m : 8;
             if (gm > p->tiles_m) gm = p->tiles_m;
             p->group_m = gm < 1 ? 1 : gm;
+        } else if (v == kSmallM) {
+            // one K slab per CTA, split over a cluster (the rows of D are one tile)
+            SmallMCfg sc;
+            if (smallm_prepare() != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
+            if (!smallm_epilog(p->epilog) || p->opt_split_k > 8 ||
+                (p->opt_bn && p->opt_bn != 16 && p->opt_bn != 32 && p->opt_bn != 64))
+                return GEMM_EPI_ERR_INVALID_ARG;
+            if (!pick_smallm(p->m, p->n, p->k, p->sm_count, p->opt_split_k, &sc))
+                return GEMM_EPI_ERR_INVALID_ARG;
+            if (p->opt_bn && p->opt_bn < sc.bn) return GEMM_EPI_ERR_INVALID_ARG;
+            if (p->opt_bn) sc.bn = p->opt_bn;
+            const int need = smallm_smem_bytes(sc.bn, sc.kb * 64, sc.split);
+            if (need > kSmemLimit) return GEMM_EPI_ERR_INVALID_ARG;
+            if (need > sc.smem) sc.smem = need;
+            p->bn = sc.bn;
+            p->tiles_m = static_cast<int>((p->n + 127) / 128);
+            p->tiles_n = static_cast<int>((p->m + sc.bn - 1) / sc.bn);
+            p->split = sc.split;
+            p->kb_per_split = sc.kb;
+            p->box_k = sc.box_k;
+            p->smem = sc.smem;
+            p->stages = 1;
+            const long long grid = static_cast<long long>(p->tiles_m) * p->tiles_n * sc.split;
+            if (grid > (1ll << 30)) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+            p->grid = static_cast<int>(grid);
         } else if (v == kRowTile) {
             if (p->opt_bn && p->opt_bn != 64 && p->opt_bn != 128 && p->opt_bn != 256)
                 return GEMM_EPI_ERR_INVALID_ARG;
@@ -309,10 +393,22 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
         if (gm > p->tiles_m) gm = p->tiles_m;
         p->group_m = gm < 1 ? 1 : gm;
     }
-    // CTA pairs take their tiles from the plan's device counter unless told otherwise (or
-    // the plan has none, as a plan on the caller's stack may not).
-    if (p->variant == kRowPair) p->dyn_order = p->opt_tile_order != 1 && p->d_sched != nullptr;
-    static const char* vname[] = {"empty", "row-tile", "swapped", "bias-only", "row-pair"};
+    // CTA pairs take their tiles from the plan's device counter on long walks (eight or more
+    // waves of tiles over the pairs), where a static order lets the pairs drift apart and
+    // lose the operand panels they share in L2; on a few waves the static order keeps the
+    // tiles per pair equal, where handing them out as pairs free up can give one pair a tile
+    // more than another.  Measured on GB300 (hot L2): 65536 x 16384 x 8192 (215 waves)
+    // 10.9 GB read and 8.98 ms dynamic against 26.4 GB and 9.89 ms static; 4096^3 (4 waves)
+    // 87.4 us dynamic against 86.0 static; FFN GEMM 1 4096 x 4096 x 1024 GELU (4 waves) 35.2
+    // against 32.4 us.  A plan on the caller's stack may have no counter: static.
+    if (p->variant == kRowPair) {
+        const long long tiles = static_cast<long long>(p->tiles_m) * p->tiles_n;
+        const long long pairs = p->grid / 2;
+        const bool want = p->opt_tile_order == 2 || (p->opt_tile_order == 0 && tiles >= 8 * pairs);
+        p->dyn_order = want && p->d_sched != nullptr;
+    }
+    static const char* vname[] = {"empty", "row-tile", "swapped", "bias-only", "row-pair",
+                                  "small-m"};
     static const char* ename[] = {"BIAS",          "RELU_BIAS",     "GELU_BIAS",
                                   "RELU_AUX_BIAS", "BIAS_RESIDUAL", "NONE",
                                   "TANH_BIAS",     "GELU_AUX_BIAS", "DRELU_BGRAD",
@@ -328,7 +424,8 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
              p->variant == kRowPair ? 256 : p->swap_m64 ? 64 : 128, p->bn,
              p->dtype == GEMM_EPI_E4M3 ? 128 : 64, p->stages, p->smem, p->tiles_m, p->tiles_n,
              p->k_blocks,
-             p->split, p->split > 1 ? (p->split_global ? "(device memory)" : "(cluster)") : "",
+             p->split,
+             p->split > 1 ? (p->split_global ? "(device memory)" : "(cluster)") : "",
              p->grid, p->group_m,
              p->variant != kRowPair ? "" : p->dyn_order ? " order=dynamic" : " order=static",
              p->sm_count);
@@ -383,6 +480,20 @@ gemm_epi_status ensure_maps(gemm_epi_plan_s* p, const void* A, const void* B, vo
     }
     const CUtensorMapDataType dt = p->dtype == GEMM_EPI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (p->variant == kSmallM) {
+        // A: K-major boxes {64 k, bn rows}; B: N-major boxes {64 n, box_k k}; D is stored
+        // without a map
+        if (!encode_2d(&p->tm_A, A, dt, p->k, p->m, 64, static_cast<uint32_t>(p->bn),
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&p->tm_B, B, dt, p->n, p->k, 64, static_cast<uint32_t>(p->box_k),
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+            return GEMM_EPI_ERR_LAUNCH;
+        p->key_A = A;
+        p->key_B = B;
+        p->key_D = D;
+        p->maps_valid = true;
+        return GEMM_EPI_OK;
+    }
     const bool rows_of_a = p->variant == kRowTile || p->variant == kRowPair;
     const uint32_t a_rows = rows_of_a ? 128u : static_cast<uint32_t>(p->bn);
     if (!encode_2d(&p->tm_A, A, dt, p->k, p->m, 64, a_rows, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -473,6 +584,7 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, in
     prm.split_count = p->d_split_count;
     prm.sched = p->dyn_order ? p->d_sched : nullptr;
     prm.swap_m64 = p->swap_m64;
+    prm.box_k = p->box_k;
     prm.prefetch = p->prefetch;
     cudaError_t e;
     if (p->variant == kRowPair && p->dtype == GEMM_EPI_E4M3)
@@ -481,6 +593,8 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, in
         e = rowpair_launch(p->bn, prm, p->grid, stream, pdl);
     else if (p->variant == kRowTile)
         e = rowtile_launch(p->bn, prm, p->grid, stream, pdl);
+    else if (p->variant == kSmallM)
+        e = smallm_launch(p->bn, prm, p->grid, p->smem, stream, pdl);
     else
         e = swapped_launch(p->bn, prm, p->grid, stream, pdl);
     if (e != cudaSuccess) {
@@ -668,7 +782,7 @@ gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt,
     gemm_epi_plan_s saved = *p;
     switch (opt) {
     case GEMM_EPI_OPT_VARIANT:
-        if (value < 0 || value > 3) return GEMM_EPI_ERR_INVALID_ARG;
+        if (value < 0 || value > 5 || value == 4) return GEMM_EPI_ERR_INVALID_ARG;
         p->opt_variant = static_cast<int>(value);
         break;
     case GEMM_EPI_OPT_TILE_N:

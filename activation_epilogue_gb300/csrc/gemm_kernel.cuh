@@ -515,15 +515,15 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
     grid_dependency_wait();
     const bool even = !PAIR || w.pair_rank == 0;
     const bool dyn = PAIR && even && p.sched != nullptr;
+    // A pair's even producer publishes tile j + 1 while it issues tile j's loads (after its
+    // third K block), so that the odd producer and the other roles never wait for it.
+    const bool publisher = PAIR && even;
     int tile = w.first;
+    int next = w.end;  // publisher: tile j + 1, published during tile j
     for (int j = 0; ok; ++j) {
         if (PAIR && j > 0) {
             if (even) {
-                if (!sched_publish(bar0, j, tile, abort_flag, p.wait_limit_ns)) {
-                    if (!*abort_flag) record_failure(p.status, abort_flag, kRoleProducer);
-                    ok = false;
-                    break;
-                }
+                tile = next;
             } else if (!sched_take(bar0, j, tile, abort_flag, p.wait_limit_ns)) {
                 if (!*abort_flag) record_failure(p.status, abort_flag, kRoleProducer);
                 ok = false;
@@ -531,9 +531,20 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
             }
         }
         if (tile >= w.end) break;
-        // The next tile: asked for now, its index is needed only after this tile's loads.
+        // The next tile: asked for now, its index is needed only a few K blocks later.
         unsigned ticket = 0;
         if (dyn) ticket = atomicAdd(p.sched, 1u);
+        bool published = !publisher;
+        auto publish_next = [&]() -> bool {
+            if (dyn) {
+                const long long nxt = static_cast<long long>(w.stride) + ticket;
+                next = nxt < w.end ? static_cast<int>(nxt) : w.end;
+            } else {
+                next = tile + w.stride < w.end ? tile + w.stride : w.end;
+            }
+            published = true;
+            return sched_publish(bar0, j + 1, next, abort_flag, p.wait_limit_ns);
+        };
         const TileInfo t = tile_info<FFN>(p, tile, w);
         if (FFN && t.prob == 1) {
             if (!wait_ffn_ready(p, t.tm, abort_flag)) {
@@ -543,7 +554,9 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
             }
             fence_proxy_async_global();
         }
-        for (int kb = (j == 0 ? w.kb_begin + pre : w.kb_begin); kb < t.kb_end; ++kb) {
+        const int kb0 = j == 0 ? w.kb_begin + pre : w.kb_begin;
+        const int kb_pub = kb0 + 2 < t.kb_end - 1 ? kb0 + 2 : t.kb_end - 1;
+        for (int kb = kb0; kb < t.kb_end; ++kb) {
             if (!wait_bounded(bar0 + 8u * (kBarEmpty + stage), phase ^ 1u, abort_flag,
                               p.wait_limit_ns)) {
                 if (!*abort_flag) record_failure(p.status, abort_flag, kRoleProducer);
@@ -558,13 +571,17 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
                 stage = 0;
                 phase ^= 1u;
             }
+            if (!published && kb == kb_pub && !publish_next()) {
+                if (!*abort_flag) record_failure(p.status, abort_flag, kRoleProducer);
+                ok = false;
+                break;
+            }
         }
-        if (dyn) {
-            const long long nxt = static_cast<long long>(w.stride) + ticket;
-            tile = nxt < w.end ? static_cast<int>(nxt) : w.end;
-        } else if (even) {
-            tile = tile + w.stride < w.end ? tile + w.stride : w.end;
+        if (ok && !published && !publish_next()) {  // (a tile without K blocks)
+            if (!*abort_flag) record_failure(p.status, abort_flag, kRoleProducer);
+            ok = false;
         }
+        if (!PAIR) tile = tile + w.stride < w.end ? tile + w.stride : w.end;
     }
     if (!ok && !(PAIR && w.pair_rank != 0)) {
         // Let the copies already issued land before the CTA can exit (in a pair, the even

@@ -106,6 +106,8 @@ struct GemmParams {
     // epilogue warp owns 16 columns of D.  Only for epilogs whose outputs are per element
     // (no mask words, no backward) and without a K split.
     int swap_m64;
+    // Small-m kernel: rows of k per copy of B (divides the K slice kb_per_split * 64).
+    int box_k;
     // The producer also prefetches into L2 the operand boxes of the K block this many
     // blocks ahead of the one it loads (0 = off), so that a first touch of a panel in
     // device memory overlaps the loads of the blocks before it.
@@ -137,6 +139,15 @@ cudaError_t swapped_prepare(int bn);
 cudaError_t swapped_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
 int swapped_smem_bytes(int bn);
 int swapped_stages(int bn);
+
+// Small-m kernel (m <= 64): 128 columns of D per CTA, K split over a cluster of `split` CTAs
+// (GemmParams::split, kb_per_split, box_k; tiles_m = column tiles, tiles_n = row tiles of bn);
+// grid = tiles_m * tiles_n * split.  smem: smallm_smem_bytes for the configuration.
+cudaError_t smallm_prepare();
+cudaError_t smallm_launch(int bn, const GemmParams& p, int grid, int smem, cudaStream_t stream,
+                          bool pdl);
+int smallm_smem_bytes(int bn, int kc, int split);
+int smallm_max_clusters(int bn, int split, int smem);
 
 // Row-tile kernel run by CTA pairs (cta_group::2): 256 x 256 tiles, clusters of 2.
 cudaError_t rowpair_prepare(int bn);

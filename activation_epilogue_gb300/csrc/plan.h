@@ -13,7 +13,7 @@
 
 namespace gemm_epi_impl {
 
-enum Variant { kEmpty = 0, kRowTile = 1, kSwapped = 2, kBiasOnly = 3, kRowPair = 4 };
+enum Variant { kEmpty = 0, kRowTile = 1, kSwapped = 2, kBiasOnly = 3, kRowPair = 4, kSmallM = 5 };
 
 constexpr int kSwappedMaxM = 256;
 // A plan's own device words: the status word (byte 0) and the tile counter (bytes 8-15).
@@ -36,6 +36,7 @@ struct gemm_epi_plan_s {
     int split_global;         // 1: the slices meet in device memory, 0: in a cluster
     int dyn_order;            // CTA-pair kernel: tiles handed out by the device counter
     int swap_m64;             // swapped kernel with 64 MMA rows (columns of D) per tile
+    int box_k;                // small-m kernel: rows of k per copy of B
     // options (0 = automatic)
     int opt_variant, opt_bn, opt_split_k, opt_grid, opt_group_m, opt_split_mode, opt_tile_m;
     int opt_tile_order;

@@ -432,6 +432,44 @@ def whole_job(secs: float, flops_per_step: float, steps: int, world: int, dist, 
     return secs, flops_per_step * steps * world / secs / 1e12
 
 
+def load_small_ncu():
+    """Per workload, the ncu kernel duration (cold caches) and DRAM bytes of the committed
+    summary of `bench.py --only small`, with the plan it was taken on."""
+    path = os.path.join(ROOT, "profiles", "small_shapes_ncu.json")
+    try:
+        with open(path) as fh:
+            return json.load(fh)
+    except Exception:
+        return {}
+
+
+def run_small_for_ncu(dev):
+    """Every workload but the headline, three calls each with L2 flushed before each: the
+    command an ncu capture of the small shapes' kernel durations runs."""
+    import torch
+
+    from activation_epilogue_gb300 import gemm_epi, workloads
+    flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    plans = {}
+    for name, g in workloads.GEMMS.items():
+        if name == HEADLINE:
+            continue
+        td = workloads.TORCH_DTYPES[g.dtype]
+        inp = workloads.gemm_inputs(g, device=dev)
+        Dg = torch.empty((g.m, g.n), dtype=td, device=dev)
+        auxg = (torch.empty((g.m, (g.n + 31) // 32), dtype=torch.int32, device=dev)
+                if g.epilog == "RELU_AUX_BIAS" else None)
+        with gemm_epi.Plan(g.m, g.n, g.k, g.dtype, g.epilog, g.bias_layout) as pg:
+            for _ in range(3):
+                flush_buf.zero_()
+                pg.execute(inp["A"], inp["B"], inp["bias"], Dg, aux=auxg)
+            torch.cuda.synchronize()
+            if pg.sync_status() != 0:
+                raise RuntimeError(f"{name}: device status {pg.sync_status()}")
+            plans[name] = pg.describe()
+    return plans
+
+
 def load_traffic(workload: str):
     """DRAM bytes per launch of the fused kernel from the committed ncu summary, if any."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -489,6 +527,9 @@ def measure_extras(plan, w, A, B, bias, D, aux, stream, peaks):
         flush_buf.zero_()
 
     per = {}
+    # ncu durations (cold caches) from the committed summary, used only when it was taken on
+    # the plan this run picks
+    small_ncu = load_small_ncu()
     for name, g in workloads.GEMMS.items():
         if name == w.name:
             continue
@@ -510,8 +551,13 @@ def measure_extras(plan, w, A, B, bias, D, aux, stream, peaks):
         e = 2
         unavoidable = (g.m * g.k + g.k * g.n + (g.m if g.bias_layout == "M1" else g.n)
                        + g.m * g.n) * e + (0 if auxg is None else auxg.numel() * 4)
+        rec = small_ncu.get(name, {})
+        ncu_us = rec.get("us") if rec.get("plan") == desc else None
         per[name] = {
             "us_per_call_cold_l2": cold * 1e6, "us_per_call_cold_l2_graph": cold_graph * 1e6,
+            "us_ncu_cold": ncu_us,
+            "hbm_frac_ncu": (unavoidable / (ncu_us * 1e-6) / 1e9 / peaks["hbm_gbs"]
+                             if ncu_us else None),
             "us_per_call_graph_hot_l2": hot * 1e6,
             "tflops_cold": g.flops / cold / 1e12,
             "hbm_gbs_cold": unavoidable / cold / 1e9,
@@ -678,7 +724,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--only", choices=["backward", "ffn", "fp8"],
+    ap.add_argument("--only", choices=["backward", "ffn", "fp8", "small"],
                     help="print only these measurements (one JSON object), for profiling")
     args = ap.parse_args(argv)
     if args.gpus < 1:
@@ -730,6 +776,8 @@ def rank_main(args):
         flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
         if args.only == "fp8":
             res = measure_fp8(dev, stream, load_peaks()[0])
+        elif args.only == "small":
+            res = run_small_for_ncu(dev)
         else:
             measure = measure_backward if args.only == "backward" else measure_ffn
             res = measure(dev, stream, flush_buf.zero_, load_peaks()[0])

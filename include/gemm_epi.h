@@ -136,8 +136,12 @@ typedef enum {
 /* Plan-time settings (gemm_epi_plan_set_option).  0 always means "automatic". */
 typedef enum {
     GEMM_EPI_OPT_VARIANT = 0,       /* 1 = row-tile kernel, 2 = swapped small-m kernel,
-                                       3 = row-tile kernel run by CTA pairs (256-row tiles);
-                                       E4M3 plans take 0 or 3 */
+                                       3 = row-tile kernel run by CTA pairs (256-row tiles),
+                                       5 = small-m kernel with the K split over a cluster
+                                       (m <= 64, forward epilogs, a K slab per CTA that
+                                       fits in shared memory; SPLIT_K sets its slices,
+                                       TILE_N its rows of D: 16, 32 or 64); E4M3 plans
+                                       take 0 or 3 */
     GEMM_EPI_OPT_TILE_N = 1,        /* N tile: 64, 128 or 256 for the row-tile kernel;
                                        224 or 256 for the CTA-pair kernel; 16, 32, 64, 128
                                        or 256 rows of D for the swapped kernel (a width
@@ -167,13 +171,14 @@ typedef enum {
                                        epilogs BIAS, RELU_BIAS, GELU_BIAS, NONE, TANH_BIAS,
                                        BIAS_RESIDUAL and GELU_AUX_BIAS, without a K split,
                                        else ERR_INVALID_ARG); the other kernels ignore it */
-    GEMM_EPI_OPT_TILE_ORDER = 11    /* CTA-pair kernel: 2 (the automatic choice) = each
-                                       pair takes its next tile, in raster order, from a
-                                       counter in the plan's device memory when it starts
-                                       one; 1 = static, pair q takes tiles q, q + pairs,
-                                       ...; the other kernels ignore it.  With 2 the plan's
-                                       launches must not overlap on the GPU (they share the
-                                       counter) */
+    GEMM_EPI_OPT_TILE_ORDER = 11    /* CTA-pair kernel: 2 = each pair takes its next tile,
+                                       in raster order, from a counter in the plan's device
+                                       memory as it goes (the automatic choice from eight
+                                       waves of tiles over the pairs up); 1 = static, pair q
+                                       takes tiles q, q + pairs, ... (the automatic choice
+                                       below that); the other kernels ignore it.  With 2 the
+                                       plan's launches must not overlap on the GPU (they
+                                       share the counter) */
 } gemm_epi_option;
 
 /*

@@ -154,8 +154,9 @@ int main(void)
 
     cudaStream_t stream;
     CHECK_CUDA(cudaStreamCreate(&stream));
-    /* swapped (small m), single-CTA row tiles with ragged edges, CTA pairs */
-    const int64_t shapes[][3] = {{16, 264, 72}, {300, 264, 136}, {2048, 2048, 200}};
+    /* small-m (K split over a cluster), swapped, single-CTA row tiles with ragged edges,
+       CTA pairs */
+    const int64_t shapes[][3] = {{16, 264, 72}, {100, 264, 72}, {300, 264, 136}, {2048, 2048, 200}};
     for (size_t s = 0; s < sizeof(shapes) / sizeof(shapes[0]); ++s)
         if (run_case(shapes[s][0], shapes[s][1], shapes[s][2], stream) != 0) return 1;
     CHECK_CUDA(cudaStreamDestroy(stream));

@@ -51,5 +51,5 @@ def test_c_caller_runs(tmp_path):
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.strip().endswith("ok"), r.stdout
     # the three kernels the shapes are meant to reach
-    for variant in ("variant=swapped", "variant=row-tile", "variant=row-pair"):
+    for variant in ("variant=small-m", "variant=swapped", "variant=row-tile", "variant=row-pair"):
         assert variant in r.stdout, r.stdout

@@ -95,11 +95,13 @@ def test_fp8_walk(order):
     _check(p, m, n, k, "RELU_AUX_BIAS", "1N", options={"GRID": 8, "TILE_ORDER": order})
 
 
-@pytest.mark.parametrize("m,n", [(65536, 16384), (4096, 4096), (1024, 1024)])
-def test_fp8_plan_is_a_pair_plan_with_dynamic_order(m, n):
+@pytest.mark.parametrize("m,n,order", [(65536, 16384, "dynamic"), (4096, 4096, "static"),
+                                       (1024, 1024, "static")])
+def test_fp8_plan_is_a_pair_plan(m, n, order):
+    # the tile counter from eight waves of tiles over the pairs up
     with gemm_epi.Plan(m, n, 8192, "e4m3", "RELU_BIAS", "1N") as plan:
         d = plan.describe()
-        assert "variant=row-pair " in d and "order=dynamic" in d
+        assert "variant=row-pair " in d and f"order={order}" in d, d
 
 
 @pytest.mark.parametrize("epilog", ["RELU_AUX_BIAS", "BIAS_RESIDUAL", "GELU_BIAS"])

@@ -96,10 +96,10 @@ def test_execute_host_rules():
 
 
 def test_execute_host_large_chunks_pair_kernel():
-    # 16 chunks of 1280 rows x 8192 columns: each chunk plan runs the CTA-pair kernel with
-    # the dynamic tile order (the chunk plans share the plan's tile counter, launching in
-    # turn on one stream); rows on and around chunk edges checked by the oracle, and the
-    # whole result against the same plan on device buffers (the same kernels)
+    # 16 chunks of 1280 rows x 8192 columns: each chunk plan runs the CTA-pair kernel (160
+    # tiles: the static order; the plan itself, on device buffers, 2560 tiles and the
+    # dynamic order); rows on and around chunk edges checked by the oracle, and the whole
+    # result against the same plan on device buffers
     m, n, k = 20480, 8192, 64
     p = workloads.random_problem(m, n, k, dtype="bf16", bias_layout="1N", residual=False,
                                  seed=2048)

@@ -62,6 +62,119 @@ def test_swapped_f16():
     check(p, m, n, k, "f16", "GELU_BIAS", "1N", options={"VARIANT": 2})
 
 
+# ---- small-m kernel: K split over a cluster, partial sums added in the leader CTA ---------
+
+@pytest.mark.parametrize("m", [1, 7, 16, 20, 33, 64])
+@pytest.mark.parametrize("epilog", EPILOGS)
+def test_smallm_parity(m, epilog):
+    n, k = 392, 1000                   # ragged column tile, 16 K blocks (last one 40 deep)
+    layout = "M1" if (m + EPILOGS.index(epilog)) % 2 else "1N"
+    dtype = "f16" if (m + EPILOGS.index(epilog)) % 3 == 0 else "bf16"
+    p = _inputs(m, n, k, dtype, layout, seed=2000 + m + 31 * EPILOGS.index(epilog))
+    _, _, _, _, desc = check(p, m, n, k, dtype, epilog, layout, options={"VARIANT": 5})
+    assert "variant=small-m" in desc, desc
+
+
+@pytest.mark.parametrize("split,effective", [(2, 2), (3, 2), (4, 4), (5, 4), (6, 4), (7, 4),
+                                             (8, 8)])
+def test_smallm_every_split(split, effective):
+    # 16 K blocks (the last one 40 deep) in slices of 8, 4 or 2 blocks; each rank owns
+    # 32 / split rows of D (a multiple of 4), so other splits are lowered to the next one
+    m, n, k = 24, 776, 1000
+    p = _inputs(m, n, k, "bf16", "1N", seed=2100 + split)
+    _, _, _, _, desc = check(p, m, n, k, "bf16", "GELU_BIAS", "1N",
+                             options={"VARIANT": 5, "SPLIT_K": split})
+    assert f"split_k={effective}(cluster)" in desc, desc
+
+
+@pytest.mark.parametrize("bn", [16, 32, 64])
+def test_smallm_row_tile_widths(bn):
+    m, n, k = 12, 264, 200
+    p = _inputs(m, n, k, "bf16", "M1", seed=2200 + bn)
+    _, _, _, _, desc = check(p, m, n, k, "bf16", "RELU_AUX_BIAS", "M1",
+                             options={"VARIANT": 5, "TILE_N": bn})
+    assert f"tile=128x{bn} " in desc, desc
+
+
+@pytest.mark.parametrize("epilog", ["BIAS", "RELU_BIAS", "RELU_AUX_BIAS", "BIAS_RESIDUAL", "NONE"])
+def test_smallm_integer_bit_exact(epilog):
+    m, n, k = 40, 520, 512             # 8 K blocks over a cluster: exact fp32 partial sums
+    p = _inputs(m, n, k, "bf16", "1N", seed=2300, kind="int")
+    check(p, m, n, k, "bf16", epilog, "1N", options={"VARIANT": 5}, exact=True)
+
+
+@pytest.mark.parametrize("t", [16, 64])
+def test_smallm_workload_shape_deterministic(t):
+    # the GELU workload shape: repeated calls give the same bits (the partial sums are added
+    # in slice order, whichever CTA stores first)
+    m, n, k = t, 3072, 768
+    p = _inputs(m, n, k, "bf16", "1N", seed=3000 + t)
+    dev = torch.device("cuda")
+    A, B, bias = p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev)
+    outs = []
+    with gemm_epi.Plan(m, n, k, "bf16", "GELU_BIAS", "1N") as plan:
+        assert "variant=small-m" in plan.describe()
+        for _ in range(3):
+            D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+            plan.execute(A, B, bias, D)
+            outs.append(D.cpu())
+        assert plan.sync_status() == 0
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+    from parity_helpers import oracle_ref
+    want, _ = oracle_ref(p, "bf16", "GELU_BIAS", "1N")
+    assert rel_err(outs[0], want) <= TOL["bf16"]
+
+
+def test_smallm_option_rules():
+    with gemm_epi.Plan(16, 264, 136, "bf16", "DRELU_BGRAD", "1N") as plan:
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.set_option("VARIANT", 5)     # no backward epilogue in the small-m kernel
+        assert e.value.status == 1
+    with gemm_epi.Plan(100, 264, 136, "bf16", "BIAS", "1N") as plan:
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.set_option("VARIANT", 5)     # m > 64
+        assert e.value.status == 1
+    with gemm_epi.Plan(16, 264, 136, "bf16", "BIAS", "1N", variant=5) as plan:
+        plan.set_option("SPLIT_K", 4)         # 3 K blocks, 16 rows: lowered to 2 slices
+        assert "variant=small-m" in plan.describe() and "split_k=2(cluster)" in plan.describe()
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.set_option("TILE_N", 8)
+        assert e.value.status == 1
+        assert "split_k=2(cluster)" in plan.describe()  # previous configuration kept
+    with gemm_epi.Plan(16, 264, 1024, "bf16", "BIAS", "1N", variant=5) as plan:
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.set_option("SPLIT_K", 1)     # one 1024-deep slab per CTA does not fit
+        assert e.value.status == 1
+    with gemm_epi.Plan(16, 264, 16384, "bf16", "BIAS", "1N") as plan:
+        # K slabs of 2048 do not fit in shared memory: the swapped kernel
+        assert "variant=swapped" in plan.describe()
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            plan.set_option("VARIANT", 5)
+        assert e.value.status == 1
+
+
+def test_smallm_timeout_path():
+    # a launch whose copies never arrive runs out the wait limit and reports it; the next
+    # launch of the same plan is correct
+    m, n, k = 16, 520, 512
+    p = _inputs(m, n, k, "bf16", "1N", seed=2400)
+    dev = torch.device("cuda")
+    A, B, bias = p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev)
+    D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    with gemm_epi.Plan(m, n, k, "bf16", "BIAS", "1N", variant=5) as plan:
+        assert "split_k=" in plan.describe() and "split_k=1 " not in plan.describe()
+        plan.set_option("WAIT_LIMIT_US", 20000)
+        plan.set_option("DEBUG_STALL", 1)
+        plan.execute(A, B, bias, D)
+        assert plan.sync_status() == 8
+        plan.set_option("DEBUG_STALL", 0)
+        plan.execute(A, B, bias, D)
+        assert plan.sync_status() == 0
+    from parity_helpers import oracle_ref
+    want, _ = oracle_ref(p, "bf16", "BIAS", "1N")
+    assert rel_err(D, want) <= TOL["bf16"]
+
+
 # ---- integer inputs: every correct result is bit-exact ------------------------------------
 
 @pytest.mark.parametrize("variant", [1, 2])
@@ -447,7 +560,8 @@ def test_swapped_narrow_tiles(m, bn, epilog):
 
 @pytest.mark.parametrize("m", [1, 16, 64, 100, 256])
 def test_small_m_tile_width_choice(m):
-    # the narrowest power-of-two tile (>= 16 rows) whose tiles all get their own SM
+    # the swapped kernel takes the narrowest power-of-two tile (>= 16 rows) whose tiles all
+    # get their own SM
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     n = 3072
     full = 16
@@ -458,7 +572,7 @@ def test_small_m_tile_width_choice(m):
         if bn < full and (n // 128) * -(-m // bn) <= sms:
             want = bn
             break
-    with gemm_epi.Plan(m, n, 768, "bf16", "GELU_BIAS", "1N") as plan:
+    with gemm_epi.Plan(m, n, 768, "bf16", "GELU_BIAS", "1N", variant=2) as plan:
         assert f"tile=128x{want}" in plan.describe(), plan.describe()
 
 
@@ -491,7 +605,7 @@ def test_swapped_m64_integer_bit_exact(epilog):
 
 
 def test_swapped_m64_only_on_request():
-    with gemm_epi.Plan(16, 3072, 768, "bf16", "GELU_BIAS", "1N") as plan:
+    with gemm_epi.Plan(16, 3072, 768, "bf16", "GELU_BIAS", "1N", variant=2) as plan:
         assert "variant=swapped tile=128x16" in plan.describe(), plan.describe()
         plan.set_option("TILE_M", 64)
         assert "variant=swapped tile=64x16" in plan.describe(), plan.describe()
@@ -527,13 +641,25 @@ def test_row_tiles_over_long_k_split_in_a_cluster():
     check(p, 1024, 512, 2048, "f16", "BIAS", "M1")
 
 
-def test_small_m_plans_swapped_without_split():
-    # split-K is measured slower than the unsplit swapped kernel on these shapes
-    with gemm_epi.Plan(16, 3072, 768, "bf16", "GELU_BIAS", "1N") as plan:
+@pytest.mark.parametrize("m,epilog,variant", [
+    (16, "GELU_BIAS", "small-m"), (64, "GELU_BIAS", "small-m"), (1, "RELU_AUX_BIAS", "small-m"),
+    (256, "GELU_BIAS", "swapped"), (16, "DRELU_BGRAD", "swapped"), (100, "BIAS", "swapped")])
+def test_small_m_plan_choice(m, epilog, variant):
+    # m <= 64 with a forward epilog: the small-m kernel, K split over a cluster so that its
+    # 24 column tiles x the slices occupy most SMs, every cluster resident at once; larger m
+    # and the backward epilogs: the swapped kernel, unsplit (a split through the swapped
+    # kernel's ring measured slower)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    with gemm_epi.Plan(m, 3072, 768, "bf16", epilog, "1N") as plan:
         desc = plan.describe()
     fields = dict(kv.split("=") for kv in desc.split() if "=" in kv)
-    assert fields["variant"] == "swapped", desc
-    assert fields["split_k"] == "1", desc
+    assert fields["variant"] == variant, desc
+    if variant == "swapped":
+        assert fields["split_k"] == "1", desc
+    else:
+        split = int(fields["split_k"].split("(")[0])
+        assert split >= 2 and fields["split_k"].endswith("(cluster)"), desc
+        assert int(fields["grid"]) == 24 * split <= sms, desc
 
 
 @pytest.mark.parametrize("variant", [1, 2])
@@ -636,8 +762,8 @@ def test_pair_dynamic_counter_back_at_zero_between_launches():
     from parity_helpers import oracle_ref
     dev = torch.device("cuda")
     shapes = [(1536, 776, 136), (768, 1288, 72)]
-    plans = [gemm_epi.Plan(m, n, k, "bf16", "RELU_AUX_BIAS", "1N", variant=3, grid=10)
-             for m, n, k in shapes]
+    plans = [gemm_epi.Plan(m, n, k, "bf16", "RELU_AUX_BIAS", "1N", variant=3, grid=10,
+                           tile_order=2) for m, n, k in shapes]
     try:
         for rep in range(4):
             for i, ((m, n, k), plan) in enumerate(zip(shapes, plans)):
@@ -662,14 +788,18 @@ def test_pair_dynamic_integer_bit_exact():
           exact=True)
 
 
-@pytest.mark.parametrize("m,n", [(65536, 16384), (8192, 16384), (4096, 4096), (4096, 1024)])
-def test_pair_order_automatic_choice(m, n):
-    # CTA-pair plans hand out their tiles from the counter unless told otherwise
+@pytest.mark.parametrize("m,n,order", [(65536, 16384, "dynamic"), (8192, 16384, "dynamic"),
+                                       (4096, 4096, "static"), (4096, 1024, "static")])
+def test_pair_order_automatic_choice(m, n, order):
+    # CTA-pair plans hand out their tiles from the counter from eight waves of tiles over
+    # the pairs up, and in the static order below that; the option overrides either way
     with gemm_epi.Plan(m, n, 4096, "bf16", "RELU_BIAS", "1N") as plan:
         d = plan.describe()
-        assert "variant=row-pair " in d and "order=dynamic" in d, d
+        assert "variant=row-pair " in d and f"order={order}" in d, d
         plan.set_option("TILE_ORDER", 1)
         assert "order=static" in plan.describe()
+        plan.set_option("TILE_ORDER", 2)
+        assert "order=dynamic" in plan.describe()
 
 
 def test_pair_option_rules():
@@ -689,7 +819,7 @@ def test_pair_option_rules():
         plan.set_option("VARIANT", 3)
         d = plan.describe()
         grid = int(d.split(" grid=")[1].split()[0])
-        assert grid % 2 == 0 and "order=dynamic" in d
+        assert grid % 2 == 0 and "order=static" in d      # 16 tiles: one wave
 
 
 @pytest.mark.parametrize("m,n,want", [(4096, 4096, 224), (8192, 16384, 256), (65536, 16384, 256),
