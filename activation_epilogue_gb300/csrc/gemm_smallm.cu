@@ -155,12 +155,27 @@ __global__ void __launch_bounds__(kSmThreads, 1) smallm_kernel(const __grid_cons
                  "+l"(pres), "+l"(pD), "+l"(paux));
 
     if (threadIdx.x == 0) {
-        prefetch_tensormap(&p.tm_A);
-        prefetch_tensormap(&p.tm_B);
         mbar_init(bar0 + 8u * kSmBarFull, 1);
         mbar_init(bar0 + 8u * kSmBarMma, 1);
         mbar_init(bar0 + 8u * kSmBarPart, 1);
         fence_mbar_init();
+        // The copies first: everything else of the set-up overlaps their flight.
+        // (debug_stall: no copy is issued, so the wait below runs out its time limit)
+        if (!p.debug_stall) {
+            // Under a programmatic dependent launch the operands may come from the previous grid.
+            grid_dependency_wait();
+            const uint32_t full = bar0 + 8u * kSmBarFull;
+            mbar_arrive_expect_tx(full, static_cast<uint32_t>(L.b_bytes() + L.a_bytes()));
+            // B: two 64-column panels of kc rows (k), in boxes of box_k rows (box_k divides kc)
+            const int boxk = p.box_k;
+            for (int pnl = 0; pnl < 2; ++pnl)
+                for (int kk = 0; kk < kc; kk += boxk)
+                    tma_load_2d(b_smem + static_cast<uint32_t>(pnl * kc * 128 + kk * 128), &p.tm_B,
+                                full, n0 + pnl * 64, k0 + kk);
+            // A: kc / 64 boxes of BN rows x 64 k
+            for (int b = 0; b < kc / 64; ++b)
+                tma_load_2d(a_smem + static_cast<uint32_t>(b * BN * 128), &p.tm_A, full, k0 + b * 64, t0);
+        }
         // every peer's partial sums of this rank's rows, on one barrier
         if (S > 1) mbar_arrive_expect_tx(bar0 + 8u * kSmBarPart, static_cast<uint32_t>(L.part_bytes()));
     }
@@ -171,22 +186,6 @@ __global__ void __launch_bounds__(kSmThreads, 1) smallm_kernel(const __grid_cons
     // Cluster barrier: every CTA of the cluster has started, its barriers initialised (its
     // shared memory may be written); waited at only just before the first remote store.
     if (S > 1) cluster_arrive_relaxed();
-    if (threadIdx.x == 0 && !p.debug_stall) {
-        // (debug_stall: no copy is issued, so the wait below runs out its time limit)
-        // Under a programmatic dependent launch the operands may come from the previous grid.
-        grid_dependency_wait();
-        const uint32_t full = bar0 + 8u * kSmBarFull;
-        mbar_arrive_expect_tx(full, static_cast<uint32_t>(L.b_bytes() + L.a_bytes()));
-        // B: two 64-column panels of kc rows (k), in boxes of box_k rows (box_k divides kc)
-        const int boxk = p.box_k;
-        for (int pnl = 0; pnl < 2; ++pnl)
-            for (int kk = 0; kk < kc; kk += boxk)
-                tma_load_2d(b_smem + static_cast<uint32_t>(pnl * kc * 128 + kk * 128), &p.tm_B, full,
-                            n0 + pnl * 64, k0 + kk);
-        // A: kc / 64 boxes of BN rows x 64 k
-        for (int b = 0; b < kc / 64; ++b)
-            tma_load_2d(a_smem + static_cast<uint32_t>(b * BN * 128), &p.tm_A, full, k0 + b * 64, t0);
-    }
     tcgen05_fence_before_sync();
     __syncthreads();
     tcgen05_fence_after_sync();
