@@ -24,8 +24,17 @@ struct gemm_epi_ffn_plan_s {
     float* stats;
     // one-launch mode: both GEMMs in one CTA-pair kernel (256 x 256 tiles)
     int opt_launches;  // GEMM_EPI_FFN_OPT_LAUNCHES value (0 = automatic)
+    int opt_split2;    // GEMM_EPI_FFN_OPT_SPLIT2 value
+    int opt_order;     // GEMM_EPI_FFN_OPT_TILE_ORDER value
     bool one_launch;   // the mode in use
-    int* ready;        // per 256-row block of H: epilogue warps done with it
+    // per (256-row block of H, GEMM-2 K slice): epilogue warps done with it; then the
+    // GEMM-2 slice counts (per tile, CTA of the pair and epilogue warp), zeroed together
+    int* ready;
+    size_t ready_bytes;
+    int split2, kb2;   // GEMM-2 K slices and K blocks per slice
+    float* ws;         // the slices' fp32 partial sums (split2 > 1)
+    size_t ws_bytes;
+    bool dynamic;      // one launch: units from the device counter
     int tiles_m, tiles_n1, tiles_n2, grid;
     const void* key_X;
     const void* key_W1;
@@ -53,6 +62,20 @@ bool pick_one_launch(const gemm_epi_ffn_plan_s* p, long long pairs)
     return tiles >= 6 * pairs;
 }
 
+// K blocks per GEMM-2 slice for `want` slices of k_blocks2 (whole 256-column tiles of H).
+// Splitting is never automatic: each slice's fp32 partial sums (128 KiB per CTA) go out to
+// L2 and the last slice reads all of them back, on the same per-SM path that feeds the
+// MMAs their operands.  Measured on GB300 (bf16, hot L2, dynamic order), 4096 x 1024 x 4096:
+// 94 us in 4 slices against 66 us unsplit (a copy-out took 3.0 us per unit, the last
+// slice's read-back and epilogue 8.7 us, and the epilogue warps fell behind the MMAs);
+// 8192 x 1024 x 4096: 173 against 104 us; 512 x 1024 x 4096: 39 against 43 us, but two
+// launches take 31 us there.
+int slice_kblocks(int k_blocks2, int want)
+{
+    const int kb = (k_blocks2 + want - 1) / want;
+    return (kb + 3) / 4 * 4;
+}
+
 gemm_epi_status configure_ffn(gemm_epi_ffn_plan_s* p)
 {
     p->maps_valid = false;
@@ -70,24 +93,64 @@ gemm_epi_status configure_ffn(gemm_epi_ffn_plan_s* p)
         return GEMM_EPI_ERR_LAUNCH;
     long long pairs = rowpair_max_clusters(256);
     if (pairs > p->g1->sm_count / 2) pairs = p->g1->sm_count / 2;
-    p->one_launch = p->t > 0 && p->d > 0 && p->f > 0 && pick_one_launch(p, pairs);
+    const int k_blocks2 = static_cast<int>((p->f + 63) / 64);
+    const bool shape_ok = p->t > 0 && p->d > 0 && p->f > 0;
+    const int want2 = p->opt_split2 > 1 ? p->opt_split2 : 1;
+    p->kb2 = want2 > 1 ? slice_kblocks(k_blocks2, want2) : k_blocks2;
+    p->split2 = shape_ok ? (k_blocks2 + p->kb2 - 1) / p->kb2 : 1;
+    if (p->split2 <= 1) {
+        p->split2 = 1;
+        p->kb2 = k_blocks2;
+    }
+    p->one_launch = shape_ok && pick_one_launch(p, pairs);
     if (p->one_launch) {
-        const long long tiles = static_cast<long long>(p->tiles_m) * (p->tiles_n1 + p->tiles_n2);
-        if (pairs > tiles) pairs = tiles;
+        const long long tiles2 = static_cast<long long>(p->tiles_m) * p->tiles_n2;
+        const long long units = static_cast<long long>(p->tiles_m) * p->tiles_n1 + tiles2 * p->split2;
+        if (pairs > units) pairs = units;
         if (pairs < 1) return GEMM_EPI_ERR_LAUNCH;
         p->grid = static_cast<int>(2 * pairs);
-        if (!p->ready && cudaMalloc(reinterpret_cast<void**>(&p->ready),
-                                    sizeof(int) * static_cast<size_t>(p->tiles_m)) != cudaSuccess) {
-            cudaGetLastError();
+        // automatic: static (units of equal size in order; the dynamic order measured 1-4 us
+        // slower unsplit), dynamic when GEMM 2 is split
+        p->dynamic = p->g1->d_sched != nullptr &&
+                     (p->opt_order == 2 || (p->opt_order == 0 && p->split2 > 1));
+        // counters: ready (row block x slice), then the slice counts (tile x CTA x warp)
+        const size_t ready_bytes =
+            sizeof(int) * static_cast<size_t>(p->tiles_m) * static_cast<size_t>(p->split2) +
+            (p->split2 > 1 ? sizeof(unsigned) * static_cast<size_t>(tiles2) * 2 * kEpilogueWarps : 0);
+        if (p->ready && p->ready_bytes < ready_bytes) {
+            cudaFree(p->ready);
             p->ready = nullptr;
-            return GEMM_EPI_ERR_ALLOC;
+        }
+        if (!p->ready) {
+            if (cudaMalloc(reinterpret_cast<void**>(&p->ready), ready_bytes) != cudaSuccess) {
+                cudaGetLastError();
+                p->ready = nullptr;
+                p->ready_bytes = 0;
+                return GEMM_EPI_ERR_ALLOC;
+            }
+            p->ready_bytes = ready_bytes;
+        }
+        const size_t ws_bytes = p->split2 > 1 ? static_cast<size_t>(tiles2) * p->split2 * 2 * 128 * 256 * 4 : 0;
+        if (p->ws && p->ws_bytes < ws_bytes) {
+            cudaFree(p->ws);
+            p->ws = nullptr;
+            p->ws_bytes = 0;
+        }
+        if (ws_bytes && !p->ws) {
+            if (cudaMalloc(reinterpret_cast<void**>(&p->ws), ws_bytes) != cudaSuccess) {
+                cudaGetLastError();
+                p->ws = nullptr;
+                return GEMM_EPI_ERR_ALLOC;
+            }
+            p->ws_bytes = ws_bytes;
         }
         snprintf(p->desc, sizeof(p->desc),
                  "one launch: t=%lld d=%lld f=%lld, CTA pairs on 256x256 tiles: %dx%d GEMM-1 tiles "
-                 "then %dx%d GEMM-2 tiles, grid=%d",
+                 "then %dx%d GEMM-2 tiles in %d K slice%s of %d blocks, grid=%d order=%s",
                  static_cast<long long>(p->t), static_cast<long long>(p->d),
                  static_cast<long long>(p->f), p->tiles_m, p->tiles_n1, p->tiles_m, p->tiles_n2,
-                 p->grid);
+                 p->split2, p->split2 > 1 ? "s" : "", p->kb2, p->grid,
+                 p->dynamic ? "dynamic" : "static");
     } else {
         snprintf(p->desc, sizeof(p->desc), "two launches: [%s] then [%s]", p->g1->desc,
                  p->g2->desc);
@@ -127,8 +190,7 @@ gemm_epi_status run_ffn_one_launch(gemm_epi_ffn_plan_s* p, const void* X, const 
 {
     gemm_epi_status st = ensure_ffn_maps(p, X, W1, W2, Y);
     if (st != GEMM_EPI_OK) return st;
-    if (cudaMemsetAsync(p->ready, 0, sizeof(int) * static_cast<size_t>(p->tiles_m), stream) !=
-        cudaSuccess)
+    if (cudaMemsetAsync(p->ready, 0, p->ready_bytes, stream) != cudaSuccess)
         return GEMM_EPI_ERR_LAUNCH;
     const gemm_epi_plan_s* g1 = p->g1;
     GemmParams prm;
@@ -139,7 +201,7 @@ gemm_epi_status run_ffn_one_launch(gemm_epi_ffn_plan_s* p, const void* X, const 
     prm.bias = b1;
     prm.D = p->H;
     prm.status = g1->d_status;
-    prm.sched = g1->dyn_order ? g1->d_sched : nullptr;
+    prm.sched = p->dynamic ? g1->d_sched : nullptr;
     prm.wait_limit_ns = g1->wait_limit_ns;
     prm.m = static_cast<int>(p->t);
     prm.n = static_cast<int>(p->f);
@@ -160,11 +222,16 @@ gemm_epi_status run_ffn_one_launch(gemm_epi_ffn_plan_s* p, const void* X, const 
     prm.bias2 = b2;
     prm.residual2 = R;
     prm.ffn_ready = p->ready;
-    prm.ffn_ready_target = p->tiles_n1 * 2 * kEpilogueWarps;
-    prm.ffn_tiles2 = p->tiles_m * p->tiles_n2;
+    prm.ffn_ready_target = 2 * kEpilogueWarps;
+    prm.ffn_tiles2 = p->tiles_m * p->tiles_n2 * p->split2;
     prm.n2 = static_cast<int>(p->d);
     prm.tiles_n2 = p->tiles_n2;
     prm.k_blocks2 = static_cast<int>((p->f + 63) / 64);
+    prm.ffn_split2 = p->split2;
+    prm.ffn_kb2 = p->kb2;
+    prm.ffn_ws = p->ws;
+    prm.ffn_count = p->split2 > 1 ? reinterpret_cast<unsigned*>(p->ready + static_cast<size_t>(p->tiles_m) * p->split2)
+                                  : nullptr;
     const cudaError_t e = ffn_pair_launch(prm, p->grid, stream);
     if (e != cudaSuccess) {
         const char* log = getenv("GEMM_EPI_LOG");
@@ -206,6 +273,9 @@ gemm_epi_status make_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d, in
     p->g2 = g2;
     p->H = nullptr;
     p->ready = nullptr;
+    p->ready_bytes = 0;
+    p->ws = nullptr;
+    p->ws_bytes = 0;
     p->stats = nullptr;
     p->layernorm = layernorm;
     if (t > 0 && f > 0) {
@@ -282,12 +352,27 @@ gemm_epi_status gemm_epi_ffn_set_option(gemm_epi_ffn_plan_t p, gemm_epi_ffn_opti
                                         int64_t value)
 {
     if (!p) return GEMM_EPI_ERR_INVALID_ARG;
-    if (opt != GEMM_EPI_FFN_OPT_LAUNCHES || value < 0 || value > 2) return GEMM_EPI_ERR_INVALID_ARG;
-    const int saved = p->opt_launches;
-    p->opt_launches = static_cast<int>(value);
+    int* field = nullptr;
+    switch (opt) {
+    case GEMM_EPI_FFN_OPT_LAUNCHES:
+        if (value < 0 || value > 2) return GEMM_EPI_ERR_INVALID_ARG;
+        field = &p->opt_launches;
+        break;
+    case GEMM_EPI_FFN_OPT_SPLIT2:
+        if (!(value == 0 || value == 1 || value == 2 || value == 4)) return GEMM_EPI_ERR_INVALID_ARG;
+        field = &p->opt_split2;
+        break;
+    case GEMM_EPI_FFN_OPT_TILE_ORDER:
+        if (value < 0 || value > 2) return GEMM_EPI_ERR_INVALID_ARG;
+        field = &p->opt_order;
+        break;
+    default: return GEMM_EPI_ERR_INVALID_ARG;
+    }
+    const int saved = *field;
+    *field = static_cast<int>(value);
     gemm_epi_status st = configure_ffn(p);
     if (st != GEMM_EPI_OK) {
-        p->opt_launches = saved;
+        *field = saved;
         configure_ffn(p);
     }
     return st;
@@ -331,6 +416,7 @@ gemm_epi_status gemm_epi_ffn_free(gemm_epi_ffn_plan_t p)
     if (!p) return GEMM_EPI_OK;
     if (p->H) cudaFree(p->H);
     if (p->ready) cudaFree(p->ready);
+    if (p->ws) cudaFree(p->ws);
     if (p->stats) cudaFree(p->stats);
     gemm_epi_free(p->g1);
     gemm_epi_free(p->g2);

@@ -233,9 +233,9 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
 __device__ __forceinline__ int split_owner(int q, int c, int split) { return (4 * c + q) % split; }
 
 // One tile of the walk: which GEMM (0, or 1 = the second GEMM of a fused FFN block), its
-// coordinates and its last K block.
+// coordinates, its K blocks [kb_begin, kb_end) and (second GEMM) its K slice.
 struct TileInfo {
-    int prob, tm, tn, kb_end;
+    int prob, tm, tn, kb_begin, kb_end, slice, tile2;
 };
 
 template <bool FFN>
@@ -246,31 +246,57 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int tile, con
     if (!FFN || tile < tiles1) {
         tile_coords(tile, p, t.tm, t.tn);
         t.prob = 0;
+        t.kb_begin = w.kb_begin;
         t.kb_end = w.kb_end;
+        t.slice = 0;
+        t.tile2 = 0;
     } else {
-        // GEMM 2 in row order: the row blocks of H finish roughly in that order
+        // GEMM 2 in row order (the row blocks of H finish roughly in that order), the K
+        // slices of a tile next to each other
         const int u = tile - tiles1;
-        t.tm = u / p.tiles_n2;
-        t.tn = u - t.tm * p.tiles_n2;
+        t.tile2 = u / p.ffn_split2;
+        t.slice = u - t.tile2 * p.ffn_split2;
+        t.tm = t.tile2 / p.tiles_n2;
+        t.tn = t.tile2 - t.tm * p.tiles_n2;
         t.prob = 1;
-        t.kb_end = p.k_blocks2;
+        t.kb_begin = t.slice * p.ffn_kb2;
+        t.kb_end = min(p.k_blocks2, t.kb_begin + p.ffn_kb2);
     }
     return t;
 }
 
-// FFN: wait until the row block of H a GEMM-2 tile reads is complete (bounded like the
+// FFN: the counter of H's row block tm and GEMM-2 K slice s, and the count that means "all
+// of it stored": GEMM-1 tile tn (columns [256 tn, 256 tn + 256) of H, GEMM-2 K blocks
+// [4 tn, 4 tn + 4)) lies in slice 4 tn / ffn_kb2.
+__device__ __forceinline__ int ffn_ready_index(const GemmParams& p, int tm, int s)
+{
+    return tm * p.ffn_split2 + s;
+}
+__device__ __forceinline__ int ffn_slice_of_tile1(const GemmParams& p, int tn)
+{
+    return 4 * tn / p.ffn_kb2;
+}
+__device__ __forceinline__ int ffn_ready_count(const GemmParams& p, int s)
+{
+    const int lo = (s * p.ffn_kb2 + 3) / 4;
+    const int hi = min(p.tiles_n, ((s + 1) * p.ffn_kb2 + 3) / 4);
+    return p.ffn_ready_target * (hi - lo);
+}
+
+// FFN: wait until the slice of H a GEMM-2 unit reads is complete (bounded like the
 // mbarrier waits; false on abort or time-out).  The acquire load orders the TMA loads that
 // follow (after a proxy fence) behind the GEMM-1 stores it observes.
-__device__ __forceinline__ bool wait_ffn_ready(const GemmParams& p, int tm,
+__device__ __forceinline__ bool wait_ffn_ready(const GemmParams& p, int tm, int s,
                                                const volatile int* abort_flag)
 {
-    const int* flag = p.ffn_ready + tm;
-    if (ld_acquire_gpu(flag) >= p.ffn_ready_target) return true;
+    const int* flag = p.ffn_ready + ffn_ready_index(p, tm, s);
+    const int target = ffn_ready_count(p, s);
+    if (ld_acquire_gpu(flag) >= target) return true;
     const uint64_t t0 = globaltimer_ns();
     const unsigned long long max_polls = p.wait_limit_ns / 32 + 1024;
     for (unsigned long long poll = 1; poll < max_polls; ++poll) {
         __nanosleep(32);
-        if (ld_acquire_gpu(flag) >= p.ffn_ready_target) return true;
+        if (ld_acquire_gpu(flag) >= target) return true;
         if ((poll & 15) == 0) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > p.wait_limit_ns) return false;
@@ -547,14 +573,14 @@ __device__ __forceinline__ void run_producer(const GemmParams& p, uint32_t sbase
         };
         const TileInfo t = tile_info<FFN>(p, tile, w);
         if (FFN && t.prob == 1) {
-            if (!wait_ffn_ready(p, t.tm, abort_flag)) {
+            if (!wait_ffn_ready(p, t.tm, t.slice, abort_flag)) {
                 if (!*abort_flag) record_failure(p.status, abort_flag, kRoleProducer);
                 ok = false;
                 break;
             }
             fence_proxy_async_global();
         }
-        const int kb0 = j == 0 ? w.kb_begin + pre : w.kb_begin;
+        const int kb0 = j == 0 ? t.kb_begin + pre : t.kb_begin;
         const int kb_pub = kb0 + 2 < t.kb_end - 1 ? kb0 + 2 : t.kb_end - 1;
         for (int kb = kb0; kb < t.kb_end; ++kb) {
             if (!wait_bounded(bar0 + 8u * (kBarEmpty + stage), phase ^ 1u, abort_flag,
@@ -644,8 +670,9 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
         }
         tcgen05_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        const int kb_end = tile_info<FFN>(p, tile, w).kb_end;
-        for (int kb = w.kb_begin; kb < kb_end; ++kb) {
+        const TileInfo t = tile_info<FFN>(p, tile, w);
+        const int kb_begin = t.kb_begin, kb_end = t.kb_end;
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
             if (!wait_bounded(bar0 + 8u * (kBarFull + stage), phase, abort_flag,
                               p.wait_limit_ns)) {
                 if (!*abort_flag) record_failure(p.status, abort_flag, kRoleMma);
@@ -672,12 +699,13 @@ __device__ __forceinline__ void run_mma(const GemmParams& p, uint32_t sbase, uin
                     ad = make_sdesc_sw128(sa + kk * 2048, 8192, 1024);
                     bd = make_sdesc_sw128(sb + kk * 32, 0, 1024);
                 }
+                const uint32_t accum = (kb > kb_begin || kk > 0) ? 1u : 0u;
                 if constexpr (PAIR && F8)
-                    mma_f8_ss_pair(d_tmem, ad, bd, idesc, (kb > w.kb_begin || kk > 0) ? 1u : 0u);
+                    mma_f8_ss_pair(d_tmem, ad, bd, idesc, accum);
                 else if constexpr (PAIR)
-                    mma_f16_ss_pair(d_tmem, ad, bd, idesc, (kb > w.kb_begin || kk > 0) ? 1u : 0u);
+                    mma_f16_ss_pair(d_tmem, ad, bd, idesc, accum);
                 else
-                    mma_f16_ss(d_tmem, ad, bd, idesc, (kb > w.kb_begin || kk > 0) ? 1u : 0u);
+                    mma_f16_ss(d_tmem, ad, bd, idesc, accum);
             }
             issued_any = true;
             // stage free (in both CTAs of a pair) once these MMAs finish
@@ -1014,6 +1042,100 @@ __device__ __noinline__ bool publish_partials_global(const GemmParams& p, uint8_
     return true;
 }
 
+// FFN kernel, GEMM 2 split along K (ffn_split2 > 1): float4 index, in the workspace, of
+// 16-byte unit u (4 fp32 columns) of 32-column chunk c of accumulator row `row` (0..127 of
+// the pair's CTA `pair_rank`) in K slice s of GEMM-2 tile `tile2`.  A warp's 32 rows of one
+// unit are 512 contiguous bytes.
+template <int BN>
+__device__ __forceinline__ long long ffn_ws_index(const GemmParams& p, int tile2, int s,
+                                                  int pair_rank, int c, int u, int row)
+{
+    return (((static_cast<long long>(tile2) * p.ffn_split2 + s) * 2 + pair_rank) * (BN / 4) + c * 8 + u) *
+               kBM + row;
+}
+
+// One epilogue warp, one K slice of a GEMM-2 tile: copy the warp's accumulator chunks
+// (part, part + kParts, ...) to the slice's place in the workspace.  Tensor memory is free
+// again once this returns.
+template <int BN, int EW>
+__device__ __forceinline__ void ffn_write_slice(const GemmParams& p, int tile2, int slice,
+                                                int pair_rank, int quarter, int part, int nchunks,
+                                                uint32_t t_lane)
+{
+    constexpr int kParts = EW / 4;
+    const int row = quarter * 32 + (threadIdx.x & 31);
+    float4* ws = reinterpret_cast<float4*>(p.ffn_ws);
+    for (int c = part; c < nchunks; c += kParts) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_load_32cols(t_lane + c * 32, r);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            __stcg(ws + ffn_ws_index<BN>(p, tile2, slice, pair_rank, c, u, row),
+                   make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                               __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])));
+    }
+}
+
+// Count this warp's slice for its share of the tile (one acquire-release atomic per warp:
+// the release publishes every lane's workspace stores, ordered before it by the warp
+// barrier; in the warp that completes the count, the acquire orders its workspace loads
+// behind the other slices' stores).  True in the warp of the slice that finished last.
+template <int EW>
+__device__ __forceinline__ bool ffn_count_slice(const GemmParams& p, int tile2, int pair_rank, int ew)
+{
+    __syncwarp();
+    unsigned before = 0;
+    if ((threadIdx.x & 31) == 0)
+        before = atom_add_acq_rel_gpu(p.ffn_count + (static_cast<long long>(tile2) * 2 + pair_rank) * EW + ew, 1u);
+    before = __shfl_sync(0xFFFFFFFFu, before, 0);
+    __syncwarp();
+    return before + 1 == static_cast<unsigned>(p.ffn_split2);
+}
+
+// The last slice's warp: chunk c of its rows summed over the K slices in slice order (the
+// sum does not depend on which slice finished last), from the workspace.  Loads are issued
+// 16 columns (every slice) at a time before any is added, so a round trip to L2 serves 16
+// columns.
+template <int BN>
+__device__ __forceinline__ void ffn_sum_chunk(const GemmParams& p, int tile2, int pair_rank,
+                                              int quarter, int c, uint32_t (&r)[32])
+{
+    const int row = quarter * 32 + (threadIdx.x & 31);
+    const int S = p.ffn_split2;
+    const float4* ws = reinterpret_cast<const float4*>(p.ffn_ws);
+#pragma unroll
+    for (int u0 = 0; u0 < 8; u0 += 4) {
+        float4 part[kFfnMaxSplit2][4];
+#pragma unroll
+        for (int s = 0; s < kFfnMaxSplit2; ++s) {
+            if (s < S) {
+#pragma unroll
+                for (int uu = 0; uu < 4; ++uu)
+                    part[s][uu] = __ldcg(ws + ffn_ws_index<BN>(p, tile2, s, pair_rank, c, u0 + uu, row));
+            }
+        }
+#pragma unroll
+        for (int uu = 0; uu < 4; ++uu) {
+            float4 a = part[0][uu];
+#pragma unroll
+            for (int s = 1; s < kFfnMaxSplit2; ++s) {
+                if (s < S) {
+                    a.x += part[s][uu].x;
+                    a.y += part[s][uu].y;
+                    a.z += part[s][uu].z;
+                    a.w += part[s][uu].w;
+                }
+            }
+            const int j = 4 * (u0 + uu);
+            r[j] = __float_as_uint(a.x);
+            r[j + 1] = __float_as_uint(a.y);
+            r[j + 2] = __float_as_uint(a.z);
+            r[j + 3] = __float_as_uint(a.w);
+        }
+    }
+}
+
 // EPI >= 0 fixes the epilog at compile time (only its code is in the kernel); -1 reads it
 // from the parameters.
 template <int BN, bool SWAP, bool PAIR = false, int EPI = -1, bool F8 = false, int EW = 8>
@@ -1174,6 +1296,23 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                                 static_cast<uint32_t>(acc * BN);
         const bool warp_live = lane_base < lane_limit;
         float lane_sum = 0.0f;  // backward, bias gradient along the lanes: this tile's sum
+        // FFN, GEMM 2 split along K: the slice's partial sums go to the workspace and tensor
+        // memory is released at once; only the warp of the slice that finished last goes on,
+        // with the sums of all slices read back from the workspace.
+        bool reduce_done = true;  // this warp runs the epilogue of the tile
+        bool from_ws = false;     // ... on values from the workspace, not tensor memory
+        bool tmem_released = false;
+        if constexpr (FFN) {
+            if (second && p.ffn_split2 > 1) {
+                ffn_write_slice<BN, EW>(p, t.tile2, t.slice, w.pair_rank, quarter, part, nchunks, t_lane);
+                tcgen05_fence_before_sync();
+                mbar_arrive_cluster(map_shared_rank(bar0 + 8u * (kBarTmemEmpty + acc),
+                                                    cluster_ctarank() & ~1u));
+                tmem_released = true;
+                reduce_done = ffn_count_slice<EW>(p, t.tile2, w.pair_rank, ew);
+                from_ws = reduce_done;
+            }
+        }
 
         // CTA-pair kernels, plain forward epilogs: each 32-column chunk in two 16-column
         // halves, the second half's TMEM load in flight while the first is processed (fewer
@@ -1184,7 +1323,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         const bool halves = kHalves && (epilog == EPI_BIAS || epilog == EPI_RELU_BIAS ||
                                         epilog == EPI_GELU_BIAS || epilog == EPI_NONE ||
                                         epilog == EPI_TANH_BIAS);
-        for (int c = part; c < nchunks; c += kParts) {
+        for (int c = part; c < (reduce_done ? nchunks : 0); c += kParts) {
             if (split_owner(quarter, c, w.split) != w.rank) continue;
             if constexpr (kHalves) {
                 if (halves) {
@@ -1259,10 +1398,16 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
             }
             uint32_t r[32];
             __syncwarp();
-            if constexpr (CH == 32)
+            if constexpr (FFN && CH == 32) {
+                if (from_ws)
+                    ffn_sum_chunk<BN>(p, t.tile2, w.pair_rank, quarter, c, r);
+                else
+                    tmem_load_32cols(t_lane + c * 32, r);
+            } else if constexpr (CH == 32) {
                 tmem_load_32cols(t_lane + c * 32, r);
-            else
+            } else {
                 tmem_load_16cols(t_lane + c * 16, r);
+            }
             float v[CH];
 #pragma unroll
             for (int j = 0; j < CH; ++j) v[j] = __uint_as_float(r[j]);
@@ -1476,12 +1621,14 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                 any_chunk = any_chunk || split_owner(quarter, c, w.split) == w.rank;
             if (any_chunk) atomicAdd(p.dbias + lane_idx, lane_sum);
         }
-        tcgen05_fence_before_sync();
-        if constexpr (PAIR)  // the even CTA's MMAs write both CTAs' accumulators
-            mbar_arrive_cluster(map_shared_rank(bar0 + 8u * (kBarTmemEmpty + acc),
-                                                cluster_ctarank() & ~1u));
-        else
-            mbar_arrive(bar0 + 8u * (kBarTmemEmpty + acc));
+        if (!tmem_released) {
+            tcgen05_fence_before_sync();
+            if constexpr (PAIR)  // the even CTA's MMAs write both CTAs' accumulators
+                mbar_arrive_cluster(map_shared_rank(bar0 + 8u * (kBarTmemEmpty + acc),
+                                                    cluster_ctarank() & ~1u));
+            else
+                mbar_arrive(bar0 + 8u * (kBarTmemEmpty + acc));
+        }
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
         if (FFN && t.prob == 0) {
@@ -1490,7 +1637,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
             if (lane == 0) {
                 bulk_wait_group<0>();
                 fence_proxy_async_global();
-                red_release_gpu_add(p.ffn_ready + tm, 1);
+                red_release_gpu_add(p.ffn_ready + ffn_ready_index(p, tm, ffn_slice_of_tile1(p, tn)), 1);
             }
             __syncwarp();
         }

@@ -113,12 +113,21 @@ struct GemmParams {
     // device memory overlaps the loads of the blocks before it.
     int prefetch;
     // FFN block in one launch (CTA-pair kernel, kEpiFfn): tiles [0, tiles_m * tiles_n) are
-    // GEMM 1, H = GELU(X.W1 + b1), described by the fields above (A = X, B = W1, D = H); the
-    // next ffn_tiles2 = tiles_m * tiles_n2 tiles are GEMM 2, Y = H.W2 + b2 + R, with the maps
-    // and sizes below.  A GEMM-2 tile loads its rows of H only once ffn_ready[its row tile]
-    // has reached ffn_ready_target, the number of epilogue warps of both CTAs over the
-    // GEMM-1 tiles of that row block, each of which adds 1 when its stores of H are done.
-    // ffn_tiles2 == 0 for every other launch.
+    // GEMM 1, H = GELU(X.W1 + b1), described by the fields above (A = X, B = W1, D = H; 256
+    // columns of H per tile); the next ffn_tiles2 = tiles_m * tiles_n2 * ffn_split2 work units
+    // are GEMM 2, Y = H.W2 + b2 + R, with the maps and sizes below.  Unit u is K slice
+    // s = u % ffn_split2 (K blocks [s * ffn_kb2, (s + 1) * ffn_kb2) of H's columns) of output
+    // tile u / ffn_split2 (row order).  A unit loads its slice of H only once
+    // ffn_ready[row tile * ffn_split2 + s] has reached ffn_ready_target times the number of
+    // GEMM-1 tiles in that slice: every epilogue warp of both CTAs adds 1 to its tile's
+    // counter when its stores of H are done, so ffn_ready_target = 2 x epilogue warps.
+    // ffn_split2 > 1 (ffn_kb2 a multiple of 4, so each GEMM-1 tile lies in one slice): every
+    // epilogue warp writes the fp32 partial sums of its rows and chunks of a unit to ffn_ws
+    // ([tile][slice][CTA of the pair][16-byte column unit][128 rows]) and counts itself in
+    // ffn_count[(tile * 2 + CTA) * epilogue warps + warp]; the warp that completes the count
+    // (the slice that finished last) adds the slices in slice order, so the sum does not
+    // depend on the arrival order, and runs the epilogue.  ffn_ready and ffn_count are zero
+    // at the launch.  ffn_tiles2 == 0 for every other launch.
     CUtensorMap tm_A2, tm_B2, tm_D2;
     const void* bias2;
     const void* residual2;
@@ -126,7 +135,13 @@ struct GemmParams {
     int ffn_ready_target;
     int ffn_tiles2;
     int n2, tiles_n2, k_blocks2;
+    int ffn_split2, ffn_kb2;
+    float* ffn_ws;
+    unsigned* ffn_count;
 };
+
+// Most K slices of the FFN kernel's second GEMM.
+constexpr int kFfnMaxSplit2 = 4;
 
 // Row-tile kernel (BN in {64, 128, 256}) and swapped small-m kernel (BN in {16 ... 256}).
 cudaError_t rowtile_prepare(int bn);

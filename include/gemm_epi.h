@@ -353,17 +353,35 @@ gemm_epi_status gemm_epi_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d
 
 /* How the plan runs the block (gemm_epi_ffn_set_option). */
 typedef enum {
-    GEMM_EPI_FFN_OPT_LAUNCHES = 0 /* 0 = automatic, 1 = one launch, 2 = two launches.
+    GEMM_EPI_FFN_OPT_LAUNCHES = 0, /* 0 = automatic, 1 = one launch, 2 = two launches.
                                      One launch: a single persistent kernel of CTA pairs
                                      (256 x 256 tiles) takes the GEMM-1 tiles first, then
-                                     the GEMM-2 tiles; a GEMM-2 tile starts loading its
-                                     256 rows of H once every GEMM-1 tile of those rows has
-                                     been stored (a per-row-block counter in device memory,
-                                     which the call zeroes on `stream` first), so GEMM 2
+                                     the GEMM-2 tiles; a GEMM-2 tile (or K slice of one)
+                                     starts loading its rows of H once every GEMM-1 tile of
+                                     those rows and columns has been stored (counters in
+                                     device memory, which the call zeroes on `stream`
+                                     first), so GEMM 2
                                      overlaps the end of GEMM 1 and H is read back while it
                                      is still in L2.  Automatic picks one launch when both
                                      GEMMs use the CTA-pair kernel and the block has at
                                      least six waves of tiles over the resident pairs. */
+    GEMM_EPI_FFN_OPT_SPLIT2 = 1,  /* one launch: K slices of each GEMM-2 tile, 0 or 1 = none
+                                     (the default), 2 or 4.  Each slice is a unit of work of
+                                     its own (waiting only for the GEMM-1 tiles of its
+                                     columns of H); the fp32 partial sums meet in a
+                                     workspace the plan allocates (256 KiB per GEMM-2 tile
+                                     and slice) and the slice that finishes last adds them
+                                     in slice order, so results do not depend on timing.
+                                     Slices are whole multiples of 256 columns of H; a
+                                     request the shape cannot meet takes fewer slices.  Not
+                                     chosen automatically: on GB300 the partial sums' round
+                                     trip through L2 costs more than the more even spread
+                                     of work gains (4096 x 1024 x 4096 bf16: 94 us in 4
+                                     slices, 66 us unsplit, 62 us in two launches). */
+    GEMM_EPI_FFN_OPT_TILE_ORDER = 2 /* one launch: 0 = automatic (static unsplit, dynamic when
+                                     GEMM 2 is split), 1 = static (pair q takes units q,
+                                     q + pairs, ...), 2 = dynamic (each pair takes the next
+                                     unit from a device counter as it becomes free). */
 } gemm_epi_ffn_option;
 
 gemm_epi_status gemm_epi_ffn_set_option(gemm_epi_ffn_plan_t p, gemm_epi_ffn_option opt,

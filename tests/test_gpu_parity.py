@@ -445,8 +445,80 @@ def test_ffn_option_rules():
         with pytest.raises(gemm_epi.GemmEpiError) as e:
             gemm_epi.gemm_epi_ffn_set_option(plan.handle, "LAUNCHES", 3)
         assert e.value.status == 1
+        assert "in 1 K slice of" in plan.describe() or plan.describe().startswith("two")
+        for bad in (3, 5, 8, -1):
+            with pytest.raises(gemm_epi.GemmEpiError) as e:
+                gemm_epi.gemm_epi_ffn_set_option(plan.handle, "SPLIT2", bad)
+            assert e.value.status == 1
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            gemm_epi.gemm_epi_ffn_set_option(plan.handle, "TILE_ORDER", 3)
+        assert e.value.status == 1
         gemm_epi.gemm_epi_ffn_set_option(plan.handle, "LAUNCHES", 2)
         assert plan.describe().startswith("two launches")
+
+
+def _ffn_inputs(t, d, f, seed):
+    g = torch.Generator().manual_seed(seed)
+
+    def r(*s, sc=1.0):
+        return (torch.randn(*s, generator=g) * sc).to(torch.bfloat16)
+    return dict(X=r(t, d, sc=0.5), W1=r(d, f, sc=0.05), b1=r(f, sc=0.1), W2=r(f, d, sc=0.05),
+                b2=r(d, sc=0.1), R=r(t, d))
+
+
+# (t, d, f, requested K slices of GEMM 2, slices the shape gives): f = 1032 has 17 K blocks
+# of H (slices of 12 or 8 blocks: 2 or 3 slices, the last one ragged); f = 776 has 13
+# (4 slices of 4, the last of 1 block: GEMM-1 tile 3 holds only 8 columns of H)
+FFN_SPLIT_CASES = [(300, 136, 1032, 2, 2), (300, 136, 1032, 4, 3), (520, 264, 776, 4, 4),
+                   (1300, 520, 1032, 4, 3), (16, 256, 2048, 4, 4), (600, 1024, 4096, 2, 2)]
+
+
+@pytest.mark.parametrize("order", [1, 2])
+@pytest.mark.parametrize("t,d,f,split2,slices", FFN_SPLIT_CASES)
+def test_ffn_one_launch_split2_parity(t, d, f, split2, slices, order):
+    """One launch with GEMM 2 split along K: each slice a unit of its own, the partial sums
+    added by the slice that finishes last, in slice order.  Against the oracle; repeated
+    calls give the same bits (the counts are back at zero and the sum order is fixed)."""
+    import oracle
+    cpu = _ffn_inputs(t, d, f, t + 7 * d + f)
+    dev = torch.device("cuda")
+    gi = {k: v.to(dev) for k, v in cpu.items()}
+    Y = torch.empty((t, d), dtype=torch.bfloat16, device=dev)
+    with gemm_epi.FfnPlan(t, d, f, launches=1, split2=split2, tile_order=order) as plan:
+        desc = plan.describe()
+        assert desc.startswith("one launch")
+        assert f"in {slices} K slices" in desc, desc
+        assert ("order=dynamic" if order == 2 else "order=static") in desc
+        outs = []
+        for _ in range(3):
+            plan.execute(gi["X"], gi["W1"], gi["b1"], gi["W2"], gi["b2"], gi["R"], Y)
+            assert plan.sync_status() == 0
+            outs.append(Y.clone())
+        H = plan.hidden().cpu()
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+    H_ref, H_exact, Y_ref = oracle.ffn(**cpu)
+    assert rel_err(H, H_exact) <= TOL["bf16"]
+    assert rel_err(Y, Y_ref) <= TOL["bf16"]
+    Y2 = oracle.gemm_epi(H, cpu["W2"], cpu["b2"], dtype="bf16", epilog="BIAS_RESIDUAL",
+                         residual=cpu["R"])
+    assert rel_err(Y, Y2) <= TOL["bf16"]
+
+
+def test_ffn_split2_order_independent():
+    """The same K slices in the static and the dynamic order give the same bits: which pair
+    runs a slice, and which slice finishes last, does not change the sum."""
+    t, d, f = 1300, 520, 1032
+    cpu = _ffn_inputs(t, d, f, 99)
+    dev = torch.device("cuda")
+    gi = {k: v.to(dev) for k, v in cpu.items()}
+    outs = []
+    for order in (1, 2):
+        Y = torch.empty((t, d), dtype=torch.bfloat16, device=dev)
+        with gemm_epi.FfnPlan(t, d, f, launches=1, split2=4, tile_order=order) as plan:
+            plan.execute(gi["X"], gi["W1"], gi["b1"], gi["W2"], gi["b2"], gi["R"], Y)
+            assert plan.sync_status() == 0
+        outs.append(Y)
+    assert torch.equal(outs[0], outs[1])
 
 
 # ---- split-K: partial sums through device memory (mode 2) or across a cluster (mode 1) -----

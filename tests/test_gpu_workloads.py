@@ -78,15 +78,17 @@ def test_ffn_full_parity():
     assert rel_err(Y, Y2) <= TOL["bf16"]
 
 
-@pytest.mark.parametrize("launches", [1, 2])
-def test_ffn_full_plan_parity(launches):
-    """The FFN plan on the full workload: one launch (both GEMMs in one persistent kernel)
-    and two launches."""
+@pytest.mark.parametrize("launches,split2", [(1, 1), (1, 4), (2, 1)])
+def test_ffn_full_plan_parity(launches, split2):
+    """The FFN plan on the full workload: one launch (both GEMMs in one persistent kernel,
+    GEMM 2 whole or in 4 K slices) and two launches."""
     f = workloads.FFNS["ffn_bf16_4096x1024x4096"]
     dev = torch.device("cuda")
     fi = workloads.ffn_inputs(f, device=dev)
     Y = torch.empty((f.t, f.d), dtype=torch.bfloat16, device=dev)
-    with gemm_epi.FfnPlan(f.t, f.d, f.f, "bf16", launches=launches) as plan:
+    with gemm_epi.FfnPlan(f.t, f.d, f.f, "bf16", launches=launches, split2=split2) as plan:
+        if launches == 1:
+            assert f"in {split2} K slice" in plan.describe(), plan.describe()
         plan.execute(fi["X"], fi["W1"], fi["b1"], fi["W2"], fi["b2"], fi["R"], Y)
         assert plan.sync_status() == 0
         H = plan.hidden().cpu()
