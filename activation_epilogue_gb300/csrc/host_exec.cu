@@ -1,8 +1,8 @@
 // gemm_epi_execute_host: the fused call on operands in host memory.  A, D (and residual,
 // aux) are split into row chunks; chunk j's host-to-device copy, GEMM and device-to-host copy
 // run on three streams the plan owns, each waiting (on events) only for what it needs, with
-// two device slots per chunked operand, so the copies of chunks j+1 and j-1 overlap the GEMM
-// of chunk j.  B and the bias are copied once per call.
+// kHostSlots device slots per chunked operand, so the copies of chunks j+1 and j-1 overlap the
+// GEMM of chunk j.  B and the bias are copied once per call.
 #include <cstring>
 #include <new>
 
@@ -12,16 +12,21 @@ using namespace gemm_epi;
 
 namespace gemm_epi_impl {
 
+// Device slots per chunked operand: the GEMM of chunk j reuses the slot of chunk j - kHostSlots,
+// so it waits for that chunk's copy out; with three slots a GEMM that runs late does not hold
+// up the copies out (with two, a GEMM only 10 % shorter than a chunk's copy out is all the
+// slack there is).
+constexpr int kHostSlots = 3;
+
 struct HostPipe {
     int64_t chunk = 0;  // rows per chunk (the last may be shorter)
     cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
     cudaEvent_t ev_start = nullptr, ev_shared = nullptr;
-    cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_comp[2] = {nullptr, nullptr},
-                ev_out[2] = {nullptr, nullptr};
-    void* dA[2] = {nullptr, nullptr};
-    void* dD[2] = {nullptr, nullptr};
-    void* dR[2] = {nullptr, nullptr};
-    void* dAux[2] = {nullptr, nullptr};
+    cudaEvent_t ev_in[kHostSlots] = {}, ev_comp[kHostSlots] = {}, ev_out[kHostSlots] = {};
+    void* dA[kHostSlots] = {};
+    void* dD[kHostSlots] = {};
+    void* dR[kHostSlots] = {};
+    void* dAux[kHostSlots] = {};
     void* dB = nullptr;
     void* dBias = nullptr;
     gemm_epi_plan_s full{}, last{};  // the chunk plans (sharing the parent's status word)
@@ -37,11 +42,15 @@ void destroy_host_pipe(gemm_epi_plan_s* p)
             cudaStreamSynchronize(st);
             cudaStreamDestroy(st);
         }
-    for (cudaEvent_t e : {h->ev_start, h->ev_shared, h->ev_in[0], h->ev_in[1], h->ev_comp[0],
-                          h->ev_comp[1], h->ev_out[0], h->ev_out[1]})
+    for (cudaEvent_t e : {h->ev_start, h->ev_shared})
         if (e) cudaEventDestroy(e);
-    for (void* b : {h->dA[0], h->dA[1], h->dD[0], h->dD[1], h->dR[0], h->dR[1], h->dAux[0],
-                    h->dAux[1], h->dB, h->dBias})
+    for (int s = 0; s < kHostSlots; ++s) {
+        for (cudaEvent_t e : {h->ev_in[s], h->ev_comp[s], h->ev_out[s]})
+            if (e) cudaEventDestroy(e);
+        for (void* b : {h->dA[s], h->dD[s], h->dR[s], h->dAux[s]})
+            if (b) cudaFree(b);
+    }
+    for (void* b : {h->dB, h->dBias})
         if (b) cudaFree(b);
     release_split_ws(&h->full);
     release_split_ws(&h->last);
@@ -51,16 +60,19 @@ void destroy_host_pipe(gemm_epi_plan_s* p)
 
 namespace {
 
-// Rows per chunk: about 1024-row chunks, at most 16 of them (a chunk of a large problem still
+// Rows per chunk: about 1024-row chunks, at most 32 of them (a chunk of a large problem still
 // fills the machine), whole 128-row tiles.  The copies out cannot start before the first
-// chunk's inputs are in and its GEMM is done, so more, smaller chunks shorten that fill;
-// measured on GB300 with ~190 GB/s each way to pinned host memory, the 65536 x 16384 x 8192
-// step is then bound by the 2 GiB copy of D out.
+// chunk's inputs are in and its GEMM is done, so more, smaller chunks shorten that fill.
+// Measured on GB300, where pinned host memory moves at 193 GB/s to the host and 211 GB/s
+// from it (the same for one copy, many, several streams, or SM-driven copies through the
+// mapped pointer): the 65536 x 16384 x 8192 step is bound by the 2 GiB copy of D out
+// (11.1 ms) plus that fill; 16 chunks and two slots 14.05 ms per step, three slots 13.99,
+// 32 chunks and three slots 13.78, 64 chunks 13.80-13.85.
 int64_t host_chunk_rows(int64_t m)
 {
     int64_t chunks = m / 1024;
     if (chunks < 1) chunks = 1;
-    if (chunks > 16) chunks = 16;
+    if (chunks > 32) chunks = 32;
     int64_t rows = (m + chunks - 1) / chunks;
     rows = (rows + 127) / 128 * 128;
     return rows < m ? rows : m;
@@ -111,9 +123,11 @@ gemm_epi_status make_host_pipe(gemm_epi_plan_s* p)
     bool ok = true;
     for (cudaStream_t* st2 : {&h->s_in, &h->s_comp, &h->s_out})
         ok = ok && cudaStreamCreateWithFlags(st2, cudaStreamNonBlocking) == cudaSuccess;
-    for (cudaEvent_t* e : {&h->ev_start, &h->ev_shared, &h->ev_in[0], &h->ev_in[1], &h->ev_comp[0],
-                           &h->ev_comp[1], &h->ev_out[0], &h->ev_out[1]})
+    for (cudaEvent_t* e : {&h->ev_start, &h->ev_shared})
         ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+    for (int s = 0; s < kHostSlots; ++s)
+        for (cudaEvent_t* e : {&h->ev_in[s], &h->ev_comp[s], &h->ev_out[s]})
+            ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
     const size_t e2 = 2;
     const size_t a_bytes = static_cast<size_t>(h->chunk) * p->k * e2;
     const size_t d_bytes = static_cast<size_t>(h->chunk) * p->n * e2;
@@ -124,7 +138,7 @@ gemm_epi_status make_host_pipe(gemm_epi_plan_s* p)
         if (!ok || bytes == 0) return;
         ok = cudaMalloc(ptr, bytes) == cudaSuccess;
     };
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kHostSlots; ++s) {
         alloc(&h->dA[s], a_bytes);
         alloc(&h->dD[s], d_bytes);
         if (p->epilog == GEMM_EPI_BIAS_RESIDUAL) alloc(&h->dR[s], d_bytes);
@@ -168,11 +182,11 @@ gemm_epi_status run_host(gemm_epi_plan_s* p, const gemm_epi_operands& o, cudaStr
     const int64_t nchunks = (p->m + h->chunk - 1) / h->chunk;
     int last_slot = 0;
     for (int64_t j = 0; ok && j < nchunks; ++j) {
-        const int s = static_cast<int>(j & 1);
+        const int s = static_cast<int>(j % kHostSlots);
         const int64_t r0 = j * h->chunk;
         const int64_t rows = p->m - r0 < h->chunk ? p->m - r0 : h->chunk;
         gemm_epi_plan_s* c = rows == h->chunk ? &h->full : &h->last;
-        // in: slot s is free once the GEMM of chunk j - 2 has read it
+        // in: slot s is free once the GEMM of chunk j - kHostSlots has read it
         ok = cudaStreamWaitEvent(h->s_in, h->ev_comp[s], 0) == cudaSuccess;
         if (ok && p->k > 0)
             ok = cudaMemcpyAsync(h->dA[s], static_cast<const char*>(o.A) + r0 * p->k * e2,
@@ -181,7 +195,7 @@ gemm_epi_status run_host(gemm_epi_plan_s* p, const gemm_epi_operands& o, cudaStr
             ok = cudaMemcpyAsync(h->dR[s], static_cast<const char*>(o.residual) + r0 * p->n * e2,
                                  static_cast<size_t>(rows) * p->n * e2, h2d, h->s_in) == cudaSuccess;
         ok = ok && cudaEventRecord(h->ev_in[s], h->s_in) == cudaSuccess;
-        // the GEMM: after its inputs, and after chunk j - 2's results left slot s
+        // the GEMM: after its inputs, and after chunk j - kHostSlots's results left slot s
         ok = ok && cudaStreamWaitEvent(h->s_comp, h->ev_in[s], 0) == cudaSuccess &&
              cudaStreamWaitEvent(h->s_comp, h->ev_shared, 0) == cudaSuccess &&
              cudaStreamWaitEvent(h->s_comp, h->ev_out[s], 0) == cudaSuccess;

@@ -266,12 +266,12 @@ gemm_epi_status gemm_epi_execute_operands(gemm_epi_plan_t p, const gemm_epi_oper
  * other calls (the call returns at once; the host buffers must stay valid and untouched
  * until `stream` reaches this point).  Forward epilogs on fp16/bf16 plans.
  *
- * The rows of A, D, residual and aux are processed in chunks (at most 16, of ~1024 rows or
+ * The rows of A, D, residual and aux are processed in chunks (at most 32, of ~1024 rows or
  * more) on three streams the plan owns: the copy in of chunk j+1, the GEMM of chunk j and
- * the copy out of chunk j-1 run at the same time, with two device slots per chunked
+ * the copy out of chunk j-1 run at the same time, with three device slots per chunked
  * operand; B and the bias are copied once per call.  The first call allocates the plan's
- * device buffers (two A chunks, two D chunks, B, bias, and residual / aux chunks when the
- * epilog has them) and creates its streams and events; a changed plan option rebuilds
+ * device buffers (three A chunks, three D chunks, B, bias, and residual / aux chunks when
+ * the epilog has them) and creates its streams and events; a changed plan option rebuilds
  * them.  Host buffers should be page-locked (cudaHostAlloc / pinned): pageable memory
  * works but its copies are slower and less overlapped.
  */

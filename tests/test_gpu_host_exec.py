@@ -96,10 +96,11 @@ def test_execute_host_rules():
 
 
 def test_execute_host_large_chunks_pair_kernel():
-    # 16 chunks of 1280 rows x 8192 columns: each chunk plan runs the CTA-pair kernel (160
-    # tiles: the static order; the plan itself, on device buffers, 2560 tiles and the
-    # dynamic order); rows on and around chunk edges checked by the oracle, and the whole
-    # result against the same plan on device buffers
+    # 20 chunks of 1024 rows x 8192 columns, so every one of the three device slots is
+    # reused several times: each chunk plan runs the CTA-pair kernel (128 tiles: the static
+    # order; the plan itself, on device buffers, 2560 tiles and the dynamic order); rows on
+    # and around chunk edges checked by the oracle, and the whole result against the same
+    # plan on device buffers
     m, n, k = 20480, 8192, 64
     p = workloads.random_problem(m, n, k, dtype="bf16", bias_layout="1N", residual=False,
                                  seed=2048)
@@ -113,7 +114,7 @@ def test_execute_host_large_chunks_pair_kernel():
         assert plan.sync_status() == 0
     assert torch.equal(D, Dd.cpu())
     assert torch.equal(aux, auxd.cpu())
-    rows = [0, 1, 1279, 1280, 1281, 2559, 2560, 10239, 10240, 20478, 20479]
+    rows = [0, 1, 1023, 1024, 1025, 2047, 2048, 3071, 3072, 10239, 10240, 20478, 20479]
     want, pre = oracle.gemm_epi(p["A"][rows], p["B"], p["bias"], dtype="bf16",
                                 epilog="RELU_AUX_BIAS", bias_layout="1N", want_pre=True)
     assert rel_err(D[rows], want) <= TOL["bf16"]
