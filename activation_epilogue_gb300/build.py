@@ -22,8 +22,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgemmepi.so")
 SOURCES = ["api.cu", "host_exec.cu", "ffn_api.cu", "layernorm_api.cu", "gemm_pair.cu",
-           "gemm_rowtile.cu", "gemm_swapped.cu", "gemm_smallm.cu", "elementwise.cu",
-           "layernorm.cu"]
+           "gemm_rowtile.cu", "gemm_swapped.cu", "gemm_fwd_bias.cu", "gemm_fwd_relu.cu",
+           "gemm_fwd_gelu.cu", "gemm_fwd_relu_aux.cu", "gemm_fwd_residual.cu",
+           "gemm_smallm.cu", "elementwise.cu", "layernorm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

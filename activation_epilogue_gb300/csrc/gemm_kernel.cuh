@@ -1766,7 +1766,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1) gemm_epi_kernel(const __grid_
         __syncwarp();
         cluster_sync_all();  // partial sums written
         if (warp >= 2 && !*abort_flag)
-            run_epilogue<BN, SWAP>(p, smem, sbase, bar0, tmem_base, abort_flag);
+            run_epilogue<BN, SWAP, PAIR, EPI, F8>(p, smem, sbase, bar0, tmem_base, abort_flag);
         __syncwarp();
         cluster_sync_all();  // the peers are done reading this CTA's partial sums
     }

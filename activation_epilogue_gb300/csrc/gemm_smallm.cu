@@ -89,13 +89,9 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
                  : "memory");
 }
 
-__device__ __forceinline__ void cluster_arrive_relaxed()
-{
-    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
-}
-
 // Arrive without release semantics: used where the arrival only says "this thread got here"
-// (what was received is already established by a byte-counting mbarrier).
+// (the barriers' initialisation is published by fence.mbarrier_init in the thread that
+// initialised them, and what was received is established by a byte-counting mbarrier).
 __device__ __forceinline__ void cluster_arrive_plain()
 {
     asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
@@ -185,7 +181,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) smallm_kernel(const __grid_cons
     }
     // Cluster barrier: every CTA of the cluster has started, its barriers initialised (its
     // shared memory may be written); waited at only just before the first remote store.
-    if (S > 1) cluster_arrive_relaxed();
+    if (S > 1) cluster_arrive_plain();
     tcgen05_fence_before_sync();
     __syncthreads();
     tcgen05_fence_after_sync();

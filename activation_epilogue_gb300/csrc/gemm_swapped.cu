@@ -1,62 +1,27 @@
 // Swapped small-m kernel instantiations: D^T tiles of 128 columns of D by BN rows of D,
-// BN in {16, 32, 64, 128, 256}.
-#include "gemm_kernel.cuh"
+// BN in {16, 32, 64, 128, 256}, with the epilog read from the parameters; the forward epilogs
+// with kernels of their own (gemm_fwd_*.cu) launch those.
+#include "gemm_single.cuh"
 
 namespace gemm_epi {
 
-namespace {
-template <int BN>
-cudaError_t prepare_one()
-{
-    return cudaFuncSetAttribute(gemm_epi_kernel<BN, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                TileCfg<BN>::kSmemBytes);
-}
-
-template <int BN>
-cudaError_t launch_one(const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = TileCfg<BN>::kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    unsigned na = 0;
-    if (pdl) {
-        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
-    if (p.split > 1 && !p.split_global) {  // split-K: one cluster of `split` CTAs per tile
-        attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = static_cast<unsigned>(p.split);
-        attr[na].val.clusterDim.y = 1;
-        attr[na].val.clusterDim.z = 1;
-        ++na;
-    }
-    cfg.attrs = na ? attr : nullptr;
-    cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemm_epi_kernel<BN, true>, p);
-}
-}  // namespace
-
-#define GEMM_EPI_SWAPPED_CASES(F) F(16) F(32) F(64) F(128) F(256)
-
 cudaError_t swapped_prepare(int bn)
 {
+    cudaError_t e;
     switch (bn) {
-#define F(X) case X: return prepare_one<X>();
+#define F(X) case X: e = single_prepare<X, true, -1>(); break;
         GEMM_EPI_SWAPPED_CASES(F)
 #undef F
     default: return cudaErrorInvalidValue;
     }
+    return e != cudaSuccess ? e : fwd_prepare(bn, true);
 }
 
 cudaError_t swapped_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
 {
+    if (fwd_specialised(p.epilog)) return fwd_launch(bn, true, p, grid, stream, pdl);
     switch (bn) {
-#define F(X) case X: return launch_one<X>(p, grid, stream, pdl);
+#define F(X) case X: return single_launch<X, true, -1>(p, grid, stream, pdl);
         GEMM_EPI_SWAPPED_CASES(F)
 #undef F
     default: return cudaErrorInvalidValue;
@@ -82,6 +47,5 @@ int swapped_stages(int bn)
     default: return 0;
     }
 }
-
 
 }  // namespace gemm_epi

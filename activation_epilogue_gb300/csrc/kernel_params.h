@@ -150,6 +150,14 @@ cudaError_t rowtile_launch(int bn, const GemmParams& p, int grid, cudaStream_t s
 int rowtile_smem_bytes(int bn);
 int rowtile_stages(int bn);
 
+// Row-tile (swap = false) and swapped (swap = true) kernels built for one forward epilog:
+// BIAS, RELU_BIAS, GELU_BIAS, RELU_AUX_BIAS, BIAS_RESIDUAL (fwd_specialised).  rowtile_* and
+// swapped_* launch them for those epilogs and the all-epilog kernels for the others.
+bool fwd_specialised(int epilog);
+cudaError_t fwd_prepare(int bn, bool swap);
+cudaError_t fwd_launch(int bn, bool swap, const GemmParams& p, int grid, cudaStream_t stream,
+                       bool pdl);
+
 cudaError_t swapped_prepare(int bn);
 cudaError_t swapped_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
 int swapped_smem_bytes(int bn);
