@@ -22,6 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgemmepi.so")
 SOURCES = ["api.cu", "host_exec.cu", "ffn_api.cu", "layernorm_api.cu", "gemm_pair.cu",
+           "gemm_pair_fp8.cu",
            "gemm_rowtile.cu", "gemm_swapped.cu", "gemm_fwd_bias.cu", "gemm_fwd_relu.cu",
            "gemm_fwd_gelu.cu", "gemm_fwd_relu_aux.cu", "gemm_fwd_residual.cu",
            "gemm_smallm.cu", "elementwise.cu", "layernorm.cu"]

@@ -224,22 +224,24 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
     } else if (p->k == 0) {
         p->variant = kBiasOnly;
     } else if (p->dtype == GEMM_EPI_E4M3) {
-        // E4M3: the CTA-pair kernel with 256 x 256 tiles and 128-deep K blocks, any shape
-        if ((p->opt_variant != 0 && p->opt_variant != 3) || (p->opt_bn != 0 && p->opt_bn != 256))
+        // E4M3: the CTA-pair kernel with 256 x 256 or 256 x 224 tiles (the width with fewer
+        // waves, as for 16-bit inputs) and 128-deep K blocks, any shape
+        if ((p->opt_variant != 0 && p->opt_variant != 3) ||
+            (p->opt_bn != 0 && p->opt_bn != 256 && p->opt_bn != 224))
             return GEMM_EPI_ERR_INVALID_ARG;
         if (fp8_pair_prepare() != cudaSuccess || rowpair_prepare(256) != cudaSuccess)
             return GEMM_EPI_ERR_LAUNCH;
-        p->variant = kRowPair;
-        p->bn = 256;
-        p->k_blocks = static_cast<int>((p->k + 127) / 128);
-        p->tiles_m = static_cast<int>((p->m + 255) / 256);
-        p->tiles_n = static_cast<int>((p->n + 255) / 256);
-        p->stages = rowpair_stages(256);
-        p->smem = rowpair_smem_bytes(256);
-        long long pairs = rowpair_max_clusters(256);
+        long long pairs = rowpair_max_clusters(256);  // same shared memory for both widths
         if (pairs > p->sm_count / 2) pairs = p->sm_count / 2;
         if (p->opt_grid > 0 && p->opt_grid / 2 < pairs) pairs = p->opt_grid / 2;
         if (pairs < 1) return GEMM_EPI_ERR_LAUNCH;
+        p->variant = kRowPair;
+        p->bn = p->opt_bn ? p->opt_bn : pick_pair_bn(p->m, p->n, pairs);
+        p->k_blocks = static_cast<int>((p->k + 127) / 128);
+        p->tiles_m = static_cast<int>((p->m + 255) / 256);
+        p->tiles_n = static_cast<int>((p->n + p->bn - 1) / p->bn);
+        p->stages = rowpair_stages(p->bn);
+        p->smem = rowpair_smem_bytes(p->bn);
         const long long tiles = static_cast<long long>(p->tiles_m) * p->tiles_n;
         if (pairs > tiles) pairs = tiles;
         p->kb_per_split = p->k_blocks;
@@ -465,10 +467,12 @@ gemm_epi_status ensure_maps(gemm_epi_plan_s* p, const void* A, const void* B, vo
     if (p->maps_valid && p->key_A == A && p->key_B == B && p->key_D == D) return GEMM_EPI_OK;
     p->maps_valid = false;
     if (p->dtype == GEMM_EPI_E4M3) {
-        // A [m][k] and B transposed [n][k], bytes, K-major boxes {128 k, 128 rows}; D bf16
+        // A [m][k] and B transposed [n][k], bytes, K-major boxes {128 k, 128 rows} (A) and
+        // {128 k, bn / 2 rows} (B: each CTA's half of a tile's columns); D bf16
         const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        const uint32_t b_rows = static_cast<uint32_t>(p->bn / 2);
         if (!encode_2d(&p->tm_A, A, u8, p->k, p->m, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
-            !encode_2d(&p->tm_B, B, u8, p->k, p->n, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
+            !encode_2d(&p->tm_B, B, u8, p->k, p->n, 128, b_rows, CU_TENSOR_MAP_SWIZZLE_128B, 1) ||
             !encode_2d(&p->tm_D, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p->n, p->m, 32, 32,
                        CU_TENSOR_MAP_SWIZZLE_64B))
             return GEMM_EPI_ERR_LAUNCH;
@@ -588,7 +592,7 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, in
     prm.prefetch = p->prefetch;
     cudaError_t e;
     if (p->variant == kRowPair && p->dtype == GEMM_EPI_E4M3)
-        e = fp8_pair_launch(prm, p->grid, stream, pdl);
+        e = fp8_pair_launch(p->bn, prm, p->grid, stream, pdl);
     else if (p->variant == kRowPair)
         e = rowpair_launch(p->bn, prm, p->grid, stream, pdl);
     else if (p->variant == kRowTile)

@@ -439,11 +439,15 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase,
     const int k0 = kb * kBK;
     if constexpr (PAIR && F8) {
         // E4M3: a K block is 128 elements (one 128-byte swizzle row); A rows and the rows of
-        // B transposed (columns of D) are K-major boxes {128 k, 128 rows} of 16 KB
-        static_assert(BN == 256, "the FP8 pair kernel runs 256-wide tiles");
+        // B transposed (columns of D) are K-major boxes of 128-byte rows: A {128 k, 128
+        // rows}, B {128 k, BN / 2 rows} (each CTA's half of the tile's columns: 112 rows at
+        // BN = 224, laid out like the first 112 of a 128-row box).  The copy bytes are what
+        // bounds this kernel, so the box holds only the rows the MMA (N = BN) reads.
+        static_assert(BN == 256 || BN == 224, "the FP8 pair kernel runs 256- or 224-wide tiles");
+        constexpr uint32_t kF8StageBytes = C::kABytes + (BN / 2) * 128;
         const uint32_t cr = cluster_ctarank();
         const uint32_t rank = cr & 1u;
-        if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::kStageBytes);
+        if (rank == 0) mbar_arrive_expect_tx(fb, 2 * kF8StageBytes);
         const uint32_t fb0 = map_shared_rank(fb, cr & ~1u);
         const int k8 = kb * 128;
         const int brow = tn * BN + static_cast<int>(rank) * (BN / 2);

@@ -153,64 +153,6 @@ int rowpair_stages(int bn)
     }
 }
 
-// ---- E4M3 inputs: 256 x 256 tiles, the forward epilogs without a 16-bit auxiliary output ----
-
-template <int EPI>
-cudaError_t fp8_prepare_one()
-{
-    return cudaFuncSetAttribute(gemm_epi_kernel<256, false, true, EPI, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                TileCfg<256, true>::kSmemBytes);
-}
-
-template <int EPI>
-cudaError_t fp8_launch_one(const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = TileCfg<256, true>::kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    unsigned na = 0;
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = 2;  // one CTA pair
-    attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = 1;
-    ++na;
-    if (pdl) {
-        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemm_epi_kernel<256, false, true, EPI, true>, p);
-}
-
-cudaError_t fp8_pair_prepare()
-{
-    const cudaError_t e[] = {fp8_prepare_one<EPI_BIAS>(), fp8_prepare_one<EPI_RELU_BIAS>(),
-                             fp8_prepare_one<EPI_GELU_BIAS>(), fp8_prepare_one<EPI_RELU_AUX_BIAS>(),
-                             fp8_prepare_one<EPI_BIAS_RESIDUAL>(), fp8_prepare_one<EPI_NONE>()};
-    for (cudaError_t x : e)
-        if (x != cudaSuccess) return x;
-    return cudaSuccess;
-}
-
-cudaError_t fp8_pair_launch(const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
-{
-    switch (p.epilog) {
-    case EPI_BIAS: return fp8_launch_one<EPI_BIAS>(p, grid, stream, pdl);
-    case EPI_RELU_BIAS: return fp8_launch_one<EPI_RELU_BIAS>(p, grid, stream, pdl);
-    case EPI_GELU_BIAS: return fp8_launch_one<EPI_GELU_BIAS>(p, grid, stream, pdl);
-    case EPI_RELU_AUX_BIAS: return fp8_launch_one<EPI_RELU_AUX_BIAS>(p, grid, stream, pdl);
-    case EPI_BIAS_RESIDUAL: return fp8_launch_one<EPI_BIAS_RESIDUAL>(p, grid, stream, pdl);
-    case EPI_NONE: return fp8_launch_one<EPI_NONE>(p, grid, stream, pdl);
-    default: return cudaErrorInvalidValue;
-    }
-}
-
 cudaError_t ffn_pair_prepare() { return prepare_one<256, kEpiFfn>(); }
 
 cudaError_t ffn_pair_launch(const GemmParams& p, int grid, cudaStream_t stream)

@@ -179,10 +179,10 @@ int rowpair_smem_bytes(int bn);
 int rowpair_stages(int bn);
 int rowpair_max_clusters(int bn);
 
-// CTA-pair kernel on E4M3 inputs (256 x 256 tiles), epilogs BIAS, RELU_BIAS, GELU_BIAS,
-// RELU_AUX_BIAS, BIAS_RESIDUAL, NONE.
+// CTA-pair kernel on E4M3 inputs (256 x bn tiles, bn 256 or 224), epilogs BIAS, RELU_BIAS,
+// GELU_BIAS, RELU_AUX_BIAS, BIAS_RESIDUAL, NONE.
 cudaError_t fp8_pair_prepare();
-cudaError_t fp8_pair_launch(const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
+cudaError_t fp8_pair_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
 
 // The FFN block in one CTA-pair launch (256 x 256 tiles); never a programmatic dependent.
 cudaError_t ffn_pair_prepare();

@@ -83,8 +83,9 @@ typedef enum {
                           k must be a multiple of 16.  D = epi(scale_a * scale_b * (A.B) +
                           bias), scale_a and scale_b device fp32 scalars in the operands.
                           Epilogs BIAS, RELU_BIAS, GELU_BIAS, RELU_AUX_BIAS, BIAS_RESIDUAL,
-                          NONE (gemm_epi_execute_operands); runs on the CTA-pair kernel; the
-                          page names FP8 among the fused matmul's types */
+                          NONE (gemm_epi_execute_operands); runs on the CTA-pair kernel
+                          (256 x 256 or 256 x 224 tiles, whichever takes fewer waves over the
+                          pairs); the page names FP8 among the fused matmul's types */
 } gemm_epi_dtype;
 
 typedef enum {

@@ -104,6 +104,44 @@ def test_fp8_plan_is_a_pair_plan(m, n, order):
         assert "variant=row-pair " in d and f"order={order}" in d, d
 
 
+@pytest.mark.parametrize("bn", [224, 256])
+@pytest.mark.parametrize("epilog", ["RELU_AUX_BIAS", "GELU_BIAS", "BIAS_RESIDUAL"])
+@pytest.mark.parametrize("shape", [(600, 520, 272), (300, 1000, 400), (520, 232, 1040)])
+def test_fp8_tile_widths(epilog, shape, bn):
+    # 256 x 224 tiles: each CTA's half of B is 112 rows, loaded in 128-row boxes (the 16 extra
+    # rows belong to the next tile or lie past the edge); n = 520, 1000, 232 leave ragged
+    # last column tiles at both widths
+    m, n, k = shape
+    layout = "M1" if (m + bn) % 3 == 0 else "1N"
+    p = workloads.random_fp8_problem(m, n, k, bias_layout=layout, seed=m + n + k + bn,
+                                     residual=True)
+    _, _, desc = _check(p, m, n, k, epilog, layout, options={"TILE_N": bn})
+    assert f"tile=256x{bn} " in desc, desc
+
+
+def test_fp8_integer_bit_exact_224():
+    m, n, k = 520, 1000, 64
+    g = torch.Generator().manual_seed(224)
+    p = {"A": torch.randint(-4, 5, (m, k), generator=g).float().to(torch.float8_e4m3fn),
+         "Bt": torch.randint(-4, 5, (n, k), generator=g).float().to(torch.float8_e4m3fn),
+         "scale_a": 1.0, "scale_b": 1.0,
+         "bias": torch.randint(-8, 9, (n,), generator=g).to(torch.bfloat16)}
+    D, _, desc = _run(p, m, n, k, "RELU_BIAS", "1N", options={"TILE_N": 224})
+    assert "tile=256x224 " in desc
+    want = oracle.gemm_epi_fp8(p["A"], p["Bt"], p["bias"], scale_a=1.0, scale_b=1.0,
+                               epilog="RELU_BIAS")
+    assert np.array_equal(D.double().numpy(), want), desc
+
+
+@pytest.mark.parametrize("m,n,bn", [(4096, 4096, 224), (65536, 16384, 256), (2048, 2048, 256)])
+def test_fp8_tile_width_choice(m, n, bn):
+    # the width with fewer waves of tiles over the pairs (224 on a tie): 4096 x 4096 is
+    # 304 tiles of 224 (4 waves) against 256 of 256 (3.4, paid as 4); 2048 x 2048 is 64
+    # tiles of 256 (one wave) against 80 of 224 (two)
+    with gemm_epi.Plan(m, n, 8192, "e4m3", "RELU_BIAS", "1N") as plan:
+        assert f"tile=256x{bn} " in plan.describe(), plan.describe()
+
+
 @pytest.mark.parametrize("epilog", ["RELU_AUX_BIAS", "BIAS_RESIDUAL", "GELU_BIAS"])
 def test_fp8_unfused(epilog):
     m, n, k = 300, 264, 208
@@ -151,6 +189,9 @@ def test_fp8_rules():
     assert e.value.status == 2
     with pytest.raises(gemm_epi.GemmEpiError) as e:
         gemm_epi.Plan(64, 64, 64, "e4m3", "BIAS", "1N", VARIANT=1)
+    assert e.value.status == 1
+    with pytest.raises(gemm_epi.GemmEpiError) as e:
+        gemm_epi.Plan(64, 64, 64, "e4m3", "BIAS", "1N", TILE_N=128)
     assert e.value.status == 1
     with pytest.raises(gemm_epi.GemmEpiError) as e:
         gemm_epi.FfnPlan(64, 64, 64, "e4m3")
