@@ -602,7 +602,8 @@ def measure_fp8(device, stream, peaks):
 
 
 def measure_ffn(device, stream, flush, peaks):
-    """The FFN block through its plan (automatic mode, and one and two launches forced) and
+    """The FFN block through its plan (automatic mode; one launch, two launches and one launch
+    with GEMM 2 in K slices forced) and
     the unfused chain (GEMM, bias+GELU pass, GEMM, bias+residual pass: four launches, two
     extra round trips of pre-activations), cold L2 and CUDA Graph replay."""
     import torch
@@ -621,8 +622,12 @@ def measure_ffn(device, stream, flush, peaks):
             p1.execute_unfused(fi["X"], fi["W1"], fi["b1"], pre1, H)
             p2.execute_unfused(H, fi["W2"], fi["b2"], pre2, Y, residual=fi["R"])
         cold_unf = time_cold(ffn_unfused, 20, stream, flush)
-        for mode, launches in [("", 0), ("_one_launch", 1), ("_two_launches", 2)]:
-            with gemm_epi.FfnPlan(f.t, f.d, f.f, "bf16", launches=launches) as fp:
+        # (one launch with GEMM 2 in 4 K slices: the more even spread of work that the
+        # slices' fp32 partial sums cost more than it gains, measured every run)
+        for mode, opts in [("", {}), ("_one_launch", {"launches": 1}),
+                           ("_two_launches", {"launches": 2}),
+                           ("_one_launch_split4", {"launches": 1, "split2": 4})]:
+            with gemm_epi.FfnPlan(f.t, f.d, f.f, "bf16", **opts) as fp:
                 def ffn():
                     fp.execute(fi["X"], fi["W1"], fi["b1"], fi["W2"], fi["b2"], fi["R"], Y)
                 cold = time_cold(ffn, 20, stream, flush)
