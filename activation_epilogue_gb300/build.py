@@ -25,7 +25,7 @@ SOURCES = ["api.cu", "host_exec.cu", "ffn_api.cu", "layernorm_api.cu", "gemm_pai
            "gemm_pair_fp8.cu",
            "gemm_rowtile.cu", "gemm_swapped.cu", "gemm_fwd_bias.cu", "gemm_fwd_relu.cu",
            "gemm_fwd_gelu.cu", "gemm_fwd_relu_aux.cu", "gemm_fwd_residual.cu",
-           "gemm_smallm.cu", "elementwise.cu", "layernorm.cu"]
+           "gemm_smallm.cu", "ffn_onchip.cu", "elementwise.cu", "layernorm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

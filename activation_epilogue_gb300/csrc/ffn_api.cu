@@ -26,7 +26,8 @@ struct gemm_epi_ffn_plan_s {
     int opt_launches;  // GEMM_EPI_FFN_OPT_LAUNCHES value (0 = automatic)
     int opt_split2;    // GEMM_EPI_FFN_OPT_SPLIT2 value
     int opt_order;     // GEMM_EPI_FFN_OPT_TILE_ORDER value
-    bool one_launch;   // the mode in use
+    bool one_launch;   // the mode in use: one CTA-pair launch, H through L2
+    bool onchip;       // ... or one launch with H kept on chip (opt_launches == 3)
     // per (256-row block of H, GEMM-2 K slice): epilogue warps done with it; then the
     // GEMM-2 slice counts (per tile, CTA of the pair and epilogue warp), zeroed together
     int* ready;
@@ -81,6 +82,8 @@ gemm_epi_status configure_ffn(gemm_epi_ffn_plan_s* p)
     p->maps_valid = false;
     if (p->layernorm) {  // the one-launch kernel runs GELU_BIAS only
         p->one_launch = false;
+        p->onchip = false;
+        if (p->opt_launches == 3) return GEMM_EPI_ERR_INVALID_ARG;
         snprintf(p->desc, sizeof(p->desc), "two launches after the row statistics: [%s] then [%s]",
                  p->g1->desc, p->g2->desc);
         return GEMM_EPI_OK;
@@ -89,6 +92,22 @@ gemm_epi_status configure_ffn(gemm_epi_ffn_plan_s* p)
     p->tiles_n1 = static_cast<int>((p->f + 255) / 256);
     p->tiles_n2 = static_cast<int>((p->d + 255) / 256);
     p->grid = 0;
+    p->onchip = p->opt_launches == 3;
+    if (p->onchip) {
+        // H kept on chip: one CTA per (128 tokens, 256 columns of Y), chunks of 256 of H
+        p->one_launch = false;
+        if (p->d % 256 != 0 || p->f % 256 != 0) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+        if (ffn_onchip_prepare() != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
+        const long long grid = ((p->t + 127) / 128) * (p->d / 256);
+        if (grid > (1ll << 30)) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
+        p->grid = static_cast<int>(grid);
+        snprintf(p->desc, sizeof(p->desc),
+                 "one launch, H on chip: t=%lld d=%lld f=%lld, one CTA per 128 tokens x 256 columns "
+                 "of Y, %lld chunks of 256 of H, grid=%d",
+                 static_cast<long long>(p->t), static_cast<long long>(p->d),
+                 static_cast<long long>(p->f), static_cast<long long>(p->f / 256), p->grid);
+        return GEMM_EPI_OK;
+    }
     if (ffn_pair_prepare() != cudaSuccess || rowpair_prepare(256) != cudaSuccess)
         return GEMM_EPI_ERR_LAUNCH;
     long long pairs = rowpair_max_clusters(256);
@@ -182,6 +201,30 @@ gemm_epi_status ensure_ffn_maps(gemm_epi_ffn_plan_s* p, const void* X, const voi
     p->key_Y = Y;
     p->maps_valid = true;
     return GEMM_EPI_OK;
+}
+
+gemm_epi_status run_ffn_onchip(gemm_epi_ffn_plan_s* p, const void* X, const void* W1,
+                               const void* b1, const void* W2, const void* b2, const void* R,
+                               void* Y, cudaStream_t stream)
+{
+    gemm_epi_status st = ensure_ffn_maps(p, X, W1, W2, Y);
+    if (st != GEMM_EPI_OK) return st;
+    OnchipFfnParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.tm_X = p->tm_X;
+    prm.tm_W1 = p->tm_W1;
+    prm.tm_W2 = p->tm_W2;
+    prm.b1 = b1;
+    prm.b2 = b2;
+    prm.R = R;
+    prm.Y = Y;
+    prm.status = p->g1->d_status;
+    prm.wait_limit_ns = p->g1->wait_limit_ns;
+    prm.t = static_cast<int>(p->t);
+    prm.d = static_cast<int>(p->d);
+    prm.f = static_cast<int>(p->f);
+    prm.bf16 = p->dtype == GEMM_EPI_BF16 ? 1 : 0;
+    return ffn_onchip_launch(prm, p->grid, stream) == cudaSuccess ? GEMM_EPI_OK : GEMM_EPI_ERR_LAUNCH;
 }
 
 gemm_epi_status run_ffn_one_launch(gemm_epi_ffn_plan_s* p, const void* X, const void* W1,
@@ -355,7 +398,7 @@ gemm_epi_status gemm_epi_ffn_set_option(gemm_epi_ffn_plan_t p, gemm_epi_ffn_opti
     int* field = nullptr;
     switch (opt) {
     case GEMM_EPI_FFN_OPT_LAUNCHES:
-        if (value < 0 || value > 2) return GEMM_EPI_ERR_INVALID_ARG;
+        if (value < 0 || value > 3) return GEMM_EPI_ERR_INVALID_ARG;
         field = &p->opt_launches;
         break;
     case GEMM_EPI_FFN_OPT_SPLIT2:
@@ -394,6 +437,7 @@ gemm_epi_status gemm_epi_ffn_execute(gemm_epi_ffn_plan_t p, const void* X, const
     if (p->t == 0 || p->d == 0) return GEMM_EPI_OK;
     st = check_device(p->g1);
     if (st != GEMM_EPI_OK) return st;
+    if (p->onchip) return run_ffn_onchip(p, X, W1, b1, W2, b2, R, Y, stream);
     if (p->one_launch) return run_ffn_one_launch(p, X, W1, b1, W2, b2, R, Y, stream);
     st = run_plan(p->g1, o1, stream, true);
     if (st != GEMM_EPI_OK) return st;

@@ -188,6 +188,27 @@ cudaError_t fp8_pair_launch(int bn, const GemmParams& p, int grid, cudaStream_t 
 cudaError_t ffn_pair_prepare();
 cudaError_t ffn_pair_launch(const GemmParams& p, int grid, cudaStream_t stream);
 
+// The FFN block with H kept on chip (csrc/ffn_onchip.cu): CTA (r, q) owns rows
+// [128 r, 128 r + 128) of X and Y and columns [256 q, 256 q + 256) of Y.  For each 256-wide
+// chunk of H: GEMM 1 H_c = X W1[:, chunk] into tensor memory, bias + GELU into a 16-bit
+// copy in shared memory (the layout GEMM 2 reads), GEMM 2 Y += H_c W2[chunk, cols] into
+// tensor memory; then Y + b2 + R.  d and f are multiples of 256.
+struct OnchipFfnParams {
+    CUtensorMap tm_X;   // X[t][d]: K-major boxes {64 k, 128 rows}, 128-byte swizzle
+    CUtensorMap tm_W1;  // W1[d][f]: N-major boxes {64 n, 64 k}, 128-byte swizzle
+    CUtensorMap tm_W2;  // W2[f][d]: N-major boxes {64 n, 64 k}, 128-byte swizzle
+    const void* b1;
+    const void* b2;
+    const void* R;
+    void* Y;
+    int* status;
+    unsigned long long wait_limit_ns;
+    int t, d, f;
+    int bf16;
+};
+cudaError_t ffn_onchip_prepare();
+cudaError_t ffn_onchip_launch(const OnchipFfnParams& p, int grid, cudaStream_t stream);
+
 
 // Elementwise epilogue over a 16-bit pre-activation (the unfused baseline's second kernel;
 // pre == nullptr means pre = 0, which serves k == 0).

@@ -622,11 +622,12 @@ def measure_ffn(device, stream, flush, peaks):
             p1.execute_unfused(fi["X"], fi["W1"], fi["b1"], pre1, H)
             p2.execute_unfused(H, fi["W2"], fi["b2"], pre2, Y, residual=fi["R"])
         cold_unf = time_cold(ffn_unfused, 20, stream, flush)
-        # (one launch with GEMM 2 in 4 K slices: the more even spread of work that the
-        # slices' fp32 partial sums cost more than it gains, measured every run)
+        # (one launch with GEMM 2 in 4 K slices, and one launch with H kept on chip: the
+        # layouts that cost more than they gain, measured every run)
         for mode, opts in [("", {}), ("_one_launch", {"launches": 1}),
                            ("_two_launches", {"launches": 2}),
-                           ("_one_launch_split4", {"launches": 1, "split2": 4})]:
+                           ("_one_launch_split4", {"launches": 1, "split2": 4}),
+                           ("_onchip", {"launches": 3})]:
             with gemm_epi.FfnPlan(f.t, f.d, f.f, "bf16", **opts) as fp:
                 def ffn():
                     fp.execute(fi["X"], fi["W1"], fi["b1"], fi["W2"], fi["b2"], fi["R"], Y)

@@ -354,7 +354,10 @@ gemm_epi_status gemm_epi_ffn_plan(gemm_epi_ffn_plan_t* out, int64_t t, int64_t d
 
 /* How the plan runs the block (gemm_epi_ffn_set_option). */
 typedef enum {
-    GEMM_EPI_FFN_OPT_LAUNCHES = 0, /* 0 = automatic, 1 = one launch, 2 = two launches.
+    GEMM_EPI_FFN_OPT_LAUNCHES = 0, /* 0 = automatic, 1 = one launch, 2 = two launches,
+                                     3 = one launch with H kept on chip (the page's fused
+                                     flowchart; for comparison: measured far slower, see
+                                     below; d and f multiples of 256, not with LayerNorm).
                                      One launch: a single persistent kernel of CTA pairs
                                      (256 x 256 tiles) takes the GEMM-1 tiles first, then
                                      the GEMM-2 tiles; a GEMM-2 tile (or K slice of one)
@@ -365,7 +368,13 @@ typedef enum {
                                      overlaps the end of GEMM 1 and H is read back while it
                                      is still in L2.  Automatic picks one launch when both
                                      GEMMs use the CTA-pair kernel and the block has at
-                                     least six waves of tiles over the resident pairs. */
+                                     least six waves of tiles over the resident pairs.
+                                     H on chip: one CTA per 128 tokens and 256 columns of
+                                     Y keeps Y's accumulator and a 256-wide chunk of H in
+                                     tensor memory and the chunk's 16-bit H in shared
+                                     memory; X and W1 are streamed again for every chunk
+                                     (they do not fit on chip), so the copies bound it.
+                                     gemm_epi_ffn_hidden's buffer is not written. */
     GEMM_EPI_FFN_OPT_SPLIT2 = 1,  /* one launch: K slices of each GEMM-2 tile, 0 or 1 = none
                                      (the default), 2 or 4.  Each slice is a unit of work of
                                      its own (waiting only for the GEMM-1 tiles of its

@@ -443,7 +443,7 @@ def test_ffn_one_launch_many_row_blocks_few_pairs():
 def test_ffn_option_rules():
     with gemm_epi.FfnPlan(300, 136, 264) as plan:
         with pytest.raises(gemm_epi.GemmEpiError) as e:
-            gemm_epi.gemm_epi_ffn_set_option(plan.handle, "LAUNCHES", 3)
+            gemm_epi.gemm_epi_ffn_set_option(plan.handle, "LAUNCHES", 4)
         assert e.value.status == 1
         assert "in 1 K slice of" in plan.describe() or plan.describe().startswith("two")
         for bad in (3, 5, 8, -1):
@@ -455,6 +455,44 @@ def test_ffn_option_rules():
         assert e.value.status == 1
         gemm_epi.gemm_epi_ffn_set_option(plan.handle, "LAUNCHES", 2)
         assert plan.describe().startswith("two launches")
+
+
+@pytest.mark.parametrize("t,d,f", [(300, 256, 512), (130, 512, 256), (1, 256, 256),
+                                   (520, 1024, 768)])
+def test_ffn_onchip_parity(t, d, f):
+    """H kept on chip (LAUNCHES = 3): Y against the oracle's chain (which rounds H to bf16 as
+    the kernel does); ragged token counts; repeated calls give the same bits."""
+    import oracle
+    cpu = _ffn_inputs(t, d, f, 11 * t + d + f)
+    dev = torch.device("cuda")
+    gi = {k: v.to(dev) for k, v in cpu.items()}
+    Y = torch.full((t, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    with gemm_epi.FfnPlan(t, d, f, launches=3) as plan:
+        assert plan.describe().startswith("one launch, H on chip"), plan.describe()
+        plan.execute(gi["X"], gi["W1"], gi["b1"], gi["W2"], gi["b2"], gi["R"], Y)
+        assert plan.sync_status() == 0
+        Y1 = Y.clone()
+        plan.execute(gi["X"], gi["W1"], gi["b1"], gi["W2"], gi["b2"], gi["R"], Y)
+        assert plan.sync_status() == 0
+        assert torch.equal(Y, Y1)
+    _, _, Y_ref = oracle.ffn(**cpu)
+    assert rel_err(Y, Y_ref) <= TOL["bf16"]
+
+
+def test_ffn_onchip_rules():
+    with gemm_epi.FfnPlan(300, 136, 264) as plan:          # d, f not multiples of 256
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            gemm_epi.gemm_epi_ffn_set_option(plan.handle, "LAUNCHES", 3)
+        assert e.value.status == 2
+        assert not plan.describe().startswith("one launch, H on chip")
+    with gemm_epi.FfnPlan(256, 256, 256, layernorm=True) as plan:
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            gemm_epi.gemm_epi_ffn_set_option(plan.handle, "LAUNCHES", 3)
+        assert e.value.status == 1
+    with gemm_epi.FfnPlan(256, 256, 256) as plan:
+        with pytest.raises(gemm_epi.GemmEpiError) as e:
+            gemm_epi.gemm_epi_ffn_set_option(plan.handle, "LAUNCHES", 4)
+        assert e.value.status == 1
 
 
 def _ffn_inputs(t, d, f, seed):

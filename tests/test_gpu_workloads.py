@@ -78,10 +78,10 @@ def test_ffn_full_parity():
     assert rel_err(Y, Y2) <= TOL["bf16"]
 
 
-@pytest.mark.parametrize("launches,split2", [(1, 1), (1, 4), (2, 1)])
+@pytest.mark.parametrize("launches,split2", [(1, 1), (1, 4), (2, 1), (3, 1)])
 def test_ffn_full_plan_parity(launches, split2):
     """The FFN plan on the full workload: one launch (both GEMMs in one persistent kernel,
-    GEMM 2 whole or in 4 K slices) and two launches."""
+    GEMM 2 whole or in 4 K slices), two launches, and one launch with H kept on chip."""
     f = workloads.FFNS["ffn_bf16_4096x1024x4096"]
     dev = torch.device("cuda")
     fi = workloads.ffn_inputs(f, device=dev)
@@ -94,7 +94,8 @@ def test_ffn_full_plan_parity(launches, split2):
         H = plan.hidden().cpu()
     cpu = {k: v.cpu() for k, v in fi.items()}
     H_ref, H_exact, Y_ref = oracle.ffn(**cpu)
-    assert rel_err(H, H_exact) <= TOL["bf16"]
+    if launches != 3:                   # (with H on chip the hidden buffer is not written)
+        assert rel_err(H, H_exact) <= TOL["bf16"]
     assert rel_err(Y, Y_ref) <= TOL["bf16"]
 
 
