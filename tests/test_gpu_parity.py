@@ -479,6 +479,31 @@ def test_ffn_onchip_parity(t, d, f):
     assert rel_err(Y, Y_ref) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("launches", [1, 2, 3])
+def test_ffn_f16_modes(launches):
+    """The FFN plan on binary16 operands (H stored in binary16) in each mode: one launch, two
+    launches, H on chip."""
+    import oracle
+    t, d, f = 300, 256, 512
+    g = torch.Generator().manual_seed(1616 + launches)
+
+    def r(*sh, sc=1.0):
+        return (torch.randn(*sh, generator=g) * sc).to(torch.float16)
+    cpu = dict(X=r(t, d, sc=0.5), W1=r(d, f, sc=0.05), b1=r(f, sc=0.1), W2=r(f, d, sc=0.05),
+               b2=r(d, sc=0.1), R=r(t, d))
+    dev = torch.device("cuda")
+    gi = {k: v.to(dev) for k, v in cpu.items()}
+    Y = torch.empty((t, d), dtype=torch.float16, device=dev)
+    with gemm_epi.FfnPlan(t, d, f, "f16", launches=launches) as plan:
+        plan.execute(gi["X"], gi["W1"], gi["b1"], gi["W2"], gi["b2"], gi["R"], Y)
+        assert plan.sync_status() == 0
+        H = plan.hidden().cpu()
+    H_ref, H_exact, Y_ref = oracle.ffn(**cpu, dtype="f16")
+    if launches != 3:
+        assert rel_err(H, H_exact) <= TOL["f16"]
+    assert rel_err(Y, Y_ref) <= TOL["f16"]
+
+
 def test_ffn_onchip_rules():
     with gemm_epi.FfnPlan(300, 136, 264) as plan:          # d, f not multiples of 256
         with pytest.raises(gemm_epi.GemmEpiError) as e:
