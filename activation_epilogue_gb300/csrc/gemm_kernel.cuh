@@ -1148,7 +1148,8 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                                              volatile int* abort_flag)
 {
     // The FFN kernel runs GELU_BIAS on GEMM-1 tiles and BIAS_RESIDUAL on GEMM-2 tiles.
-    constexpr bool FFN = EPI == kEpiFfn;
+    constexpr bool FFN = is_ffn(EPI);
+    constexpr bool FFN_SPLIT = EPI == kEpiFfnSplit;
     const int epilog0 = FFN ? EPI_GELU_BIAS : (EPI >= 0 ? EPI : p.epilog);
     using C = TileCfg<BN, PAIR, EW>;
     constexpr int CH = C::kChunk;
@@ -1306,7 +1307,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         bool reduce_done = true;  // this warp runs the epilogue of the tile
         bool from_ws = false;     // ... on values from the workspace, not tensor memory
         bool tmem_released = false;
-        if constexpr (FFN) {
+        if constexpr (FFN_SPLIT) {
             if (second && p.ffn_split2 > 1) {
                 ffn_write_slice<BN, EW>(p, t.tile2, t.slice, w.pair_rank, quarter, part, nchunks, t_lane);
                 tcgen05_fence_before_sync();
@@ -1402,7 +1403,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
             }
             uint32_t r[32];
             __syncwarp();
-            if constexpr (FFN && CH == 32) {
+            if constexpr (FFN_SPLIT && CH == 32) {
                 if (from_ws)
                     ffn_sum_chunk<BN>(p, t.tile2, w.pair_rank, quarter, c, r);
                 else
@@ -1670,7 +1671,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1) gemm_epi_kernel(const __grid_
     const int lane = threadIdx.x & 31;
     int pre = 0;  // stages the prologue issued (thread 0, which is also the producer)
 
-    constexpr bool FFN = EPI == kEpiFfn;
+    constexpr bool FFN = is_ffn(EPI);
     if (threadIdx.x == 0) {
         prefetch_tensormap(&p.tm_A);
         prefetch_tensormap(&p.tm_B);

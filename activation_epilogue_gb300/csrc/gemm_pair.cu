@@ -153,10 +153,15 @@ int rowpair_stages(int bn)
     }
 }
 
-cudaError_t ffn_pair_prepare() { return prepare_one<256, kEpiFfn>(); }
+cudaError_t ffn_pair_prepare()
+{
+    const cudaError_t e = prepare_one<256, kEpiFfn>();
+    return e != cudaSuccess ? e : prepare_one<256, kEpiFfnSplit>();
+}
 
 cudaError_t ffn_pair_launch(const GemmParams& p, int grid, cudaStream_t stream)
 {
+    if (p.ffn_split2 > 1) return launch_one<256, kEpiFfnSplit>(p, grid, stream, false);
     return launch_one<256, kEpiFfn>(p, grid, stream, false);
 }
 

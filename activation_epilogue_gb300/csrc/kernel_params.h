@@ -21,8 +21,12 @@ enum Epilog : int {
     EPI_LN_GELU_BIAS = 10   // D = GELU(rstd_i (A.B - mu_i c_j) + b'_j): LayerNorm folded in
 };
 
-// Template value of the CTA-pair kernel that runs a whole FFN block (two GEMMs) in one launch.
+// Template values of the CTA-pair kernel that runs a whole FFN block (two GEMMs) in one
+// launch: GEMM 2 whole, or in K slices (ffn_split2 > 1; only that instantiation carries the
+// slices' partial-sum code, which cost the other one 32 registers and ~1.2 us per call).
 constexpr int kEpiFfn = 100;
+constexpr int kEpiFfnSplit = 101;
+__host__ __device__ constexpr bool is_ffn(int epi) { return epi == kEpiFfn || epi == kEpiFfnSplit; }
 
 // Epilogue warps per CTA (two per 32-lane quarter of tensor memory).
 constexpr int kEpilogueWarps = 8;
