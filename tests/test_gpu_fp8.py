@@ -221,6 +221,8 @@ def test_fp8_random_cases(i):
     opts = {"VARIANT": 3, "TILE_ORDER": r.choice([1, 2])}
     if r.random() < 0.3:
         opts["GRID"] = r.choice([4, 8])
+    if r.random() < 0.5:
+        opts["TILE_N"] = r.choice([224, 256])
     p = workloads.random_fp8_problem(m, n, k, bias_layout=layout, seed=r.randint(0, 10 ** 6),
                                      residual=True)
     _check(p, m, n, k, epilog, layout, options=opts)
