@@ -49,7 +49,8 @@ EncodeTiledFn encode_fn()
 // 8.1/7.5/7.5 us hot, against 11.0 / 6.8 us unsplit; the publish, count and reload of the
 // partial tiles cost more than the shorter K loop saves.  Narrower swapped tiles (below)
 // add CTAs without any of that.  The one automatic split: row tiles that leave half the
-// SMs idle over 16 or more K blocks take two slices through a cluster (configure()).
+// SMs idle over 16 or more K blocks take 2 to 4 slices through a cluster, their partial
+// sums meeting in L2 (pick_auto_split).
 constexpr int kMaxClusterSplit = 4;  // CTAs per cluster (kernel: kMaxSplit)
 constexpr int kMaxGlobalSplit = 8;   // K slices through device memory (kernel: kMaxGSplit)
 
@@ -81,6 +82,64 @@ int pick_rowtile_bn(int64_t m, int64_t n, int k_blocks, int sm_count)
         }
     }
     return best;
+}
+
+// Time model of the busiest CTA, used to choose K splits and between the swapped and the
+// row-tile kernel for small m.  These kernels are bound by streaming their operand slabs
+// into the SMs and, when K is split, by sending partial sums out; measured on GB300: ~84 GB/s
+// per SM into row tiles 64 wide, ~110 GB/s into wider ones, ~62 GB/s into swapped tiles
+// (W streamed as 128-column panels) and ~50 GB/s per SM of fp32 partial sums out through
+// L2; a K split adds ~3 us of fixed cost (the cluster barrier, the partial sums' reload,
+// the epilogue starting after both).  Fitted on 1024 x 512 x 2048, 512 x 512 x 4096,
+// 1024 x 1024 x 2048, 2048 x 512 x 2048, 256 x 1024 x 8192, 768 x 768 x 3072 and
+// 1024 x 256 x 4096 (CUDA graph, hot L2).
+double slab_us(int k_blocks, int bn, double bytes_per_us)
+{
+    return k_blocks * (16384.0 + 128.0 * bn) / bytes_per_us;
+}
+
+double rowtile_rate(int bn) { return bn == 64 ? 84e3 : 110e3; }
+
+constexpr double kSwappedRate = 62e3;
+constexpr double kPartialOutRate = 50e3;
+constexpr double kSplitFixedUs = 3.0;
+
+// Unsplit row tiles: waves of tiles, each a whole K loop.
+double rowtile_us(int64_t m, int64_t n, int k_blocks, int sm_count, int bn)
+{
+    const int64_t tiles = ((m + 127) / 128) * ((n + bn - 1) / bn);
+    const int64_t waves = (tiles + sm_count - 1) / sm_count;
+    return static_cast<double>(waves) * slab_us(k_blocks, bn, rowtile_rate(bn));
+}
+
+// Row tiles with K split over a cluster, partial sums through L2: over the tile widths
+// (fixed_bn, or 64, 128 and 256) and 2 to 4 slices whose tiles x slices fit one wave and
+// whose slices are at least 4 K blocks deep, the fastest in the model.  At 1024 x 512 x 2048
+// BIAS fp16 (hot / L2 flushed): 128 x 128 tiles in 4 slices 9.8 / 9.9 us (the choice), in 3
+// 10.2 / 10.6, 128 x 256 in 4 10.5 / 11.1, 128 x 64 in 2 10.8 / 11.3, unsplit 12.2 / 12.7;
+// the same 4 slices over distributed shared memory 15.2 / 16.1 us.
+bool pick_auto_split(int64_t m, int64_t n, int k_blocks, int sm_count, int fixed_bn, int* bn_out,
+                     int* split_out, double* us_out)
+{
+    const int64_t tm = (m + 127) / 128;
+    double best = 1e300;
+    for (int bn : {64, 128, 256}) {
+        if (fixed_bn && bn != fixed_bn) continue;
+        const int64_t tiles = tm * ((n + bn - 1) / bn);
+        for (int s = 2; s <= kMaxClusterSplit; ++s) {
+            const int kpb = (k_blocks + s - 1) / s;
+            if (tiles * s > sm_count || kpb < 4) continue;
+            const double t = slab_us(kpb, bn, rowtile_rate(bn)) +
+                             (s - 1.0) / s * 128.0 * bn * 4.0 / kPartialOutRate + kSplitFixedUs;
+            if (t < best) {
+                best = t;
+                *bn_out = bn;
+                *split_out = s;
+            }
+        }
+    }
+    *us_out = best;
+    return best < 1e300;
 }
 
 // Tile width (rows of D) of the swapped small-m kernel: the narrowest that still gives
@@ -215,6 +274,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
     p->group_m = 1;
     p->split = 1;
     p->split_global = 0;
+    p->split_l2 = 0;
     p->dyn_order = 0;
     p->swap_m64 = 0;
     p->box_k = 0;
@@ -267,6 +327,22 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
                 smallm_prepare() == cudaSuccess &&
                 pick_smallm(p->m, p->n, p->k, p->sm_count, 0, &sc))
                 v = kSmallM;
+            // otherwise, over a long K loop: row tiles with K split over a cluster when the
+            // model puts them well ahead of the swapped kernel, which streams each 128-column
+            // panel of B through one SM (256 x 1024 x 8192 BIAS: 37.8 us swapped, 15.5 us as
+            // 128 x 64 row tiles in 4 slices; the swapped kernel keeps T x 3072 x 768)
+            if (v == kSwapped && p->opt_split_k == 0 && p->opt_bn == 0 && p->opt_split_mode != 2) {
+                const int kb = static_cast<int>((p->k + 63) / 64);
+                const int sbn = pick_swapped_bn(p->m, p->n, p->sm_count);
+                const int64_t sw_tiles = ((p->n + 127) / 128) * ((p->m + sbn - 1) / sbn);
+                const double sw_us = static_cast<double>((sw_tiles + p->sm_count - 1) / p->sm_count) *
+                                     slab_us(kb, sbn, kSwappedRate);
+                int sp_bn = 0, sp_split = 0;
+                double sp_us = 0.0;
+                if (pick_auto_split(p->m, p->n, kb, p->sm_count, 0, &sp_bn, &sp_split, &sp_us) &&
+                    sp_us < 0.7 * sw_us)
+                    v = kRowTile;
+            }
         }
         // (option values: 1 row-tile, 2 swapped, 3 CTA pairs, 5 small-m; the internal
         // Variant codes differ)
@@ -361,20 +437,30 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
     }
     if (p->variant == kRowTile || p->variant == kSwapped) {
         const int v = p->variant;
+        int want_split = p->opt_split_k > 0 ? p->opt_split_k : 1;
+        bool via_cluster = p->opt_split_mode == 1 || p->opt_split_mode == 3;
+        bool via_l2 = p->opt_split_mode == 3;
+        int auto_bn = 0, auto_split = 0;
+        double split_us = 0.0;
+        if (p->opt_split_k == 0 && v == kRowTile && p->opt_split_mode != 2 &&
+            pick_auto_split(p->m, p->n, p->k_blocks, p->sm_count, p->opt_bn, &auto_bn, &auto_split,
+                            &split_us) &&
+            split_us < rowtile_us(p->m, p->n, p->k_blocks, p->sm_count, p->bn)) {
+            // Row tiles whose K loop is long against the work's spread over the SMs: K slices
+            // through a cluster, the partial sums through L2 unless SPLIT_MODE asks for
+            // distributed shared memory (pick_auto_split); through device memory alone (no
+            // cluster) 1024 x 512 x 2048 took 15.0 / 17.2 us.
+            want_split = auto_split;
+            via_cluster = true;
+            via_l2 = p->opt_split_mode != 1;
+            p->bn = auto_bn;
+            p->tiles_n = static_cast<int>((p->n + p->bn - 1) / p->bn);
+            p->stages = rowtile_stages(p->bn);
+            p->smem = rowtile_smem_bytes(p->bn);
+        }
         const long long tiles = static_cast<long long>(p->tiles_m) * p->tiles_n;
         cudaError_t e = v == kRowTile ? rowtile_prepare(p->bn) : swapped_prepare(p->bn);
         if (e != cudaSuccess) return GEMM_EPI_ERR_LAUNCH;
-        int want_split = p->opt_split_k > 0 ? p->opt_split_k : 1;
-        bool via_cluster = p->opt_split_mode == 1;
-        if (p->opt_split_k == 0 && v == kRowTile && tiles * 2 <= p->sm_count &&
-            p->k_blocks >= 16 && p->opt_split_mode != 2) {
-            // Row tiles that leave half the SMs idle over a long K loop: two K slices per
-            // tile through a cluster.  Measured on GB300 at 1024 x 512 x 2048 BIAS fp16 (64
-            // tiles of 128 x 64, 32 K blocks): 11.7 us hot / 13.1 us cold against 12.6 /
-            // 13.3 us unsplit; through device memory it was slower (15.0 / 17.2 us).
-            want_split = 2;
-            via_cluster = true;
-        }
         if (want_split > (via_cluster ? kMaxClusterSplit : kMaxGlobalSplit))
             return GEMM_EPI_ERR_INVALID_ARG;
         p->split = normalise_split(want_split, p->k_blocks, &p->kb_per_split);
@@ -383,6 +469,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             // one CTA per (tile, K slice), not persistent; in clusters of `split` CTAs when
             // the slices meet on chip
             p->split_global = via_cluster ? 0 : 1;
+            p->split_l2 = via_cluster && via_l2 ? 1 : 0;
             grid = tiles * p->split;
             if (grid > (1ll << 30)) return GEMM_EPI_ERR_UNSUPPORTED_SHAPE;
         } else {
@@ -427,13 +514,16 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
              p->dtype == GEMM_EPI_E4M3 ? 128 : 64, p->stages, p->smem, p->tiles_m, p->tiles_n,
              p->k_blocks,
              p->split,
-             p->split > 1 ? (p->split_global ? "(device memory)" : "(cluster)") : "",
+             p->split > 1 ? (p->split_global ? "(device memory)"
+                             : p->split_l2   ? "(cluster+L2)"
+                                             : "(cluster)")
+                          : "",
              p->grid, p->group_m,
              p->variant != kRowPair ? "" : p->dyn_order ? " order=dynamic" : " order=static",
              p->sm_count);
     const char* log = getenv("GEMM_EPI_LOG");
     if (log && log[0] == '1') fprintf(stderr, "[gemm_epi] plan: %s\n", p->desc);
-    if (p->split_global) return ensure_split_ws(p);
+    if (p->split_global || p->split_l2) return ensure_split_ws(p);
     return GEMM_EPI_OK;
 }
 
@@ -586,6 +676,7 @@ gemm_epi_status launch_gemm(gemm_epi_plan_s* p, const gemm_epi_operands& ops, in
     prm.split_global = p->split_global;
     prm.split_ws = p->d_split_ws;
     prm.split_count = p->d_split_count;
+    prm.split_l2 = p->split_l2;
     prm.sched = p->dyn_order ? p->d_sched : nullptr;
     prm.swap_m64 = p->swap_m64;
     prm.box_k = p->box_k;
@@ -800,7 +891,7 @@ gemm_epi_status gemm_epi_plan_set_option(gemm_epi_plan_t p, gemm_epi_option opt,
         p->opt_split_k = static_cast<int>(value);
         break;
     case GEMM_EPI_OPT_SPLIT_MODE:
-        if (value < 0 || value > 2) return GEMM_EPI_ERR_INVALID_ARG;
+        if (value < 0 || value > 3) return GEMM_EPI_ERR_INVALID_ARG;
         p->opt_split_mode = static_cast<int>(value);
         break;
     case GEMM_EPI_OPT_TILE_M:

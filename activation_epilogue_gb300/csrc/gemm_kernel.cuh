@@ -35,7 +35,9 @@
 // round-robin by the cluster ranks; every CTA writes the partial sums of the chunks it does
 // not own into its (by then idle) stage ring, the cluster synchronises, and each owner adds
 // the peers' partials over distributed shared memory before running the epilogue on its
-// chunks.  Device memory: independent CTAs write their fp32 partial tiles to a workspace
+// chunks (or, with split_l2, the partials go to a device-memory workspace and the owners
+// read them from L2: an SM moves data to and from L2 several times faster than over
+// distributed shared memory).  Device memory: independent CTAs write their fp32 partial tiles to a workspace
 // (it stays in L2) and count themselves per tile; the CTA that arrives last adds the
 // slices in slice order and runs the epilogue.  No CTA waits for another.
 //
@@ -110,6 +112,9 @@ constexpr int kBarSchedFull = 24;         // [8] in each CTA: slot written
 constexpr int kBarSchedEmpty = 32;        // [8] in the even CTA: slot read by every consumer
 constexpr int kOffSchedSlot = 40 * 8;     // int[8] in each CTA: the tile indices
 static_assert(kOffLast + 4 <= kBarSchedFull * 8, "barrier area layout");
+// Split-K across a cluster through L2 (single CTAs): the shared memory each epilogue warp
+// receives its peers' partial sums in (in the idle stage ring)
+constexpr int kL2SlotBytes = 16 * 1024;
 
 constexpr unsigned long long kDrainLimitNs = 20ull * 1000 * 1000;  // 20 ms
 
@@ -229,8 +234,14 @@ __device__ __forceinline__ WorkRange work_range(const GemmParams& p)
 
 // Split-K: the rank of the cluster that owns (reduces, then runs the epilogue of) chunk c
 // of TMEM lane quarter q.  Spreading (quarter, chunk) units over the ranks shares the
-// reduction among the CTAs even when a tile has a single chunk.
-__device__ __forceinline__ int split_owner(int q, int c, int split) { return (4 * c + q) % split; }
+// reduction among the CTAs even when a tile has a single chunk.  The epilogue warp of
+// quarter q with index `part` takes chunks part, part + 2, ...; as it walks them the owner
+// steps through the ranks, so every warp both publishes and reduces, about 1/split of its
+// chunks each (the warp index 4 part + q offsets the cycle).
+__device__ __forceinline__ int split_owner(int q, int c, int split)
+{
+    return (4 * (c & 1) + q + (c >> 1)) % split;
+}
 
 // One tile of the walk: which GEMM (0, or 1 = the second GEMM of a fused FFN block), its
 // coordinates, its K blocks [kb_begin, kb_end) and (second GEMM) its K slice.
@@ -861,6 +872,65 @@ __device__ __forceinline__ void store_pre_row(const GemmParams& p, const float (
     }
 }
 
+// Split-K through device memory: float4 index of 16-byte unit u (4 fp32 columns) of chunk c
+// of accumulator row `row` in K slice s of tile `tile`.  One unit of a warp's 32 rows is
+// 512 contiguous bytes.
+template <int BN>
+__device__ __forceinline__ long long gsplit_index(const GemmParams& p, int tile, int s, int c,
+                                                  int u, int row)
+{
+    constexpr int CH = TileCfg<BN>::kChunk;
+    return ((static_cast<long long>(tile) * p.split + s) * (BN / 4) + c * (CH / 4) + u) * kBM + row;
+}
+
+// Split-K across a cluster through L2 (split_l2): float4 index, in the workspace, of 16-byte
+// unit u of lane `lane` in the block (lane quarter q, chunk c) of cluster rank s's partial
+// sums of tile `tile`.  A block (32 rows x CH columns, 128 * CH bytes) is contiguous, so
+// its owner fetches it with one bulk copy; in it, unit u of the 32 lanes is 512 bytes.
+template <int BN>
+__device__ __forceinline__ long long l2split_index(const GemmParams& p, int tile, int s, int q,
+                                                   int c, int u, int lane)
+{
+    constexpr int CH = TileCfg<BN>::kChunk;
+    return ((((static_cast<long long>(tile) * p.split + s) * 4 + q) * (BN / CH) + c) * (CH / 4) + u) *
+               32 + lane;
+}
+
+// Split-K across a cluster through L2, an owning epilogue warp (quarter, part) right after
+// the cluster barrier: copy the peers' partial sums of its chunks into its slots in the
+// idle stage ring (at `slots` from the start of shared memory), each lane its own 16-byte
+// units, every copy in flight at once; the lane waits for its copies before reading them
+// (cp_async_wait_all) and reads only what it copied.  The cluster barrier (release /
+// acquire) has ordered the peers' stores before these loads.
+template <int BN>
+__device__ __forceinline__ void fetch_peer_partials(const GemmParams& p, uint32_t sbase,
+                                                    uint32_t slots, int tile, int rank, int split,
+                                                    int quarter, int part, int nchunks)
+{
+    constexpr int CH = TileCfg<BN>::kChunk;
+    constexpr uint32_t kBlk = 128u * CH;
+    // A warp takes J = ceil(chunks / 2) chunks and owns at most ceil(J / split) of them (the
+    // owner cycles through the ranks), each with split - 1 peer blocks: within its slots.
+    constexpr int J = (BN / CH + 1) / 2;
+    static_assert(((J + 1) / 2) * 1 * kBlk <= kL2SlotBytes && ((J + 2) / 3) * 2 * kBlk <= kL2SlotBytes &&
+                      ((J + 3) / 4) * 3 * kBlk <= kL2SlotBytes,
+                  "a warp's peer blocks fit its slots for 2, 3 and 4 slices");
+    const int lane = threadIdx.x & 31;
+    const float4* ws = reinterpret_cast<const float4*>(p.split_ws);
+    int oi = 0;
+    for (int c = part; c < nchunks; c += 2) {
+        if (split_owner(quarter, c, split) != rank) continue;
+        for (int pi = 0; pi < split - 1; ++pi) {
+            const int peer = pi < rank ? pi : pi + 1;
+            const float4* src = ws + l2split_index<BN>(p, tile, peer, quarter, c, 0, lane);
+            const uint32_t dst = sbase + slots + (oi * (split - 1) + pi) * kBlk + lane * 16;
+#pragma unroll
+            for (int u = 0; u < CH / 4; ++u) cp_async_16(dst + u * 512, src + u * 32);
+        }
+        ++oi;
+    }
+}
+
 // Split-K, before the cluster synchronises: write this CTA's partial sums of the chunks
 // it does not own into its partial-tile buffer (the stage ring, idle once every MMA of the
 // tile has completed).
@@ -887,6 +957,8 @@ __device__ __forceinline__ void publish_partials(const GemmParams& p, uint8_t* s
     }
     tcgen05_fence_after_sync();
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    // The workspace may still be read by a programmatic predecessor grid.
+    if (p.split_l2) grid_dependency_wait();
     // The bias is read after the cluster barrier: start bringing it into L2 now.
     if (p.epilog != EPI_NONE) {
         const int nb = (SWAP ? p.bias_layout == 0 : p.bias_layout == 1) ? col_limit : (SWAP ? p.n : p.m);
@@ -902,24 +974,23 @@ __device__ __forceinline__ void publish_partials(const GemmParams& p, uint8_t* s
             tmem_load_32cols(t_lane + c * 32, r);
         else
             tmem_load_16cols(t_lane + c * 16, r);
+        if (p.split_l2) {
+            // (one block of the workspace: 512 contiguous bytes per unit for the warp)
+            float4* ws = reinterpret_cast<float4*>(p.split_ws);
 #pragma unroll
-        for (int u = 0; u < CH / 4; ++u) {
-            uint4 q = make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
-            *reinterpret_cast<uint4*>(smem + red_offset<BN>(row, c * (CH / 4) + u)) = q;
+            for (int u = 0; u < CH / 4; ++u)
+                __stcg(ws + l2split_index<BN>(p, w.first, w.rank, quarter, c, u, lane),
+                       make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                                   __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])));
+        } else {
+#pragma unroll
+            for (int u = 0; u < CH / 4; ++u) {
+                uint4 q = make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+                *reinterpret_cast<uint4*>(smem + red_offset<BN>(row, c * (CH / 4) + u)) = q;
+            }
         }
     }
     tcgen05_fence_before_sync();
-}
-
-// Split-K through device memory: float4 index of 16-byte unit u (4 fp32 columns) of chunk c
-// of accumulator row `row` in K slice s of tile `tile`.  One unit of a warp's 32 rows is
-// 512 contiguous bytes.
-template <int BN>
-__device__ __forceinline__ long long gsplit_index(const GemmParams& p, int tile, int s, int c,
-                                                  int u, int row)
-{
-    constexpr int CH = TileCfg<BN>::kChunk;
-    return ((static_cast<long long>(tile) * p.split + s) * (BN / 4) + c * (CH / 4) + u) * kBM + row;
 }
 
 // Split-K through device memory, every epilogue thread of every CTA: write this CTA's
@@ -1168,6 +1239,19 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
     float* sbias = EW == 8 ? reinterpret_cast<float*>(smem + C::kOffBias) + ew * 512 : nullptr;
     uint8_t* epi_buf = smem + C::kOffEpi + ew * 2048;
     const uint32_t epi_buf_u32 = sbase + C::kOffEpi + ew * 2048;
+    // Split-K across a cluster through L2 (one tile per CTA): start copying the peers'
+    // partial sums of this warp's chunks (written by this grid) before anything else.
+    const uint32_t l2_slots = static_cast<uint32_t>(ew) * kL2SlotBytes;  // (from shared memory)
+    if constexpr (!PAIR) {
+        static_assert(PAIR || kEpiWarps * kL2SlotBytes <= C::kStages * C::kStageBytes,
+                      "every warp's slots fit the stage ring");
+        if (w.split > 1 && p.split_l2) {
+            int tm0, tn0;
+            tile_coords(w.first, p, tm0, tn0);
+            const int nch = (min(BN, (SWAP ? p.m : p.n) - tn0 * BN) + CH - 1) / CH;
+            fetch_peer_partials<BN>(p, sbase, l2_slots, w.first, w.rank, w.split, quarter, part, nch);
+        }
+    }
     // Bias, residual and the outputs may belong to a programmatic predecessor grid.
     grid_dependency_wait();
     // E4M3 inputs: the per-tensor dequantisation scales
@@ -1328,8 +1412,13 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
         const bool halves = kHalves && (epilog == EPI_BIAS || epilog == EPI_RELU_BIAS ||
                                         epilog == EPI_GELU_BIAS || epilog == EPI_NONE ||
                                         epilog == EPI_TANH_BIAS);
+        // Split-K across a cluster through L2: the peers' partial sums of this warp's chunks,
+        // copied into its slots in shared memory at the start (below), have landed.
+        if (!PAIR && w.split > 1 && p.split_l2) cp_async_wait_all();
+        int own_index = -1;  // owned chunks so far (split-K)
         for (int c = part; c < (reduce_done ? nchunks : 0); c += kParts) {
             if (split_owner(quarter, c, w.split) != w.rank) continue;
+            ++own_index;
             if constexpr (kHalves) {
                 if (halves) {
                     float bcur = 0.0f;  // more warps: this lane's bias value for the chunk
@@ -1418,7 +1507,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
             for (int j = 0; j < CH; ++j) v[j] = __uint_as_float(r[j]);
             if (w.split > 1) {
                 // Add the other ranks' partial sums of this chunk (distributed shared
-                // memory) in batches of 16-byte units: every load of a batch (units x
+                // memory, or the workspace in L2) in batches of 16-byte units: every load of a batch (units x
                 // peers) is issued before any is consumed, so one remote round trip serves
                 // a whole 16-column chunk (two units per trip for 32-column chunks, whose
                 // registers are needed elsewhere).
@@ -1433,8 +1522,15 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
                             const uint32_t peer = static_cast<uint32_t>(pi < w.rank ? pi : pi + 1);
 #pragma unroll
                             for (int uu = 0; uu < kUB; ++uu)
-                                part[pi][uu] = ld_shared_cluster_v4(map_shared_rank(
-                                    sbase + red_offset<BN>(row, c * (CH / 4) + u0 + uu), peer));
+                                part[pi][uu] =
+                                    p.split_l2
+                                        ? *reinterpret_cast<const float4*>(
+                                              smem + l2_slots +
+                                              (own_index * (w.split - 1) + pi) * (128 * CH) +
+                                              ((u0 + uu) * 32 + lane) * 16)
+                                        : ld_shared_cluster_v4(map_shared_rank(
+                                              sbase + red_offset<BN>(row, c * (CH / 4) + u0 + uu),
+                                              peer));
                         }
                     }
 #pragma unroll
@@ -1773,7 +1869,9 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1) gemm_epi_kernel(const __grid_
         if (warp >= 2 && !*abort_flag)
             run_epilogue<BN, SWAP, PAIR, EPI, F8>(p, smem, sbase, bar0, tmem_base, abort_flag);
         __syncwarp();
-        cluster_sync_all();  // the peers are done reading this CTA's partial sums
+        // the peers are done reading this CTA's partial sums (in its shared memory; those in
+        // the workspace are next written by a later grid, after this one has completed)
+        if (!p.split_l2) cluster_sync_all();
     }
 
     tcgen05_fence_before_sync();

@@ -96,6 +96,11 @@ struct GemmParams {
     int split_global;
     float* split_ws;
     unsigned* split_count;
+    // Split-K across a cluster whose partial sums meet in split_ws (same layout, slice =
+    // cluster rank) instead of in the peers' shared memory: split_l2 == 1, split_global == 0.
+    // Each CTA writes the partials of the chunks it does not own, the cluster barrier orders
+    // them, and each owner reads its peers' partials from L2 (split_count is not used).
+    int split_l2;
     // CTA-pair kernels: order of the tiles.  sched == nullptr: static, pair q takes tiles
     // q, q + pairs, q + 2 pairs, ...  Otherwise each pair takes tile q first and then the
     // tile pairs + atomicAdd(&sched[0], 1) each time it starts one, until the walk ends;

@@ -34,6 +34,7 @@ struct gemm_epi_plan_s {
     int variant, bn, stages, smem, grid, group_m, tiles_m, tiles_n, k_blocks;
     int split, kb_per_split;  // split-K slices (split == 1: persistent kernel)
     int split_global;         // 1: the slices meet in device memory, 0: in a cluster
+    int split_l2;             // cluster slices whose partial sums meet in device memory
     int dyn_order;            // CTA-pair kernel: tiles handed out by the device counter
     int swap_m64;             // swapped kernel with 64 MMA rows (columns of D) per tile
     int box_k;                // small-m kernel: rows of k per copy of B

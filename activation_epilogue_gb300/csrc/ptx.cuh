@@ -114,6 +114,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 }
 
 // Prefetch one box of a 2-D tiled tensor into L2 (no shared memory, no completion).
+// 16-byte asynchronous copy from global (cached in L2 only) into shared memory, and the
+// wait for all of this thread's such copies (generic proxy: ordered by the usual acquire /
+// release synchronisation, no proxy fence).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t c0, int32_t c1)
 {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

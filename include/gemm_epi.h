@@ -166,7 +166,10 @@ typedef enum {
                                        device-memory workspace the plan owns (slices 1..8;
                                        the last CTA of a tile adds them in slice order);
                                        1 = within a thread-block cluster over distributed
-                                       shared memory (slices 1..4) */
+                                       shared memory (slices 1..4); 3 = within a cluster,
+                                       the partial sums passing through a device-memory
+                                       workspace the plan owns (slices 1..4; each rank
+                                       adds the peers' sums of the chunks it owns) */
     GEMM_EPI_OPT_TILE_M = 10,       /* swapped kernel: columns of D per tile (MMA rows), 128
                                        (the automatic choice) or 64 (on request; only the
                                        epilogs BIAS, RELU_BIAS, GELU_BIAS, NONE, TANH_BIAS,

@@ -1,7 +1,8 @@
 """The C ABI from a plain C11 program (tests/c_caller.c): the header compiles as C with
 warnings as errors and every call the program makes links against libgemmepi.so (CPU);
 on a GPU the program runs RELU_AUX_BIAS plans for the swapped, row-tile and CTA-pair
-kernels and checks D and the mask bit for bit against integer arithmetic."""
+kernels and checks D and the mask bit for bit against integer arithmetic, then runs the FFN
+block in each of its modes (and without allocation) against its own double-precision sum."""
 import os
 import shutil
 import subprocess
@@ -31,7 +32,7 @@ def _compile(tmp_path):
     exe = str(tmp_path / "c_caller")
     cmd = [cc, "-std=c11", "-O2", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
            "-I", os.path.join(cuda, "include"), SRC, "-L", libdir, "-lgemmepi", "-L", cudalib,
-           "-lcudart", f"-Wl,-rpath,{libdir}", f"-Wl,-rpath,{cudalib}", "-o", exe]
+           "-lcudart", "-lm", f"-Wl,-rpath,{libdir}", f"-Wl,-rpath,{cudalib}", "-o", exe]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
     return exe
@@ -53,3 +54,6 @@ def test_c_caller_runs(tmp_path):
     # the three kernels the shapes are meant to reach
     for variant in ("variant=small-m", "variant=swapped", "variant=row-tile", "variant=row-pair"):
         assert variant in r.stdout, r.stdout
+    # the FFN block's modes
+    for mode in ("ffn one launch:", "ffn two launches:", "ffn one launch, H on chip", "ffn noalloc"):
+        assert mode in r.stdout, r.stdout

@@ -146,8 +146,11 @@ def test_smallm_option_rules():
             plan.set_option("SPLIT_K", 1)     # one 1024-deep slab per CTA does not fit
         assert e.value.status == 1
     with gemm_epi.Plan(16, 264, 16384, "bf16", "BIAS", "1N") as plan:
-        # K slabs of 2048 do not fit in shared memory: the swapped kernel
-        assert "variant=swapped" in plan.describe()
+        # K slabs of 2048 do not fit in shared memory: not the small-m kernel; over 256 K
+        # blocks, row tiles with K split over a cluster (the swapped kernel would stream
+        # each 128-column panel of B through one of 3 SMs)
+        d = plan.describe()
+        assert "variant=row-tile" in d and "(cluster+L2)" in d, d
         with pytest.raises(gemm_epi.GemmEpiError) as e:
             plan.set_option("VARIANT", 5)
         assert e.value.status == 1
@@ -584,10 +587,15 @@ def test_ffn_split2_order_independent():
     assert torch.equal(outs[0], outs[1])
 
 
-# ---- split-K: partial sums through device memory (mode 2) or across a cluster (mode 1) -----
+# ---- split-K: partial sums through device memory (mode 2), across a cluster (mode 1), or
+# across a cluster through an L2 workspace (mode 3) ------------------------------------------
+
+SPLIT_WHERE = {1: "(cluster)", 2: "(device memory)", 3: "(cluster+L2)"}
 
 SPLIT_CASES = [(1, 1, 64, 2), (1, 1, 128, 3), (1, 1, 256, 4), (1, 1, 64, 4),
                (1, 2, 0, 2), (1, 2, 0, 3), (1, 2, 0, 4),
+               (3, 1, 64, 2), (3, 1, 128, 3), (3, 1, 256, 4), (3, 1, 128, 4),
+               (3, 2, 0, 2), (3, 2, 0, 4),
                (2, 1, 64, 2), (2, 1, 128, 3), (2, 1, 256, 4), (2, 1, 64, 8),
                (2, 2, 0, 2), (2, 2, 0, 6), (2, 2, 0, 8), (2, 2, 16, 5)]
 
@@ -603,11 +611,11 @@ def test_split_k_parity(mode, variant, bn, split, epilog):
         opts["TILE_N"] = bn
     _, _, _, _, desc = check(p, m, n, k, "bf16", epilog, layout, options=opts)
     kpb = -(-16 // split)                       # K blocks per slice; no slice is left empty
-    where = "(device memory)" if mode == 2 else "(cluster)"
-    assert f"split_k={-(-16 // kpb)}{where}" in desc
+    assert f"split_k={-(-16 // kpb)}{SPLIT_WHERE[mode]}" in desc
 
 
-@pytest.mark.parametrize("mode,variant,split", [(1, 1, 4), (1, 2, 3), (2, 1, 4), (2, 2, 6)])
+@pytest.mark.parametrize("mode,variant,split", [(1, 1, 4), (1, 2, 3), (2, 1, 4), (2, 2, 6),
+                                                (3, 1, 4), (3, 1, 2), (3, 2, 3)])
 def test_split_k_integer_bit_exact(mode, variant, split):
     m, n, k = (256 if variant == 1 else 16), 264, 512
     p = _inputs(m, n, k, "bf16", "1N", seed=31, kind="int")
@@ -628,6 +636,35 @@ def test_split_k_device_memory_repeats_and_is_deterministic():
         assert "split_k=7(device memory)" in plan.describe()
         for seed in (1, 2):
             p = _inputs(m, n, k, "bf16", "1N", seed=500 + seed)
+            A, B, bias = p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev)
+            outs = []
+            for _ in range(4):
+                D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+                plan.execute(A, B, bias, D)
+                outs.append(D)
+            assert plan.sync_status() == 0
+            for D in outs[1:]:
+                assert torch.equal(D, outs[0])
+            want, _ = oracle_ref(p, "bf16", "GELU_BIAS", "1N")
+            assert rel_err(outs[0], want) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("variant,bn,m", [(1, 128, 300), (2, 0, 24)])
+def test_split_k_cluster_l2_repeats_and_is_deterministic(variant, bn, m):
+    # Cluster slices whose partial sums pass through the workspace: the owner adds its own
+    # and the peers' sums in rank order, so repeated launches (each a programmatic dependent
+    # of the one before, rewriting the workspace) give the same bits.
+    from parity_helpers import oracle_ref
+    n, k = 776, 1544
+    dev = torch.device("cuda")
+    with gemm_epi.Plan(m, n, k, "bf16", "GELU_BIAS", "1N", variant=variant) as plan:
+        if bn:
+            plan.set_option("TILE_N", bn)
+        plan.set_option("SPLIT_K", 4)
+        plan.set_option("SPLIT_MODE", 3)
+        assert "split_k=4(cluster+L2)" in plan.describe()
+        for seed in (1, 2):
+            p = _inputs(m, n, k, "bf16", "1N", seed=700 + seed)
             A, B, bias = p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev)
             outs = []
             for _ in range(4):
@@ -669,12 +706,13 @@ def test_split_option_rules():
             plan.set_option("SPLIT_K", 9)
         assert e.value.status == 1
         with pytest.raises(gemm_epi.GemmEpiError) as e:
-            plan.set_option("SPLIT_MODE", 3)
+            plan.set_option("SPLIT_MODE", 4)
         assert e.value.status == 1
-        plan.set_option("SPLIT_MODE", 1)
-        with pytest.raises(gemm_epi.GemmEpiError) as e:
-            plan.set_option("SPLIT_K", 5)            # a cluster holds at most 4 slices
-        assert e.value.status == 1
+        for mode in (1, 3):
+            plan.set_option("SPLIT_MODE", mode)
+            with pytest.raises(gemm_epi.GemmEpiError) as e:
+                plan.set_option("SPLIT_K", 5)        # a cluster holds at most 4 slices
+            assert e.value.status == 1
         plan.set_option("SPLIT_MODE", 2)
         plan.set_option("SPLIT_K", 5)
         assert "split_k=4(device memory)" in plan.describe()   # 16 K blocks: 4 x 4
@@ -766,14 +804,34 @@ def test_swapped_m64_option_rules():
 
 
 def test_row_tiles_over_long_k_split_in_a_cluster():
-    # 64 row tiles of 128 x 64 on 152 SMs over 32 K blocks: two K slices through a cluster
+    # 64 row tiles of 128 x 64 on 152 SMs over 32 K blocks: the model's choice, 32 tiles of
+    # 128 x 128 in 4 K slices through a cluster, the partial sums through L2
     with gemm_epi.Plan(1024, 512, 2048, "f16", "BIAS", "M1") as plan:
         d = plan.describe()
-    assert "variant=row-tile" in d and "split_k=2(cluster)" in d, d
+        assert "variant=row-tile" in d and "tile=128x128" in d and "split_k=4(cluster+L2)" in d, d
+        plan.set_option("SPLIT_MODE", 1)               # the same slices over DSMEM
+        assert "tile=128x128" in plan.describe() and "split_k=4(cluster) " in plan.describe()
+        plan.set_option("SPLIT_MODE", 0)
+        plan.set_option("TILE_N", 64)                  # a fixed width: the slices for it
+        assert "tile=128x64" in plan.describe() and "split_k=2(cluster+L2)" in plan.describe()
     with gemm_epi.Plan(1024, 512, 512, "f16", "BIAS", "M1") as plan:   # 8 K blocks: no split
         assert "split_k=1 " in plan.describe()
     p = _inputs(1024, 512, 2048, "f16", "M1", seed=1001)
     check(p, 1024, 512, 2048, "f16", "BIAS", "M1")
+    check(p, 1024, 512, 2048, "f16", "BIAS", "M1", options={"SPLIT_MODE": 1})
+
+
+@pytest.mark.parametrize("m,n,k,variant", [(256, 1024, 8192, "row-tile"), (64, 3072, 8192, "row-tile"),
+                                           (256, 3072, 768, "swapped"), (100, 3072, 768, "swapped"),
+                                           (200, 512, 256, "swapped")])
+def test_small_m_long_k_plan_choice(m, n, k, variant):
+    # m <= 256 beyond the small-m kernel: the swapped kernel, unless K is long enough that
+    # row tiles with K split over a cluster are well ahead in the model
+    p = _inputs(m, n, k, "bf16", "1N", seed=3100 + m)
+    _, _, _, _, desc = check(p, m, n, k, "bf16", "BIAS", "1N")
+    assert f"variant={variant}" in desc, desc
+    if variant == "row-tile":
+        assert "(cluster+L2)" in desc, desc
 
 
 @pytest.mark.parametrize("m,epilog,variant", [

@@ -45,9 +45,9 @@ def _case(i):
     if variant == 2 and r.random() < 0.3:
         opts["TILE_N"] = r.choice([16, 32, 64, 128, 256])
     if variant in (1, 2) and r.random() < 0.3:
-        mode = r.choice([1, 2])                  # cluster, device memory
+        mode = r.choice([1, 2, 3])               # cluster, device memory, cluster via L2
         opts["SPLIT_MODE"] = mode
-        opts["SPLIT_K"] = r.randint(2, 4 if mode == 1 else 8)
+        opts["SPLIT_K"] = r.randint(2, 8 if mode == 2 else 4)
     return dict(m=m, n=n, k=k, dtype=r.choice(["bf16", "f16"]), epilog=r.choice(EPILOGS),
                 layout=r.choice(["M1", "1N"]), opts=opts, unfused=r.random() < 0.15,
                 seed=r.randint(0, 10 ** 6))
