@@ -162,14 +162,21 @@ typedef enum {
                                        programmatic dependent of the previous work on the
                                        stream (its set-up overlaps that work; every global
                                        access still waits for it); 0: plain launch */
-    GEMM_EPI_OPT_SPLIT_MODE = 9,    /* split-K partial sums: 0 (default) or 2 = through a
-                                       device-memory workspace the plan owns (slices 1..8;
-                                       the last CTA of a tile adds them in slice order);
-                                       1 = within a thread-block cluster over distributed
-                                       shared memory (slices 1..4); 3 = within a cluster,
-                                       the partial sums passing through a device-memory
-                                       workspace the plan owns (slices 1..4; each rank
-                                       adds the peers' sums of the chunks it owns) */
+    GEMM_EPI_OPT_SPLIT_MODE = 9,    /* how the K slices' partial sums meet.  With SPLIT_K
+                                       set: 0 (default) or 2 = through a device-memory
+                                       workspace the plan owns (slices 1..8; the last CTA of
+                                       a tile adds them in slice order); 1 = within a
+                                       thread-block cluster over distributed shared memory
+                                       (slices 1..4); 3 = within a cluster, through a
+                                       device-memory workspace the plan owns (slices 1..4;
+                                       each rank adds the peers' sums of the chunks it
+                                       owns, in rank order).  Without SPLIT_K a row-tile
+                                       plan (and a plan of m <= 256 that would otherwise
+                                       run the swapped kernel) may take 2..4 slices per
+                                       tile by itself, with the tile width, where a per-SM
+                                       time model puts that ahead: through the cluster
+                                       and L2 (0 or 3), over distributed shared memory (1);
+                                       2 turns that choice off */
     GEMM_EPI_OPT_TILE_M = 10,       /* swapped kernel: columns of D per tile (MMA rows), 128
                                        (the automatic choice) or 64 (on request; only the
                                        epilogs BIAS, RELU_BIAS, GELU_BIAS, NONE, TANH_BIAS,
