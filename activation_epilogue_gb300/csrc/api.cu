@@ -539,12 +539,12 @@ void release_split_ws(gemm_epi_plan_s* p)
 
 bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,
                uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw,
-               uint64_t elem_bytes)
+               uint64_t elem_bytes, uint64_t row_elems)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * elem_bytes};
+    const cuuint64_t strides[1] = {(row_elems ? row_elems : inner) * elem_bytes};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -592,10 +592,12 @@ gemm_epi_status ensure_maps(gemm_epi_plan_s* p, const void* A, const void* B, vo
     const uint32_t a_rows = rows_of_a ? 128u : static_cast<uint32_t>(p->bn);
     if (!encode_2d(&p->tm_A, A, dt, p->k, p->m, 64, a_rows, CU_TENSOR_MAP_SWIZZLE_128B))
         return GEMM_EPI_ERR_LAUNCH;
-    if (!encode_2d(&p->tm_B, B, dt, p->n, p->k, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode_2d(&p->tm_B, B, dt, p->n, p->k, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, 2,
+                   static_cast<uint64_t>(p->ldb)))
         return GEMM_EPI_ERR_LAUNCH;
     if (rows_of_a) {
-        if (!encode_2d(&p->tm_D, D, dt, p->n, p->m, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        if (!encode_2d(&p->tm_D, D, dt, p->n, p->m, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, 2,
+                       static_cast<uint64_t>(p->ldd)))
             return GEMM_EPI_ERR_LAUNCH;
     } else {
         // swapped kernel: boxes of 32 columns (16 with 64-column tiles) x (up to) 32 rows

@@ -38,6 +38,9 @@ struct gemm_epi_plan_s {
     int dyn_order;            // CTA-pair kernel: tiles handed out by the device counter
     int swap_m64;             // swapped kernel with 64 MMA rows (columns of D) per tile
     int box_k;                // small-m kernel: rows of k per copy of B
+    // Row strides of B and D in elements (0: n, the dense layout).  Set only on the host
+    // pipeline's column-panel plans (a panel of B and of D inside the full matrices).
+    int64_t ldb, ldd;
     // options (0 = automatic)
     int opt_variant, opt_bn, opt_split_k, opt_grid, opt_group_m, opt_split_mode, opt_tile_m;
     int opt_tile_order;
@@ -78,7 +81,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p);
 void release_split_ws(gemm_epi_plan_s* p);
 bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,
                uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw,
-               uint64_t elem_bytes = 2);
+               uint64_t elem_bytes = 2, uint64_t row_elems = 0);
 gemm_epi_status ensure_maps(gemm_epi_plan_s* p, const void* A, const void* B, void* D);
 gemm_epi_status check_device(const gemm_epi_plan_s* p);
 // The current device, checked to be sm_103, and its SM count.

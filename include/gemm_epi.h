@@ -278,11 +278,14 @@ gemm_epi_status gemm_epi_execute_operands(gemm_epi_plan_t p, const gemm_epi_oper
  * until `stream` reaches this point).  Forward epilogs on fp16/bf16 plans.
  *
  * The rows of A, D, residual and aux are processed in chunks (at most 32, of ~1024 rows or
- * more) on three streams the plan owns: the copy in of chunk j+1, the GEMM of chunk j and
- * the copy out of chunk j-1 run at the same time, with three device slots per chunked
- * operand; B and the bias are copied once per call.  The first call allocates the plan's
- * device buffers (three A chunks, three D chunks, B, bias, and residual / aux chunks when
- * the epilog has them) and creates its streams and events; a changed plan option rebuilds
+ * more) on three streams the plan owns: the copies in run ahead, and the GEMM of chunk j
+ * and the copy out of chunk j-1 run at the same time, with three device slots per output
+ * (D, aux) and up to one per chunk, within 2 GiB, per input (A, residual); B and the bias
+ * are copied once per call.  When B is 32 MiB or more and the epilog writes D alone (BIAS,
+ * RELU_BIAS, GELU_BIAS, NONE, TANH_BIAS), the first chunks' rows of A are copied first and
+ * B follows in column panels, each followed by those chunks' columns of D, so that D starts
+ * leaving before all of B has arrived.  The first call allocates the plan's device buffers
+ * (the slots, B, bias) and creates its streams and events; a changed plan option rebuilds
  * them.  Host buffers should be page-locked (cudaHostAlloc / pinned): pageable memory
  * works but its copies are slower and less overlapped.
  */

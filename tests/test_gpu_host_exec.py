@@ -120,3 +120,34 @@ def test_execute_host_large_chunks_pair_kernel():
     assert rel_err(D[rows], want) <= TOL["bf16"]
     words = aux[rows].numpy().view(np.uint32)
     assert aux_bad_bits(words, pre, AUX_BAND) == 0
+
+
+@pytest.mark.parametrize("m,n,k,dtype,epilog,layout", [
+    (4096, 8192, 2048, "bf16", "RELU_BIAS", "1N"),    # 2 panels of 4096 over 3 chunks
+    (4096, 8200, 2048, "f16", "GELU_BIAS", "M1"),     # panels of 4352 and 3848 columns
+    (3072, 8192, 2048, "bf16", "NONE", "1N"),         # exactly 3 chunks, all in panels
+    (3300, 12288, 2048, "bf16", "TANH_BIAS", "1N"),   # 2 full chunks in panels, a shorter one after
+    (8192, 16384, 2048, "bf16", "BIAS", "1N"),        # 2 panels of 8192, then 5 more chunks
+])
+def test_execute_host_column_panels(m, n, k, dtype, epilog, layout):
+    # B of 32 MiB or more: the first chunks' columns of D are computed panel by panel of B
+    # while B is still coming in; the whole result must equal the same plan on device
+    # buffers bit for bit (the same K order per element), and rows on chunk edges the oracle
+    p = workloads.random_problem(m, n, k, dtype=dtype, bias_layout=layout, residual=False,
+                                 seed=m + n)
+    with gemm_epi.Plan(m, n, k, dtype, epilog, layout) as plan:
+        D, _ = _run_host(p, m, n, k, dtype, epilog, layout, plan=plan)
+        dev = torch.device("cuda")
+        Dd = torch.empty((m, n), dtype=TD[dtype], device=dev)
+        bias = p["bias"].to(dev) if epilog != "NONE" else None
+        plan.execute(p["A"].to(dev), p["B"].to(dev), bias, Dd)
+        assert plan.sync_status() == 0
+    assert torch.equal(D, Dd.cpu())
+    chunks = max(1, min(32, m // 1024))       # the pipeline's rows per chunk
+    chunk = min(m, -(-(-(-m // chunks)) // 128) * 128)
+    rows = sorted(r for r in {0, 1, chunk - 1, chunk, 2 * chunk - 1, 2 * chunk, 3 * chunk, m - 1}
+                  if r < m)
+    want = oracle.gemm_epi(p["A"][rows], p["B"], None if epilog == "NONE" else
+                           (p["bias"][rows] if layout == "M1" else p["bias"]),
+                           dtype=dtype, epilog=epilog, bias_layout=layout)
+    assert rel_err(D[rows], want) <= TOL[dtype]
