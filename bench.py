@@ -496,13 +496,18 @@ def measure_e2e(plan, w, A, B, bias, D, aux, stream, args):
     def e2e_step():
         plan.execute_host(Ah, Bh, bh, Dh, aux=auxh)
 
+    # The host link and host memory are shared with the machine's other GPUs: a single call
+    # now and then takes 18-130 ms instead of 13.5 (seen with every build), so the figure is
+    # the median of three timed runs of `steps` calls each (every run reported).
     steps = max(2, min(args.steps, 5))
-    secs = time_steps(e2e_step, steps, 1, stream)
+    runs = [time_steps(e2e_step, steps, 1 if r == 0 else 0, stream) for r in range(3)]
+    secs = sorted(runs)[1]
     h2d = (A.numel() + B.numel() + bias.numel()) * A.element_size()
     d2h = D.numel() * D.element_size() + (0 if aux is None else aux.numel() * 4)
     return {"value": float(w.flops) * steps / secs / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": secs / steps * 1e3, "steps": steps}
+            "ms_per_step": secs / steps * 1e3, "steps": steps, "stat": "median of 3 runs",
+            "runs_ms_per_step": [round(r / steps * 1e3, 3) for r in runs]}
 
 
 def measure_extras(plan, w, A, B, bias, D, aux, stream, peaks):
