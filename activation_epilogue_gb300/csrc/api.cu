@@ -7,6 +7,7 @@
 // and bias layout and chooses the kernel configuration ("nvmath-python: cuBLAS and cuSOLVER
 // bindings", matmul-planning checklist: plan() picks the algorithm); execute() is
 // asynchronous; free() releases the plan.
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -113,11 +114,27 @@ double rowtile_us(int64_t m, int64_t n, int k_blocks, int sm_count, int bn)
 }
 
 // Row tiles with K split over a cluster, partial sums through L2: over the tile widths
-// (fixed_bn, or 64, 128 and 256) and 2 to 4 slices whose tiles x slices fit one wave and
-// whose slices are at least 4 K blocks deep, the fastest in the model.  At 1024 x 512 x 2048
+// (fixed_bn, or 64, 128 and 256) and 2 to 4 slices whose clusters are all resident at once
+// (cudaOccupancyMaxActiveClusters: clusters of 3 leave SMs of a GPC unused, so 48 of them
+// did not fit and ran as two waves, 15.7 against 9.2 us at 256 x 3072 x 768) and whose
+// slices are at least 4 K blocks deep, the fastest in the model.  At 1024 x 512 x 2048
 // BIAS fp16 (hot / L2 flushed): 128 x 128 tiles in 4 slices 9.8 / 9.9 us (the choice), in 3
 // 10.2 / 10.6, 128 x 256 in 4 10.5 / 11.1, 128 x 64 in 2 10.8 / 11.3, unsplit 12.2 / 12.7;
 // the same 4 slices over distributed shared memory 15.2 / 16.1 us.
+// rowtile_max_clusters per (width, slices), queried once per process (every device of a
+// process is taken to be the same GPU model, as elsewhere in the planner)
+int max_clusters_cached(int bn, int split)
+{
+    static std::atomic<int> cache[3][kMaxClusterSplit + 1];
+    static std::atomic<bool> known[3][kMaxClusterSplit + 1];
+    const int w = bn == 64 ? 0 : bn == 128 ? 1 : 2;
+    if (!known[w][split].load()) {
+        cache[w][split].store(rowtile_max_clusters(bn, split));
+        known[w][split].store(true);
+    }
+    return cache[w][split].load();
+}
+
 bool pick_auto_split(int64_t m, int64_t n, int k_blocks, int sm_count, int fixed_bn, int* bn_out,
                      int* split_out, double* us_out)
 {
@@ -129,6 +146,7 @@ bool pick_auto_split(int64_t m, int64_t n, int k_blocks, int sm_count, int fixed
         for (int s = 2; s <= kMaxClusterSplit; ++s) {
             const int kpb = (k_blocks + s - 1) / s;
             if (tiles * s > sm_count || kpb < 4) continue;
+            if (tiles > max_clusters_cached(bn, s)) continue;
             const double t = slab_us(kpb, bn, rowtile_rate(bn)) +
                              (s - 1.0) / s * 128.0 * bn * 4.0 / kPartialOutRate + kSplitFixedUs;
             if (t < best) {

@@ -74,6 +74,16 @@ cudaError_t rowtile_launch(int bn, const GemmParams& p, int grid, cudaStream_t s
     }
 }
 
+int rowtile_max_clusters(int bn, int split)
+{
+    switch (bn) {
+#define F(X) case X: return single_max_clusters<X, false, -1>(split);
+        GEMM_EPI_ROWTILE_CASES(F)
+#undef F
+    default: return 0;
+    }
+}
+
 int rowtile_smem_bytes(int bn)
 {
     switch (bn) {

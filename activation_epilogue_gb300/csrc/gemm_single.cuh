@@ -42,6 +42,34 @@ cudaError_t single_launch(const GemmParams& p, int grid, cudaStream_t stream, bo
     return cudaLaunchKernelEx(&cfg, gemm_epi_kernel<BN, SWAP, false, EPI>, p);
 }
 
+// Clusters of `split` CTAs of this kernel that the GPU holds at once (0 if the query fails).
+template <int BN, bool SWAP, int EPI>
+int single_max_clusters(int split)
+{
+    if (single_prepare<BN, SWAP, EPI>() != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(split), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = TileCfg<BN>::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_epi_kernel<BN, SWAP, false, EPI>, &cfg) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 #define GEMM_EPI_ROWTILE_CASES(F) F(64) F(128) F(256)
 #define GEMM_EPI_SWAPPED_CASES(F) F(16) F(32) F(64) F(128) F(256)
 

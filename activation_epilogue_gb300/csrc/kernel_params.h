@@ -157,6 +157,8 @@ cudaError_t rowtile_prepare(int bn);
 // pdl: launch as a programmatic dependent of the previous grid on the stream.
 cudaError_t rowtile_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
 int rowtile_smem_bytes(int bn);
+// Clusters of `split` row-tile CTAs of width bn that the GPU holds at once.
+int rowtile_max_clusters(int bn, int split);
 int rowtile_stages(int bn);
 
 // Row-tile (swap = false) and swapped (swap = true) kernels built for one forward epilog:

@@ -823,7 +823,8 @@ def test_row_tiles_over_long_k_split_in_a_cluster():
 
 @pytest.mark.parametrize("m,n,k,variant", [(256, 1024, 8192, "row-tile"), (64, 3072, 8192, "row-tile"),
                                            (256, 3072, 768, "swapped"), (100, 3072, 768, "swapped"),
-                                           (200, 512, 256, "swapped")])
+                                           (200, 512, 256, "swapped"), (256, 3072, 1536, "swapped"),
+                                           (256, 4096, 4096, "row-tile")])
 def test_small_m_long_k_plan_choice(m, n, k, variant):
     # m <= 256 beyond the small-m kernel: the swapped kernel, unless K is long enough that
     # row tiles with K split over a cluster are well ahead in the model
@@ -832,6 +833,18 @@ def test_small_m_long_k_plan_choice(m, n, k, variant):
     assert f"variant={variant}" in desc, desc
     if variant == "row-tile":
         assert "(cluster+L2)" in desc, desc
+
+
+def test_auto_split_clusters_all_resident():
+    # 48 tiles of 128 x 128 in clusters of 3 do not all fit on the GPU at once (a GPC's SMs
+    # are not a multiple of 3), so the automatic choice never takes them
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for m, n, k in [(256, 3072, 1536), (256, 3072, 768), (384, 2048, 3072)]:
+        with gemm_epi.Plan(m, n, k, "bf16", "GELU_BIAS", "1N") as plan:
+            fields = dict(kv.split("=", 1) for kv in plan.describe().split() if "=" in kv)
+        split = int(fields["split_k"].split("(")[0])
+        if split > 1:
+            assert int(fields["grid"]) <= sms and split != 3, fields
 
 
 @pytest.mark.parametrize("m,epilog,variant", [
