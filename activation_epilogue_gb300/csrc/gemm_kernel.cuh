@@ -1743,8 +1743,10 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
             __syncwarp();
         }
     }
-    // Shared memory may be released once the stores have read it; the grid's writes are
-    // complete when the grid is.
+    // Shared memory may be released once the stores have read it, and once this lane's
+    // copies of peers' partial sums (split-K through L2) have landed, also when the tile
+    // loop was left early; the grid's writes are complete when the grid is.
+    if constexpr (!PAIR) cp_async_wait_all();
     if (lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
 }

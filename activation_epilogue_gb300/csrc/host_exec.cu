@@ -105,17 +105,29 @@ int64_t host_chunk_rows(int64_t m)
     return rows < m ? rows : m;
 }
 
-gemm_epi_status chunk_plan(const gemm_epi_plan_s* p, int64_t rows, gemm_epi_plan_s* c)
+// The fields a chunk or panel plan takes from the parent (shape set by the caller); it shares
+// the parent's status word and tile counter (its launches run in stream order on one stream).
+void derive_plan(const gemm_epi_plan_s* p, int64_t rows, int64_t cols, gemm_epi_plan_s* c)
 {
     memset(c, 0, sizeof(*c));
     c->m = rows;
-    c->n = p->n;
+    c->n = cols;
     c->k = p->k;
     c->dtype = p->dtype;
     c->epilog = p->epilog;
     c->bias_layout = p->bias_layout;
     c->device = p->device;
     c->sm_count = p->sm_count;
+    c->prefetch = p->prefetch;
+    c->no_pdl = p->no_pdl;
+    c->wait_limit_ns = p->wait_limit_ns;
+    c->d_status = p->d_status;
+    c->d_sched = p->d_sched;
+}
+
+gemm_epi_status chunk_plan(const gemm_epi_plan_s* p, int64_t rows, gemm_epi_plan_s* c)
+{
+    derive_plan(p, rows, p->n, c);
     c->opt_variant = p->opt_variant;
     c->opt_bn = p->opt_bn;
     c->opt_split_k = p->opt_split_k;
@@ -123,11 +135,6 @@ gemm_epi_status chunk_plan(const gemm_epi_plan_s* p, int64_t rows, gemm_epi_plan
     c->opt_tile_m = p->opt_tile_m;
     c->opt_grid = p->opt_grid;
     c->opt_group_m = p->opt_group_m;
-    c->prefetch = p->prefetch;
-    c->no_pdl = p->no_pdl;
-    c->wait_limit_ns = p->wait_limit_ns;
-    c->d_status = p->d_status;
-    c->d_sched = p->d_sched;  // (the chunk launches run in stream order on one stream)
     c->opt_tile_order = p->opt_tile_order;
     return configure(c);
 }
@@ -148,21 +155,8 @@ bool panel_epilog(int e)
 
 gemm_epi_status panel_plan(const gemm_epi_plan_s* p, int64_t rows, int64_t width, gemm_epi_plan_s* c)
 {
-    memset(c, 0, sizeof(*c));
-    c->m = rows;
-    c->n = width;
-    c->k = p->k;
-    c->dtype = p->dtype;
-    c->epilog = p->epilog;
-    c->bias_layout = p->bias_layout;
-    c->device = p->device;
-    c->sm_count = p->sm_count;
+    derive_plan(p, rows, width, c);
     c->opt_split_k = 1;  // no split-K workspace
-    c->prefetch = p->prefetch;
-    c->no_pdl = p->no_pdl;
-    c->wait_limit_ns = p->wait_limit_ns;
-    c->d_status = p->d_status;
-    c->d_sched = p->d_sched;
     c->ldb = p->n;
     c->ldd = p->n;
     gemm_epi_status st = configure(c);
