@@ -19,8 +19,9 @@
 //     counted in bytes on one mbarrier of the receiver, so every SM takes in the same small
 //     share; each rank adds its rows' partials in rank order (the sum does not depend on
 //     arrival order), adds the bias, applies the activation and writes its R rows of D (and
-//     the mask or the stored pre-activation) with plain coalesced stores, one thread per
-//     column of D.  One kernel per epilog; the exchange and the epilogue are rolled loops
+//     the mask or the stored pre-activation) with plain coalesced stores, two threads per
+//     column of D taking alternate groups of four rows (with one per column, one warp per
+//     scheduler, the loop was bound by the latency of its dependent steps).  One kernel per epilog; the exchange and the epilogue are rolled loops
 //     over a shared-memory copy of the accumulator (the kernel runs for a few microseconds,
 //     and there an instruction-cache miss costs as much as a row's arithmetic).
 // The copies, the MMAs and the partial sums are waited for with a time limit; on expiry the
@@ -36,7 +37,14 @@ namespace gemm_epi {
 namespace {
 
 constexpr int kSmTN = 128;            // columns of D per tile (MMA M)
-constexpr int kSmThreads = 128;       // one thread per TMEM lane (column of D)
+// Threads per CTA: one per column of D (TMEM lane) for 16-row tiles, two for wider ones,
+// where the first 128 read the accumulator and both halves take part in the exchange and the
+// epilogue, taking alternate groups of four rows.  Measured on GB300 (GELU X[T,768].W[768,3072],
+// CUDA graph, hot / L2 flushed): T = 32 4.15 -> 4.03 / 5.8 -> 5.7-5.8 us, T = 64 5.35 -> 5.14 /
+// 7.0 -> 6.8-6.9 us; at T = 16 (one row group per rank) the extra warps only cost: 3.61 ->
+// 3.78 / 5.0 -> 5.4 us.
+__host__ __device__ constexpr int sm_threads(int bn) { return bn >= 32 ? 256 : 128; }
+constexpr int kSmMaxSplit = 8;        // K slices per cluster at most
 
 // Shared-memory layout of one CTA (offsets from a 1024-byte aligned base):
 //   [B panels: 2 x kc rows x 128 B][A boxes: kc/64 x BN rows x 128 B]
@@ -117,7 +125,7 @@ __device__ __forceinline__ void load_acc(uint32_t taddr, float (&v)[BN])
 }
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(kSmThreads, 1) smallm_kernel(const __grid_constant__ GemmParams p)
+__global__ void __launch_bounds__(sm_threads(BN), 1) smallm_kernel(const __grid_constant__ GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -214,7 +222,10 @@ __global__ void __launch_bounds__(kSmThreads, 1) smallm_kernel(const __grid_cons
     }
     __syncwarp();
 
-    // ---- every thread: its column's BN accumulator values ------------------------------------
+    // ---- the first 128 threads: their column's BN accumulator values -----------------------
+    const int cidx = static_cast<int>(threadIdx.x) & (kSmTN - 1);  // column of the tile
+    const int half = static_cast<int>(threadIdx.x) / kSmTN;        // first row group
+    constexpr int kHalves = sm_threads(BN) / kSmTN;                // row-group stride
     float v[BN];
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     if (!sm_wait(bar0 + 8u * kSmBarMma, 0, p.wait_limit_ns)) {
@@ -222,7 +233,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) smallm_kernel(const __grid_cons
         sm_fail(p.status);
     }
     tcgen05_fence_after_sync();
-    if (ok) {
+    if (ok && half == 0) {
         load_acc<BN>(t_lane, v);
     } else {
 #pragma unroll
@@ -235,7 +246,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) smallm_kernel(const __grid_cons
         tcgen05_fence_after_sync();
         tmem_dealloc(tmem, BN < 32 ? 32 : BN);
     }
-    const int col = n0 + threadIdx.x;       // this thread's column of D
+    const int col = n0 + cidx;              // this thread's column of D
     const bool col_ok = col < pn;
 
     // Bias, residual and the outputs may belong to a programmatic predecessor grid.
@@ -262,13 +273,19 @@ __global__ void __launch_bounds__(kSmThreads, 1) smallm_kernel(const __grid_cons
     // exchange and the epilogue below are rolled loops that read it back (unrolled over BN
     // rows with run-time tests of which rows a rank owns, each row ran code fetched for the
     // first time, one instruction-cache miss per row).
-    const uint32_t mine = sbase + static_cast<uint32_t>(L.mine_off()) + static_cast<uint32_t>(threadIdx.x * 16);
-    const uint32_t part = sbase + static_cast<uint32_t>(L.part_off()) + static_cast<uint32_t>(threadIdx.x * 16);
+    const uint32_t mine = sbase + static_cast<uint32_t>(L.mine_off()) + static_cast<uint32_t>(cidx * 16);
+    const uint32_t part = sbase + static_cast<uint32_t>(L.part_off()) + static_cast<uint32_t>(cidx * 16);
+    // (the same, for plain loads that the compiler may schedule around the stores to D)
+    const float4* mine_p = reinterpret_cast<const float4*>(smem + L.mine_off()) + cidx;
+    const float4* part_p = reinterpret_cast<const float4*>(smem + L.part_off()) + cidx;
+    if (half == 0) {
 #pragma unroll
-    for (int j4 = 0; j4 < BN / 4; ++j4)
-        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(mine + static_cast<uint32_t>(j4 * kSmTN * 16)),
-                     "f"(v[4 * j4]), "f"(v[4 * j4 + 1]), "f"(v[4 * j4 + 2]), "f"(v[4 * j4 + 3])
-                     : "memory");
+        for (int j4 = 0; j4 < BN / 4; ++j4)
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(mine + static_cast<uint32_t>(j4 * kSmTN * 16)),
+                         "f"(v[4 * j4]), "f"(v[4 * j4 + 1]), "f"(v[4 * j4 + 2]), "f"(v[4 * j4 + 3])
+                         : "memory");
+    }
+    __syncthreads();  // (the second half reads the columns the first half stored)
     if (S > 1) {
         // ---- reduce-scatter: each peer's rows to it, then this rank's rows from them ------
         cluster_wait();
@@ -276,12 +293,8 @@ __global__ void __launch_bounds__(kSmThreads, 1) smallm_kernel(const __grid_cons
             if (q == rank) continue;
             const int slot = rank < q ? rank : rank - 1;
             const uint32_t qbar = map_shared_rank(bar0 + 8u * kSmBarPart, static_cast<uint32_t>(q));
-            for (int g = 0; g < R / 4; ++g) {
-                float4 a;
-                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                             : "=f"(a.x), "=f"(a.y), "=f"(a.z), "=f"(a.w)
-                             : "r"(mine + static_cast<uint32_t>((q * (R / 4) + g) * kSmTN * 16))
-                             : "memory");
+            for (int g = half; g < R / 4; g += kHalves) {
+                const float4 a = mine_p[(q * (R / 4) + g) * kSmTN];
                 const uint32_t dst = part + static_cast<uint32_t>((slot * (R / 4) + g) * kSmTN * 16);
                 st_async_v4(map_shared_rank(dst, static_cast<uint32_t>(q)), a.x, a.y, a.z, a.w, qbar);
             }
@@ -295,22 +308,21 @@ __global__ void __launch_bounds__(kSmThreads, 1) smallm_kernel(const __grid_cons
     if (ok) {
         // ---- this rank's rows: own partial + the senders' in rank order, then the epilogue ----
         uint16_t* D = static_cast<uint16_t*>(pD);
-        for (int g = 0; g < R / 4; ++g) {
-            float4 a;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(a.x), "=f"(a.y), "=f"(a.z), "=f"(a.w)
-                         : "r"(mine + static_cast<uint32_t>((lo / 4 + g) * kSmTN * 16))
-                         : "memory");
-            for (int sl = 0; sl < S - 1; ++sl) {
-                float4 w;
-                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                             : "=f"(w.x), "=f"(w.y), "=f"(w.z), "=f"(w.w)
-                             : "r"(part + static_cast<uint32_t>((sl * (R / 4) + g) * kSmTN * 16))
-                             : "memory");
-                a.x += w.x;
-                a.y += w.y;
-                a.z += w.z;
-                a.w += w.w;
+        for (int g = half; g < R / 4; g += kHalves) {
+            float4 a = mine_p[(lo / 4 + g) * kSmTN];
+            // the senders' partial sums in rank order (all loads issued before the adds)
+            float4 w[kSmMaxSplit - 1];
+#pragma unroll
+            for (int sl = 0; sl < kSmMaxSplit - 1; ++sl)
+                if (sl < S - 1) w[sl] = part_p[(sl * (R / 4) + g) * kSmTN];
+#pragma unroll
+            for (int sl = 0; sl < kSmMaxSplit - 1; ++sl) {
+                if (sl < S - 1) {
+                    a.x += w[sl].x;
+                    a.y += w[sl].y;
+                    a.z += w[sl].z;
+                    a.w += w[sl].w;
+                }
             }
             const float xs[4] = {a.x, a.y, a.z, a.w};
             float rb[4] = {0.0f, 0.0f, 0.0f, 0.0f}, rr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -332,7 +344,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) smallm_kernel(const __grid_cons
                 float x = xs[e] + cb + rb[e];
                 if constexpr (EPI == EPI_RELU_AUX_BIAS) {
                     const uint32_t word = __ballot_sync(0xFFFFFFFFu, col_ok && x > 0.0f);
-                    const int widx = (n0 + warp * 32) / 32;
+                    const int widx = (n0 + (warp & 3) * 32) / 32;
                     if (lane == 0 && row < pm && widx < paux_ld)
                         static_cast<uint32_t*>(paux)[static_cast<long long>(row) * paux_ld + widx] = word;
                 } else if constexpr (EPI == EPI_GELU_AUX_BIAS) {
@@ -378,12 +390,12 @@ const void* smallm_fn(int bn, int epilog)
     return nullptr;
 }
 
-cudaError_t smallm_launch_fn(const void* fn, const GemmParams& p, int grid, int smem,
+cudaError_t smallm_launch_fn(const void* fn, const GemmParams& p, int grid, int smem, int threads,
                              cudaStream_t stream, bool pdl)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(kSmThreads, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -438,7 +450,7 @@ int smallm_max_clusters(int bn, int split, int smem)
     if (!f) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(split), 1, 1);
-    cfg.blockDim = dim3(kSmThreads, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(sm_threads(bn)), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -459,7 +471,7 @@ cudaError_t smallm_launch(int bn, const GemmParams& p, int grid, int smem, cudaS
 {
     const void* f = smallm_fn(bn, p.epilog);
     if (!f) return cudaErrorInvalidValue;
-    return smallm_launch_fn(f, p, grid, smem, stream, pdl);
+    return smallm_launch_fn(f, p, grid, smem, sm_threads(bn), stream, pdl);
 }
 
 }  // namespace gemm_epi
