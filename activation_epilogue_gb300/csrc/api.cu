@@ -42,16 +42,15 @@ EncodeTiledFn encode_fn()
     return g_encode;
 }
 
-// Split-K is used only when GEMM_EPI_OPT_SPLIT_K asks for it.  Measured on GB300 it does
-// not pay on the under-filled shapes tried.  Through a cluster (DSMEM): 1024x512x2048
-// 15.5 us unsplit vs 19-20 us split; GELU T=16/64/256 x 3072 x 768 9.2/11.1/16.8 us unsplit
-// vs 10.2/22/28 us with split 4 (T=16 graph-replayed: 6.5 us against 6.8 us, the one gain).
-// Through device memory: GELU T=16 x 3072 x 768 with 2/4/6 slices 13.0/13.0/13.5 us cold,
-// 8.1/7.5/7.5 us hot, against 11.0 / 6.8 us unsplit; the publish, count and reload of the
-// partial tiles cost more than the shorter K loop saves.  Narrower swapped tiles (below)
-// add CTAs without any of that.  The one automatic split: row tiles that leave half the
-// SMs idle over 16 or more K blocks take 2 to 4 slices through a cluster, their partial
-// sums meeting in L2 (pick_auto_split).
+// Split-K on the swapped kernel is used only when GEMM_EPI_OPT_SPLIT_K asks for it: measured
+// on GB300 it did not pay there.  GELU T=16/64/256 x 3072 x 768 through a cluster (DSMEM):
+// 9.2/11.1/16.8 us unsplit vs 10.2/22/28 us with split 4 (T=16 graph-replayed: 6.5 us
+// against 6.8 us, the one gain); through device memory with 2/4/6 slices at T=16:
+// 13.0/13.0/13.5 us cold, 8.1/7.5/7.5 us hot, against 11.0 / 6.8 us unsplit (narrower
+// swapped tiles, below, add CTAs without any exchange; m <= 64 now runs the small-m
+// kernel).  Row tiles take 2 to 4 K slices through a cluster by themselves where the time
+// model says so, the partial sums meeting in L2 (pick_auto_split), and so do plans of
+// m <= 256 with a long K that would otherwise run the swapped kernel.
 constexpr int kMaxClusterSplit = 4;  // CTAs per cluster (kernel: kMaxSplit)
 constexpr int kMaxGlobalSplit = 8;   // K slices through device memory (kernel: kMaxGSplit)
 

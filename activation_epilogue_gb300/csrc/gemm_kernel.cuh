@@ -30,16 +30,19 @@
 // registers until the tile is done, sums across the 32 lanes of a warp come from one
 // transpose-and-add butterfly; either way one fp32 atomic per warp and bias entry per tile.
 //
-// Split-K (small grids), two forms.  Cluster: the CTAs of a cluster share one output tile,
-// each accumulating a slice of K in its own TMEM.  The tile's 32-column chunks are owned
-// round-robin by the cluster ranks; every CTA writes the partial sums of the chunks it does
-// not own into its (by then idle) stage ring, the cluster synchronises, and each owner adds
-// the peers' partials over distributed shared memory before running the epilogue on its
-// chunks (or, with split_l2, the partials go to a device-memory workspace and the owners
-// read them from L2: an SM moves data to and from L2 several times faster than over
-// distributed shared memory).  Device memory: independent CTAs write their fp32 partial tiles to a workspace
-// (it stays in L2) and count themselves per tile; the CTA that arrives last adds the
-// slices in slice order and runs the epilogue.  No CTA waits for another.
+// Split-K (small grids), three forms.  Cluster: the CTAs of a cluster share one output tile,
+// each accumulating a slice of K in its own TMEM.  The tile's (lane quarter, 32-column
+// chunk) blocks are owned by the ranks in a cycle along each epilogue warp's chunks
+// (split_owner); every CTA publishes the blocks it does not own, the cluster synchronises,
+// and each owner adds the peers' blocks in rank order before running the epilogue on its
+// chunks.  The blocks meet either in a device-memory workspace (split_l2: stored with
+// st.global, copied back into the owner's idle stage ring with cp.async right after the
+// barrier; an SM moves data to and from L2 several times faster than over distributed
+// shared memory) or in the publishing CTA's idle stage ring, read by the owners over
+// distributed shared memory.  Device memory alone: independent CTAs write their fp32
+// partial tiles to a workspace (it stays in L2) and count themselves per tile; the CTA that
+// arrives last adds the slices in slice order and runs the epilogue.  No CTA waits for
+// another.
 //
 // Every mbarrier wait is bounded by a time limit; on expiry the waiting thread records the
 // failure in the plan's status word and raises a shared abort flag, every role leaves its

@@ -84,7 +84,8 @@ struct GemmParams {
     // Split-K across a thread-block cluster: split > 1 launches tiles * split CTAs in
     // clusters of `split`; rank r of a cluster accumulates K blocks
     // [r * kb_per_split, (r + 1) * kb_per_split) of the cluster's tile, and the partial
-    // sums are added on chip (distributed shared memory) before the epilogue.
+    // sums are added before the epilogue (over distributed shared memory, or through L2
+    // with split_l2 below).
     int split;
     int kb_per_split;
     // Split-K through device memory instead (split_global == 1, split > 1): tiles * split
@@ -96,8 +97,10 @@ struct GemmParams {
     int split_global;
     float* split_ws;
     unsigned* split_count;
-    // Split-K across a cluster whose partial sums meet in split_ws (same layout, slice =
-    // cluster rank) instead of in the peers' shared memory: split_l2 == 1, split_global == 0.
+    // Split-K across a cluster whose partial sums meet in split_ws instead of in the peers'
+    // shared memory (split_l2 == 1, split_global == 0), laid out as blocks of 32 rows x one
+    // chunk (4 KB at 32 columns), [tile][rank][lane quarter][chunk], each [16-byte unit][lane],
+    // so that a warp's stores and copies of a block are contiguous 512-byte runs.
     // Each CTA writes the partials of the chunks it does not own, the cluster barrier orders
     // them, and each owner reads its peers' partials from L2 (split_count is not used).
     int split_l2;
