@@ -101,6 +101,10 @@ VARIANTS = [
     ("split2_swapped", 24, 264, 264, {"VARIANT": 2, "SPLIT_K": 2}),
     ("split3_rowtile_cluster", 260, 264, 520, {"VARIANT": 1, "TILE_N": 128, "SPLIT_K": 3,
                                                "SPLIT_MODE": 1}),
+    ("split4_rowtile_cluster_l2", 260, 264, 520, {"VARIANT": 1, "TILE_N": 128, "SPLIT_K": 4,
+                                                  "SPLIT_MODE": 3}),
+    ("split2_swapped_cluster_l2", 40, 392, 776, {"VARIANT": 2, "SPLIT_K": 2, "SPLIT_MODE": 3}),
+    ("auto_split_rowtile", 1024, 512, 2048, None),
     ("split6_swapped", 40, 392, 776, {"VARIANT": 2, "TILE_N": 16, "SPLIT_K": 6}),
     ("swapped_narrow", 100, 392, 200, {"VARIANT": 2, "TILE_N": 32}),
     ("pair_static", 1000, 520, 200, {"VARIANT": 3, "TILE_ORDER": 1}),

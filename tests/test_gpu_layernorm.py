@@ -154,6 +154,8 @@ VARIANTS = [
     ("pair_dynamic_walk", 1000, 600, 136, {"VARIANT": 3, "TILE_ORDER": 2, "GRID": 4}),
     ("split3", 260, 264, 520, {"VARIANT": 1, "TILE_N": 128, "SPLIT_K": 3}),
     ("split3_cluster", 260, 264, 520, {"VARIANT": 1, "TILE_N": 128, "SPLIT_K": 3, "SPLIT_MODE": 1}),
+    ("split4_cluster_l2", 260, 264, 520, {"VARIANT": 1, "TILE_N": 128, "SPLIT_K": 4, "SPLIT_MODE": 3}),
+    ("auto_split", 1024, 512, 2048, None),
     ("small_m_default", 16, 3072, 768, None),
     ("default", 1000, 776, 328, None),
 ]
