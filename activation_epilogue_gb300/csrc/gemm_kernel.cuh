@@ -888,8 +888,8 @@ __device__ __forceinline__ long long gsplit_index(const GemmParams& p, int tile,
 
 // Split-K across a cluster through L2 (split_l2): float4 index, in the workspace, of 16-byte
 // unit u of lane `lane` in the block (lane quarter q, chunk c) of cluster rank s's partial
-// sums of tile `tile`.  A block (32 rows x CH columns, 128 * CH bytes) is contiguous, so
-// its owner fetches it with one bulk copy; in it, unit u of the 32 lanes is 512 bytes.
+// sums of tile `tile`.  A block (32 rows x CH columns, 128 * CH bytes) is contiguous; in
+// it, unit u of the 32 lanes is 512 contiguous bytes (one warp-wide store or copy).
 template <int BN>
 __device__ __forceinline__ long long l2split_index(const GemmParams& p, int tile, int s, int q,
                                                    int c, int u, int lane)
@@ -1509,11 +1509,12 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, uint8_t* smem,
 #pragma unroll
             for (int j = 0; j < CH; ++j) v[j] = __uint_as_float(r[j]);
             if (w.split > 1) {
-                // Add the other ranks' partial sums of this chunk (distributed shared
-                // memory, or the workspace in L2) in batches of 16-byte units: every load of a batch (units x
-                // peers) is issued before any is consumed, so one remote round trip serves
-                // a whole 16-column chunk (two units per trip for 32-column chunks, whose
-                // registers are needed elsewhere).
+                // Add the other ranks' partial sums of this chunk (over distributed shared
+                // memory, or from this warp's slots, which hold the blocks copied from L2) in
+                // batches of 16-byte units: every load of a batch (units x peers) is issued
+                // before any is consumed, so one remote round trip serves a whole 16-column
+                // chunk (two units per trip for 32-column chunks, whose registers are needed
+                // elsewhere).
                 const int row = quarter * 32 + lane;
                 constexpr int kUB = CH == 16 ? 4 : 2;
 #pragma unroll
