@@ -129,14 +129,14 @@ def test_execute_host_large_chunks_pair_kernel():
     (3300, 12288, 2048, "bf16", "TANH_BIAS", "1N"),   # 2 full chunks in panels, a shorter one after
     (8192, 16384, 2048, "bf16", "BIAS", "1N"),        # 2 panels of 8192, then 5 more chunks
 ])
-def test_execute_host_column_panels(m, n, k, dtype, epilog, layout):
+def test_execute_host_column_panels(m, n, k, dtype, epilog, layout, pinned=True):
     # B of 32 MiB or more: the first chunks' columns of D are computed panel by panel of B
     # while B is still coming in; the whole result must equal the same plan on device
     # buffers bit for bit (the same K order per element), and rows on chunk edges the oracle
     p = workloads.random_problem(m, n, k, dtype=dtype, bias_layout=layout, residual=False,
                                  seed=m + n)
     with gemm_epi.Plan(m, n, k, dtype, epilog, layout) as plan:
-        D, _ = _run_host(p, m, n, k, dtype, epilog, layout, plan=plan)
+        D, _ = _run_host(p, m, n, k, dtype, epilog, layout, plan=plan, pinned=pinned)
         dev = torch.device("cuda")
         Dd = torch.empty((m, n), dtype=TD[dtype], device=dev)
         bias = p["bias"].to(dev) if epilog != "NONE" else None
@@ -151,3 +151,13 @@ def test_execute_host_column_panels(m, n, k, dtype, epilog, layout):
                            (p["bias"][rows] if layout == "M1" else p["bias"]),
                            dtype=dtype, epilog=epilog, bias_layout=layout)
     assert rel_err(D[rows], want) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("m,n,k,dtype,epilog,layout", [
+    (4096, 8192, 2048, "bf16", "RELU_BIAS", "1N"),
+    (3300, 12288, 2048, "f16", "GELU_BIAS", "M1"),
+])
+def test_execute_host_column_panels_pageable(m, n, k, dtype, epilog, layout):
+    # the same with pageable host buffers (the 2-D copies of B's panels and D's columns are
+    # staged by the driver)
+    test_execute_host_column_panels(m, n, k, dtype, epilog, layout, pinned=False)
