@@ -161,3 +161,21 @@ def test_execute_host_column_panels_pageable(m, n, k, dtype, epilog, layout):
     # the same with pageable host buffers (the 2-D copies of B's panels and D's columns are
     # staged by the driver)
     test_execute_host_column_panels(m, n, k, dtype, epilog, layout, pinned=False)
+
+
+def test_execute_host_chunks_with_automatic_split():
+    # chunk plans of 1024 x 512 x 2048 take K slices through a cluster and L2 by themselves
+    # (each chunk plan owns its workspace); bias along the rows, offset per chunk
+    m, n, k = 2048, 512, 2048
+    p = workloads.random_problem(m, n, k, dtype="f16", bias_layout="M1", residual=False, seed=77)
+    with gemm_epi.Plan(m, n, k, "f16", "BIAS", "M1") as plan:
+        D, _ = _run_host(p, m, n, k, "f16", "BIAS", "M1", plan=plan)
+        dev = torch.device("cuda")
+        Dd = torch.empty((m, n), dtype=torch.float16, device=dev)
+        plan.execute(p["A"].to(dev), p["B"].to(dev), p["bias"].to(dev), Dd)
+        assert plan.sync_status() == 0
+    rows = [0, 1, 1023, 1024, 1025, 2047]
+    want = oracle.gemm_epi(p["A"][rows], p["B"], p["bias"][rows], dtype="f16", epilog="BIAS",
+                           bias_layout="M1")
+    assert rel_err(D[rows], want) <= TOL["f16"]
+    assert rel_err(Dd.cpu()[rows], want) <= TOL["f16"]
