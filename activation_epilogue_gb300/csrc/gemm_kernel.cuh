@@ -441,11 +441,15 @@ __device__ __forceinline__ uint16_t to16(float a, int bf16)
 // ------------------------------------------------------------------------------------------
 // producer: TMA loads
 // ------------------------------------------------------------------------------------------
-// Arm stage `stage` for K block `kb` of tile (tm, tn) and issue its TMA loads.
-template <int BN, bool SWAP, bool PAIR = false, bool F8 = false>
+// Arm stage `stage` for K block `kb` of tile (tm, tn) and issue its TMA loads.  Single
+// CTAs only, PART = 1: arm the stage and copy B alone; PART = 2: copy A alone (into a stage
+// that PART 1 armed).
+template <int BN, bool SWAP, bool PAIR = false, bool F8 = false, int PART = 0>
 __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase, uint32_t bar0,
                                             int stage, int tm, int tn, int kb, int prob = 0)
 {
+    static_assert(PART == 0 || !PAIR, "CTA pairs copy a stage in one part");
+    constexpr bool kArm = PART != 2, kCopyA = PART != 1, kCopyB = PART != 2;
     using C = TileCfg<BN, PAIR>;
     const uint32_t fb = bar0 + 8u * (kBarFull + stage);
     const uint32_t sa = sbase + stage * C::kStageBytes;
@@ -487,21 +491,25 @@ __device__ __forceinline__ void issue_stage(const GemmParams& p, uint32_t sbase,
         return;
     }
     if (!SWAP) {
-        mbar_arrive_expect_tx(fb, C::kStageBytes);
-        tma_load_2d(sa, &p.tm_A, fb, k0, tm * kBM);
+        if (kArm) mbar_arrive_expect_tx(fb, C::kStageBytes);
+        if (kCopyA) tma_load_2d(sa, &p.tm_A, fb, k0, tm * kBM);
+        if (kCopyB) {
 #pragma unroll
-        for (int q = 0; q < BN / 64; ++q)
-            tma_load_2d(sb + q * 8192, &p.tm_B, fb, tn * BN + q * 64, k0);
+            for (int q = 0; q < BN / 64; ++q)
+                tma_load_2d(sb + q * 8192, &p.tm_B, fb, tn * BN + q * 64, k0);
+        }
     } else if (p.swap_m64) {
         // 64 MMA rows: one 64-column box of B (the second half of the A area stays unused)
-        mbar_arrive_expect_tx(fb, C::kStageBytes - 8192);
-        tma_load_2d(sa, &p.tm_B, fb, tm * 64, k0);
-        tma_load_2d(sb, &p.tm_A, fb, k0, tn * BN);
+        if (kArm) mbar_arrive_expect_tx(fb, C::kStageBytes - 8192);
+        if (kCopyB) tma_load_2d(sa, &p.tm_B, fb, tm * 64, k0);
+        if (kCopyA) tma_load_2d(sb, &p.tm_A, fb, k0, tn * BN);
     } else {
-        mbar_arrive_expect_tx(fb, C::kStageBytes);
-        tma_load_2d(sa, &p.tm_B, fb, tm * kBM, k0);
-        tma_load_2d(sa + 8192, &p.tm_B, fb, tm * kBM + 64, k0);
-        tma_load_2d(sb, &p.tm_A, fb, k0, tn * BN);
+        if (kArm) mbar_arrive_expect_tx(fb, C::kStageBytes);
+        if (kCopyB) {
+            tma_load_2d(sa, &p.tm_B, fb, tm * kBM, k0);
+            tma_load_2d(sa + 8192, &p.tm_B, fb, tm * kBM + 64, k0);
+        }
+        if (kCopyA) tma_load_2d(sb, &p.tm_A, fb, k0, tn * BN);
     }
 }
 
@@ -534,12 +542,21 @@ __device__ __forceinline__ int producer_prologue(const GemmParams& p, uint32_t s
     using C = TileCfg<BN>;
     const WorkRange w = work_range(p);
     if (w.first >= w.end || p.debug_stall) return 0;
-    // Under a programmatic dependent launch the operands may come from the previous grid.
-    grid_dependency_wait();
     int tm, tn;
     tile_coords(w.first, p, tm, tn);
     const int n = min(C::kStages, w.kb_end - w.kb_begin);
-    for (int i = 0; i < n; ++i) issue_stage<BN, SWAP>(p, sbase, bar0, i, tm, tn, w.kb_begin + i);
+    // Under a programmatic dependent launch the operands may come from the previous grid;
+    // B not, when the plan was told so (b_ready): its stages are copied before the wait.
+    if (p.b_ready) {
+        for (int i = 0; i < n; ++i)
+            issue_stage<BN, SWAP, false, false, 1>(p, sbase, bar0, i, tm, tn, w.kb_begin + i);
+        grid_dependency_wait();
+        for (int i = 0; i < n; ++i)
+            issue_stage<BN, SWAP, false, false, 2>(p, sbase, bar0, i, tm, tn, w.kb_begin + i);
+    } else {
+        grid_dependency_wait();
+        for (int i = 0; i < n; ++i) issue_stage<BN, SWAP>(p, sbase, bar0, i, tm, tn, w.kb_begin + i);
+    }
     for (int i = 0; i < p.prefetch && w.kb_begin + n + i < w.kb_end; ++i)
         prefetch_stage<BN, SWAP>(p, tm, tn, w.kb_begin + n + i);
     return n;

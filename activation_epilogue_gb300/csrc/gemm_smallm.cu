@@ -166,8 +166,9 @@ __global__ void __launch_bounds__(sm_threads(BN), 1) smallm_kernel(const __grid_
         // The copies first: everything else of the set-up overlaps their flight.
         // (debug_stall: no copy is issued, so the wait below runs out its time limit)
         if (!p.debug_stall) {
-            // Under a programmatic dependent launch the operands may come from the previous grid.
-            grid_dependency_wait();
+            // Under a programmatic dependent launch the operands may come from the previous
+            // grid: B too, unless the plan was told that grid does not write it (b_ready).
+            if (!p.b_ready) grid_dependency_wait();
             const uint32_t full = bar0 + 8u * kSmBarFull;
             mbar_arrive_expect_tx(full, static_cast<uint32_t>(L.b_bytes() + L.a_bytes()));
             // B: two 64-column panels of kc rows (k), in boxes of box_k rows (box_k divides kc)
@@ -176,12 +177,25 @@ __global__ void __launch_bounds__(sm_threads(BN), 1) smallm_kernel(const __grid_
                 for (int kk = 0; kk < kc; kk += boxk)
                     tma_load_2d(b_smem + static_cast<uint32_t>(pnl * kc * 128 + kk * 128), &p.tm_B,
                                 full, n0 + pnl * 64, k0 + kk);
+            if (p.b_ready) grid_dependency_wait();
             // A: kc / 64 boxes of BN rows x 64 k
             for (int b = 0; b < kc / 64; ++b)
                 tma_load_2d(a_smem + static_cast<uint32_t>(b * BN * 128), &p.tm_A, full, k0 + b * 64, t0);
         }
         // every peer's partial sums of this rank's rows, on one barrier
         if (S > 1) mbar_arrive_expect_tx(bar0 + 8u * kSmBarPart, static_cast<uint32_t>(L.part_bytes()));
+    }
+    // Without b_ready under a programmatic dependent launch: this CTA's slab of B (kc rows
+    // of 128 columns, up to three 128-byte lines a row) brought into L2 while the previous
+    // grid may still run; the copies above then find it there once the wait returns.
+    if (p.b_l2 != nullptr && threadIdx.x >= 32) {
+        const char* b = static_cast<const char*>(p.b_l2);
+        for (int i = static_cast<int>(threadIdx.x) - 32; i < 3 * kc;
+             i += static_cast<int>(blockDim.x) - 32) {
+            const int r = k0 + i / 3;
+            const int c = min(n0 + (i % 3) * 64 - (i % 3 == 2 ? 1 : 0), pn - 1);
+            if (r < p.k) prefetch_global_l2(b + (static_cast<long long>(r) * p.b_ld + c) * 2);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(holder), BN < 32 ? 32 : BN);

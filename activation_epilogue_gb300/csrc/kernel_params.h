@@ -120,6 +120,16 @@ struct GemmParams {
     int swap_m64;
     // Small-m kernel: rows of k per copy of B (divides the K slice kb_per_split * 64).
     int box_k;
+    // Launched as a programmatic dependent, the kernel may start while the previous grid on
+    // the stream still runs.  b_ready == 1: nothing that grid does writes B (a weight that
+    // stays in place), so the small-m kernel and the single-CTA producers copy B's first K
+    // blocks into shared memory before waiting for that grid, and A after.  b_l2 != nullptr
+    // (small-m kernel, without b_ready): B's element (0, 0), with row stride b_ld elements;
+    // the CTA's threads bring its slab of B into L2 at entry (L2 is coherent with that grid's
+    // writes, so this needs no promise) and the copies into shared memory follow the wait.
+    int b_ready;
+    const void* b_l2;
+    long long b_ld;
     // The producer also prefetches into L2 the operand boxes of the K block this many
     // blocks ahead of the one it loads (0 = off), so that a first touch of a panel in
     // device memory overlaps the loads of the blocks before it.

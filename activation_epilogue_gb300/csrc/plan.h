@@ -51,6 +51,7 @@ struct gemm_epi_plan_s {
     size_t split_ws_bytes, split_count_len;
     int prefetch;  // L2 prefetch distance in K blocks (GEMM_EPI_OPT_PREFETCH)
     int no_pdl;    // 1: launch without programmatic dependent launch (GEMM_EPI_OPT_PDL = 0)
+    int b_ready;   // 1: no earlier work on the stream writes B (GEMM_EPI_OPT_B_READY)
     unsigned long long wait_limit_ns;
     int debug_stall;
     int* d_status;

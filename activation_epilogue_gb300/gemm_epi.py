@@ -23,7 +23,7 @@ BACKWARD = ("DRELU_BGRAD", "DGELU_BGRAD")
 BIAS_LAYOUT = {"M1": 0, "1N": 1}
 OPTION = {"VARIANT": 0, "TILE_N": 1, "SPLIT_K": 2, "GRID": 3, "GROUP_M": 4,
           "WAIT_LIMIT_US": 5, "DEBUG_STALL": 6, "PREFETCH": 7, "PDL": 8, "SPLIT_MODE": 9,
-          "TILE_M": 10, "TILE_ORDER": 11}
+          "TILE_M": 10, "TILE_ORDER": 11, "B_READY": 12}
 STATUS = {0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED_SHAPE", 3: "ERR_MISALIGNED",
           4: "ERR_NO_DEVICE", 5: "ERR_ARCH", 6: "ERR_ALLOC", 7: "ERR_LAUNCH",
           8: "ERR_DEVICE_TIMEOUT", 9: "ERR_SCRATCH_LIMIT"}

@@ -128,6 +128,21 @@ def ffn_inputs(w: Ffn, device="cpu") -> dict:
     }
 
 
+def layer_stack_inputs(t: int, d: int, f: int, layers: int, *, dtype: str = "bf16",
+                       seed: int = 0, device="cpu") -> dict:
+    """A stack of FFN layers at small batch: X[t,d] ~ N(0,1), then for each layer W1[d,f],
+    b1[f], W2[f,d], b2[d] ~ N(0, 0.02) (the small-batch GELU_BIAS workload's and the FFN
+    block's distributions), drawn in that order; returns {"X": X, "layers": [(W1, b1, W2,
+    b2), ...]}."""
+    g = _generator(seed, device)
+    X = _draw(g, (t, d), 1.0, dtype, device)
+    stack = []
+    for _ in range(layers):
+        stack.append((_draw(g, (d, f), 0.02, dtype, device), _draw(g, (f,), 0.02, dtype, device),
+                      _draw(g, (f, d), 0.02, dtype, device), _draw(g, (d,), 0.02, dtype, device)))
+    return {"X": X, "layers": stack}
+
+
 def random_problem(m: int, n: int, k: int, *, dtype: str = "bf16", bias_layout: str = "1N",
                    residual: bool = False, seed: int = 0, kind: str = "normal",
                    sigma_a: float | None = None, device="cpu") -> dict:

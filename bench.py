@@ -577,6 +577,48 @@ def measure_extras(plan, w, A, B, bias, D, aux, stream, peaks):
     out["workloads"] = per
     out["backward"] = measure_backward(A.device, stream, flush, peaks)
     out["fp8"] = measure_fp8(A.device, stream, peaks)
+    out["layer_stack"] = measure_layer_stack(A.device, stream, peaks)
+    return out
+
+
+def measure_layer_stack(device, stream, peaks):
+    """Small-batch FFN layers back to back, as a decoder runs them: X[T,768] -> GELU_BIAS up
+    to 3072 -> BIAS_RESIDUAL down to 768 (in place: X += H.W2 + b2), 24 layers with weights
+    of their own (226 MB, more than L2, so each replay reads them from HBM again), captured
+    in a CUDA graph and replayed.  Microseconds per GEMM call with plain launches, with
+    programmatic dependent launch (the default), and with the weights promised ready
+    (B_READY: each call copies its weight while the previous call still runs)."""
+    import torch
+
+    from activation_epilogue_gb300 import gemm_epi, workloads
+    d, f, layers = 768, 3072, 24
+    out = {}
+    for t in (16, 64):
+        inp = workloads.layer_stack_inputs(t, d, f, layers, seed=4000 + t, device=device)
+        X = inp["X"].clone()
+        H = torch.empty((t, f), dtype=torch.bfloat16, device=device)
+        # bytes a call must move: weight, bias, input, output (and the residual)
+        up_bytes = (d * f + f + t * d + t * f) * 2
+        down_bytes = (f * d + d + t * f + t * d + t * d) * 2
+        call_bytes = (up_bytes + down_bytes) / 2
+        rec = {"bytes_per_call": call_bytes, "layers": layers}
+        for mode, opts in (("plain", {"PDL": 0}), ("pdl", {}), ("pdl_b_ready", {"B_READY": 1})):
+            with gemm_epi.Plan(t, f, d, "bf16", "GELU_BIAS", "1N", **opts) as up, \
+                    gemm_epi.Plan(t, d, f, "bf16", "BIAS_RESIDUAL", "1N", **opts) as down:
+                def stack():
+                    for W1, b1, W2, b2 in inp["layers"]:
+                        up.execute(X, W1, b1, H)
+                        down.execute(H, W2, b2, X, residual=X)
+                secs = min(time_graph(stack, 1, 20, stream) for _ in range(3))
+                us = secs / (2 * layers) * 1e6
+                rec[mode] = {"us_per_call": us,
+                             "hbm_gbs": call_bytes / (us * 1e-6) / 1e9,
+                             "hbm_frac": call_bytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+                             "status": up.sync_status() | down.sync_status(),
+                             "plans": [up.describe(), down.describe()]}
+        out[f"t{t}_d{d}_f{f}"] = rec
+        del inp, X, H
+        torch.cuda.empty_cache()
     return out
 
 
@@ -737,7 +779,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--only", choices=["backward", "ffn", "fp8", "small"],
+    ap.add_argument("--only", choices=["backward", "ffn", "fp8", "small", "stack"],
                     help="print only these measurements (one JSON object), for profiling")
     args = ap.parse_args(argv)
     if args.gpus < 1:
@@ -791,6 +833,8 @@ def rank_main(args):
             res = measure_fp8(dev, stream, load_peaks()[0])
         elif args.only == "small":
             res = run_small_for_ncu(dev)
+        elif args.only == "stack":
+            res = measure_layer_stack(dev, stream, load_peaks()[0])
         else:
             measure = measure_backward if args.only == "backward" else measure_ffn
             res = measure(dev, stream, flush_buf.zero_, load_peaks()[0])

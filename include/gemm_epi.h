@@ -182,7 +182,7 @@ typedef enum {
                                        epilogs BIAS, RELU_BIAS, GELU_BIAS, NONE, TANH_BIAS,
                                        BIAS_RESIDUAL and GELU_AUX_BIAS, without a K split,
                                        else ERR_INVALID_ARG); the other kernels ignore it */
-    GEMM_EPI_OPT_TILE_ORDER = 11    /* CTA-pair kernel: 2 = each pair takes its next tile,
+    GEMM_EPI_OPT_TILE_ORDER = 11,   /* CTA-pair kernel: 2 = each pair takes its next tile,
                                        in raster order, from a counter in the plan's device
                                        memory as it goes (the automatic choice from eight
                                        waves of tiles over the pairs up); 1 = static, pair q
@@ -190,6 +190,18 @@ typedef enum {
                                        below that); the other kernels ignore it.  With 2 the
                                        plan's launches must not overlap on the GPU (they
                                        share the counter) */
+    GEMM_EPI_OPT_B_READY = 12       /* 1: no earlier work on the stream writes B (a weight
+                                       that stays in place between calls), so under the
+                                       programmatic dependent launch (PDL = 1) the small-m,
+                                       swapped and single-CTA row-tile kernels copy B's
+                                       first K blocks into shared memory while that work
+                                       still runs, and only A's copies wait for it (the
+                                       CTA-pair kernels ignore it).  The caller keeps the
+                                       promise: B written by the previous kernel on the
+                                       stream gives undefined results.  0 (default): every
+                                       read waits; the small-m kernel then only brings its
+                                       slab of B into L2 ahead of the wait, which needs no
+                                       promise.  The host-buffer call ignores it */
 } gemm_epi_option;
 
 /*
