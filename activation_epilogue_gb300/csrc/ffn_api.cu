@@ -409,6 +409,12 @@ gemm_epi_status gemm_epi_ffn_set_option(gemm_epi_ffn_plan_t p, gemm_epi_ffn_opti
         if (value < 0 || value > 2) return GEMM_EPI_ERR_INVALID_ARG;
         field = &p->opt_order;
         break;
+    case GEMM_EPI_FFN_OPT_B_READY:
+        // (launch-time only: the GEMM plans' configuration does not change)
+        if (value != 0 && value != 1) return GEMM_EPI_ERR_INVALID_ARG;
+        p->g1->b_ready = static_cast<int>(value);
+        p->g2->b_ready = static_cast<int>(value);
+        return GEMM_EPI_OK;
     default: return GEMM_EPI_ERR_INVALID_ARG;
     }
     const int saved = *field;

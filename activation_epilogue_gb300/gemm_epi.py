@@ -39,7 +39,7 @@ EXPORTS = ["gemm_epi_plan", "gemm_epi_plan_set_option", "gemm_epi_execute",
            "gemm_epi_ffn_plan_describe", "gemm_epi_layernorm", "gemm_epi_layernorm_stats",
            "gemm_epi_layernorm_fold", "gemm_epi_ffn_plan_layernorm",
            "gemm_epi_ffn_execute_layernorm", "gemm_epi_execute_host"]
-FFN_OPTION = {"LAUNCHES": 0, "SPLIT2": 1, "TILE_ORDER": 2}
+FFN_OPTION = {"LAUNCHES": 0, "SPLIT2": 1, "TILE_ORDER": 2, "B_READY": 3}
 
 # Largest t * f the allocation-free FFN call accepts (its static scratch holds H).
 FFN_NOALLOC_MAX_HIDDEN = 16 * 1024 * 1024

@@ -413,10 +413,15 @@ typedef enum {
                                      trip through L2 costs more than the more even spread
                                      of work gains (4096 x 1024 x 4096 bf16: 94 us in 4
                                      slices, 66 us unsplit, 62 us in two launches). */
-    GEMM_EPI_FFN_OPT_TILE_ORDER = 2 /* one launch: 0 = automatic (static unsplit, dynamic when
-                                     GEMM 2 is split), 1 = static (pair q takes units q,
+    GEMM_EPI_FFN_OPT_TILE_ORDER = 2, /* one launch: 0 = automatic (static unsplit, dynamic
+                                     when GEMM 2 is split), 1 = static (pair q takes units q,
                                      q + pairs, ...), 2 = dynamic (each pair takes the next
                                      unit from a device counter as it becomes free). */
+    GEMM_EPI_FFN_OPT_B_READY = 3  /* 1: no earlier work on the stream writes W1 or W2 (the
+                                     layer's weights), so in two launches each GEMM copies
+                                     its weight ahead of its programmatic dependency (as
+                                     GEMM_EPI_OPT_B_READY; GEMM 2's may start before GEMM 1
+                                     ends).  0 (default): no promise. */
 } gemm_epi_ffn_option;
 
 gemm_epi_status gemm_epi_ffn_set_option(gemm_epi_ffn_plan_t p, gemm_epi_ffn_option opt,

@@ -132,9 +132,37 @@ def test_down_projection_plan_widens_the_row_tile(t):
     check_stack(inp, X, H, "bf16", descs)
 
 
+@pytest.mark.parametrize("t,d,f,b_ready", [(16, 768, 3072, 1), (16, 768, 3072, 0), (40, 264, 520, 1)])
+def test_ffn_calls_back_to_back(t, d, f, b_ready):
+    # the FFN entry point layer after layer (R = the layer's input), with the weights
+    # promised ready: each layer's Y against the oracle's FFN on that layer's GPU input
+    dev = torch.device("cuda")
+    layers = 3
+    inp = workloads.layer_stack_inputs(t, d, f, layers, seed=7300 + t + b_ready)
+    X = [inp["X"].to(dev)] + [torch.full((t, d), float("nan"), dtype=torch.bfloat16,
+                                         device=dev) for _ in range(layers)]
+    W = [[w.to(dev) for w in layer] for layer in inp["layers"]]
+    with gemm_epi.FfnPlan(t, d, f, b_ready=b_ready) as plan:
+        for l in range(layers):
+            W1, b1, W2, b2 = W[l]
+            plan.execute(X[l], W1, b1, W2, b2, X[l], X[l + 1])
+        torch.cuda.synchronize()
+        assert plan.sync_status() == 0
+        desc = plan.describe()
+    Xc = [x.cpu() for x in X]
+    for l, (W1, b1, W2, b2) in enumerate(inp["layers"]):
+        _, _, want = oracle.ffn(Xc[l], W1, b1, W2, b2, Xc[l], dtype="bf16")
+        err = rel_err(Xc[l + 1], want)
+        assert err <= TOL["bf16"], f"layer {l}: rel err {err:.3e} ({desc})"
+
+
 def test_b_ready_option_values():
     with gemm_epi.Plan(16, 256, 128, "bf16", "BIAS", "1N") as plan:
         plan.set_option("B_READY", 1)
         plan.set_option("B_READY", 0)
         with pytest.raises(gemm_epi.GemmEpiError):
             plan.set_option("B_READY", 2)
+    with gemm_epi.FfnPlan(16, 256, 512) as plan:
+        gemm_epi.gemm_epi_ffn_set_option(plan.handle, "B_READY", 1)
+        with pytest.raises(gemm_epi.GemmEpiError):
+            gemm_epi.gemm_epi_ffn_set_option(plan.handle, "B_READY", 2)
