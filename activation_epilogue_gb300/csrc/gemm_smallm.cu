@@ -276,6 +276,19 @@ __global__ void __launch_bounds__(sm_threads(BN), 1) smallm_kernel(const __grid_
         for (int i = 0; i < R && t0 + lo + i < pm; ++i)
             prefetch_global_l2(static_cast<const uint16_t*>(pres) +
                                static_cast<long long>(t0 + lo + i) * pn + col);
+    // The residual of this thread's first group of four rows, loaded now so that its latency
+    // overlaps the exchange (a thread's further groups, where it has several, load in the
+    // epilogue loop); kept as 16-bit words until used.
+    uint16_t rr0[4] = {0, 0, 0, 0};
+    if constexpr (EPI == EPI_BIAS_RESIDUAL) {
+        if (half < R / 4 && col_ok) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int row = t0 + lo + 4 * half + e;
+                if (row < pm) rr0[e] = static_cast<const uint16_t*>(pres)[static_cast<long long>(row) * pn + col];
+            }
+        }
+    }
     // Bias along the rows ((m,1) layout): this rank's R values into shared memory now, so
     // that the epilogue loop reads no global memory.
     float* rowb = reinterpret_cast<float*>(smem + L.rowb_off());
@@ -349,7 +362,8 @@ __global__ void __launch_bounds__(sm_threads(BN), 1) smallm_kernel(const __grid_
                 for (int e = 0; e < 4; ++e) {
                     const int row = t0 + lo + 4 * g + e;
                     if (row < pm && col_ok)
-                        rr[e] = load_16bit(pres, static_cast<long long>(row) * pn + col, pbf16);
+                        rr[e] = g == half ? decode16(rr0[e], pbf16)
+                                          : load_16bit(pres, static_cast<long long>(row) * pn + col, pbf16);
                 }
             }
 #pragma unroll
