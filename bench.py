@@ -582,8 +582,9 @@ def measure_extras(plan, w, A, B, bias, D, aux, stream, peaks):
 
 
 def measure_layer_stack(device, stream, peaks):
-    """Small-batch FFN layers back to back, as a decoder runs them: X[T,768] -> GELU_BIAS up
-    to 3072 -> BIAS_RESIDUAL down to 768 (in place: X += H.W2 + b2), 24 layers with weights
+    """Small-batch FFN layers back to back, as a decoder runs them (T = 16, 64, 256):
+    X[T,768] -> GELU_BIAS up to 3072 -> BIAS_RESIDUAL down to 768 (in place: X += H.W2 +
+    b2), 24 layers with weights
     of their own (226 MB, more than L2, so each replay reads them from HBM again), captured
     in a CUDA graph and replayed.  Microseconds per GEMM call with plain launches, with
     programmatic dependent launch (the default), and with the weights promised ready
@@ -593,7 +594,7 @@ def measure_layer_stack(device, stream, peaks):
     from activation_epilogue_gb300 import gemm_epi, workloads
     d, f, layers = 768, 3072, 24
     out = {}
-    for t in (16, 64):
+    for t in (16, 64, 256):
         inp = workloads.layer_stack_inputs(t, d, f, layers, seed=4000 + t, device=device)
         X = inp["X"].clone()
         H = torch.empty((t, f), dtype=torch.bfloat16, device=device)
