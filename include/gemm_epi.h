@@ -46,7 +46,8 @@
  *     default stream) and return launch-time errors only; a device-side wait that ran out
  *     its time limit is reported by gemm_epi_sync_status.  The fused kernel is launched as
  *     a programmatic dependent of the stream's previous work: it may start its set-up
- *     early, but reads and writes device memory only after that work has completed.
+ *     early, but reads and writes device memory only after that work has completed (except
+ *     B under GEMM_EPI_OPT_B_READY, and prefetches of B into L2, which change no result).
  *   - A plan belongs to the device that was current when it was made; execute with that
  *     device current.  Free it only after the work that uses it has completed.  One plan
  *     must not be executed from several host threads at the same time, and its launches
