@@ -210,32 +210,30 @@ bool smallm_epilog(int e)
            e == GEMM_EPI_TANH_BIAS || e == GEMM_EPI_GELU_AUX_BIAS;
 }
 
-bool pick_smallm_bn(int64_t n, int64_t k, int sms, int want_split, SmallMCfg* c);
+bool pick_smallm_bn(int64_t n, int64_t k, int want_split, SmallMCfg* c);
 
 // The narrowest tile of rows that holds m (or want_bn), else a wider one: a wider tile lets
 // the K slab be cut into more slices (each rank's rows of the tile come in fours), which is
 // what fits a long K into shared memory (16 x 768 x 3072: no 16-row configuration fits; 32
 // rows in 8 slices measured 6.5 us against 9.6 for the row tiles it replaced, graph, hot L2).
-bool pick_smallm(int64_t m, int64_t n, int64_t k, int sms, int want_split, int want_bn,
-                 SmallMCfg* c)
+bool pick_smallm(int64_t m, int64_t n, int64_t k, int want_split, int want_bn, SmallMCfg* c)
 {
     if (m < 1 || m > kSmallMMaxM || n < 1 || k < 1) return false;
     const int natural = m <= 16 ? 16 : m <= 32 ? 32 : 64;
     if (want_bn) {
         if (want_bn < natural) return false;
         c->bn = want_bn;
-        return pick_smallm_bn(n, k, sms, want_split, c);
+        return pick_smallm_bn(n, k, want_split, c);
     }
     for (int bn = natural; bn <= 64; bn *= 2) {
         c->bn = bn;
-        if (pick_smallm_bn(n, k, sms, want_split, c)) return true;
+        if (pick_smallm_bn(n, k, want_split, c)) return true;
     }
     return false;
 }
 
-bool pick_smallm_bn(int64_t n, int64_t k, int sms, int want_split, SmallMCfg* c)
+bool pick_smallm_bn(int64_t n, int64_t k, int want_split, SmallMCfg* c)
 {
-    (void)sms;
     const int64_t tiles = (n + 127) / 128;
     const int kblocks = static_cast<int>((k + 63) / 64);
     const int top = want_split > 0 ? want_split : (kblocks < 8 ? kblocks : 8);
@@ -364,7 +362,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             SmallMCfg sc;
             if (v == kSwapped && smallm_epilog(p->epilog) && p->opt_split_k == 0 &&
                 smallm_prepare() == cudaSuccess &&
-                pick_smallm(p->m, p->n, p->k, p->sm_count, 0, 0, &sc))
+                pick_smallm(p->m, p->n, p->k, 0, 0, &sc))
                 v = kSmallM;
             // otherwise, over a long K loop: row tiles with K split over a cluster when the
             // model puts them well ahead of the swapped kernel, which streams each 128-column
@@ -420,7 +418,7 @@ gemm_epi_status configure(gemm_epi_plan_s* p)
             if (!smallm_epilog(p->epilog) || p->opt_split_k > 8 ||
                 (p->opt_bn && p->opt_bn != 16 && p->opt_bn != 32 && p->opt_bn != 64))
                 return GEMM_EPI_ERR_INVALID_ARG;
-            if (!pick_smallm(p->m, p->n, p->k, p->sm_count, p->opt_split_k, p->opt_bn, &sc))
+            if (!pick_smallm(p->m, p->n, p->k, p->opt_split_k, p->opt_bn, &sc))
                 return GEMM_EPI_ERR_INVALID_ARG;
             const int need = smallm_smem_bytes(sc.bn, sc.kb * 64, sc.split);
             if (need > kSmemLimit) return GEMM_EPI_ERR_INVALID_ARG;
