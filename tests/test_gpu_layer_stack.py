@@ -102,6 +102,28 @@ def test_layer_stack_matches_oracle(t, d, f, layers, options, kernel):
     check_stack(inp, X, H, "bf16", descs)
 
 
+def _random_stack_case(i):
+    import random
+    r = random.Random(9100 + i)
+    t = r.choice([1, 3, 8, 16, 17, 32, 40, 64, 65, 100, 130, 200, 256, 300])
+    d = 8 * r.randint(2, 64)
+    f = 8 * r.randint(2, 200)
+    options = {"B_READY": r.choice([0, 1, 1])}
+    if r.random() < 0.3:
+        options["PDL"] = r.choice([0, 1])
+    if t <= 64 and r.random() < 0.3:
+        options["VARIANT"] = 2
+    return t, d, f, options
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_layer_stacks(i):
+    # seeded random shapes (ragged t, d and f) and launch options, three layers each
+    t, d, f, options = _random_stack_case(i)
+    inp, X, H, descs = run_stack(t, d, f, 3, options, seed=9200 + i)
+    check_stack(inp, X, H, "bf16", descs)
+
+
 @pytest.mark.parametrize("options", [{}, {"B_READY": 1}])
 def test_layer_stack_in_a_graph(options):
     inp, X, H, descs = run_stack(16, 768, 3072, 3, options, seed=7101, graph=True)
